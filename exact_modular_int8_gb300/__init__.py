@@ -1,0 +1,313 @@
+"""Exact matrix products through residues modulo the odd primes below 256, on GB300.
+
+Thin Python binding of the C-ABI library ``_build/libresgemm.so`` (declared in
+``include/resgemm.h``).  The functions here only marshal arguments: they take
+torch tensors, allocate outputs and a cached workspace with torch, and pass raw
+pointers and the current CUDA stream to the library.  Every step of the
+computation runs in the library's CUDA kernels; there is no CPU fallback, and
+importing the functions fails loudly if the library has not been built
+(``python -m exact_modular_int8_gb300.build`` or ``__graft_entry__.build()``).
+
+Entry points (same names as the C ABI):
+  res_gemm_i64(A, B)             exact int64 product
+  res_gemm_limbs(A, B, lc)       exact multi-limb product
+  enclose_gemm_f64(A, B)         (lo, hi) with lo <= A @ B <= hi exactly
+  res_gemm_stage(RA, RB, ...)    the per-prime tensor-core stage alone
+Helpers: width_ulps, digest, get_plan, workspace_bytes.
+"""
+from __future__ import annotations
+
+import ctypes
+import hashlib
+import os
+import threading
+
+import torch
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "_build", "libresgemm.so")
+
+RG_OK = 0
+RG_ERR_ARG = 1
+RG_ERR_RANGE = 2
+RG_ERR_NONFINITE = 3
+RG_ERR_LOSSY = 4
+RG_ERR_WORKSPACE = 5
+RG_ERR_CUDA = 6
+RG_ERR_TIMEOUT = 7
+RG_FLAG_SYNC = 1
+RG_FLAG_HOST = 2
+RG_OP_I64, RG_OP_LIMBS, RG_OP_ENCLOSE, RG_OP_STAGE = 0, 1, 2, 3
+MAX_K = 131072
+NUM_PRIMES = 53
+
+EXPORTED = (
+    "res_gemm_i64", "res_gemm_limbs", "enclose_gemm_f64", "res_gemm_stage", "rg_workspace_bytes",
+    "rg_workspace_layout", "rg_get_plan", "rg_status", "rg_prime", "rg_strerror", "rg_set_wait_limit_ns",
+    "rg_inject_fault",
+)
+
+
+class ResGemmError(RuntimeError):
+    """A library call returned a non-zero status."""
+
+    def __init__(self, code: int, where: str):
+        self.code = code
+        super().__init__(f"{where}: {strerror(code)} (status {code})")
+
+
+class Layout(ctypes.Structure):
+    _fields_ = [("ra", ctypes.c_size_t), ("rb", ctypes.c_size_t), ("rc", ctypes.c_size_t),
+                ("lda", ctypes.c_int64), ("ldb", ctypes.c_int64), ("ldc", ctypes.c_int64), ("pmax", ctypes.c_int)]
+
+
+class PlanInfo(ctypes.Structure):
+    _fields_ = [("status", ctypes.c_int), ("nprimes", ctypes.c_int), ("bits_a", ctypes.c_int),
+                ("bits_b", ctypes.c_int), ("bound_bits", ctypes.c_int), ("f_a", ctypes.c_int),
+                ("f_b", ctypes.c_int), ("lossless", ctypes.c_int)]
+
+    def as_dict(self):
+        return {k: getattr(self, k) for k, _ in self._fields_}
+
+
+_lib = None
+_lib_lock = threading.Lock()
+
+
+def library():
+    """The loaded C library (raises if it has not been built)."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    with _lib_lock:
+        if _lib is None:
+            if not os.path.exists(LIB_PATH):
+                raise ImportError(f"{LIB_PATH} is missing: build it with `python -m exact_modular_int8_gb300.build`")
+            lib = ctypes.CDLL(LIB_PATH)
+            vp, i64, ci, cu, sz = ctypes.c_void_p, ctypes.c_int64, ctypes.c_int, ctypes.c_uint, ctypes.c_size_t
+            lib.res_gemm_i64.argtypes = [vp, vp, vp, i64, i64, i64, ci, cu, vp, sz, vp]
+            lib.res_gemm_limbs.argtypes = [vp, ci, vp, ci, vp, ci, i64, i64, i64, ci, cu, vp, sz, vp]
+            lib.enclose_gemm_f64.argtypes = [vp, vp, vp, vp, i64, i64, i64, cu, vp, sz, vp]
+            lib.res_gemm_stage.argtypes = [vp, i64, vp, i64, vp, i64, ci, i64, i64, i64, cu, vp, sz, vp]
+            for f in ("res_gemm_i64", "res_gemm_limbs", "enclose_gemm_f64", "res_gemm_stage"):
+                getattr(lib, f).restype = ci
+            lib.rg_workspace_bytes.argtypes = [ci, i64, i64, i64, ci, ci, ci, ci, cu]
+            lib.rg_workspace_bytes.restype = sz
+            lib.rg_workspace_layout.argtypes = [ci, i64, i64, i64, ci, ci, ci, ci, cu, ctypes.POINTER(Layout)]
+            lib.rg_workspace_layout.restype = ci
+            lib.rg_get_plan.argtypes = [vp, vp, ctypes.POINTER(PlanInfo)]
+            lib.rg_get_plan.restype = ci
+            lib.rg_status.argtypes = [vp, vp]
+            lib.rg_status.restype = ci
+            lib.rg_prime.argtypes = [ci]
+            lib.rg_prime.restype = ci
+            lib.rg_strerror.argtypes = [ci]
+            lib.rg_strerror.restype = ctypes.c_char_p
+            lib.rg_set_wait_limit_ns.argtypes = [ctypes.c_uint64]
+            lib.rg_set_wait_limit_ns.restype = ctypes.c_uint64
+            lib.rg_inject_fault.argtypes = [ci]
+            lib.rg_inject_fault.restype = None
+            _lib = lib
+    return _lib
+
+
+def strerror(code: int) -> str:
+    return library().rg_strerror(int(code)).decode()
+
+
+def primes() -> list[int]:
+    """The residue base, largest first: 251, 241, ..., 3."""
+    return [library().rg_prime(i) for i in range(NUM_PRIMES)]
+
+
+def workspace_bytes(op, M, N, K, la=1, lb=1, lc=1, nprimes=0, host=False) -> int:
+    return int(library().rg_workspace_bytes(op, M, N, K, la, lb, lc, nprimes, RG_FLAG_HOST if host else 0))
+
+
+def workspace_layout(op, M, N, K, la=1, lb=1, lc=1, nprimes=0, host=False) -> Layout:
+    out = Layout()
+    rc = library().rg_workspace_layout(op, M, N, K, la, lb, lc, nprimes, RG_FLAG_HOST if host else 0,
+                                       ctypes.byref(out))
+    if rc:
+        raise ResGemmError(rc, "rg_workspace_layout")
+    return out
+
+
+# ---------------------------------------------------------------------------
+# workspace cache: one growing device buffer per (device, stream)
+# ---------------------------------------------------------------------------
+_ws_cache: dict = {}
+
+
+def workspace(nbytes: int, device: torch.device, stream=None) -> torch.Tensor:
+    """A device buffer of at least nbytes, reused across calls on one stream."""
+    stream = stream or torch.cuda.current_stream(device)
+    key = (device.index, stream.cuda_stream)
+    buf = _ws_cache.get(key)
+    if buf is None or buf.numel() < nbytes:
+        _ws_cache.pop(key, None)
+        buf = torch.empty(max(nbytes, 4096), dtype=torch.uint8, device=device)
+        _ws_cache[key] = buf
+    return buf
+
+
+def release_workspaces():
+    _ws_cache.clear()
+
+
+def _device_of(*ts):
+    devs = {t.device for t in ts}
+    if len(devs) != 1:
+        raise ValueError("operands must be on one device")
+    return devs.pop()
+
+
+def _call_ctx(A, B):
+    """(device for the work, flags) for operands on a CUDA device or on the host."""
+    dev = _device_of(A, B)
+    if dev.type == "cuda":
+        return dev, 0
+    if dev.type == "cpu":
+        return torch.device("cuda", torch.cuda.current_device()), RG_FLAG_HOST
+    raise ValueError(f"unsupported device {dev}")
+
+
+def _check(rc, where):
+    if rc != RG_OK:
+        raise ResGemmError(rc, where)
+
+
+def res_gemm_i64(A: torch.Tensor, B: torch.Tensor, nprimes: int = 0, sync: bool = True, out=None,
+                 ws: torch.Tensor | None = None) -> torch.Tensor:
+    """Exact C = A @ B for int64 matrices (CUDA tensors, or CPU tensors staged through the device)."""
+    if A.dtype != torch.int64 or B.dtype != torch.int64 or A.dim() != 2 or B.dim() != 2 or A.shape[1] != B.shape[0]:
+        raise ValueError("A [M,K] and B [K,N] int64 expected")
+    A, B = A.contiguous(), B.contiguous()
+    M, K = A.shape
+    N = B.shape[1]
+    dev, flags = _call_ctx(A, B)
+    if sync:
+        flags |= RG_FLAG_SYNC
+    C = out if out is not None else torch.empty((M, N), dtype=torch.int64, device=A.device,
+                                                pin_memory=bool(flags & RG_FLAG_HOST))
+    with torch.cuda.device(dev):
+        need = workspace_bytes(RG_OP_I64, M, N, K, nprimes=nprimes, host=bool(flags & RG_FLAG_HOST))
+        if need == 0:
+            raise ResGemmError(RG_ERR_ARG, "res_gemm_i64")
+        w = ws if ws is not None else workspace(need, dev)
+        rc = library().res_gemm_i64(A.data_ptr(), B.data_ptr(), C.data_ptr(), M, N, K, nprimes, flags,
+                                    w.data_ptr(), w.numel(), torch.cuda.current_stream(dev).cuda_stream)
+    _check(rc, "res_gemm_i64")
+    return C
+
+
+def res_gemm_limbs(A: torch.Tensor, B: torch.Tensor, lc: int, nprimes: int = 0, sync: bool = True, out=None,
+                   ws: torch.Tensor | None = None) -> torch.Tensor:
+    """Exact C = A @ B for multi-limb int64 operands A [M,K,la], B [K,N,lb]; returns [M,N,lc]."""
+    if A.dtype != torch.int64 or B.dtype != torch.int64 or A.dim() != 3 or B.dim() != 3 or A.shape[1] != B.shape[0]:
+        raise ValueError("A [M,K,la] and B [K,N,lb] int64 expected")
+    A, B = A.contiguous(), B.contiguous()
+    M, K, la = A.shape
+    N, lb = B.shape[1], B.shape[2]
+    dev, flags = _call_ctx(A, B)
+    if sync:
+        flags |= RG_FLAG_SYNC
+    C = out if out is not None else torch.empty((M, N, lc), dtype=torch.int64, device=A.device,
+                                                pin_memory=bool(flags & RG_FLAG_HOST))
+    with torch.cuda.device(dev):
+        need = workspace_bytes(RG_OP_LIMBS, M, N, K, la, lb, lc, nprimes, host=bool(flags & RG_FLAG_HOST))
+        if need == 0:
+            raise ResGemmError(RG_ERR_ARG, "res_gemm_limbs")
+        w = ws if ws is not None else workspace(need, dev)
+        rc = library().res_gemm_limbs(A.data_ptr(), la, B.data_ptr(), lb, C.data_ptr(), lc, M, N, K, nprimes, flags,
+                                      w.data_ptr(), w.numel(), torch.cuda.current_stream(dev).cuda_stream)
+    _check(rc, "res_gemm_limbs")
+    return C
+
+
+def enclose_gemm_f64(A: torch.Tensor, B: torch.Tensor, sync: bool = True, ws: torch.Tensor | None = None):
+    """(lo, hi) float64 with lo <= A @ B <= hi entrywise in exact arithmetic."""
+    if A.dtype != torch.float64 or B.dtype != torch.float64 or A.dim() != 2 or B.dim() != 2 or A.shape[1] != B.shape[0]:
+        raise ValueError("A [M,K] and B [K,N] float64 expected")
+    A, B = A.contiguous(), B.contiguous()
+    M, K = A.shape
+    N = B.shape[1]
+    dev, flags = _call_ctx(A, B)
+    if sync:
+        flags |= RG_FLAG_SYNC
+    pin = bool(flags & RG_FLAG_HOST)
+    lo = torch.empty((M, N), dtype=torch.float64, device=A.device, pin_memory=pin)
+    hi = torch.empty((M, N), dtype=torch.float64, device=A.device, pin_memory=pin)
+    with torch.cuda.device(dev):
+        need = workspace_bytes(RG_OP_ENCLOSE, M, N, K, host=pin)
+        if need == 0:
+            raise ResGemmError(RG_ERR_ARG, "enclose_gemm_f64")
+        w = ws if ws is not None else workspace(need, dev)
+        rc = library().enclose_gemm_f64(A.data_ptr(), B.data_ptr(), lo.data_ptr(), hi.data_ptr(), M, N, K, flags,
+                                        w.data_ptr(), w.numel(), torch.cuda.current_stream(dev).cuda_stream)
+    _check(rc, "enclose_gemm_f64")
+    return lo, hi
+
+
+def res_gemm_stage(RA: torch.Tensor, RB: torch.Tensor, nprimes: int, M: int, N: int, K: int, RC=None,
+                   sync: bool = True) -> torch.Tensor:
+    """RC[p] = (RA[p] @ RB[p]) mod q_p for fp16 residues RA [P,M,lda], RB [P,K,ldb]; RC uint8 [P,M,ldc]."""
+    if RA.dtype != torch.float16 or RB.dtype != torch.float16:
+        raise ValueError("fp16 residues expected")
+    if not (RA.is_contiguous() and RB.is_contiguous()):
+        raise ValueError("contiguous residue planes expected")
+    lda, ldb = RA.shape[-1], RB.shape[-1]
+    ldc = (N + 15) // 16 * 16
+    if RC is None:
+        RC = torch.empty((nprimes, M, ldc), dtype=torch.uint8, device=RA.device)
+    dev = RA.device
+    with torch.cuda.device(dev):
+        w = workspace(4096, dev)
+        rc = library().res_gemm_stage(RA.data_ptr(), lda, RB.data_ptr(), ldb, RC.data_ptr(), RC.shape[-1], nprimes,
+                                      M, N, K, RG_FLAG_SYNC if sync else 0, w.data_ptr(), w.numel(),
+                                      torch.cuda.current_stream(dev).cuda_stream)
+    _check(rc, "res_gemm_stage")
+    return RC
+
+
+def get_plan(ws: torch.Tensor | None = None, device=None) -> dict:
+    """The plan of the last call on the cached workspace of `device` (or on `ws`)."""
+    dev = torch.device("cuda", torch.cuda.current_device()) if device is None else torch.device(device)
+    w = ws if ws is not None else workspace(4096, dev)
+    info = PlanInfo()
+    with torch.cuda.device(dev):
+        _check(library().rg_get_plan(w.data_ptr(), torch.cuda.current_stream(dev).cuda_stream, ctypes.byref(info)),
+               "rg_get_plan")
+    return info.as_dict()
+
+
+def status(ws: torch.Tensor | None = None, device=None) -> int:
+    dev = torch.device("cuda", torch.cuda.current_device()) if device is None else torch.device(device)
+    w = ws if ws is not None else workspace(4096, dev)
+    with torch.cuda.device(dev):
+        return int(library().rg_status(w.data_ptr(), torch.cuda.current_stream(dev).cuda_stream))
+
+
+# ---------------------------------------------------------------------------
+# helpers ("enclosure-gemm", Usage: width_ulps and digest)
+# ---------------------------------------------------------------------------
+
+
+def _ordered(x: torch.Tensor) -> torch.Tensor:
+    """float64 -> int64 key increasing with the value (+0 and -0 share 0)."""
+    b = x.contiguous().view(torch.int64)
+    mag = b & 0x7FFFFFFFFFFFFFFF
+    return torch.where(b < 0, -mag, mag)
+
+
+def width_ulps(lo: torch.Tensor, hi: torch.Tensor) -> torch.Tensor:
+    """Number of representable steps from lo to hi (0 when lo == hi)."""
+    return _ordered(hi) - _ordered(lo)
+
+
+def digest(lo: torch.Tensor, hi: torch.Tensor) -> str:
+    """SHA-256 over the raw bytes of lo then hi."""
+    h = hashlib.sha256()
+    h.update(lo.detach().contiguous().cpu().numpy().tobytes())
+    h.update(hi.detach().contiguous().cpu().numpy().tobytes())
+    return h.hexdigest()

@@ -1,0 +1,277 @@
+// api.cu -- the C ABI (include/resgemm.h): validation, workspace layout and
+// the launch sequence planner -> split -> per-prime GEMM -> Garner.
+//
+// The sequence keeps the data path free of host synchronisation: the planner
+// reductions, the prime count and the scale exponents all live in the
+// workspace's plan block, and every kernel reads them there.  Only
+// RG_FLAG_SYNC / RG_FLAG_HOST calls, rg_status() and rg_get_plan() wait for the
+// device.
+#include <atomic>
+#include <cstdint>
+#include <cstring>
+
+#include "rg_kernels.h"
+
+namespace {
+using namespace rg;
+
+constexpr size_t kPlanBytes = 4096;
+constexpr size_t kAlign = 4096;
+
+std::atomic<unsigned long long> g_wait_ns{1000000000ull};
+std::atomic<int> g_fault{0};
+
+size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
+long long round_up(long long x, long long a) { return (x + a - 1) / a * a; }
+
+int ceil_log2(long long k) {
+  int c = 0;
+  while ((1LL << c) < k) ++c;
+  return c;
+}
+
+int primes_for_bound_host(int T) {
+  const Tables& t = host_tables();
+  for (int n = 1; n <= kNumPrimes; ++n)
+    if (t.log2P[n] >= T + 1) return n;
+  return kNumPrimes;
+}
+
+// Largest prime count a call can need when it plans on the device.
+int pmax_for(int op, long long K, int la, int lb, int nprimes) {
+  if (nprimes > 0) return nprimes;
+  int ck = ceil_log2(K);
+  switch (op) {
+    case RG_OP_I64:
+      // K * max|A| * max|B| <= 2^63 - 1 bounds bits_a + bits_b + ceil(log2 K) by 65.
+      return primes_for_bound_host(65);
+    case RG_OP_LIMBS: {
+      int T = 64 * la + 64 * lb + ck;
+      return primes_for_bound_host(T < RG_MAX_BOUND_BITS ? T : RG_MAX_BOUND_BITS);
+    }
+    default:
+      return kNumPrimes;
+  }
+}
+
+struct Layout {
+  size_t plan, ra, rb, rc, a, b, c, c2, total;
+  long long lda, ldb, ldc;
+  int pmax;
+};
+
+bool make_layout(int op, long long M, long long N, long long K, int la, int lb, int lc, int nprimes, unsigned flags,
+                 Layout* L) {
+  if (M <= 0 || N <= 0 || K <= 0) return false;
+  if (nprimes < 0 || nprimes > kNumPrimes) return false;
+  if (op == RG_OP_LIMBS && (la < 1 || la > RG_MAX_LIMBS_IN || lb < 1 || lb > RG_MAX_LIMBS_IN || lc < 1 ||
+                            lc > RG_MAX_LIMBS_OUT))
+    return false;
+  if (op != RG_OP_LIMBS) la = lb = lc = 1;
+  std::memset(L, 0, sizeof(*L));
+  L->lda = round_up(K, 8);
+  L->ldb = round_up(N, 64);
+  L->ldc = round_up(N, 16);
+  L->plan = 0;
+  size_t off = kPlanBytes;
+  if (op == RG_OP_STAGE) {
+    L->total = off;
+    L->pmax = nprimes;
+    return true;
+  }
+  int pmax = pmax_for(op, K, la, lb, nprimes);
+  L->pmax = pmax;
+  L->ra = off;
+  off = align_up(off + (size_t)pmax * M * L->lda * 2, kAlign);
+  L->rb = off;
+  off = align_up(off + (size_t)pmax * K * L->ldb * 2, kAlign);
+  L->rc = off;
+  off = align_up(off + (size_t)pmax * M * L->ldc, kAlign);
+  if (flags & RG_FLAG_HOST) {
+    size_t ea = op == RG_OP_LIMBS ? 8 * (size_t)la : 8, eb = op == RG_OP_LIMBS ? 8 * (size_t)lb : 8;
+    size_t ec = op == RG_OP_LIMBS ? 8 * (size_t)lc : 8;
+    L->a = off;
+    off = align_up(off + (size_t)M * K * ea, kAlign);
+    L->b = off;
+    off = align_up(off + (size_t)K * N * eb, kAlign);
+    L->c = off;
+    off = align_up(off + (size_t)M * N * ec, kAlign);
+    if (op == RG_OP_ENCLOSE) {
+      L->c2 = off;
+      off = align_up(off + (size_t)M * N * 8, kAlign);
+    }
+  }
+  L->total = off;
+  return true;
+}
+
+int finish(void* ws, cudaStream_t s, unsigned flags) {
+  if (!(flags & (RG_FLAG_SYNC | RG_FLAG_HOST))) return RG_OK;
+  int st = 0;
+  DevPlan* plan = static_cast<DevPlan*>(ws);
+  if (cudaMemcpyAsync(&st, &plan->status, sizeof(int), cudaMemcpyDeviceToHost, s) != cudaSuccess) return RG_ERR_CUDA;
+  if (cudaStreamSynchronize(s) != cudaSuccess) return RG_ERR_CUDA;
+  return st;
+}
+
+#define RG_TRY(x)                          \
+  do {                                     \
+    cudaError_t e_ = (x);                  \
+    if (e_ != cudaSuccess) return RG_ERR_CUDA; \
+  } while (0)
+
+// Shared driver for the three integer/fp64 entry points.
+int run(int op, const void* A, int la, const void* B, int lb, void* C, void* C2, int lc, long long M, long long N,
+        long long K, int nprimes, unsigned flags, void* ws, size_t ws_bytes, void* stream) {
+  if (!A || !B || !C || !ws || (op == RG_OP_ENCLOSE && !C2)) return RG_ERR_ARG;
+  if ((reinterpret_cast<uintptr_t>(ws) & 255u) != 0) return RG_ERR_ARG;
+  if (M <= 0 || N <= 0 || K <= 0 || nprimes < 0 || nprimes > kNumPrimes) return RG_ERR_ARG;
+  if (op == RG_OP_LIMBS &&
+      (la < 1 || la > RG_MAX_LIMBS_IN || lb < 1 || lb > RG_MAX_LIMBS_IN || lc < 1 || lc > RG_MAX_LIMBS_OUT))
+    return RG_ERR_ARG;
+  if (K > RG_MAX_K) return RG_ERR_RANGE;
+  if (M > (1LL << 31) - 1 || N > (1LL << 31) - 1) return RG_ERR_ARG;
+  Layout L;
+  if (!make_layout(op, M, N, K, la, lb, lc, nprimes, flags, &L)) return RG_ERR_ARG;
+  if (ws_bytes < L.total) return RG_ERR_WORKSPACE;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  RG_TRY(upload_tables());
+  uint8_t* w = static_cast<uint8_t*>(ws);
+  DevPlan* plan = reinterpret_cast<DevPlan*>(w + L.plan);
+  const size_t ea = op == RG_OP_LIMBS ? 8 * (size_t)la : 8, eb = op == RG_OP_LIMBS ? 8 * (size_t)lb : 8;
+  const size_t ec = op == RG_OP_LIMBS ? 8 * (size_t)lc : 8;
+  const void* dA = A;
+  const void* dB = B;
+  void* dC = C;
+  void* dC2 = C2;
+  if (flags & RG_FLAG_HOST) {
+    dA = w + L.a;
+    dB = w + L.b;
+    dC = w + L.c;
+    dC2 = op == RG_OP_ENCLOSE ? static_cast<void*>(w + L.c2) : nullptr;
+    RG_TRY(cudaMemcpyAsync(const_cast<void*>(dA), A, (size_t)M * K * ea, cudaMemcpyHostToDevice, s));
+    RG_TRY(cudaMemcpyAsync(const_cast<void*>(dB), B, (size_t)K * N * eb, cudaMemcpyHostToDevice, s));
+  }
+  RG_TRY(cudaMemsetAsync(plan, 0, sizeof(DevPlan), s));
+  if (op == RG_OP_I64 && nprimes == 0)
+    RG_TRY(launch_plan_i64(static_cast<const int64_t*>(dA), M * K, static_cast<const int64_t*>(dB), K * N, plan, s));
+  else if (op == RG_OP_LIMBS && nprimes == 0)
+    RG_TRY(launch_plan_limbs(static_cast<const int64_t*>(dA), M * K, la, static_cast<const int64_t*>(dB), K * N, lb,
+                             plan, s));
+  else if (op == RG_OP_ENCLOSE)
+    RG_TRY(launch_plan_f64(static_cast<const double*>(dA), M * K, static_cast<const double*>(dB), K * N, plan, s));
+  RG_TRY(launch_split(op, dA, dB, op == RG_OP_LIMBS ? la : 1, op == RG_OP_LIMBS ? lb : 1, op == RG_OP_LIMBS ? lc : 1,
+                      M, N, K, L.lda, L.ldb, w + L.ra, w + L.rb, op == RG_OP_ENCLOSE ? 0 : nprimes, plan, s));
+  int fault = g_fault.exchange(0);
+  RG_TRY(launch_gemm(w + L.ra, L.lda, w + L.rb, L.ldb, w + L.rc, L.ldc, L.pmax, 0, M, N, K, plan, s, fault,
+                     g_wait_ns.load()));
+  RG_TRY(launch_garner(op, w + L.rc, L.ldc, (long long)M * L.ldc, M, N, op == RG_OP_LIMBS ? lc : 1, plan, dC, dC2, s));
+  if (flags & RG_FLAG_HOST) {
+    RG_TRY(cudaMemcpyAsync(C, dC, (size_t)M * N * ec, cudaMemcpyDeviceToHost, s));
+    if (op == RG_OP_ENCLOSE) RG_TRY(cudaMemcpyAsync(C2, dC2, (size_t)M * N * 8, cudaMemcpyDeviceToHost, s));
+  }
+  return finish(ws, s, flags);
+}
+
+}  // namespace
+
+extern "C" {
+
+int res_gemm_i64(const int64_t* A, const int64_t* B, int64_t* C, int64_t M, int64_t N, int64_t K, int nprimes,
+                 unsigned flags, void* ws, size_t ws_bytes, void* stream) {
+  return run(RG_OP_I64, A, 1, B, 1, C, nullptr, 1, M, N, K, nprimes, flags, ws, ws_bytes, stream);
+}
+
+int res_gemm_limbs(const int64_t* A, int la, const int64_t* B, int lb, int64_t* C, int lc, int64_t M, int64_t N,
+                   int64_t K, int nprimes, unsigned flags, void* ws, size_t ws_bytes, void* stream) {
+  return run(RG_OP_LIMBS, A, la, B, lb, C, nullptr, lc, M, N, K, nprimes, flags, ws, ws_bytes, stream);
+}
+
+int enclose_gemm_f64(const double* A, const double* B, double* lo, double* hi, int64_t M, int64_t N, int64_t K,
+                     unsigned flags, void* ws, size_t ws_bytes, void* stream) {
+  return run(RG_OP_ENCLOSE, A, 1, B, 1, lo, hi, 1, M, N, K, 0, flags, ws, ws_bytes, stream);
+}
+
+int res_gemm_stage(const uint16_t* RA, int64_t lda, const uint16_t* RB, int64_t ldb, uint8_t* RC, int64_t ldc,
+                   int nprimes, int64_t M, int64_t N, int64_t K, unsigned flags, void* ws, size_t ws_bytes,
+                   void* stream) {
+  if (!RA || !RB || !RC || !ws || (flags & RG_FLAG_HOST)) return RG_ERR_ARG;
+  if (M <= 0 || N <= 0 || K <= 0 || nprimes < 1 || nprimes > kNumPrimes) return RG_ERR_ARG;
+  if (lda < K || lda % 8 || ldb < N || ldb % 64 || ldc < N || ldc % 16) return RG_ERR_ARG;
+  if ((reinterpret_cast<uintptr_t>(RA) | reinterpret_cast<uintptr_t>(RB) | reinterpret_cast<uintptr_t>(RC)) & 15u)
+    return RG_ERR_ARG;
+  if ((reinterpret_cast<uintptr_t>(ws) & 255u) != 0) return RG_ERR_ARG;
+  if (K > RG_MAX_K) return RG_ERR_RANGE;
+  if (ws_bytes < kPlanBytes) return RG_ERR_WORKSPACE;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  DevPlan* plan = static_cast<DevPlan*>(ws);
+  RG_TRY(cudaMemsetAsync(plan, 0, sizeof(DevPlan), s));
+  int fault = g_fault.exchange(0);
+  RG_TRY(launch_gemm(RA, lda, RB, ldb, RC, ldc, nprimes, nprimes, M, N, K, plan, s, fault, g_wait_ns.load()));
+  return finish(ws, s, flags);
+}
+
+size_t rg_workspace_bytes(int op, int64_t M, int64_t N, int64_t K, int la, int lb, int lc, int nprimes,
+                          unsigned flags) {
+  Layout L;
+  if (op < RG_OP_I64 || op > RG_OP_STAGE) return 0;
+  if (!make_layout(op, M, N, K, la, lb, lc, nprimes, flags, &L)) return 0;
+  return L.total;
+}
+
+int rg_workspace_layout(int op, int64_t M, int64_t N, int64_t K, int la, int lb, int lc, int nprimes,
+                        unsigned flags, rg_layout* out) {
+  Layout L;
+  if (!out || op < RG_OP_I64 || op > RG_OP_STAGE) return RG_ERR_ARG;
+  if (!make_layout(op, M, N, K, la, lb, lc, nprimes, flags, &L)) return RG_ERR_ARG;
+  out->ra = L.ra;
+  out->rb = L.rb;
+  out->rc = L.rc;
+  out->lda = L.lda;
+  out->ldb = L.ldb;
+  out->ldc = L.ldc;
+  out->pmax = L.pmax;
+  return RG_OK;
+}
+
+int rg_get_plan(const void* ws, void* stream, rg_plan_info* out) {
+  if (!ws || !out) return RG_ERR_ARG;
+  DevPlan p;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if (cudaMemcpyAsync(&p, ws, sizeof(p), cudaMemcpyDeviceToHost, s) != cudaSuccess) return RG_ERR_CUDA;
+  if (cudaStreamSynchronize(s) != cudaSuccess) return RG_ERR_CUDA;
+  out->status = p.status;
+  out->nprimes = p.P;
+  out->bits_a = p.bits_a;
+  out->bits_b = p.bits_b;
+  out->bound_bits = p.bound_bits;
+  out->f_a = p.f_a;
+  out->f_b = p.f_b;
+  out->lossless = p.lossless;
+  return RG_OK;
+}
+
+int rg_status(const void* ws, void* stream) {
+  if (!ws) return RG_ERR_ARG;
+  return finish(const_cast<void*>(ws), static_cast<cudaStream_t>(stream), RG_FLAG_SYNC);
+}
+
+const char* rg_strerror(int code) {
+  switch (code) {
+    case RG_OK: return "ok";
+    case RG_ERR_ARG: return "invalid argument";
+    case RG_ERR_RANGE: return "out of range: K > 2^17 or the product bound exceeds the primes or the output width";
+    case RG_ERR_NONFINITE: return "an fp64 operand entry is inf or nan";
+    case RG_ERR_LOSSY: return "fp64 operands do not scale losslessly into the 256-bit fixed point";
+    case RG_ERR_WORKSPACE: return "workspace too small";
+    case RG_ERR_CUDA: return "CUDA error";
+    case RG_ERR_TIMEOUT: return "a bounded wait inside a kernel expired";
+    default: return "unknown status";
+  }
+}
+
+uint64_t rg_set_wait_limit_ns(uint64_t ns) { return g_wait_ns.exchange(ns ? ns : 1000000000ull); }
+
+void rg_inject_fault(int kind) { g_fault.store(kind); }
+
+}  // extern "C"

@@ -1,0 +1,527 @@
+// gemm_tc.cu -- the per-prime residue product on the sm_103a tensor cores.
+//
+// Page "exact-solve", Method: each step's per-prime product is one batched
+// tensor-core GEMM on balanced residues; page "enclosure-gemm", Requirements:
+// K <= 2^17, set by the accumulator.
+//
+// sm_103a has no integer tcgen05 MMA, so the residues (|r| <= 125) go through
+// tcgen05.mma kind::f16 as exactly representable fp16 values, accumulating in
+// fp32 in tensor memory.  Every product is an integer below 2^14 in magnitude;
+// a chunk of Kc = 1024 products therefore sums to less than 1024 * 15625 <
+// 2^24 and stays an exact fp32 integer.  After each chunk the accumulator is
+// reduced modulo q in place (|remainder| <= 1.5 q), so the next chunk adds
+// onto a small value and never reaches 2^24.  Two accumulators alternate
+// chunks, so the reduction of one overlaps the products of the other; the
+// last two chunks of a tile are reduced to [0, q), summed, and written as
+// uint8 residues through shared memory and a TMA store.
+//
+// Warp roles (one CTA per SM, persistent over tiles of (prime, m, n)):
+//   warp 0      TMA producer: A tile 128x64 (K-major) and B tile 64x256
+//               (N-major) per pipeline stage, 128-byte swizzle.
+//   warp 1      owns the tensor memory and issues the MMAs (one thread).
+//   warps 2..5  epilogue: tcgen05.ld, reduction mod q, tcgen05.st / output.
+// Every wait is bounded; on expiry the kernel records RG_ERR_TIMEOUT, lets
+// in-flight copies and MMAs finish, frees its tensor memory and returns.
+#include <cuda.h>
+#include <cudaTypedefs.h>
+
+#include <cstdint>
+#include <mutex>
+
+#include "rg_common.cuh"
+#include "rg_kernels.h"
+
+namespace rg {
+namespace {
+
+constexpr int BM = 128;
+constexpr int BN = 256;
+constexpr int BK = 64;  // fp16 per k-block: one 128-byte swizzle row
+constexpr int STAGES = 4;
+constexpr int KC_BLOCKS = 16;  // k-blocks per exact fp32 chunk: Kc = 1024
+constexpr int A_BYTES = BM * BK * 2;
+constexpr int B_SLAB = 64 * BK * 2;  // one 64-column slab of B
+constexpr int B_BYTES = BN * BK * 2;
+constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
+constexpr int OUT_HALF = 128 * 128;  // uint8 staging: two 128x128 halves
+constexpr int OUT_BYTES = 2 * OUT_HALF;
+constexpr int TMEM_COLS = 2 * BN;
+constexpr int NUM_THREADS = 192;
+constexpr int BAR_BYTES = 256;
+constexpr int SMEM_BYTES = 1024 + STAGES * STAGE_BYTES + OUT_BYTES + BAR_BYTES;
+static_assert(SMEM_BYTES <= 232448, "shared memory");
+
+// Instruction descriptor, kind::f16: D f32, A and B f16, A K-major, B MN-major,
+// N = 256, M = 128.
+constexpr uint32_t IDESC = (1u << 4) | (0u << 7) | (0u << 10) | (0u << 15) | (1u << 16) | ((uint32_t)(BN >> 3) << 17) |
+                           ((uint32_t)(BM >> 4) << 24);
+
+struct GemmParams {
+  int M, N, K;
+  int mt, nt;
+  int kb_total;
+  int P_fixed;  // 0: read the prime count from the plan
+  int fault;
+  unsigned long long wait_ns;
+  float qf[kNumPrimes];
+  float invq[kNumPrimes];
+};
+
+// ---------------------------------------------------------------------------
+// PTX wrappers
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ uint32_t smem_u32(const void* p) { return (uint32_t)__cvta_generic_to_shared(p); }
+
+__device__ __forceinline__ unsigned long long globaltimer() {
+  unsigned long long t;
+  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+  return t;
+}
+
+__device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");
+}
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint32_t bar, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes) : "memory");
+}
+__device__ __forceinline__ void mbar_arrive(uint32_t bar) {
+  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
+}
+__device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n selp.u32 %0, 1, 0, p;\n}\n"
+      : "=r"(ok)
+      : "r"(bar), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+
+struct Ctl {
+  volatile int* abort;
+  int* status;
+  int* where;
+  unsigned long long limit_ns;
+};
+
+// Wait for the phase of `parity` to complete, for at most ctl.limit_ns.
+__device__ bool wait_bounded(uint32_t bar, uint32_t parity, const Ctl& ctl, int where) {
+  if (mbar_try_wait(bar, parity)) return true;
+  unsigned long long t0 = globaltimer();
+  for (uint32_t i = 1;; ++i) {
+    if (mbar_try_wait(bar, parity)) return true;
+    if ((i & 63u) == 0) {
+      if (*ctl.abort) return false;
+      if (globaltimer() - t0 > ctl.limit_ns) {
+        *ctl.abort = 1;
+        atomicCAS(ctl.status, 0, RG_ERR_TIMEOUT);
+        atomicCAS(ctl.where, 0, where);
+        return false;
+      }
+    }
+  }
+}
+
+__device__ __forceinline__ void tma_load_3d(uint32_t dst, const CUtensorMap* map, uint32_t bar, int c0, int c1,
+                                            int c2) {
+  asm volatile(
+      "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%3, %4, %5}], "
+      "[%2];" ::"r"(dst),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(bar), "r"(c0), "r"(c1), "r"(c2)
+      : "memory");
+}
+__device__ __forceinline__ void tma_store_3d(const CUtensorMap* map, uint32_t src, int c0, int c1, int c2) {
+  asm volatile("cp.async.bulk.tensor.3d.global.shared::cta.tile.bulk_group [%0, {%2, %3, %4}], [%1];" ::"l"(
+                   reinterpret_cast<uint64_t>(map)),
+               "r"(src), "r"(c0), "r"(c1), "r"(c2)
+               : "memory");
+}
+__device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
+__device__ __forceinline__ void bulk_wait_read0() { asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory"); }
+__device__ __forceinline__ void bulk_wait0() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
+__device__ __forceinline__ void fence_proxy_async_smem() {
+  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+__device__ __forceinline__ void epilogue_bar() { asm volatile("bar.sync 1, 128;" ::: "memory"); }
+
+__device__ __forceinline__ void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
+__device__ __forceinline__ void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
+
+__device__ __forceinline__ void umma_f16(uint32_t d, uint64_t adesc, uint64_t bdesc, uint32_t idesc, uint32_t acc) {
+  asm volatile(
+      "{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n}\n" ::"r"(d),
+      "l"(adesc), "l"(bdesc), "r"(idesc), "r"(acc)
+      : "memory");
+}
+__device__ __forceinline__ void umma_commit(uint32_t bar) {
+  asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar) : "memory");
+}
+
+// Shared-memory matrix descriptor, 128-byte swizzle.  lbo/sbo in bytes.
+__device__ __forceinline__ uint64_t sw128_desc(uint32_t saddr, uint32_t lbo, uint32_t sbo) {
+  uint64_t d = (uint64_t)((saddr >> 4) & 0x3FFFu);
+  d |= (uint64_t)((lbo >> 4) & 0x3FFFu) << 16;
+  d |= (uint64_t)((sbo >> 4) & 0x3FFFu) << 32;
+  d |= (uint64_t)1 << 46;  // descriptor version
+  d |= (uint64_t)2 << 61;  // 128-byte swizzle
+  return d;
+}
+
+#define RG_R8(i) "=r"(r[i]), "=r"(r[i + 1]), "=r"(r[i + 2]), "=r"(r[i + 3]), "=r"(r[i + 4]), "=r"(r[i + 5]), "=r"(r[i + 6]), "=r"(r[i + 7])
+#define RG_W8(i) "r"(r[i]), "r"(r[i + 1]), "r"(r[i + 2]), "r"(r[i + 3]), "r"(r[i + 4]), "r"(r[i + 5]), "r"(r[i + 6]), "r"(r[i + 7])
+
+__device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t (&r)[32]) {
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16,%17,%18,%19,"
+      "%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];"
+      : RG_R8(0), RG_R8(8), RG_R8(16), RG_R8(24)
+      : "r"(taddr));
+}
+__device__ __forceinline__ void tmem_st32(uint32_t taddr, const uint32_t (&r)[32]) {
+  asm volatile(
+      "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16,%17,%18,"
+      "%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31,%32};" ::"r"(taddr),
+      RG_W8(0), RG_W8(8), RG_W8(16), RG_W8(24)
+      : "memory");
+}
+__device__ __forceinline__ void tmem_wait_ld() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
+__device__ __forceinline__ void tmem_wait_st() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
+
+// Byte offset of (row, 16-byte chunk j) in a 128-row x 128-byte swizzled half.
+__device__ __forceinline__ uint32_t sw128_off(int row, int j) { return (uint32_t)(row * 128 + ((j ^ (row & 7)) << 4)); }
+
+struct TileCoord {
+  int p, m, n;
+};
+__device__ __forceinline__ TileCoord tile_coord(int t, int mt, int nt) {
+  int per = mt * nt;
+  TileCoord c;
+  c.p = t / per;
+  int r = t - c.p * per;
+  c.n = r / mt;  // consecutive CTAs share a B column block
+  c.m = r - c.n * mt;
+  return c;
+}
+
+// ---------------------------------------------------------------------------
+// The kernel
+// ---------------------------------------------------------------------------
+__global__ void __launch_bounds__(NUM_THREADS, 1)
+    residue_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
+                        const __grid_constant__ CUtensorMap tmC, const __grid_constant__ GemmParams gp,
+                        DevPlan* plan) {
+  extern __shared__ uint8_t smem_raw[];
+  if (plan->status) return;
+  const int P = gp.P_fixed ? gp.P_fixed : plan->P;
+  const int total = P * gp.mt * gp.nt;
+  const int nc_tile = (gp.kb_total + KC_BLOCKS - 1) / KC_BLOCKS;
+
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint8_t* stage_base = smem;
+  uint8_t* out_base = smem + STAGES * STAGE_BYTES;
+  uint64_t* bars = reinterpret_cast<uint64_t*>(out_base + OUT_BYTES);
+  uint64_t* full = bars;
+  uint64_t* empty = bars + STAGES;
+  uint64_t* tfull = bars + 2 * STAGES;
+  uint64_t* tempty = bars + 2 * STAGES + 2;
+  uint64_t* drain = bars + 2 * STAGES + 4;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 2 * STAGES + 5);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+  volatile int* ep_flag = reinterpret_cast<volatile int*>(tmem_slot + 2);  // two ints
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  Ctl ctl{abort_flag, &plan->status, &plan->timeout_where, gp.wait_ns};
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < STAGES; ++s) {
+      mbar_init(smem_u32(&full[s]), 1);
+      mbar_init(smem_u32(&empty[s]), 1);
+    }
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(smem_u32(&tfull[b]), 1);
+      mbar_init(smem_u32(&tempty[b]), 4);
+    }
+    mbar_init(smem_u32(drain), 1);
+    *abort_flag = 0;
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+  }
+  if (warp == 1) {
+    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(tmem_slot)),
+                 "r"((uint32_t)TMEM_COLS));
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;");
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem_base = *tmem_slot;
+
+  if (warp == 0) {
+    // ------------------------------------------------------------ producer
+    if (lane == 0) {
+      int stage = 0;
+      uint32_t phase = 0;
+      bool issued[STAGES] = {};
+      uint32_t issued_phase[STAGES] = {};
+      bool ok = true;
+      for (int t = blockIdx.x; t < total && ok; t += gridDim.x) {
+        TileCoord tc = tile_coord(t, gp.mt, gp.nt);
+        for (int kb = 0; kb < gp.kb_total; ++kb) {
+          if (!wait_bounded(smem_u32(&empty[stage]), phase ^ 1u, ctl, 1)) {
+            ok = false;
+            break;
+          }
+          uint32_t fb = smem_u32(&full[stage]);
+          mbar_arrive_expect_tx(fb, STAGE_BYTES);
+          uint32_t a_dst = smem_u32(stage_base + stage * STAGE_BYTES);
+          uint32_t b_dst = a_dst + A_BYTES;
+          tma_load_3d(a_dst, &tmA, fb, kb * BK, tc.m * BM, tc.p);
+#pragma unroll
+          for (int j = 0; j < BN / 64; ++j) tma_load_3d(b_dst + j * B_SLAB, &tmB, fb, tc.n * BN + 64 * j, kb * BK, tc.p);
+          issued[stage] = true;
+          issued_phase[stage] = phase;
+          if (++stage == STAGES) {
+            stage = 0;
+            phase ^= 1u;
+          }
+        }
+      }
+      if (!ok) {  // let issued copies land before the block exits
+        Ctl drain_ctl = ctl;
+        volatile int never = 0;
+        drain_ctl.abort = &never;
+        for (int s = 0; s < STAGES; ++s)
+          if (issued[s]) wait_bounded(smem_u32(&full[s]), issued_phase[s], drain_ctl, 0);
+      }
+    }
+  } else if (warp == 1) {
+    // ------------------------------------------------------------ MMA issuer
+    if (lane == 0) {
+      int stage = 0;
+      uint32_t phase = 0, acc_iter = 0;
+      bool ok = true, any = false;
+      for (int t = blockIdx.x; t < total && ok; t += gridDim.x) {
+        for (int c = 0; c < nc_tile && ok; ++c) {
+          const uint32_t b = acc_iter & 1u, aph = (acc_iter >> 1) & 1u;
+          if (!wait_bounded(smem_u32(&tempty[b]), aph ^ 1u, ctl, 2)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint32_t d = tmem_base + b * BN;
+          const int kb0 = c * KC_BLOCKS;
+          const int kb1 = min(kb0 + KC_BLOCKS, gp.kb_total);
+          for (int kb = kb0; kb < kb1; ++kb) {
+            if (!wait_bounded(smem_u32(&full[stage]), phase, ctl, 3)) {
+              ok = false;
+              break;
+            }
+            tc_fence_after();
+            const uint32_t a_addr = smem_u32(stage_base + stage * STAGE_BYTES);
+            const uint64_t adesc = sw128_desc(a_addr, 16, 1024);
+            const uint64_t bdesc = sw128_desc(a_addr + A_BYTES, B_SLAB, 1024);
+#pragma unroll
+            for (int kk = 0; kk < BK / 16; ++kk) {
+              const uint32_t acc = (c >= 2 || kb > kb0 || kk > 0) ? 1u : 0u;
+              umma_f16(d, adesc + (uint64_t)(2 * kk), bdesc + (uint64_t)(128 * kk), IDESC, acc);
+            }
+            any = true;
+            umma_commit(smem_u32(&empty[stage]));
+            if (++stage == STAGES) {
+              stage = 0;
+              phase ^= 1u;
+            }
+          }
+          if (!ok) break;
+          if (!(gp.fault == 1 && acc_iter == 0)) umma_commit(smem_u32(&tfull[b]));
+          ++acc_iter;
+        }
+      }
+      if (!ok && any) {  // all issued MMAs must finish before the memory is freed
+        Ctl drain_ctl = ctl;
+        volatile int never = 0;
+        drain_ctl.abort = &never;
+        umma_commit(smem_u32(drain));
+        wait_bounded(smem_u32(drain), 0, drain_ctl, 0);
+      }
+    }
+  } else {
+    // ------------------------------------------------------------ epilogue
+    const int q4 = warp & 3;  // tensor-memory lane quarter this warp may access
+    const int row = q4 * 32 + lane;
+    const int et = threadIdx.x - 64;  // 0..127
+    uint32_t acc_iter = 0;
+    bool ok = true;
+    const uint32_t out_s = smem_u32(out_base);
+    for (int t = blockIdx.x; t < total && ok; t += gridDim.x) {
+      TileCoord tc = tile_coord(t, gp.mt, gp.nt);
+      const float q = gp.qf[tc.p], iq = gp.invq[tc.p];
+      bool first_write = true;
+      for (int c = 0; c < nc_tile; ++c) {
+        const uint32_t b = acc_iter & 1u, aph = (acc_iter >> 1) & 1u;
+        // One thread waits (bounded) and publishes the outcome, so all 128
+        // threads take the same branch; the flag is double-buffered because a
+        // thread can reach the next chunk's wait before the others read it.
+        if (et == 0) ep_flag[acc_iter & 1u] = wait_bounded(smem_u32(&tfull[b]), aph, ctl, 4) ? 1 : 0;
+        epilogue_bar();
+        if (!ep_flag[acc_iter & 1u]) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        const uint32_t taddr = tmem_base + ((uint32_t)(q4 * 32) << 16) + b * BN;
+        const int mode = (c + 2 < nc_tile) ? 0 : (c + 2 == nc_tile ? 1 : 2);  // partial, carry, final
+        if (mode != 0 && first_write) {
+          if (et == 0) bulk_wait_read0();  // the previous tile's store has read the staging
+          epilogue_bar();
+          first_write = false;
+        }
+#pragma unroll 1
+        for (int col = 0; col < BN; col += 32) {
+          uint32_t r[32];
+          tmem_ld32(taddr + col, r);
+          tmem_wait_ld();
+          if (mode == 0) {
+            const float magic = 12582912.0f;
+#pragma unroll
+            for (int i = 0; i < 32; ++i) {
+              float x = __uint_as_float(r[i]);
+              float tq = __fadd_rn(__fmaf_rn(x, iq, magic), -magic);
+              r[i] = __float_as_uint(__fmaf_rn(-tq, q, x));
+            }
+            tmem_st32(taddr + col, r);
+          } else {
+            const int half = col >> 7;
+            const int j0 = (col & 127) >> 4;
+            uint8_t* hbase = out_base + half * OUT_HALF;
+            uint4* p0 = reinterpret_cast<uint4*>(hbase + sw128_off(row, j0));
+            uint4* p1 = reinterpret_cast<uint4*>(hbase + sw128_off(row, j0 + 1));
+            uint32_t carry[8] = {0, 0, 0, 0, 0, 0, 0, 0};
+            if (mode == 2 && nc_tile >= 2) {
+              uint4 c0 = *p0, c1 = *p1;
+              carry[0] = c0.x; carry[1] = c0.y; carry[2] = c0.z; carry[3] = c0.w;
+              carry[4] = c1.x; carry[5] = c1.y; carry[6] = c1.z; carry[7] = c1.w;
+            }
+            uint32_t packed[8];
+#pragma unroll
+            for (int w = 0; w < 8; ++w) {
+              uint32_t word = 0;
+#pragma unroll
+              for (int k = 0; k < 4; ++k) {
+                float v = pos_mod(__uint_as_float(r[4 * w + k]), q, iq);
+                v += (float)((carry[w] >> (8 * k)) & 0xFFu);
+                v = v >= q ? v - q : v;
+                word |= ((uint32_t)v) << (8 * k);
+              }
+              packed[w] = word;
+            }
+            *p0 = make_uint4(packed[0], packed[1], packed[2], packed[3]);
+            *p1 = make_uint4(packed[4], packed[5], packed[6], packed[7]);
+          }
+        }
+        if (mode == 0) tmem_wait_st();
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(smem_u32(&tempty[b]));
+        if (mode == 2) {
+          fence_proxy_async_smem();
+          epilogue_bar();
+          if (et == 0) {
+            tma_store_3d(&tmC, out_s, tc.n * BN, tc.m * BM, tc.p);
+            if (tc.n * BN + 128 < gp.N) tma_store_3d(&tmC, out_s + OUT_HALF, tc.n * BN + 128, tc.m * BM, tc.p);
+            bulk_commit();
+          }
+        }
+        ++acc_iter;
+      }
+    }
+    if (et == 0) bulk_wait0();
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem_base), "r"((uint32_t)TMEM_COLS));
+  }
+}
+
+// ---------------------------------------------------------------------------
+// Host side
+// ---------------------------------------------------------------------------
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    cudaDriverEntryPointQueryResult qr;
+    void* p = nullptr;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &qr) ==
+            cudaSuccess &&
+        qr == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+  });
+  return fn;
+}
+
+bool make_map_3d(CUtensorMap* m, CUtensorMapDataType dt, int esize, const void* base, uint64_t d0, uint64_t d1,
+                 uint64_t d2, uint64_t stride1_bytes, uint64_t stride2_bytes, uint32_t b0, uint32_t b1) {
+  auto fn = encode_fn();
+  if (!fn) return false;
+  cuuint64_t dims[3] = {d0, d1, d2};
+  cuuint64_t strides[2] = {stride1_bytes, stride2_bytes};
+  cuuint32_t box[3] = {b0, b1, 1};
+  cuuint32_t es[3] = {1, 1, 1};
+  (void)esize;
+  CUresult r = fn(m, dt, 3, const_cast<void*>(base), dims, strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                  CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
+int g_gemm_ready[64];
+
+}  // namespace
+
+cudaError_t launch_gemm(const void* RA, long long lda, const void* RB, long long ldb, void* RC, long long ldc,
+                        int pmax, int P_fixed, long long M, long long N, long long K, DevPlan* plan, cudaStream_t st,
+                        int fault, unsigned long long wait_ns) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+  static int sms[64];
+  if (!g_gemm_ready[dev]) {
+    e = cudaFuncSetAttribute(residue_gemm_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
+    if (e != cudaSuccess) return e;
+    cudaDeviceGetAttribute(&sms[dev], cudaDevAttrMultiProcessorCount, dev);
+    g_gemm_ready[dev] = 1;
+  }
+  CUtensorMap ma, mb, mc;
+  if (!make_map_3d(&ma, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, RA, (uint64_t)K, (uint64_t)M, (uint64_t)pmax,
+                   (uint64_t)lda * 2, (uint64_t)M * lda * 2, BK, BM) ||
+      !make_map_3d(&mb, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, RB, (uint64_t)N, (uint64_t)K, (uint64_t)pmax,
+                   (uint64_t)ldb * 2, (uint64_t)K * ldb * 2, 64, BK) ||
+      !make_map_3d(&mc, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, RC, (uint64_t)N, (uint64_t)M, (uint64_t)pmax, (uint64_t)ldc,
+                   (uint64_t)M * ldc, 128, 128))
+    return cudaErrorInvalidValue;
+  GemmParams gp;
+  gp.M = (int)M;
+  gp.N = (int)N;
+  gp.K = (int)K;
+  gp.mt = (int)((M + BM - 1) / BM);
+  gp.nt = (int)((N + BN - 1) / BN);
+  gp.kb_total = (int)((K + BK - 1) / BK);
+  gp.P_fixed = P_fixed;
+  gp.fault = fault;
+  gp.wait_ns = wait_ns;
+  const Tables& t = host_tables();
+  for (int i = 0; i < kNumPrimes; ++i) {
+    gp.qf[i] = t.qf[i];
+    gp.invq[i] = t.invq[i];
+  }
+  long long tiles = (long long)pmax * gp.mt * gp.nt;
+  int grid = (int)(tiles < sms[dev] ? tiles : sms[dev]);
+  if (grid < 1) grid = 1;
+  residue_gemm_kernel<<<grid, NUM_THREADS, SMEM_BYTES, st>>>(ma, mb, mc, gp, plan);
+  return cudaGetLastError();
+}
+
+}  // namespace rg

@@ -1,0 +1,91 @@
+// rg_common.cuh -- types, tables and device helpers shared by the library's
+// translation units (never by the oracle).
+#pragma once
+#include <cstddef>
+#include <cstdint>
+
+#include <cuda_runtime.h>
+
+#include "../../include/resgemm.h"
+
+namespace rg {
+
+constexpr int kNumPrimes = RG_NUM_PRIMES;  // odd primes 3..251, largest first
+constexpr int kChunkBits = 12;             // operand split into 12-bit chunks
+constexpr int kMaxChunks = 24;             // covers 256-bit operands (22) with slack
+constexpr int kGarnerWords = 14;           // ceil(53 / 4) int8x4 words per Garner row
+constexpr int kMaxLimbsOut = RG_MAX_LIMBS_OUT;
+
+// Plan of one call, kept in the first bytes of the workspace.  The planner
+// kernels fill the reduction fields with atomics (so the host zeroes the block
+// first); the split kernel derives the rest identically in every block and
+// block 0 writes it back for the later kernels.
+struct DevPlan {
+  int status;             // RG_OK or the first device-side error (atomicCAS from 0)
+  int P;                  // primes used
+  int bits_a, bits_b;     // bit length of max |entry| (scaled entries for fp64)
+  int bound_bits;         // bits_a + bits_b + ceil(log2 K)
+  int f_a, f_b;           // fp64 scale exponents
+  int lossless;           // fp64: 1 if the scaling is exact
+  int nchunk_a, nchunk_b; // 12-bit chunks the split reads per entry
+  int pad0[6];
+  // reductions written by the planner kernels
+  unsigned long long maxmag_a, maxmag_b;  // int64 operands: max |x|
+  int maxbits_a, maxbits_b;               // limb operands: max bit length of |x|
+  int maxe_a, maxe_b;                     // fp64: max of max(biased exponent, 1) over nonzero entries
+  int inv_mine_a, inv_mine_b;             // fp64: 4096 - min of that exponent (0 = no nonzero entry)
+  int nonfinite;                          // fp64: an inf or nan entry was seen
+  int pad1[7];
+  // diagnostics of a bounded wait that expired (which role, which wait)
+  int timeout_where;
+  int pad2[15];
+};
+static_assert(sizeof(DevPlan) <= 256, "plan block");
+
+// Constant tables for the split and Garner kernels, computed on the host once.
+struct Tables {
+  int q[kNumPrimes];                          // q_0 = 251 > q_1 > ... > q_52 = 3
+  float qf[kNumPrimes];                       // q as float
+  float invq[kNumPrimes];                     // fl(1/q)
+  float chunk_w[kNumPrimes][kMaxChunks];      // balanced 2^(12c) mod q, as float
+  int log2P[kNumPrimes + 1];                  // floor(log2(q_0 * ... * q_{n-1})), n = 0..53
+  // Balanced Garner: v_i = bal( ginv[i] * r_i - sum_{j<i} gd[i][j] * v_j  mod q_i )
+  // with ginv[i] = bal(Q_i^-1 mod q_i), gd[i][j] = bal((Q_j mod q_i) * Q_i^-1 mod q_i),
+  // Q_i = q_0 * ... * q_{i-1}.  gd rows are packed 4 per int32 for dp4a.
+  int ginv[kNumPrimes];
+  int gd_packed[kNumPrimes][kGarnerWords];
+};
+
+// Host side: the tables (built once) and the primes.
+const Tables& host_tables();
+
+// ---------------------------------------------------------------------------
+// Device helpers
+// ---------------------------------------------------------------------------
+
+// Balanced residue of an integer-valued float s, |s| < 2^24, modulo odd q:
+// the unique r == s (mod q) with |r| <= (q-1)/2.  The quotient estimate
+// rint(s * fl(1/q)) is within one of round(s/q), so one correction on each
+// side suffices; every operation is exact on these integers.
+__device__ __forceinline__ float bal_mod(float s, float q, float invq) {
+  const float magic = 12582912.0f;  // 1.5 * 2^23: adding it rounds to an integer
+  float t = __fadd_rn(__fmaf_rn(s, invq, magic), -magic);
+  float r = __fmaf_rn(-t, q, s);
+  float h = 0.5f * (q - 1.0f);
+  r = r > h ? r - q : r;
+  r = r < -h ? r + q : r;
+  return r;
+}
+
+// Residue in [0, q) of an integer-valued float s, |s| < 2^24.
+__device__ __forceinline__ float pos_mod(float s, float q, float invq) {
+  float t = floorf(s * invq);
+  float r = __fmaf_rn(-t, q, s);
+  r = r < 0.0f ? r + q : r;
+  r = r >= q ? r - q : r;
+  return r;
+}
+
+__device__ __forceinline__ void set_status(int* status, int code) { atomicCAS(status, 0, code); }
+
+}  // namespace rg

@@ -1,0 +1,98 @@
+// tables.cpp -- host computation of the residue base and its constants.
+//
+// The residue base is the 53 odd primes below 256, largest first.  The pages
+// ("exact-solve" and "enclosure-gemm", Method) use the primes below 256 and
+// need an odd modulus; their capacity gate bits_a + bits_b + ceil(log2 K) <= 332
+// is exactly floor(log2((P - 1) / 2)) for the product P of the 53 odd primes.
+#include <cstdint>
+#include <cstring>
+#include <mutex>
+
+#include "rg_common.cuh"
+
+namespace rg {
+namespace {
+
+int mod_pow(int a, int e, int q) {
+  long long r = 1, b = a % q;
+  while (e > 0) {
+    if (e & 1) r = r * b % q;
+    b = b * b % q;
+    e >>= 1;
+  }
+  return (int)r;
+}
+
+int balanced(int r, int q) {  // r in [0, q) -> [-(q-1)/2, (q-1)/2]
+  return r > (q - 1) / 2 ? r - q : r;
+}
+
+void build(Tables& t) {
+  std::memset(&t, 0, sizeof(t));
+  // odd primes below 256, descending
+  bool composite[256] = {};
+  int n = 0;
+  int asc[kNumPrimes];
+  for (int i = 2; i < 256; ++i) {
+    if (composite[i]) continue;
+    for (int j = i * i; j < 256; j += i) composite[j] = true;
+    if (i != 2) asc[n++] = i;
+  }
+  for (int i = 0; i < kNumPrimes; ++i) t.q[i] = asc[kNumPrimes - 1 - i];
+
+  for (int i = 0; i < kNumPrimes; ++i) {
+    int q = t.q[i];
+    t.qf[i] = (float)q;
+    t.invq[i] = 1.0f / (float)q;
+    for (int c = 0; c < kMaxChunks; ++c) t.chunk_w[i][c] = (float)balanced(mod_pow(2, kChunkBits * c, q), q);
+  }
+
+  // floor(log2) of the running product, with an exact multi-word product.
+  uint32_t big[16] = {1};
+  t.log2P[0] = 0;
+  for (int n2 = 1; n2 <= kNumPrimes; ++n2) {
+    uint64_t carry = 0;
+    for (int w = 0; w < 16; ++w) {
+      uint64_t v = (uint64_t)big[w] * (uint64_t)t.q[n2 - 1] + carry;
+      big[w] = (uint32_t)v;
+      carry = v >> 32;
+    }
+    int top = 15;
+    while (top > 0 && big[top] == 0) --top;
+    int b = 31;
+    while (!((big[top] >> b) & 1)) --b;
+    t.log2P[n2] = 32 * top + b;
+  }
+
+  // Garner constants.
+  for (int i = 0; i < kNumPrimes; ++i) {
+    int q = t.q[i];
+    long long Qi = 1;  // Q_i mod q
+    for (int j = 0; j < i; ++j) Qi = Qi * t.q[j] % q;
+    int inv = mod_pow((int)Qi, q - 2, q);  // q prime
+    t.ginv[i] = balanced(inv, q);
+    long long Qj = 1;  // Q_j mod q, j = 0..i-1
+    for (int j = 0; j < i; ++j) {
+      int d = balanced((int)(Qj * inv % q), q);
+      uint32_t byte = (uint32_t)(uint8_t)(int8_t)d;
+      t.gd_packed[i][j / 4] |= (int)(byte << (8 * (j % 4)));
+      Qj = Qj * t.q[j] % q;
+    }
+  }
+}
+
+}  // namespace
+
+const Tables& host_tables() {
+  static Tables t;
+  static std::once_flag once;
+  std::call_once(once, [] { build(t); });
+  return t;
+}
+
+}  // namespace rg
+
+extern "C" int rg_prime(int i) {
+  if (i < 0 || i >= rg::kNumPrimes) return 0;
+  return rg::host_tables().q[i];
+}

@@ -1,0 +1,205 @@
+/*
+ * resgemm.h -- exact matrix products through residues modulo small primes,
+ * for one GB300 (sm_103a) GPU.
+ *
+ * The method (pages "exact-solve" and "enclosure-gemm", section Method):
+ * every integer operand entry is reduced to a balanced residue modulo each
+ * of the odd primes below 256 that the bound needs; one tensor-core product
+ * per prime yields the product matrix modulo that prime; balanced Garner
+ * mixed-radix reconstruction then rebuilds every signed entry exactly.  For
+ * binary64 operands, a power-of-two fixed-point scaling turns the operands
+ * into integers first, and an integer-only epilogue rounds the exact product
+ * outward once into an IEEE (lo, hi) pair.
+ *
+ * Conventions shared by every entry point
+ * ----------------------------------------
+ *  - Matrices are dense and row-major: A is [M][K], B is [K][N], outputs are
+ *    [M][N].  Multi-limb integers keep their limbs innermost ([.][.][L]):
+ *    little-endian 64-bit limbs, two's complement, signed top limb.
+ *  - Pointers are device pointers, unless RG_FLAG_HOST is set; then A, B and
+ *    the outputs are host pointers (pinned memory gives asynchronous
+ *    copies) and the library stages them through the workspace.
+ *  - The caller owns every buffer, including the workspace `ws` of
+ *    `ws_bytes` bytes (device memory, 256-byte aligned), sized by
+ *    rg_workspace_bytes().  The library allocates no device memory.
+ *  - All work is ordered on `stream` (a cudaStream_t; NULL = legacy default
+ *    stream).  Without RG_FLAG_SYNC a call only enqueues work: it returns
+ *    RG_OK once the arguments are accepted, and errors found on the device
+ *    (range, non-finite operand, time-out) are read later with rg_status().
+ *    With RG_FLAG_SYNC (implied by RG_FLAG_HOST) the call synchronises the
+ *    stream and returns the device status.
+ *  - On any error the outputs are unspecified.
+ *  - Calls sharing one workspace must not overlap on the GPU; calls on
+ *    different workspaces may run concurrently.
+ */
+#ifndef RESGEMM_H
+#define RESGEMM_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Status codes. */
+#define RG_OK 0
+#define RG_ERR_ARG 1        /* null pointer, non-positive size, bad limb count, misaligned workspace */
+#define RG_ERR_RANGE 2      /* K > 2^17, or the product bound exceeds the primes or the output width */
+#define RG_ERR_NONFINITE 3  /* an fp64 operand entry is inf or nan */
+#define RG_ERR_LOSSY 4      /* fp64 operands do not scale losslessly into the fixed point */
+#define RG_ERR_WORKSPACE 5  /* workspace too small */
+#define RG_ERR_CUDA 6       /* a CUDA runtime or driver call failed */
+#define RG_ERR_TIMEOUT 7    /* a bounded wait inside a kernel expired; the kernel stopped early */
+
+/* Flags. */
+#define RG_FLAG_SYNC 1u /* synchronise the stream before returning; return the device status */
+#define RG_FLAG_HOST 2u /* A, B and the outputs are host pointers; implies RG_FLAG_SYNC */
+
+/* Operations, for rg_workspace_bytes() and rg_workspace_layout(). */
+#define RG_OP_I64 0
+#define RG_OP_LIMBS 1
+#define RG_OP_ENCLOSE 2
+#define RG_OP_STAGE 3
+
+/* Limits. */
+#define RG_MAX_K 131072 /* K <= 2^17 ("exact-solve" and "enclosure-gemm", Requirements and limits) */
+#define RG_NUM_PRIMES 53 /* the odd primes 3..251 */
+#define RG_MAX_BOUND_BITS 332 /* bits_a + bits_b + ceil(log2 K) <= 332 ("enclosure-gemm", Requirements) */
+#define RG_MAX_LIMBS_IN 4 /* operands of up to 256 bits ("enclosure-gemm", Method: four int64 limbs) */
+#define RG_MAX_LIMBS_OUT 6 /* results of up to 384 bits ("enclosure-gemm", Method: signed 384-bit arithmetic) */
+
+/*
+ * Exact C = A * B for int64 A [M][K] and B [K][N]; C is int64 [M][N].
+ * ("exact-solve", Method: one product per prime below 256 on balanced
+ * residues, balanced-Garner reconstruction.)
+ *
+ * nprimes = 0 plans on the device: it takes max |A|, max |B| and uses the
+ * fewest primes (largest first) whose product P satisfies
+ * P > 2^(bits_a + bits_b + ceil(log2 K) + 1), bits_x being the bit length of
+ * max |x|.  nprimes in [1, 53] skips the planner: the caller then guarantees
+ * |C| <= (P - 1) / 2 for the product P of the nprimes largest primes, and the
+ * entries must fit in 64 bits, as they always do.
+ * Errors: RG_ERR_ARG (sizes <= 0, null pointers, nprimes out of range),
+ * RG_ERR_RANGE (K > 2^17; the exact bound K * max|A| * max|B| exceeds
+ * 2^63 - 1, so C might not fit int64), RG_ERR_WORKSPACE, RG_ERR_CUDA,
+ * RG_ERR_TIMEOUT.
+ */
+int res_gemm_i64(const int64_t* A, const int64_t* B, int64_t* C, int64_t M, int64_t N, int64_t K, int nprimes,
+                 unsigned flags, void* ws, size_t ws_bytes, void* stream);
+
+/*
+ * Exact C = A * B for multi-limb operands: A [M][K][la], B [K][N][lb]
+ * (1 <= la, lb <= 4), C [M][N][lc] (1 <= lc <= 6), limb layout as above.
+ * ("enclosure-gemm", Method: integers of up to four int64 limbs, balanced
+ * Garner digits in signed 384-bit arithmetic.)
+ *
+ * nprimes as for res_gemm_i64, with bits_x the bit length of the largest
+ * |entry|.  Errors: RG_ERR_RANGE when K > 2^17, when
+ * bits_a + bits_b + ceil(log2 K) > 332 (the 53 primes cannot hold the
+ * product), or when that bound exceeds 64 * lc - 1 bits (C might not fit lc
+ * limbs); otherwise as for res_gemm_i64.
+ */
+int res_gemm_limbs(const int64_t* A, int la, const int64_t* B, int lb, int64_t* C, int lc, int64_t M, int64_t N,
+                   int64_t K, int nprimes, unsigned flags, void* ws, size_t ws_bytes, void* stream);
+
+/*
+ * Outward enclosure of the exact product of binary64 matrices:
+ * lo[i][j] <= sum_k A[i][k] * B[k][j] <= hi[i][j] in exact real arithmetic.
+ * ("enclosure-gemm", Method.)
+ *
+ * Each operand is scaled by its own power of two 2^F, F being the finest
+ * binary point among its entries, so every scaled entry is an integer
+ * (lossless).  The exact integer S = sum A'B' and Q = F_a + F_b are turned
+ * into bit patterns: a zero remainder gives lo == hi == S * 2^-Q; otherwise
+ * the truncated value is the endpoint toward zero and the next encoding the
+ * endpoint away from zero; beyond the largest finite value the endpoint
+ * toward zero is +-max finite and the other +-inf.  S == 0 gives +0.0 for
+ * both; a negative value too small for a subnormal gives [-2^-1074, -0.0].
+ * No floating-point instruction touches the result.
+ * Errors: RG_ERR_NONFINITE (an inf or nan entry), RG_ERR_LOSSY (an operand
+ * spans more than 255 bits, or bits_a + bits_b + ceil(log2 K) > 332: the
+ * lossy regime of the page is not provided), RG_ERR_RANGE (K > 2^17), and
+ * the errors of res_gemm_i64.
+ */
+int enclose_gemm_f64(const double* A, const double* B, double* lo, double* hi, int64_t M, int64_t N, int64_t K,
+                     unsigned flags, void* ws, size_t ws_bytes, void* stream);
+
+/*
+ * The per-prime tensor-core stage alone, on caller-provided residues:
+ * RC[p][m][n] = (sum_k RA[p][m][k] * RB[p][k][n]) mod q_p, in [0, q_p), for
+ * the nprimes largest primes q_0 = 251 > q_1 = 241 > ...
+ * ("exact-solve", Method: per-prime products as one batched GEMM.)
+ *
+ * RA: fp16 bit patterns [nprimes][M][lda], lda >= K, lda % 8 == 0.
+ * RB: fp16 bit patterns [nprimes][K][ldb], ldb >= N, ldb % 64 == 0.
+ * RC: uint8 [nprimes][M][ldc], ldc >= N, ldc % 16 == 0.
+ * Every residue must be an integer in [-125, 125]; RA columns k >= K and RB
+ * columns n >= N are not read.  ws needs rg_workspace_bytes(RG_OP_STAGE, ...).
+ * Errors: RG_ERR_ARG, RG_ERR_RANGE (K > 2^17), RG_ERR_CUDA, RG_ERR_TIMEOUT.
+ */
+int res_gemm_stage(const uint16_t* RA, int64_t lda, const uint16_t* RB, int64_t ldb, uint8_t* RC, int64_t ldc,
+                   int nprimes, int64_t M, int64_t N, int64_t K, unsigned flags, void* ws, size_t ws_bytes,
+                   void* stream);
+
+/*
+ * Workspace size in bytes for one call of `op` (RG_OP_*) with these shapes.
+ * la, lb, lc are the limb counts (1 for RG_OP_I64 / RG_OP_ENCLOSE); nprimes
+ * is the value the call will pass (0 = plan on the device).  flags must
+ * match the call's RG_FLAG_HOST bit.  Returns 0 for invalid arguments.
+ */
+size_t rg_workspace_bytes(int op, int64_t M, int64_t N, int64_t K, int la, int lb, int lc, int nprimes,
+                          unsigned flags);
+
+/* Offsets (bytes from ws) of the stage buffers a call leaves in its
+ * workspace, for inspection:
+ *   ra: fp16 residues of A, [pmax][M][lda]   (lda = K rounded up to 8)
+ *   rb: fp16 residues of B, [pmax][K][ldb]   (ldb = N rounded up to 64)
+ *   rc: uint8 product residues, [pmax][M][ldc] (ldc = N rounded up to 16)
+ * Residue planes follow the prime order q_0 = 251, q_1 = 241, ... */
+typedef struct {
+  size_t ra, rb, rc;
+  int64_t lda, ldb, ldc;
+  int pmax;
+} rg_layout;
+int rg_workspace_layout(int op, int64_t M, int64_t N, int64_t K, int la, int lb, int lc, int nprimes,
+                        unsigned flags, rg_layout* out);
+
+/* The plan a call chose, read back from its workspace after the stream is
+ * synchronised ("enclosure-gemm", Method: return_info reports the regime). */
+typedef struct {
+  int status;   /* RG_OK or the first error the device recorded */
+  int nprimes;  /* primes used */
+  int bits_a;   /* bit length of the largest |entry| (scaled entry for fp64) */
+  int bits_b;
+  int bound_bits; /* bits_a + bits_b + ceil(log2 K) */
+  int f_a;      /* fp64 only: A' = A * 2^f_a */
+  int f_b;
+  int lossless; /* fp64 only: 1 if both operands scaled exactly */
+} rg_plan_info;
+int rg_get_plan(const void* ws, void* stream, rg_plan_info* out);
+
+/* Synchronise `stream` and return the device status of the last call that
+ * used `ws` (RG_OK, RG_ERR_RANGE, RG_ERR_NONFINITE, RG_ERR_LOSSY,
+ * RG_ERR_TIMEOUT) or RG_ERR_CUDA. */
+int rg_status(const void* ws, void* stream);
+
+/* The i-th prime of the residue base, largest first (251, 241, ...);
+ * 0 if i is out of range. */
+int rg_prime(int i);
+
+/* A static description of a status code. */
+const char* rg_strerror(int code);
+
+/* Test hook: the time limit (nanoseconds) of every bounded wait inside the
+ * library's kernels (default one second), and a fault to inject into the next
+ * tensor-core stage: 1 = its producer never signals the first accumulator,
+ * so the consumer's wait must expire and return RG_ERR_TIMEOUT.  Returns the
+ * previous limit.  Not thread-safe; for tests only. */
+uint64_t rg_set_wait_limit_ns(uint64_t ns);
+void rg_inject_fault(int kind);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* RESGEMM_H */

@@ -1,0 +1,117 @@
+"""The C-ABI library loads and exports what include/resgemm.h declares (no GPU).
+
+Only entry points that return before touching the device are called here:
+argument validation, workspace sizing and the prime table.
+"""
+import ctypes
+import os
+import re
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "resgemm.h")
+
+
+@pytest.fixture(scope="module")
+def rg():
+    from exact_modular_int8_gb300 import build as b
+    b.build()
+    import exact_modular_int8_gb300 as m
+    return m
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    names = re.findall(r"^\s*(?:const\s+)?[A-Za-z_][A-Za-z0-9_]*\s*\*?\s*([a-z_][a-z0-9_]*)\s*\(", text, flags=re.M)
+    return sorted(set(n for n in names if n not in {"if", "while", "for", "return", "sizeof"}))
+
+
+def test_header_declares_the_entry_points():
+    names = declared_functions()
+    for f in ("res_gemm_i64", "res_gemm_limbs", "enclose_gemm_f64"):
+        assert f in names
+
+
+def test_every_declared_symbol_is_exported(rg):
+    lib = ctypes.CDLL(rg.LIB_PATH)
+    missing = [n for n in declared_functions() if not hasattr(lib, n)]
+    assert not missing, missing
+    assert set(rg.EXPORTED) == set(declared_functions())
+
+
+def _is_prime(n):
+    return n > 1 and all(n % d for d in range(2, int(n**0.5) + 1))
+
+
+def test_prime_base(rg):
+    ps = rg.primes()
+    assert ps == sorted([p for p in range(3, 256) if _is_prime(p)], reverse=True)
+    assert len(ps) == 53 and ps[0] == 251 and ps[-1] == 3
+    assert rg.library().rg_prime(53) == 0 and rg.library().rg_prime(-1) == 0
+    # The pages' gate bits_a + bits_b + ceil(log2 K) <= 332 is floor(log2((P-1)/2))
+    # for the product P of these primes.
+    P = 1
+    for p in ps:
+        P *= p
+    assert ((P - 1) // 2).bit_length() - 1 == 332
+
+
+def test_strerror(rg):
+    assert rg.strerror(0) == "ok"
+    for code in range(1, 8):
+        assert rg.strerror(code) != "unknown status"
+    assert rg.strerror(99) == "unknown status"
+
+
+def test_workspace_sizes(rg):
+    # i64 plans for at most 9 primes; planes of fp16 A and B residues and uint8 C residues.
+    L = rg.workspace_layout(rg.RG_OP_I64, 64, 64, 64)
+    assert L.pmax == 9 and L.lda == 64 and L.ldb == 64 and L.ldc == 64
+    n = rg.workspace_bytes(rg.RG_OP_I64, 64, 64, 64)
+    assert n >= 4096 + 9 * (64 * 64 * 2 * 2 + 64 * 64)
+    assert rg.workspace_bytes(rg.RG_OP_I64, 64, 64, 64, nprimes=7) < n
+    L = rg.workspace_layout(rg.RG_OP_I64, 65, 77, 129)
+    assert (L.lda, L.ldb, L.ldc) == (136, 128, 80)
+    assert L.ra % 4096 == 0 and L.rb % 4096 == 0 and L.rc % 4096 == 0
+    assert rg.workspace_layout(rg.RG_OP_ENCLOSE, 8, 8, 8).pmax == 53
+    assert rg.workspace_bytes(rg.RG_OP_I64, 64, 64, 64, host=True) > n
+    assert rg.workspace_bytes(rg.RG_OP_I64, 0, 64, 64) == 0
+    assert rg.workspace_bytes(rg.RG_OP_LIMBS, 4, 4, 4, la=5, lb=1, lc=2) == 0
+    assert rg.workspace_bytes(rg.RG_OP_LIMBS, 4, 4, 4, la=2, lb=2, lc=7) == 0
+
+
+def test_argument_errors_need_no_device(rg):
+    lib = rg.library()
+    buf = (ctypes.c_int64 * 16)()
+    p = ctypes.addressof(buf)
+    ws = (ctypes.c_uint8 * 8192)()
+    wsp = (ctypes.addressof(ws) + 255) // 256 * 256
+    # null operand
+    assert lib.res_gemm_i64(None, p, p, 2, 2, 2, 0, 0, wsp, 4096, None) == rg.RG_ERR_ARG
+    # bad sizes
+    assert lib.res_gemm_i64(p, p, p, 0, 2, 2, 0, 0, wsp, 4096, None) == rg.RG_ERR_ARG
+    assert lib.res_gemm_i64(p, p, p, 2, 2, 2, 54, 0, wsp, 4096, None) == rg.RG_ERR_ARG
+    # K > 2^17
+    assert lib.res_gemm_i64(p, p, p, 2, 2, 2**17 + 1, 0, 0, wsp, 4096, None) == rg.RG_ERR_RANGE
+    # workspace too small
+    assert lib.res_gemm_i64(p, p, p, 2, 2, 2, 0, 0, wsp, 16, None) == rg.RG_ERR_WORKSPACE
+    # misaligned workspace
+    assert lib.res_gemm_i64(p, p, p, 2, 2, 2, 0, 0, wsp + 8, 1 << 20, None) == rg.RG_ERR_ARG
+    # limb counts
+    assert lib.res_gemm_limbs(p, 5, p, 1, p, 2, 2, 2, 2, 0, 0, wsp, 4096, None) == rg.RG_ERR_ARG
+    assert lib.res_gemm_limbs(p, 1, p, 1, p, 7, 2, 2, 2, 0, 0, wsp, 4096, None) == rg.RG_ERR_ARG
+    # enclosure needs both outputs
+    assert lib.enclose_gemm_f64(p, p, p, None, 2, 2, 2, 0, wsp, 4096, None) == rg.RG_ERR_ARG
+    # stage: leading dimensions and prime count
+    assert lib.res_gemm_stage(p, 7, p, 64, p, 16, 1, 2, 2, 2, 0, wsp, 4096, None) == rg.RG_ERR_ARG
+    assert lib.res_gemm_stage(p, 8, p, 64, p, 16, 0, 2, 2, 2, 0, wsp, 4096, None) == rg.RG_ERR_ARG
+    assert lib.res_gemm_stage(p, 8, p, 32, p, 16, 1, 2, 2, 2, 0, wsp, 4096, None) == rg.RG_ERR_ARG
+    assert lib.res_gemm_stage(p, 2**17 + 8, p, 64, p, 16, 1, 2, 2, 2**17 + 1, 0, wsp, 4096, None) == rg.RG_ERR_RANGE
+
+
+def test_wait_limit_roundtrip(rg):
+    lib = rg.library()
+    old = lib.rg_set_wait_limit_ns(12345)
+    assert lib.rg_set_wait_limit_ns(old) == 12345

@@ -1,0 +1,118 @@
+"""GPU parity of the fp64 enclosure (enclose_gemm_f64) against the CPU oracle.
+
+Both IEEE endpoints must match the oracle bit for bit wherever the scaling is
+lossless ("enclosure-gemm", Correctness: equal to the exact floor and ceiling
+in the format).
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from tests.gpu_util import dev, host, rg  # noqa: F401
+from tests.test_oracle_enclose import HAND_CASES
+from workloads import WORKLOADS, normal_matrices, sample_rows
+
+pytestmark = pytest.mark.gpu
+
+
+def bits(x):
+    return np.ascontiguousarray(x).view(np.uint64)
+
+
+def check_equal(rg, A, B, rows=None):
+    lo, hi = rg.enclose_gemm_f64(dev(A), dev(B))
+    lo, hi = host(lo), host(hi)
+    rlo, rhi = oracle.enclose_f64(A, B, rows=rows)
+    if rows is not None:
+        lo, hi = lo[rows], hi[rows]
+    assert np.array_equal(bits(lo), bits(rlo))
+    assert np.array_equal(bits(hi), bits(rhi))
+
+
+@pytest.mark.parametrize("A,B,lo,hi", HAND_CASES)
+def test_hand_cases(rg, A, B, lo, hi):
+    A = np.array(A, dtype=np.float64)
+    B = np.array(B, dtype=np.float64)
+    try:
+        glo, ghi = rg.enclose_gemm_f64(dev(A), dev(B))
+    except rg.ResGemmError as e:
+        assert e.code == rg.RG_ERR_LOSSY
+        pytest.skip("operand spread exceeds the lossless fixed point")
+    assert bits(host(glo))[0, 0] == bits(np.array([lo]))[0]
+    assert bits(host(ghi))[0, 0] == bits(np.array([hi]))[0]
+
+
+@pytest.mark.parametrize("M,N,K,seed", [(3, 4, 8, 0), (65, 77, 129, 1), (130, 260, 1030, 2), (1, 1, 1, 3),
+                                        (40, 300, 4096, 4)])
+def test_random_normal(rg, M, N, K, seed):
+    A, B = normal_matrices(M, N, K, seed)
+    check_equal(rg, A, B)
+
+
+def test_scaled_and_subnormal_operands(rg):
+    rng = np.random.default_rng(7)
+    A = rng.standard_normal((30, 50)) * 2.0**-1040  # subnormal and tiny normals
+    B = rng.standard_normal((50, 20)) * 2.0**-30
+    A[0, :4] = [5e-324, -5e-324, 1.5e-323, 0.0]
+    check_equal(rg, A, B)
+    A = rng.standard_normal((30, 50)) * 2.0**900
+    B = rng.standard_normal((50, 20)) * 2.0**120  # overflows to +-inf in places
+    check_equal(rg, A, B)
+    lo, hi = rg.enclose_gemm_f64(dev(A), dev(B))
+    assert bool(torch.isinf(hi).any() | torch.isinf(lo).any())
+
+
+def test_integer_operands_equal_plain_product(rg):
+    rng = np.random.default_rng(0)
+    A = rng.integers(-(2**20), 2**20, size=(70, 64)).astype(np.float64)
+    B = rng.integers(-(2**20), 2**20, size=(64, 90)).astype(np.float64)
+    lo, hi = rg.enclose_gemm_f64(dev(A), dev(B))
+    ref = A @ B
+    assert np.array_equal(host(lo), ref) and np.array_equal(host(hi), ref)
+
+
+def test_cancellation(rg):
+    A = np.array([[1e300, 1.0, -1e300, 2.0**-60]], dtype=np.float64)
+    B = np.ones((4, 1))
+    with pytest.raises(rg.ResGemmError) as e:  # 1e300 .. 2^-60 spans > 255 bits
+        rg.enclose_gemm_f64(dev(A), dev(B))
+    assert e.value.code == rg.RG_ERR_LOSSY
+    A = np.array([[2.0**100, 1.0, -(2.0**100), 3 * 2.0**-60]], dtype=np.float64)
+    check_equal(rg, A, B)
+
+
+def test_nonfinite_rejected(rg):
+    A = np.ones((4, 4))
+    A[1, 2] = np.nan
+    with pytest.raises(rg.ResGemmError) as e:
+        rg.enclose_gemm_f64(dev(A), dev(np.ones((4, 4))))
+    assert e.value.code == rg.RG_ERR_NONFINITE
+    B = np.ones((4, 4))
+    B[3, 3] = -np.inf
+    with pytest.raises(rg.ResGemmError) as e:
+        rg.enclose_gemm_f64(dev(np.ones((4, 4))), dev(B))
+    assert e.value.code == rg.RG_ERR_NONFINITE
+
+
+def test_enclose_normal_workload(rg):
+    w = WORKLOADS["enclose_normal"]
+    A, B = w.generate()
+    lo, hi = rg.enclose_gemm_f64(dev(A), dev(B))
+    plan = rg.get_plan()
+    assert plan["lossless"] == 1 and plan["status"] == 0
+    # one representable step everywhere ("enclosure-gemm", Usage: width_ulps(...).max() == 1)
+    width = rg.width_ulps(lo, hi)
+    assert int(width.max()) == 1 and int(width.min()) >= 0
+    rows = sample_rows(w.M, w.seed)
+    rlo, rhi = oracle.enclose_f64(A, B, rows=rows)
+    assert np.array_equal(bits(host(lo)[rows]), bits(rlo))
+    assert np.array_equal(bits(host(hi)[rows]), bits(rhi))
+
+
+def test_host_buffers_and_digest(rg):
+    A, B = normal_matrices(33, 44, 55, 9)
+    lo1, hi1 = rg.enclose_gemm_f64(dev(A), dev(B))
+    lo2, hi2 = rg.enclose_gemm_f64(torch.from_numpy(A), torch.from_numpy(B))
+    assert lo2.device.type == "cpu"
+    assert rg.digest(lo1, hi1) == rg.digest(lo2, hi2)

@@ -1,0 +1,142 @@
+"""GPU parity of the exact int64 path (res_gemm_i64) against the CPU oracle.
+
+Bit-exact comparison, element by element: in full on the small and 1024^3
+workloads and on ragged shapes that span several tiles and a tail, on seeded
+sample rows for the long-K workload at full size, plus closed forms.
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from tests.gpu_util import balanced_mod, dev, host, rg, stage_buffers  # noqa: F401
+from workloads import WORKLOADS, int_matrices, sample_rows
+
+pytestmark = pytest.mark.gpu
+
+
+def test_exact24_64_full(rg):
+    w = WORKLOADS["exact24_64"]
+    A, B = w.generate()
+    C = host(rg.res_gemm_i64(dev(A), dev(B)))
+    ref = oracle.matmul_i64(A, B, lc=1)[:, :, 0]
+    assert np.array_equal(C, ref)
+    plan = rg.get_plan()
+    assert plan["status"] == 0 and plan["nprimes"] == 7  # |C| < 2^(24+24+6): 7 primes
+
+
+def test_exact24_64_stages(rg):
+    """Each stage against its definition: x mod q for the split, (A B) mod q for the GEMM stage."""
+    w = WORKLOADS["exact24_64"]
+    A, B = w.generate()
+    rg.res_gemm_i64(dev(A), dev(B))
+    ra, rb, rc, L = stage_buffers(rg, rg.RG_OP_I64, w.M, w.N, w.K)
+    P = rg.get_plan()["nprimes"]
+    ps = rg.primes()
+    C = oracle.matmul_i64(A, B, lc=1)[:, :, 0]
+    ra, rb, rc = host(ra.float()).astype(np.int64), host(rb.float()).astype(np.int64), host(rc).astype(np.int64)
+    for p in range(P):
+        q = ps[p]
+        assert np.array_equal(ra[p, :, :w.K], balanced_mod(A, q)), p
+        assert np.array_equal(rb[p, :, :w.N], balanced_mod(B, q)), p
+        assert np.array_equal(rc[p, :, :w.N], np.mod(C, q)), p
+        assert not ra[p, :, w.K:].any() and not rb[p, :, w.N:].any()
+
+
+def test_exact24_1024_full(rg):
+    w = WORKLOADS["exact24_1024"]
+    A, B = w.generate()
+    C = host(rg.res_gemm_i64(dev(A), dev(B)))
+    ref = oracle.matmul_i64(A, B, lc=1)[:, :, 0]
+    assert np.array_equal(C, ref)
+    assert rg.get_plan()["nprimes"] == 8
+
+
+RAGGED = [
+    (1, 1, 1, -(2**23), 2**23),
+    (3, 5, 7, -(2**29), 2**29),
+    (65, 77, 129, -(2**23), 2**23),
+    (127, 129, 1025, -(2**23), 2**23),  # two K chunks
+    (130, 300, 2049, -(2**20), 2**20),  # three chunks, ragged M and N tiles
+    (257, 513, 4100, -(2**12), 2**12),  # five chunks
+    (200, 64, 30, -(2**29), 2**29),  # K * 2^58 < 2^63
+    (40, 700, 33, -(2**28), 2**28),
+]
+
+
+@pytest.mark.parametrize("M,N,K,lo,hi", RAGGED)
+def test_ragged_shapes(rg, M, N, K, lo, hi):
+    A, B = int_matrices(M, N, K, lo, hi, seed=M * 7 + N * 3 + K)
+    C = host(rg.res_gemm_i64(dev(A), dev(B)))
+    assert np.array_equal(C, oracle.matmul_i64(A, B, lc=1)[:, :, 0])
+
+
+def test_extreme_values(rg):
+    # K * max|A| * max|B| <= 2^63 - 1 is the only limit: int64 extremes with K = 1.
+    A = np.array([[2**62], [-(2**62)], [-(2**63) + 1], [2**63 - 1]], dtype=np.int64)
+    B = np.array([[1, -1, 0]], dtype=np.int64)
+    C = host(rg.res_gemm_i64(dev(A), dev(B)))
+    assert np.array_equal(C, oracle.matmul_i64(A, B, lc=1)[:, :, 0])
+    # INT64_MIN against zero
+    A = np.full((3, 2), -(2**63), dtype=np.int64)
+    B = np.zeros((2, 4), dtype=np.int64)
+    assert not host(rg.res_gemm_i64(dev(A), dev(B))).any()
+
+
+def test_range_error(rg):
+    A = np.full((2, 4), 2**40, dtype=np.int64)
+    B = np.full((4, 2), 2**40, dtype=np.int64)
+    with pytest.raises(rg.ResGemmError) as e:
+        rg.res_gemm_i64(dev(A), dev(B))
+    assert e.value.code == rg.RG_ERR_RANGE
+    # the context stays usable
+    A, B = int_matrices(8, 8, 8, -100, 100, 1)
+    assert np.array_equal(host(rg.res_gemm_i64(dev(A), dev(B))), A @ B)
+
+
+@pytest.mark.parametrize("nprimes", [8, 9, 20, 53])
+def test_fixed_prime_count(rg, nprimes):
+    # CRT uniqueness: any prime count covering the bound gives the same integers.
+    A, B = int_matrices(100, 90, 300, -(2**23), 2**23, 17)
+    C = host(rg.res_gemm_i64(dev(A), dev(B), nprimes=nprimes))
+    assert np.array_equal(C, A @ B)
+
+
+def test_longk_int8_sampled_rows(rg):
+    w = WORKLOADS["longk_int8"]
+    A, B = w.generate()
+    C = host(rg.res_gemm_i64(dev(A), dev(B)))
+    rows = sample_rows(w.M, w.seed)
+    ref = oracle.matmul_i64(A, B, lc=1, rows=rows)[:, :, 0]
+    assert np.array_equal(C[rows], ref)
+    assert rg.get_plan()["nprimes"] == 5
+
+
+def test_longk_closed_form(rg):
+    # all entries -128 at K = 2^17: every entry is exactly 2^31.
+    K = 2**17
+    A = torch.full((130, K), -128, dtype=torch.int64, device="cuda")
+    B = torch.full((K, 70), -128, dtype=torch.int64, device="cuda")
+    C = rg.res_gemm_i64(A, B)
+    assert bool((C == 2**31).all())
+
+
+def test_host_buffers(rg):
+    A, B = int_matrices(70, 50, 90, -(2**23), 2**23, 5)
+    C = rg.res_gemm_i64(torch.from_numpy(A).pin_memory(), torch.from_numpy(B).pin_memory())
+    assert C.device.type == "cpu"
+    assert np.array_equal(C.numpy(), A @ B)
+
+
+def test_async_call_then_status(rg):
+    A, B = int_matrices(64, 64, 64, -(2**23), 2**23, 6)
+    C = rg.res_gemm_i64(dev(A), dev(B), sync=False)
+    assert rg.status() == rg.RG_OK
+    assert np.array_equal(host(C), A @ B)
+
+
+def test_repeatable(rg):
+    A, B = int_matrices(300, 200, 1500, -(2**23), 2**23, 8)
+    C1 = host(rg.res_gemm_i64(dev(A), dev(B)))
+    C2 = host(rg.res_gemm_i64(dev(A), dev(B)))
+    assert np.array_equal(C1, C2)

@@ -1,0 +1,79 @@
+"""GPU parity of the multi-limb path (res_gemm_limbs) against the CPU oracle."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from tests.gpu_util import dev, host, rg  # noqa: F401
+from workloads import WORKLOADS, limb_matrices, sample_rows
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.mark.parametrize("M,N,K,la,lb,lc", [
+    (33, 65, 70, 2, 2, 6),
+    (1, 1, 1, 2, 2, 5),
+    (130, 260, 1030, 2, 2, 6),  # two K chunks, ragged tiles
+    (20, 30, 40, 1, 3, 5),
+    (17, 9, 11, 3, 1, 5),
+    (5, 300, 9, 1, 1, 3),
+])
+def test_random_full_width(rg, M, N, K, la, lb, lc):
+    rng = np.random.default_rng(M + 10 * N + 100 * K + la)
+    full = dict(low=-(2**63), high=2**63 - 1, endpoint=True, dtype=np.int64)
+    A = rng.integers(size=(M, K, la), **full)
+    B = rng.integers(size=(K, N, lb), **full)
+    C = host(rg.res_gemm_limbs(dev(A), dev(B), lc))
+    ref = oracle.matmul_limbs(A, B, lc)
+    assert np.array_equal(C, ref)
+
+
+def test_extremes_and_signs(rg):
+    vals = [-(2**127), 2**127 - 1, -1, 0, 1, 2**64, -(2**64), 2**100 + 3, -(2**99)]
+    rng = np.random.default_rng(3)
+    M, N, K = 7, 6, 9
+    A = np.array([[oracle.int_to_limbs(int(rng.choice(vals)), 2) for _ in range(K)] for _ in range(M)], dtype=np.int64)
+    B = np.array([[oracle.int_to_limbs(int(rng.choice(vals)), 2) for _ in range(N)] for _ in range(K)], dtype=np.int64)
+    C = host(rg.res_gemm_limbs(dev(A), dev(B), 6))
+    want = oracle.matmul_py(oracle.to_pyint_matrix(A), oracle.to_pyint_matrix(B))
+    got = [[oracle.limbs_to_int(C[i, j]) for j in range(N)] for i in range(M)]
+    assert got == want
+
+
+def test_small_values_in_wide_limbs(rg):
+    # 256-bit containers holding small values: the planner reads the real widths.
+    A0 = np.random.default_rng(1).integers(-1000, 1000, size=(40, 50))
+    B0 = np.random.default_rng(2).integers(-1000, 1000, size=(50, 30))
+    A = np.stack([A0] + [np.where(A0 < 0, -1, 0)] * 3, axis=-1).astype(np.int64)
+    B = np.stack([B0] + [np.where(B0 < 0, -1, 0)] * 3, axis=-1).astype(np.int64)
+    C = host(rg.res_gemm_limbs(dev(A), dev(B), 1))
+    assert np.array_equal(C[:, :, 0], A0 @ B0)
+    assert rg.get_plan()["nprimes"] <= 5
+
+
+def test_wide128_2048_sampled_rows(rg):
+    w = WORKLOADS["wide128_2048"]
+    A, B = w.generate()
+    C = host(rg.res_gemm_limbs(dev(A), dev(B), w.out_limbs))
+    rows = sample_rows(w.M, w.seed)
+    ref = oracle.matmul_limbs(A, B, w.out_limbs, rows=rows)
+    assert np.array_equal(C[rows], ref)
+    plan = rg.get_plan()
+    assert plan["bits_a"] == 128 and plan["bits_b"] == 128 and plan["bound_bits"] == 128 + 128 + 11
+
+
+def test_wide128_all_primes(rg):
+    A, B = limb_matrices(64, 64, 256, 2, 9)
+    C = host(rg.res_gemm_limbs(dev(A), dev(B), 6, nprimes=53))
+    assert np.array_equal(C, oracle.matmul_limbs(A, B, 6))
+
+
+def test_range_errors(rg):
+    A, B = limb_matrices(4, 4, 4, 4, 5)
+    with pytest.raises(rg.ResGemmError) as e:  # 256 + 256 + 2 > 332
+        rg.res_gemm_limbs(dev(A), dev(B), 6)
+    assert e.value.code == rg.RG_ERR_RANGE
+    A, B = limb_matrices(4, 4, 4, 2, 6)
+    with pytest.raises(rg.ResGemmError) as e:  # needs 259 bits, 2 limbs hold 127
+        rg.res_gemm_limbs(dev(A), dev(B), 2)
+    assert e.value.code == rg.RG_ERR_RANGE
