@@ -59,7 +59,8 @@ def test_wide128_2048_sampled_rows(rg):
     ref = oracle.matmul_limbs(A, B, w.out_limbs, rows=rows)
     assert np.array_equal(C[rows], ref)
     plan = rg.get_plan()
-    assert plan["bits_a"] == 128 and plan["bits_b"] == 128 and plan["bound_bits"] == 128 + 128 + 11
+    # max |x| of values uniform in [-2^127, 2^127) has bit length 127
+    assert plan["bits_a"] == 127 and plan["bits_b"] == 127 and plan["bound_bits"] == 127 + 127 + 11
 
 
 def test_wide128_all_primes(rg):
