@@ -44,7 +44,7 @@ NUM_PRIMES = 53
 EXPORTED = (
     "res_gemm_i64", "res_gemm_limbs", "enclose_gemm_f64", "res_gemm_stage", "rg_workspace_bytes",
     "rg_workspace_layout", "rg_get_plan", "rg_status", "rg_prime", "rg_strerror", "rg_set_wait_limit_ns",
-    "rg_inject_fault",
+    "rg_inject_fault", "res_gemm_i64_noalloc", "rg_noalloc_scratch_bytes",
 )
 
 
@@ -311,3 +311,25 @@ def digest(lo: torch.Tensor, hi: torch.Tensor) -> str:
     h.update(lo.detach().contiguous().cpu().numpy().tobytes())
     h.update(hi.detach().contiguous().cpu().numpy().tobytes())
     return h.hexdigest()
+
+
+def res_gemm_i64_noalloc(A: torch.Tensor, B: torch.Tensor, nprimes: int = 0, sync: bool = True,
+                         out=None) -> torch.Tensor:
+    """res_gemm_i64 on the library's fixed static scratch: for callers that cannot
+    allocate device memory (the output is allocated here only when `out` is None)."""
+    if A.dtype != torch.int64 or B.dtype != torch.int64 or A.dim() != 2 or B.dim() != 2 or A.shape[1] != B.shape[0]:
+        raise ValueError("A [M,K] and B [K,N] int64 expected")
+    if A.device.type != "cuda" or B.device != A.device:
+        raise ValueError("device tensors on one GPU expected")
+    M, K = A.shape
+    N = B.shape[1]
+    C = out if out is not None else torch.empty((M, N), dtype=torch.int64, device=A.device)
+    f = library().res_gemm_i64_noalloc
+    f.argtypes = [ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int64, ctypes.c_int64, ctypes.c_int64,
+                  ctypes.c_int, ctypes.c_uint, ctypes.c_void_p]
+    f.restype = ctypes.c_int
+    with torch.cuda.device(A.device):
+        rc = f(A.contiguous().data_ptr(), B.contiguous().data_ptr(), C.data_ptr(), M, N, K, nprimes,
+               RG_FLAG_SYNC if sync else 0, torch.cuda.current_stream(A.device).cuda_stream)
+    _check(rc, "res_gemm_i64_noalloc")
+    return C

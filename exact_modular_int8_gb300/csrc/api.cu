@@ -7,6 +7,7 @@
 // RG_FLAG_SYNC / RG_FLAG_HOST calls, rg_status() and rg_get_plan() wait for the
 // device.
 #include <atomic>
+#include <mutex>
 #include <cstdint>
 #include <cstring>
 
@@ -275,3 +276,53 @@ uint64_t rg_set_wait_limit_ns(uint64_t ns) { return g_wait_ns.exchange(ns ? ns :
 void rg_inject_fault(int kind) { g_fault.store(kind); }
 
 }  // extern "C"
+
+// ---------------------------------------------------------------------------
+// Allocation-free variant of res_gemm_i64.
+//
+// Some callers cannot allocate device memory at call time: code running
+// inside a host framework that owns every byte of device memory through its
+// own arena, code on a latency-critical path where cudaMalloc's implicit
+// device synchronisation is not allowed, and code whose only device memory
+// is the buffers it was handed.  For them, res_gemm_i64_noalloc keeps its
+// scratch (plan block and residue planes) in one fixed static device array.
+// The array is part of this library's module: every GPU that loads the
+// library holds it until the process exits.
+// ---------------------------------------------------------------------------
+namespace {
+
+constexpr size_t kNoAllocScratchBytes = size_t(64) << 20;  // 64 MiB
+__device__ __align__(256) unsigned char g_noalloc_scratch[kNoAllocScratchBytes];
+
+std::mutex g_noalloc_mu;
+void* g_noalloc_ptr[64];  // device address of the array, per device
+
+// The array's name is only a host-side stand-in; its device address is looked
+// up once per device, with that device current.
+int noalloc_scratch(void** out) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return RG_ERR_CUDA;
+  std::lock_guard<std::mutex> lock(g_noalloc_mu);
+  if (!g_noalloc_ptr[dev]) {
+    void* p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_noalloc_scratch) != cudaSuccess || !p) return RG_ERR_CUDA;
+    g_noalloc_ptr[dev] = p;
+  }
+  *out = g_noalloc_ptr[dev];
+  return RG_OK;
+}
+
+}  // namespace
+
+extern "C" size_t rg_noalloc_scratch_bytes(void) { return kNoAllocScratchBytes; }
+
+extern "C" int res_gemm_i64_noalloc(const int64_t* A, const int64_t* B, int64_t* C, int64_t M, int64_t N, int64_t K,
+                                    int nprimes, unsigned flags, void* stream) {
+  Layout L;
+  if (!make_layout(RG_OP_I64, M, N, K, 1, 1, 1, nprimes, flags, &L)) return RG_ERR_ARG;
+  if (L.total > kNoAllocScratchBytes) return RG_ERR_WORKSPACE;  // before any device work
+  void* ws = nullptr;
+  int rc = noalloc_scratch(&ws);
+  if (rc != RG_OK) return rc;
+  return run(RG_OP_I64, A, 1, B, 1, C, nullptr, 1, M, N, K, nprimes, flags, ws, kNoAllocScratchBytes, stream);
+}

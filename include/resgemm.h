@@ -143,6 +143,35 @@ int res_gemm_stage(const uint16_t* RA, int64_t lda, const uint16_t* RB, int64_t 
                    void* stream);
 
 /*
+ * res_gemm_i64 without a caller workspace and without any allocation.  The
+ * pages have no counterpart; this entry point exists for callers that cannot
+ * allocate device memory when they call: code inside a host framework that
+ * owns all device memory through its own arena, latency-critical code where
+ * cudaMalloc's implicit synchronisation is not allowed, and code whose only
+ * device memory is the buffers it was handed.
+ *
+ * Arguments and results are those of res_gemm_i64 (the caller still passes
+ * A, B and C).  The scratch is one fixed static device array of
+ * rg_noalloc_scratch_bytes() bytes (64 MiB) inside the library, which every
+ * GPU that loads the library holds until the process exits.  A problem whose
+ * scratch (rg_workspace_bytes(RG_OP_I64, ...)) exceeds it returns
+ * RG_ERR_WORKSPACE before any device work.  No cudaMalloc, cudaFree or other
+ * allocating routine is called.
+ *
+ * The first call on each device looks up the array's device address (and
+ * copies the constant tables), so make that first call before any stream
+ * capture on that device.  Every call shares the one array and its leftover
+ * contents; each call clears what must start at zero.  Calls that overlap on
+ * the GPU (on different streams, or from several host threads) race on the
+ * array: serialise them.
+ */
+int res_gemm_i64_noalloc(const int64_t* A, const int64_t* B, int64_t* C, int64_t M, int64_t N, int64_t K, int nprimes,
+                         unsigned flags, void* stream);
+
+/* Size in bytes of the fixed scratch of res_gemm_i64_noalloc (64 MiB). */
+size_t rg_noalloc_scratch_bytes(void);
+
+/*
  * Workspace size in bytes for one call of `op` (RG_OP_*) with these shapes.
  * la, lb, lc are the limb counts (1 for RG_OP_I64 / RG_OP_ENCLOSE); nprimes
  * is the value the call will pass (0 = plan on the device).  flags must
