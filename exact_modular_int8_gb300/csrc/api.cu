@@ -154,15 +154,9 @@ int run(int op, const void* A, int la, const void* B, int lb, void* C, void* C2,
     RG_TRY(cudaMemcpyAsync(const_cast<void*>(dB), B, (size_t)K * N * eb, cudaMemcpyHostToDevice, s));
   }
   RG_TRY(cudaMemsetAsync(plan, 0, sizeof(DevPlan), s));
-  if (op == RG_OP_I64 && nprimes == 0)
-    RG_TRY(launch_plan_i64(static_cast<const int64_t*>(dA), M * K, static_cast<const int64_t*>(dB), K * N, plan, s));
-  else if (op == RG_OP_LIMBS && nprimes == 0)
-    RG_TRY(launch_plan_limbs(static_cast<const int64_t*>(dA), M * K, la, static_cast<const int64_t*>(dB), K * N, lb,
-                             plan, s));
-  else if (op == RG_OP_ENCLOSE)
-    RG_TRY(launch_plan_f64(static_cast<const double*>(dA), M * K, static_cast<const double*>(dB), K * N, plan, s));
-  RG_TRY(launch_split(op, dA, dB, op == RG_OP_LIMBS ? la : 1, op == RG_OP_LIMBS ? lb : 1, op == RG_OP_LIMBS ? lc : 1,
-                      M, N, K, L.lda, L.ldb, w + L.ra, w + L.rb, op == RG_OP_ENCLOSE ? 0 : nprimes, plan, s));
+  const int la1 = op == RG_OP_LIMBS ? la : 1, lb1 = op == RG_OP_LIMBS ? lb : 1, lc1 = op == RG_OP_LIMBS ? lc : 1;
+  RG_TRY(launch_plan(op, dA, M * K, la1, dB, K * N, lb1, lc1, K, op == RG_OP_ENCLOSE ? 0 : nprimes, plan, s));
+  RG_TRY(launch_split(op, dA, dB, la1, lb1, M, N, K, L.lda, L.ldb, w + L.ra, w + L.rb, plan, s));
   int fault = g_fault.exchange(0);
   RG_TRY(launch_gemm(w + L.ra, L.lda, w + L.rb, L.ldb, w + L.rc, L.ldc, L.pmax, 0, M, N, K, plan, s, fault,
                      g_wait_ns.load()));

@@ -39,11 +39,11 @@ __device__ __forceinline__ unsigned long long warp_max_u64(unsigned long long v)
 
 __device__ __forceinline__ int warp_max_i32(int v) { return __reduce_max_sync(0xffffffffu, v); }
 
-// Block-wide max of a 64-bit value; result valid in thread 0.
+// Block-wide max; result valid in thread 0.
 __device__ unsigned long long block_max_u64(unsigned long long v) {
   __shared__ unsigned long long s[32];
   v = warp_max_u64(v);
-  int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   if (lane == 0) s[warp] = v;
   __syncthreads();
   if (warp == 0) {
@@ -57,7 +57,7 @@ __device__ unsigned long long block_max_u64(unsigned long long v) {
 __device__ int block_max_i32(int v) {
   __shared__ int s[32];
   v = warp_max_i32(v);
-  int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   if (lane == 0) s[warp] = v;
   __syncthreads();
   if (warp == 0) {
@@ -68,34 +68,154 @@ __device__ int block_max_i32(int v) {
   return v;
 }
 
+__device__ __forceinline__ unsigned long long abs_u64(unsigned long long v) {
+  return (long long)v < 0 ? 0ull - v : v;
+}
+
 // ---------------------------------------------------------------------------
-// Planner reductions ("enclosure-gemm", Method: three reductions over the
-// exponent field, stacked and read together; for integer operands the bound
-// K * max|A| * max|B| fixes the prime count)
+// The plan ("enclosure-gemm", Method: three reductions over the exponent
+// field, stacked and read together; Requirements: K <= 2^17 and
+// bits_a + bits_b + ceil(log2 K) <= 332).  The planner kernels reduce into the
+// plan block with atomics; the last block to finish derives the prime count,
+// the chunk counts and the fp64 scales once, for all later kernels.
 // ---------------------------------------------------------------------------
 
-// max |x| of A and of B (int64), one launch: blocks [0, nbA) read A.
-__global__ void plan_i64_kernel(const int64_t* __restrict__ A, long long nA, const int64_t* __restrict__ B,
-                                long long nB, int nbA, DevPlan* plan) {
-  bool isA = (int)blockIdx.x < nbA;
-  const int64_t* X = isA ? A : B;
-  long long n = isA ? nA : nB;
-  long long b0 = isA ? blockIdx.x : blockIdx.x - nbA;
-  long long nb = isA ? nbA : gridDim.x - nbA;
-  unsigned long long m = 0;
-  for (long long i = b0 * blockDim.x + threadIdx.x; i < n; i += nb * blockDim.x) {
-    long long x = X[i];
-    unsigned long long a = x < 0 ? 0ull - (unsigned long long)x : (unsigned long long)x;
-    m = a > m ? a : m;
+struct PlanArgs {
+  int op;
+  long long K;
+  int nprimes_fixed, la, lb, lc;
+};
+
+struct LocalPlan {
+  int status, P, bits_a, bits_b, T, f_a, f_b, lossless, nchunk_a, nchunk_b;
+};
+
+__device__ int primes_for_bound(int T) {  // fewest primes with P > 2^(T+1); 0 if none
+  for (int n = 1; n <= kNumPrimes; ++n)
+    if (c_tab.log2P[n] >= T + 1) return n;
+  return 0;
+}
+
+// Reads the reductions through L2 (they were written with device atomics).
+__device__ LocalPlan finalize_plan(DevPlan* plan, const PlanArgs& a) {
+  LocalPlan p = {};
+  const int ck = ceil_log2_i64(a.K);
+  auto full_chunks = [](int L) { return (64 * L + kChunkBits - 1) / kChunkBits; };
+  if (a.op == RG_OP_I64) {
+    const unsigned long long ma = __ldcg(&plan->maxmag_a), mb = __ldcg(&plan->maxmag_b);
+    p.bits_a = bitlen64(ma);
+    p.bits_b = bitlen64(mb);
+    p.T = p.bits_a + p.bits_b + ck;
+    if (a.nprimes_fixed) {
+      p.nchunk_a = p.nchunk_b = full_chunks(1);
+    } else {
+      // entries with |x| <= 2^23 are exact fp32 values: no chunks (nchunk 0)
+      p.nchunk_a = ma <= (1ull << 23) ? 0 : (p.bits_a + 1 + kChunkBits - 1) / kChunkBits;
+      p.nchunk_b = mb <= (1ull << 23) ? 0 : (p.bits_b + 1 + kChunkBits - 1) / kChunkBits;
+      // exact range check: K * max|A| * max|B| <= 2^63 - 1
+      const unsigned __int128 prod = (unsigned __int128)ma * mb;
+      const unsigned __int128 lim = (unsigned __int128)0x7FFFFFFFFFFFFFFFull / (unsigned long long)a.K;
+      if (prod > lim) p.status = RG_ERR_RANGE;
+    }
+  } else if (a.op == RG_OP_LIMBS) {
+    p.bits_a = __ldcg(&plan->maxbits_a);
+    p.bits_b = __ldcg(&plan->maxbits_b);
+    p.T = p.bits_a + p.bits_b + ck;
+    if (a.nprimes_fixed) {
+      p.nchunk_a = full_chunks(a.la);
+      p.nchunk_b = full_chunks(a.lb);
+    } else {
+      p.nchunk_a = p.bits_a <= 23 ? 0 : min((p.bits_a + 1 + kChunkBits - 1) / kChunkBits, full_chunks(a.la));
+      p.nchunk_b = p.bits_b <= 23 ? 0 : min((p.bits_b + 1 + kChunkBits - 1) / kChunkBits, full_chunks(a.lb));
+      if (p.T > RG_MAX_BOUND_BITS || p.T > 64 * a.lc - 1) p.status = RG_ERR_RANGE;
+    }
+  } else {  // RG_OP_ENCLOSE
+    if (__ldcg(&plan->nonfinite)) {
+      p.status = RG_ERR_NONFINITE;
+      return p;
+    }
+    const int ea = __ldcg(&plan->maxe_a), eb = __ldcg(&plan->maxe_b);
+    const int mina = 4096 - __ldcg(&plan->inv_mine_a), minb = 4096 - __ldcg(&plan->inv_mine_b);
+    p.bits_a = ea ? ea - mina + 53 : 0;  // |A * 2^f_a| < 2^bits_a
+    p.bits_b = eb ? eb - minb + 53 : 0;
+    p.f_a = ea ? 1075 - mina : 0;        // finest binary point of A: 2^-f_a
+    p.f_b = eb ? 1075 - minb : 0;
+    p.T = p.bits_a + p.bits_b + ck;
+    p.lossless = p.bits_a <= 255 && p.bits_b <= 255 && p.T <= RG_MAX_BOUND_BITS;
+    if (!p.lossless) p.status = RG_ERR_LOSSY;
   }
+  if (p.status) return p;
+  p.P = a.nprimes_fixed ? a.nprimes_fixed : primes_for_bound(p.T);
+  if (p.P == 0) p.status = RG_ERR_RANGE;
+  return p;
+}
+
+// Called at the end of every planner block: the last block writes the plan.
+__device__ void planner_finish(DevPlan* plan, const PlanArgs& a) {
+  __shared__ int s_last;
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    __threadfence();
+    const unsigned done = atomicAdd(&plan->blocks_done, 1u);
+    s_last = done == gridDim.x - 1;
+  }
+  __syncthreads();
+  if (s_last && threadIdx.x == 0) {
+    __threadfence();
+    const LocalPlan lp = finalize_plan(plan, a);
+    plan->P = lp.P;
+    plan->bits_a = lp.bits_a;
+    plan->bits_b = lp.bits_b;
+    plan->bound_bits = lp.T;
+    plan->f_a = lp.f_a;
+    plan->f_b = lp.f_b;
+    plan->lossless = lp.lossless;
+    plan->nchunk_a = lp.nchunk_a;
+    plan->nchunk_b = lp.nchunk_b;
+    if (lp.status) set_status(&plan->status, lp.status);
+  }
+}
+
+// Blocks [0, nbA) read A, the others read B.
+struct PlannerSide {
+  long long b0, nb, stride;
+  bool isA;
+};
+__device__ __forceinline__ PlannerSide planner_side(int nbA) {
+  PlannerSide s;
+  s.isA = (int)blockIdx.x < nbA;
+  s.b0 = s.isA ? blockIdx.x : blockIdx.x - nbA;
+  s.nb = s.isA ? nbA : gridDim.x - nbA;
+  s.stride = s.nb * blockDim.x;
+  return s;
+}
+
+// max |x| of int64 A and B; 16-byte loads when aligned, scalar tail.
+__global__ void __launch_bounds__(256) plan_i64_kernel(const int64_t* __restrict__ A, long long nA,
+                                                       const int64_t* __restrict__ B, long long nB, int nbA,
+                                                       DevPlan* plan, PlanArgs pa) {
+  const PlannerSide sd = planner_side(nbA);
+  const unsigned long long* X = reinterpret_cast<const unsigned long long*>(sd.isA ? A : B);
+  const long long n = sd.isA ? nA : nB;
+  const long long nv = (reinterpret_cast<uintptr_t>(X) & 15u) == 0 ? n / 2 : 0;
+  const ulonglong2* X2 = reinterpret_cast<const ulonglong2*>(X);
+  unsigned long long m = 0;
+#pragma unroll 4
+  for (long long i = sd.b0 * blockDim.x + threadIdx.x; i < nv; i += sd.stride) {
+    const ulonglong2 v = __ldg(X2 + i);
+    m = max(m, max(abs_u64(v.x), abs_u64(v.y)));
+  }
+  for (long long i = 2 * nv + sd.b0 * blockDim.x + threadIdx.x; i < n; i += sd.stride)
+    m = max(m, abs_u64(__ldg(X + i)));
   m = block_max_u64(m);
-  if (threadIdx.x == 0 && m) atomicMax(isA ? &plan->maxmag_a : &plan->maxmag_b, m);
+  if (threadIdx.x == 0 && m) atomicMax(sd.isA ? &plan->maxmag_a : &plan->maxmag_b, m);
+  planner_finish(plan, pa);
 }
 
 // Bit length of |x| for multi-limb x (two's complement, signed top limb).
 __device__ __forceinline__ int limb_magnitude_bits(const int64_t* x, int L) {
   unsigned long long w[RG_MAX_LIMBS_IN];
-  bool neg = x[L - 1] < 0;
+  const bool neg = x[L - 1] < 0;
   unsigned long long carry = 1;
 #pragma unroll
   for (int i = 0; i < RG_MAX_LIMBS_IN; ++i) {
@@ -108,124 +228,70 @@ __device__ __forceinline__ int limb_magnitude_bits(const int64_t* x, int L) {
       w[i] = v;
     }
   }
-  for (int i = L - 1; i >= 0; --i)
-    if (w[i]) return 64 * i + bitlen64(w[i]);
-  return 0;
+  int b = 0;
+#pragma unroll
+  for (int i = 0; i < RG_MAX_LIMBS_IN; ++i)
+    if (i < L && w[i]) b = 64 * i + bitlen64(w[i]);
+  return b;
 }
 
-__global__ void plan_limbs_kernel(const int64_t* __restrict__ A, long long nA, int la, const int64_t* __restrict__ B,
-                                  long long nB, int lb, int nbA, DevPlan* plan) {
-  bool isA = (int)blockIdx.x < nbA;
-  const int64_t* X = isA ? A : B;
-  long long n = isA ? nA : nB;
-  int L = isA ? la : lb;
-  long long b0 = isA ? blockIdx.x : blockIdx.x - nbA;
-  long long nb = isA ? nbA : gridDim.x - nbA;
+__global__ void __launch_bounds__(256) plan_limbs_kernel(const int64_t* __restrict__ A, long long nA, int la,
+                                                         const int64_t* __restrict__ B, long long nB, int lb, int nbA,
+                                                         DevPlan* plan, PlanArgs pa) {
+  const PlannerSide sd = planner_side(nbA);
+  const int64_t* X = sd.isA ? A : B;
+  const long long n = sd.isA ? nA : nB;
+  const int L = sd.isA ? la : lb;
   int m = 0;
-  for (long long i = b0 * blockDim.x + threadIdx.x; i < n; i += nb * blockDim.x) {
-    int b = limb_magnitude_bits(X + i * L, L);
+  for (long long i = sd.b0 * blockDim.x + threadIdx.x; i < n; i += sd.stride) {
+    const int b = limb_magnitude_bits(X + i * L, L);
     m = b > m ? b : m;
   }
   m = block_max_i32(m);
-  if (threadIdx.x == 0 && m) atomicMax(isA ? &plan->maxbits_a : &plan->maxbits_b, m);
+  if (threadIdx.x == 0 && m) atomicMax(sd.isA ? &plan->maxbits_a : &plan->maxbits_b, m);
+  planner_finish(plan, pa);
 }
 
-// fp64: max and min of max(biased exponent, 1) over nonzero entries, and a
-// non-finite flag.  Reads only the bit patterns.
-__global__ void plan_f64_kernel(const unsigned long long* __restrict__ A, long long nA,
-                                const unsigned long long* __restrict__ B, long long nB, int nbA, DevPlan* plan) {
-  bool isA = (int)blockIdx.x < nbA;
-  const unsigned long long* X = isA ? A : B;
-  long long n = isA ? nA : nB;
-  long long b0 = isA ? blockIdx.x : blockIdx.x - nbA;
-  long long nb = isA ? nbA : gridDim.x - nbA;
-  int emax = 0, einv = 0, bad = 0;
-  for (long long i = b0 * blockDim.x + threadIdx.x; i < n; i += nb * blockDim.x) {
-    unsigned long long v = X[i];
-    int be = (int)((v >> 52) & 0x7FF);
-    if (be == 0x7FF) {
-      bad = 1;
-      continue;
-    }
-    if ((v << 1) == 0) continue;  // +-0
-    int e = be > 1 ? be : 1;
+// fp64: max and min of max(biased exponent, 1) over nonzero entries and a
+// non-finite flag, from the bit patterns only.
+__device__ __forceinline__ void exponent_stats(unsigned long long v, int& emax, int& einv, int& bad) {
+  const int be = (int)((v >> 52) & 0x7FF);
+  const int e = be > 1 ? be : 1;
+  const bool nonzero = (v << 1) != 0;
+  const bool finite = be != 0x7FF;
+  bad |= finite ? 0 : 1;
+  if (finite && nonzero) {
     emax = e > emax ? e : emax;
     einv = (4096 - e) > einv ? (4096 - e) : einv;
   }
+}
+
+__global__ void __launch_bounds__(256) plan_f64_kernel(const unsigned long long* __restrict__ A, long long nA,
+                                                       const unsigned long long* __restrict__ B, long long nB,
+                                                       int nbA, DevPlan* plan, PlanArgs pa) {
+  const PlannerSide sd = planner_side(nbA);
+  const unsigned long long* X = sd.isA ? A : B;
+  const long long n = sd.isA ? nA : nB;
+  const long long nv = (reinterpret_cast<uintptr_t>(X) & 15u) == 0 ? n / 2 : 0;
+  const ulonglong2* X2 = reinterpret_cast<const ulonglong2*>(X);
+  int emax = 0, einv = 0, bad = 0;
+#pragma unroll 4
+  for (long long i = sd.b0 * blockDim.x + threadIdx.x; i < nv; i += sd.stride) {
+    const ulonglong2 v = __ldg(X2 + i);
+    exponent_stats(v.x, emax, einv, bad);
+    exponent_stats(v.y, emax, einv, bad);
+  }
+  for (long long i = 2 * nv + sd.b0 * blockDim.x + threadIdx.x; i < n; i += sd.stride)
+    exponent_stats(__ldg(X + i), emax, einv, bad);
   emax = block_max_i32(emax);
   einv = block_max_i32(einv);
   bad = block_max_i32(bad);
   if (threadIdx.x == 0) {
-    if (emax) atomicMax(isA ? &plan->maxe_a : &plan->maxe_b, emax);
-    if (einv) atomicMax(isA ? &plan->inv_mine_a : &plan->inv_mine_b, einv);
+    if (emax) atomicMax(sd.isA ? &plan->maxe_a : &plan->maxe_b, emax);
+    if (einv) atomicMax(sd.isA ? &plan->inv_mine_a : &plan->inv_mine_b, einv);
     if (bad) atomicMax(&plan->nonfinite, 1);
   }
-}
-
-// ---------------------------------------------------------------------------
-// Plan finalisation, evaluated identically by every block of the split kernel
-// ---------------------------------------------------------------------------
-
-struct LocalPlan {
-  int status, P, bits_a, bits_b, T, f_a, f_b, lossless, nchunk_a, nchunk_b;
-};
-
-__device__ int primes_for_bound(int T) {  // fewest primes with P > 2^(T+1); 0 if none
-  for (int n = 1; n <= kNumPrimes; ++n)
-    if (c_tab.log2P[n] >= T + 1) return n;
-  return 0;
-}
-
-__device__ LocalPlan finalize_plan(const DevPlan* plan, int op, long long K, int nprimes_fixed, int la, int lb,
-                                   int lc) {
-  LocalPlan p = {};
-  int ck = ceil_log2_i64(K);
-  auto full_chunks = [](int L) { return (64 * L + kChunkBits - 1) / kChunkBits; };
-  if (op == RG_OP_I64) {
-    unsigned long long ma = plan->maxmag_a, mb = plan->maxmag_b;
-    p.bits_a = bitlen64(ma);
-    p.bits_b = bitlen64(mb);
-    p.T = p.bits_a + p.bits_b + ck;
-    if (nprimes_fixed) {
-      p.nchunk_a = p.nchunk_b = full_chunks(1);
-    } else {
-      p.nchunk_a = (p.bits_a + 1 + kChunkBits - 1) / kChunkBits;
-      p.nchunk_b = (p.bits_b + 1 + kChunkBits - 1) / kChunkBits;
-      unsigned __int128 prod = (unsigned __int128)ma * mb;
-      unsigned __int128 lim = (unsigned __int128)0x7FFFFFFFFFFFFFFFull / (unsigned long long)K;
-      if (prod > lim) p.status = RG_ERR_RANGE;
-    }
-  } else if (op == RG_OP_LIMBS) {
-    p.bits_a = plan->maxbits_a;
-    p.bits_b = plan->maxbits_b;
-    p.T = p.bits_a + p.bits_b + ck;
-    if (nprimes_fixed) {
-      p.nchunk_a = full_chunks(la);
-      p.nchunk_b = full_chunks(lb);
-    } else {
-      p.nchunk_a = min((p.bits_a + 1 + kChunkBits - 1) / kChunkBits, full_chunks(la));
-      p.nchunk_b = min((p.bits_b + 1 + kChunkBits - 1) / kChunkBits, full_chunks(lb));
-      if (p.T > RG_MAX_BOUND_BITS || p.T > 64 * lc - 1) p.status = RG_ERR_RANGE;
-    }
-  } else {  // RG_OP_ENCLOSE
-    if (plan->nonfinite) {
-      p.status = RG_ERR_NONFINITE;
-      return p;
-    }
-    int ea = plan->maxe_a, eb = plan->maxe_b;
-    int mina = 4096 - plan->inv_mine_a, minb = 4096 - plan->inv_mine_b;
-    p.bits_a = ea ? ea - mina + 53 : 0;  // |A * 2^f_a| < 2^bits_a
-    p.bits_b = eb ? eb - minb + 53 : 0;
-    p.f_a = ea ? 1075 - mina : 0;        // finest binary point of A: 2^-f_a
-    p.f_b = eb ? 1075 - minb : 0;
-    p.T = p.bits_a + p.bits_b + ck;
-    p.lossless = p.bits_a <= 255 && p.bits_b <= 255 && p.T <= RG_MAX_BOUND_BITS;
-    if (!p.lossless) p.status = RG_ERR_LOSSY;
-  }
-  if (p.status) return p;
-  p.P = nprimes_fixed ? nprimes_fixed : primes_for_bound(p.T);
-  if (p.P == 0) p.status = RG_ERR_RANGE;
-  return p;
+  planner_finish(plan, pa);
 }
 
 // ---------------------------------------------------------------------------
@@ -238,7 +304,7 @@ __device__ LocalPlan finalize_plan(const DevPlan* plan, int op, long long K, int
 // at most 22 chunks the sum stays below 2^24 and is formed exactly in fp32;
 // one reciprocal-based reduction then yields the balanced residue, written as
 // fp16 (exact for |r| <= 125).  Columns from C up to the padded row length
-// are written as zeros.
+// are written as zeros.  Grid-stride over the items of A, then of B.
 // ---------------------------------------------------------------------------
 
 struct SplitSide {
@@ -249,154 +315,189 @@ struct SplitSide {
   long long items; // R * ldy / VEC
 };
 
-// 12 bits starting at bit `pos` of the sign-extended two's-complement value x[0..L).
-__device__ __forceinline__ unsigned chunk_bits(const int64_t* x, int L, int pos) {
-  int w = pos >> 6, off = pos & 63;
-  unsigned long long sign = (unsigned long long)(x[L - 1] >> 63);
-  unsigned long long lo = w < L ? (unsigned long long)x[w] : sign;
+// 12 bits starting at bit `pos` (a compile-time constant after unrolling) of
+// the sign-extended two's-complement value held in registers x[0..L).
+template <int LMAX>
+__device__ __forceinline__ unsigned chunk_bits(const unsigned long long (&x)[LMAX], int L, int pos) {
+  const int w = pos >> 6, off = pos & 63;
+  // sign word of the top limb x[L-1], selected with masks so that every
+  // register index stays a compile-time constant
+  unsigned long long sign = 0ull;
+#pragma unroll
+  for (int k = 0; k < LMAX; ++k)
+    sign |= (unsigned long long)((long long)x[k] >> 63) & (0ull - (unsigned long long)(k == L - 1));
+  const unsigned long long lo = (w < LMAX && w < L) ? x[w < LMAX ? w : 0] : sign;
   unsigned long long v = lo >> off;
   if (off > 64 - kChunkBits) {
-    unsigned long long hi = (w + 1) < L ? (unsigned long long)x[w + 1] : sign;
+    const unsigned long long hi = (w + 1 < LMAX && w + 1 < L) ? x[w + 1 < LMAX ? w + 1 : 0] : sign;
     v |= hi << (64 - off);
   }
   return (unsigned)(v & 0xFFFu);
 }
 
+// Writes the balanced residues of VEC entries for every prime.  nch == 0:
+// cf[e][0] holds the entry itself (|x| <= 2^23, exact in fp32).  Otherwise
+// s = sum_c cf[e][c] w_{q,c}; with at most 16 chunks |s| < 2^23 as well, so the
+// reduction needs no correction step.
 template <int VEC, int NCH>
 __device__ __forceinline__ void emit_residues(const float (&cf)[VEC][NCH], int nch, int P, __half* y,
                                               long long plane) {
+  static_assert(VEC % 2 == 0, "residues are written as half2 pairs");
   for (int p = 0; p < P; ++p) {
     const float q = c_tab.qf[p], iq = c_tab.invq[p];
-    __half h[VEC];
+    float r[VEC];
+    if (nch == 0) {
 #pragma unroll
-    for (int e = 0; e < VEC; ++e) {
-      float s = 0.0f;
+      for (int e = 0; e < VEC; ++e) r[e] = bal_mod_small(cf[e][0], q, iq);
+    } else {
 #pragma unroll
-      for (int c = 0; c < NCH; ++c)
-        if (c < nch) s = __fmaf_rn(cf[e][c], c_tab.chunk_w[p][c], s);
-      h[e] = __float2half_rn(bal_mod(s, q, iq));
+      for (int e = 0; e < VEC; ++e) {
+        float s = 0.0f;
+#pragma unroll
+        for (int c = 0; c < NCH; ++c)
+          if (c < nch) s = __fmaf_rn(cf[e][c], c_tab.chunk_w[p][c], s);
+        r[e] = NCH <= 16 ? bal_mod_small(s, q, iq) : bal_mod(s, q, iq);
+      }
     }
+    __half2 h[VEC / 2];
+#pragma unroll
+    for (int e = 0; e < VEC / 2; ++e) h[e] = __floats2half2_rn(r[2 * e], r[2 * e + 1]);
     __half* dst = y + (long long)p * plane;
     if constexpr (VEC == 8) {
       *reinterpret_cast<uint4*>(dst) = *reinterpret_cast<const uint4*>(h);
     } else if constexpr (VEC == 4) {
       *reinterpret_cast<uint2*>(dst) = *reinterpret_cast<const uint2*>(h);
     } else {
-#pragma unroll
-      for (int e = 0; e < VEC; ++e) dst[e] = h[e];
+      *reinterpret_cast<__half2*>(dst) = h[0];
     }
   }
 }
 
-// Integer operands (int64 when L == 1, or limbs).  VEC consecutive columns per thread.
-template <int VEC, int NCH>
-__global__ void __launch_bounds__(256) split_int_kernel(SplitSide sa, SplitSide sb, long long nbA, DevPlan* plan,
-                                                        int op, long long K, int nprimes_fixed, int la, int lb,
-                                                        int lc) {
-  LocalPlan lp = finalize_plan(plan, op, K, nprimes_fixed, la, lb, lc);
-  if (blockIdx.x == 0 && threadIdx.x == 0) {
-    plan->P = lp.P;
-    plan->bits_a = lp.bits_a;
-    plan->bits_b = lp.bits_b;
-    plan->bound_bits = lp.T;
-    plan->nchunk_a = lp.nchunk_a;
-    plan->nchunk_b = lp.nchunk_b;
-    if (lp.status) set_status(&plan->status, lp.status);
-  }
-  if (lp.status) return;
-  bool isA = (long long)blockIdx.x < nbA;
-  const SplitSide& s = isA ? sa : sb;
-  int nch = isA ? lp.nchunk_a : lp.nchunk_b;
-  long long item = (isA ? (long long)blockIdx.x : (long long)blockIdx.x - nbA) * blockDim.x + threadIdx.x;
-  if (item >= s.items) return;
-  long long per_row = s.ldy / VEC;
-  long long row = item / per_row;
-  long long col0 = (item - row * per_row) * VEC;
-  const int64_t* X = static_cast<const int64_t*>(s.X);
-  float cf[VEC][NCH];
+// Integer operands: int64 (L = 1) or limbs (L <= LMAX).  VEC consecutive
+// columns per item; their VEC * L words are contiguous and are read with
+// 16-byte loads when they lie fully inside the row and are aligned.
+template <int VEC, int NCH, int LMAX>
+__global__ void __launch_bounds__(256) split_int_kernel(SplitSide sa, SplitSide sb, const DevPlan* plan) {
+  if (plan->status) return;
+  const int P = plan->P;
+  const int nch_a = plan->nchunk_a, nch_b = plan->nchunk_b;
+  const long long total = sa.items + sb.items;
+  for (long long it = (long long)blockIdx.x * blockDim.x + threadIdx.x; it < total;
+       it += (long long)gridDim.x * blockDim.x) {
+    const bool isA = it < sa.items;
+    const SplitSide& s = isA ? sa : sb;
+    const int nch = isA ? nch_a : nch_b;
+    const long long item = isA ? it : it - sa.items;
+    const long long per_row = s.ldy / VEC;
+    const long long row = item / per_row;
+    const long long col0 = (item - row * per_row) * VEC;
+    const int L = s.L;
+    const unsigned long long* X = static_cast<const unsigned long long*>(s.X) + (row * s.C + col0) * L;
+    unsigned long long xw[VEC][LMAX];
+    if (col0 + VEC <= s.C && L == LMAX && ((reinterpret_cast<uintptr_t>(X) & 15u) == 0) &&
+        (VEC * LMAX) % 2 == 0) {
 #pragma unroll
-  for (int e = 0; e < VEC; ++e) {
-    long long col = col0 + e;
-    if (col < s.C) {
-      const int64_t* x = X + (row * s.C + col) * s.L;
-#pragma unroll
-      for (int c = 0; c < NCH; ++c) {
-        if (c < nch) {
-          unsigned a = chunk_bits(x, s.L, c * kChunkBits);
-          int v = (c == nch - 1) ? (int)((a ^ 0x800u) - 0x800u) : (int)a;  // top chunk signed
-          cf[e][c] = (float)v;
-        } else {
-          cf[e][c] = 0.0f;
-        }
+      for (int t = 0; t < VEC * LMAX / 2; ++t) {
+        const ulonglong2 v = __ldg(reinterpret_cast<const ulonglong2*>(X) + t);
+        xw[(2 * t) / LMAX][(2 * t) % LMAX] = v.x;
+        xw[(2 * t + 1) / LMAX][(2 * t + 1) % LMAX] = v.y;
       }
     } else {
 #pragma unroll
-      for (int c = 0; c < NCH; ++c) cf[e][c] = 0.0f;
+      for (int e = 0; e < VEC; ++e)
+#pragma unroll
+        for (int k = 0; k < LMAX; ++k) xw[e][k] = (col0 + e < s.C && k < L) ? __ldg(X + e * L + k) : 0ull;
     }
+    float cf[VEC][NCH];
+    if (nch == 0) {  // |x| <= 2^23: the low word is the value
+#pragma unroll
+      for (int e = 0; e < VEC; ++e) {
+        cf[e][0] = (float)(long long)xw[e][0];
+#pragma unroll
+        for (int c = 1; c < NCH; ++c) cf[e][c] = 0.0f;
+      }
+    } else {
+#pragma unroll
+      for (int e = 0; e < VEC; ++e) {
+#pragma unroll
+        for (int c = 0; c < NCH; ++c) {
+          const unsigned a = chunk_bits<LMAX>(xw[e], L, c * kChunkBits);
+          const int v = (c == nch - 1) ? (int)((a ^ 0x800u) - 0x800u) : (int)a;  // top chunk signed
+          cf[e][c] = c < nch ? (float)v : 0.0f;
+        }
+      }
+    }
+    emit_residues<VEC, NCH>(cf, nch, P, s.Y + row * s.ldy + col0, s.plane);
   }
-  emit_residues<VEC, NCH>(cf, nch, lp.P, s.Y + row * s.ldy + col0, s.plane);
 }
 
 // Binary64 operands: X' = x * 2^f = +-m * 2^sh with sh = max(be,1) - min(be',1)
 // >= 0; the 53-bit significand shifted by sh % 12 is cut into six chunks
 // starting at chunk index sh / 12.  No floating-point instruction reads x.
 template <int VEC>
-__global__ void __launch_bounds__(256) split_f64_kernel(SplitSide sa, SplitSide sb, long long nbA, DevPlan* plan,
-                                                        long long K) {
+__global__ void __launch_bounds__(256) split_f64_kernel(SplitSide sa, SplitSide sb, const DevPlan* plan) {
   __shared__ float w_s[kNumPrimes][kMaxChunks];
-  LocalPlan lp = finalize_plan(plan, RG_OP_ENCLOSE, K, 0, 1, 1, 1);
-  if (blockIdx.x == 0 && threadIdx.x == 0) {
-    plan->P = lp.P;
-    plan->bits_a = lp.bits_a;
-    plan->bits_b = lp.bits_b;
-    plan->bound_bits = lp.T;
-    plan->f_a = lp.f_a;
-    plan->f_b = lp.f_b;
-    plan->lossless = lp.lossless;
-    if (lp.status) set_status(&plan->status, lp.status);
-  }
-  if (lp.status) return;
-  for (int i = threadIdx.x; i < lp.P * kMaxChunks; i += blockDim.x)
+  if (plan->status) return;
+  const int P = plan->P;
+  const int emin_a = 4096 - plan->inv_mine_a, emin_b = 4096 - plan->inv_mine_b;
+  for (int i = threadIdx.x; i < P * kMaxChunks; i += blockDim.x)
     w_s[i / kMaxChunks][i % kMaxChunks] = c_tab.chunk_w[i / kMaxChunks][i % kMaxChunks];
   __syncthreads();
-  bool isA = (long long)blockIdx.x < nbA;
-  const SplitSide& s = isA ? sa : sb;
-  int emin = isA ? 4096 - plan->inv_mine_a : 4096 - plan->inv_mine_b;
-  long long item = (isA ? (long long)blockIdx.x : (long long)blockIdx.x - nbA) * blockDim.x + threadIdx.x;
-  if (item >= s.items) return;
-  long long per_row = s.ldy / VEC;
-  long long row = item / per_row;
-  long long col0 = (item - row * per_row) * VEC;
-  const unsigned long long* X = static_cast<const unsigned long long*>(s.X);
-  constexpr int NC = 6;
-  float cf[VEC][NC];
-  int c0[VEC];
+  const long long total = sa.items + sb.items;
+  for (long long it = (long long)blockIdx.x * blockDim.x + threadIdx.x; it < total;
+       it += (long long)gridDim.x * blockDim.x) {
+    const bool isA = it < sa.items;
+    const SplitSide& s = isA ? sa : sb;
+    const int emin = isA ? emin_a : emin_b;
+    const long long item = isA ? it : it - sa.items;
+    const long long per_row = s.ldy / VEC;
+    const long long row = item / per_row;
+    const long long col0 = (item - row * per_row) * VEC;
+    const unsigned long long* X = static_cast<const unsigned long long*>(s.X) + row * s.C + col0;
+    unsigned long long xv[VEC];
+    if (col0 + VEC <= s.C && ((reinterpret_cast<uintptr_t>(X) & 15u) == 0)) {
 #pragma unroll
-  for (int e = 0; e < VEC; ++e) {
-    long long col = col0 + e;
-    unsigned long long v = col < s.C ? X[row * s.C + col] : 0ull;
-    int be = (int)((v >> 52) & 0x7FF);
-    unsigned long long m = (v & 0xFFFFFFFFFFFFFull) | (be ? (1ull << 52) : 0ull);
-    int sh = (be > 1 ? be : 1) - emin;
-    if (m == 0) sh = 0;
-    c0[e] = sh / kChunkBits;
-    unsigned long long t = m << (sh % kChunkBits);
-    float sg = (v >> 63) ? -1.0f : 1.0f;
+      for (int t = 0; t < VEC / 2; ++t) {
+        const ulonglong2 v = __ldg(reinterpret_cast<const ulonglong2*>(X) + t);
+        xv[2 * t] = v.x;
+        xv[2 * t + 1] = v.y;
+      }
+    } else {
 #pragma unroll
-    for (int c = 0; c < NC; ++c) cf[e][c] = sg * (float)(unsigned)((t >> (kChunkBits * c)) & 0xFFFu);
-  }
-  __half* y = s.Y + row * s.ldy + col0;
-  for (int p = 0; p < lp.P; ++p) {
-    const float q = c_tab.qf[p], iq = c_tab.invq[p];
-    __half h[VEC];
+      for (int e = 0; e < VEC; ++e) xv[e] = col0 + e < s.C ? __ldg(X + e) : 0ull;
+    }
+    constexpr int NC = 6;
+    float cf[VEC][NC];
+    int c0[VEC];
 #pragma unroll
     for (int e = 0; e < VEC; ++e) {
-      float acc = 0.0f;
+      const unsigned long long v = xv[e];
+      const int be = (int)((v >> 52) & 0x7FF);
+      const unsigned long long m = (v & 0xFFFFFFFFFFFFFull) | (be ? (1ull << 52) : 0ull);
+      int sh = (be > 1 ? be : 1) - emin;
+      if (m == 0) sh = 0;
+      c0[e] = sh / kChunkBits;
+      const unsigned long long t = m << (sh % kChunkBits);
+      const float sg = (v >> 63) ? -1.0f : 1.0f;
 #pragma unroll
-      for (int c = 0; c < NC; ++c) acc = __fmaf_rn(cf[e][c], w_s[p][c0[e] + c], acc);
-      h[e] = __float2half_rn(bal_mod(acc, q, iq));
+      for (int c = 0; c < NC; ++c) cf[e][c] = sg * (float)(unsigned)((t >> (kChunkBits * c)) & 0xFFFu);
     }
-    *reinterpret_cast<uint4*>(y + (long long)p * s.plane) = *reinterpret_cast<const uint4*>(h);
+    __half* y = s.Y + row * s.ldy + col0;
+    for (int p = 0; p < P; ++p) {
+      const float q = c_tab.qf[p], iq = c_tab.invq[p];
+      float r[VEC];
+#pragma unroll
+      for (int e = 0; e < VEC; ++e) {
+        float acc = 0.0f;
+#pragma unroll
+        for (int c = 0; c < NC; ++c) acc = __fmaf_rn(cf[e][c], w_s[p][c0[e] + c], acc);
+        r[e] = bal_mod_small(acc, q, iq);  // |acc| < 6 * 4095 * 125 < 2^23
+      }
+      __half2 h[VEC / 2];
+#pragma unroll
+      for (int e = 0; e < VEC / 2; ++e) h[e] = __floats2half2_rn(r[2 * e], r[2 * e + 1]);
+      *reinterpret_cast<uint4*>(y + (long long)p * s.plane) = *reinterpret_cast<const uint4*>(h);
+    }
   }
 }
 
@@ -406,63 +507,102 @@ __global__ void __launch_bounds__(256) split_f64_kernel(SplitSide sa, SplitSide 
 //   v_i = bal( (r_i - sum_{j<i} v_j Q_j) Q_i^-1  mod q_i ),  |v_i| <= (q_i-1)/2,
 // give x = sum_i v_i Q_i, the unique representative with |x| <= (P-1)/2.
 // Each digit costs one int8x4 dot product per four earlier digits and one
-// reciprocal reduction; x is then evaluated by Horner from the top digit.
+// reciprocal reduction, and is added into x at once: after digit i,
+// |x| < Q_{i+1} / 2 < 2^(8(i+1) - 1), so only the low i/4 + 2 words of x can
+// differ from its sign extension and only those are updated.  Residues are
+// fetched eight primes at a time, so the loads of a batch are in flight
+// together; the loop stops at the plan's prime count.
 // ---------------------------------------------------------------------------
 
-constexpr int kGE = 4;  // output elements per thread (one 32-bit residue load per prime)
+// Output elements per thread: four (one 32-bit residue load per prime) for
+// narrow results, two for wide ones to bound register use.
+template <int W>
+struct GarnerGE {
+  static constexpr int value = W <= 4 ? 4 : 2;
+};
 
-__device__ __forceinline__ void garner_digits(const uint8_t* __restrict__ rc, long long plane, int P,
-                                              uint32_t (&V)[kGE][kGarnerWords]) {
+constexpr int kGarnerBatch = 8;
+
+// x[e] (W 32-bit words, two's complement) = the reconstructed integers of the
+// GE residue vectors starting at rc (plane = distance between primes).
+template <int W, int GE>
+__device__ __forceinline__ void garner_reconstruct(const uint8_t* __restrict__ rc, long long plane, int P,
+                                                   uint32_t (&x)[GE][W]) {
+  uint32_t V[GE][kGarnerWords];
 #pragma unroll
-  for (int e = 0; e < kGE; ++e)
+  for (int e = 0; e < GE; ++e) {
 #pragma unroll
     for (int w = 0; w < kGarnerWords; ++w) V[e][w] = 0u;
 #pragma unroll
-  for (int i = 0; i < kNumPrimes; ++i) {
-    if (i < P) {
-      uint32_t rw = __ldg(reinterpret_cast<const uint32_t*>(rc + (long long)i * plane));
+    for (int k = 0; k < W; ++k) x[e][k] = 0u;
+  }
+#pragma unroll
+  for (int i0 = 0; i0 < kNumPrimes; i0 += kGarnerBatch) {
+    if (i0 >= P) break;
+    uint32_t rw[kGarnerBatch];
+#pragma unroll
+    for (int j = 0; j < kGarnerBatch; ++j) {
+      const int i = i0 + j;
+      if constexpr (GE == 4)
+        rw[j] = (i < P) ? __ldg(reinterpret_cast<const uint32_t*>(rc + (long long)i * plane)) : 0u;
+      else
+        rw[j] = (i < P) ? (uint32_t)__ldg(reinterpret_cast<const unsigned short*>(rc + (long long)i * plane)) : 0u;
+    }
+#pragma unroll
+    for (int j = 0; j < kGarnerBatch; ++j) {
+      const int i = i0 + j;
+      if (i >= kNumPrimes || i >= P) break;
       const float q = c_tab.qf[i], iq = c_tab.invq[i];
       const int gi = c_tab.ginv[i];
 #pragma unroll
-      for (int e = 0; e < kGE; ++e) {
-        int s = gi * (int)((rw >> (8 * e)) & 0xFFu);
+      for (int e = 0; e < GE; ++e) {
+        const int s = gi * (int)((rw[j] >> (8 * e)) & 0xFFu);
         int acc = 0;
 #pragma unroll
         for (int w = 0; w < kGarnerWords; ++w)
           if (4 * w < i) acc = __dp4a((int)V[e][w], c_tab.gd_packed[i][w], acc);
-        s -= acc;
-        int v = (int)bal_mod((float)s, q, iq);
+        const int v = (int)bal_mod_small((float)(s - acc), q, iq);  // |s - acc| < 2^20
         V[e][i / 4] |= ((uint32_t)v & 0xFFu) << (8 * (i % 4));
+        if constexpr (W == 2) {
+          // one 64-bit word: x += v * (Q_i mod 2^64), wrapping; exact because
+          // the final value fits the output word
+          const unsigned long long Qi = ((unsigned long long)c_tab.Qw[i][1] << 32) | c_tab.Qw[i][0];
+          const unsigned long long x64 = (((unsigned long long)x[e][1] << 32) | x[e][0]) +
+                                         (unsigned long long)(long long)v * Qi;
+          x[e][0] = (uint32_t)x64;
+          x[e][1] = (uint32_t)(x64 >> 32);
+        } else {
+          // x += v * Q_i over the words that can be significant after this
+          // digit; a word entering that range first takes the sign of the word
+          // below it.
+          if (i > 0 && (i % 4) == 0 && i / 4 + 1 < W) x[e][i / 4 + 1] = (uint32_t)((int)x[e][i / 4] >> 31);
+          long long carry = 0;
+#pragma unroll
+          for (int k = 0; k < W; ++k) {
+            if (k < i / 4 + 2) {
+              const long long qk = k < kQWords ? (long long)c_tab.Qw[i][k < kQWords ? k : 0] : 0ll;
+              const long long t = (long long)x[e][k] + qk * v + carry;
+              x[e][k] = (uint32_t)t;
+              carry = t >> 32;
+            }
+          }
+        }
       }
     }
   }
-}
-
-__device__ __forceinline__ int digit(const uint32_t (&V)[kGarnerWords], int i) {
-  return (int)(int8_t)((V[i / 4] >> (8 * (i % 4))) & 0xFFu);
-}
-
-// x (W 32-bit words, two's complement, mod 2^(32W)) = sum_i v_i Q_i by Horner.
-template <int W>
-__device__ __forceinline__ void horner_words(const uint32_t (&V)[kGarnerWords], int P, uint32_t (&x)[W]) {
+  if constexpr (W == 2) return;  // the 64-bit form is complete
+  // sign-extend from the last significant word (branch-free, so x stays in
+  // registers: every index is a compile-time constant)
+  const int top = (P - 1) / 4 + 2;
 #pragma unroll
-  for (int k = 0; k < W; ++k) x[k] = 0u;
+  for (int e = 0; e < GE; ++e) {
+    uint32_t sign = 0u;
 #pragma unroll
-  for (int i = kNumPrimes - 1; i >= 0; --i) {
-    if (i < P) {
-      // x = x * q_i + v_i
-      // The digit is added sign-extended to W words; all arithmetic is mod 2^(32W).
-      const uint32_t q = (uint32_t)c_tab.q[i];
-      const int v = digit(V, i);
-      const uint32_t ext = v < 0 ? 0xFFFFFFFFu : 0u;
-      unsigned long long carry = 0ull;
-#pragma unroll
-      for (int k = 0; k < W; ++k) {
-        const unsigned long long t =
-            (unsigned long long)x[k] * q + (k == 0 ? (unsigned long long)(uint32_t)v : (unsigned long long)ext) + carry;
-        x[k] = (uint32_t)t;
-        carry = t >> 32;
-      }
+    for (int k = 0; k < W; ++k) {
+      const uint32_t at_top = 0u - (uint32_t)(k == top - 1);
+      const uint32_t above = 0u - (uint32_t)(k >= top);
+      sign = (sign & ~at_top) | ((uint32_t)((int)x[e][k] >> 31) & at_top);
+      x[e][k] = (x[e][k] & ~above) | (sign & above);
     }
   }
 }
@@ -471,23 +611,33 @@ template <int LC>
 __global__ void __launch_bounds__(128) garner_int_kernel(const uint8_t* __restrict__ RC, long long ldc,
                                                          long long plane, long long M, long long N, DevPlan* plan,
                                                          int64_t* __restrict__ C) {
+  constexpr int W = 2 * LC, GE = GarnerGE<W>::value;
   if (plan->status) return;
-  int P = plan->P;
-  long long per_row = (N + kGE - 1) / kGE;
-  long long item = (long long)blockIdx.x * blockDim.x + threadIdx.x;
+  const int P = plan->P;
+  const long long per_row = (N + GE - 1) / GE;
+  const long long item = (long long)blockIdx.x * blockDim.x + threadIdx.x;
   if (item >= M * per_row) return;
-  long long m = item / per_row;
-  long long n0 = (item - m * per_row) * kGE;
-  uint32_t V[kGE][kGarnerWords];
-  garner_digits(RC + m * ldc + n0, plane, P, V);
+  const long long m = item / per_row;
+  const long long n0 = (item - m * per_row) * GE;
+  uint32_t x[GE][W];
+  garner_reconstruct<W, GE>(RC + m * ldc + n0, plane, P, x);
+  int64_t* out = C + (m * N + n0) * LC;
+  if (n0 + GE <= N && ((reinterpret_cast<uintptr_t>(out) & 15u) == 0)) {
+    // GE * LC consecutive int64: 16-byte stores
 #pragma unroll
-  for (int e = 0; e < kGE; ++e) {
-    if (n0 + e >= N) break;
-    uint32_t x[2 * LC];
-    horner_words<2 * LC>(V[e], P, x);
-    int64_t* out = C + ((m * N) + n0 + e) * LC;
+    for (int t = 0; t < GE * LC / 2; ++t) {
+      const int e0 = (2 * t) / LC, l0 = (2 * t) % LC, e1 = (2 * t + 1) / LC, l1 = (2 * t + 1) % LC;
+      *reinterpret_cast<uint4*>(out + 2 * t) =
+          make_uint4(x[e0][2 * l0], x[e0][2 * l0 + 1], x[e1][2 * l1], x[e1][2 * l1 + 1]);
+    }
+  } else {
 #pragma unroll
-    for (int l = 0; l < LC; ++l) out[l] = (int64_t)(((unsigned long long)x[2 * l + 1] << 32) | x[2 * l]);
+    for (int e = 0; e < GE; ++e) {
+      if (n0 + e >= N) break;
+#pragma unroll
+      for (int l = 0; l < LC; ++l)
+        out[e * LC + l] = (int64_t)(((unsigned long long)x[e][2 * l + 1] << 32) | x[e][2 * l]);
+    }
   }
 }
 
@@ -499,12 +649,12 @@ __device__ __forceinline__ void outward_bits(const uint32_t (&x)[kEncW], int Q, 
                                              unsigned long long& hi) {
   const unsigned long long kMaxFinite = 0x7FEFFFFFFFFFFFFFull, kInf = 0x7FF0000000000000ull,
                            kSign = 0x8000000000000000ull;
-  bool neg = (x[kEncW - 1] >> 31) != 0;
+  const bool neg = (x[kEncW - 1] >> 31) != 0;
   uint32_t mag[kEncW];
   unsigned long long carry = neg ? 1ull : 0ull;
 #pragma unroll
   for (int k = 0; k < kEncW; ++k) {
-    unsigned long long t = (unsigned long long)(neg ? ~x[k] : x[k]) + carry;
+    const unsigned long long t = (unsigned long long)(neg ? ~x[k] : x[k]) + carry;
     mag[k] = (uint32_t)t;
     carry = t >> 32;
   }
@@ -516,33 +666,33 @@ __device__ __forceinline__ void outward_bits(const uint32_t (&x)[kEncW], int Q, 
     lo = hi = 0ull;
     return;
   }
-  int E = L - Q;  // floor(log2 |S 2^-Q|)
+  const int E = L - Q;  // floor(log2 |S 2^-Q|)
   if (E > 1023) {
     lo = neg ? (kSign | kInf) : kMaxFinite;
     hi = neg ? (kSign | kMaxFinite) : kInf;
     return;
   }
-  int u = E - 52 > -1074 ? E - 52 : -1074;  // exponent of one ulp at this magnitude
-  int sh = u + Q;                            // bit of |S| holding that ulp
+  const int u = E - 52 > -1074 ? E - 52 : -1074;  // exponent of one ulp at this magnitude
+  const int sh = u + Q;                            // bit of |S| holding that ulp
   unsigned long long T = 0ull;
   bool rem = false;
   if (sh <= 0) {
     // exact: |S| < 2^53 after the shift, since L - sh <= 52
 #pragma unroll
     for (int k = 0; k < 3; ++k) {
-      int b = 32 * k - sh;  // destination bit of word k
+      const int b = 32 * k - sh;  // destination bit of word k
       if (b < 64 && k < kEncW) T |= (unsigned long long)mag[k] << b;
     }
   } else {
     // T = bits [sh, sh + 53) of |S|; rem = any bit below sh
 #pragma unroll
     for (int k = 0; k < kEncW; ++k) {
-      int lo_bit = 32 * k, hi_bit = 32 * k + 32;
-      unsigned long long w = mag[k];
+      const int lo_bit = 32 * k, hi_bit = 32 * k + 32;
+      const unsigned long long w = mag[k];
       if (hi_bit <= sh) {
         rem |= w != 0;
       } else if (lo_bit < sh) {
-        int cut = sh - lo_bit;
+        const int cut = sh - lo_bit;
         rem |= (w & ((1ull << cut) - 1ull)) != 0;
         T |= w >> cut;
       } else if (lo_bit - sh < 64) {
@@ -551,7 +701,7 @@ __device__ __forceinline__ void outward_bits(const uint32_t (&x)[kEncW], int Q, 
     }
     T &= (1ull << 53) - 1ull;
   }
-  unsigned long long enc = (E >= -1022 ? (unsigned long long)(E + 1022) << 52 : 0ull) + T;
+  const unsigned long long enc = (E >= -1022 ? (unsigned long long)(E + 1022) << 52 : 0ull) + T;
   if (!rem) {
     lo = hi = (neg ? kSign : 0ull) | enc;
   } else if (!neg) {
@@ -567,25 +717,35 @@ __global__ void __launch_bounds__(128) garner_enclose_kernel(const uint8_t* __re
                                                              long long plane, long long M, long long N,
                                                              DevPlan* plan, unsigned long long* __restrict__ lo,
                                                              unsigned long long* __restrict__ hi) {
+  constexpr int GE = GarnerGE<kEncW>::value;
   if (plan->status) return;
-  int P = plan->P;
-  int Q = plan->f_a + plan->f_b;
-  long long per_row = (N + kGE - 1) / kGE;
-  long long item = (long long)blockIdx.x * blockDim.x + threadIdx.x;
+  const int P = plan->P;
+  const int Q = plan->f_a + plan->f_b;
+  const long long per_row = (N + GE - 1) / GE;
+  const long long item = (long long)blockIdx.x * blockDim.x + threadIdx.x;
   if (item >= M * per_row) return;
-  long long m = item / per_row;
-  long long n0 = (item - m * per_row) * kGE;
-  uint32_t V[kGE][kGarnerWords];
-  garner_digits(RC + m * ldc + n0, plane, P, V);
+  const long long m = item / per_row;
+  const long long n0 = (item - m * per_row) * GE;
+  uint32_t x[GE][kEncW];
+  garner_reconstruct<kEncW, GE>(RC + m * ldc + n0, plane, P, x);
+  unsigned long long l[GE], h[GE];
 #pragma unroll
-  for (int e = 0; e < kGE; ++e) {
-    if (n0 + e >= N) break;
-    uint32_t x[kEncW];
-    horner_words<kEncW>(V[e], P, x);
-    unsigned long long l, h;
-    outward_bits(x, Q, l, h);
-    lo[m * N + n0 + e] = l;
-    hi[m * N + n0 + e] = h;
+  for (int e = 0; e < GE; ++e) outward_bits(x[e], Q, l[e], h[e]);
+  unsigned long long* plo = lo + m * N + n0;
+  unsigned long long* phi = hi + m * N + n0;
+  if (n0 + GE <= N && ((reinterpret_cast<uintptr_t>(plo) & 15u) == 0)) {
+#pragma unroll
+    for (int t = 0; t < GE / 2; ++t) {
+      reinterpret_cast<ulonglong2*>(plo)[t] = make_ulonglong2(l[2 * t], l[2 * t + 1]);
+      reinterpret_cast<ulonglong2*>(phi)[t] = make_ulonglong2(h[2 * t], h[2 * t + 1]);
+    }
+  } else {
+#pragma unroll
+    for (int e = 0; e < GE; ++e) {
+      if (n0 + e >= N) break;
+      plo[e] = l[e];
+      phi[e] = h[e];
+    }
   }
 }
 
@@ -625,29 +785,24 @@ cudaError_t upload_tables() {
 
 static int planner_blocks(long long n) {
   long long b = (n + 256LL * 8 - 1) / (256LL * 8);
-  long long cap = 2LL * sm_count();
+  long long cap = 4LL * sm_count();
   return (int)(b < 1 ? 1 : (b > cap ? cap : b));
 }
 
-cudaError_t launch_plan_i64(const int64_t* A, long long nA, const int64_t* B, long long nB, DevPlan* plan,
-                            cudaStream_t s) {
-  int ba = planner_blocks(nA), bb = planner_blocks(nB);
-  plan_i64_kernel<<<ba + bb, 256, 0, s>>>(A, nA, B, nB, ba, plan);
-  return cudaGetLastError();
-}
-
-cudaError_t launch_plan_limbs(const int64_t* A, long long nA, int la, const int64_t* B, long long nB, int lb,
-                              DevPlan* plan, cudaStream_t s) {
-  int ba = planner_blocks(nA), bb = planner_blocks(nB);
-  plan_limbs_kernel<<<ba + bb, 256, 0, s>>>(A, nA, la, B, nB, lb, ba, plan);
-  return cudaGetLastError();
-}
-
-cudaError_t launch_plan_f64(const double* A, long long nA, const double* B, long long nB, DevPlan* plan,
-                            cudaStream_t s) {
-  int ba = planner_blocks(nA), bb = planner_blocks(nB);
-  plan_f64_kernel<<<ba + bb, 256, 0, s>>>(reinterpret_cast<const unsigned long long*>(A), nA,
-                                          reinterpret_cast<const unsigned long long*>(B), nB, ba, plan);
+cudaError_t launch_plan(int op, const void* A, long long nA, int la, const void* B, long long nB, int lb, int lc,
+                        long long K, int nprimes_fixed, DevPlan* plan, cudaStream_t s) {
+  PlanArgs pa{op, K, nprimes_fixed, la, lb, lc};
+  if (nprimes_fixed) nA = nB = 0;  // only the finalisation is needed
+  const int ba = planner_blocks(nA), bb = planner_blocks(nB);
+  if (op == RG_OP_I64)
+    plan_i64_kernel<<<ba + bb, 256, 0, s>>>(static_cast<const int64_t*>(A), nA, static_cast<const int64_t*>(B), nB,
+                                            ba, plan, pa);
+  else if (op == RG_OP_LIMBS)
+    plan_limbs_kernel<<<ba + bb, 256, 0, s>>>(static_cast<const int64_t*>(A), nA, la,
+                                              static_cast<const int64_t*>(B), nB, lb, ba, plan, pa);
+  else
+    plan_f64_kernel<<<ba + bb, 256, 0, s>>>(static_cast<const unsigned long long*>(A), nA,
+                                            static_cast<const unsigned long long*>(B), nB, ba, plan, pa);
   return cudaGetLastError();
 }
 
@@ -664,60 +819,56 @@ static SplitSide make_side(const void* X, __half* Y, long long R, long long C, l
   return s;
 }
 
-cudaError_t launch_split(int op, const void* A, const void* B, int la, int lb, int lc, long long M, long long N,
-                         long long K, long long lda, long long ldb, void* RA, void* RB, int nprimes_fixed,
-                         DevPlan* plan, cudaStream_t st) {
+static unsigned split_grid(long long items) {
+  long long b = (items + 255) / 256;
+  const long long cap = 8LL * sm_count();
+  return (unsigned)(b < 1 ? 1 : (b > cap ? cap : b));
+}
+
+cudaError_t launch_split(int op, const void* A, const void* B, int la, int lb, long long M, long long N, long long K,
+                         long long lda, long long ldb, void* RA, void* RB, DevPlan* plan, cudaStream_t st) {
   __half* ra = static_cast<__half*>(RA);
   __half* rb = static_cast<__half*>(RB);
   if (op == RG_OP_ENCLOSE) {
     constexpr int V = 8;
-    SplitSide sa = make_side(A, ra, M, K, lda, 1, V), sb = make_side(B, rb, K, N, ldb, 1, V);
-    long long nbA = (sa.items + 255) / 256, nbB = (sb.items + 255) / 256;
-    split_f64_kernel<V><<<(unsigned)(nbA + nbB), 256, 0, st>>>(sa, sb, nbA, plan, K);
+    const SplitSide sa = make_side(A, ra, M, K, lda, 1, V), sb = make_side(B, rb, K, N, ldb, 1, V);
+    split_f64_kernel<V><<<split_grid(sa.items + sb.items), 256, 0, st>>>(sa, sb, plan);
     return cudaGetLastError();
   }
-  int L = la > lb ? la : lb;
+  const int L = la > lb ? la : lb;
   if (L <= 1) {
     constexpr int V = 8;
-    SplitSide sa = make_side(A, ra, M, K, lda, la, V), sb = make_side(B, rb, K, N, ldb, lb, V);
-    long long nbA = (sa.items + 255) / 256, nbB = (sb.items + 255) / 256;
-    split_int_kernel<V, 6><<<(unsigned)(nbA + nbB), 256, 0, st>>>(sa, sb, nbA, plan, op, K, nprimes_fixed, la, lb,
-                                                                  lc);
+    const SplitSide sa = make_side(A, ra, M, K, lda, la, V), sb = make_side(B, rb, K, N, ldb, lb, V);
+    split_int_kernel<V, 6, 1><<<split_grid(sa.items + sb.items), 256, 0, st>>>(sa, sb, plan);
   } else if (L <= 2) {
     constexpr int V = 4;
-    SplitSide sa = make_side(A, ra, M, K, lda, la, V), sb = make_side(B, rb, K, N, ldb, lb, V);
-    long long nbA = (sa.items + 255) / 256, nbB = (sb.items + 255) / 256;
-    split_int_kernel<V, 11><<<(unsigned)(nbA + nbB), 256, 0, st>>>(sa, sb, nbA, plan, op, K, nprimes_fixed, la, lb,
-                                                                   lc);
+    const SplitSide sa = make_side(A, ra, M, K, lda, la, V), sb = make_side(B, rb, K, N, ldb, lb, V);
+    split_int_kernel<V, 11, 2><<<split_grid(sa.items + sb.items), 256, 0, st>>>(sa, sb, plan);
   } else {
     constexpr int V = 2;
-    SplitSide sa = make_side(A, ra, M, K, lda, la, V), sb = make_side(B, rb, K, N, ldb, lb, V);
-    long long nbA = (sa.items + 255) / 256, nbB = (sb.items + 255) / 256;
-    split_int_kernel<V, 22><<<(unsigned)(nbA + nbB), 256, 0, st>>>(sa, sb, nbA, plan, op, K, nprimes_fixed, la, lb,
-                                                                   lc);
+    const SplitSide sa = make_side(A, ra, M, K, lda, la, V), sb = make_side(B, rb, K, N, ldb, lb, V);
+    split_int_kernel<V, 22, 4><<<split_grid(sa.items + sb.items), 256, 0, st>>>(sa, sb, plan);
   }
   return cudaGetLastError();
 }
 
 cudaError_t launch_garner(int op, const void* RC, long long ldc, long long plane, long long M, long long N, int lc,
                           DevPlan* plan, void* out0, void* out1, cudaStream_t st) {
-  long long items = M * ((N + kGE - 1) / kGE);
-  unsigned blocks = (unsigned)((items + 127) / 128);
   const uint8_t* rc = static_cast<const uint8_t*>(RC);
+  auto blocks_for = [&](int ge) { return (unsigned)((M * ((N + ge - 1) / ge) + 127) / 128); };
   if (op == RG_OP_ENCLOSE) {
-    garner_enclose_kernel<<<blocks, 128, 0, st>>>(rc, ldc, plane, M, N, plan,
-                                                  static_cast<unsigned long long*>(out0),
-                                                  static_cast<unsigned long long*>(out1));
+    garner_enclose_kernel<<<blocks_for(GarnerGE<kEncW>::value), 128, 0, st>>>(
+        rc, ldc, plane, M, N, plan, static_cast<unsigned long long*>(out0), static_cast<unsigned long long*>(out1));
     return cudaGetLastError();
   }
   int64_t* C = static_cast<int64_t*>(out0);
   switch (lc) {
-    case 1: garner_int_kernel<1><<<blocks, 128, 0, st>>>(rc, ldc, plane, M, N, plan, C); break;
-    case 2: garner_int_kernel<2><<<blocks, 128, 0, st>>>(rc, ldc, plane, M, N, plan, C); break;
-    case 3: garner_int_kernel<3><<<blocks, 128, 0, st>>>(rc, ldc, plane, M, N, plan, C); break;
-    case 4: garner_int_kernel<4><<<blocks, 128, 0, st>>>(rc, ldc, plane, M, N, plan, C); break;
-    case 5: garner_int_kernel<5><<<blocks, 128, 0, st>>>(rc, ldc, plane, M, N, plan, C); break;
-    case 6: garner_int_kernel<6><<<blocks, 128, 0, st>>>(rc, ldc, plane, M, N, plan, C); break;
+    case 1: garner_int_kernel<1><<<blocks_for(GarnerGE<2>::value), 128, 0, st>>>(rc, ldc, plane, M, N, plan, C); break;
+    case 2: garner_int_kernel<2><<<blocks_for(GarnerGE<4>::value), 128, 0, st>>>(rc, ldc, plane, M, N, plan, C); break;
+    case 3: garner_int_kernel<3><<<blocks_for(GarnerGE<6>::value), 128, 0, st>>>(rc, ldc, plane, M, N, plan, C); break;
+    case 4: garner_int_kernel<4><<<blocks_for(GarnerGE<8>::value), 128, 0, st>>>(rc, ldc, plane, M, N, plan, C); break;
+    case 5: garner_int_kernel<5><<<blocks_for(GarnerGE<10>::value), 128, 0, st>>>(rc, ldc, plane, M, N, plan, C); break;
+    case 6: garner_int_kernel<6><<<blocks_for(GarnerGE<12>::value), 128, 0, st>>>(rc, ldc, plane, M, N, plan, C); break;
     default: return cudaErrorInvalidValue;
   }
   return cudaGetLastError();

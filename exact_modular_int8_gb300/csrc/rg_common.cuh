@@ -14,6 +14,7 @@ constexpr int kNumPrimes = RG_NUM_PRIMES;  // odd primes 3..251, largest first
 constexpr int kChunkBits = 12;             // operand split into 12-bit chunks
 constexpr int kMaxChunks = 24;             // covers 256-bit operands (22) with slack
 constexpr int kGarnerWords = 14;           // ceil(53 / 4) int8x4 words per Garner row
+constexpr int kQWords = 11;                // 32-bit words of the mixed-radix weights Q_i
 constexpr int kMaxLimbsOut = RG_MAX_LIMBS_OUT;
 
 // Plan of one call, kept in the first bytes of the workspace.  The planner
@@ -28,7 +29,8 @@ struct DevPlan {
   int f_a, f_b;           // fp64 scale exponents
   int lossless;           // fp64: 1 if the scaling is exact
   int nchunk_a, nchunk_b; // 12-bit chunks the split reads per entry
-  int pad0[6];
+  unsigned blocks_done;   // planner blocks finished (the last one derives the plan)
+  int pad0[5];
   // reductions written by the planner kernels
   unsigned long long maxmag_a, maxmag_b;  // int64 operands: max |x|
   int maxbits_a, maxbits_b;               // limb operands: max bit length of |x|
@@ -54,6 +56,8 @@ struct Tables {
   // Q_i = q_0 * ... * q_{i-1}.  gd rows are packed 4 per int32 for dp4a.
   int ginv[kNumPrimes];
   int gd_packed[kNumPrimes][kGarnerWords];
+  // Q_i = q_0 * ... * q_{i-1} as little-endian 32-bit words (Q_52 < 2^330).
+  uint32_t Qw[kNumPrimes][kQWords];
 };
 
 // Host side: the tables (built once) and the primes.
@@ -75,6 +79,16 @@ __device__ __forceinline__ float bal_mod(float s, float q, float invq) {
   r = r > h ? r - q : r;
   r = r < -h ? r + q : r;
   return r;
+}
+
+// The same for |s| <= 2^23, without corrections: |s * fl(1/q) - s/q| <
+// |s/q| 2^-24 <= 1/(2q), while s/q (s an integer, q odd) lies at least 1/(2q)
+// from every half-integer, so rint(s * fl(1/q)) == round(s/q) exactly and
+// s - q * round(s/q) is already the balanced residue.
+__device__ __forceinline__ float bal_mod_small(float s, float q, float invq) {
+  const float magic = 12582912.0f;
+  const float t = __fadd_rn(__fmaf_rn(s, invq, magic), -magic);
+  return __fmaf_rn(-t, q, s);
 }
 
 // Residue in [0, q) of an integer-valued float s, |s| < 2^24.

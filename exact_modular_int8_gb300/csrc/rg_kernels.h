@@ -11,19 +11,16 @@ namespace rg {
 // Copies the constant tables to the current device once.
 cudaError_t upload_tables();
 
-// Planner reductions into plan (the host zeroes the plan block first).
-cudaError_t launch_plan_i64(const int64_t* A, long long nA, const int64_t* B, long long nB, DevPlan* plan,
-                            cudaStream_t s);
-cudaError_t launch_plan_limbs(const int64_t* A, long long nA, int la, const int64_t* B, long long nB, int lb,
-                              DevPlan* plan, cudaStream_t s);
-cudaError_t launch_plan_f64(const double* A, long long nA, const double* B, long long nB, DevPlan* plan,
-                            cudaStream_t s);
+// Planner: reductions over A and B into the plan block (the host zeroes it
+// first); the last block derives the prime count, chunk counts and fp64
+// scales.  With nprimes_fixed > 0 only that derivation runs.
+cudaError_t launch_plan(int op, const void* A, long long nA, int la, const void* B, long long nB, int lb, int lc,
+                        long long K, int nprimes_fixed, DevPlan* plan, cudaStream_t s);
 
 // Residue split of A [M][K] into RA [pmax][M][lda] and of B [K][N] into
-// RB [pmax][K][ldb] (fp16 balanced residues); also finalises the plan.
-cudaError_t launch_split(int op, const void* A, const void* B, int la, int lb, int lc, long long M, long long N,
-                         long long K, long long lda, long long ldb, void* RA, void* RB, int nprimes_fixed,
-                         DevPlan* plan, cudaStream_t st);
+// RB [pmax][K][ldb] (fp16 balanced residues), for the plan's prime count.
+cudaError_t launch_split(int op, const void* A, const void* B, int la, int lb, long long M, long long N, long long K,
+                         long long lda, long long ldb, void* RA, void* RB, DevPlan* plan, cudaStream_t st);
 
 // Per-prime tensor-core product RC[p] = RA[p] * RB[p] mod q_p (uint8).
 cudaError_t launch_gemm(const void* RA, long long lda, const void* RB, long long ldb, void* RC, long long ldc,

@@ -64,6 +64,20 @@ void build(Tables& t) {
     t.log2P[n2] = 32 * top + b;
   }
 
+  // Mixed-radix weights Q_i as words.
+  {
+    uint32_t q_words[kQWords] = {1};
+    for (int i = 0; i < kNumPrimes; ++i) {
+      for (int w = 0; w < kQWords; ++w) t.Qw[i][w] = q_words[w];
+      uint64_t carry = 0;
+      for (int w = 0; w < kQWords; ++w) {
+        uint64_t v = (uint64_t)q_words[w] * (uint64_t)t.q[i] + carry;
+        q_words[w] = (uint32_t)v;
+        carry = v >> 32;
+      }
+    }
+  }
+
   // Garner constants.
   for (int i = 0; i < kNumPrimes; ++i) {
     int q = t.q[i];
