@@ -522,19 +522,53 @@ struct GarnerGE {
 };
 
 constexpr int kGarnerBatch = 8;
+constexpr float kMagic = 12582912.0f;     // 1.5 * 2^23
+constexpr int kMagicBits = 0x4B400000;    // its bit pattern
+
+// Exact conversions without the conversion unit, for |v| < 2^22: the integer
+// sits in the low mantissa bits of kMagic + v.
+__device__ __forceinline__ float int_to_float_exact(int v) { return __int_as_float(kMagicBits + v) - kMagic; }
+__device__ __forceinline__ int float_bits_offset(float v) { return __float_as_int(v + kMagic); }  // = kMagicBits + v
+
+// x (W 32-bit words, two's complement, mod 2^(32W)) += D * Q_i, for the words
+// that can be significant once digits up to `last` are in (|x| < 2^(8(last+1)-1)).
+template <int W>
+__device__ __forceinline__ void add_scaled_weight(uint32_t (&x)[W], int D, int i, int last) {
+  if constexpr (W == 2) {
+    const unsigned long long Qi = ((unsigned long long)c_tab.Qw[i][1] << 32) | c_tab.Qw[i][0];
+    const unsigned long long x64 = (((unsigned long long)x[1] << 32) | x[0]) + (unsigned long long)(long long)D * Qi;
+    x[0] = (uint32_t)x64;
+    x[1] = (uint32_t)(x64 >> 32);
+  } else {
+    long long carry = 0;
+#pragma unroll
+    for (int k = 0; k < W; ++k) {
+      if (k < last / 4 + 2) {
+        const long long qk = k < kQWords ? (long long)c_tab.Qw[i][k < kQWords ? k : 0] : 0ll;
+        const long long t = (long long)x[k] + qk * D + carry;
+        x[k] = (uint32_t)t;
+        carry = t >> 32;
+      }
+    }
+  }
+}
 
 // x[e] (W 32-bit words, two's complement) = the reconstructed integers of the
 // GE residue vectors starting at rc (plane = distance between primes).
+// Digits are combined in pairs, D = v_i + q_i v_{i+1} (|D| < 2^15, exact in
+// fp32), so the wide accumulation runs once per two primes.
 template <int W, int GE>
 __device__ __forceinline__ void garner_reconstruct(const uint8_t* __restrict__ rc, long long plane, int P,
                                                    uint32_t (&x)[GE][W]) {
   uint32_t V[GE][kGarnerWords];
+  float pend[GE];  // the even digit of the current pair, as float
 #pragma unroll
   for (int e = 0; e < GE; ++e) {
 #pragma unroll
     for (int w = 0; w < kGarnerWords; ++w) V[e][w] = 0u;
 #pragma unroll
     for (int k = 0; k < W; ++k) x[e][k] = 0u;
+    pend[e] = 0.0f;
   }
 #pragma unroll
   for (int i0 = 0; i0 < kNumPrimes; i0 += kGarnerBatch) {
@@ -554,38 +588,30 @@ __device__ __forceinline__ void garner_reconstruct(const uint8_t* __restrict__ r
       if (i >= kNumPrimes || i >= P) break;
       const float q = c_tab.qf[i], iq = c_tab.invq[i];
       const int gi = c_tab.ginv[i];
+      // byte selector that inserts a new low byte at position i % 4
+      constexpr unsigned kSel[4] = {0x3214u, 0x3240u, 0x3410u, 0x4210u};
 #pragma unroll
       for (int e = 0; e < GE; ++e) {
-        const int s = gi * (int)((rw[j] >> (8 * e)) & 0xFFu);
-        int acc = 0;
+        // s = Q_i^-1 r_i - sum_{j<i} (Q_j Q_i^-1 mod q_i) v_j, |s| < 2^20
+        int acc = gi * (int)((rw[j] >> (8 * e)) & 0xFFu);
 #pragma unroll
         for (int w = 0; w < kGarnerWords; ++w)
           if (4 * w < i) acc = __dp4a((int)V[e][w], c_tab.gd_packed[i][w], acc);
-        const int v = (int)bal_mod_small((float)(s - acc), q, iq);  // |s - acc| < 2^20
-        V[e][i / 4] |= ((uint32_t)v & 0xFFu) << (8 * (i % 4));
-        if constexpr (W == 2) {
-          // one 64-bit word: x += v * (Q_i mod 2^64), wrapping; exact because
-          // the final value fits the output word
-          const unsigned long long Qi = ((unsigned long long)c_tab.Qw[i][1] << 32) | c_tab.Qw[i][0];
-          const unsigned long long x64 = (((unsigned long long)x[e][1] << 32) | x[e][0]) +
-                                         (unsigned long long)(long long)v * Qi;
-          x[e][0] = (uint32_t)x64;
-          x[e][1] = (uint32_t)(x64 >> 32);
-        } else {
-          // x += v * Q_i over the words that can be significant after this
-          // digit; a word entering that range first takes the sign of the word
-          // below it.
-          if (i > 0 && (i % 4) == 0 && i / 4 + 1 < W) x[e][i / 4 + 1] = (uint32_t)((int)x[e][i / 4] >> 31);
-          long long carry = 0;
-#pragma unroll
-          for (int k = 0; k < W; ++k) {
-            if (k < i / 4 + 2) {
-              const long long qk = k < kQWords ? (long long)c_tab.Qw[i][k < kQWords ? k : 0] : 0ll;
-              const long long t = (long long)x[e][k] + qk * v + carry;
-              x[e][k] = (uint32_t)t;
-              carry = t >> 32;
-            }
+        const float vf = bal_mod_small(int_to_float_exact(acc), q, iq);
+        const int vb = float_bits_offset(vf);
+        V[e][i / 4] = __byte_perm(V[e][i / 4], (uint32_t)vb, kSel[i % 4]);
+        if ((i & 1) == 0) {
+          pend[e] = vf;
+          if (i + 1 >= P) {  // unpaired last digit
+            if (W > 2 && (i % 4) == 0 && i > 0 && i / 4 + 1 < W)
+              x[e][i / 4 + 1] = (uint32_t)((int)x[e][i / 4] >> 31);
+            add_scaled_weight<W>(x[e], vb - kMagicBits, i, i);
           }
+        } else {
+          const float D = __fmaf_rn(vf, c_tab.qf[i - 1], pend[e]);  // v_{i-1} + q_{i-1} v_i
+          if (W > 2 && ((i - 1) % 4) == 0 && i > 1 && (i - 1) / 4 + 1 < W)
+            x[e][(i - 1) / 4 + 1] = (uint32_t)((int)x[e][(i - 1) / 4] >> 31);
+          add_scaled_weight<W>(x[e], float_bits_offset(D) - kMagicBits, i - 1, i);
         }
       }
     }

@@ -51,8 +51,8 @@ struct Tables {
   float invq[kNumPrimes];                     // fl(1/q)
   float chunk_w[kNumPrimes][kMaxChunks];      // balanced 2^(12c) mod q, as float
   int log2P[kNumPrimes + 1];                  // floor(log2(q_0 * ... * q_{n-1})), n = 0..53
-  // Balanced Garner: v_i = bal( ginv[i] * r_i - sum_{j<i} gd[i][j] * v_j  mod q_i )
-  // with ginv[i] = bal(Q_i^-1 mod q_i), gd[i][j] = bal((Q_j mod q_i) * Q_i^-1 mod q_i),
+  // Balanced Garner: v_i = bal( ginv[i] * r_i + sum_{j<i} gd[i][j] * v_j  mod q_i )
+  // with ginv[i] = bal(Q_i^-1 mod q_i), gd[i][j] = bal(-(Q_j mod q_i) * Q_i^-1 mod q_i),
   // Q_i = q_0 * ... * q_{i-1}.  gd rows are packed 4 per int32 for dp4a.
   int ginv[kNumPrimes];
   int gd_packed[kNumPrimes][kGarnerWords];

@@ -87,7 +87,8 @@ void build(Tables& t) {
     t.ginv[i] = balanced(inv, q);
     long long Qj = 1;  // Q_j mod q, j = 0..i-1
     for (int j = 0; j < i; ++j) {
-      int d = balanced((int)(Qj * inv % q), q);
+      // negated, so that the digit is Q_i^-1 r_i + sum_j gd[i][j] v_j
+      int d = balanced((int)((q - Qj * inv % q) % q), q);
       uint32_t byte = (uint32_t)(uint8_t)(int8_t)d;
       t.gd_packed[i][j / 4] |= (int)(byte << (8 * (j % 4)));
       Qj = Qj * t.q[j] % q;

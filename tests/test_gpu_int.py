@@ -140,3 +140,22 @@ def test_repeatable(rg):
     C1 = host(rg.res_gemm_i64(dev(A), dev(B)))
     C2 = host(rg.res_gemm_i64(dev(A), dev(B)))
     assert np.array_equal(C1, C2)
+
+
+@pytest.mark.parametrize("bits", [1, 4, 8, 12, 16, 20, 24, 28, 31])
+def test_every_small_prime_count(rg, bits):
+    # value ranges that make the planner pick 1, 2, ..., 9 primes
+    # K = 1 keeps K * max|A| * max|B| < 2^62 for 31-bit entries
+    A, B = int_matrices(300, 700, 1, -(2**bits) + 1, 2**bits, bits)
+    C = host(rg.res_gemm_i64(dev(A), dev(B)))
+    assert np.array_equal(C, A @ B)
+    T = 2 * bits
+    P = rg.get_plan()["nprimes"]
+    assert 1 <= P <= 9 and P == next(n for n in range(1, 54) if _log2_prod(rg, n) >= T + 1)
+
+
+def _log2_prod(rg, n):
+    prod = 1
+    for q in rg.primes()[:n]:
+        prod *= q
+    return prod.bit_length() - 1

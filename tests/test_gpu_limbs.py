@@ -63,9 +63,11 @@ def test_wide128_2048_sampled_rows(rg):
     assert plan["bits_a"] == 127 and plan["bits_b"] == 127 and plan["bound_bits"] == 127 + 127 + 11
 
 
-def test_wide128_all_primes(rg):
+@pytest.mark.parametrize("nprimes", [42, 43, 52, 53])
+def test_wide128_fixed_prime_counts(rg, nprimes):
+    # both parities of the prime count on the multi-word reconstruction
     A, B = limb_matrices(64, 64, 256, 2, 9)
-    C = host(rg.res_gemm_limbs(dev(A), dev(B), 6, nprimes=53))
+    C = host(rg.res_gemm_limbs(dev(A), dev(B), 6, nprimes=nprimes))
     assert np.array_equal(C, oracle.matmul_limbs(A, B, 6))
 
 
