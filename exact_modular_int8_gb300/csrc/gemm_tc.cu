@@ -211,6 +211,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                         const __grid_constant__ CUtensorMap tmC, const __grid_constant__ GemmParams gp,
                         DevPlan* plan) {
   extern __shared__ uint8_t smem_raw[];
+  wait_for_predecessor();
   if (plan->status) return;
   const int P = gp.P_fixed ? gp.P_fixed : plan->P;
   const int total = P * gp.mt * gp.nt;
@@ -439,6 +440,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
 
   tc_fence_before();
   __syncthreads();
+  allow_dependents();
   if (warp == 1) {
     tc_fence_after();
     asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem_base), "r"((uint32_t)TMEM_COLS));
@@ -520,8 +522,7 @@ cudaError_t launch_gemm(const void* RA, long long lda, const void* RB, long long
   long long tiles = (long long)pmax * gp.mt * gp.nt;
   int grid = (int)(tiles < sms[dev] ? tiles : sms[dev]);
   if (grid < 1) grid = 1;
-  residue_gemm_kernel<<<grid, NUM_THREADS, SMEM_BYTES, st>>>(ma, mb, mc, gp, plan);
-  return cudaGetLastError();
+  return launch_dependent(residue_gemm_kernel, dim3(grid), dim3(NUM_THREADS), SMEM_BYTES, st, ma, mb, mc, gp, plan);
 }
 
 }  // namespace rg

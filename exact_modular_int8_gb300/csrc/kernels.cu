@@ -174,6 +174,8 @@ __device__ void planner_finish(DevPlan* plan, const PlanArgs& a) {
     plan->nchunk_b = lp.nchunk_b;
     if (lp.status) set_status(&plan->status, lp.status);
   }
+  __syncthreads();
+  allow_dependents();
 }
 
 // Blocks [0, nbA) read A, the others read B.
@@ -378,6 +380,7 @@ __device__ __forceinline__ void emit_residues(const float (&cf)[VEC][NCH], int n
 // 16-byte loads when they lie fully inside the row and are aligned.
 template <int VEC, int NCH, int LMAX>
 __global__ void __launch_bounds__(256) split_int_kernel(SplitSide sa, SplitSide sb, const DevPlan* plan) {
+  wait_for_predecessor();
   if (plan->status) return;
   const int P = plan->P;
   const int nch_a = plan->nchunk_a, nch_b = plan->nchunk_b;
@@ -429,6 +432,7 @@ __global__ void __launch_bounds__(256) split_int_kernel(SplitSide sa, SplitSide 
     }
     emit_residues<VEC, NCH>(cf, nch, P, s.Y + row * s.ldy + col0, s.plane);
   }
+  allow_dependents();
 }
 
 // Binary64 operands: X' = x * 2^f = +-m * 2^sh with sh = max(be,1) - min(be',1)
@@ -437,6 +441,7 @@ __global__ void __launch_bounds__(256) split_int_kernel(SplitSide sa, SplitSide 
 template <int VEC>
 __global__ void __launch_bounds__(256) split_f64_kernel(SplitSide sa, SplitSide sb, const DevPlan* plan) {
   __shared__ float w_s[kNumPrimes][kMaxChunks];
+  wait_for_predecessor();
   if (plan->status) return;
   const int P = plan->P;
   const int emin_a = 4096 - plan->inv_mine_a, emin_b = 4096 - plan->inv_mine_b;
@@ -499,6 +504,7 @@ __global__ void __launch_bounds__(256) split_f64_kernel(SplitSide sa, SplitSide 
       *reinterpret_cast<uint4*>(y + (long long)p * s.plane) = *reinterpret_cast<const uint4*>(h);
     }
   }
+  allow_dependents();
 }
 
 // ---------------------------------------------------------------------------
@@ -638,6 +644,7 @@ __global__ void __launch_bounds__(128) garner_int_kernel(const uint8_t* __restri
                                                          long long plane, long long M, long long N, DevPlan* plan,
                                                          int64_t* __restrict__ C) {
   constexpr int W = 2 * LC, GE = GarnerGE<W>::value;
+  wait_for_predecessor();
   if (plan->status) return;
   const int P = plan->P;
   const long long per_row = (N + GE - 1) / GE;
@@ -744,6 +751,7 @@ __global__ void __launch_bounds__(128) garner_enclose_kernel(const uint8_t* __re
                                                              DevPlan* plan, unsigned long long* __restrict__ lo,
                                                              unsigned long long* __restrict__ hi) {
   constexpr int GE = GarnerGE<kEncW>::value;
+  wait_for_predecessor();
   if (plan->status) return;
   const int P = plan->P;
   const int Q = plan->f_a + plan->f_b;
@@ -858,22 +866,25 @@ cudaError_t launch_split(int op, const void* A, const void* B, int la, int lb, l
   if (op == RG_OP_ENCLOSE) {
     constexpr int V = 8;
     const SplitSide sa = make_side(A, ra, M, K, lda, 1, V), sb = make_side(B, rb, K, N, ldb, 1, V);
-    split_f64_kernel<V><<<split_grid(sa.items + sb.items), 256, 0, st>>>(sa, sb, plan);
-    return cudaGetLastError();
+    return launch_dependent(split_f64_kernel<V>, split_grid(sa.items + sb.items), 256, 0, st, sa, sb,
+                            (const DevPlan*)plan);
   }
   const int L = la > lb ? la : lb;
   if (L <= 1) {
     constexpr int V = 8;
     const SplitSide sa = make_side(A, ra, M, K, lda, la, V), sb = make_side(B, rb, K, N, ldb, lb, V);
-    split_int_kernel<V, 6, 1><<<split_grid(sa.items + sb.items), 256, 0, st>>>(sa, sb, plan);
+    return launch_dependent(split_int_kernel<V, 6, 1>, split_grid(sa.items + sb.items), 256, 0, st, sa, sb,
+                            (const DevPlan*)plan);
   } else if (L <= 2) {
     constexpr int V = 4;
     const SplitSide sa = make_side(A, ra, M, K, lda, la, V), sb = make_side(B, rb, K, N, ldb, lb, V);
-    split_int_kernel<V, 11, 2><<<split_grid(sa.items + sb.items), 256, 0, st>>>(sa, sb, plan);
+    return launch_dependent(split_int_kernel<V, 11, 2>, split_grid(sa.items + sb.items), 256, 0, st, sa, sb,
+                            (const DevPlan*)plan);
   } else {
     constexpr int V = 2;
     const SplitSide sa = make_side(A, ra, M, K, lda, la, V), sb = make_side(B, rb, K, N, ldb, lb, V);
-    split_int_kernel<V, 22, 4><<<split_grid(sa.items + sb.items), 256, 0, st>>>(sa, sb, plan);
+    return launch_dependent(split_int_kernel<V, 22, 4>, split_grid(sa.items + sb.items), 256, 0, st, sa, sb,
+                            (const DevPlan*)plan);
   }
   return cudaGetLastError();
 }
@@ -881,23 +892,20 @@ cudaError_t launch_split(int op, const void* A, const void* B, int la, int lb, l
 cudaError_t launch_garner(int op, const void* RC, long long ldc, long long plane, long long M, long long N, int lc,
                           DevPlan* plan, void* out0, void* out1, cudaStream_t st) {
   const uint8_t* rc = static_cast<const uint8_t*>(RC);
-  auto blocks_for = [&](int ge) { return (unsigned)((M * ((N + ge - 1) / ge) + 127) / 128); };
-  if (op == RG_OP_ENCLOSE) {
-    garner_enclose_kernel<<<blocks_for(GarnerGE<kEncW>::value), 128, 0, st>>>(
-        rc, ldc, plane, M, N, plan, static_cast<unsigned long long*>(out0), static_cast<unsigned long long*>(out1));
-    return cudaGetLastError();
-  }
+  auto blocks_for = [&](int ge) { return dim3((unsigned)((M * ((N + ge - 1) / ge) + 127) / 128)); };
+  if (op == RG_OP_ENCLOSE)
+    return launch_dependent(garner_enclose_kernel, blocks_for(GarnerGE<kEncW>::value), 128, 0, st, rc, ldc, plane, M,
+                            N, plan, static_cast<unsigned long long*>(out0), static_cast<unsigned long long*>(out1));
   int64_t* C = static_cast<int64_t*>(out0);
   switch (lc) {
-    case 1: garner_int_kernel<1><<<blocks_for(GarnerGE<2>::value), 128, 0, st>>>(rc, ldc, plane, M, N, plan, C); break;
-    case 2: garner_int_kernel<2><<<blocks_for(GarnerGE<4>::value), 128, 0, st>>>(rc, ldc, plane, M, N, plan, C); break;
-    case 3: garner_int_kernel<3><<<blocks_for(GarnerGE<6>::value), 128, 0, st>>>(rc, ldc, plane, M, N, plan, C); break;
-    case 4: garner_int_kernel<4><<<blocks_for(GarnerGE<8>::value), 128, 0, st>>>(rc, ldc, plane, M, N, plan, C); break;
-    case 5: garner_int_kernel<5><<<blocks_for(GarnerGE<10>::value), 128, 0, st>>>(rc, ldc, plane, M, N, plan, C); break;
-    case 6: garner_int_kernel<6><<<blocks_for(GarnerGE<12>::value), 128, 0, st>>>(rc, ldc, plane, M, N, plan, C); break;
+    case 1: return launch_dependent(garner_int_kernel<1>, blocks_for(GarnerGE<2>::value), 128, 0, st, rc, ldc, plane, M, N, plan, C);
+    case 2: return launch_dependent(garner_int_kernel<2>, blocks_for(GarnerGE<4>::value), 128, 0, st, rc, ldc, plane, M, N, plan, C);
+    case 3: return launch_dependent(garner_int_kernel<3>, blocks_for(GarnerGE<6>::value), 128, 0, st, rc, ldc, plane, M, N, plan, C);
+    case 4: return launch_dependent(garner_int_kernel<4>, blocks_for(GarnerGE<8>::value), 128, 0, st, rc, ldc, plane, M, N, plan, C);
+    case 5: return launch_dependent(garner_int_kernel<5>, blocks_for(GarnerGE<10>::value), 128, 0, st, rc, ldc, plane, M, N, plan, C);
+    case 6: return launch_dependent(garner_int_kernel<6>, blocks_for(GarnerGE<12>::value), 128, 0, st, rc, ldc, plane, M, N, plan, C);
     default: return cudaErrorInvalidValue;
   }
-  return cudaGetLastError();
 }
 
 }  // namespace rg
