@@ -44,7 +44,7 @@ NUM_PRIMES = 53
 EXPORTED = (
     "res_gemm_i64", "res_gemm_limbs", "enclose_gemm_f64", "res_gemm_stage", "rg_workspace_bytes",
     "rg_workspace_layout", "rg_get_plan", "rg_status", "rg_prime", "rg_strerror", "rg_set_wait_limit_ns",
-    "rg_inject_fault", "res_gemm_i64_noalloc", "rg_noalloc_scratch_bytes",
+    "rg_inject_fault", "res_gemm_i64_noalloc", "rg_noalloc_scratch_bytes", "rg_set_gemm_variant",
 )
 
 
@@ -107,6 +107,8 @@ def library():
             lib.rg_set_wait_limit_ns.restype = ctypes.c_uint64
             lib.rg_inject_fault.argtypes = [ci]
             lib.rg_inject_fault.restype = None
+            lib.rg_set_gemm_variant.argtypes = [ci]
+            lib.rg_set_gemm_variant.restype = ci
             _lib = lib
     return _lib
 

@@ -26,6 +26,7 @@
 #include <cudaTypedefs.h>
 
 #include <cstdint>
+#include <atomic>
 #include <mutex>
 
 #include "rg_common.cuh"
@@ -448,6 +449,343 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
 }
 
 // ---------------------------------------------------------------------------
+// The CTA-pair kernel (tcgen05 cta_group::2)
+//
+// Two CTAs of a cluster share one 256 x 256 tile: each holds 128 rows of A and
+// 128 columns of B per stage (32 KB, six stages), the first CTA of the pair
+// issues M = 256, N = 256 MMAs that read both CTAs' shared memory, and each
+// CTA's tensor memory receives its own 128 rows of the accumulator.  Per
+// multiply-add the pair moves a third fewer operand bytes from L2 than two
+// single-CTA tiles, and the deeper pipeline hides more load latency.
+// Protocol: both CTAs' TMA loads complete on the first CTA's "full" barrier
+// (64 KB per stage); the first CTA's MMA commits multicast to both CTAs'
+// "empty" and "tfull" barriers; both epilogues arrive on the first CTA's
+// "tempty" barrier (8 warps).  The epilogue is the single-CTA one.
+// ---------------------------------------------------------------------------
+constexpr int STAGES2 = 6;
+constexpr int B2_BYTES = 128 * BK * 2;  // this CTA's 128 columns of B
+constexpr int STAGE2_BYTES = A_BYTES + B2_BYTES;
+constexpr int SMEM2_BYTES = 1024 + STAGES2 * STAGE2_BYTES + OUT_BYTES + BAR_BYTES;
+static_assert(SMEM2_BYTES <= 232448, "shared memory");
+// M = 256, N = 256, otherwise as IDESC.
+constexpr uint32_t IDESC2 = (1u << 4) | (0u << 7) | (0u << 10) | (0u << 15) | (1u << 16) | ((uint32_t)(256 >> 3) << 17) |
+                            ((uint32_t)(256 >> 4) << 24);
+
+__device__ __forceinline__ uint32_t cluster_rank() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+  return r;
+}
+// Address of the same shared variable in CTA `rank` of the cluster.
+__device__ __forceinline__ uint32_t mapa_shared(uint32_t addr, uint32_t rank) {
+  uint32_t r;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(addr), "r"(rank));
+  return r;
+}
+__device__ __forceinline__ bool mbar_try_wait_cluster(uint32_t bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n .reg .pred p;\n mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n selp.u32 %0, 1, 0, p;\n}\n"
+      : "=r"(ok)
+      : "r"(bar), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+__device__ __forceinline__ void mbar_arrive_cluster(uint32_t bar_cluster_addr) {
+  asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(bar_cluster_addr) : "memory");
+}
+__device__ __forceinline__ void cluster_sync() {
+  asm volatile("barrier.cluster.arrive.release.aligned;\nbarrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void tma_load_3d_pair(uint32_t dst, const CUtensorMap* map, uint32_t bar_cluster_addr,
+                                                 int c0, int c1, int c2) {
+  asm volatile(
+      "cp.async.bulk.tensor.3d.cta_group::2.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%3, "
+      "%4, %5}], [%2];" ::"r"(dst),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(bar_cluster_addr), "r"(c0), "r"(c1), "r"(c2)
+      : "memory");
+}
+__device__ __forceinline__ void umma_f16_pair(uint32_t d, uint64_t adesc, uint64_t bdesc, uint32_t idesc,
+                                              uint32_t acc) {
+  asm volatile(
+      "{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n tcgen05.mma.cta_group::2.kind::f16 [%0], %1, %2, %3, p;\n}\n" ::"r"(d),
+      "l"(adesc), "l"(bdesc), "r"(idesc), "r"(acc)
+      : "memory");
+}
+// Arrive on the barrier at this shared offset in both CTAs of the pair once
+// all earlier MMAs of this thread have completed.
+__device__ __forceinline__ void umma_commit_pair(uint32_t bar) {
+  asm volatile(
+      "tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64 [%0], %1;" ::"r"(bar),
+      "h"((uint16_t)3)
+      : "memory");
+}
+__device__ __forceinline__ void umma_commit_pair_local(uint32_t bar) {
+  asm volatile("tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar) : "memory");
+}
+
+// Bounded wait with cluster-scope acquire (barriers that receive arrivals from
+// the peer CTA or from its copies).
+__device__ bool wait_bounded_cluster(uint32_t bar, uint32_t parity, const Ctl& ctl, int where) {
+  if (mbar_try_wait_cluster(bar, parity)) return true;
+  const unsigned long long t0 = globaltimer();
+  for (uint32_t i = 1;; ++i) {
+    if (mbar_try_wait_cluster(bar, parity)) return true;
+    if ((i & 63u) == 0) {
+      if (*ctl.abort) return false;
+      if (globaltimer() - t0 > ctl.limit_ns) {
+        *ctl.abort = 1;
+        atomicCAS(ctl.status, 0, RG_ERR_TIMEOUT);
+        atomicCAS(ctl.where, 0, where);
+        return false;
+      }
+    }
+  }
+}
+
+__global__ void __launch_bounds__(NUM_THREADS, 1)
+    residue_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
+                             const __grid_constant__ CUtensorMap tmC, const __grid_constant__ GemmParams gp,
+                             DevPlan* plan) {
+  extern __shared__ uint8_t smem_raw[];
+  wait_for_predecessor();
+  if (plan->status) return;  // the same decision in both CTAs of the pair
+  const int P = gp.P_fixed ? gp.P_fixed : plan->P;
+  const int mt2 = (gp.M + 255) / 256;
+  const int total = P * mt2 * gp.nt;
+  const int nc_tile = (gp.kb_total + KC_BLOCKS - 1) / KC_BLOCKS;
+  const uint32_t rank = cluster_rank();
+  const int cid = blockIdx.x >> 1, ncl = gridDim.x >> 1;
+
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint8_t* stage_base = smem;
+  uint8_t* out_base = smem + STAGES2 * STAGE2_BYTES;
+  uint64_t* bars = reinterpret_cast<uint64_t*>(out_base + OUT_BYTES);
+  uint64_t* full = bars;
+  uint64_t* empty = bars + STAGES2;
+  uint64_t* tfull = bars + 2 * STAGES2;
+  uint64_t* tempty = bars + 2 * STAGES2 + 2;
+  uint64_t* drain = bars + 2 * STAGES2 + 4;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 2 * STAGES2 + 5);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+  volatile int* ep_flag = reinterpret_cast<volatile int*>(tmem_slot + 2);  // two ints
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  Ctl ctl{abort_flag, &plan->status, &plan->timeout_where, gp.wait_ns};
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < STAGES2; ++s) {
+      mbar_init(smem_u32(&full[s]), 1);
+      mbar_init(smem_u32(&empty[s]), 1);
+    }
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(smem_u32(&tfull[b]), 1);
+      mbar_init(smem_u32(&tempty[b]), 8);  // four epilogue warps in each CTA
+    }
+    mbar_init(smem_u32(drain), 1);
+    *abort_flag = 0;
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+  }
+  if (warp == 1) {  // one warp in each CTA allocates for the pair
+    asm volatile("tcgen05.alloc.cta_group::2.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(tmem_slot)),
+                 "r"((uint32_t)TMEM_COLS));
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::2.sync.aligned;");
+  }
+  tc_fence_before();
+  cluster_sync();  // barriers of both CTAs are initialised before any remote arrival
+  tc_fence_after();
+  const uint32_t tmem_base = *tmem_slot;
+
+  if (warp == 0) {
+    // ------------------------------------------------------------ producer (both CTAs)
+    if (lane == 0) {
+      int stage = 0;
+      uint32_t phase = 0;
+      bool ok = true;
+      for (int t = cid; t < total && ok; t += ncl) {
+        TileCoord tc = tile_coord(t, mt2, gp.nt);
+        for (int kb = 0; kb < gp.kb_total; ++kb) {
+          if (!wait_bounded_cluster(smem_u32(&empty[stage]), phase ^ 1u, ctl, 11)) {
+            ok = false;
+            break;
+          }
+          const uint32_t fb_local = smem_u32(&full[stage]);
+          if (rank == 0) mbar_arrive_expect_tx(fb_local, 2 * STAGE2_BYTES);
+          const uint32_t fb = mapa_shared(fb_local, 0);
+          const uint32_t a_dst = smem_u32(stage_base + stage * STAGE2_BYTES);
+          const uint32_t b_dst = a_dst + A_BYTES;
+          tma_load_3d_pair(a_dst, &tmA, fb, kb * BK, tc.m * 256 + (int)rank * 128, tc.p);
+#pragma unroll
+          for (int j = 0; j < 2; ++j)
+            tma_load_3d_pair(b_dst + j * B_SLAB, &tmB, fb, tc.n * BN + (int)rank * 128 + 64 * j, kb * BK, tc.p);
+          if (++stage == STAGES2) {
+            stage = 0;
+            phase ^= 1u;
+          }
+        }
+      }
+    }
+  } else if (warp == 1) {
+    // ------------------------------------------------------------ MMA issuer (first CTA)
+    if (lane == 0 && rank == 0) {
+      int stage = 0;
+      uint32_t phase = 0, acc_iter = 0;
+      bool ok = true, any = false;
+      for (int t = cid; t < total && ok; t += ncl) {
+        for (int c = 0; c < nc_tile && ok; ++c) {
+          const uint32_t b = acc_iter & 1u, aph = (acc_iter >> 1) & 1u;
+          if (!wait_bounded_cluster(smem_u32(&tempty[b]), aph ^ 1u, ctl, 12)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint32_t d = tmem_base + b * BN;
+          const int kb0 = c * KC_BLOCKS;
+          const int kb1 = min(kb0 + KC_BLOCKS, gp.kb_total);
+          for (int kb = kb0; kb < kb1; ++kb) {
+            if (!wait_bounded_cluster(smem_u32(&full[stage]), phase, ctl, 13)) {
+              ok = false;
+              break;
+            }
+            tc_fence_after();
+            const uint32_t a_addr = smem_u32(stage_base + stage * STAGE2_BYTES);
+            const uint64_t adesc = sw128_desc(a_addr, 16, 1024);
+            const uint64_t bdesc = sw128_desc(a_addr + A_BYTES, B_SLAB, 1024);
+#pragma unroll
+            for (int kk = 0; kk < BK / 16; ++kk) {
+              const uint32_t acc = (c >= 2 || kb > kb0 || kk > 0) ? 1u : 0u;
+              umma_f16_pair(d, adesc + (uint64_t)(2 * kk), bdesc + (uint64_t)(128 * kk), IDESC2, acc);
+            }
+            any = true;
+            umma_commit_pair(smem_u32(&empty[stage]));
+            if (++stage == STAGES2) {
+              stage = 0;
+              phase ^= 1u;
+            }
+          }
+          if (!ok) break;
+          if (!(gp.fault == 1 && acc_iter == 0)) umma_commit_pair(smem_u32(&tfull[b]));
+          ++acc_iter;
+        }
+      }
+      if (!ok && any) {  // all issued MMAs must finish before the memory is freed
+        Ctl drain_ctl = ctl;
+        volatile int never = 0;
+        drain_ctl.abort = &never;
+        umma_commit_pair_local(smem_u32(drain));
+        wait_bounded(smem_u32(drain), 0, drain_ctl, 0);
+      }
+    }
+  } else {
+    // ------------------------------------------------------------ epilogue (both CTAs)
+    const int q4 = warp & 3;
+    const int row = q4 * 32 + lane;
+    const int et = threadIdx.x - 64;
+    uint32_t acc_iter = 0;
+    bool ok = true;
+    const uint32_t out_s = smem_u32(out_base);
+    const uint32_t tempty_leader[2] = {mapa_shared(smem_u32(&tempty[0]), 0), mapa_shared(smem_u32(&tempty[1]), 0)};
+    for (int t = cid; t < total && ok; t += ncl) {
+      TileCoord tc = tile_coord(t, mt2, gp.nt);
+      const float q = gp.qf[tc.p], iq = gp.invq[tc.p];
+      const int row0 = tc.m * 256 + (int)rank * 128;
+      bool first_write = true;
+      for (int c = 0; c < nc_tile; ++c) {
+        const uint32_t b = acc_iter & 1u, aph = (acc_iter >> 1) & 1u;
+        if (et == 0) ep_flag[acc_iter & 1u] = wait_bounded_cluster(smem_u32(&tfull[b]), aph, ctl, 14) ? 1 : 0;
+        epilogue_bar();
+        if (!ep_flag[acc_iter & 1u]) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        const uint32_t taddr = tmem_base + ((uint32_t)(q4 * 32) << 16) + b * BN;
+        const int mode = (c + 2 < nc_tile) ? 0 : (c + 2 == nc_tile ? 1 : 2);  // partial, carry, final
+        if (mode != 0 && first_write) {
+          if (et == 0) bulk_wait_read0();
+          epilogue_bar();
+          first_write = false;
+        }
+#pragma unroll 1
+        for (int col = 0; col < BN; col += 32) {
+          uint32_t r[32];
+          tmem_ld32(taddr + col, r);
+          tmem_wait_ld();
+          if (mode == 0) {
+            const float magic = 12582912.0f;
+#pragma unroll
+            for (int i = 0; i < 32; ++i) {
+              const float x = __uint_as_float(r[i]);
+              const float tq = __fadd_rn(__fmaf_rn(x, iq, magic), -magic);
+              r[i] = __float_as_uint(__fmaf_rn(-tq, q, x));
+            }
+            tmem_st32(taddr + col, r);
+          } else {
+            const int half = col >> 7;
+            const int j0 = (col & 127) >> 4;
+            uint8_t* hbase = out_base + half * OUT_HALF;
+            uint4* p0 = reinterpret_cast<uint4*>(hbase + sw128_off(row, j0));
+            uint4* p1 = reinterpret_cast<uint4*>(hbase + sw128_off(row, j0 + 1));
+            uint32_t carry[8] = {0, 0, 0, 0, 0, 0, 0, 0};
+            if (mode == 2 && nc_tile >= 2) {
+              const uint4 c0 = *p0, c1 = *p1;
+              carry[0] = c0.x; carry[1] = c0.y; carry[2] = c0.z; carry[3] = c0.w;
+              carry[4] = c1.x; carry[5] = c1.y; carry[6] = c1.z; carry[7] = c1.w;
+            }
+            uint32_t packed[8];
+#pragma unroll
+            for (int w = 0; w < 8; ++w) {
+              uint32_t word = 0;
+#pragma unroll
+              for (int k = 0; k < 4; ++k) {
+                float v = pos_mod(__uint_as_float(r[4 * w + k]), q, iq);
+                v += (float)((carry[w] >> (8 * k)) & 0xFFu);
+                v = v >= q ? v - q : v;
+                word |= ((uint32_t)v) << (8 * k);
+              }
+              packed[w] = word;
+            }
+            *p0 = make_uint4(packed[0], packed[1], packed[2], packed[3]);
+            *p1 = make_uint4(packed[4], packed[5], packed[6], packed[7]);
+          }
+        }
+        if (mode == 0) tmem_wait_st();
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive_cluster(tempty_leader[b]);
+        if (mode == 2) {
+          fence_proxy_async_smem();
+          epilogue_bar();
+          if (et == 0 && row0 < gp.M) {
+            tma_store_3d(&tmC, out_s, tc.n * BN, row0, tc.p);
+            if (tc.n * BN + 128 < gp.N) tma_store_3d(&tmC, out_s + OUT_HALF, tc.n * BN + 128, row0, tc.p);
+            bulk_commit();
+          }
+        }
+        ++acc_iter;
+      }
+    }
+    if (et == 0) bulk_wait0();
+  }
+
+  if (*abort_flag) {
+    // an aborted role may leave copies in flight that signal either CTA:
+    // give them time to land before the pair leaves
+    const unsigned long long t0 = globaltimer();
+    while (globaltimer() - t0 < 200000ull) {
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  allow_dependents();
+  cluster_sync();  // neither CTA frees the pair's memory while the other still uses it
+  if (warp == 1) {
+    tc_fence_after();
+    asm volatile("tcgen05.dealloc.cta_group::2.sync.aligned.b32 %0, %1;" ::"r"(tmem_base), "r"((uint32_t)TMEM_COLS));
+  }
+}
+
+// ---------------------------------------------------------------------------
 // Host side
 // ---------------------------------------------------------------------------
 PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
@@ -479,6 +817,7 @@ bool make_map_3d(CUtensorMap* m, CUtensorMapDataType dt, int esize, const void* 
 }
 
 int g_gemm_ready[64];
+std::atomic<int> g_gemm_variant{0};  // 0 automatic, 1 single-CTA, 2 CTA pair
 
 }  // namespace
 
@@ -493,9 +832,14 @@ cudaError_t launch_gemm(const void* RA, long long lda, const void* RB, long long
   if (!g_gemm_ready[dev]) {
     e = cudaFuncSetAttribute(residue_gemm_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
     if (e != cudaSuccess) return e;
+    e = cudaFuncSetAttribute(residue_gemm_pair_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM2_BYTES);
+    if (e != cudaSuccess) return e;
     cudaDeviceGetAttribute(&sms[dev], cudaDevAttrMultiProcessorCount, dev);
     g_gemm_ready[dev] = 1;
   }
+  // the pair kernel loads A in 128-row halves of a 256-row tile
+  const int variant = g_gemm_variant.load();
+  const bool pair = variant == 2 || (variant == 0 && M > BM);
   CUtensorMap ma, mb, mc;
   if (!make_map_3d(&ma, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, RA, (uint64_t)K, (uint64_t)M, (uint64_t)pmax,
                    (uint64_t)lda * 2, (uint64_t)M * lda * 2, BK, BM) ||
@@ -519,10 +863,45 @@ cudaError_t launch_gemm(const void* RA, long long lda, const void* RB, long long
     gp.qf[i] = t.qf[i];
     gp.invq[i] = t.invq[i];
   }
-  long long tiles = (long long)pmax * gp.mt * gp.nt;
-  int grid = (int)(tiles < sms[dev] ? tiles : sms[dev]);
-  if (grid < 1) grid = 1;
-  return launch_dependent(residue_gemm_kernel, dim3(grid), dim3(NUM_THREADS), SMEM_BYTES, st, ma, mb, mc, gp, plan);
+  if (!pair) {
+    const long long tiles = (long long)pmax * gp.mt * gp.nt;
+    int grid = (int)(tiles < sms[dev] ? tiles : sms[dev]);
+    if (grid < 1) grid = 1;
+    return launch_dependent(residue_gemm_kernel, dim3(grid), dim3(NUM_THREADS), SMEM_BYTES, st, ma, mb, mc, gp, plan);
+  }
+  cudaLaunchConfig_t cfg = {};
+  cfg.blockDim = dim3(NUM_THREADS);
+  cfg.dynamicSmemBytes = SMEM2_BYTES;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[2];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = 2;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[1].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 2;
+  // persistent: as many pairs as can be resident at once (not every SM can
+  // be paired within its GPC), never more than there are tiles
+  static int max_pairs[64];
+  if (!max_pairs[dev]) {
+    int n = 0;
+    cfg.gridDim = dim3((unsigned)(sms[dev] & ~1));
+    if (cudaOccupancyMaxActiveClusters(&n, residue_gemm_pair_kernel, &cfg) != cudaSuccess || n < 1) n = sms[dev] / 2;
+    max_pairs[dev] = n;
+  }
+  const long long tiles2 = (long long)pmax * ((M + 255) / 256) * gp.nt;
+  long long clusters = max_pairs[dev];
+  if (tiles2 < clusters) clusters = tiles2;
+  if (clusters < 1) clusters = 1;
+  cfg.gridDim = dim3((unsigned)(2 * clusters));
+  return cudaLaunchKernelEx(&cfg, residue_gemm_pair_kernel, ma, mb, mc, gp, plan);
 }
 
 }  // namespace rg
+
+extern "C" int rg_set_gemm_variant(int variant) {
+  if (variant < 0 || variant > 2) return -1;
+  return rg::g_gemm_variant.exchange(variant);
+}

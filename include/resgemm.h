@@ -228,6 +228,12 @@ const char* rg_strerror(int code);
 uint64_t rg_set_wait_limit_ns(uint64_t ns);
 void rg_inject_fault(int kind);
 
+/* Test hook: which tensor-core kernel runs the per-prime stage.  0 = choose
+ * by shape (the CTA-pair kernel when M > 128), 1 = single-CTA kernel,
+ * 2 = CTA-pair kernel.  Returns the previous choice, or -1 for an invalid
+ * value.  Not thread-safe; for tests and measurements only. */
+int rg_set_gemm_variant(int variant);
+
 #ifdef __cplusplus
 }
 #endif

@@ -15,6 +15,15 @@ from tests.gpu_util import host, rg  # noqa: F401
 pytestmark = pytest.mark.gpu
 
 
+@pytest.fixture(params=[1, 2], ids=["single_cta", "cta_pair"])
+def variant(rg, request):
+    """Runs the test on the single-CTA and on the CTA-pair tensor-core kernel."""
+    lib = rg.library()
+    old = lib.rg_set_gemm_variant(request.param)
+    yield request.param
+    lib.rg_set_gemm_variant(old)
+
+
 def expected(ra, rb, ps):
     out = []
     for p, q in enumerate(ps):
@@ -52,7 +61,7 @@ def patterns(kind, P, M, N, K, rng):
 
 
 @pytest.mark.parametrize("kind", ["all_plus", "all_minus_plus", "signs", "random_extreme", "random"])
-def test_long_k_adversarial(rg, kind):
+def test_long_k_adversarial(rg, variant, kind):
     P, M, N, K = 3, 130, 260, 2**17
     rng = np.random.default_rng(1)
     ra, rb = patterns(kind, P, M, N, K, rng)
@@ -61,7 +70,7 @@ def test_long_k_adversarial(rg, kind):
 
 
 @pytest.mark.parametrize("K", [1, 16, 63, 64, 1000, 1024, 1025, 2048, 3000, 5000])
-def test_k_tails_all_primes(rg, K):
+def test_k_tails_all_primes(rg, variant, K):
     P, M, N = 53, 129, 257
     rng = np.random.default_rng(K)
     ra, rb = patterns("random_extreme", P, M, N, K, rng)
@@ -69,10 +78,10 @@ def test_k_tails_all_primes(rg, K):
     assert np.array_equal(got, expected(ra, rb, rg.primes()))
 
 
-def test_wait_expiry_returns_timeout(rg):
+def test_wait_expiry_returns_timeout(rg, variant):
     """A wait that can never complete expires, reports RG_ERR_TIMEOUT, and the context stays usable."""
     lib = rg.library()
-    P, M, N, K = 2, 128, 256, 4096
+    P, M, N, K = 2, 256, 256, 4096
     rng = np.random.default_rng(2)
     ra, rb = patterns("random", P, M, N, K, rng)
     old = lib.rg_set_wait_limit_ns(50_000_000)  # 50 ms
