@@ -200,16 +200,22 @@ def run_reference(args):
 
 
 def gemm_traffic_record(path_src):
-    """Per-launch DRAM bytes of the GEMM kernel from the committed ncu summary,
-    if it was taken on the current kernel source; else None."""
-    rec_path = os.path.join(ROOT, "profiles", "residue_gemm_traffic.json")
+    """Per-launch DRAM bytes of the GEMM kernel from the committed ncu summary
+    (profiles/residue_gemm_traffic.txt), if it was taken on the current kernel
+    source; else None."""
+    rec_path = os.path.join(ROOT, "profiles", "residue_gemm_traffic.txt")
     try:
+        rec = {}
         with open(rec_path) as f:
-            rec = json.load(f)
+            for line in f:
+                line = line.strip()
+                if line and not line.startswith("#") and "=" in line:
+                    k, v = line.split("=", 1)
+                    rec[k.strip()] = v.strip()
         with open(path_src, "rb") as f:
             sha = hashlib.sha256(f.read()).hexdigest()
         return rec if rec.get("source_sha256") == sha else None
-    except (OSError, ValueError):
+    except OSError:
         return None
 
 
@@ -321,9 +327,11 @@ def main():
     traffic = gemm_traffic_record(os.path.join(ROOT, "exact_modular_int8_gb300", "csrc", "gemm_tc.cu"))
     traffic_bytes = None
     if traffic and traffic.get("workload") == w.name:
-        traffic_bytes = traffic.get("traffic_bytes_per_launch")
+        traffic_bytes = int(traffic["traffic_bytes_per_launch"])
+    kernel = ("residue_gemm_pair_kernel (tcgen05.mma cta_group::2 kind::f16, fp32 TMEM)" if w.M > 128 else
+              "residue_gemm_kernel (tcgen05.mma cta_group::1 kind::f16, fp32 TMEM)")
     roofline = {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s", "frac": achieved / peak,
-                "traffic": traffic_bytes, "kernel": "residue_gemm_kernel (tcgen05.mma kind::f16, fp32 TMEM)",
+                "traffic": traffic_bytes, "kernel": kernel,
                 "peak_source": f"{peak_src} bf16 dense burst (MEASURED_PEAKS.json); fp16 nominal rate equals bf16",
                 "algorithmic_flops_per_launch": gemm_flops, "avg_launch_ms": gemm_ms, "primes": P}
 
