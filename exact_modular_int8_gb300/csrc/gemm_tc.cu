@@ -9,11 +9,12 @@
 // fp32 in tensor memory.  Every product is an integer below 2^14 in magnitude;
 // a chunk of Kc = 1024 products therefore sums to less than 1024 * 15625 <
 // 2^24 and stays an exact fp32 integer.  After each chunk the accumulator is
-// reduced modulo q in place (|remainder| <= 1.5 q), so the next chunk adds
+// reduced modulo q in place (|remainder| <= 2.2 q), so the next chunk adds
 // onto a small value and never reaches 2^24.  Two accumulators alternate
 // chunks, so the reduction of one overlaps the products of the other; the
 // last two chunks of a tile are reduced to [0, q), summed, and written as
-// uint8 residues through shared memory and a TMA store.
+// uint8 residues through shared memory and a TMA store.  (The in-place
+// remainder is at most 2.2 q, so a chunk ends below 1024 * 125^2 + 553 < 2^24.)
 //
 // Warp roles (one CTA per SM, persistent over tiles of (prime, m, n)):
 //   warp 0      TMA producer: A tile 128x64 (K-major) and B tile 64x256
@@ -187,6 +188,46 @@ __device__ __forceinline__ void tmem_st32(uint32_t taddr, const uint32_t (&r)[32
 }
 __device__ __forceinline__ void tmem_wait_ld() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
 __device__ __forceinline__ void tmem_wait_st() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
+
+// x - q * t with t an integer within 1.7 of x/q, for any |x| < 2^24: y + 2^24
+// rounds to an integer (spacing 1 or 2) for |y| <= 2^23.  The result is an
+// integer with |r| <= 2.2 q, small enough to carry into the next chunk
+// (1024 * 125^2 + 2.2 * 251 < 2^24).
+__device__ __forceinline__ float partial_residue(float x, float q, float iq) {
+  const float two24 = 16777216.0f;
+  const float t = __fadd_rn(__fmaf_rn(x, iq, two24), -two24);
+  return __fmaf_rn(-t, q, x);
+}
+
+// Final residues of 32 accumulator values (|x| < 2^24) plus an optional byte
+// carry, packed four per word, using only FMA-pipe and byte-permute
+// instructions.  The first reduction leaves |r| <= 2.2 q; the second is exact
+// (|r| < 2^23, see the split kernel's reduction), giving the balanced residue,
+// moved to [0, q).  Bytes enter and leave the float domain through
+// the low mantissa bits of 2^23.
+__device__ __forceinline__ void final_residues(const uint32_t (&r)[32], const uint32_t (&carry)[8], bool add_carry,
+                                               float q, float iq, uint32_t (&packed)[8]) {
+  const float magic = 12582912.0f, two23 = 8388608.0f;
+#pragma unroll
+  for (int w = 0; w < 8; ++w) {
+    uint32_t b[4];
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+      float v = partial_residue(__uint_as_float(r[4 * w + k]), q, iq);
+      const float t = __fadd_rn(__fmaf_rn(v, iq, magic), -magic);
+      v = __fmaf_rn(-t, q, v);
+      v = v < 0.0f ? v + q : v;
+      if (add_carry) {
+        // 0x4B0000cc is the float 2^23 + c for the carry byte c
+        const float c = __uint_as_float(__byte_perm(carry[w], 0x4B000000u, 0x7540u + (uint32_t)k)) - two23;
+        v = v + c;
+        v = v >= q ? v - q : v;
+      }
+      b[k] = __float_as_uint(v + two23);  // low byte = v
+    }
+    packed[w] = __byte_perm(__byte_perm(b[0], b[1], 0x0040u), __byte_perm(b[2], b[3], 0x0040u), 0x5410u);
+  }
+}
 
 // Byte offset of (row, 16-byte chunk j) in a 128-row x 128-byte swizzled half.
 __device__ __forceinline__ uint32_t sw128_off(int row, int j) { return (uint32_t)(row * 128 + ((j ^ (row & 7)) << 4)); }
@@ -383,13 +424,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
           tmem_ld32(taddr + col, r);
           tmem_wait_ld();
           if (mode == 0) {
-            const float magic = 12582912.0f;
 #pragma unroll
-            for (int i = 0; i < 32; ++i) {
-              float x = __uint_as_float(r[i]);
-              float tq = __fadd_rn(__fmaf_rn(x, iq, magic), -magic);
-              r[i] = __float_as_uint(__fmaf_rn(-tq, q, x));
-            }
+            for (int i = 0; i < 32; ++i) r[i] = __float_as_uint(partial_residue(__uint_as_float(r[i]), q, iq));
             tmem_st32(taddr + col, r);
           } else {
             const int half = col >> 7;
@@ -404,18 +440,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
               carry[4] = c1.x; carry[5] = c1.y; carry[6] = c1.z; carry[7] = c1.w;
             }
             uint32_t packed[8];
-#pragma unroll
-            for (int w = 0; w < 8; ++w) {
-              uint32_t word = 0;
-#pragma unroll
-              for (int k = 0; k < 4; ++k) {
-                float v = pos_mod(__uint_as_float(r[4 * w + k]), q, iq);
-                v += (float)((carry[w] >> (8 * k)) & 0xFFu);
-                v = v >= q ? v - q : v;
-                word |= ((uint32_t)v) << (8 * k);
-              }
-              packed[w] = word;
-            }
+            final_residues(r, carry, mode == 2 && nc_tile >= 2, q, iq, packed);
             *p0 = make_uint4(packed[0], packed[1], packed[2], packed[3]);
             *p1 = make_uint4(packed[4], packed[5], packed[6], packed[7]);
           }
@@ -712,13 +737,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
           tmem_ld32(taddr + col, r);
           tmem_wait_ld();
           if (mode == 0) {
-            const float magic = 12582912.0f;
 #pragma unroll
-            for (int i = 0; i < 32; ++i) {
-              const float x = __uint_as_float(r[i]);
-              const float tq = __fadd_rn(__fmaf_rn(x, iq, magic), -magic);
-              r[i] = __float_as_uint(__fmaf_rn(-tq, q, x));
-            }
+            for (int i = 0; i < 32; ++i) r[i] = __float_as_uint(partial_residue(__uint_as_float(r[i]), q, iq));
             tmem_st32(taddr + col, r);
           } else {
             const int half = col >> 7;
@@ -733,18 +753,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
               carry[4] = c1.x; carry[5] = c1.y; carry[6] = c1.z; carry[7] = c1.w;
             }
             uint32_t packed[8];
-#pragma unroll
-            for (int w = 0; w < 8; ++w) {
-              uint32_t word = 0;
-#pragma unroll
-              for (int k = 0; k < 4; ++k) {
-                float v = pos_mod(__uint_as_float(r[4 * w + k]), q, iq);
-                v += (float)((carry[w] >> (8 * k)) & 0xFFu);
-                v = v >= q ? v - q : v;
-                word |= ((uint32_t)v) << (8 * k);
-              }
-              packed[w] = word;
-            }
+            final_residues(r, carry, mode == 2 && nc_tile >= 2, q, iq, packed);
             *p0 = make_uint4(packed[0], packed[1], packed[2], packed[3]);
             *p1 = make_uint4(packed[4], packed[5], packed[6], packed[7]);
           }

@@ -112,10 +112,11 @@ __device__ LocalPlan finalize_plan(DevPlan* plan, const PlanArgs& a) {
       // entries with |x| <= 2^23 are exact fp32 values: no chunks (nchunk 0)
       p.nchunk_a = ma <= (1ull << 23) ? 0 : (p.bits_a + 1 + kChunkBits - 1) / kChunkBits;
       p.nchunk_b = mb <= (1ull << 23) ? 0 : (p.bits_b + 1 + kChunkBits - 1) / kChunkBits;
-      // exact range check: K * max|A| * max|B| <= 2^63 - 1
-      const unsigned __int128 prod = (unsigned __int128)ma * mb;
-      const unsigned __int128 lim = (unsigned __int128)0x7FFFFFFFFFFFFFFFull / (unsigned long long)a.K;
-      if (prod > lim) p.status = RG_ERR_RANGE;
+      // exact range check: K * max|A| * max|B| <= 2^63 - 1, with 64x64 -> 128
+      // products only
+      const unsigned long long ab_hi = __umul64hi(ma, mb), ab = ma * mb;
+      const unsigned long long k = (unsigned long long)a.K;
+      if (ab_hi != 0 || __umul64hi(ab, k) != 0 || ab * k > 0x7FFFFFFFFFFFFFFFull) p.status = RG_ERR_RANGE;
     }
   } else if (a.op == RG_OP_LIMBS) {
     p.bits_a = __ldcg(&plan->maxbits_a);
@@ -819,7 +820,7 @@ cudaError_t upload_tables() {
 
 static int planner_blocks(long long n) {
   long long b = (n + 256LL * 8 - 1) / (256LL * 8);
-  long long cap = 4LL * sm_count();
+  long long cap = sm_count();  // few blocks: each one ends with atomics on the plan block
   return (int)(b < 1 ? 1 : (b > cap ? cap : b));
 }
 

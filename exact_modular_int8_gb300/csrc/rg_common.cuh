@@ -91,15 +91,6 @@ __device__ __forceinline__ float bal_mod_small(float s, float q, float invq) {
   return __fmaf_rn(-t, q, s);
 }
 
-// Residue in [0, q) of an integer-valued float s, |s| < 2^24.
-__device__ __forceinline__ float pos_mod(float s, float q, float invq) {
-  float t = floorf(s * invq);
-  float r = __fmaf_rn(-t, q, s);
-  r = r < 0.0f ? r + q : r;
-  r = r >= q ? r - q : r;
-  return r;
-}
-
 __device__ __forceinline__ void set_status(int* status, int code) { atomicCAS(status, 0, code); }
 
 // Programmatic dependent launch: a kernel launched with programmatic stream

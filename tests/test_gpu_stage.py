@@ -69,6 +69,20 @@ def test_long_k_adversarial(rg, variant, kind):
     assert np.array_equal(got, expected(ra, rb, rg.primes()[:P]))
 
 
+def test_long_k_unreduced_residues_all_primes(rg, variant):
+    """Residues of +-125 for every prime, the smallest (q = 3) included: each
+    chunk of 1024 products reaches +-1.6e7, the largest sums the accumulator
+    sees, and their quotients by 3 are the largest the reductions see."""
+    P, M, N, K = 53, 40, 70, 2**17
+    ra = np.full((P, M, K), -125, dtype=np.int8)
+    ra[:, 1::2, :] = 125
+    rb = np.full((P, K, N), 125, dtype=np.int8)
+    rb[:, :, 2::3] = -125
+    rb[:, K // 2:, 1::2] = 123
+    got = run_stage(rg, ra, rb, M, N, K)
+    assert np.array_equal(got, expected(ra, rb, rg.primes()))
+
+
 @pytest.mark.parametrize("K", [1, 16, 63, 64, 1000, 1024, 1025, 2048, 3000, 5000])
 def test_k_tails_all_primes(rg, variant, K):
     P, M, N = 53, 129, 257
