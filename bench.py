@@ -219,6 +219,51 @@ def gemm_traffic_record(path_src):
         return None
 
 
+# ---------------------------------------------------------------------------
+# ranks: one process per GPU; bookkeeping only (the data path has no collective)
+# ---------------------------------------------------------------------------
+
+
+def rank_info():
+    """(world, rank, local_rank) from the torch.distributed.run environment."""
+    return (int(os.environ.get("WORLD_SIZE", "1")), int(os.environ.get("RANK", "0")),
+            int(os.environ.get("LOCAL_RANK", "0")))
+
+
+def init_ranks(world):
+    """A gloo group for the barrier and the timing reduction (host tensors only)."""
+    if world > 1:
+        import torch.distributed as dist
+
+        dist.init_process_group("gloo")
+
+
+def barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+
+        dist.barrier()
+
+
+def max_over_ranks(x: float, world: int) -> float:
+    """The slowest rank's value: the whole job ends when its last rank ends."""
+    if world == 1:
+        return x
+    import torch
+    import torch.distributed as dist
+
+    t = torch.tensor([x], dtype=torch.float64)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_throughput(total_ms_max: float, steps: int, macs: int, world: int):
+    """(value in TOPS, ms per step): every rank processed `steps` problems of
+    `macs` multiply-adds (weak scaling); the job took the slowest rank's time."""
+    value = world * steps * 2.0 * macs / (total_ms_max * 1e-3) / 1e12
+    return value, total_ms_max / steps
+
+
 def main():
     args = parse_args()
     if args.impl == "reference":
@@ -227,13 +272,8 @@ def main():
     import numpy as np
     import torch
 
-    world = int(os.environ.get("WORLD_SIZE", "1"))
-    rank = int(os.environ.get("RANK", "0"))
-    local = int(os.environ.get("LOCAL_RANK", "0"))
-    if world > 1:
-        import torch.distributed as dist
-
-        dist.init_process_group("gloo")
+    world, rank, local = rank_info()
+    init_ranks(world)
     torch.cuda.set_device(local)
     dev = torch.device("cuda", local)
 
@@ -266,8 +306,7 @@ def main():
 
     clocks = ClockSampler(local)
     clocks.start()
-    if world > 1:
-        torch.distributed.barrier()
+    barrier(world)
     torch.cuda.synchronize(dev)
     times = []
     for _ in range(args.steps):
@@ -279,8 +318,7 @@ def main():
         e1.record(stream)
         times.append((e0, e1))
     torch.cuda.synchronize(dev)
-    if world > 1:
-        torch.distributed.barrier()
+    barrier(world)
     clock_info = clocks.stop()
     step_ms = [a.elapsed_time(b) for a, b in times]
     total_ms = sum(step_ms)
@@ -289,12 +327,8 @@ def main():
     same = all(torch.equal(x, y) for x, y in zip(out, ref_out)) if isinstance(out, tuple) else torch.equal(out, ref_out)
     if not same:
         raise SystemExit("timed results differ from the warm-up result")
-    if world > 1:
-        t = torch.tensor([total_ms], dtype=torch.float64)
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        total_ms = float(t.item())
-    ms_per_step = total_ms / args.steps
-    value = world * args.steps * 2.0 * w.macs / (total_ms * 1e-3) / 1e12
+    total_ms = max_over_ranks(total_ms, world)
+    value, ms_per_step = job_throughput(total_ms, args.steps, w.macs, world)
 
     # ---- dominant kernel: the per-prime tensor-core GEMM, timed alone on the
     # residue planes the last call left in the workspace (same launch shape)
