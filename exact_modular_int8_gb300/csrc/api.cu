@@ -155,11 +155,15 @@ int run(int op, const void* A, int la, const void* B, int lb, void* C, void* C2,
   }
   RG_TRY(cudaMemsetAsync(plan, 0, sizeof(DevPlan), s));
   const int la1 = op == RG_OP_LIMBS ? la : 1, lb1 = op == RG_OP_LIMBS ? lb : 1, lc1 = op == RG_OP_LIMBS ? lc : 1;
-  RG_TRY(launch_plan(op, dA, M * K, la1, dB, K * N, lb1, lc1, K, op == RG_OP_ENCLOSE ? 0 : nprimes, plan, s));
-  RG_TRY(launch_split(op, dA, dB, la1, lb1, M, N, K, L.lda, L.ldb, w + L.ra, w + L.rb, plan, s));
+  // int64: the split reduces max |A|, max |B| itself and the GEMM derives the
+  // plan; the other operations run the planner kernel first
+  const bool i64 = op == RG_OP_I64;
+  if (!i64)
+    RG_TRY(launch_plan(op, dA, M * K, la1, dB, K * N, lb1, lc1, K, op == RG_OP_ENCLOSE ? 0 : nprimes, plan, s));
+  RG_TRY(launch_split(op, dA, dB, la1, lb1, M, N, K, L.lda, L.ldb, w + L.ra, w + L.rb, plan, L.pmax, s));
   int fault = g_fault.exchange(0);
-  RG_TRY(launch_gemm(w + L.ra, L.lda, w + L.rb, L.ldb, w + L.rc, L.ldc, L.pmax, 0, M, N, K, plan, s, fault,
-                     g_wait_ns.load()));
+  RG_TRY(launch_gemm(w + L.ra, L.lda, w + L.rb, L.ldb, w + L.rc, L.ldc, L.pmax, i64 ? nprimes : 0, M, N, K, plan, s,
+                     fault, g_wait_ns.load(), i64));
   RG_TRY(launch_garner(op, w + L.rc, L.ldc, (long long)M * L.ldc, M, N, op == RG_OP_LIMBS ? lc : 1, plan, dC, dC2, s));
   if (flags & RG_FLAG_HOST) {
     RG_TRY(cudaMemcpyAsync(C, dC, (size_t)M * N * ec, cudaMemcpyDeviceToHost, s));
@@ -202,7 +206,7 @@ int res_gemm_stage(const uint16_t* RA, int64_t lda, const uint16_t* RB, int64_t 
   DevPlan* plan = static_cast<DevPlan*>(ws);
   RG_TRY(cudaMemsetAsync(plan, 0, sizeof(DevPlan), s));
   int fault = g_fault.exchange(0);
-  RG_TRY(launch_gemm(RA, lda, RB, ldb, RC, ldc, nprimes, nprimes, M, N, K, plan, s, fault, g_wait_ns.load()));
+  RG_TRY(launch_gemm(RA, lda, RB, ldb, RC, ldc, nprimes, nprimes, M, N, K, plan, s, fault, g_wait_ns.load(), false));
   return finish(ws, s, flags);
 }
 

@@ -20,7 +20,10 @@
 //   warp 0      TMA producer: A tile 128x64 (K-major) and B tile 64x256
 //               (N-major) per pipeline stage, 128-byte swizzle.
 //   warp 1      owns the tensor memory and issues the MMAs (one thread).
-//   warps 2..5  epilogue: tcgen05.ld, reduction mod q, tcgen05.st / output.
+//   warps 2..9  epilogue, two warpgroups of four (each warp may only reach
+//               the tensor-memory lanes of its warp index mod 4; each
+//               warpgroup drains 128 of the 256 columns): tcgen05.ld,
+//               reduction mod q, tcgen05.st / output.
 // Every wait is bounded; on expiry the kernel records RG_ERR_TIMEOUT, lets
 // in-flight copies and MMAs finish, frees its tensor memory and returns.
 #include <cuda.h>
@@ -48,7 +51,8 @@ constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
 constexpr int OUT_HALF = 128 * 128;  // uint8 staging: two 128x128 halves
 constexpr int OUT_BYTES = 2 * OUT_HALF;
 constexpr int TMEM_COLS = 2 * BN;
-constexpr int NUM_THREADS = 192;
+constexpr int EPI_WARPS = 8;  // two warpgroups, each draining 128 of the 256 columns
+constexpr int NUM_THREADS = 64 + 32 * EPI_WARPS;
 constexpr int BAR_BYTES = 256;
 constexpr int SMEM_BYTES = 1024 + STAGES * STAGE_BYTES + OUT_BYTES + BAR_BYTES;
 static_assert(SMEM_BYTES <= 232448, "shared memory");
@@ -62,12 +66,47 @@ struct GemmParams {
   int M, N, K;
   int mt, nt;
   int kb_total;
-  int P_fixed;  // 0: read the prime count from the plan
+  int P_fixed;     // 0: read (or derive) the prime count from the plan
+  int derive_i64;  // derive the int64 plan from max |A|, max |B|
+  int ceil_log2_k;
   int fault;
   unsigned long long wait_ns;
   float qf[kNumPrimes];
   float invq[kNumPrimes];
+  int log2P[kNumPrimes + 1];  // floor(log2(q_0 ... q_{n-1}))
 };
+
+// The prime count of this launch, or 0 if the call has already failed.  For
+// the int64 path without a planner pass every CTA derives the same plan from
+// the split's reductions (fewest primes with product > 2^(T+1),
+// T = bits(max|A|) + bits(max|B|) + ceil(log2 K), and the exact check
+// K * max|A| * max|B| <= 2^63 - 1); CTA 0 records it for the Garner kernel.
+__device__ int launch_primes(const GemmParams& gp, DevPlan* plan) {
+  if (!gp.derive_i64) {
+    if (plan->status) return 0;
+    return gp.P_fixed ? gp.P_fixed : plan->P;
+  }
+  const unsigned long long ma = __ldcg(&plan->maxmag_a), mb = __ldcg(&plan->maxmag_b);
+  const int bits_a = ma ? 64 - __clzll(ma) : 0, bits_b = mb ? 64 - __clzll(mb) : 0;
+  const int T = bits_a + bits_b + gp.ceil_log2_k;
+  int P = gp.P_fixed;
+  bool range = false;
+  if (!P) {
+    const unsigned long long k = (unsigned long long)gp.K, ab = ma * mb;
+    range = __umul64hi(ma, mb) != 0 || __umul64hi(ab, k) != 0 || ab * k > 0x7FFFFFFFFFFFFFFFull;
+    for (int n = 1; n <= kNumPrimes && !P; ++n)
+      if (gp.log2P[n] >= T + 1) P = n;
+    if (!P) range = true;
+  }
+  if (blockIdx.x == 0 && threadIdx.x == 0) {
+    plan->P = range ? 0 : P;
+    plan->bits_a = bits_a;
+    plan->bits_b = bits_b;
+    plan->bound_bits = T;
+    if (range) atomicCAS(&plan->status, 0, RG_ERR_RANGE);
+  }
+  return range ? 0 : P;
+}
 
 // ---------------------------------------------------------------------------
 // PTX wrappers
@@ -144,7 +183,7 @@ __device__ __forceinline__ void bulk_wait0() { asm volatile("cp.async.bulk.wait_
 __device__ __forceinline__ void fence_proxy_async_smem() {
   asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
 }
-__device__ __forceinline__ void epilogue_bar() { asm volatile("bar.sync 1, 128;" ::: "memory"); }
+__device__ __forceinline__ void epilogue_bar() { asm volatile("bar.sync 1, 256;" ::: "memory"); }
 
 __device__ __forceinline__ void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
 __device__ __forceinline__ void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
@@ -254,8 +293,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                         DevPlan* plan) {
   extern __shared__ uint8_t smem_raw[];
   wait_for_predecessor();
-  if (plan->status) return;
-  const int P = gp.P_fixed ? gp.P_fixed : plan->P;
+  const int P = launch_primes(gp, plan);
+  if (P == 0) return;
   const int total = P * gp.mt * gp.nt;
   const int nc_tile = (gp.kb_total + KC_BLOCKS - 1) / KC_BLOCKS;
 
@@ -282,7 +321,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     }
     for (int b = 0; b < 2; ++b) {
       mbar_init(smem_u32(&tfull[b]), 1);
-      mbar_init(smem_u32(&tempty[b]), 4);
+      mbar_init(smem_u32(&tempty[b]), EPI_WARPS);
     }
     mbar_init(smem_u32(drain), 1);
     *abort_flag = 0;
@@ -391,7 +430,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     // ------------------------------------------------------------ epilogue
     const int q4 = warp & 3;  // tensor-memory lane quarter this warp may access
     const int row = q4 * 32 + lane;
-    const int et = threadIdx.x - 64;  // 0..127
+    const int et = threadIdx.x - 64;  // 0..255
+    const int col_begin = (et >> 7) * (BN / 2);  // this warpgroup's half of the columns
     uint32_t acc_iter = 0;
     bool ok = true;
     const uint32_t out_s = smem_u32(out_base);
@@ -419,7 +459,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
           first_write = false;
         }
 #pragma unroll 1
-        for (int col = 0; col < BN; col += 32) {
+        for (int col = col_begin; col < col_begin + BN / 2; col += 32) {
           uint32_t r[32];
           tmem_ld32(taddr + col, r);
           tmem_wait_ld();
@@ -574,8 +614,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                              DevPlan* plan) {
   extern __shared__ uint8_t smem_raw[];
   wait_for_predecessor();
-  if (plan->status) return;  // the same decision in both CTAs of the pair
-  const int P = gp.P_fixed ? gp.P_fixed : plan->P;
+  const int P = launch_primes(gp, plan);  // the same decision in both CTAs of the pair
+  if (P == 0) return;
   const int mt2 = (gp.M + 255) / 256;
   const int total = P * mt2 * gp.nt;
   const int nc_tile = (gp.kb_total + KC_BLOCKS - 1) / KC_BLOCKS;
@@ -605,7 +645,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     }
     for (int b = 0; b < 2; ++b) {
       mbar_init(smem_u32(&tfull[b]), 1);
-      mbar_init(smem_u32(&tempty[b]), 8);  // four epilogue warps in each CTA
+      mbar_init(smem_u32(&tempty[b]), 2 * EPI_WARPS);  // the epilogue warps of both CTAs
     }
     mbar_init(smem_u32(drain), 1);
     *abort_flag = 0;
@@ -705,7 +745,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     // ------------------------------------------------------------ epilogue (both CTAs)
     const int q4 = warp & 3;
     const int row = q4 * 32 + lane;
-    const int et = threadIdx.x - 64;
+    const int et = threadIdx.x - 64;  // 0..255
+    const int col_begin = (et >> 7) * (BN / 2);  // this warpgroup's half of the columns
     uint32_t acc_iter = 0;
     bool ok = true;
     const uint32_t out_s = smem_u32(out_base);
@@ -732,7 +773,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
           first_write = false;
         }
 #pragma unroll 1
-        for (int col = 0; col < BN; col += 32) {
+        for (int col = col_begin; col < col_begin + BN / 2; col += 32) {
           uint32_t r[32];
           tmem_ld32(taddr + col, r);
           tmem_wait_ld();
@@ -832,7 +873,7 @@ std::atomic<int> g_gemm_variant{0};  // 0 automatic, 1 single-CTA, 2 CTA pair
 
 cudaError_t launch_gemm(const void* RA, long long lda, const void* RB, long long ldb, void* RC, long long ldc,
                         int pmax, int P_fixed, long long M, long long N, long long K, DevPlan* plan, cudaStream_t st,
-                        int fault, unsigned long long wait_ns) {
+                        int fault, unsigned long long wait_ns, bool derive_i64) {
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
@@ -865,6 +906,9 @@ cudaError_t launch_gemm(const void* RA, long long lda, const void* RB, long long
   gp.nt = (int)((N + BN - 1) / BN);
   gp.kb_total = (int)((K + BK - 1) / BK);
   gp.P_fixed = P_fixed;
+  gp.derive_i64 = derive_i64 ? 1 : 0;
+  gp.ceil_log2_k = 0;
+  while ((1LL << gp.ceil_log2_k) < K) ++gp.ceil_log2_k;
   gp.fault = fault;
   gp.wait_ns = wait_ns;
   const Tables& t = host_tables();
@@ -872,6 +916,7 @@ cudaError_t launch_gemm(const void* RA, long long lda, const void* RB, long long
     gp.qf[i] = t.qf[i];
     gp.invq[i] = t.invq[i];
   }
+  for (int i = 0; i <= kNumPrimes; ++i) gp.log2P[i] = t.log2P[i];
   if (!pair) {
     const long long tiles = (long long)pmax * gp.mt * gp.nt;
     int grid = (int)(tiles < sms[dev] ? tiles : sms[dev]);

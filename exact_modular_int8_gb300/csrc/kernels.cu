@@ -436,6 +436,81 @@ __global__ void __launch_bounds__(256) split_int_kernel(SplitSide sa, SplitSide 
   allow_dependents();
 }
 
+// int64 operands without a planner pass: every entry's residues are written
+// for `P` primes (the most the bound can need, or the caller's count), the
+// chunk count is decided per warp from the warp's largest |x|, and max |A|,
+// max |B| are reduced on the side for the GEMM kernel to derive the prime count
+// and check the range.  Saves one read of A and B and one kernel launch.
+template <int VEC>
+__global__ void __launch_bounds__(256) split_i64_kernel(SplitSide sa, SplitSide sb, DevPlan* plan, int P) {
+  constexpr int NCH = 6;
+  wait_for_predecessor();
+  const int lane = threadIdx.x & 31;
+  const long long total = sa.items + sb.items;
+  const long long stride = (long long)gridDim.x * blockDim.x;
+  unsigned long long max_a = 0, max_b = 0;
+  for (long long base = (long long)blockIdx.x * blockDim.x + (threadIdx.x & ~31); base < total; base += stride) {
+    const long long it = base + lane;
+    const bool valid = it < total;
+    const bool isA = it < sa.items;
+    const SplitSide& s = isA ? sa : sb;
+    const long long item = isA ? it : it - sa.items;
+    const long long per_row = s.ldy / VEC;
+    const long long row = item / per_row;
+    const long long col0 = (item - row * per_row) * VEC;
+    const unsigned long long* X = static_cast<const unsigned long long*>(s.X) + row * s.C + col0;
+    unsigned long long xw[VEC][1];
+    if (valid && col0 + VEC <= s.C && ((reinterpret_cast<uintptr_t>(X) & 15u) == 0)) {
+#pragma unroll
+      for (int t = 0; t < VEC / 2; ++t) {
+        const ulonglong2 v = __ldg(reinterpret_cast<const ulonglong2*>(X) + t);
+        xw[2 * t][0] = v.x;
+        xw[2 * t + 1][0] = v.y;
+      }
+    } else {
+#pragma unroll
+      for (int e = 0; e < VEC; ++e) xw[e][0] = (valid && col0 + e < s.C) ? __ldg(X + e) : 0ull;
+    }
+    unsigned long long m = 0;
+#pragma unroll
+    for (int e = 0; e < VEC; ++e) m = max(m, abs_u64(xw[e][0]));
+    if (isA) max_a = max(max_a, m);
+    else max_b = max(max_b, m);
+    // chunk count for the whole warp: none when every |x| <= 2^23
+    const int bits = __reduce_max_sync(0xffffffffu, (unsigned)bitlen64(m));
+    const int nch = (bits <= 23 || (bits == 24 && __all_sync(0xffffffffu, m <= (1ull << 23))))
+                        ? 0 : (bits + 1 + kChunkBits - 1) / kChunkBits;
+    if (!valid) continue;
+    float cf[VEC][NCH];
+    if (nch == 0) {
+#pragma unroll
+      for (int e = 0; e < VEC; ++e) {
+        cf[e][0] = (float)(long long)xw[e][0];
+#pragma unroll
+        for (int c = 1; c < NCH; ++c) cf[e][c] = 0.0f;
+      }
+    } else {
+#pragma unroll
+      for (int e = 0; e < VEC; ++e) {
+#pragma unroll
+        for (int c = 0; c < NCH; ++c) {
+          const unsigned a = chunk_bits<1>(xw[e], 1, c * kChunkBits);
+          const int v = (c == nch - 1) ? (int)((a ^ 0x800u) - 0x800u) : (int)a;
+          cf[e][c] = c < nch ? (float)v : 0.0f;
+        }
+      }
+    }
+    emit_residues<VEC, NCH>(cf, nch, P, s.Y + row * s.ldy + col0, s.plane);
+  }
+  max_a = block_max_u64(max_a);
+  max_b = block_max_u64(max_b);
+  if (threadIdx.x == 0) {
+    if (max_a) atomicMax(&plan->maxmag_a, max_a);
+    if (max_b) atomicMax(&plan->maxmag_b, max_b);
+  }
+  allow_dependents();
+}
+
 // Binary64 operands: X' = x * 2^f = +-m * 2^sh with sh = max(be,1) - min(be',1)
 // >= 0; the 53-bit significand shifted by sh % 12 is cut into six chunks
 // starting at chunk index sh / 12.  No floating-point instruction reads x.
@@ -861,7 +936,8 @@ static unsigned split_grid(long long items) {
 }
 
 cudaError_t launch_split(int op, const void* A, const void* B, int la, int lb, long long M, long long N, long long K,
-                         long long lda, long long ldb, void* RA, void* RB, DevPlan* plan, cudaStream_t st) {
+                         long long lda, long long ldb, void* RA, void* RB, DevPlan* plan, int i64_planes,
+                         cudaStream_t st) {
   __half* ra = static_cast<__half*>(RA);
   __half* rb = static_cast<__half*>(RB);
   if (op == RG_OP_ENCLOSE) {
@@ -871,6 +947,11 @@ cudaError_t launch_split(int op, const void* A, const void* B, int la, int lb, l
                             (const DevPlan*)plan);
   }
   const int L = la > lb ? la : lb;
+  if (op == RG_OP_I64) {
+    constexpr int V = 8;
+    const SplitSide sa = make_side(A, ra, M, K, lda, 1, V), sb = make_side(B, rb, K, N, ldb, 1, V);
+    return launch_dependent(split_i64_kernel<V>, split_grid(sa.items + sb.items), 256, 0, st, sa, sb, plan, i64_planes);
+  }
   if (L <= 1) {
     constexpr int V = 8;
     const SplitSide sa = make_side(A, ra, M, K, lda, la, V), sb = make_side(B, rb, K, N, ldb, lb, V);
