@@ -164,7 +164,8 @@ int run(int op, const void* A, int la, const void* B, int lb, void* C, void* C2,
   int fault = g_fault.exchange(0);
   RG_TRY(launch_gemm(w + L.ra, L.lda, w + L.rb, L.ldb, w + L.rc, L.ldc, L.pmax, i64 ? nprimes : 0, M, N, K, plan, s,
                      fault, g_wait_ns.load(), i64));
-  RG_TRY(launch_garner(op, w + L.rc, L.ldc, (long long)M * L.ldc, M, N, op == RG_OP_LIMBS ? lc : 1, plan, dC, dC2, s));
+  RG_TRY(launch_garner(op, w + L.rc, L.ldc, (long long)M * L.ldc, M, N, K, op == RG_OP_LIMBS ? lc : 1, plan, dC, dC2,
+                       s));
   if (flags & RG_FLAG_HOST) {
     RG_TRY(cudaMemcpyAsync(C, dC, (size_t)M * N * ec, cudaMemcpyDeviceToHost, s));
     if (op == RG_OP_ENCLOSE) RG_TRY(cudaMemcpyAsync(C2, dC2, (size_t)M * N * 8, cudaMemcpyDeviceToHost, s));

@@ -137,13 +137,26 @@ __device__ LocalPlan finalize_plan(DevPlan* plan, const PlanArgs& a) {
     }
     const int ea = __ldcg(&plan->maxe_a), eb = __ldcg(&plan->maxe_b);
     const int mina = 4096 - __ldcg(&plan->inv_mine_a), minb = 4096 - __ldcg(&plan->inv_mine_b);
-    p.bits_a = ea ? ea - mina + 53 : 0;  // |A * 2^f_a| < 2^bits_a
-    p.bits_b = eb ? eb - minb + 53 : 0;
-    p.f_a = ea ? 1075 - mina : 0;        // finest binary point of A: 2^-f_a
-    p.f_b = eb ? 1075 - minb : 0;
-    p.T = p.bits_a + p.bits_b + ck;
-    p.lossless = p.bits_a <= 255 && p.bits_b <= 255 && p.T <= RG_MAX_BOUND_BITS;
-    if (!p.lossless) p.status = RG_ERR_LOSSY;
+    // finest binary point holding every entry exactly: |A * 2^f_a| < 2^bits_a
+    const int bits_a0 = ea ? ea - mina + 53 : 0, bits_b0 = eb ? eb - minb + 53 : 0;
+    // coarsened until each operand fits 256-bit two's complement and the
+    // product fits the residue range (enclosure-gemm, Method): the larger
+    // operand gives up bits first
+    int ba = min(bits_a0, 255), bb = min(bits_b0, 255);
+    int excess = ba + bb + ck - RG_MAX_BOUND_BITS;
+    if (excess > 0) {
+      const int d = min(excess, abs(ba - bb));
+      if (ba >= bb) ba -= d; else bb -= d;
+      excess -= d;
+      ba -= (excess + 1) / 2;
+      bb -= excess / 2;
+    }
+    p.bits_a = ba;
+    p.bits_b = bb;
+    p.f_a = ea ? 1075 - mina - (bits_a0 - ba) : 0;
+    p.f_b = eb ? 1075 - minb - (bits_b0 - bb) : 0;
+    p.T = ba + bb + ck;
+    p.lossless = ba == bits_a0 && bb == bits_b0;
   }
   if (p.status) return p;
   p.P = a.nprimes_fixed ? a.nprimes_fixed : primes_for_bound(p.T);
@@ -520,7 +533,7 @@ __global__ void __launch_bounds__(256) split_f64_kernel(SplitSide sa, SplitSide 
   wait_for_predecessor();
   if (plan->status) return;
   const int P = plan->P;
-  const int emin_a = 4096 - plan->inv_mine_a, emin_b = 4096 - plan->inv_mine_b;
+  const int fa = plan->f_a, fb = plan->f_b;
   for (int i = threadIdx.x; i < P * kMaxChunks; i += blockDim.x)
     w_s[i / kMaxChunks][i % kMaxChunks] = c_tab.chunk_w[i / kMaxChunks][i % kMaxChunks];
   __syncthreads();
@@ -529,7 +542,7 @@ __global__ void __launch_bounds__(256) split_f64_kernel(SplitSide sa, SplitSide 
        it += (long long)gridDim.x * blockDim.x) {
     const bool isA = it < sa.items;
     const SplitSide& s = isA ? sa : sb;
-    const int emin = isA ? emin_a : emin_b;
+    const int f = isA ? fa : fb;
     const long long item = isA ? it : it - sa.items;
     const long long per_row = s.ldy / VEC;
     const long long row = item / per_row;
@@ -554,12 +567,24 @@ __global__ void __launch_bounds__(256) split_f64_kernel(SplitSide sa, SplitSide 
     for (int e = 0; e < VEC; ++e) {
       const unsigned long long v = xv[e];
       const int be = (int)((v >> 52) & 0x7FF);
-      const unsigned long long m = (v & 0xFFFFFFFFFFFFFull) | (be ? (1ull << 52) : 0ull);
-      int sh = (be > 1 ? be : 1) - emin;
-      if (m == 0) sh = 0;
-      c0[e] = sh / kChunkBits;
-      const unsigned long long t = m << (sh % kChunkBits);
-      const float sg = (v >> 63) ? -1.0f : 1.0f;
+      const bool neg = (v >> 63) != 0;
+      unsigned long long m = (v & 0xFFFFFFFFFFFFFull) | (be ? (1ull << 52) : 0ull);
+      int sh = (be > 1 ? be : 1) - 1075 + f;  // x * 2^f = +-m * 2^sh
+      unsigned long long t;
+      if (m == 0 || sh >= 0) {
+        // exact: +-m * 2^sh, cut at chunk sh / 12
+        if (m == 0) sh = 0;
+        c0[e] = sh / kChunkBits;
+        t = m << (sh % kChunkBits);
+      } else {
+        // coarsened (lossy) point: floor(+-m * 2^sh), below 2^53 in magnitude
+        const int r = -sh;
+        const unsigned long long q = r >= 64 ? 0ull : m >> r;
+        const bool lost = r >= 64 ? true : (m & ((1ull << r) - 1ull)) != 0ull;
+        t = (neg && lost) ? q + 1ull : q;  // floor of a negative value rounds away from zero
+        c0[e] = 0;
+      }
+      const float sg = neg ? -1.0f : 1.0f;
 #pragma unroll
       for (int c = 0; c < NC; ++c) cf[e][c] = sg * (float)(unsigned)((t >> (kChunkBits * c)) & 0xFFFu);
     }
@@ -822,9 +847,26 @@ __device__ __forceinline__ void outward_bits(const uint32_t (&x)[kEncW], int Q, 
   }
 }
 
+// x (kEncW words, two's complement) += sign * (v << shift), v < 2^31, shift >= 0.
+__device__ __forceinline__ void add_shifted(uint32_t (&x)[kEncW], long long v, int shift, int sign) {
+  const int w0 = shift >> 5, b = shift & 31;
+  const unsigned long long part = (unsigned long long)v << b;  // < 2^63: two words
+  long long carry = 0;
+#pragma unroll
+  for (int k = 0; k < kEncW; ++k) {
+    long long add = 0;
+    if (k == w0) add = (long long)(part & 0xFFFFFFFFull);
+    if (k == w0 + 1) add = (long long)(part >> 32);
+    const long long t = (long long)x[k] + sign * add + carry;
+    x[k] = (uint32_t)t;
+    carry = t >> 32;
+  }
+}
+
 __global__ void __launch_bounds__(128) garner_enclose_kernel(const uint8_t* __restrict__ RC, long long ldc,
                                                              long long plane, long long M, long long N,
-                                                             DevPlan* plan, unsigned long long* __restrict__ lo,
+                                                             long long K, DevPlan* plan,
+                                                             unsigned long long* __restrict__ lo,
                                                              unsigned long long* __restrict__ hi) {
   constexpr int GE = GarnerGE<kEncW>::value;
   wait_for_predecessor();
@@ -839,8 +881,30 @@ __global__ void __launch_bounds__(128) garner_enclose_kernel(const uint8_t* __re
   uint32_t x[GE][kEncW];
   garner_reconstruct<kEncW, GE>(RC + m * ldc + n0, plane, P, x);
   unsigned long long l[GE], h[GE];
+  if (plan->lossless) {
 #pragma unroll
-  for (int e = 0; e < GE; ++e) outward_bits(x[e], Q, l[e], h[e]);
+    for (int e = 0; e < GE; ++e) outward_bits(x[e], Q, l[e], h[e]);
+  } else {
+    // Coarsened operands A' = floor(A 2^f_a), B' = floor(B 2^f_b) leave
+    // remainders in [0, 1) per entry; with |A'| <= 2^bits_a, |B'| <= 2^bits_b
+    // the exact (A 2^f_a)(B 2^f_b) lies in S + (-K(2^a + 2^b), K(2^a + 2^b) + K)
+    // ("enclosure-gemm", Method: the termwise bound added back outward).
+    const int ba = plan->bits_a, bb = plan->bits_b;
+#pragma unroll
+    for (int e = 0; e < GE; ++e) {
+      uint32_t xl[kEncW], xh[kEncW];
+#pragma unroll
+      for (int k = 0; k < kEncW; ++k) xl[k] = xh[k] = x[e][k];
+      add_shifted(xl, K, ba, -1);
+      add_shifted(xl, K, bb, -1);
+      add_shifted(xh, K, ba, 1);
+      add_shifted(xh, K, bb, 1);
+      add_shifted(xh, K, 0, 1);
+      unsigned long long unused;
+      outward_bits(xl, Q, l[e], unused);
+      outward_bits(xh, Q, unused, h[e]);
+    }
+  }
   unsigned long long* plo = lo + m * N + n0;
   unsigned long long* phi = hi + m * N + n0;
   if (n0 + GE <= N && ((reinterpret_cast<uintptr_t>(plo) & 15u) == 0)) {
@@ -971,13 +1035,14 @@ cudaError_t launch_split(int op, const void* A, const void* B, int la, int lb, l
   return cudaGetLastError();
 }
 
-cudaError_t launch_garner(int op, const void* RC, long long ldc, long long plane, long long M, long long N, int lc,
-                          DevPlan* plan, void* out0, void* out1, cudaStream_t st) {
+cudaError_t launch_garner(int op, const void* RC, long long ldc, long long plane, long long M, long long N,
+                          long long K, int lc, DevPlan* plan, void* out0, void* out1, cudaStream_t st) {
   const uint8_t* rc = static_cast<const uint8_t*>(RC);
   auto blocks_for = [&](int ge) { return dim3((unsigned)((M * ((N + ge - 1) / ge) + 127) / 128)); };
   if (op == RG_OP_ENCLOSE)
     return launch_dependent(garner_enclose_kernel, blocks_for(GarnerGE<kEncW>::value), 128, 0, st, rc, ldc, plane, M,
-                            N, plan, static_cast<unsigned long long*>(out0), static_cast<unsigned long long*>(out1));
+                            N, K, plan, static_cast<unsigned long long*>(out0),
+                            static_cast<unsigned long long*>(out1));
   int64_t* C = static_cast<int64_t*>(out0);
   switch (lc) {
     case 1: return launch_dependent(garner_int_kernel<1>, blocks_for(GarnerGE<2>::value), 128, 0, st, rc, ldc, plane, M, N, plan, C);

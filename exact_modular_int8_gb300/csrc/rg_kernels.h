@@ -34,7 +34,7 @@ cudaError_t launch_gemm(const void* RA, long long lda, const void* RB, long long
 
 // Balanced Garner: RC [P][M][ldc] -> int64 limbs C [M][N][lc] (op I64/LIMBS),
 // or the outward pair (lo, hi) as binary64 bit patterns (op ENCLOSE).
-cudaError_t launch_garner(int op, const void* RC, long long ldc, long long plane, long long M, long long N, int lc,
-                          DevPlan* plan, void* out0, void* out1, cudaStream_t st);
+cudaError_t launch_garner(int op, const void* RC, long long ldc, long long plane, long long M, long long N,
+                          long long K, int lc, DevPlan* plan, void* out0, void* out1, cudaStream_t st);
 
 }  // namespace rg

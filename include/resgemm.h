@@ -47,7 +47,7 @@ extern "C" {
 #define RG_ERR_ARG 1        /* null pointer, non-positive size, bad limb count, misaligned workspace */
 #define RG_ERR_RANGE 2      /* K > 2^17, or the product bound exceeds the primes or the output width */
 #define RG_ERR_NONFINITE 3  /* an fp64 operand entry is inf or nan */
-#define RG_ERR_LOSSY 4      /* fp64 operands do not scale losslessly into the fixed point */
+#define RG_ERR_LOSSY 4      /* reserved: wide fp64 operands now get a valid, looser bracket (rg_get_plan) */
 #define RG_ERR_WORKSPACE 5  /* workspace too small */
 #define RG_ERR_CUDA 6       /* a CUDA runtime or driver call failed */
 #define RG_ERR_TIMEOUT 7    /* a bounded wait inside a kernel expired; the kernel stopped early */
@@ -117,10 +117,15 @@ int res_gemm_limbs(const int64_t* A, int la, const int64_t* B, int lb, int64_t* 
  * toward zero is +-max finite and the other +-inf.  S == 0 gives +0.0 for
  * both; a negative value too small for a subnormal gives [-2^-1074, -0.0].
  * No floating-point instruction touches the result.
- * Errors: RG_ERR_NONFINITE (an inf or nan entry), RG_ERR_LOSSY (an operand
- * spans more than 255 bits, or bits_a + bits_b + ceil(log2 K) > 332: the
- * lossy regime of the page is not provided), RG_ERR_RANGE (K > 2^17), and
- * the errors of res_gemm_i64.
+ * Operands wider than the fixed point (more than 255 bits, or
+ * bits_a + bits_b + ceil(log2 K) > 332) are coarsened: the larger operand
+ * gives up bits first, entries are floored at the coarser point (remainder in
+ * [0, 1) per entry), and the interval (-K(2^bits_a + 2^bits_b),
+ * K(2^bits_a + 2^bits_b) + K) bounding the induced error is added to S before
+ * each endpoint is rounded outward: a valid, looser bracket, reported by
+ * rg_get_plan() with lossless = 0 ("enclosure-gemm", Method).
+ * Errors: RG_ERR_NONFINITE (an inf or nan entry), RG_ERR_RANGE (K > 2^17),
+ * and the errors of res_gemm_i64.
  */
 int enclose_gemm_f64(const double* A, const double* B, double* lo, double* hi, int64_t M, int64_t N, int64_t K,
                      unsigned flags, void* ws, size_t ws_bytes, void* stream);
