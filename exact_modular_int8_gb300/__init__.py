@@ -37,6 +37,7 @@ RG_ERR_CUDA = 6
 RG_ERR_TIMEOUT = 7
 RG_FLAG_SYNC = 1
 RG_FLAG_HOST = 2
+RG_FLAG_TRANS_B = 4
 RG_OP_I64, RG_OP_LIMBS, RG_OP_ENCLOSE, RG_OP_STAGE = 0, 1, 2, 3
 MAX_K = 131072
 NUM_PRIMES = 53
@@ -122,13 +123,17 @@ def primes() -> list[int]:
     return [library().rg_prime(i) for i in range(NUM_PRIMES)]
 
 
-def workspace_bytes(op, M, N, K, la=1, lb=1, lc=1, nprimes=0, host=False) -> int:
-    return int(library().rg_workspace_bytes(op, M, N, K, la, lb, lc, nprimes, RG_FLAG_HOST if host else 0))
+def _layout_flags(host, transb):
+    return (RG_FLAG_HOST if host else 0) | (RG_FLAG_TRANS_B if transb else 0)
 
 
-def workspace_layout(op, M, N, K, la=1, lb=1, lc=1, nprimes=0, host=False) -> Layout:
+def workspace_bytes(op, M, N, K, la=1, lb=1, lc=1, nprimes=0, host=False, transb=False) -> int:
+    return int(library().rg_workspace_bytes(op, M, N, K, la, lb, lc, nprimes, _layout_flags(host, transb)))
+
+
+def workspace_layout(op, M, N, K, la=1, lb=1, lc=1, nprimes=0, host=False, transb=False) -> Layout:
     out = Layout()
-    rc = library().rg_workspace_layout(op, M, N, K, la, lb, lc, nprimes, RG_FLAG_HOST if host else 0,
+    rc = library().rg_workspace_layout(op, M, N, K, la, lb, lc, nprimes, _layout_flags(host, transb),
                                        ctypes.byref(out))
     if rc:
         raise ResGemmError(rc, "rg_workspace_layout")
@@ -180,20 +185,24 @@ def _check(rc, where):
 
 
 def res_gemm_i64(A: torch.Tensor, B: torch.Tensor, nprimes: int = 0, sync: bool = True, out=None,
-                 ws: torch.Tensor | None = None) -> torch.Tensor:
-    """Exact C = A @ B for int64 matrices (CUDA tensors, or CPU tensors staged through the device)."""
-    if A.dtype != torch.int64 or B.dtype != torch.int64 or A.dim() != 2 or B.dim() != 2 or A.shape[1] != B.shape[0]:
-        raise ValueError("A [M,K] and B [K,N] int64 expected")
+                 ws: torch.Tensor | None = None, transb: bool = False) -> torch.Tensor:
+    """Exact C = A @ B for int64 matrices (CUDA tensors, or CPU tensors staged through the device).
+    With transb, B is given as [N, K] and C = A @ B.T, without a transposed copy."""
+    if A.dtype != torch.int64 or B.dtype != torch.int64 or A.dim() != 2 or B.dim() != 2 or \
+            A.shape[1] != B.shape[1 if transb else 0]:
+        raise ValueError("A [M,K] and B [K,N] (transb: [N,K]) int64 expected")
     A, B = A.contiguous(), B.contiguous()
     M, K = A.shape
-    N = B.shape[1]
+    N = B.shape[0 if transb else 1]
     dev, flags = _call_ctx(A, B)
     if sync:
         flags |= RG_FLAG_SYNC
+    if transb:
+        flags |= RG_FLAG_TRANS_B
     C = out if out is not None else torch.empty((M, N), dtype=torch.int64, device=A.device,
                                                 pin_memory=bool(flags & RG_FLAG_HOST))
     with torch.cuda.device(dev):
-        need = workspace_bytes(RG_OP_I64, M, N, K, nprimes=nprimes, host=bool(flags & RG_FLAG_HOST))
+        need = workspace_bytes(RG_OP_I64, M, N, K, nprimes=nprimes, host=bool(flags & RG_FLAG_HOST), transb=transb)
         if need == 0:
             raise ResGemmError(RG_ERR_ARG, "res_gemm_i64")
         w = ws if ws is not None else workspace(need, dev)
@@ -204,20 +213,25 @@ def res_gemm_i64(A: torch.Tensor, B: torch.Tensor, nprimes: int = 0, sync: bool 
 
 
 def res_gemm_limbs(A: torch.Tensor, B: torch.Tensor, lc: int, nprimes: int = 0, sync: bool = True, out=None,
-                   ws: torch.Tensor | None = None) -> torch.Tensor:
-    """Exact C = A @ B for multi-limb int64 operands A [M,K,la], B [K,N,lb]; returns [M,N,lc]."""
-    if A.dtype != torch.int64 or B.dtype != torch.int64 or A.dim() != 3 or B.dim() != 3 or A.shape[1] != B.shape[0]:
-        raise ValueError("A [M,K,la] and B [K,N,lb] int64 expected")
+                   ws: torch.Tensor | None = None, transb: bool = False) -> torch.Tensor:
+    """Exact C = A @ B for multi-limb int64 operands A [M,K,la], B [K,N,lb]; returns [M,N,lc].
+    With transb, B is given as [N,K,lb] and C = A @ B.T."""
+    if A.dtype != torch.int64 or B.dtype != torch.int64 or A.dim() != 3 or B.dim() != 3 or \
+            A.shape[1] != B.shape[1 if transb else 0]:
+        raise ValueError("A [M,K,la] and B [K,N,lb] (transb: [N,K,lb]) int64 expected")
     A, B = A.contiguous(), B.contiguous()
     M, K, la = A.shape
-    N, lb = B.shape[1], B.shape[2]
+    N, lb = B.shape[0 if transb else 1], B.shape[2]
     dev, flags = _call_ctx(A, B)
     if sync:
         flags |= RG_FLAG_SYNC
+    if transb:
+        flags |= RG_FLAG_TRANS_B
     C = out if out is not None else torch.empty((M, N, lc), dtype=torch.int64, device=A.device,
                                                 pin_memory=bool(flags & RG_FLAG_HOST))
     with torch.cuda.device(dev):
-        need = workspace_bytes(RG_OP_LIMBS, M, N, K, la, lb, lc, nprimes, host=bool(flags & RG_FLAG_HOST))
+        need = workspace_bytes(RG_OP_LIMBS, M, N, K, la, lb, lc, nprimes, host=bool(flags & RG_FLAG_HOST),
+                               transb=transb)
         if need == 0:
             raise ResGemmError(RG_ERR_ARG, "res_gemm_limbs")
         w = ws if ws is not None else workspace(need, dev)
@@ -227,21 +241,26 @@ def res_gemm_limbs(A: torch.Tensor, B: torch.Tensor, lc: int, nprimes: int = 0, 
     return C
 
 
-def enclose_gemm_f64(A: torch.Tensor, B: torch.Tensor, sync: bool = True, ws: torch.Tensor | None = None):
-    """(lo, hi) float64 with lo <= A @ B <= hi entrywise in exact arithmetic."""
-    if A.dtype != torch.float64 or B.dtype != torch.float64 or A.dim() != 2 or B.dim() != 2 or A.shape[1] != B.shape[0]:
-        raise ValueError("A [M,K] and B [K,N] float64 expected")
+def enclose_gemm_f64(A: torch.Tensor, B: torch.Tensor, sync: bool = True, ws: torch.Tensor | None = None,
+                     transb: bool = False):
+    """(lo, hi) float64 with lo <= A @ B <= hi entrywise in exact arithmetic.
+    With transb, B is given as [N, K] and the bracket is of A @ B.T."""
+    if A.dtype != torch.float64 or B.dtype != torch.float64 or A.dim() != 2 or B.dim() != 2 or \
+            A.shape[1] != B.shape[1 if transb else 0]:
+        raise ValueError("A [M,K] and B [K,N] (transb: [N,K]) float64 expected")
     A, B = A.contiguous(), B.contiguous()
     M, K = A.shape
-    N = B.shape[1]
+    N = B.shape[0 if transb else 1]
     dev, flags = _call_ctx(A, B)
     if sync:
         flags |= RG_FLAG_SYNC
+    if transb:
+        flags |= RG_FLAG_TRANS_B
     pin = bool(flags & RG_FLAG_HOST)
     lo = torch.empty((M, N), dtype=torch.float64, device=A.device, pin_memory=pin)
     hi = torch.empty((M, N), dtype=torch.float64, device=A.device, pin_memory=pin)
     with torch.cuda.device(dev):
-        need = workspace_bytes(RG_OP_ENCLOSE, M, N, K, host=pin)
+        need = workspace_bytes(RG_OP_ENCLOSE, M, N, K, host=pin, transb=transb)
         if need == 0:
             raise ResGemmError(RG_ERR_ARG, "enclose_gemm_f64")
         w = ws if ws is not None else workspace(need, dev)
@@ -251,9 +270,20 @@ def enclose_gemm_f64(A: torch.Tensor, B: torch.Tensor, sync: bool = True, ws: to
     return lo, hi
 
 
+def mm_enclose(A: torch.Tensor, B: torch.Tensor):
+    """lo <= A @ B <= hi entrywise, exactly ("enclosure-gemm", Usage: mm_enclose)."""
+    return enclose_gemm_f64(A, B)
+
+
+def mm_enclose_nt(A: torch.Tensor, Bt: torch.Tensor):
+    """The bracket of A @ Bt.T without a transposed copy ("enclosure-gemm", Usage: mm_enclose_nt)."""
+    return enclose_gemm_f64(A, Bt, transb=True)
+
+
 def res_gemm_stage(RA: torch.Tensor, RB: torch.Tensor, nprimes: int, M: int, N: int, K: int, RC=None,
-                   sync: bool = True) -> torch.Tensor:
-    """RC[p] = (RA[p] @ RB[p]) mod q_p for fp16 residues RA [P,M,lda], RB [P,K,ldb]; RC uint8 [P,M,ldc]."""
+                   sync: bool = True, transb: bool = False) -> torch.Tensor:
+    """RC[p] = (RA[p] @ RB[p]) mod q_p for fp16 residues RA [P,M,lda], RB [P,K,ldb]
+    (transb: RB [P,N,ldb], the product RA[p] @ RB[p].T); RC uint8 [P,M,ldc]."""
     if RA.dtype != torch.float16 or RB.dtype != torch.float16:
         raise ValueError("fp16 residues expected")
     if not (RA.is_contiguous() and RB.is_contiguous()):
@@ -263,10 +293,11 @@ def res_gemm_stage(RA: torch.Tensor, RB: torch.Tensor, nprimes: int, M: int, N: 
     if RC is None:
         RC = torch.empty((nprimes, M, ldc), dtype=torch.uint8, device=RA.device)
     dev = RA.device
+    flags = (RG_FLAG_SYNC if sync else 0) | (RG_FLAG_TRANS_B if transb else 0)
     with torch.cuda.device(dev):
         w = workspace(4096, dev)
         rc = library().res_gemm_stage(RA.data_ptr(), lda, RB.data_ptr(), ldb, RC.data_ptr(), RC.shape[-1], nprimes,
-                                      M, N, K, RG_FLAG_SYNC if sync else 0, w.data_ptr(), w.numel(),
+                                      M, N, K, flags, w.data_ptr(), w.numel(),
                                       torch.cuda.current_stream(dev).cuda_stream)
     _check(rc, "res_gemm_stage")
     return RC

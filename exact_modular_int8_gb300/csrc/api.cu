@@ -70,8 +70,9 @@ bool make_layout(int op, long long M, long long N, long long K, int la, int lb, 
     return false;
   if (op != RG_OP_LIMBS) la = lb = lc = 1;
   std::memset(L, 0, sizeof(*L));
+  const bool transb = (flags & RG_FLAG_TRANS_B) != 0;
   L->lda = round_up(K, 8);
-  L->ldb = round_up(N, 64);
+  L->ldb = transb ? round_up(K, 8) : round_up(N, 64);
   L->ldc = round_up(N, 16);
   L->plan = 0;
   size_t off = kPlanBytes;
@@ -85,7 +86,7 @@ bool make_layout(int op, long long M, long long N, long long K, int la, int lb, 
   L->ra = off;
   off = align_up(off + (size_t)pmax * M * L->lda * 2, kAlign);
   L->rb = off;
-  off = align_up(off + (size_t)pmax * K * L->ldb * 2, kAlign);
+  off = align_up(off + (size_t)pmax * (transb ? N : K) * L->ldb * 2, kAlign);
   L->rc = off;
   off = align_up(off + (size_t)pmax * M * L->ldc, kAlign);
   if (flags & RG_FLAG_HOST) {
@@ -160,10 +161,11 @@ int run(int op, const void* A, int la, const void* B, int lb, void* C, void* C2,
   const bool i64 = op == RG_OP_I64;
   if (!i64)
     RG_TRY(launch_plan(op, dA, M * K, la1, dB, K * N, lb1, lc1, K, op == RG_OP_ENCLOSE ? 0 : nprimes, plan, s));
-  RG_TRY(launch_split(op, dA, dB, la1, lb1, M, N, K, L.lda, L.ldb, w + L.ra, w + L.rb, plan, L.pmax, s));
+  const bool transb = (flags & RG_FLAG_TRANS_B) != 0;
+  RG_TRY(launch_split(op, dA, dB, la1, lb1, M, N, K, L.lda, L.ldb, w + L.ra, w + L.rb, plan, L.pmax, transb, s));
   int fault = g_fault.exchange(0);
   RG_TRY(launch_gemm(w + L.ra, L.lda, w + L.rb, L.ldb, w + L.rc, L.ldc, L.pmax, i64 ? nprimes : 0, M, N, K, plan, s,
-                     fault, g_wait_ns.load(), i64));
+                     fault, g_wait_ns.load(), i64, transb));
   RG_TRY(launch_garner(op, w + L.rc, L.ldc, (long long)M * L.ldc, M, N, K, op == RG_OP_LIMBS ? lc : 1, plan, dC, dC2,
                        s));
   if (flags & RG_FLAG_HOST) {
@@ -197,7 +199,9 @@ int res_gemm_stage(const uint16_t* RA, int64_t lda, const uint16_t* RB, int64_t 
                    void* stream) {
   if (!RA || !RB || !RC || !ws || (flags & RG_FLAG_HOST)) return RG_ERR_ARG;
   if (M <= 0 || N <= 0 || K <= 0 || nprimes < 1 || nprimes > kNumPrimes) return RG_ERR_ARG;
-  if (lda < K || lda % 8 || ldb < N || ldb % 64 || ldc < N || ldc % 16) return RG_ERR_ARG;
+  const bool transb = (flags & RG_FLAG_TRANS_B) != 0;
+  if (lda < K || lda % 8 || ldc < N || ldc % 16) return RG_ERR_ARG;
+  if (transb ? (ldb < K || ldb % 8) : (ldb < N || ldb % 64)) return RG_ERR_ARG;
   if ((reinterpret_cast<uintptr_t>(RA) | reinterpret_cast<uintptr_t>(RB) | reinterpret_cast<uintptr_t>(RC)) & 15u)
     return RG_ERR_ARG;
   if ((reinterpret_cast<uintptr_t>(ws) & 255u) != 0) return RG_ERR_ARG;
@@ -207,7 +211,8 @@ int res_gemm_stage(const uint16_t* RA, int64_t lda, const uint16_t* RB, int64_t 
   DevPlan* plan = static_cast<DevPlan*>(ws);
   RG_TRY(cudaMemsetAsync(plan, 0, sizeof(DevPlan), s));
   int fault = g_fault.exchange(0);
-  RG_TRY(launch_gemm(RA, lda, RB, ldb, RC, ldc, nprimes, nprimes, M, N, K, plan, s, fault, g_wait_ns.load(), false));
+  RG_TRY(launch_gemm(RA, lda, RB, ldb, RC, ldc, nprimes, nprimes, M, N, K, plan, s, fault, g_wait_ns.load(), false,
+                     transb));
   return finish(ws, s, flags);
 }
 

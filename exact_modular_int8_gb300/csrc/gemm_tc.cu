@@ -287,6 +287,9 @@ __device__ __forceinline__ TileCoord tile_coord(int t, int mt, int nt) {
 // ---------------------------------------------------------------------------
 // The kernel
 // ---------------------------------------------------------------------------
+// B_KMAJOR: residues of B arrive as [N][K] (a transposed operand) instead of
+// [K][N]; the tiles are then staged like A's and read as a K-major operand.
+template <bool B_KMAJOR>
 __global__ void __launch_bounds__(NUM_THREADS, 1)
     residue_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                         const __grid_constant__ CUtensorMap tmC, const __grid_constant__ GemmParams gp,
@@ -357,8 +360,13 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
           uint32_t a_dst = smem_u32(stage_base + stage * STAGE_BYTES);
           uint32_t b_dst = a_dst + A_BYTES;
           tma_load_3d(a_dst, &tmA, fb, kb * BK, tc.m * BM, tc.p);
+          if constexpr (B_KMAJOR) {
+            tma_load_3d(b_dst, &tmB, fb, kb * BK, tc.n * BN, tc.p);  // BN rows of 64 K
+          } else {
 #pragma unroll
-          for (int j = 0; j < BN / 64; ++j) tma_load_3d(b_dst + j * B_SLAB, &tmB, fb, tc.n * BN + 64 * j, kb * BK, tc.p);
+            for (int j = 0; j < BN / 64; ++j)
+              tma_load_3d(b_dst + j * B_SLAB, &tmB, fb, tc.n * BN + 64 * j, kb * BK, tc.p);
+          }
           issued[stage] = true;
           issued_phase[stage] = phase;
           if (++stage == STAGES) {
@@ -400,11 +408,14 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             tc_fence_after();
             const uint32_t a_addr = smem_u32(stage_base + stage * STAGE_BYTES);
             const uint64_t adesc = sw128_desc(a_addr, 16, 1024);
-            const uint64_t bdesc = sw128_desc(a_addr + A_BYTES, B_SLAB, 1024);
+            const uint64_t bdesc = B_KMAJOR ? sw128_desc(a_addr + A_BYTES, 16, 1024)
+                                            : sw128_desc(a_addr + A_BYTES, B_SLAB, 1024);
+            constexpr uint32_t b_step = B_KMAJOR ? 2 : 128;  // 16 K: 32 bytes along a row, or 16 rows of 128 bytes
+            constexpr uint32_t idesc = B_KMAJOR ? (IDESC & ~(1u << 16)) : IDESC;
 #pragma unroll
             for (int kk = 0; kk < BK / 16; ++kk) {
               const uint32_t acc = (c >= 2 || kb > kb0 || kk > 0) ? 1u : 0u;
-              umma_f16(d, adesc + (uint64_t)(2 * kk), bdesc + (uint64_t)(128 * kk), IDESC, acc);
+              umma_f16(d, adesc + (uint64_t)(2 * kk), bdesc + (uint64_t)(b_step * kk), idesc, acc);
             }
             any = true;
             umma_commit(smem_u32(&empty[stage]));
@@ -608,6 +619,7 @@ __device__ bool wait_bounded_cluster(uint32_t bar, uint32_t parity, const Ctl& c
   }
 }
 
+template <bool B_KMAJOR>
 __global__ void __launch_bounds__(NUM_THREADS, 1)
     residue_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                              const __grid_constant__ CUtensorMap tmC, const __grid_constant__ GemmParams gp,
@@ -680,9 +692,13 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
           const uint32_t a_dst = smem_u32(stage_base + stage * STAGE2_BYTES);
           const uint32_t b_dst = a_dst + A_BYTES;
           tma_load_3d_pair(a_dst, &tmA, fb, kb * BK, tc.m * 256 + (int)rank * 128, tc.p);
+          if constexpr (B_KMAJOR) {
+            tma_load_3d_pair(b_dst, &tmB, fb, kb * BK, tc.n * BN + (int)rank * 128, tc.p);  // 128 rows of 64 K
+          } else {
 #pragma unroll
-          for (int j = 0; j < 2; ++j)
-            tma_load_3d_pair(b_dst + j * B_SLAB, &tmB, fb, tc.n * BN + (int)rank * 128 + 64 * j, kb * BK, tc.p);
+            for (int j = 0; j < 2; ++j)
+              tma_load_3d_pair(b_dst + j * B_SLAB, &tmB, fb, tc.n * BN + (int)rank * 128 + 64 * j, kb * BK, tc.p);
+          }
           if (++stage == STAGES2) {
             stage = 0;
             phase ^= 1u;
@@ -715,11 +731,14 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             tc_fence_after();
             const uint32_t a_addr = smem_u32(stage_base + stage * STAGE2_BYTES);
             const uint64_t adesc = sw128_desc(a_addr, 16, 1024);
-            const uint64_t bdesc = sw128_desc(a_addr + A_BYTES, B_SLAB, 1024);
+            const uint64_t bdesc = B_KMAJOR ? sw128_desc(a_addr + A_BYTES, 16, 1024)
+                                            : sw128_desc(a_addr + A_BYTES, B_SLAB, 1024);
+            constexpr uint32_t b_step = B_KMAJOR ? 2 : 128;
+            constexpr uint32_t idesc = B_KMAJOR ? (IDESC2 & ~(1u << 16)) : IDESC2;
 #pragma unroll
             for (int kk = 0; kk < BK / 16; ++kk) {
               const uint32_t acc = (c >= 2 || kb > kb0 || kk > 0) ? 1u : 0u;
-              umma_f16_pair(d, adesc + (uint64_t)(2 * kk), bdesc + (uint64_t)(128 * kk), IDESC2, acc);
+              umma_f16_pair(d, adesc + (uint64_t)(2 * kk), bdesc + (uint64_t)(b_step * kk), idesc, acc);
             }
             any = true;
             umma_commit_pair(smem_u32(&empty[stage]));
@@ -873,17 +892,21 @@ std::atomic<int> g_gemm_variant{0};  // 0 automatic, 1 single-CTA, 2 CTA pair
 
 cudaError_t launch_gemm(const void* RA, long long lda, const void* RB, long long ldb, void* RC, long long ldc,
                         int pmax, int P_fixed, long long M, long long N, long long K, DevPlan* plan, cudaStream_t st,
-                        int fault, unsigned long long wait_ns, bool derive_i64) {
+                        int fault, unsigned long long wait_ns, bool derive_i64, bool b_kmajor) {
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
   if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
   static int sms[64];
   if (!g_gemm_ready[dev]) {
-    e = cudaFuncSetAttribute(residue_gemm_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
-    if (e != cudaSuccess) return e;
-    e = cudaFuncSetAttribute(residue_gemm_pair_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM2_BYTES);
-    if (e != cudaSuccess) return e;
+    for (auto k : {residue_gemm_kernel<false>, residue_gemm_kernel<true>}) {
+      e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
+      if (e != cudaSuccess) return e;
+    }
+    for (auto k : {residue_gemm_pair_kernel<false>, residue_gemm_pair_kernel<true>}) {
+      e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM2_BYTES);
+      if (e != cudaSuccess) return e;
+    }
     cudaDeviceGetAttribute(&sms[dev], cudaDevAttrMultiProcessorCount, dev);
     g_gemm_ready[dev] = 1;
   }
@@ -893,8 +916,10 @@ cudaError_t launch_gemm(const void* RA, long long lda, const void* RB, long long
   CUtensorMap ma, mb, mc;
   if (!make_map_3d(&ma, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, RA, (uint64_t)K, (uint64_t)M, (uint64_t)pmax,
                    (uint64_t)lda * 2, (uint64_t)M * lda * 2, BK, BM) ||
-      !make_map_3d(&mb, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, RB, (uint64_t)N, (uint64_t)K, (uint64_t)pmax,
-                   (uint64_t)ldb * 2, (uint64_t)K * ldb * 2, 64, BK) ||
+      !(b_kmajor ? make_map_3d(&mb, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, RB, (uint64_t)K, (uint64_t)N, (uint64_t)pmax,
+                               (uint64_t)ldb * 2, (uint64_t)N * ldb * 2, BK, pair ? 128 : BN)
+                 : make_map_3d(&mb, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, RB, (uint64_t)N, (uint64_t)K, (uint64_t)pmax,
+                               (uint64_t)ldb * 2, (uint64_t)K * ldb * 2, 64, BK)) ||
       !make_map_3d(&mc, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, RC, (uint64_t)N, (uint64_t)M, (uint64_t)pmax, (uint64_t)ldc,
                    (uint64_t)M * ldc, 128, 128))
     return cudaErrorInvalidValue;
@@ -921,7 +946,10 @@ cudaError_t launch_gemm(const void* RA, long long lda, const void* RB, long long
     const long long tiles = (long long)pmax * gp.mt * gp.nt;
     int grid = (int)(tiles < sms[dev] ? tiles : sms[dev]);
     if (grid < 1) grid = 1;
-    return launch_dependent(residue_gemm_kernel, dim3(grid), dim3(NUM_THREADS), SMEM_BYTES, st, ma, mb, mc, gp, plan);
+    return b_kmajor ? launch_dependent(residue_gemm_kernel<true>, dim3(grid), dim3(NUM_THREADS), SMEM_BYTES, st, ma,
+                                       mb, mc, gp, plan)
+                    : launch_dependent(residue_gemm_kernel<false>, dim3(grid), dim3(NUM_THREADS), SMEM_BYTES, st, ma,
+                                       mb, mc, gp, plan);
   }
   cudaLaunchConfig_t cfg = {};
   cfg.blockDim = dim3(NUM_THREADS);
@@ -942,7 +970,8 @@ cudaError_t launch_gemm(const void* RA, long long lda, const void* RB, long long
   if (!max_pairs[dev]) {
     int n = 0;
     cfg.gridDim = dim3((unsigned)(sms[dev] & ~1));
-    if (cudaOccupancyMaxActiveClusters(&n, residue_gemm_pair_kernel, &cfg) != cudaSuccess || n < 1) n = sms[dev] / 2;
+    if (cudaOccupancyMaxActiveClusters(&n, residue_gemm_pair_kernel<false>, &cfg) != cudaSuccess || n < 1)
+      n = sms[dev] / 2;
     max_pairs[dev] = n;
   }
   const long long tiles2 = (long long)pmax * ((M + 255) / 256) * gp.nt;
@@ -950,7 +979,8 @@ cudaError_t launch_gemm(const void* RA, long long lda, const void* RB, long long
   if (tiles2 < clusters) clusters = tiles2;
   if (clusters < 1) clusters = 1;
   cfg.gridDim = dim3((unsigned)(2 * clusters));
-  return cudaLaunchKernelEx(&cfg, residue_gemm_pair_kernel, ma, mb, mc, gp, plan);
+  return b_kmajor ? cudaLaunchKernelEx(&cfg, residue_gemm_pair_kernel<true>, ma, mb, mc, gp, plan)
+                  : cudaLaunchKernelEx(&cfg, residue_gemm_pair_kernel<false>, ma, mb, mc, gp, plan);
 }
 
 }  // namespace rg

@@ -1000,35 +1000,37 @@ static unsigned split_grid(long long items) {
 }
 
 cudaError_t launch_split(int op, const void* A, const void* B, int la, int lb, long long M, long long N, long long K,
-                         long long lda, long long ldb, void* RA, void* RB, DevPlan* plan, int i64_planes,
+                         long long lda, long long ldb, void* RA, void* RB, DevPlan* plan, int i64_planes, bool transb,
                          cudaStream_t st) {
   __half* ra = static_cast<__half*>(RA);
   __half* rb = static_cast<__half*>(RB);
+  // B [K][N] -> RB [P][K][ldb]; a transposed B [N][K] -> RB [P][N][ldb], laid out like A
+  const long long brows = transb ? N : K, bcols = transb ? K : N;
   if (op == RG_OP_ENCLOSE) {
     constexpr int V = 8;
-    const SplitSide sa = make_side(A, ra, M, K, lda, 1, V), sb = make_side(B, rb, K, N, ldb, 1, V);
+    const SplitSide sa = make_side(A, ra, M, K, lda, 1, V), sb = make_side(B, rb, brows, bcols, ldb, 1, V);
     return launch_dependent(split_f64_kernel<V>, split_grid(sa.items + sb.items), 256, 0, st, sa, sb,
                             (const DevPlan*)plan);
   }
   const int L = la > lb ? la : lb;
   if (op == RG_OP_I64) {
     constexpr int V = 8;
-    const SplitSide sa = make_side(A, ra, M, K, lda, 1, V), sb = make_side(B, rb, K, N, ldb, 1, V);
+    const SplitSide sa = make_side(A, ra, M, K, lda, 1, V), sb = make_side(B, rb, brows, bcols, ldb, 1, V);
     return launch_dependent(split_i64_kernel<V>, split_grid(sa.items + sb.items), 256, 0, st, sa, sb, plan, i64_planes);
   }
   if (L <= 1) {
     constexpr int V = 8;
-    const SplitSide sa = make_side(A, ra, M, K, lda, la, V), sb = make_side(B, rb, K, N, ldb, lb, V);
+    const SplitSide sa = make_side(A, ra, M, K, lda, la, V), sb = make_side(B, rb, brows, bcols, ldb, lb, V);
     return launch_dependent(split_int_kernel<V, 6, 1>, split_grid(sa.items + sb.items), 256, 0, st, sa, sb,
                             (const DevPlan*)plan);
   } else if (L <= 2) {
     constexpr int V = 4;
-    const SplitSide sa = make_side(A, ra, M, K, lda, la, V), sb = make_side(B, rb, K, N, ldb, lb, V);
+    const SplitSide sa = make_side(A, ra, M, K, lda, la, V), sb = make_side(B, rb, brows, bcols, ldb, lb, V);
     return launch_dependent(split_int_kernel<V, 11, 2>, split_grid(sa.items + sb.items), 256, 0, st, sa, sb,
                             (const DevPlan*)plan);
   } else {
     constexpr int V = 2;
-    const SplitSide sa = make_side(A, ra, M, K, lda, la, V), sb = make_side(B, rb, K, N, ldb, lb, V);
+    const SplitSide sa = make_side(A, ra, M, K, lda, la, V), sb = make_side(B, rb, brows, bcols, ldb, lb, V);
     return launch_dependent(split_int_kernel<V, 22, 4>, split_grid(sa.items + sb.items), 256, 0, st, sa, sb,
                             (const DevPlan*)plan);
   }

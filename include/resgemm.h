@@ -55,6 +55,8 @@ extern "C" {
 /* Flags. */
 #define RG_FLAG_SYNC 1u /* synchronise the stream before returning; return the device status */
 #define RG_FLAG_HOST 2u /* A, B and the outputs are host pointers; implies RG_FLAG_SYNC */
+#define RG_FLAG_TRANS_B 4u /* B is given transposed: [N][K] (limbs [N][K][lb]); the product is A * B^T,
+                              without a transposed copy ("enclosure-gemm", Usage: mm_enclose_nt) */
 
 /* Operations, for rg_workspace_bytes() and rg_workspace_layout(). */
 #define RG_OP_I64 0
@@ -137,7 +139,8 @@ int enclose_gemm_f64(const double* A, const double* B, double* lo, double* hi, i
  * ("exact-solve", Method: per-prime products as one batched GEMM.)
  *
  * RA: fp16 bit patterns [nprimes][M][lda], lda >= K, lda % 8 == 0.
- * RB: fp16 bit patterns [nprimes][K][ldb], ldb >= N, ldb % 64 == 0.
+ * RB: fp16 bit patterns [nprimes][K][ldb], ldb >= N, ldb % 64 == 0; with
+ *     RG_FLAG_TRANS_B, [nprimes][N][ldb], ldb >= K, ldb % 8 == 0.
  * RC: uint8 [nprimes][M][ldc], ldc >= N, ldc % 16 == 0.
  * Every residue must be an integer in [-125, 125]; RA columns k >= K and RB
  * columns n >= N are not read.  ws needs rg_workspace_bytes(RG_OP_STAGE, ...).
@@ -180,7 +183,8 @@ size_t rg_noalloc_scratch_bytes(void);
  * Workspace size in bytes for one call of `op` (RG_OP_*) with these shapes.
  * la, lb, lc are the limb counts (1 for RG_OP_I64 / RG_OP_ENCLOSE); nprimes
  * is the value the call will pass (0 = plan on the device).  flags must
- * match the call's RG_FLAG_HOST bit.  Returns 0 for invalid arguments.
+ * match the call's RG_FLAG_HOST and RG_FLAG_TRANS_B bits.  Returns 0 for
+ * invalid arguments.
  */
 size_t rg_workspace_bytes(int op, int64_t M, int64_t N, int64_t K, int la, int lb, int lc, int nprimes,
                           unsigned flags);
@@ -188,7 +192,8 @@ size_t rg_workspace_bytes(int op, int64_t M, int64_t N, int64_t K, int la, int l
 /* Offsets (bytes from ws) of the stage buffers a call leaves in its
  * workspace, for inspection:
  *   ra: fp16 residues of A, [pmax][M][lda]   (lda = K rounded up to 8)
- *   rb: fp16 residues of B, [pmax][K][ldb]   (ldb = N rounded up to 64)
+ *   rb: fp16 residues of B, [pmax][K][ldb]   (ldb = N rounded up to 64), or
+ *       [pmax][N][ldb] with RG_FLAG_TRANS_B    (ldb = K rounded up to 8)
  *   rc: uint8 product residues, [pmax][M][ldc] (ldc = N rounded up to 16)
  * Residue planes follow the prime order q_0 = 251, q_1 = 241, ... */
 typedef struct {

@@ -20,6 +20,15 @@ def rg():
     return library()
 
 
+@pytest.fixture(params=[1, 2], ids=["single_cta", "cta_pair"])
+def variant(rg, request):
+    """Runs the test on the single-CTA and on the CTA-pair tensor-core kernel."""
+    lib = rg.library()
+    old = lib.rg_set_gemm_variant(request.param)
+    yield request.param
+    lib.rg_set_gemm_variant(old)
+
+
 def dev(x):
     return torch.from_numpy(np.ascontiguousarray(x)).cuda()
 

@@ -10,18 +10,9 @@ import numpy as np
 import pytest
 import torch
 
-from tests.gpu_util import host, rg  # noqa: F401
+from tests.gpu_util import host, rg, variant  # noqa: F401
 
 pytestmark = pytest.mark.gpu
-
-
-@pytest.fixture(params=[1, 2], ids=["single_cta", "cta_pair"])
-def variant(rg, request):
-    """Runs the test on the single-CTA and on the CTA-pair tensor-core kernel."""
-    lib = rg.library()
-    old = lib.rg_set_gemm_variant(request.param)
-    yield request.param
-    lib.rg_set_gemm_variant(old)
 
 
 def expected(ra, rb, ps):
@@ -32,15 +23,19 @@ def expected(ra, rb, ps):
     return np.stack(out)
 
 
-def run_stage(rg, ra, rb, M, N, K):
+def run_stage(rg, ra, rb, M, N, K, transb=False):
+    """rb is [P, K, N]; with transb it is handed to the kernel as [P, N, K]."""
     P = ra.shape[0]
     lda = (K + 7) // 8 * 8
-    ldb = (N + 63) // 64 * 64
     RA = torch.zeros((P, M, lda), dtype=torch.float16)
-    RB = torch.zeros((P, K, ldb), dtype=torch.float16)
     RA[:, :, :K] = torch.from_numpy(ra.astype(np.float16))
-    RB[:, :, :N] = torch.from_numpy(rb.astype(np.float16))
-    RC = rg.res_gemm_stage(RA.cuda(), RB.cuda(), P, M, N, K)
+    if transb:
+        RB = torch.zeros((P, N, lda), dtype=torch.float16)
+        RB[:, :, :K] = torch.from_numpy(np.ascontiguousarray(np.swapaxes(rb, 1, 2)).astype(np.float16))
+    else:
+        RB = torch.zeros((P, K, (N + 63) // 64 * 64), dtype=torch.float16)
+        RB[:, :, :N] = torch.from_numpy(rb.astype(np.float16))
+    RC = rg.res_gemm_stage(RA.cuda(), RB.cuda(), P, M, N, K, transb=transb)
     return host(RC)[:, :, :N].astype(np.int64)
 
 
@@ -90,6 +85,17 @@ def test_k_tails_all_primes(rg, variant, K):
     ra, rb = patterns("random_extreme", P, M, N, K, rng)
     got = run_stage(rg, ra, rb, M, N, K)
     assert np.array_equal(got, expected(ra, rb, rg.primes()))
+
+
+@pytest.mark.parametrize("kind", ["signs", "random_extreme"])
+@pytest.mark.parametrize("M,N,K", [(129, 257, 1025), (40, 70, 2**15 + 8), (256, 512, 64)])
+def test_k_major_b(rg, variant, kind, M, N, K):
+    """B handed over K-major ([P, N, K]): the same residues as the N-major layout."""
+    P = 5
+    rng = np.random.default_rng(M + N + K)
+    ra, rb = patterns(kind, P, M, N, K, rng)
+    got = run_stage(rg, ra, rb, M, N, K, transb=True)
+    assert np.array_equal(got, expected(ra, rb, rg.primes()[:P]))
 
 
 def test_wait_expiry_returns_timeout(rg, variant):
