@@ -46,6 +46,8 @@ EXPORTED = (
     "res_gemm_i64", "res_gemm_limbs", "enclose_gemm_f64", "res_gemm_stage", "rg_workspace_bytes",
     "rg_workspace_layout", "rg_get_plan", "rg_status", "rg_prime", "rg_strerror", "rg_set_wait_limit_ns",
     "rg_inject_fault", "res_gemm_i64_noalloc", "rg_noalloc_scratch_bytes", "rg_set_gemm_variant",
+    "res_gemm_i64_batched", "res_gemm_limbs_batched", "enclose_gemm_f64_batched", "rg_workspace_bytes_batched",
+    "rg_workspace_layout_batched",
 )
 
 
@@ -90,12 +92,21 @@ def library():
             lib.res_gemm_limbs.argtypes = [vp, ci, vp, ci, vp, ci, i64, i64, i64, ci, cu, vp, sz, vp]
             lib.enclose_gemm_f64.argtypes = [vp, vp, vp, vp, i64, i64, i64, cu, vp, sz, vp]
             lib.res_gemm_stage.argtypes = [vp, i64, vp, i64, vp, i64, ci, i64, i64, i64, cu, vp, sz, vp]
-            for f in ("res_gemm_i64", "res_gemm_limbs", "enclose_gemm_f64", "res_gemm_stage"):
+            lib.res_gemm_i64_batched.argtypes = [vp, vp, vp, i64, i64, i64, i64, ci, cu, vp, sz, vp]
+            lib.res_gemm_limbs_batched.argtypes = [vp, ci, vp, ci, vp, ci, i64, i64, i64, i64, ci, cu, vp, sz, vp]
+            lib.enclose_gemm_f64_batched.argtypes = [vp, vp, vp, vp, i64, i64, i64, i64, cu, vp, sz, vp]
+            for f in ("res_gemm_i64", "res_gemm_limbs", "enclose_gemm_f64", "res_gemm_stage", "res_gemm_i64_batched",
+                      "res_gemm_limbs_batched", "enclose_gemm_f64_batched"):
                 getattr(lib, f).restype = ci
             lib.rg_workspace_bytes.argtypes = [ci, i64, i64, i64, ci, ci, ci, ci, cu]
             lib.rg_workspace_bytes.restype = sz
+            lib.rg_workspace_bytes_batched.argtypes = [ci, i64, i64, i64, i64, ci, ci, ci, ci, cu]
+            lib.rg_workspace_bytes_batched.restype = sz
             lib.rg_workspace_layout.argtypes = [ci, i64, i64, i64, ci, ci, ci, ci, cu, ctypes.POINTER(Layout)]
             lib.rg_workspace_layout.restype = ci
+            lib.rg_workspace_layout_batched.argtypes = [ci, i64, i64, i64, i64, ci, ci, ci, ci, cu,
+                                                        ctypes.POINTER(Layout)]
+            lib.rg_workspace_layout_batched.restype = ci
             lib.rg_get_plan.argtypes = [vp, vp, ctypes.POINTER(PlanInfo)]
             lib.rg_get_plan.restype = ci
             lib.rg_status.argtypes = [vp, vp]
@@ -127,14 +138,15 @@ def _layout_flags(host, transb):
     return (RG_FLAG_HOST if host else 0) | (RG_FLAG_TRANS_B if transb else 0)
 
 
-def workspace_bytes(op, M, N, K, la=1, lb=1, lc=1, nprimes=0, host=False, transb=False) -> int:
-    return int(library().rg_workspace_bytes(op, M, N, K, la, lb, lc, nprimes, _layout_flags(host, transb)))
+def workspace_bytes(op, M, N, K, la=1, lb=1, lc=1, nprimes=0, host=False, transb=False, batch=1) -> int:
+    return int(library().rg_workspace_bytes_batched(op, batch, M, N, K, la, lb, lc, nprimes,
+                                                    _layout_flags(host, transb)))
 
 
-def workspace_layout(op, M, N, K, la=1, lb=1, lc=1, nprimes=0, host=False, transb=False) -> Layout:
+def workspace_layout(op, M, N, K, la=1, lb=1, lc=1, nprimes=0, host=False, transb=False, batch=1) -> Layout:
     out = Layout()
-    rc = library().rg_workspace_layout(op, M, N, K, la, lb, lc, nprimes, _layout_flags(host, transb),
-                                       ctypes.byref(out))
+    rc = library().rg_workspace_layout_batched(op, batch, M, N, K, la, lb, lc, nprimes, _layout_flags(host, transb),
+                                               ctypes.byref(out))
     if rc:
         raise ResGemmError(rc, "rg_workspace_layout")
     return out
@@ -184,30 +196,51 @@ def _check(rc, where):
         raise ResGemmError(rc, where)
 
 
+def _shapes(A, B, transb, core):
+    """(batch, M, N, K, la, lb) of operands with `core` trailing dims per entry
+    (0 for int64/float64 matrices, 1 for limb vectors), batched when they have one
+    more leading dimension."""
+    if A.dim() != B.dim() or A.dim() not in (2 + core, 3 + core):
+        return None
+    batched = A.dim() == 3 + core
+    if batched and A.shape[0] != B.shape[0]:
+        return None
+    a, b = A.shape[int(batched):], B.shape[int(batched):]
+    M, K = a[0], a[1]
+    N, Kb = (b[0], b[1]) if transb else (b[1], b[0])
+    if K != Kb:
+        return None
+    batch = A.shape[0] if batched else 1
+    return batched, batch, M, N, K, (a[2] if core else 1), (b[2] if core else 1)
+
+
+def _prepare(A, B, sync, transb):
+    A, B = A.contiguous(), B.contiguous()
+    dev, flags = _call_ctx(A, B)
+    flags |= (RG_FLAG_SYNC if sync else 0) | (RG_FLAG_TRANS_B if transb else 0)
+    return A, B, dev, flags
+
+
 def res_gemm_i64(A: torch.Tensor, B: torch.Tensor, nprimes: int = 0, sync: bool = True, out=None,
                  ws: torch.Tensor | None = None, transb: bool = False) -> torch.Tensor:
     """Exact C = A @ B for int64 matrices (CUDA tensors, or CPU tensors staged through the device).
-    With transb, B is given as [N, K] and C = A @ B.T, without a transposed copy."""
-    if A.dtype != torch.int64 or B.dtype != torch.int64 or A.dim() != 2 or B.dim() != 2 or \
-            A.shape[1] != B.shape[1 if transb else 0]:
-        raise ValueError("A [M,K] and B [K,N] (transb: [N,K]) int64 expected")
-    A, B = A.contiguous(), B.contiguous()
-    M, K = A.shape
-    N = B.shape[0 if transb else 1]
-    dev, flags = _call_ctx(A, B)
-    if sync:
-        flags |= RG_FLAG_SYNC
-    if transb:
-        flags |= RG_FLAG_TRANS_B
-    C = out if out is not None else torch.empty((M, N), dtype=torch.int64, device=A.device,
-                                                pin_memory=bool(flags & RG_FLAG_HOST))
+    With transb, B is given as [N, K] and C = A @ B.T, without a transposed copy.  A [b, M, K] and
+    B [b, K, N] run as one batched call with one plan."""
+    sh = _shapes(A, B, transb, 0) if A.dtype == torch.int64 and B.dtype == torch.int64 else None
+    if sh is None:
+        raise ValueError("A [M,K] and B [K,N] (transb: [N,K]) int64 expected, optionally with a batch dimension")
+    batched, batch, M, N, K, _, _ = sh
+    A, B, dev, flags = _prepare(A, B, sync, transb)
+    host = bool(flags & RG_FLAG_HOST)
+    shape = (batch, M, N) if batched else (M, N)
+    C = out if out is not None else torch.empty(shape, dtype=torch.int64, device=A.device, pin_memory=host)
     with torch.cuda.device(dev):
-        need = workspace_bytes(RG_OP_I64, M, N, K, nprimes=nprimes, host=bool(flags & RG_FLAG_HOST), transb=transb)
+        need = workspace_bytes(RG_OP_I64, M, N, K, nprimes=nprimes, host=host, transb=transb, batch=batch)
         if need == 0:
             raise ResGemmError(RG_ERR_ARG, "res_gemm_i64")
         w = ws if ws is not None else workspace(need, dev)
-        rc = library().res_gemm_i64(A.data_ptr(), B.data_ptr(), C.data_ptr(), M, N, K, nprimes, flags,
-                                    w.data_ptr(), w.numel(), torch.cuda.current_stream(dev).cuda_stream)
+        rc = library().res_gemm_i64_batched(A.data_ptr(), B.data_ptr(), C.data_ptr(), batch, M, N, K, nprimes, flags,
+                                            w.data_ptr(), w.numel(), torch.cuda.current_stream(dev).cuda_stream)
     _check(rc, "res_gemm_i64")
     return C
 
@@ -215,28 +248,24 @@ def res_gemm_i64(A: torch.Tensor, B: torch.Tensor, nprimes: int = 0, sync: bool 
 def res_gemm_limbs(A: torch.Tensor, B: torch.Tensor, lc: int, nprimes: int = 0, sync: bool = True, out=None,
                    ws: torch.Tensor | None = None, transb: bool = False) -> torch.Tensor:
     """Exact C = A @ B for multi-limb int64 operands A [M,K,la], B [K,N,lb]; returns [M,N,lc].
-    With transb, B is given as [N,K,lb] and C = A @ B.T."""
-    if A.dtype != torch.int64 or B.dtype != torch.int64 or A.dim() != 3 or B.dim() != 3 or \
-            A.shape[1] != B.shape[1 if transb else 0]:
-        raise ValueError("A [M,K,la] and B [K,N,lb] (transb: [N,K,lb]) int64 expected")
-    A, B = A.contiguous(), B.contiguous()
-    M, K, la = A.shape
-    N, lb = B.shape[0 if transb else 1], B.shape[2]
-    dev, flags = _call_ctx(A, B)
-    if sync:
-        flags |= RG_FLAG_SYNC
-    if transb:
-        flags |= RG_FLAG_TRANS_B
-    C = out if out is not None else torch.empty((M, N, lc), dtype=torch.int64, device=A.device,
-                                                pin_memory=bool(flags & RG_FLAG_HOST))
+    With transb, B is given as [N,K,lb] and C = A @ B.T.  A leading batch dimension runs one
+    batched call with one plan."""
+    sh = _shapes(A, B, transb, 1) if A.dtype == torch.int64 and B.dtype == torch.int64 else None
+    if sh is None:
+        raise ValueError("A [M,K,la] and B [K,N,lb] (transb: [N,K,lb]) int64 expected, optionally batched")
+    batched, batch, M, N, K, la, lb = sh
+    A, B, dev, flags = _prepare(A, B, sync, transb)
+    host = bool(flags & RG_FLAG_HOST)
+    shape = (batch, M, N, lc) if batched else (M, N, lc)
+    C = out if out is not None else torch.empty(shape, dtype=torch.int64, device=A.device, pin_memory=host)
     with torch.cuda.device(dev):
-        need = workspace_bytes(RG_OP_LIMBS, M, N, K, la, lb, lc, nprimes, host=bool(flags & RG_FLAG_HOST),
-                               transb=transb)
+        need = workspace_bytes(RG_OP_LIMBS, M, N, K, la, lb, lc, nprimes, host=host, transb=transb, batch=batch)
         if need == 0:
             raise ResGemmError(RG_ERR_ARG, "res_gemm_limbs")
         w = ws if ws is not None else workspace(need, dev)
-        rc = library().res_gemm_limbs(A.data_ptr(), la, B.data_ptr(), lb, C.data_ptr(), lc, M, N, K, nprimes, flags,
-                                      w.data_ptr(), w.numel(), torch.cuda.current_stream(dev).cuda_stream)
+        rc = library().res_gemm_limbs_batched(A.data_ptr(), la, B.data_ptr(), lb, C.data_ptr(), lc, batch, M, N, K,
+                                              nprimes, flags, w.data_ptr(), w.numel(),
+                                              torch.cuda.current_stream(dev).cuda_stream)
     _check(rc, "res_gemm_limbs")
     return C
 
@@ -244,28 +273,25 @@ def res_gemm_limbs(A: torch.Tensor, B: torch.Tensor, lc: int, nprimes: int = 0, 
 def enclose_gemm_f64(A: torch.Tensor, B: torch.Tensor, sync: bool = True, ws: torch.Tensor | None = None,
                      transb: bool = False):
     """(lo, hi) float64 with lo <= A @ B <= hi entrywise in exact arithmetic.
-    With transb, B is given as [N, K] and the bracket is of A @ B.T."""
-    if A.dtype != torch.float64 or B.dtype != torch.float64 or A.dim() != 2 or B.dim() != 2 or \
-            A.shape[1] != B.shape[1 if transb else 0]:
-        raise ValueError("A [M,K] and B [K,N] (transb: [N,K]) float64 expected")
-    A, B = A.contiguous(), B.contiguous()
-    M, K = A.shape
-    N = B.shape[0 if transb else 1]
-    dev, flags = _call_ctx(A, B)
-    if sync:
-        flags |= RG_FLAG_SYNC
-    if transb:
-        flags |= RG_FLAG_TRANS_B
+    With transb, B is given as [N, K] and the bracket is of A @ B.T.  A [b, M, K] and B [b, K, N]
+    run as one batched call sharing one plan."""
+    sh = _shapes(A, B, transb, 0) if A.dtype == torch.float64 and B.dtype == torch.float64 else None
+    if sh is None:
+        raise ValueError("A [M,K] and B [K,N] (transb: [N,K]) float64 expected, optionally with a batch dimension")
+    batched, batch, M, N, K, _, _ = sh
+    A, B, dev, flags = _prepare(A, B, sync, transb)
     pin = bool(flags & RG_FLAG_HOST)
-    lo = torch.empty((M, N), dtype=torch.float64, device=A.device, pin_memory=pin)
-    hi = torch.empty((M, N), dtype=torch.float64, device=A.device, pin_memory=pin)
+    shape = (batch, M, N) if batched else (M, N)
+    lo = torch.empty(shape, dtype=torch.float64, device=A.device, pin_memory=pin)
+    hi = torch.empty(shape, dtype=torch.float64, device=A.device, pin_memory=pin)
     with torch.cuda.device(dev):
-        need = workspace_bytes(RG_OP_ENCLOSE, M, N, K, host=pin, transb=transb)
+        need = workspace_bytes(RG_OP_ENCLOSE, M, N, K, host=pin, transb=transb, batch=batch)
         if need == 0:
             raise ResGemmError(RG_ERR_ARG, "enclose_gemm_f64")
         w = ws if ws is not None else workspace(need, dev)
-        rc = library().enclose_gemm_f64(A.data_ptr(), B.data_ptr(), lo.data_ptr(), hi.data_ptr(), M, N, K, flags,
-                                        w.data_ptr(), w.numel(), torch.cuda.current_stream(dev).cuda_stream)
+        rc = library().enclose_gemm_f64_batched(A.data_ptr(), B.data_ptr(), lo.data_ptr(), hi.data_ptr(), batch, M,
+                                                N, K, flags, w.data_ptr(), w.numel(),
+                                                torch.cuda.current_stream(dev).cuda_stream)
     _check(rc, "enclose_gemm_f64")
     return lo, hi
 
@@ -278,6 +304,14 @@ def mm_enclose(A: torch.Tensor, B: torch.Tensor):
 def mm_enclose_nt(A: torch.Tensor, Bt: torch.Tensor):
     """The bracket of A @ Bt.T without a transposed copy ("enclosure-gemm", Usage: mm_enclose_nt)."""
     return enclose_gemm_f64(A, Bt, transb=True)
+
+
+def bmm_enclose(A: torch.Tensor, B: torch.Tensor):
+    """Brackets of the batch A [b, M, K] @ B [b, K, N] with one shared plan
+    ("enclosure-gemm", Usage: bmm_enclose)."""
+    if A.dim() != 3 or B.dim() != 3:
+        raise ValueError("A [b,M,K] and B [b,K,N] expected")
+    return enclose_gemm_f64(A, B)
 
 
 def res_gemm_stage(RA: torch.Tensor, RB: torch.Tensor, nprimes: int, M: int, N: int, K: int, RC=None,

@@ -61,9 +61,12 @@ struct Layout {
   int pmax;
 };
 
-bool make_layout(int op, long long M, long long N, long long K, int la, int lb, int lc, int nprimes, unsigned flags,
-                 Layout* L) {
-  if (M <= 0 || N <= 0 || K <= 0) return false;
+// An empty problem (batch, M, N or K zero) needs only the plan block.
+bool is_empty(long long batch, long long M, long long N, long long K) { return !batch || !M || !N || !K; }
+
+bool make_layout(int op, long long batch, long long M, long long N, long long K, int la, int lb, int lc, int nprimes,
+                 unsigned flags, Layout* L) {
+  if (batch < 0 || M < 0 || N < 0 || K < 0) return false;
   if (nprimes < 0 || nprimes > kNumPrimes) return false;
   if (op == RG_OP_LIMBS && (la < 1 || la > RG_MAX_LIMBS_IN || lb < 1 || lb > RG_MAX_LIMBS_IN || lc < 1 ||
                             lc > RG_MAX_LIMBS_OUT))
@@ -76,7 +79,7 @@ bool make_layout(int op, long long M, long long N, long long K, int la, int lb, 
   L->ldc = round_up(N, 16);
   L->plan = 0;
   size_t off = kPlanBytes;
-  if (op == RG_OP_STAGE) {
+  if (op == RG_OP_STAGE || is_empty(batch, M, N, K)) {
     L->total = off;
     L->pmax = nprimes;
     return true;
@@ -84,23 +87,23 @@ bool make_layout(int op, long long M, long long N, long long K, int la, int lb, 
   int pmax = pmax_for(op, K, la, lb, nprimes);
   L->pmax = pmax;
   L->ra = off;
-  off = align_up(off + (size_t)pmax * M * L->lda * 2, kAlign);
+  off = align_up(off + (size_t)pmax * batch * M * L->lda * 2, kAlign);
   L->rb = off;
-  off = align_up(off + (size_t)pmax * (transb ? N : K) * L->ldb * 2, kAlign);
+  off = align_up(off + (size_t)pmax * batch * (transb ? N : K) * L->ldb * 2, kAlign);
   L->rc = off;
-  off = align_up(off + (size_t)pmax * M * L->ldc, kAlign);
+  off = align_up(off + (size_t)pmax * batch * M * L->ldc, kAlign);
   if (flags & RG_FLAG_HOST) {
     size_t ea = op == RG_OP_LIMBS ? 8 * (size_t)la : 8, eb = op == RG_OP_LIMBS ? 8 * (size_t)lb : 8;
     size_t ec = op == RG_OP_LIMBS ? 8 * (size_t)lc : 8;
     L->a = off;
-    off = align_up(off + (size_t)M * K * ea, kAlign);
+    off = align_up(off + (size_t)batch * M * K * ea, kAlign);
     L->b = off;
-    off = align_up(off + (size_t)K * N * eb, kAlign);
+    off = align_up(off + (size_t)batch * K * N * eb, kAlign);
     L->c = off;
-    off = align_up(off + (size_t)M * N * ec, kAlign);
+    off = align_up(off + (size_t)batch * M * N * ec, kAlign);
     if (op == RG_OP_ENCLOSE) {
       L->c2 = off;
-      off = align_up(off + (size_t)M * N * 8, kAlign);
+      off = align_up(off + (size_t)batch * M * N * 8, kAlign);
     }
   }
   L->total = off;
@@ -122,26 +125,46 @@ int finish(void* ws, cudaStream_t s, unsigned flags) {
     if (e_ != cudaSuccess) return RG_ERR_CUDA; \
   } while (0)
 
-// Shared driver for the three integer/fp64 entry points.
-int run(int op, const void* A, int la, const void* B, int lb, void* C, void* C2, int lc, long long M, long long N,
-        long long K, int nprimes, unsigned flags, void* ws, size_t ws_bytes, void* stream) {
-  if (!A || !B || !C || !ws || (op == RG_OP_ENCLOSE && !C2)) return RG_ERR_ARG;
-  if ((reinterpret_cast<uintptr_t>(ws) & 255u) != 0) return RG_ERR_ARG;
-  if (M <= 0 || N <= 0 || K <= 0 || nprimes < 0 || nprimes > kNumPrimes) return RG_ERR_ARG;
+// Shared driver for the integer/fp64 entry points; `batch` products of the
+// same shape share one plan (one prime count, one pair of scale exponents).
+int run(int op, const void* A, int la, const void* B, int lb, void* C, void* C2, int lc, long long batch, long long M,
+        long long N, long long K, int nprimes, unsigned flags, void* ws, size_t ws_bytes, void* stream) {
+  if (!ws || (reinterpret_cast<uintptr_t>(ws) & 255u) != 0) return RG_ERR_ARG;
+  if (batch < 0 || M < 0 || N < 0 || K < 0 || nprimes < 0 || nprimes > kNumPrimes) return RG_ERR_ARG;
+  // an empty problem reads no operand, and writes outputs only if it has entries
+  const bool empty = is_empty(batch, M, N, K), has_out = batch && M && N;
+  if ((!empty && (!A || !B)) || (has_out && (!C || (op == RG_OP_ENCLOSE && !C2)))) return RG_ERR_ARG;
   if (op == RG_OP_LIMBS &&
       (la < 1 || la > RG_MAX_LIMBS_IN || lb < 1 || lb > RG_MAX_LIMBS_IN || lc < 1 || lc > RG_MAX_LIMBS_OUT))
     return RG_ERR_ARG;
   if (K > RG_MAX_K) return RG_ERR_RANGE;
-  if (M > (1LL << 31) - 1 || N > (1LL << 31) - 1) return RG_ERR_ARG;
+  if (M > (1LL << 31) - 1 || N > (1LL << 31) - 1 || batch > (1LL << 31) - 1) return RG_ERR_ARG;
   Layout L;
-  if (!make_layout(op, M, N, K, la, lb, lc, nprimes, flags, &L)) return RG_ERR_ARG;
+  if (!make_layout(op, batch, M, N, K, la, lb, lc, nprimes, flags, &L)) return RG_ERR_ARG;
   if (ws_bytes < L.total) return RG_ERR_WORKSPACE;
+  // the persistent GEMM numbers its tiles (plane, row block, column block) in int
+  if ((long long)L.pmax * batch * ((M + 127) / 128) * ((N + 255) / 256) > (1LL << 31) - 1) return RG_ERR_ARG;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
-  RG_TRY(upload_tables());
   uint8_t* w = static_cast<uint8_t*>(ws);
   DevPlan* plan = reinterpret_cast<DevPlan*>(w + L.plan);
   const size_t ea = op == RG_OP_LIMBS ? 8 * (size_t)la : 8, eb = op == RG_OP_LIMBS ? 8 * (size_t)lb : 8;
   const size_t ec = op == RG_OP_LIMBS ? 8 * (size_t)lc : 8;
+  const size_t out_bytes = (size_t)batch * M * N * ec;
+  if (empty) {
+    // Nothing to multiply; an empty sum is exactly zero (lo = hi = +0).
+    RG_TRY(cudaMemsetAsync(plan, 0, sizeof(DevPlan), s));
+    if (out_bytes) {
+      if (flags & RG_FLAG_HOST) {
+        std::memset(C, 0, out_bytes);
+        if (op == RG_OP_ENCLOSE) std::memset(C2, 0, out_bytes);
+      } else {
+        RG_TRY(cudaMemsetAsync(C, 0, out_bytes, s));
+        if (op == RG_OP_ENCLOSE) RG_TRY(cudaMemsetAsync(C2, 0, out_bytes, s));
+      }
+    }
+    return finish(ws, s, flags);
+  }
+  RG_TRY(upload_tables());
   const void* dA = A;
   const void* dB = B;
   void* dC = C;
@@ -151,8 +174,8 @@ int run(int op, const void* A, int la, const void* B, int lb, void* C, void* C2,
     dB = w + L.b;
     dC = w + L.c;
     dC2 = op == RG_OP_ENCLOSE ? static_cast<void*>(w + L.c2) : nullptr;
-    RG_TRY(cudaMemcpyAsync(const_cast<void*>(dA), A, (size_t)M * K * ea, cudaMemcpyHostToDevice, s));
-    RG_TRY(cudaMemcpyAsync(const_cast<void*>(dB), B, (size_t)K * N * eb, cudaMemcpyHostToDevice, s));
+    RG_TRY(cudaMemcpyAsync(const_cast<void*>(dA), A, (size_t)batch * M * K * ea, cudaMemcpyHostToDevice, s));
+    RG_TRY(cudaMemcpyAsync(const_cast<void*>(dB), B, (size_t)batch * K * N * eb, cudaMemcpyHostToDevice, s));
   }
   RG_TRY(cudaMemsetAsync(plan, 0, sizeof(DevPlan), s));
   const int la1 = op == RG_OP_LIMBS ? la : 1, lb1 = op == RG_OP_LIMBS ? lb : 1, lc1 = op == RG_OP_LIMBS ? lc : 1;
@@ -160,17 +183,20 @@ int run(int op, const void* A, int la, const void* B, int lb, void* C, void* C2,
   // plan; the other operations run the planner kernel first
   const bool i64 = op == RG_OP_I64;
   if (!i64)
-    RG_TRY(launch_plan(op, dA, M * K, la1, dB, K * N, lb1, lc1, K, op == RG_OP_ENCLOSE ? 0 : nprimes, plan, s));
+    RG_TRY(launch_plan(op, dA, batch * M * K, la1, dB, batch * K * N, lb1, lc1, K, op == RG_OP_ENCLOSE ? 0 : nprimes,
+                       plan, s));
   const bool transb = (flags & RG_FLAG_TRANS_B) != 0;
-  RG_TRY(launch_split(op, dA, dB, la1, lb1, M, N, K, L.lda, L.ldb, w + L.ra, w + L.rb, plan, L.pmax, transb, s));
+  RG_TRY(launch_split(op, dA, dB, la1, lb1, batch, M, N, K, L.lda, L.ldb, w + L.ra, w + L.rb, plan, L.pmax, transb,
+                      s));
   int fault = g_fault.exchange(0);
-  RG_TRY(launch_gemm(w + L.ra, L.lda, w + L.rb, L.ldb, w + L.rc, L.ldc, L.pmax, i64 ? nprimes : 0, M, N, K, plan, s,
-                     fault, g_wait_ns.load(), i64, transb));
-  RG_TRY(launch_garner(op, w + L.rc, L.ldc, (long long)M * L.ldc, M, N, K, op == RG_OP_LIMBS ? lc : 1, plan, dC, dC2,
-                       s));
+  RG_TRY(launch_gemm(w + L.ra, L.lda, w + L.rb, L.ldb, w + L.rc, L.ldc, L.pmax, (int)batch, i64 ? nprimes : 0, M, N,
+                     K, plan, s, fault, g_wait_ns.load(), i64, transb));
+  // Garner sees the batch as batch * M rows of one plane per prime
+  RG_TRY(launch_garner(op, w + L.rc, L.ldc, batch * M * L.ldc, batch * M, N, K, op == RG_OP_LIMBS ? lc : 1, plan, dC,
+                       dC2, s));
   if (flags & RG_FLAG_HOST) {
-    RG_TRY(cudaMemcpyAsync(C, dC, (size_t)M * N * ec, cudaMemcpyDeviceToHost, s));
-    if (op == RG_OP_ENCLOSE) RG_TRY(cudaMemcpyAsync(C2, dC2, (size_t)M * N * 8, cudaMemcpyDeviceToHost, s));
+    RG_TRY(cudaMemcpyAsync(C, dC, out_bytes, cudaMemcpyDeviceToHost, s));
+    if (op == RG_OP_ENCLOSE) RG_TRY(cudaMemcpyAsync(C2, dC2, out_bytes, cudaMemcpyDeviceToHost, s));
   }
   return finish(ws, s, flags);
 }
@@ -181,17 +207,33 @@ extern "C" {
 
 int res_gemm_i64(const int64_t* A, const int64_t* B, int64_t* C, int64_t M, int64_t N, int64_t K, int nprimes,
                  unsigned flags, void* ws, size_t ws_bytes, void* stream) {
-  return run(RG_OP_I64, A, 1, B, 1, C, nullptr, 1, M, N, K, nprimes, flags, ws, ws_bytes, stream);
+  return run(RG_OP_I64, A, 1, B, 1, C, nullptr, 1, 1, M, N, K, nprimes, flags, ws, ws_bytes, stream);
 }
 
 int res_gemm_limbs(const int64_t* A, int la, const int64_t* B, int lb, int64_t* C, int lc, int64_t M, int64_t N,
                    int64_t K, int nprimes, unsigned flags, void* ws, size_t ws_bytes, void* stream) {
-  return run(RG_OP_LIMBS, A, la, B, lb, C, nullptr, lc, M, N, K, nprimes, flags, ws, ws_bytes, stream);
+  return run(RG_OP_LIMBS, A, la, B, lb, C, nullptr, lc, 1, M, N, K, nprimes, flags, ws, ws_bytes, stream);
 }
 
 int enclose_gemm_f64(const double* A, const double* B, double* lo, double* hi, int64_t M, int64_t N, int64_t K,
                      unsigned flags, void* ws, size_t ws_bytes, void* stream) {
-  return run(RG_OP_ENCLOSE, A, 1, B, 1, lo, hi, 1, M, N, K, 0, flags, ws, ws_bytes, stream);
+  return run(RG_OP_ENCLOSE, A, 1, B, 1, lo, hi, 1, 1, M, N, K, 0, flags, ws, ws_bytes, stream);
+}
+
+int res_gemm_i64_batched(const int64_t* A, const int64_t* B, int64_t* C, int64_t batch, int64_t M, int64_t N,
+                         int64_t K, int nprimes, unsigned flags, void* ws, size_t ws_bytes, void* stream) {
+  return run(RG_OP_I64, A, 1, B, 1, C, nullptr, 1, batch, M, N, K, nprimes, flags, ws, ws_bytes, stream);
+}
+
+int res_gemm_limbs_batched(const int64_t* A, int la, const int64_t* B, int lb, int64_t* C, int lc, int64_t batch,
+                           int64_t M, int64_t N, int64_t K, int nprimes, unsigned flags, void* ws, size_t ws_bytes,
+                           void* stream) {
+  return run(RG_OP_LIMBS, A, la, B, lb, C, nullptr, lc, batch, M, N, K, nprimes, flags, ws, ws_bytes, stream);
+}
+
+int enclose_gemm_f64_batched(const double* A, const double* B, double* lo, double* hi, int64_t batch, int64_t M,
+                             int64_t N, int64_t K, unsigned flags, void* ws, size_t ws_bytes, void* stream) {
+  return run(RG_OP_ENCLOSE, A, 1, B, 1, lo, hi, 1, batch, M, N, K, 0, flags, ws, ws_bytes, stream);
 }
 
 int res_gemm_stage(const uint16_t* RA, int64_t lda, const uint16_t* RB, int64_t ldb, uint8_t* RC, int64_t ldc,
@@ -211,24 +253,29 @@ int res_gemm_stage(const uint16_t* RA, int64_t lda, const uint16_t* RB, int64_t 
   DevPlan* plan = static_cast<DevPlan*>(ws);
   RG_TRY(cudaMemsetAsync(plan, 0, sizeof(DevPlan), s));
   int fault = g_fault.exchange(0);
-  RG_TRY(launch_gemm(RA, lda, RB, ldb, RC, ldc, nprimes, nprimes, M, N, K, plan, s, fault, g_wait_ns.load(), false,
+  RG_TRY(launch_gemm(RA, lda, RB, ldb, RC, ldc, nprimes, 1, nprimes, M, N, K, plan, s, fault, g_wait_ns.load(), false,
                      transb));
   return finish(ws, s, flags);
 }
 
-size_t rg_workspace_bytes(int op, int64_t M, int64_t N, int64_t K, int la, int lb, int lc, int nprimes,
-                          unsigned flags) {
+size_t rg_workspace_bytes_batched(int op, int64_t batch, int64_t M, int64_t N, int64_t K, int la, int lb, int lc,
+                                  int nprimes, unsigned flags) {
   Layout L;
   if (op < RG_OP_I64 || op > RG_OP_STAGE) return 0;
-  if (!make_layout(op, M, N, K, la, lb, lc, nprimes, flags, &L)) return 0;
+  if (!make_layout(op, batch, M, N, K, la, lb, lc, nprimes, flags, &L)) return 0;
   return L.total;
 }
 
-int rg_workspace_layout(int op, int64_t M, int64_t N, int64_t K, int la, int lb, int lc, int nprimes,
-                        unsigned flags, rg_layout* out) {
+size_t rg_workspace_bytes(int op, int64_t M, int64_t N, int64_t K, int la, int lb, int lc, int nprimes,
+                          unsigned flags) {
+  return rg_workspace_bytes_batched(op, 1, M, N, K, la, lb, lc, nprimes, flags);
+}
+
+int rg_workspace_layout_batched(int op, int64_t batch, int64_t M, int64_t N, int64_t K, int la, int lb, int lc,
+                                int nprimes, unsigned flags, rg_layout* out) {
   Layout L;
   if (!out || op < RG_OP_I64 || op > RG_OP_STAGE) return RG_ERR_ARG;
-  if (!make_layout(op, M, N, K, la, lb, lc, nprimes, flags, &L)) return RG_ERR_ARG;
+  if (!make_layout(op, batch, M, N, K, la, lb, lc, nprimes, flags, &L)) return RG_ERR_ARG;
   out->ra = L.ra;
   out->rb = L.rb;
   out->rc = L.rc;
@@ -237,6 +284,11 @@ int rg_workspace_layout(int op, int64_t M, int64_t N, int64_t K, int la, int lb,
   out->ldc = L.ldc;
   out->pmax = L.pmax;
   return RG_OK;
+}
+
+int rg_workspace_layout(int op, int64_t M, int64_t N, int64_t K, int la, int lb, int lc, int nprimes,
+                        unsigned flags, rg_layout* out) {
+  return rg_workspace_layout_batched(op, 1, M, N, K, la, lb, lc, nprimes, flags, out);
 }
 
 int rg_get_plan(const void* ws, void* stream, rg_plan_info* out) {
@@ -323,10 +375,10 @@ extern "C" size_t rg_noalloc_scratch_bytes(void) { return kNoAllocScratchBytes; 
 extern "C" int res_gemm_i64_noalloc(const int64_t* A, const int64_t* B, int64_t* C, int64_t M, int64_t N, int64_t K,
                                     int nprimes, unsigned flags, void* stream) {
   Layout L;
-  if (!make_layout(RG_OP_I64, M, N, K, 1, 1, 1, nprimes, flags, &L)) return RG_ERR_ARG;
+  if (!make_layout(RG_OP_I64, 1, M, N, K, 1, 1, 1, nprimes, flags, &L)) return RG_ERR_ARG;
   if (L.total > kNoAllocScratchBytes) return RG_ERR_WORKSPACE;  // before any device work
   void* ws = nullptr;
   int rc = noalloc_scratch(&ws);
   if (rc != RG_OK) return rc;
-  return run(RG_OP_I64, A, 1, B, 1, C, nullptr, 1, M, N, K, nprimes, flags, ws, kNoAllocScratchBytes, stream);
+  return run(RG_OP_I64, A, 1, B, 1, C, nullptr, 1, 1, M, N, K, nprimes, flags, ws, kNoAllocScratchBytes, stream);
 }

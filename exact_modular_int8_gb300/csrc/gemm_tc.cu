@@ -66,6 +66,7 @@ struct GemmParams {
   int M, N, K;
   int mt, nt;
   int kb_total;
+  int batch;       // independent products per prime; plane = prime * batch + product
   int P_fixed;     // 0: read (or derive) the prime count from the plan
   int derive_i64;  // derive the int64 plan from max |A|, max |B|
   int ceil_log2_k;
@@ -271,13 +272,15 @@ __device__ __forceinline__ void final_residues(const uint32_t (&r)[32], const ui
 // Byte offset of (row, 16-byte chunk j) in a 128-row x 128-byte swizzled half.
 __device__ __forceinline__ uint32_t sw128_off(int row, int j) { return (uint32_t)(row * 128 + ((j ^ (row & 7)) << 4)); }
 
+// p: the residue plane (prime-major, then product of the batch); pr: its prime.
 struct TileCoord {
-  int p, m, n;
+  int p, pr, m, n;
 };
-__device__ __forceinline__ TileCoord tile_coord(int t, int mt, int nt) {
+__device__ __forceinline__ TileCoord tile_coord(int t, int mt, int nt, int batch) {
   int per = mt * nt;
   TileCoord c;
   c.p = t / per;
+  c.pr = c.p / batch;
   int r = t - c.p * per;
   c.n = r / mt;  // consecutive CTAs share a B column block
   c.m = r - c.n * mt;
@@ -298,7 +301,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
   wait_for_predecessor();
   const int P = launch_primes(gp, plan);
   if (P == 0) return;
-  const int total = P * gp.mt * gp.nt;
+  const int total = P * gp.batch * gp.mt * gp.nt;
   const int nc_tile = (gp.kb_total + KC_BLOCKS - 1) / KC_BLOCKS;
 
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -349,7 +352,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       uint32_t issued_phase[STAGES] = {};
       bool ok = true;
       for (int t = blockIdx.x; t < total && ok; t += gridDim.x) {
-        TileCoord tc = tile_coord(t, gp.mt, gp.nt);
+        TileCoord tc = tile_coord(t, gp.mt, gp.nt, gp.batch);
         for (int kb = 0; kb < gp.kb_total; ++kb) {
           if (!wait_bounded(smem_u32(&empty[stage]), phase ^ 1u, ctl, 1)) {
             ok = false;
@@ -447,8 +450,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     bool ok = true;
     const uint32_t out_s = smem_u32(out_base);
     for (int t = blockIdx.x; t < total && ok; t += gridDim.x) {
-      TileCoord tc = tile_coord(t, gp.mt, gp.nt);
-      const float q = gp.qf[tc.p], iq = gp.invq[tc.p];
+      TileCoord tc = tile_coord(t, gp.mt, gp.nt, gp.batch);
+      const float q = gp.qf[tc.pr], iq = gp.invq[tc.pr];
       bool first_write = true;
       for (int c = 0; c < nc_tile; ++c) {
         const uint32_t b = acc_iter & 1u, aph = (acc_iter >> 1) & 1u;
@@ -629,7 +632,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
   const int P = launch_primes(gp, plan);  // the same decision in both CTAs of the pair
   if (P == 0) return;
   const int mt2 = (gp.M + 255) / 256;
-  const int total = P * mt2 * gp.nt;
+  const int total = P * gp.batch * mt2 * gp.nt;
   const int nc_tile = (gp.kb_total + KC_BLOCKS - 1) / KC_BLOCKS;
   const uint32_t rank = cluster_rank();
   const int cid = blockIdx.x >> 1, ncl = gridDim.x >> 1;
@@ -680,7 +683,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       uint32_t phase = 0;
       bool ok = true;
       for (int t = cid; t < total && ok; t += ncl) {
-        TileCoord tc = tile_coord(t, mt2, gp.nt);
+        TileCoord tc = tile_coord(t, mt2, gp.nt, gp.batch);
         for (int kb = 0; kb < gp.kb_total; ++kb) {
           if (!wait_bounded_cluster(smem_u32(&empty[stage]), phase ^ 1u, ctl, 11)) {
             ok = false;
@@ -771,8 +774,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     const uint32_t out_s = smem_u32(out_base);
     const uint32_t tempty_leader[2] = {mapa_shared(smem_u32(&tempty[0]), 0), mapa_shared(smem_u32(&tempty[1]), 0)};
     for (int t = cid; t < total && ok; t += ncl) {
-      TileCoord tc = tile_coord(t, mt2, gp.nt);
-      const float q = gp.qf[tc.p], iq = gp.invq[tc.p];
+      TileCoord tc = tile_coord(t, mt2, gp.nt, gp.batch);
+      const float q = gp.qf[tc.pr], iq = gp.invq[tc.pr];
       const int row0 = tc.m * 256 + (int)rank * 128;
       bool first_write = true;
       for (int c = 0; c < nc_tile; ++c) {
@@ -891,8 +894,8 @@ std::atomic<int> g_gemm_variant{0};  // 0 automatic, 1 single-CTA, 2 CTA pair
 }  // namespace
 
 cudaError_t launch_gemm(const void* RA, long long lda, const void* RB, long long ldb, void* RC, long long ldc,
-                        int pmax, int P_fixed, long long M, long long N, long long K, DevPlan* plan, cudaStream_t st,
-                        int fault, unsigned long long wait_ns, bool derive_i64, bool b_kmajor) {
+                        int pmax, int batch, int P_fixed, long long M, long long N, long long K, DevPlan* plan,
+                        cudaStream_t st, int fault, unsigned long long wait_ns, bool derive_i64, bool b_kmajor) {
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
@@ -914,13 +917,14 @@ cudaError_t launch_gemm(const void* RA, long long lda, const void* RB, long long
   const int variant = g_gemm_variant.load();
   const bool pair = variant == 2 || (variant == 0 && M > BM);
   CUtensorMap ma, mb, mc;
-  if (!make_map_3d(&ma, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, RA, (uint64_t)K, (uint64_t)M, (uint64_t)pmax,
+  const uint64_t planes = (uint64_t)pmax * (uint64_t)batch;
+  if (!make_map_3d(&ma, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, RA, (uint64_t)K, (uint64_t)M, planes,
                    (uint64_t)lda * 2, (uint64_t)M * lda * 2, BK, BM) ||
-      !(b_kmajor ? make_map_3d(&mb, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, RB, (uint64_t)K, (uint64_t)N, (uint64_t)pmax,
+      !(b_kmajor ? make_map_3d(&mb, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, RB, (uint64_t)K, (uint64_t)N, planes,
                                (uint64_t)ldb * 2, (uint64_t)N * ldb * 2, BK, pair ? 128 : BN)
-                 : make_map_3d(&mb, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, RB, (uint64_t)N, (uint64_t)K, (uint64_t)pmax,
+                 : make_map_3d(&mb, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, RB, (uint64_t)N, (uint64_t)K, planes,
                                (uint64_t)ldb * 2, (uint64_t)K * ldb * 2, 64, BK)) ||
-      !make_map_3d(&mc, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, RC, (uint64_t)N, (uint64_t)M, (uint64_t)pmax, (uint64_t)ldc,
+      !make_map_3d(&mc, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, RC, (uint64_t)N, (uint64_t)M, planes, (uint64_t)ldc,
                    (uint64_t)M * ldc, 128, 128))
     return cudaErrorInvalidValue;
   GemmParams gp;
@@ -930,6 +934,7 @@ cudaError_t launch_gemm(const void* RA, long long lda, const void* RB, long long
   gp.mt = (int)((M + BM - 1) / BM);
   gp.nt = (int)((N + BN - 1) / BN);
   gp.kb_total = (int)((K + BK - 1) / BK);
+  gp.batch = batch;
   gp.P_fixed = P_fixed;
   gp.derive_i64 = derive_i64 ? 1 : 0;
   gp.ceil_log2_k = 0;
@@ -943,7 +948,7 @@ cudaError_t launch_gemm(const void* RA, long long lda, const void* RB, long long
   }
   for (int i = 0; i <= kNumPrimes; ++i) gp.log2P[i] = t.log2P[i];
   if (!pair) {
-    const long long tiles = (long long)pmax * gp.mt * gp.nt;
+    const long long tiles = (long long)planes * gp.mt * gp.nt;
     int grid = (int)(tiles < sms[dev] ? tiles : sms[dev]);
     if (grid < 1) grid = 1;
     return b_kmajor ? launch_dependent(residue_gemm_kernel<true>, dim3(grid), dim3(NUM_THREADS), SMEM_BYTES, st, ma,
@@ -974,7 +979,7 @@ cudaError_t launch_gemm(const void* RA, long long lda, const void* RB, long long
       n = sms[dev] / 2;
     max_pairs[dev] = n;
   }
-  const long long tiles2 = (long long)pmax * ((M + 255) / 256) * gp.nt;
+  const long long tiles2 = (long long)planes * ((M + 255) / 256) * gp.nt;
   long long clusters = max_pairs[dev];
   if (tiles2 < clusters) clusters = tiles2;
   if (clusters < 1) clusters = 1;

@@ -999,13 +999,16 @@ static unsigned split_grid(long long items) {
   return (unsigned)(b < 1 ? 1 : (b > cap ? cap : b));
 }
 
-cudaError_t launch_split(int op, const void* A, const void* B, int la, int lb, long long M, long long N, long long K,
-                         long long lda, long long ldb, void* RA, void* RB, DevPlan* plan, int i64_planes, bool transb,
-                         cudaStream_t st) {
+cudaError_t launch_split(int op, const void* A, const void* B, int la, int lb, long long batch, long long Mb,
+                         long long N, long long K, long long lda, long long ldb, void* RA, void* RB, DevPlan* plan,
+                         int i64_planes, bool transb, cudaStream_t st) {
   __half* ra = static_cast<__half*>(RA);
   __half* rb = static_cast<__half*>(RB);
-  // B [K][N] -> RB [P][K][ldb]; a transposed B [N][K] -> RB [P][N][ldb], laid out like A
-  const long long brows = transb ? N : K, bcols = transb ? K : N;
+  // The products of a batch lie back to back, so each side is one matrix of
+  // batch * rows rows.  B [K][N] -> RB [P][K][ldb]; a transposed B [N][K] ->
+  // RB [P][N][ldb], laid out like A.
+  const long long M = batch * Mb;
+  const long long brows = batch * (transb ? N : K), bcols = transb ? K : N;
   if (op == RG_OP_ENCLOSE) {
     constexpr int V = 8;
     const SplitSide sa = make_side(A, ra, M, K, lda, 1, V), sb = make_side(B, rb, brows, bcols, ldb, 1, V);

@@ -22,17 +22,21 @@ cudaError_t launch_plan(int op, const void* A, long long nA, int la, const void*
 // For op I64 no planner runs first: the split writes i64_planes planes and
 // reduces max |A|, max |B| into the plan; the GEMM derives the rest.
 // transb: B is given transposed, [N][K], and RB becomes [pmax][N][ldb].
-cudaError_t launch_split(int op, const void* A, const void* B, int la, int lb, long long M, long long N, long long K,
-                         long long lda, long long ldb, void* RA, void* RB, DevPlan* plan, int i64_planes, bool transb,
-                         cudaStream_t st);
+// batch: A and B hold `batch` products back to back ([batch][M][K] and
+// [batch][K][N]); the residue planes become [pmax][batch][..][..].
+cudaError_t launch_split(int op, const void* A, const void* B, int la, int lb, long long batch, long long M,
+                         long long N, long long K, long long lda, long long ldb, void* RA, void* RB, DevPlan* plan,
+                         int i64_planes, bool transb, cudaStream_t st);
 
 // Per-prime tensor-core product RC[p] = RA[p] * RB[p] mod q_p (uint8).
 // derive_i64: the prime count is derived here from max |A|, max |B| (or
 // taken from P_fixed), with the int64 range check, and written to the plan.
 // b_kmajor: RB is [pmax][N][ldb] (K contiguous) instead of [pmax][K][ldb].
+// batch: every prime's planes hold `batch` independent products
+// (RA [pmax][batch][M][lda], RB and RC likewise).
 cudaError_t launch_gemm(const void* RA, long long lda, const void* RB, long long ldb, void* RC, long long ldc,
-                        int pmax, int P_fixed, long long M, long long N, long long K, DevPlan* plan, cudaStream_t st,
-                        int fault, unsigned long long wait_ns, bool derive_i64, bool b_kmajor);
+                        int pmax, int batch, int P_fixed, long long M, long long N, long long K, DevPlan* plan,
+                        cudaStream_t st, int fault, unsigned long long wait_ns, bool derive_i64, bool b_kmajor);
 
 // Balanced Garner: RC [P][M][ldc] -> int64 limbs C [M][N][lc] (op I64/LIMBS),
 // or the outward pair (lo, hi) as binary64 bit patterns (op ENCLOSE).

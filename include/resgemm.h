@@ -44,7 +44,7 @@ extern "C" {
 
 /* Status codes. */
 #define RG_OK 0
-#define RG_ERR_ARG 1        /* null pointer, non-positive size, bad limb count, misaligned workspace */
+#define RG_ERR_ARG 1        /* null pointer, negative size, bad limb count, misaligned workspace */
 #define RG_ERR_RANGE 2      /* K > 2^17, or the product bound exceeds the primes or the output width */
 #define RG_ERR_NONFINITE 3  /* an fp64 operand entry is inf or nan */
 #define RG_ERR_LOSSY 4      /* reserved: wide fp64 operands now get a valid, looser bracket (rg_get_plan) */
@@ -82,7 +82,9 @@ extern "C" {
  * max |x|.  nprimes in [1, 53] skips the planner: the caller then guarantees
  * |C| <= (P - 1) / 2 for the product P of the nprimes largest primes, and the
  * entries must fit in 64 bits, as they always do.
- * Errors: RG_ERR_ARG (sizes <= 0, null pointers, nprimes out of range),
+ * M, N or K = 0 is an empty problem: C (when it has entries) is set to 0
+ * and no kernel runs; K = 0 gives the empty sum, exactly 0.
+ * Errors: RG_ERR_ARG (negative sizes, null pointers, nprimes out of range),
  * RG_ERR_RANGE (K > 2^17; the exact bound K * max|A| * max|B| exceeds
  * 2^63 - 1, so C might not fit int64), RG_ERR_WORKSPACE, RG_ERR_CUDA,
  * RG_ERR_TIMEOUT.
@@ -131,6 +133,26 @@ int res_gemm_limbs(const int64_t* A, int la, const int64_t* B, int lb, int64_t* 
  */
 int enclose_gemm_f64(const double* A, const double* B, double* lo, double* hi, int64_t M, int64_t N, int64_t K,
                      unsigned flags, void* ws, size_t ws_bytes, void* stream);
+
+/*
+ * Batched forms: `batch` independent products of one shape, each operand's
+ * products stored back to back: A [batch][M][K], B [batch][K][N] (with
+ * RG_FLAG_TRANS_B [batch][N][K]; limbs add a last dimension as above),
+ * outputs [batch][M][N].  One plan covers the whole batch: one prime count
+ * from the largest entry of all of A and of all of B and, for fp64, one pair
+ * of scale exponents, so the batch pays the planning cost once ("enclosure-
+ * gemm", Usage: bmm_enclose; Method: a batch shares one plan).  A shared
+ * scale is the finest binary point of the whole batch, so each product's
+ * bracket is the one a separate call would give when the call is lossless.
+ * batch = 0 is an empty problem.  Errors as for the unbatched forms.
+ */
+int res_gemm_i64_batched(const int64_t* A, const int64_t* B, int64_t* C, int64_t batch, int64_t M, int64_t N,
+                         int64_t K, int nprimes, unsigned flags, void* ws, size_t ws_bytes, void* stream);
+int res_gemm_limbs_batched(const int64_t* A, int la, const int64_t* B, int lb, int64_t* C, int lc, int64_t batch,
+                           int64_t M, int64_t N, int64_t K, int nprimes, unsigned flags, void* ws, size_t ws_bytes,
+                           void* stream);
+int enclose_gemm_f64_batched(const double* A, const double* B, double* lo, double* hi, int64_t batch, int64_t M,
+                             int64_t N, int64_t K, unsigned flags, void* ws, size_t ws_bytes, void* stream);
 
 /*
  * The per-prime tensor-core stage alone, on caller-provided residues:
@@ -184,10 +206,13 @@ size_t rg_noalloc_scratch_bytes(void);
  * la, lb, lc are the limb counts (1 for RG_OP_I64 / RG_OP_ENCLOSE); nprimes
  * is the value the call will pass (0 = plan on the device).  flags must
  * match the call's RG_FLAG_HOST and RG_FLAG_TRANS_B bits.  Returns 0 for
- * invalid arguments.
+ * invalid arguments.  An empty problem needs the 4 KiB plan block only.
  */
 size_t rg_workspace_bytes(int op, int64_t M, int64_t N, int64_t K, int la, int lb, int lc, int nprimes,
                           unsigned flags);
+/* The same for a batched call of `batch` products. */
+size_t rg_workspace_bytes_batched(int op, int64_t batch, int64_t M, int64_t N, int64_t K, int la, int lb, int lc,
+                                  int nprimes, unsigned flags);
 
 /* Offsets (bytes from ws) of the stage buffers a call leaves in its
  * workspace, for inspection:
@@ -195,7 +220,9 @@ size_t rg_workspace_bytes(int op, int64_t M, int64_t N, int64_t K, int la, int l
  *   rb: fp16 residues of B, [pmax][K][ldb]   (ldb = N rounded up to 64), or
  *       [pmax][N][ldb] with RG_FLAG_TRANS_B    (ldb = K rounded up to 8)
  *   rc: uint8 product residues, [pmax][M][ldc] (ldc = N rounded up to 16)
- * Residue planes follow the prime order q_0 = 251, q_1 = 241, ... */
+ * Residue planes follow the prime order q_0 = 251, q_1 = 241, ...; a batched
+ * call stores each prime's planes for all products back to back
+ * ([pmax][batch][M][lda] and so on). */
 typedef struct {
   size_t ra, rb, rc;
   int64_t lda, ldb, ldc;
@@ -203,6 +230,8 @@ typedef struct {
 } rg_layout;
 int rg_workspace_layout(int op, int64_t M, int64_t N, int64_t K, int la, int lb, int lc, int nprimes,
                         unsigned flags, rg_layout* out);
+int rg_workspace_layout_batched(int op, int64_t batch, int64_t M, int64_t N, int64_t K, int la, int lb, int lc,
+                                int nprimes, unsigned flags, rg_layout* out);
 
 /* The plan a call chose, read back from its workspace after the stream is
  * synchronised ("enclosure-gemm", Method: return_info reports the regime). */

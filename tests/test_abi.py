@@ -77,7 +77,18 @@ def test_workspace_sizes(rg):
     assert L.ra % 4096 == 0 and L.rb % 4096 == 0 and L.rc % 4096 == 0
     assert rg.workspace_layout(rg.RG_OP_ENCLOSE, 8, 8, 8).pmax == 53
     assert rg.workspace_bytes(rg.RG_OP_I64, 64, 64, 64, host=True) > n
-    assert rg.workspace_bytes(rg.RG_OP_I64, 0, 64, 64) == 0
+    assert rg.workspace_bytes(rg.RG_OP_I64, -1, 64, 64) == 0
+    assert rg.workspace_bytes(rg.RG_OP_I64, 0, 64, 64) == 4096  # an empty problem: the plan block only
+    assert rg.workspace_bytes(rg.RG_OP_ENCLOSE, 8, 8, 0) == 4096
+    assert rg.workspace_bytes(rg.RG_OP_I64, 8, 8, 8, batch=0) == 4096
+    assert rg.workspace_bytes(rg.RG_OP_I64, 8, 8, 8, batch=-1) == 0
+    # a batch scales every plane: [pmax][batch][rows][ld]
+    one, five = (rg.workspace_layout(rg.RG_OP_I64, 65, 77, 129, batch=b) for b in (1, 5))
+    assert (five.lda, five.ldb, five.ldc, five.pmax) == (one.lda, one.ldb, one.ldc, one.pmax)
+    assert five.rb - five.ra >= 5 * 9 * 65 * 136 * 2 and five.rc - five.rb >= 5 * 9 * 129 * 128 * 2
+    assert rg.workspace_bytes(rg.RG_OP_I64, 65, 77, 129, batch=5) > 4 * rg.workspace_bytes(rg.RG_OP_I64, 65, 77, 129)
+    Lt = rg.workspace_layout(rg.RG_OP_I64, 65, 77, 129, transb=True)
+    assert Lt.ldb == 136 and Lt.rc - Lt.rb >= 9 * 77 * 136 * 2
     assert rg.workspace_bytes(rg.RG_OP_LIMBS, 4, 4, 4, la=5, lb=1, lc=2) == 0
     assert rg.workspace_bytes(rg.RG_OP_LIMBS, 4, 4, 4, la=2, lb=2, lc=7) == 0
 
@@ -91,7 +102,10 @@ def test_argument_errors_need_no_device(rg):
     # null operand
     assert lib.res_gemm_i64(None, p, p, 2, 2, 2, 0, 0, wsp, 4096, None) == rg.RG_ERR_ARG
     # bad sizes
-    assert lib.res_gemm_i64(p, p, p, 0, 2, 2, 0, 0, wsp, 4096, None) == rg.RG_ERR_ARG
+    assert lib.res_gemm_i64(p, p, p, -1, 2, 2, 0, 0, wsp, 4096, None) == rg.RG_ERR_ARG
+    assert lib.res_gemm_i64(p, p, p, 2, 2, -2, 0, 0, wsp, 4096, None) == rg.RG_ERR_ARG
+    assert lib.res_gemm_i64_batched(p, p, p, -1, 2, 2, 2, 0, 0, wsp, 4096, None) == rg.RG_ERR_ARG
+    assert lib.enclose_gemm_f64_batched(p, p, p, None, 3, 2, 2, 2, 0, wsp, 4096, None) == rg.RG_ERR_ARG
     assert lib.res_gemm_i64(p, p, p, 2, 2, 2, 54, 0, wsp, 4096, None) == rg.RG_ERR_ARG
     # K > 2^17
     assert lib.res_gemm_i64(p, p, p, 2, 2, 2**17 + 1, 0, 0, wsp, 4096, None) == rg.RG_ERR_RANGE
