@@ -64,6 +64,9 @@ def _load():
         lib.oracle_matmul_limbs.restype = ctypes.c_long
         lib.oracle_enclose_f64.argtypes = [dp, dp, dp, dp, ci, ci, ci, i64p, ci, ci]
         lib.oracle_enclose_f64.restype = ci
+        fp = ctypes.POINTER(ctypes.c_float)
+        lib.oracle_enclose_f32.argtypes = [fp, fp, fp, fp, ci, ci, ci, i64p, ci, ci]
+        lib.oracle_enclose_f32.restype = ci
         lib.oracle_threads.argtypes = [ci]
         lib.oracle_threads.restype = ci
         _lib = lib
@@ -152,6 +155,28 @@ def enclose_f64(A, B, rows=None, threads: int | None = None):
     return lo, hi
 
 
+def enclose_f32(A, B, rows=None, threads: int | None = None):
+    """(lo, hi) float32 [R,N]: the tightest floats bracketing the exact A @ B of float32 matrices."""
+    A = np.ascontiguousarray(A, dtype=np.float32)
+    B = np.ascontiguousarray(B, dtype=np.float32)
+    M, K = A.shape
+    K2, N = B.shape
+    assert K == K2
+    r, nr = _rows_arg(rows, M)
+    lo = np.zeros((nr, N), dtype=np.float32)
+    hi = np.zeros((nr, N), dtype=np.float32)
+    rp = _ptr(r, ctypes.c_int64) if r is not None else None
+    rc = _load().oracle_enclose_f32(_ptr(A, ctypes.c_float), _ptr(B, ctypes.c_float), _ptr(lo, ctypes.c_float),
+                                    _ptr(hi, ctypes.c_float), M, N, K, rp, nr, threads or default_threads())
+    if rc == -1:
+        raise ValueError("non-finite operand")
+    if rc == -3:
+        raise MemoryError("oracle_enclose_f32")
+    if rc != 0:
+        raise RuntimeError("oracle outward search did not converge")
+    return lo, hi
+
+
 # ---------------------------------------------------------------------------
 # Pure-Python oracle (tiny cases only)
 # ---------------------------------------------------------------------------
@@ -218,10 +243,37 @@ def enclose_exact_py(exact: Fraction):
     return lo, hi
 
 
-def enclose_py(A, B):
-    """(lo, hi) as nested lists for small float matrices, via Fraction."""
-    A = np.asarray(A, dtype=np.float64)
-    B = np.asarray(B, dtype=np.float64)
+def enclose_exact_py32(exact: Fraction):
+    """(lo, hi): largest float32 <= exact and smallest float32 >= exact, as
+    numpy float32 (+0 for an exact zero; infinite beyond the largest finite)."""
+    f32 = np.float32
+    if exact == 0:
+        return f32(0.0), f32(0.0)
+    top = Fraction(float(np.finfo(np.float32).max))
+    if exact > top:
+        c = f32(np.inf)
+    elif exact < -top:
+        c = f32(-np.inf)
+    else:
+        c = f32(float(exact))  # float() rounds once more; the walk below corrects it
+    while c == np.inf or (c != -np.inf and Fraction(float(c)) > exact):
+        c = np.nextafter(c, f32(-np.inf))
+    while c != np.inf:
+        n = np.nextafter(c, f32(np.inf))
+        if n == np.inf or Fraction(float(n)) > exact:
+            break
+        c = n
+    lo = c
+    hi = lo if (lo != -np.inf and Fraction(float(lo)) == exact) else np.nextafter(lo, f32(np.inf))
+    return lo, hi
+
+
+def enclose_py(A, B, dtype=np.float64):
+    """(lo, hi) as nested lists for small float matrices, via Fraction; with
+    dtype float32 the operands are binary32 and the bounds are binary32."""
+    A = np.asarray(A, dtype=dtype)
+    B = np.asarray(B, dtype=dtype)
+    rnd = enclose_exact_py32 if dtype == np.float32 else enclose_exact_py
     M, K = A.shape
     N = B.shape[1]
     lo = [[0.0] * N for _ in range(M)]
@@ -231,7 +283,7 @@ def enclose_py(A, B):
     for i in range(M):
         for j in range(N):
             s = sum((Af[i][k] * Bf[k][j] for k in range(K)), Fraction(0))
-            lo[i][j], hi[i][j] = enclose_exact_py(s)
+            lo[i][j], hi[i][j] = rnd(s)
     return lo, hi
 
 

@@ -19,10 +19,15 @@
  *     comparing exactly ("enclosure-gemm" page, Correctness: the reference is
  *     exact rational arithmetic; lo/hi must bracket the exact product and, when
  *     scaling is lossless, equal its floor and ceiling in the format).
+ *   - oracle_enclose_f32: the same for binary32 operands, whose floor and
+ *     ceiling are taken in binary32 ("enclosure-gemm" page, Usage: operands
+ *     are float32 or float64; every binary32 value is also a binary64 value,
+ *     so the exact sum is formed the same way).
  *
  * Parallelism: OpenMP over output rows only; every entry is computed by the
  * same sequential loop over k.
  */
+#include <float.h>
 #include <math.h>
 #include <stdint.h>
 #include <stdlib.h>
@@ -299,6 +304,79 @@ static int outward(const exact_t *V, double *lo, double *hi) {
   return 0;
 }
 
+/* The same search over the binary32 values: lo = the largest float (or -inf)
+ * <= V, hi = the smallest float (or +inf) >= V.  Every float is a double, so
+ * the comparison is the exact one above. */
+static int outward_f32(const exact_t *V, float *lo, float *hi) {
+  if (V->sgn == 0) {
+    *lo = 0.0f;
+    *hi = 0.0f;
+    return 0;
+  }
+  double r = rough_value(V);
+  float c = fabs(r) > FLT_MAX ? (r > 0 ? INFINITY : -INFINITY) : (float)r;
+  int steps = 0;
+  while (cmp_exact_double(V, (double)c) < 0) {
+    c = nextafterf(c, -INFINITY);
+    if (++steps > MAX_STEPS) return -1;
+  }
+  for (;;) {
+    if (c == INFINITY) break;
+    float n = nextafterf(c, INFINITY);
+    if (cmp_exact_double(V, (double)n) >= 0)
+      c = n;
+    else
+      break;
+    if (++steps > MAX_STEPS) return -1;
+  }
+  *lo = c;
+  *hi = cmp_exact_double(V, (double)c) == 0 ? c : nextafterf(c, INFINITY);
+  return 0;
+}
+
+/* The exact value of row i of A[M][K] times column j of B[K][N]. */
+static void exact_entry(const double *A, const double *B, int64_t i, int j, int N, int K, exact_t *V) {
+  grid_t pos, neg;
+  memset(&pos, 0, sizeof(pos));
+  memset(&neg, 0, sizeof(neg));
+  for (int k = 0; k < K; k++) {
+    int sa, sb, ea, eb;
+    uint64_t ma, mb;
+    decompose(A[(size_t)i * K + k], &sa, &ma, &ea);
+    decompose(B[(size_t)k * N + j], &sb, &mb, &eb);
+    if (ma == 0 || mb == 0) continue;
+    grid_add((sa ^ sb) ? &neg : &pos, (u128)ma * mb, ea + eb);
+  }
+  int c = grid_cmp(&pos, &neg);
+  if (c >= 0)
+    grid_sub(&pos, &neg, &V->mag);
+  else
+    grid_sub(&neg, &pos, &V->mag);
+  V->sgn = grid_is_zero(&V->mag) ? 0 : c;
+}
+
+/* Rows of the bracket; lo/hi are double (f32 = 0) or float (f32 = 1). */
+static int enclose_rows(const double *A, const double *B, void *lo, void *hi, int f32, int M, int N, int K,
+                        const int64_t *rows, int nrows, int threads) {
+  int broken = 0;
+  (void)M;
+  set_threads(threads);
+#pragma omp parallel for schedule(dynamic, 1) reduction(| : broken)
+  for (int r = 0; r < nrows; r++) {
+    int64_t i = rows ? rows[r] : r;
+    for (int j = 0; j < N; j++) {
+      exact_t V;
+      exact_entry(A, B, i, j, N, K, &V);
+      size_t o = (size_t)r * N + j;
+      if (f32)
+        broken |= outward_f32(&V, (float *)lo + o, (float *)hi + o) != 0;
+      else
+        broken |= outward(&V, (double *)lo + o, (double *)hi + o) != 0;
+    }
+  }
+  return broken ? -2 : 0;
+}
+
 /*
  * lo[r][j], hi[r][j] for row rows[r] (NULL = all rows) of the exact product
  * A[M][K] * B[K][N] of binary64 matrices.  Returns 0, -1 if an operand entry
@@ -306,39 +384,34 @@ static int outward(const exact_t *V, double *lo, double *hi) {
  */
 int oracle_enclose_f64(const double *A, const double *B, double *lo, double *hi, int M, int N, int K,
                        const int64_t *rows, int nrows, int threads) {
-  int broken = 0;
   if (!rows) nrows = M;
   for (size_t t = 0; t < (size_t)M * K; t++)
     if (!isfinite(A[t])) return -1;
   for (size_t t = 0; t < (size_t)K * N; t++)
     if (!isfinite(B[t])) return -1;
-  set_threads(threads);
-#pragma omp parallel for schedule(dynamic, 1) reduction(| : broken)
-  for (int r = 0; r < nrows; r++) {
-    int64_t i = rows ? rows[r] : r;
-    grid_t pos, neg;
-    for (int j = 0; j < N; j++) {
-      memset(&pos, 0, sizeof(pos));
-      memset(&neg, 0, sizeof(neg));
-      for (int k = 0; k < K; k++) {
-        int sa, sb, ea, eb;
-        uint64_t ma, mb;
-        decompose(A[(size_t)i * K + k], &sa, &ma, &ea);
-        decompose(B[(size_t)k * N + j], &sb, &mb, &eb);
-        if (ma == 0 || mb == 0) continue;
-        grid_add((sa ^ sb) ? &neg : &pos, (u128)ma * mb, ea + eb);
-      }
-      exact_t V;
-      int c = grid_cmp(&pos, &neg);
-      if (c >= 0)
-        grid_sub(&pos, &neg, &V.mag);
-      else
-        grid_sub(&neg, &pos, &V.mag);
-      V.sgn = grid_is_zero(&V.mag) ? 0 : c;
-      broken |= outward(&V, &lo[(size_t)r * N + j], &hi[(size_t)r * N + j]) != 0;
-    }
+  return enclose_rows(A, B, lo, hi, 0, M, N, K, rows, nrows, threads);
+}
+
+/* The same for binary32 matrices and binary32 bounds.  Returns -3 if the
+ * double copies of the operands cannot be allocated. */
+int oracle_enclose_f32(const float *A, const float *B, float *lo, float *hi, int M, int N, int K,
+                       const int64_t *rows, int nrows, int threads) {
+  if (!rows) nrows = M;
+  for (size_t t = 0; t < (size_t)M * K; t++)
+    if (!isfinite(A[t])) return -1;
+  for (size_t t = 0; t < (size_t)K * N; t++)
+    if (!isfinite(B[t])) return -1;
+  double *Ad = malloc(((size_t)M * K + 1) * sizeof(double));
+  double *Bd = malloc(((size_t)K * N + 1) * sizeof(double));
+  int rc = -3;
+  if (Ad && Bd) {
+    for (size_t t = 0; t < (size_t)M * K; t++) Ad[t] = (double)A[t]; /* exact */
+    for (size_t t = 0; t < (size_t)K * N; t++) Bd[t] = (double)B[t];
+    rc = enclose_rows(Ad, Bd, lo, hi, 1, M, N, K, rows, nrows, threads);
   }
-  return broken ? -2 : 0;
+  free(Ad);
+  free(Bd);
+  return rc;
 }
 
 /* Number of OpenMP threads a parallel region will use. */
