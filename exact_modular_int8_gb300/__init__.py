@@ -38,7 +38,7 @@ RG_ERR_TIMEOUT = 7
 RG_FLAG_SYNC = 1
 RG_FLAG_HOST = 2
 RG_FLAG_TRANS_B = 4
-RG_OP_I64, RG_OP_LIMBS, RG_OP_ENCLOSE, RG_OP_STAGE = 0, 1, 2, 3
+RG_OP_I64, RG_OP_LIMBS, RG_OP_ENCLOSE, RG_OP_STAGE, RG_OP_ENCLOSE_F32 = 0, 1, 2, 3, 4
 MAX_K = 131072
 NUM_PRIMES = 53
 
@@ -47,7 +47,7 @@ EXPORTED = (
     "rg_workspace_layout", "rg_get_plan", "rg_status", "rg_prime", "rg_strerror", "rg_set_wait_limit_ns",
     "rg_inject_fault", "res_gemm_i64_noalloc", "rg_noalloc_scratch_bytes", "rg_set_gemm_variant",
     "res_gemm_i64_batched", "res_gemm_limbs_batched", "enclose_gemm_f64_batched", "rg_workspace_bytes_batched",
-    "rg_workspace_layout_batched",
+    "rg_workspace_layout_batched", "enclose_gemm_f32", "enclose_gemm_f32_batched",
 )
 
 
@@ -95,8 +95,11 @@ def library():
             lib.res_gemm_i64_batched.argtypes = [vp, vp, vp, i64, i64, i64, i64, ci, cu, vp, sz, vp]
             lib.res_gemm_limbs_batched.argtypes = [vp, ci, vp, ci, vp, ci, i64, i64, i64, i64, ci, cu, vp, sz, vp]
             lib.enclose_gemm_f64_batched.argtypes = [vp, vp, vp, vp, i64, i64, i64, i64, cu, vp, sz, vp]
+            lib.enclose_gemm_f32.argtypes = [vp, vp, vp, vp, i64, i64, i64, cu, vp, sz, vp]
+            lib.enclose_gemm_f32_batched.argtypes = [vp, vp, vp, vp, i64, i64, i64, i64, cu, vp, sz, vp]
             for f in ("res_gemm_i64", "res_gemm_limbs", "enclose_gemm_f64", "res_gemm_stage", "res_gemm_i64_batched",
-                      "res_gemm_limbs_batched", "enclose_gemm_f64_batched"):
+                      "res_gemm_limbs_batched", "enclose_gemm_f64_batched", "enclose_gemm_f32",
+                      "enclose_gemm_f32_batched"):
                 getattr(lib, f).restype = ci
             lib.rg_workspace_bytes.argtypes = [ci, i64, i64, i64, ci, ci, ci, ci, cu]
             lib.rg_workspace_bytes.restype = sz
@@ -270,40 +273,62 @@ def res_gemm_limbs(A: torch.Tensor, B: torch.Tensor, lc: int, nprimes: int = 0, 
     return C
 
 
-def enclose_gemm_f64(A: torch.Tensor, B: torch.Tensor, sync: bool = True, ws: torch.Tensor | None = None,
-                     transb: bool = False):
-    """(lo, hi) float64 with lo <= A @ B <= hi entrywise in exact arithmetic.
-    With transb, B is given as [N, K] and the bracket is of A @ B.T.  A [b, M, K] and B [b, K, N]
-    run as one batched call sharing one plan."""
-    sh = _shapes(A, B, transb, 0) if A.dtype == torch.float64 and B.dtype == torch.float64 else None
+def enclose_gemm(A: torch.Tensor, B: torch.Tensor, sync: bool = True, ws: torch.Tensor | None = None,
+                 transb: bool = False):
+    """(lo, hi) with lo <= A @ B <= hi entrywise in exact arithmetic, in the operands' format
+    (float64 or float32).  With transb, B is given as [N, K] and the bracket is of A @ B.T.
+    A [b, M, K] and B [b, K, N] run as one batched call sharing one plan."""
+    if A.dtype != B.dtype or A.dtype not in (torch.float64, torch.float32):
+        raise ValueError("float64 or float32 operands of one dtype expected")
+    sh = _shapes(A, B, transb, 0)
     if sh is None:
-        raise ValueError("A [M,K] and B [K,N] (transb: [N,K]) float64 expected, optionally with a batch dimension")
+        raise ValueError("A [M,K] and B [K,N] (transb: [N,K]) expected, optionally with a batch dimension")
     batched, batch, M, N, K, _, _ = sh
+    f32 = A.dtype == torch.float32
+    op = RG_OP_ENCLOSE_F32 if f32 else RG_OP_ENCLOSE
     A, B, dev, flags = _prepare(A, B, sync, transb)
     pin = bool(flags & RG_FLAG_HOST)
     shape = (batch, M, N) if batched else (M, N)
-    lo = torch.empty(shape, dtype=torch.float64, device=A.device, pin_memory=pin)
-    hi = torch.empty(shape, dtype=torch.float64, device=A.device, pin_memory=pin)
+    lo = torch.empty(shape, dtype=A.dtype, device=A.device, pin_memory=pin)
+    hi = torch.empty(shape, dtype=A.dtype, device=A.device, pin_memory=pin)
+    name = "enclose_gemm_f32" if f32 else "enclose_gemm_f64"
     with torch.cuda.device(dev):
-        need = workspace_bytes(RG_OP_ENCLOSE, M, N, K, host=pin, transb=transb, batch=batch)
+        need = workspace_bytes(op, M, N, K, host=pin, transb=transb, batch=batch)
         if need == 0:
-            raise ResGemmError(RG_ERR_ARG, "enclose_gemm_f64")
+            raise ResGemmError(RG_ERR_ARG, name)
         w = ws if ws is not None else workspace(need, dev)
-        rc = library().enclose_gemm_f64_batched(A.data_ptr(), B.data_ptr(), lo.data_ptr(), hi.data_ptr(), batch, M,
-                                                N, K, flags, w.data_ptr(), w.numel(),
-                                                torch.cuda.current_stream(dev).cuda_stream)
-    _check(rc, "enclose_gemm_f64")
+        rc = getattr(library(), name + "_batched")(A.data_ptr(), B.data_ptr(), lo.data_ptr(), hi.data_ptr(), batch,
+                                                   M, N, K, flags, w.data_ptr(), w.numel(),
+                                                   torch.cuda.current_stream(dev).cuda_stream)
+    _check(rc, name)
     return lo, hi
 
 
+def enclose_gemm_f64(A: torch.Tensor, B: torch.Tensor, sync: bool = True, ws: torch.Tensor | None = None,
+                     transb: bool = False):
+    """enclose_gemm for float64 operands (float64 bounds)."""
+    if A.dtype != torch.float64 or B.dtype != torch.float64:
+        raise ValueError("float64 operands expected")
+    return enclose_gemm(A, B, sync, ws, transb)
+
+
+def enclose_gemm_f32(A: torch.Tensor, B: torch.Tensor, sync: bool = True, ws: torch.Tensor | None = None,
+                     transb: bool = False):
+    """enclose_gemm for float32 operands (float32 bounds)."""
+    if A.dtype != torch.float32 or B.dtype != torch.float32:
+        raise ValueError("float32 operands expected")
+    return enclose_gemm(A, B, sync, ws, transb)
+
+
 def mm_enclose(A: torch.Tensor, B: torch.Tensor):
-    """lo <= A @ B <= hi entrywise, exactly ("enclosure-gemm", Usage: mm_enclose)."""
-    return enclose_gemm_f64(A, B)
+    """lo <= A @ B <= hi entrywise, exactly, for float64 or float32 operands
+    ("enclosure-gemm", Usage: mm_enclose)."""
+    return enclose_gemm(A, B)
 
 
 def mm_enclose_nt(A: torch.Tensor, Bt: torch.Tensor):
     """The bracket of A @ Bt.T without a transposed copy ("enclosure-gemm", Usage: mm_enclose_nt)."""
-    return enclose_gemm_f64(A, Bt, transb=True)
+    return enclose_gemm(A, Bt, transb=True)
 
 
 def bmm_enclose(A: torch.Tensor, B: torch.Tensor):
@@ -311,7 +336,7 @@ def bmm_enclose(A: torch.Tensor, B: torch.Tensor):
     ("enclosure-gemm", Usage: bmm_enclose)."""
     if A.dim() != 3 or B.dim() != 3:
         raise ValueError("A [b,M,K] and B [b,K,N] expected")
-    return enclose_gemm_f64(A, B)
+    return enclose_gemm(A, B)
 
 
 def res_gemm_stage(RA: torch.Tensor, RB: torch.Tensor, nprimes: int, M: int, N: int, K: int, RC=None,

@@ -61,6 +61,13 @@ struct Layout {
   int pmax;
 };
 
+bool is_enclose(int op) { return op == RG_OP_ENCLOSE || op == RG_OP_ENCLOSE_F32; }
+
+// Bytes of one operand or output entry: limbs of int64, one int64, one double or one float.
+size_t elem_bytes(int op, int limbs) {
+  return op == RG_OP_LIMBS ? 8 * (size_t)limbs : op == RG_OP_ENCLOSE_F32 ? 4 : 8;
+}
+
 // An empty problem (batch, M, N or K zero) needs only the plan block.
 bool is_empty(long long batch, long long M, long long N, long long K) { return !batch || !M || !N || !K; }
 
@@ -93,17 +100,16 @@ bool make_layout(int op, long long batch, long long M, long long N, long long K,
   L->rc = off;
   off = align_up(off + (size_t)pmax * batch * M * L->ldc, kAlign);
   if (flags & RG_FLAG_HOST) {
-    size_t ea = op == RG_OP_LIMBS ? 8 * (size_t)la : 8, eb = op == RG_OP_LIMBS ? 8 * (size_t)lb : 8;
-    size_t ec = op == RG_OP_LIMBS ? 8 * (size_t)lc : 8;
+    size_t ea = elem_bytes(op, la), eb = elem_bytes(op, lb), ec = elem_bytes(op, lc);
     L->a = off;
     off = align_up(off + (size_t)batch * M * K * ea, kAlign);
     L->b = off;
     off = align_up(off + (size_t)batch * K * N * eb, kAlign);
     L->c = off;
     off = align_up(off + (size_t)batch * M * N * ec, kAlign);
-    if (op == RG_OP_ENCLOSE) {
+    if (is_enclose(op)) {
       L->c2 = off;
-      off = align_up(off + (size_t)batch * M * N * 8, kAlign);
+      off = align_up(off + (size_t)batch * M * N * ec, kAlign);
     }
   }
   L->total = off;
@@ -133,7 +139,7 @@ int run(int op, const void* A, int la, const void* B, int lb, void* C, void* C2,
   if (batch < 0 || M < 0 || N < 0 || K < 0 || nprimes < 0 || nprimes > kNumPrimes) return RG_ERR_ARG;
   // an empty problem reads no operand, and writes outputs only if it has entries
   const bool empty = is_empty(batch, M, N, K), has_out = batch && M && N;
-  if ((!empty && (!A || !B)) || (has_out && (!C || (op == RG_OP_ENCLOSE && !C2)))) return RG_ERR_ARG;
+  if ((!empty && (!A || !B)) || (has_out && (!C || (is_enclose(op) && !C2)))) return RG_ERR_ARG;
   if (op == RG_OP_LIMBS &&
       (la < 1 || la > RG_MAX_LIMBS_IN || lb < 1 || lb > RG_MAX_LIMBS_IN || lc < 1 || lc > RG_MAX_LIMBS_OUT))
     return RG_ERR_ARG;
@@ -147,8 +153,7 @@ int run(int op, const void* A, int la, const void* B, int lb, void* C, void* C2,
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   uint8_t* w = static_cast<uint8_t*>(ws);
   DevPlan* plan = reinterpret_cast<DevPlan*>(w + L.plan);
-  const size_t ea = op == RG_OP_LIMBS ? 8 * (size_t)la : 8, eb = op == RG_OP_LIMBS ? 8 * (size_t)lb : 8;
-  const size_t ec = op == RG_OP_LIMBS ? 8 * (size_t)lc : 8;
+  const size_t ea = elem_bytes(op, la), eb = elem_bytes(op, lb), ec = elem_bytes(op, lc);
   const size_t out_bytes = (size_t)batch * M * N * ec;
   if (empty) {
     // Nothing to multiply; an empty sum is exactly zero (lo = hi = +0).
@@ -156,10 +161,10 @@ int run(int op, const void* A, int la, const void* B, int lb, void* C, void* C2,
     if (out_bytes) {
       if (flags & RG_FLAG_HOST) {
         std::memset(C, 0, out_bytes);
-        if (op == RG_OP_ENCLOSE) std::memset(C2, 0, out_bytes);
+        if (is_enclose(op)) std::memset(C2, 0, out_bytes);
       } else {
         RG_TRY(cudaMemsetAsync(C, 0, out_bytes, s));
-        if (op == RG_OP_ENCLOSE) RG_TRY(cudaMemsetAsync(C2, 0, out_bytes, s));
+        if (is_enclose(op)) RG_TRY(cudaMemsetAsync(C2, 0, out_bytes, s));
       }
     }
     return finish(ws, s, flags);
@@ -173,7 +178,7 @@ int run(int op, const void* A, int la, const void* B, int lb, void* C, void* C2,
     dA = w + L.a;
     dB = w + L.b;
     dC = w + L.c;
-    dC2 = op == RG_OP_ENCLOSE ? static_cast<void*>(w + L.c2) : nullptr;
+    dC2 = is_enclose(op) ? static_cast<void*>(w + L.c2) : nullptr;
     RG_TRY(cudaMemcpyAsync(const_cast<void*>(dA), A, (size_t)batch * M * K * ea, cudaMemcpyHostToDevice, s));
     RG_TRY(cudaMemcpyAsync(const_cast<void*>(dB), B, (size_t)batch * K * N * eb, cudaMemcpyHostToDevice, s));
   }
@@ -183,7 +188,7 @@ int run(int op, const void* A, int la, const void* B, int lb, void* C, void* C2,
   // plan; the other operations run the planner kernel first
   const bool i64 = op == RG_OP_I64;
   if (!i64)
-    RG_TRY(launch_plan(op, dA, batch * M * K, la1, dB, batch * K * N, lb1, lc1, K, op == RG_OP_ENCLOSE ? 0 : nprimes,
+    RG_TRY(launch_plan(op, dA, batch * M * K, la1, dB, batch * K * N, lb1, lc1, K, is_enclose(op) ? 0 : nprimes,
                        plan, s));
   const bool transb = (flags & RG_FLAG_TRANS_B) != 0;
   RG_TRY(launch_split(op, dA, dB, la1, lb1, batch, M, N, K, L.lda, L.ldb, w + L.ra, w + L.rb, plan, L.pmax, transb,
@@ -196,7 +201,7 @@ int run(int op, const void* A, int la, const void* B, int lb, void* C, void* C2,
                        dC2, s));
   if (flags & RG_FLAG_HOST) {
     RG_TRY(cudaMemcpyAsync(C, dC, out_bytes, cudaMemcpyDeviceToHost, s));
-    if (op == RG_OP_ENCLOSE) RG_TRY(cudaMemcpyAsync(C2, dC2, out_bytes, cudaMemcpyDeviceToHost, s));
+    if (is_enclose(op)) RG_TRY(cudaMemcpyAsync(C2, dC2, out_bytes, cudaMemcpyDeviceToHost, s));
   }
   return finish(ws, s, flags);
 }
@@ -218,6 +223,16 @@ int res_gemm_limbs(const int64_t* A, int la, const int64_t* B, int lb, int64_t* 
 int enclose_gemm_f64(const double* A, const double* B, double* lo, double* hi, int64_t M, int64_t N, int64_t K,
                      unsigned flags, void* ws, size_t ws_bytes, void* stream) {
   return run(RG_OP_ENCLOSE, A, 1, B, 1, lo, hi, 1, 1, M, N, K, 0, flags, ws, ws_bytes, stream);
+}
+
+int enclose_gemm_f32(const float* A, const float* B, float* lo, float* hi, int64_t M, int64_t N, int64_t K,
+                     unsigned flags, void* ws, size_t ws_bytes, void* stream) {
+  return run(RG_OP_ENCLOSE_F32, A, 1, B, 1, lo, hi, 1, 1, M, N, K, 0, flags, ws, ws_bytes, stream);
+}
+
+int enclose_gemm_f32_batched(const float* A, const float* B, float* lo, float* hi, int64_t batch, int64_t M,
+                             int64_t N, int64_t K, unsigned flags, void* ws, size_t ws_bytes, void* stream) {
+  return run(RG_OP_ENCLOSE_F32, A, 1, B, 1, lo, hi, 1, batch, M, N, K, 0, flags, ws, ws_bytes, stream);
 }
 
 int res_gemm_i64_batched(const int64_t* A, const int64_t* B, int64_t* C, int64_t batch, int64_t M, int64_t N,
@@ -261,7 +276,7 @@ int res_gemm_stage(const uint16_t* RA, int64_t lda, const uint16_t* RB, int64_t 
 size_t rg_workspace_bytes_batched(int op, int64_t batch, int64_t M, int64_t N, int64_t K, int la, int lb, int lc,
                                   int nprimes, unsigned flags) {
   Layout L;
-  if (op < RG_OP_I64 || op > RG_OP_STAGE) return 0;
+  if (op < RG_OP_I64 || op > RG_OP_ENCLOSE_F32) return 0;
   if (!make_layout(op, batch, M, N, K, la, lb, lc, nprimes, flags, &L)) return 0;
   return L.total;
 }
@@ -274,7 +289,7 @@ size_t rg_workspace_bytes(int op, int64_t M, int64_t N, int64_t K, int la, int l
 int rg_workspace_layout_batched(int op, int64_t batch, int64_t M, int64_t N, int64_t K, int la, int lb, int lc,
                                 int nprimes, unsigned flags, rg_layout* out) {
   Layout L;
-  if (!out || op < RG_OP_I64 || op > RG_OP_STAGE) return RG_ERR_ARG;
+  if (!out || op < RG_OP_I64 || op > RG_OP_ENCLOSE_F32) return RG_ERR_ARG;
   if (!make_layout(op, batch, M, N, K, la, lb, lc, nprimes, flags, &L)) return RG_ERR_ARG;
   out->ra = L.ra;
   out->rb = L.rb;

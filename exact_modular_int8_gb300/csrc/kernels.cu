@@ -73,6 +73,28 @@ __device__ __forceinline__ unsigned long long abs_u64(unsigned long long v) {
 }
 
 // ---------------------------------------------------------------------------
+// IEEE binary formats of the enclosure's operands and bounds ("enclosure-gemm",
+// Usage: operands are float32 or float64), read and written as bit patterns.
+// A finite nonzero x is (-1)^s * m * 2^(max(be, 1) - kLsbBias), with m the
+// significand including its hidden bit (kFracBits + 1 bits).
+// ---------------------------------------------------------------------------
+template <typename Bits>
+struct FloatFormat;
+template <>
+struct FloatFormat<unsigned long long> {  // binary64
+  static constexpr int kFracBits = 52, kExpMask = 0x7FF, kLsbBias = 1075, kEmax = 1023, kEminNormal = -1022,
+                       kUlpMin = -1074;
+  static constexpr unsigned long long kMaxFinite = 0x7FEFFFFFFFFFFFFFull, kInf = 0x7FF0000000000000ull,
+                                      kSign = 0x8000000000000000ull;
+};
+template <>
+struct FloatFormat<uint32_t> {  // binary32
+  static constexpr int kFracBits = 23, kExpMask = 0xFF, kLsbBias = 150, kEmax = 127, kEminNormal = -126,
+                       kUlpMin = -149;
+  static constexpr uint32_t kMaxFinite = 0x7F7FFFFFu, kInf = 0x7F800000u, kSign = 0x80000000u;
+};
+
+// ---------------------------------------------------------------------------
 // The plan ("enclosure-gemm", Method: three reductions over the exponent
 // field, stacked and read together; Requirements: K <= 2^17 and
 // bits_a + bits_b + ceil(log2 K) <= 332).  The planner kernels reduce into the
@@ -130,15 +152,18 @@ __device__ LocalPlan finalize_plan(DevPlan* plan, const PlanArgs& a) {
       p.nchunk_b = p.bits_b <= 23 ? 0 : min((p.bits_b + 1 + kChunkBits - 1) / kChunkBits, full_chunks(a.lb));
       if (p.T > RG_MAX_BOUND_BITS || p.T > 64 * a.lc - 1) p.status = RG_ERR_RANGE;
     }
-  } else {  // RG_OP_ENCLOSE
+  } else {  // RG_OP_ENCLOSE, RG_OP_ENCLOSE_F32
     if (__ldcg(&plan->nonfinite)) {
       p.status = RG_ERR_NONFINITE;
       return p;
     }
+    const bool f32 = a.op == RG_OP_ENCLOSE_F32;
+    const int sig = f32 ? FloatFormat<uint32_t>::kFracBits + 1 : FloatFormat<unsigned long long>::kFracBits + 1;
+    const int bias = f32 ? FloatFormat<uint32_t>::kLsbBias : FloatFormat<unsigned long long>::kLsbBias;
     const int ea = __ldcg(&plan->maxe_a), eb = __ldcg(&plan->maxe_b);
     const int mina = 4096 - __ldcg(&plan->inv_mine_a), minb = 4096 - __ldcg(&plan->inv_mine_b);
     // finest binary point holding every entry exactly: |A * 2^f_a| < 2^bits_a
-    const int bits_a0 = ea ? ea - mina + 53 : 0, bits_b0 = eb ? eb - minb + 53 : 0;
+    const int bits_a0 = ea ? ea - mina + sig : 0, bits_b0 = eb ? eb - minb + sig : 0;
     // coarsened until each operand fits 256-bit two's complement and the
     // product fits the residue range (enclosure-gemm, Method): the larger
     // operand gives up bits first
@@ -153,8 +178,8 @@ __device__ LocalPlan finalize_plan(DevPlan* plan, const PlanArgs& a) {
     }
     p.bits_a = ba;
     p.bits_b = bb;
-    p.f_a = ea ? 1075 - mina - (bits_a0 - ba) : 0;
-    p.f_b = eb ? 1075 - minb - (bits_b0 - bb) : 0;
+    p.f_a = ea ? bias - mina - (bits_a0 - ba) : 0;
+    p.f_b = eb ? bias - minb - (bits_b0 - bb) : 0;
     p.T = ba + bb + ck;
     p.lossless = ba == bits_a0 && bb == bits_b0;
   }
@@ -268,13 +293,15 @@ __global__ void __launch_bounds__(256) plan_limbs_kernel(const int64_t* __restri
   planner_finish(plan, pa);
 }
 
-// fp64: max and min of max(biased exponent, 1) over nonzero entries and a
-// non-finite flag, from the bit patterns only.
-__device__ __forceinline__ void exponent_stats(unsigned long long v, int& emax, int& einv, int& bad) {
-  const int be = (int)((v >> 52) & 0x7FF);
+// Floating-point operands: max and min of max(biased exponent, 1) over nonzero
+// entries and a non-finite flag, from the bit patterns only.
+template <typename Bits>
+__device__ __forceinline__ void exponent_stats(Bits v, int& emax, int& einv, int& bad) {
+  using F = FloatFormat<Bits>;
+  const int be = (int)((v >> F::kFracBits) & F::kExpMask);
   const int e = be > 1 ? be : 1;
-  const bool nonzero = (v << 1) != 0;
-  const bool finite = be != 0x7FF;
+  const bool nonzero = (Bits)(v << 1) != 0;
+  const bool finite = be != F::kExpMask;
   bad |= finite ? 0 : 1;
   if (finite && nonzero) {
     emax = e > emax ? e : emax;
@@ -282,22 +309,31 @@ __device__ __forceinline__ void exponent_stats(unsigned long long v, int& emax, 
   }
 }
 
-__global__ void __launch_bounds__(256) plan_f64_kernel(const unsigned long long* __restrict__ A, long long nA,
-                                                       const unsigned long long* __restrict__ B, long long nB,
-                                                       int nbA, DevPlan* plan, PlanArgs pa) {
+template <typename Bits>
+__global__ void __launch_bounds__(256) plan_float_kernel(const Bits* __restrict__ A, long long nA,
+                                                         const Bits* __restrict__ B, long long nB, int nbA,
+                                                         DevPlan* plan, PlanArgs pa) {
+  constexpr int PER = 16 / sizeof(Bits);  // entries per 16-byte load
   const PlannerSide sd = planner_side(nbA);
-  const unsigned long long* X = sd.isA ? A : B;
+  const Bits* X = sd.isA ? A : B;
   const long long n = sd.isA ? nA : nB;
-  const long long nv = (reinterpret_cast<uintptr_t>(X) & 15u) == 0 ? n / 2 : 0;
-  const ulonglong2* X2 = reinterpret_cast<const ulonglong2*>(X);
+  const long long nv = (reinterpret_cast<uintptr_t>(X) & 15u) == 0 ? n / PER : 0;
+  const uint4* X4 = reinterpret_cast<const uint4*>(X);
   int emax = 0, einv = 0, bad = 0;
 #pragma unroll 4
   for (long long i = sd.b0 * blockDim.x + threadIdx.x; i < nv; i += sd.stride) {
-    const ulonglong2 v = __ldg(X2 + i);
-    exponent_stats(v.x, emax, einv, bad);
-    exponent_stats(v.y, emax, einv, bad);
+    const uint4 v = __ldg(X4 + i);
+    if constexpr (PER == 4) {
+      exponent_stats<Bits>(v.x, emax, einv, bad);
+      exponent_stats<Bits>(v.y, emax, einv, bad);
+      exponent_stats<Bits>(v.z, emax, einv, bad);
+      exponent_stats<Bits>(v.w, emax, einv, bad);
+    } else {
+      exponent_stats<Bits>(((unsigned long long)v.y << 32) | v.x, emax, einv, bad);
+      exponent_stats<Bits>(((unsigned long long)v.w << 32) | v.z, emax, einv, bad);
+    }
   }
-  for (long long i = 2 * nv + sd.b0 * blockDim.x + threadIdx.x; i < n; i += sd.stride)
+  for (long long i = PER * nv + sd.b0 * blockDim.x + threadIdx.x; i < n; i += sd.stride)
     exponent_stats(__ldg(X + i), emax, einv, bad);
   emax = block_max_i32(emax);
   einv = block_max_i32(einv);
@@ -524,11 +560,17 @@ __global__ void __launch_bounds__(256) split_i64_kernel(SplitSide sa, SplitSide 
   allow_dependents();
 }
 
-// Binary64 operands: X' = x * 2^f = +-m * 2^sh with sh = max(be,1) - min(be',1)
-// >= 0; the 53-bit significand shifted by sh % 12 is cut into six chunks
-// starting at chunk index sh / 12.  No floating-point instruction reads x.
-template <int VEC>
-__global__ void __launch_bounds__(256) split_f64_kernel(SplitSide sa, SplitSide sb, const DevPlan* plan) {
+// Floating-point operands: X' = x * 2^f = +-m * 2^sh with
+// sh = max(be,1) - min(be',1) >= 0 when lossless; the significand (53 bits for
+// binary64, 24 for binary32) shifted by sh % 12 is cut into NC chunks starting
+// at chunk index sh / 12.  No floating-point instruction reads x.
+template <typename Bits, int VEC>
+__global__ void __launch_bounds__(256) split_float_kernel(SplitSide sa, SplitSide sb, const DevPlan* plan) {
+  using F = FloatFormat<Bits>;
+  // the significand shifted left by up to 11 bits spans NC chunks: 6 (binary64) or 3 (binary32)
+  constexpr int kSpan = F::kFracBits + 1 + kChunkBits - 1;
+  constexpr int NC = (kSpan + kChunkBits - 1) / kChunkBits;
+  constexpr int PER = 16 / sizeof(Bits);
   __shared__ float w_s[kNumPrimes][kMaxChunks];
   wait_for_predecessor();
   if (plan->status) return;
@@ -547,29 +589,28 @@ __global__ void __launch_bounds__(256) split_f64_kernel(SplitSide sa, SplitSide 
     const long long per_row = s.ldy / VEC;
     const long long row = item / per_row;
     const long long col0 = (item - row * per_row) * VEC;
-    const unsigned long long* X = static_cast<const unsigned long long*>(s.X) + row * s.C + col0;
-    unsigned long long xv[VEC];
+    const Bits* X = static_cast<const Bits*>(s.X) + row * s.C + col0;
+    Bits xv[VEC];
     if (col0 + VEC <= s.C && ((reinterpret_cast<uintptr_t>(X) & 15u) == 0)) {
 #pragma unroll
-      for (int t = 0; t < VEC / 2; ++t) {
-        const ulonglong2 v = __ldg(reinterpret_cast<const ulonglong2*>(X) + t);
-        xv[2 * t] = v.x;
-        xv[2 * t + 1] = v.y;
+      for (int t = 0; t < VEC / PER; ++t) {
+        const uint4 v = __ldg(reinterpret_cast<const uint4*>(X) + t);
+        memcpy(xv + PER * t, &v, 16);
       }
     } else {
 #pragma unroll
-      for (int e = 0; e < VEC; ++e) xv[e] = col0 + e < s.C ? __ldg(X + e) : 0ull;
+      for (int e = 0; e < VEC; ++e) xv[e] = col0 + e < s.C ? __ldg(X + e) : (Bits)0;
     }
-    constexpr int NC = 6;
     float cf[VEC][NC];
     int c0[VEC];
 #pragma unroll
     for (int e = 0; e < VEC; ++e) {
-      const unsigned long long v = xv[e];
-      const int be = (int)((v >> 52) & 0x7FF);
-      const bool neg = (v >> 63) != 0;
-      unsigned long long m = (v & 0xFFFFFFFFFFFFFull) | (be ? (1ull << 52) : 0ull);
-      int sh = (be > 1 ? be : 1) - 1075 + f;  // x * 2^f = +-m * 2^sh
+      const Bits v = xv[e];
+      const int be = (int)((v >> F::kFracBits) & F::kExpMask);
+      const bool neg = (v & F::kSign) != 0;
+      const unsigned long long hidden = 1ull << F::kFracBits;
+      unsigned long long m = ((unsigned long long)v & (hidden - 1ull)) | (be ? hidden : 0ull);
+      int sh = (be > 1 ? be : 1) - F::kLsbBias + f;  // x * 2^f = +-m * 2^sh
       unsigned long long t;
       if (m == 0 || sh >= 0) {
         // exact: +-m * 2^sh, cut at chunk sh / 12
@@ -577,7 +618,7 @@ __global__ void __launch_bounds__(256) split_f64_kernel(SplitSide sa, SplitSide 
         c0[e] = sh / kChunkBits;
         t = m << (sh % kChunkBits);
       } else {
-        // coarsened (lossy) point: floor(+-m * 2^sh), below 2^53 in magnitude
+        // coarsened (lossy) point: floor(+-m * 2^sh), below 2^(kFracBits+1) in magnitude
         const int r = -sh;
         const unsigned long long q = r >= 64 ? 0ull : m >> r;
         const bool lost = r >= 64 ? true : (m & ((1ull << r) - 1ull)) != 0ull;
@@ -597,7 +638,7 @@ __global__ void __launch_bounds__(256) split_f64_kernel(SplitSide sa, SplitSide 
         float acc = 0.0f;
 #pragma unroll
         for (int c = 0; c < NC; ++c) acc = __fmaf_rn(cf[e][c], w_s[p][c0[e] + c], acc);
-        r[e] = bal_mod_small(acc, q, iq);  // |acc| < 6 * 4095 * 125 < 2^23
+        r[e] = bal_mod_small(acc, q, iq);  // |acc| <= NC * 4095 * 125 < 2^23
       }
       __half2 h[VEC / 2];
 #pragma unroll
@@ -776,13 +817,15 @@ __global__ void __launch_bounds__(128) garner_int_kernel(const uint8_t* __restri
 }
 
 // Outward bit-pattern epilogue ("enclosure-gemm", Method): S (W words, two's
-// complement) times 2^-Q -> (lo, hi) IEEE binary64 bit patterns.
+// complement) times 2^-Q -> (lo, hi) IEEE bit patterns of the format of Bits
+// (binary64 or binary32).
 constexpr int kEncW = 11;  // 352 bits hold |S| < 2^333 with its sign
 
-__device__ __forceinline__ void outward_bits(const uint32_t (&x)[kEncW], int Q, unsigned long long& lo,
-                                             unsigned long long& hi) {
-  const unsigned long long kMaxFinite = 0x7FEFFFFFFFFFFFFFull, kInf = 0x7FF0000000000000ull,
-                           kSign = 0x8000000000000000ull;
+template <typename Bits>
+__device__ __forceinline__ void outward_bits(const uint32_t (&x)[kEncW], int Q, Bits& lo, Bits& hi) {
+  using F = FloatFormat<Bits>;
+  constexpr Bits kMaxFinite = F::kMaxFinite, kInf = F::kInf, kSign = F::kSign;
+  constexpr int kFrac = F::kFracBits;
   const bool neg = (x[kEncW - 1] >> 31) != 0;
   uint32_t mag[kEncW];
   unsigned long long carry = neg ? 1ull : 0ull;
@@ -797,28 +840,28 @@ __device__ __forceinline__ void outward_bits(const uint32_t (&x)[kEncW], int Q, 
   for (int k = kEncW - 1; k >= 0; --k)
     if (L < 0 && mag[k]) L = 32 * k + 31 - __clz(mag[k]);
   if (L < 0) {  // S == 0
-    lo = hi = 0ull;
+    lo = hi = 0;
     return;
   }
   const int E = L - Q;  // floor(log2 |S 2^-Q|)
-  if (E > 1023) {
+  if (E > F::kEmax) {
     lo = neg ? (kSign | kInf) : kMaxFinite;
     hi = neg ? (kSign | kMaxFinite) : kInf;
     return;
   }
-  const int u = E - 52 > -1074 ? E - 52 : -1074;  // exponent of one ulp at this magnitude
-  const int sh = u + Q;                            // bit of |S| holding that ulp
+  const int u = E - kFrac > F::kUlpMin ? E - kFrac : F::kUlpMin;  // exponent of one ulp at this magnitude
+  const int sh = u + Q;                                            // bit of |S| holding that ulp
   unsigned long long T = 0ull;
   bool rem = false;
   if (sh <= 0) {
-    // exact: |S| < 2^53 after the shift, since L - sh <= 52
+    // exact: |S| < 2^(kFrac+1) after the shift, since L - sh <= kFrac
 #pragma unroll
     for (int k = 0; k < 3; ++k) {
       const int b = 32 * k - sh;  // destination bit of word k
       if (b < 64 && k < kEncW) T |= (unsigned long long)mag[k] << b;
     }
   } else {
-    // T = bits [sh, sh + 53) of |S|; rem = any bit below sh
+    // T = bits [sh, sh + kFrac + 1) of |S|; rem = any bit below sh
 #pragma unroll
     for (int k = 0; k < kEncW; ++k) {
       const int lo_bit = 32 * k, hi_bit = 32 * k + 32;
@@ -833,16 +876,17 @@ __device__ __forceinline__ void outward_bits(const uint32_t (&x)[kEncW], int Q, 
         T |= w << (lo_bit - sh);
       }
     }
-    T &= (1ull << 53) - 1ull;
+    T &= (1ull << (kFrac + 1)) - 1ull;
   }
-  const unsigned long long enc = (E >= -1022 ? (unsigned long long)(E + 1022) << 52 : 0ull) + T;
+  // the hidden bit of T carries into the exponent field: biased exponent E + bias
+  const Bits enc = (Bits)((E >= F::kEminNormal ? (unsigned long long)(E - F::kEminNormal) << kFrac : 0ull) + T);
   if (!rem) {
-    lo = hi = (neg ? kSign : 0ull) | enc;
+    lo = hi = (neg ? kSign : (Bits)0) | enc;
   } else if (!neg) {
     lo = enc;
-    hi = enc + 1ull;
+    hi = (Bits)(enc + 1);
   } else {
-    lo = kSign | (enc + 1ull);
+    lo = kSign | (Bits)(enc + 1);
     hi = kSign | enc;
   }
 }
@@ -863,12 +907,13 @@ __device__ __forceinline__ void add_shifted(uint32_t (&x)[kEncW], long long v, i
   }
 }
 
+template <typename Bits>
 __global__ void __launch_bounds__(128) garner_enclose_kernel(const uint8_t* __restrict__ RC, long long ldc,
                                                              long long plane, long long M, long long N,
-                                                             long long K, DevPlan* plan,
-                                                             unsigned long long* __restrict__ lo,
-                                                             unsigned long long* __restrict__ hi) {
+                                                             long long K, DevPlan* plan, Bits* __restrict__ lo,
+                                                             Bits* __restrict__ hi) {
   constexpr int GE = GarnerGE<kEncW>::value;
+  static_assert(GE == 2, "the bound stores below write GE entries as one vector");
   wait_for_predecessor();
   if (plan->status) return;
   const int P = plan->P;
@@ -880,7 +925,7 @@ __global__ void __launch_bounds__(128) garner_enclose_kernel(const uint8_t* __re
   const long long n0 = (item - m * per_row) * GE;
   uint32_t x[GE][kEncW];
   garner_reconstruct<kEncW, GE>(RC + m * ldc + n0, plane, P, x);
-  unsigned long long l[GE], h[GE];
+  Bits l[GE], h[GE];
   if (plan->lossless) {
 #pragma unroll
     for (int e = 0; e < GE; ++e) outward_bits(x[e], Q, l[e], h[e]);
@@ -900,18 +945,27 @@ __global__ void __launch_bounds__(128) garner_enclose_kernel(const uint8_t* __re
       add_shifted(xh, K, ba, 1);
       add_shifted(xh, K, bb, 1);
       add_shifted(xh, K, 0, 1);
-      unsigned long long unused;
+      Bits unused;
       outward_bits(xl, Q, l[e], unused);
       outward_bits(xh, Q, unused, h[e]);
     }
   }
-  unsigned long long* plo = lo + m * N + n0;
-  unsigned long long* phi = hi + m * N + n0;
-  if (n0 + GE <= N && ((reinterpret_cast<uintptr_t>(plo) & 15u) == 0)) {
-#pragma unroll
-    for (int t = 0; t < GE / 2; ++t) {
-      reinterpret_cast<ulonglong2*>(plo)[t] = make_ulonglong2(l[2 * t], l[2 * t + 1]);
-      reinterpret_cast<ulonglong2*>(phi)[t] = make_ulonglong2(h[2 * t], h[2 * t + 1]);
+  Bits* plo = lo + m * N + n0;
+  Bits* phi = hi + m * N + n0;
+  constexpr unsigned kRowBytes = GE * sizeof(Bits);  // 16 (binary64) or 8 (binary32)
+  if (n0 + GE <= N && ((reinterpret_cast<uintptr_t>(plo) & (kRowBytes - 1)) == 0)) {
+    if constexpr (kRowBytes == 16) {
+      uint4 vl, vh;
+      memcpy(&vl, l, 16);
+      memcpy(&vh, h, 16);
+      *reinterpret_cast<uint4*>(plo) = vl;
+      *reinterpret_cast<uint4*>(phi) = vh;
+    } else {
+      uint2 vl, vh;
+      memcpy(&vl, l, 8);
+      memcpy(&vh, h, 8);
+      *reinterpret_cast<uint2*>(plo) = vl;
+      *reinterpret_cast<uint2*>(phi) = vh;
     }
   } else {
 #pragma unroll
@@ -974,9 +1028,13 @@ cudaError_t launch_plan(int op, const void* A, long long nA, int la, const void*
   else if (op == RG_OP_LIMBS)
     plan_limbs_kernel<<<ba + bb, 256, 0, s>>>(static_cast<const int64_t*>(A), nA, la,
                                               static_cast<const int64_t*>(B), nB, lb, ba, plan, pa);
+  else if (op == RG_OP_ENCLOSE)
+    plan_float_kernel<unsigned long long><<<ba + bb, 256, 0, s>>>(static_cast<const unsigned long long*>(A), nA,
+                                                                  static_cast<const unsigned long long*>(B), nB, ba,
+                                                                  plan, pa);
   else
-    plan_f64_kernel<<<ba + bb, 256, 0, s>>>(static_cast<const unsigned long long*>(A), nA,
-                                            static_cast<const unsigned long long*>(B), nB, ba, plan, pa);
+    plan_float_kernel<uint32_t><<<ba + bb, 256, 0, s>>>(static_cast<const uint32_t*>(A), nA,
+                                                        static_cast<const uint32_t*>(B), nB, ba, plan, pa);
   return cudaGetLastError();
 }
 
@@ -1009,10 +1067,13 @@ cudaError_t launch_split(int op, const void* A, const void* B, int la, int lb, l
   // RB [P][N][ldb], laid out like A.
   const long long M = batch * Mb;
   const long long brows = batch * (transb ? N : K), bcols = transb ? K : N;
-  if (op == RG_OP_ENCLOSE) {
+  if (op == RG_OP_ENCLOSE || op == RG_OP_ENCLOSE_F32) {
     constexpr int V = 8;
     const SplitSide sa = make_side(A, ra, M, K, lda, 1, V), sb = make_side(B, rb, brows, bcols, ldb, 1, V);
-    return launch_dependent(split_f64_kernel<V>, split_grid(sa.items + sb.items), 256, 0, st, sa, sb,
+    if (op == RG_OP_ENCLOSE)
+      return launch_dependent(split_float_kernel<unsigned long long, V>, split_grid(sa.items + sb.items), 256, 0, st,
+                              sa, sb, (const DevPlan*)plan);
+    return launch_dependent(split_float_kernel<uint32_t, V>, split_grid(sa.items + sb.items), 256, 0, st, sa, sb,
                             (const DevPlan*)plan);
   }
   const int L = la > lb ? la : lb;
@@ -1045,9 +1106,12 @@ cudaError_t launch_garner(int op, const void* RC, long long ldc, long long plane
   const uint8_t* rc = static_cast<const uint8_t*>(RC);
   auto blocks_for = [&](int ge) { return dim3((unsigned)((M * ((N + ge - 1) / ge) + 127) / 128)); };
   if (op == RG_OP_ENCLOSE)
-    return launch_dependent(garner_enclose_kernel, blocks_for(GarnerGE<kEncW>::value), 128, 0, st, rc, ldc, plane, M,
-                            N, K, plan, static_cast<unsigned long long*>(out0),
+    return launch_dependent(garner_enclose_kernel<unsigned long long>, blocks_for(GarnerGE<kEncW>::value), 128, 0, st,
+                            rc, ldc, plane, M, N, K, plan, static_cast<unsigned long long*>(out0),
                             static_cast<unsigned long long*>(out1));
+  if (op == RG_OP_ENCLOSE_F32)
+    return launch_dependent(garner_enclose_kernel<uint32_t>, blocks_for(GarnerGE<kEncW>::value), 128, 0, st, rc, ldc,
+                            plane, M, N, K, plan, static_cast<uint32_t*>(out0), static_cast<uint32_t*>(out1));
   int64_t* C = static_cast<int64_t*>(out0);
   switch (lc) {
     case 1: return launch_dependent(garner_int_kernel<1>, blocks_for(GarnerGE<2>::value), 128, 0, st, rc, ldc, plane, M, N, plan, C);

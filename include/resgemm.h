@@ -63,6 +63,7 @@ extern "C" {
 #define RG_OP_LIMBS 1
 #define RG_OP_ENCLOSE 2
 #define RG_OP_STAGE 3
+#define RG_OP_ENCLOSE_F32 4
 
 /* Limits. */
 #define RG_MAX_K 131072 /* K <= 2^17 ("exact-solve" and "enclosure-gemm", Requirements and limits) */
@@ -135,6 +136,20 @@ int enclose_gemm_f64(const double* A, const double* B, double* lo, double* hi, i
                      unsigned flags, void* ws, size_t ws_bytes, void* stream);
 
 /*
+ * enclose_gemm_f64 for binary32 operands, with binary32 bounds: lo and hi are
+ * the largest and smallest floats bracketing the exact product; overflow
+ * gives +-max finite toward zero and +-inf away from it, and a negative value
+ * too small for a subnormal gives [-2^-149, -0.0] ("enclosure-gemm", Usage:
+ * operands are float32 or float64; Correctness: the floor and ceiling in the
+ * format).  The scale exponents come from the binary32 exponent field and the
+ * 24-bit significand, so a float32 operand needs no more bits than its values
+ * span.  Regimes, workspace (RG_OP_ENCLOSE_F32) and errors as for
+ * enclose_gemm_f64.
+ */
+int enclose_gemm_f32(const float* A, const float* B, float* lo, float* hi, int64_t M, int64_t N, int64_t K,
+                     unsigned flags, void* ws, size_t ws_bytes, void* stream);
+
+/*
  * Batched forms: `batch` independent products of one shape, each operand's
  * products stored back to back: A [batch][M][K], B [batch][K][N] (with
  * RG_FLAG_TRANS_B [batch][N][K]; limbs add a last dimension as above),
@@ -152,6 +167,8 @@ int res_gemm_limbs_batched(const int64_t* A, int la, const int64_t* B, int lb, i
                            int64_t M, int64_t N, int64_t K, int nprimes, unsigned flags, void* ws, size_t ws_bytes,
                            void* stream);
 int enclose_gemm_f64_batched(const double* A, const double* B, double* lo, double* hi, int64_t batch, int64_t M,
+                             int64_t N, int64_t K, unsigned flags, void* ws, size_t ws_bytes, void* stream);
+int enclose_gemm_f32_batched(const float* A, const float* B, float* lo, float* hi, int64_t batch, int64_t M,
                              int64_t N, int64_t K, unsigned flags, void* ws, size_t ws_bytes, void* stream);
 
 /*
@@ -203,7 +220,7 @@ size_t rg_noalloc_scratch_bytes(void);
 
 /*
  * Workspace size in bytes for one call of `op` (RG_OP_*) with these shapes.
- * la, lb, lc are the limb counts (1 for RG_OP_I64 / RG_OP_ENCLOSE); nprimes
+ * la, lb, lc are the limb counts (1 for RG_OP_I64 / RG_OP_ENCLOSE[_F32]); nprimes
  * is the value the call will pass (0 = plan on the device).  flags must
  * match the call's RG_FLAG_HOST and RG_FLAG_TRANS_B bits.  Returns 0 for
  * invalid arguments.  An empty problem needs the 4 KiB plan block only.
