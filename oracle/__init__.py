@@ -67,6 +67,10 @@ def _load():
         fp = ctypes.POINTER(ctypes.c_float)
         lib.oracle_enclose_f32.argtypes = [fp, fp, fp, fp, ci, ci, ci, i64p, ci, ci]
         lib.oracle_enclose_f32.restype = ci
+        lib.oracle_interval_f64.argtypes = [dp, dp, dp, dp, dp, dp, ci, ci, ci, i64p, ci, ci]
+        lib.oracle_interval_f64.restype = ci
+        lib.oracle_interval_f32.argtypes = [fp, fp, fp, fp, fp, fp, ci, ci, ci, i64p, ci, ci]
+        lib.oracle_interval_f32.restype = ci
         lib.oracle_threads.argtypes = [ci]
         lib.oracle_threads.restype = ci
         _lib = lib
@@ -172,6 +176,33 @@ def enclose_f32(A, B, rows=None, threads: int | None = None):
         raise ValueError("non-finite operand")
     if rc == -3:
         raise MemoryError("oracle_enclose_f32")
+    if rc != 0:
+        raise RuntimeError("oracle outward search did not converge")
+    return lo, hi
+
+
+def interval(Am, Ar, Bm, Br, rows=None, threads: int | None = None):
+    """(lo, hi) [R,N] bracketing Rump's midpoint-radius product <Am, Ar> * <Bm, Br>:
+    the tightest values of the operands' format (float64 or float32) below
+    Am @ Bm - (|Am| @ Br + Ar @ |Bm| + Ar @ Br) and above Am @ Bm + (...), all exact."""
+    dt = np.float32 if np.asarray(Am).dtype == np.float32 else np.float64
+    Am, Ar, Bm, Br = (np.ascontiguousarray(x, dtype=dt) for x in (Am, Ar, Bm, Br))
+    M, K = Am.shape
+    K2, N = Bm.shape
+    assert K == K2 and Ar.shape == Am.shape and Br.shape == Bm.shape
+    r, nr = _rows_arg(rows, M)
+    lo = np.zeros((nr, N), dtype=dt)
+    hi = np.zeros((nr, N), dtype=dt)
+    ct = ctypes.c_float if dt == np.float32 else ctypes.c_double
+    fn = _load().oracle_interval_f32 if dt == np.float32 else _load().oracle_interval_f64
+    rp = _ptr(r, ctypes.c_int64) if r is not None else None
+    rc = fn(*(_ptr(x, ct) for x in (Am, Ar, Bm, Br, lo, hi)), M, N, K, rp, nr, threads or default_threads())
+    if rc == -1:
+        raise ValueError("non-finite operand")
+    if rc == -4:
+        raise ValueError("negative radius")
+    if rc == -3:
+        raise MemoryError("oracle_interval")
     if rc != 0:
         raise RuntimeError("oracle outward search did not converge")
     return lo, hi
@@ -290,3 +321,24 @@ def enclose_py(A, B, dtype=np.float64):
 def exact_dot_fraction(a_row, b_col) -> Fraction:
     """The exact real inner product of two float64 vectors."""
     return sum((Fraction(float(x)) * Fraction(float(y)) for x, y in zip(a_row, b_col)), Fraction(0))
+
+
+def interval_py(Am, Ar, Bm, Br, dtype=np.float64):
+    """interval() for tiny matrices via Fraction: midpoint S and radius R as
+    exact rationals, then the outward floor of S - R and ceiling of S + R."""
+    Am, Ar, Bm, Br = (np.asarray(x, dtype=dtype) for x in (Am, Ar, Bm, Br))
+    rnd = enclose_exact_py32 if dtype == np.float32 else enclose_exact_py
+    M, K = Am.shape
+    N = Bm.shape[1]
+    F = [[[Fraction(float(v)) for v in row] for row in X] for X in (Am, Ar, Bm, Br)]
+    fam, far, fbm, fbr = F
+    lo = [[0.0] * N for _ in range(M)]
+    hi = [[0.0] * N for _ in range(M)]
+    for i in range(M):
+        for j in range(N):
+            S = sum((fam[i][k] * fbm[k][j] for k in range(K)), Fraction(0))
+            R = sum((abs(fam[i][k]) * fbr[k][j] + far[i][k] * abs(fbm[k][j]) + far[i][k] * fbr[k][j]
+                     for k in range(K)), Fraction(0))
+            lo[i][j] = rnd(S - R)[0]
+            hi[i][j] = rnd(S + R)[1]
+    return lo, hi

@@ -23,6 +23,12 @@
  *     ceiling are taken in binary32 ("enclosure-gemm" page, Usage: operands
  *     are float32 or float64; every binary32 value is also a binary64 value,
  *     so the exact sum is formed the same way).
+ *   - oracle_interval_f64 / _f32: Rump's midpoint-radius product of interval
+ *     matrices <Am, Ar> and <Bm, Br> (radii >= 0): the exact midpoint
+ *     S = Am * Bm and the exact radius R = |Am| * Br + Ar * |Bm| + Ar * Br,
+ *     then the largest value of the format <= S - R and the smallest >= S + R
+ *     ("enclosure-gemm" page, Method: Rump's bound with its products and
+ *     radius formed exactly, so the only overestimation is the bound's).
  *
  * Parallelism: OpenMP over output rows only; every entry is computed by the
  * same sequential loop over k.
@@ -412,6 +418,132 @@ int oracle_enclose_f32(const float *A, const float *B, float *lo, float *hi, int
   free(Ad);
   free(Bd);
   return rc;
+}
+
+/* acc += sign * v, exactly (sign-magnitude). */
+static void exact_add(exact_t *acc, const exact_t *v, int sign) {
+  int vs = v->sgn * sign;
+  if (vs == 0) return;
+  if (acc->sgn == 0) {
+    acc->mag = v->mag;
+    acc->sgn = vs;
+    return;
+  }
+  if (acc->sgn == vs) {
+    uint64_t carry = 0;
+    for (int i = 0; i < GRID_W; i++) {
+      u128 t = (u128)acc->mag.w[i] + v->mag.w[i] + carry;
+      acc->mag.w[i] = (uint64_t)t;
+      carry = (uint64_t)(t >> 64);
+    }
+    return;
+  }
+  int c = grid_cmp(&acc->mag, &v->mag);
+  if (c == 0) {
+    memset(&acc->mag, 0, sizeof(acc->mag));
+    acc->sgn = 0;
+  } else if (c > 0) {
+    grid_sub(&acc->mag, &v->mag, &acc->mag);
+  } else {
+    grid_t r;
+    grid_sub(&v->mag, &acc->mag, &r);
+    acc->mag = r;
+    acc->sgn = vs;
+  }
+}
+
+/* Interval rows from double copies of the operands (radii already checked). */
+static int interval_rows(const double *Am, const double *Ar, const double *Bm, const double *Br, void *lo, void *hi,
+                         int f32, int M, int N, int K, const int64_t *rows, int nrows, int threads) {
+  double *aAm = malloc(((size_t)M * K + 1) * sizeof(double));
+  double *aBm = malloc(((size_t)K * N + 1) * sizeof(double));
+  if (!aAm || !aBm) {
+    free(aAm);
+    free(aBm);
+    return -3;
+  }
+  for (size_t t = 0; t < (size_t)M * K; t++) aAm[t] = fabs(Am[t]);
+  for (size_t t = 0; t < (size_t)K * N; t++) aBm[t] = fabs(Bm[t]);
+  int broken = 0;
+  set_threads(threads);
+#pragma omp parallel for schedule(dynamic, 1) reduction(| : broken)
+  for (int r = 0; r < nrows; r++) {
+    int64_t i = rows ? rows[r] : r;
+    for (int j = 0; j < N; j++) {
+      exact_t S, R, t, L, H;
+      exact_entry(Am, Bm, i, j, N, K, &S);
+      exact_entry(aAm, Br, i, j, N, K, &R);
+      exact_entry(Ar, aBm, i, j, N, K, &t);
+      exact_add(&R, &t, 1);
+      exact_entry(Ar, Br, i, j, N, K, &t);
+      exact_add(&R, &t, 1);
+      L = S;
+      exact_add(&L, &R, -1);
+      H = S;
+      exact_add(&H, &R, 1);
+      size_t o = (size_t)r * N + j;
+      if (f32) {
+        float unused;
+        broken |= outward_f32(&L, (float *)lo + o, &unused) != 0;
+        broken |= outward_f32(&H, &unused, (float *)hi + o) != 0;
+      } else {
+        double unused;
+        broken |= outward(&L, (double *)lo + o, &unused) != 0;
+        broken |= outward(&H, &unused, (double *)hi + o) != 0;
+      }
+    }
+  }
+  free(aAm);
+  free(aBm);
+  return broken ? -2 : 0;
+}
+
+/* Checks for the interval operands: -1 for a non-finite entry, -4 for a
+ * negative radius (a sign bit on a nonzero radius), else 0. */
+static int check_interval(const double *Am, const double *Ar, size_t n) {
+  for (size_t t = 0; t < n; t++) {
+    if (!isfinite(Am[t]) || !isfinite(Ar[t])) return -1;
+    if (Ar[t] < 0) return -4;
+  }
+  return 0;
+}
+
+/*
+ * lo, hi [nrows][N] of the interval product <Am, Ar> * <Bm, Br> for binary64
+ * operands (A [M][K], B [K][N]).  Returns 0, -1 (non-finite entry), -2 (the
+ * outward search did not converge: a defect), -3 (no memory), -4 (negative
+ * radius).
+ */
+int oracle_interval_f64(const double *Am, const double *Ar, const double *Bm, const double *Br, double *lo,
+                        double *hi, int M, int N, int K, const int64_t *rows, int nrows, int threads) {
+  if (!rows) nrows = M;
+  int c = check_interval(Am, Ar, (size_t)M * K);
+  if (!c) c = check_interval(Bm, Br, (size_t)K * N);
+  if (c) return c;
+  return interval_rows(Am, Ar, Bm, Br, lo, hi, 0, M, N, K, rows, nrows, threads);
+}
+
+/* The same for binary32 operands and binary32 bounds. */
+int oracle_interval_f32(const float *Am, const float *Ar, const float *Bm, const float *Br, float *lo, float *hi,
+                        int M, int N, int K, const int64_t *rows, int nrows, int threads) {
+  if (!rows) nrows = M;
+  size_t na = (size_t)M * K, nb = (size_t)K * N;
+  double *d = malloc((2 * na + 2 * nb + 1) * sizeof(double));
+  if (!d) return -3;
+  double *dAm = d, *dAr = d + na, *dBm = d + 2 * na, *dBr = d + 2 * na + nb;
+  for (size_t t = 0; t < na; t++) {
+    dAm[t] = (double)Am[t]; /* exact */
+    dAr[t] = (double)Ar[t];
+  }
+  for (size_t t = 0; t < nb; t++) {
+    dBm[t] = (double)Bm[t];
+    dBr[t] = (double)Br[t];
+  }
+  int c = check_interval(dAm, dAr, na);
+  if (!c) c = check_interval(dBm, dBr, nb);
+  if (!c) c = interval_rows(dAm, dAr, dBm, dBr, lo, hi, 1, M, N, K, rows, nrows, threads);
+  free(d);
+  return c;
 }
 
 /* Number of OpenMP threads a parallel region will use. */
