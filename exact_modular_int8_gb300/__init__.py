@@ -35,10 +35,12 @@ RG_ERR_LOSSY = 4
 RG_ERR_WORKSPACE = 5
 RG_ERR_CUDA = 6
 RG_ERR_TIMEOUT = 7
+RG_ERR_RADIUS = 8
 RG_FLAG_SYNC = 1
 RG_FLAG_HOST = 2
 RG_FLAG_TRANS_B = 4
 RG_OP_I64, RG_OP_LIMBS, RG_OP_ENCLOSE, RG_OP_STAGE, RG_OP_ENCLOSE_F32 = 0, 1, 2, 3, 4
+RG_OP_INTERVAL, RG_OP_INTERVAL_F32 = 5, 6
 MAX_K = 131072
 NUM_PRIMES = 53
 
@@ -47,7 +49,8 @@ EXPORTED = (
     "rg_workspace_layout", "rg_get_plan", "rg_status", "rg_prime", "rg_strerror", "rg_set_wait_limit_ns",
     "rg_inject_fault", "res_gemm_i64_noalloc", "rg_noalloc_scratch_bytes", "rg_set_gemm_variant",
     "res_gemm_i64_batched", "res_gemm_limbs_batched", "enclose_gemm_f64_batched", "rg_workspace_bytes_batched",
-    "rg_workspace_layout_batched", "enclose_gemm_f32", "enclose_gemm_f32_batched",
+    "rg_workspace_layout_batched", "enclose_gemm_f32", "enclose_gemm_f32_batched", "interval_gemm_f64",
+    "interval_gemm_f32", "interval_gemm_f64_batched", "interval_gemm_f32_batched",
 )
 
 
@@ -97,9 +100,14 @@ def library():
             lib.enclose_gemm_f64_batched.argtypes = [vp, vp, vp, vp, i64, i64, i64, i64, cu, vp, sz, vp]
             lib.enclose_gemm_f32.argtypes = [vp, vp, vp, vp, i64, i64, i64, cu, vp, sz, vp]
             lib.enclose_gemm_f32_batched.argtypes = [vp, vp, vp, vp, i64, i64, i64, i64, cu, vp, sz, vp]
+            for f in ("interval_gemm_f64", "interval_gemm_f32"):
+                getattr(lib, f).argtypes = [vp, vp, vp, vp, vp, vp, i64, i64, i64, cu, vp, sz, vp]
+            for f in ("interval_gemm_f64_batched", "interval_gemm_f32_batched"):
+                getattr(lib, f).argtypes = [vp, vp, vp, vp, vp, vp, i64, i64, i64, i64, cu, vp, sz, vp]
             for f in ("res_gemm_i64", "res_gemm_limbs", "enclose_gemm_f64", "res_gemm_stage", "res_gemm_i64_batched",
                       "res_gemm_limbs_batched", "enclose_gemm_f64_batched", "enclose_gemm_f32",
-                      "enclose_gemm_f32_batched"):
+                      "enclose_gemm_f32_batched", "interval_gemm_f64", "interval_gemm_f32",
+                      "interval_gemm_f64_batched", "interval_gemm_f32_batched"):
                 getattr(lib, f).restype = ci
             lib.rg_workspace_bytes.argtypes = [ci, i64, i64, i64, ci, ci, ci, ci, cu]
             lib.rg_workspace_bytes.restype = sz
@@ -329,6 +337,50 @@ def mm_enclose(A: torch.Tensor, B: torch.Tensor):
 def mm_enclose_nt(A: torch.Tensor, Bt: torch.Tensor):
     """The bracket of A @ Bt.T without a transposed copy ("enclosure-gemm", Usage: mm_enclose_nt)."""
     return enclose_gemm(A, Bt, transb=True)
+
+
+def interval_gemm(Am: torch.Tensor, Ar: torch.Tensor, Bm: torch.Tensor, Br: torch.Tensor, sync: bool = True,
+                  ws: torch.Tensor | None = None, transb: bool = False):
+    """(lo, hi) enclosing every product A @ B with A in <Am, Ar>, B in <Bm, Br> (midpoint, radius >= 0),
+    by Rump's bound formed exactly and rounded outward once, in the operands' format (float64 or
+    float32).  transb gives Bm and Br as [N, K]; a leading batch dimension shares one plan."""
+    ts = (Am, Ar, Bm, Br)
+    if any(t.dtype != Am.dtype for t in ts) or Am.dtype not in (torch.float64, torch.float32):
+        raise ValueError("float64 or float32 operands of one dtype expected")
+    if Ar.shape != Am.shape or Br.shape != Bm.shape:
+        raise ValueError("each radius must have its midpoint's shape")
+    sh = _shapes(Am, Bm, transb, 0)
+    if sh is None:
+        raise ValueError("Am [M,K] and Bm [K,N] (transb: [N,K]) expected, optionally with a batch dimension")
+    batched, batch, M, N, K, _, _ = sh
+    f32 = Am.dtype == torch.float32
+    op = RG_OP_INTERVAL_F32 if f32 else RG_OP_INTERVAL
+    Am, Ar, Bm, Br = (t.contiguous() for t in ts)
+    dev, flags = _call_ctx(torch.empty(0, device=Am.device), torch.empty(0, device=Bm.device))
+    if {t.device for t in (Am, Ar, Bm, Br)} != {Am.device}:
+        raise ValueError("operands must be on one device")
+    flags |= (RG_FLAG_SYNC if sync else 0) | (RG_FLAG_TRANS_B if transb else 0)
+    pin = bool(flags & RG_FLAG_HOST)
+    shape = (batch, M, N) if batched else (M, N)
+    lo = torch.empty(shape, dtype=Am.dtype, device=Am.device, pin_memory=pin)
+    hi = torch.empty(shape, dtype=Am.dtype, device=Am.device, pin_memory=pin)
+    name = "interval_gemm_f32" if f32 else "interval_gemm_f64"
+    with torch.cuda.device(dev):
+        need = workspace_bytes(op, M, N, K, host=pin, transb=transb, batch=batch)
+        if need == 0:
+            raise ResGemmError(RG_ERR_ARG, name)
+        w = ws if ws is not None else workspace(need, dev)
+        rc = getattr(library(), name + "_batched")(Am.data_ptr(), Ar.data_ptr(), Bm.data_ptr(), Br.data_ptr(),
+                                                   lo.data_ptr(), hi.data_ptr(), batch, M, N, K, flags,
+                                                   w.data_ptr(), w.numel(), torch.cuda.current_stream(dev).cuda_stream)
+    _check(rc, name)
+    return lo, hi
+
+
+def mm_interval(A_mid: torch.Tensor, A_rad: torch.Tensor, B_mid: torch.Tensor, B_rad: torch.Tensor):
+    """Rump's midpoint-radius product of interval matrices as an outward (lo, hi)
+    ("enclosure-gemm", Usage: mm_interval)."""
+    return interval_gemm(A_mid, A_rad, B_mid, B_rad)
 
 
 def bmm_enclose(A: torch.Tensor, B: torch.Tensor):

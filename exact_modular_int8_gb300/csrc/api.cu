@@ -61,11 +61,17 @@ struct Layout {
   int pmax;
 };
 
-bool is_enclose(int op) { return op == RG_OP_ENCLOSE || op == RG_OP_ENCLOSE_F32; }
+bool is_interval(int op) { return op == RG_OP_INTERVAL || op == RG_OP_INTERVAL_F32; }
+// operations with two outputs (lo, hi)
+bool is_enclose(int op) { return op == RG_OP_ENCLOSE || op == RG_OP_ENCLOSE_F32 || is_interval(op); }
+// residue planes per product and prime: intervals need three products
+int planes_per_product(int op) { return is_interval(op) ? 3 : 1; }
+// arrays per operand: an interval operand is a midpoint and a radius array
+int arrays_per_operand(int op) { return is_interval(op) ? 2 : 1; }
 
 // Bytes of one operand or output entry: limbs of int64, one int64, one double or one float.
 size_t elem_bytes(int op, int limbs) {
-  return op == RG_OP_LIMBS ? 8 * (size_t)limbs : op == RG_OP_ENCLOSE_F32 ? 4 : 8;
+  return op == RG_OP_LIMBS ? 8 * (size_t)limbs : (op == RG_OP_ENCLOSE_F32 || op == RG_OP_INTERVAL_F32) ? 4 : 8;
 }
 
 // An empty problem (batch, M, N or K zero) needs only the plan block.
@@ -93,18 +99,20 @@ bool make_layout(int op, long long batch, long long M, long long N, long long K,
   }
   int pmax = pmax_for(op, K, la, lb, nprimes);
   L->pmax = pmax;
+  const size_t planes = (size_t)pmax * planes_per_product(op) * batch;
   L->ra = off;
-  off = align_up(off + (size_t)pmax * batch * M * L->lda * 2, kAlign);
+  off = align_up(off + planes * M * L->lda * 2, kAlign);
   L->rb = off;
-  off = align_up(off + (size_t)pmax * batch * (transb ? N : K) * L->ldb * 2, kAlign);
+  off = align_up(off + planes * (transb ? N : K) * L->ldb * 2, kAlign);
   L->rc = off;
-  off = align_up(off + (size_t)pmax * batch * M * L->ldc, kAlign);
+  off = align_up(off + planes * M * L->ldc, kAlign);
   if (flags & RG_FLAG_HOST) {
     size_t ea = elem_bytes(op, la), eb = elem_bytes(op, lb), ec = elem_bytes(op, lc);
+    const size_t arrays = arrays_per_operand(op);
     L->a = off;
-    off = align_up(off + (size_t)batch * M * K * ea, kAlign);
+    off = align_up(off + arrays * batch * M * K * ea, kAlign);
     L->b = off;
-    off = align_up(off + (size_t)batch * K * N * eb, kAlign);
+    off = align_up(off + arrays * batch * K * N * eb, kAlign);
     L->c = off;
     off = align_up(off + (size_t)batch * M * N * ec, kAlign);
     if (is_enclose(op)) {
@@ -131,15 +139,18 @@ int finish(void* ws, cudaStream_t s, unsigned flags) {
     if (e_ != cudaSuccess) return RG_ERR_CUDA; \
   } while (0)
 
-// Shared driver for the integer/fp64 entry points; `batch` products of the
-// same shape share one plan (one prime count, one pair of scale exponents).
-int run(int op, const void* A, int la, const void* B, int lb, void* C, void* C2, int lc, long long batch, long long M,
-        long long N, long long K, int nprimes, unsigned flags, void* ws, size_t ws_bytes, void* stream) {
+// Shared driver for every entry point; `batch` products of the same shape
+// share one plan (one prime count, one pair of scale exponents).  A2 and B2
+// are the radii of interval operands (null otherwise).
+int run(int op, const void* A, const void* A2, int la, const void* B, const void* B2, int lb, void* C, void* C2,
+        int lc, long long batch, long long M, long long N, long long K, int nprimes, unsigned flags, void* ws,
+        size_t ws_bytes, void* stream) {
   if (!ws || (reinterpret_cast<uintptr_t>(ws) & 255u) != 0) return RG_ERR_ARG;
   if (batch < 0 || M < 0 || N < 0 || K < 0 || nprimes < 0 || nprimes > kNumPrimes) return RG_ERR_ARG;
   // an empty problem reads no operand, and writes outputs only if it has entries
   const bool empty = is_empty(batch, M, N, K), has_out = batch && M && N;
-  if ((!empty && (!A || !B)) || (has_out && (!C || (is_enclose(op) && !C2)))) return RG_ERR_ARG;
+  if ((!empty && (!A || !B || (is_interval(op) && (!A2 || !B2)))) || (has_out && (!C || (is_enclose(op) && !C2))))
+    return RG_ERR_ARG;
   if (op == RG_OP_LIMBS &&
       (la < 1 || la > RG_MAX_LIMBS_IN || lb < 1 || lb > RG_MAX_LIMBS_IN || lc < 1 || lc > RG_MAX_LIMBS_OUT))
     return RG_ERR_ARG;
@@ -149,7 +160,8 @@ int run(int op, const void* A, int la, const void* B, int lb, void* C, void* C2,
   if (!make_layout(op, batch, M, N, K, la, lb, lc, nprimes, flags, &L)) return RG_ERR_ARG;
   if (ws_bytes < L.total) return RG_ERR_WORKSPACE;
   // the persistent GEMM numbers its tiles (plane, row block, column block) in int
-  if ((long long)L.pmax * batch * ((M + 127) / 128) * ((N + 255) / 256) > (1LL << 31) - 1) return RG_ERR_ARG;
+  const long long gemm_batch = batch * planes_per_product(op);
+  if ((long long)L.pmax * gemm_batch * ((M + 127) / 128) * ((N + 255) / 256) > (1LL << 31) - 1) return RG_ERR_ARG;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   uint8_t* w = static_cast<uint8_t*>(ws);
   DevPlan* plan = reinterpret_cast<DevPlan*>(w + L.plan);
@@ -171,16 +183,25 @@ int run(int op, const void* A, int la, const void* B, int lb, void* C, void* C2,
   }
   RG_TRY(upload_tables());
   const void* dA = A;
+  const void* dA2 = A2;
   const void* dB = B;
+  const void* dB2 = B2;
   void* dC = C;
   void* dC2 = C2;
   if (flags & RG_FLAG_HOST) {
+    const size_t na = (size_t)batch * M * K * ea, nb = (size_t)batch * K * N * eb;
     dA = w + L.a;
     dB = w + L.b;
     dC = w + L.c;
     dC2 = is_enclose(op) ? static_cast<void*>(w + L.c2) : nullptr;
-    RG_TRY(cudaMemcpyAsync(const_cast<void*>(dA), A, (size_t)batch * M * K * ea, cudaMemcpyHostToDevice, s));
-    RG_TRY(cudaMemcpyAsync(const_cast<void*>(dB), B, (size_t)batch * K * N * eb, cudaMemcpyHostToDevice, s));
+    RG_TRY(cudaMemcpyAsync(const_cast<void*>(dA), A, na, cudaMemcpyHostToDevice, s));
+    RG_TRY(cudaMemcpyAsync(const_cast<void*>(dB), B, nb, cudaMemcpyHostToDevice, s));
+    if (is_interval(op)) {  // radii right after the midpoints
+      dA2 = w + L.a + na;
+      dB2 = w + L.b + nb;
+      RG_TRY(cudaMemcpyAsync(const_cast<void*>(dA2), A2, na, cudaMemcpyHostToDevice, s));
+      RG_TRY(cudaMemcpyAsync(const_cast<void*>(dB2), B2, nb, cudaMemcpyHostToDevice, s));
+    }
   }
   RG_TRY(cudaMemsetAsync(plan, 0, sizeof(DevPlan), s));
   const int la1 = op == RG_OP_LIMBS ? la : 1, lb1 = op == RG_OP_LIMBS ? lb : 1, lc1 = op == RG_OP_LIMBS ? lc : 1;
@@ -188,17 +209,19 @@ int run(int op, const void* A, int la, const void* B, int lb, void* C, void* C2,
   // plan; the other operations run the planner kernel first
   const bool i64 = op == RG_OP_I64;
   if (!i64)
-    RG_TRY(launch_plan(op, dA, batch * M * K, la1, dB, batch * K * N, lb1, lc1, K, is_enclose(op) ? 0 : nprimes,
-                       plan, s));
+    RG_TRY(launch_plan(op, dA, dA2, batch * M * K, la1, dB, dB2, batch * K * N, lb1, lc1, K,
+                       is_enclose(op) ? 0 : nprimes, plan, s));
   const bool transb = (flags & RG_FLAG_TRANS_B) != 0;
-  RG_TRY(launch_split(op, dA, dB, la1, lb1, batch, M, N, K, L.lda, L.ldb, w + L.ra, w + L.rb, plan, L.pmax, transb,
-                      s));
+  RG_TRY(launch_split(op, dA, dA2, dB, dB2, la1, lb1, batch, M, N, K, L.lda, L.ldb, w + L.ra, w + L.rb, plan, L.pmax,
+                      transb, s));
   int fault = g_fault.exchange(0);
-  RG_TRY(launch_gemm(w + L.ra, L.lda, w + L.rb, L.ldb, w + L.rc, L.ldc, L.pmax, (int)batch, i64 ? nprimes : 0, M, N,
-                     K, plan, s, fault, g_wait_ns.load(), i64, transb));
-  // Garner sees the batch as batch * M rows of one plane per prime
-  RG_TRY(launch_garner(op, w + L.rc, L.ldc, batch * M * L.ldc, batch * M, N, K, op == RG_OP_LIMBS ? lc : 1, plan, dC,
-                       dC2, s));
+  RG_TRY(launch_gemm(w + L.ra, L.lda, w + L.rb, L.ldb, w + L.rc, L.ldc, L.pmax, (int)gemm_batch, i64 ? nprimes : 0,
+                     M, N, K, plan, s, fault, g_wait_ns.load(), i64, transb));
+  // Garner sees the batch as batch * M rows of each plane; an interval's
+  // three product planes lie batch * M rows apart
+  const long long sub = batch * M * L.ldc;
+  RG_TRY(launch_garner(op, w + L.rc, L.ldc, planes_per_product(op) * sub, sub, batch * M, N, K,
+                       op == RG_OP_LIMBS ? lc : 1, plan, dC, dC2, s));
   if (flags & RG_FLAG_HOST) {
     RG_TRY(cudaMemcpyAsync(C, dC, out_bytes, cudaMemcpyDeviceToHost, s));
     if (is_enclose(op)) RG_TRY(cudaMemcpyAsync(C2, dC2, out_bytes, cudaMemcpyDeviceToHost, s));
@@ -212,43 +235,69 @@ extern "C" {
 
 int res_gemm_i64(const int64_t* A, const int64_t* B, int64_t* C, int64_t M, int64_t N, int64_t K, int nprimes,
                  unsigned flags, void* ws, size_t ws_bytes, void* stream) {
-  return run(RG_OP_I64, A, 1, B, 1, C, nullptr, 1, 1, M, N, K, nprimes, flags, ws, ws_bytes, stream);
+  return run(RG_OP_I64, A, nullptr, 1, B, nullptr, 1, C, nullptr, 1, 1, M, N, K, nprimes, flags, ws, ws_bytes, stream);
 }
 
 int res_gemm_limbs(const int64_t* A, int la, const int64_t* B, int lb, int64_t* C, int lc, int64_t M, int64_t N,
                    int64_t K, int nprimes, unsigned flags, void* ws, size_t ws_bytes, void* stream) {
-  return run(RG_OP_LIMBS, A, la, B, lb, C, nullptr, lc, 1, M, N, K, nprimes, flags, ws, ws_bytes, stream);
+  return run(RG_OP_LIMBS, A, nullptr, la, B, nullptr, lb, C, nullptr, lc, 1, M, N, K, nprimes,
+             flags, ws, ws_bytes, stream);
 }
 
 int enclose_gemm_f64(const double* A, const double* B, double* lo, double* hi, int64_t M, int64_t N, int64_t K,
                      unsigned flags, void* ws, size_t ws_bytes, void* stream) {
-  return run(RG_OP_ENCLOSE, A, 1, B, 1, lo, hi, 1, 1, M, N, K, 0, flags, ws, ws_bytes, stream);
+  return run(RG_OP_ENCLOSE, A, nullptr, 1, B, nullptr, 1, lo, hi, 1, 1, M, N, K, 0, flags, ws, ws_bytes, stream);
 }
 
 int enclose_gemm_f32(const float* A, const float* B, float* lo, float* hi, int64_t M, int64_t N, int64_t K,
                      unsigned flags, void* ws, size_t ws_bytes, void* stream) {
-  return run(RG_OP_ENCLOSE_F32, A, 1, B, 1, lo, hi, 1, 1, M, N, K, 0, flags, ws, ws_bytes, stream);
+  return run(RG_OP_ENCLOSE_F32, A, nullptr, 1, B, nullptr, 1, lo, hi, 1, 1, M, N, K, 0, flags, ws, ws_bytes, stream);
 }
 
 int enclose_gemm_f32_batched(const float* A, const float* B, float* lo, float* hi, int64_t batch, int64_t M,
                              int64_t N, int64_t K, unsigned flags, void* ws, size_t ws_bytes, void* stream) {
-  return run(RG_OP_ENCLOSE_F32, A, 1, B, 1, lo, hi, 1, batch, M, N, K, 0, flags, ws, ws_bytes, stream);
+  return run(RG_OP_ENCLOSE_F32, A, nullptr, 1, B, nullptr, 1, lo, hi, 1, batch, M, N, K, 0,
+             flags, ws, ws_bytes, stream);
+}
+
+int interval_gemm_f64_batched(const double* Am, const double* Ar, const double* Bm, const double* Br, double* lo,
+                              double* hi, int64_t batch, int64_t M, int64_t N, int64_t K, unsigned flags, void* ws,
+                              size_t ws_bytes, void* stream) {
+  return run(RG_OP_INTERVAL, Am, Ar, 1, Bm, Br, 1, lo, hi, 1, batch, M, N, K, 0, flags, ws, ws_bytes, stream);
+}
+
+int interval_gemm_f64(const double* Am, const double* Ar, const double* Bm, const double* Br, double* lo, double* hi,
+                      int64_t M, int64_t N, int64_t K, unsigned flags, void* ws, size_t ws_bytes, void* stream) {
+  return run(RG_OP_INTERVAL, Am, Ar, 1, Bm, Br, 1, lo, hi, 1, 1, M, N, K, 0, flags, ws, ws_bytes, stream);
+}
+
+int interval_gemm_f32_batched(const float* Am, const float* Ar, const float* Bm, const float* Br, float* lo,
+                              float* hi, int64_t batch, int64_t M, int64_t N, int64_t K, unsigned flags, void* ws,
+                              size_t ws_bytes, void* stream) {
+  return run(RG_OP_INTERVAL_F32, Am, Ar, 1, Bm, Br, 1, lo, hi, 1, batch, M, N, K, 0, flags, ws, ws_bytes, stream);
+}
+
+int interval_gemm_f32(const float* Am, const float* Ar, const float* Bm, const float* Br, float* lo, float* hi,
+                      int64_t M, int64_t N, int64_t K, unsigned flags, void* ws, size_t ws_bytes, void* stream) {
+  return run(RG_OP_INTERVAL_F32, Am, Ar, 1, Bm, Br, 1, lo, hi, 1, 1, M, N, K, 0, flags, ws, ws_bytes, stream);
 }
 
 int res_gemm_i64_batched(const int64_t* A, const int64_t* B, int64_t* C, int64_t batch, int64_t M, int64_t N,
                          int64_t K, int nprimes, unsigned flags, void* ws, size_t ws_bytes, void* stream) {
-  return run(RG_OP_I64, A, 1, B, 1, C, nullptr, 1, batch, M, N, K, nprimes, flags, ws, ws_bytes, stream);
+  return run(RG_OP_I64, A, nullptr, 1, B, nullptr, 1, C, nullptr, 1, batch, M, N, K, nprimes,
+             flags, ws, ws_bytes, stream);
 }
 
 int res_gemm_limbs_batched(const int64_t* A, int la, const int64_t* B, int lb, int64_t* C, int lc, int64_t batch,
                            int64_t M, int64_t N, int64_t K, int nprimes, unsigned flags, void* ws, size_t ws_bytes,
                            void* stream) {
-  return run(RG_OP_LIMBS, A, la, B, lb, C, nullptr, lc, batch, M, N, K, nprimes, flags, ws, ws_bytes, stream);
+  return run(RG_OP_LIMBS, A, nullptr, la, B, nullptr, lb, C, nullptr, lc, batch, M, N, K, nprimes,
+             flags, ws, ws_bytes, stream);
 }
 
 int enclose_gemm_f64_batched(const double* A, const double* B, double* lo, double* hi, int64_t batch, int64_t M,
                              int64_t N, int64_t K, unsigned flags, void* ws, size_t ws_bytes, void* stream) {
-  return run(RG_OP_ENCLOSE, A, 1, B, 1, lo, hi, 1, batch, M, N, K, 0, flags, ws, ws_bytes, stream);
+  return run(RG_OP_ENCLOSE, A, nullptr, 1, B, nullptr, 1, lo, hi, 1, batch, M, N, K, 0, flags, ws, ws_bytes, stream);
 }
 
 int res_gemm_stage(const uint16_t* RA, int64_t lda, const uint16_t* RB, int64_t ldb, uint8_t* RC, int64_t ldc,
@@ -276,7 +325,7 @@ int res_gemm_stage(const uint16_t* RA, int64_t lda, const uint16_t* RB, int64_t 
 size_t rg_workspace_bytes_batched(int op, int64_t batch, int64_t M, int64_t N, int64_t K, int la, int lb, int lc,
                                   int nprimes, unsigned flags) {
   Layout L;
-  if (op < RG_OP_I64 || op > RG_OP_ENCLOSE_F32) return 0;
+  if (op < RG_OP_I64 || op > RG_OP_INTERVAL_F32) return 0;
   if (!make_layout(op, batch, M, N, K, la, lb, lc, nprimes, flags, &L)) return 0;
   return L.total;
 }
@@ -289,7 +338,7 @@ size_t rg_workspace_bytes(int op, int64_t M, int64_t N, int64_t K, int la, int l
 int rg_workspace_layout_batched(int op, int64_t batch, int64_t M, int64_t N, int64_t K, int la, int lb, int lc,
                                 int nprimes, unsigned flags, rg_layout* out) {
   Layout L;
-  if (!out || op < RG_OP_I64 || op > RG_OP_ENCLOSE_F32) return RG_ERR_ARG;
+  if (!out || op < RG_OP_I64 || op > RG_OP_INTERVAL_F32) return RG_ERR_ARG;
   if (!make_layout(op, batch, M, N, K, la, lb, lc, nprimes, flags, &L)) return RG_ERR_ARG;
   out->ra = L.ra;
   out->rb = L.rb;
@@ -338,6 +387,7 @@ const char* rg_strerror(int code) {
     case RG_ERR_WORKSPACE: return "workspace too small";
     case RG_ERR_CUDA: return "CUDA error";
     case RG_ERR_TIMEOUT: return "a bounded wait inside a kernel expired";
+    case RG_ERR_RADIUS: return "an interval radius entry is negative";
     default: return "unknown status";
   }
 }
@@ -395,5 +445,6 @@ extern "C" int res_gemm_i64_noalloc(const int64_t* A, const int64_t* B, int64_t*
   void* ws = nullptr;
   int rc = noalloc_scratch(&ws);
   if (rc != RG_OK) return rc;
-  return run(RG_OP_I64, A, 1, B, 1, C, nullptr, 1, 1, M, N, K, nprimes, flags, ws, kNoAllocScratchBytes, stream);
+  return run(RG_OP_I64, A, nullptr, 1, B, nullptr, 1, C, nullptr, 1, 1, M, N, K, nprimes,
+             flags, ws, kNoAllocScratchBytes, stream);
 }

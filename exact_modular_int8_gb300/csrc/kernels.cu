@@ -152,12 +152,19 @@ __device__ LocalPlan finalize_plan(DevPlan* plan, const PlanArgs& a) {
       p.nchunk_b = p.bits_b <= 23 ? 0 : min((p.bits_b + 1 + kChunkBits - 1) / kChunkBits, full_chunks(a.lb));
       if (p.T > RG_MAX_BOUND_BITS || p.T > 64 * a.lc - 1) p.status = RG_ERR_RANGE;
     }
-  } else {  // RG_OP_ENCLOSE, RG_OP_ENCLOSE_F32
+  } else {  // RG_OP_ENCLOSE[_F32], RG_OP_INTERVAL[_F32]
     if (__ldcg(&plan->nonfinite)) {
       p.status = RG_ERR_NONFINITE;
       return p;
     }
-    const bool f32 = a.op == RG_OP_ENCLOSE_F32;
+    if (__ldcg(&plan->neg_radius)) {
+      p.status = RG_ERR_RADIUS;
+      return p;
+    }
+    const bool f32 = a.op == RG_OP_ENCLOSE_F32 || a.op == RG_OP_INTERVAL_F32;
+    // intervals: the midpoint and the two radius products add up to at most
+    // 4 K 2^(bits_a + bits_b), two bits above a point product
+    const int extra = (a.op == RG_OP_INTERVAL || a.op == RG_OP_INTERVAL_F32) ? 2 : 0;
     const int sig = f32 ? FloatFormat<uint32_t>::kFracBits + 1 : FloatFormat<unsigned long long>::kFracBits + 1;
     const int bias = f32 ? FloatFormat<uint32_t>::kLsbBias : FloatFormat<unsigned long long>::kLsbBias;
     const int ea = __ldcg(&plan->maxe_a), eb = __ldcg(&plan->maxe_b);
@@ -168,7 +175,7 @@ __device__ LocalPlan finalize_plan(DevPlan* plan, const PlanArgs& a) {
     // product fits the residue range (enclosure-gemm, Method): the larger
     // operand gives up bits first
     int ba = min(bits_a0, 255), bb = min(bits_b0, 255);
-    int excess = ba + bb + ck - RG_MAX_BOUND_BITS;
+    int excess = ba + bb + ck + extra - RG_MAX_BOUND_BITS;
     if (excess > 0) {
       const int d = min(excess, abs(ba - bb));
       if (ba >= bb) ba -= d; else bb -= d;
@@ -180,7 +187,7 @@ __device__ LocalPlan finalize_plan(DevPlan* plan, const PlanArgs& a) {
     p.bits_b = bb;
     p.f_a = ea ? bias - mina - (bits_a0 - ba) : 0;
     p.f_b = eb ? bias - minb - (bits_b0 - bb) : 0;
-    p.T = ba + bb + ck;
+    p.T = ba + bb + ck + extra;
     p.lossless = ba == bits_a0 && bb == bits_b0;
   }
   if (p.status) return p;
@@ -309,39 +316,57 @@ __device__ __forceinline__ void exponent_stats(Bits v, int& emax, int& einv, int
   }
 }
 
+// One array's share of the exponent reductions (16-byte loads when aligned);
+// a radius array also flags negative entries (a set sign bit on a nonzero).
 template <typename Bits>
-__global__ void __launch_bounds__(256) plan_float_kernel(const Bits* __restrict__ A, long long nA,
-                                                         const Bits* __restrict__ B, long long nB, int nbA,
-                                                         DevPlan* plan, PlanArgs pa) {
+__device__ __forceinline__ void scan_float(const Bits* __restrict__ X, long long n, const PlannerSide& sd,
+                                           bool radius, int& emax, int& einv, int& bad, int& negr) {
+  using F = FloatFormat<Bits>;
   constexpr int PER = 16 / sizeof(Bits);  // entries per 16-byte load
-  const PlannerSide sd = planner_side(nbA);
-  const Bits* X = sd.isA ? A : B;
-  const long long n = sd.isA ? nA : nB;
   const long long nv = (reinterpret_cast<uintptr_t>(X) & 15u) == 0 ? n / PER : 0;
   const uint4* X4 = reinterpret_cast<const uint4*>(X);
-  int emax = 0, einv = 0, bad = 0;
+  auto one = [&](Bits v) {
+    exponent_stats<Bits>(v, emax, einv, bad);
+    if (radius && (v & F::kSign) && (Bits)(v << 1) != 0) negr = 1;
+  };
 #pragma unroll 4
   for (long long i = sd.b0 * blockDim.x + threadIdx.x; i < nv; i += sd.stride) {
     const uint4 v = __ldg(X4 + i);
     if constexpr (PER == 4) {
-      exponent_stats<Bits>(v.x, emax, einv, bad);
-      exponent_stats<Bits>(v.y, emax, einv, bad);
-      exponent_stats<Bits>(v.z, emax, einv, bad);
-      exponent_stats<Bits>(v.w, emax, einv, bad);
+      one(v.x);
+      one(v.y);
+      one(v.z);
+      one(v.w);
     } else {
-      exponent_stats<Bits>(((unsigned long long)v.y << 32) | v.x, emax, einv, bad);
-      exponent_stats<Bits>(((unsigned long long)v.w << 32) | v.z, emax, einv, bad);
+      one(((unsigned long long)v.y << 32) | v.x);
+      one(((unsigned long long)v.w << 32) | v.z);
     }
   }
-  for (long long i = PER * nv + sd.b0 * blockDim.x + threadIdx.x; i < n; i += sd.stride)
-    exponent_stats(__ldg(X + i), emax, einv, bad);
+  for (long long i = PER * nv + sd.b0 * blockDim.x + threadIdx.x; i < n; i += sd.stride) one(__ldg(X + i));
+}
+
+// A and B, each with an optional radius array of the same size (intervals:
+// one scale covers an operand's midpoints and radii).
+template <typename Bits>
+__global__ void __launch_bounds__(256) plan_float_kernel(const Bits* __restrict__ A, const Bits* __restrict__ A2,
+                                                         long long nA, const Bits* __restrict__ B,
+                                                         const Bits* __restrict__ B2, long long nB, int nbA,
+                                                         DevPlan* plan, PlanArgs pa) {
+  const PlannerSide sd = planner_side(nbA);
+  const long long n = sd.isA ? nA : nB;
+  const Bits* X2 = sd.isA ? A2 : B2;
+  int emax = 0, einv = 0, bad = 0, negr = 0;
+  scan_float<Bits>(sd.isA ? A : B, n, sd, false, emax, einv, bad, negr);
+  if (X2) scan_float<Bits>(X2, n, sd, true, emax, einv, bad, negr);
   emax = block_max_i32(emax);
   einv = block_max_i32(einv);
   bad = block_max_i32(bad);
+  negr = block_max_i32(negr);
   if (threadIdx.x == 0) {
     if (emax) atomicMax(sd.isA ? &plan->maxe_a : &plan->maxe_b, emax);
     if (einv) atomicMax(sd.isA ? &plan->inv_mine_a : &plan->inv_mine_b, einv);
     if (bad) atomicMax(&plan->nonfinite, 1);
+    if (negr) atomicMax(&plan->neg_radius, 1);
   }
   planner_finish(plan, pa);
 }
@@ -560,6 +585,31 @@ __global__ void __launch_bounds__(256) split_i64_kernel(SplitSide sa, SplitSide 
   allow_dependents();
 }
 
+// |x| * 2^f for a floating-point x, from its bit pattern: at a lossless point
+// |x| 2^f = t * 2^(12 c0) exactly (lost = false); at a coarsened point
+// t = floor(|x| 2^f), c0 = 0, and lost tells whether any bit was dropped.
+template <typename Bits>
+__device__ __forceinline__ void scaled_magnitude(Bits v, int f, bool& neg, unsigned long long& t, bool& lost,
+                                                 int& c0) {
+  using F = FloatFormat<Bits>;
+  const int be = (int)((v >> F::kFracBits) & F::kExpMask);
+  neg = (v & F::kSign) != 0;
+  const unsigned long long hidden = 1ull << F::kFracBits;
+  const unsigned long long m = ((unsigned long long)v & (hidden - 1ull)) | (be ? hidden : 0ull);
+  int sh = (be > 1 ? be : 1) - F::kLsbBias + f;  // |x| * 2^f = m * 2^sh
+  if (m == 0 || sh >= 0) {
+    if (m == 0) sh = 0;
+    c0 = sh / kChunkBits;
+    t = m << (sh % kChunkBits);
+    lost = false;
+  } else {
+    const int r = -sh;
+    t = r >= 64 ? 0ull : m >> r;
+    lost = r >= 64 ? true : (m & ((1ull << r) - 1ull)) != 0ull;
+    c0 = 0;
+  }
+}
+
 // Floating-point operands: X' = x * 2^f = +-m * 2^sh with
 // sh = max(be,1) - min(be',1) >= 0 when lossless; the significand (53 bits for
 // binary64, 24 for binary32) shifted by sh % 12 is cut into NC chunks starting
@@ -605,26 +655,10 @@ __global__ void __launch_bounds__(256) split_float_kernel(SplitSide sa, SplitSid
     int c0[VEC];
 #pragma unroll
     for (int e = 0; e < VEC; ++e) {
-      const Bits v = xv[e];
-      const int be = (int)((v >> F::kFracBits) & F::kExpMask);
-      const bool neg = (v & F::kSign) != 0;
-      const unsigned long long hidden = 1ull << F::kFracBits;
-      unsigned long long m = ((unsigned long long)v & (hidden - 1ull)) | (be ? hidden : 0ull);
-      int sh = (be > 1 ? be : 1) - F::kLsbBias + f;  // x * 2^f = +-m * 2^sh
+      bool neg, lost;
       unsigned long long t;
-      if (m == 0 || sh >= 0) {
-        // exact: +-m * 2^sh, cut at chunk sh / 12
-        if (m == 0) sh = 0;
-        c0[e] = sh / kChunkBits;
-        t = m << (sh % kChunkBits);
-      } else {
-        // coarsened (lossy) point: floor(+-m * 2^sh), below 2^(kFracBits+1) in magnitude
-        const int r = -sh;
-        const unsigned long long q = r >= 64 ? 0ull : m >> r;
-        const bool lost = r >= 64 ? true : (m & ((1ull << r) - 1ull)) != 0ull;
-        t = (neg && lost) ? q + 1ull : q;  // floor of a negative value rounds away from zero
-        c0[e] = 0;
-      }
+      scaled_magnitude<Bits>(xv[e], f, neg, t, lost, c0[e]);
+      if (neg && lost) ++t;  // floor of a negative value rounds away from zero
       const float sg = neg ? -1.0f : 1.0f;
 #pragma unroll
       for (int c = 0; c < NC; ++c) cf[e][c] = sg * (float)(unsigned)((t >> (kChunkBits * c)) & 0xFFFu);
@@ -644,6 +678,121 @@ __global__ void __launch_bounds__(256) split_float_kernel(SplitSide sa, SplitSid
 #pragma unroll
       for (int e = 0; e < VEC / 2; ++e) h[e] = __floats2half2_rn(r[2 * e], r[2 * e + 1]);
       *reinterpret_cast<uint4*>(y + (long long)p * s.plane) = *reinterpret_cast<const uint4*>(h);
+    }
+  }
+  allow_dependents();
+}
+
+// Interval operands ("enclosure-gemm", Method: Rump's midpoint-radius bound,
+// its three products formed exactly): mid(C) = Am Bm and
+// rad(C) = |Am| Br + Ar (|Bm| + Br).  The split writes three residue planes per
+// prime for each operand, A -> (Am, |Am|, Ar) and B -> (Bm, Br, |Bm| + Br), so
+// the per-prime GEMM over the three planes forms the three products in one
+// launch.  At a coarsened point midpoints are floored (their error is bounded
+// in the epilogue) and every magnitude in the radius is rounded up, so the
+// radius products stay upper bounds.  The residue of |Am| comes from that of
+// floor(Am): ceil(|x| 2^f) is -floor(x 2^f) for x < 0 and floor(x 2^f) + lost
+// otherwise.
+struct IvSide {
+  const void* Xm;   // midpoints [R][C]
+  const void* Xr;   // radii [R][C]
+  __half* Y;        // [pmax][3][R][ldy]
+  long long R, C, ldy, sub, plane;  // sub = R * ldy (plane to plane), plane = 3 * sub (prime to prime)
+  long long items;  // R * ldy / VEC
+};
+
+template <typename Bits, int VEC>
+__global__ void __launch_bounds__(256) split_interval_kernel(IvSide sa, IvSide sb, const DevPlan* plan) {
+  using F = FloatFormat<Bits>;
+  constexpr int kSpan = F::kFracBits + 1 + kChunkBits - 1;
+  constexpr int NC = (kSpan + kChunkBits - 1) / kChunkBits;
+  constexpr int PER = 16 / sizeof(Bits);
+  static_assert(VEC == 4 && (VEC * sizeof(Bits)) % 16 == 0, "four entries per item, whole 16-byte loads");
+  __shared__ float w_s[kNumPrimes][kMaxChunks];
+  wait_for_predecessor();
+  if (plan->status) return;
+  const int P = plan->P;
+  const int fa = plan->f_a, fb = plan->f_b;
+  for (int i = threadIdx.x; i < P * kMaxChunks; i += blockDim.x)
+    w_s[i / kMaxChunks][i % kMaxChunks] = c_tab.chunk_w[i / kMaxChunks][i % kMaxChunks];
+  __syncthreads();
+  const long long total = sa.items + sb.items;
+  for (long long it = (long long)blockIdx.x * blockDim.x + threadIdx.x; it < total;
+       it += (long long)gridDim.x * blockDim.x) {
+    const bool isA = it < sa.items;
+    const IvSide& s = isA ? sa : sb;
+    const int f = isA ? fa : fb;
+    const long long item = isA ? it : it - sa.items;
+    const long long per_row = s.ldy / VEC;
+    const long long row = item / per_row;
+    const long long col0 = (item - row * per_row) * VEC;
+    Bits xm[VEC], xr[VEC];
+    {
+      const Bits* Xm = static_cast<const Bits*>(s.Xm) + row * s.C + col0;
+      const Bits* Xr = static_cast<const Bits*>(s.Xr) + row * s.C + col0;
+      if (col0 + VEC <= s.C && (((reinterpret_cast<uintptr_t>(Xm) | reinterpret_cast<uintptr_t>(Xr)) & 15u) == 0)) {
+#pragma unroll
+        for (int t = 0; t < VEC / PER; ++t) {
+          const uint4 a = __ldg(reinterpret_cast<const uint4*>(Xm) + t);
+          const uint4 b = __ldg(reinterpret_cast<const uint4*>(Xr) + t);
+          memcpy(xm + PER * t, &a, 16);
+          memcpy(xr + PER * t, &b, 16);
+        }
+      } else {
+#pragma unroll
+        for (int e = 0; e < VEC; ++e) {
+          xm[e] = col0 + e < s.C ? __ldg(Xm + e) : (Bits)0;
+          xr[e] = col0 + e < s.C ? __ldg(Xr + e) : (Bits)0;
+        }
+      }
+    }
+    float cm[VEC][NC], cr[VEC][NC];
+    int c0m[VEC], c0r[VEC];
+    bool negm[VEC], lostm[VEC];
+#pragma unroll
+    for (int e = 0; e < VEC; ++e) {
+      unsigned long long t;
+      bool neg, lost;
+      scaled_magnitude<Bits>(xm[e], f, negm[e], t, lostm[e], c0m[e]);
+      if (negm[e] && lostm[e]) ++t;  // |floor(x 2^f)|
+      const float sg = negm[e] ? -1.0f : 1.0f;
+#pragma unroll
+      for (int c = 0; c < NC; ++c) cm[e][c] = sg * (float)(unsigned)((t >> (kChunkBits * c)) & 0xFFFu);
+      scaled_magnitude<Bits>(xr[e], f, neg, t, lost, c0r[e]);  // radii are >= 0 (the planner checked)
+      if (lost) ++t;                                             // ceil(r 2^f)
+#pragma unroll
+      for (int c = 0; c < NC; ++c) cr[e][c] = (float)(unsigned)((t >> (kChunkBits * c)) & 0xFFFu);
+    }
+    __half* y = s.Y + row * s.ldy + col0;
+    for (int p = 0; p < P; ++p) {
+      const float q = c_tab.qf[p], iq = c_tab.invq[p];
+      float r0[VEC], r1[VEC], r2[VEC];
+#pragma unroll
+      for (int e = 0; e < VEC; ++e) {
+        float am = 0.0f, ar = 0.0f;
+#pragma unroll
+        for (int c = 0; c < NC; ++c) {
+          am = __fmaf_rn(cm[e][c], w_s[p][c0m[e] + c], am);
+          ar = __fmaf_rn(cr[e][c], w_s[p][c0r[e] + c], ar);
+        }
+        const float rm = bal_mod_small(am, q, iq);  // |am|, |ar| <= NC * 4095 * 125 < 2^23
+        const float rr = bal_mod_small(ar, q, iq);
+        const float rabs = negm[e] ? -rm : bal_mod_small(rm + (lostm[e] ? 1.0f : 0.0f), q, iq);  // ceil |x| 2^f
+        r0[e] = rm;
+        r1[e] = isA ? rabs : rr;
+        r2[e] = isA ? rr : bal_mod_small(rabs + rr, q, iq);
+      }
+      __half* yp = y + (long long)p * s.plane;
+      __half2 h[VEC / 2];
+#pragma unroll
+      for (int e = 0; e < VEC / 2; ++e) h[e] = __floats2half2_rn(r0[2 * e], r0[2 * e + 1]);
+      *reinterpret_cast<uint2*>(yp) = *reinterpret_cast<const uint2*>(h);
+#pragma unroll
+      for (int e = 0; e < VEC / 2; ++e) h[e] = __floats2half2_rn(r1[2 * e], r1[2 * e + 1]);
+      *reinterpret_cast<uint2*>(yp + s.sub) = *reinterpret_cast<const uint2*>(h);
+#pragma unroll
+      for (int e = 0; e < VEC / 2; ++e) h[e] = __floats2half2_rn(r2[2 * e], r2[2 * e + 1]);
+      *reinterpret_cast<uint2*>(yp + 2 * s.sub) = *reinterpret_cast<const uint2*>(h);
     }
   }
   allow_dependents();
@@ -725,10 +874,13 @@ __device__ __forceinline__ void garner_reconstruct(const uint8_t* __restrict__ r
 #pragma unroll
     for (int j = 0; j < kGarnerBatch; ++j) {
       const int i = i0 + j;
+      static_assert(GE == 1 || GE == 2 || GE == 4, "one, two or four adjacent entries");
       if constexpr (GE == 4)
         rw[j] = (i < P) ? __ldg(reinterpret_cast<const uint32_t*>(rc + (long long)i * plane)) : 0u;
-      else
+      else if constexpr (GE == 2)
         rw[j] = (i < P) ? (uint32_t)__ldg(reinterpret_cast<const unsigned short*>(rc + (long long)i * plane)) : 0u;
+      else
+        rw[j] = (i < P) ? (uint32_t)__ldg(rc + (long long)i * plane) : 0u;
     }
 #pragma unroll
     for (int j = 0; j < kGarnerBatch; ++j) {
@@ -977,6 +1129,62 @@ __global__ void __launch_bounds__(128) garner_enclose_kernel(const uint8_t* __re
   }
 }
 
+// x += sign * y, kEncW-word two's complement (sign = +1 or -1).
+__device__ __forceinline__ void add_words(uint32_t (&x)[kEncW], const uint32_t (&y)[kEncW], int sign) {
+  unsigned long long carry = sign < 0 ? 1ull : 0ull;  // x - y = x + ~y + 1
+#pragma unroll
+  for (int k = 0; k < kEncW; ++k) {
+    const unsigned long long t = (unsigned long long)x[k] + (sign < 0 ? ~y[k] : y[k]) + carry;
+    x[k] = (uint32_t)t;
+    carry = t >> 32;
+  }
+}
+
+// Interval epilogue ("enclosure-gemm", Method: Rump's bound with the
+// midpoint and radius as exact integers, rounded outward once): from the
+// three product planes S1 = Am Bm, S2 = |Am| Br, S3 = Ar (|Bm| + Br) at rows
+// `sub` bytes apart, lo = down(S1 - S2 - S3) and hi = up(S1 + S2 + S3), with
+// the midpoint's flooring bound widened outward at a coarsened point.
+template <typename Bits>
+__global__ void __launch_bounds__(128) garner_interval_kernel(const uint8_t* __restrict__ RC, long long ldc,
+                                                              long long plane, long long sub, long long M,
+                                                              long long N, long long K, DevPlan* plan,
+                                                              Bits* __restrict__ lo, Bits* __restrict__ hi) {
+  constexpr int GE = 1;
+  wait_for_predecessor();
+  if (plan->status) return;
+  const int P = plan->P;
+  const int Q = plan->f_a + plan->f_b;
+  const long long item = (long long)blockIdx.x * blockDim.x + threadIdx.x;
+  if (item >= M * N) return;
+  const long long m = item / N, n = item - m * N;
+  const uint8_t* base = RC + m * ldc + n;
+  uint32_t x[GE][kEncW], xl[kEncW], xh[kEncW];
+  garner_reconstruct<kEncW, GE>(base, plane, P, x);
+#pragma unroll
+  for (int k = 0; k < kEncW; ++k) xl[k] = xh[k] = x[0][k];
+  garner_reconstruct<kEncW, GE>(base + sub, plane, P, x);
+  add_words(xl, x[0], -1);
+  add_words(xh, x[0], 1);
+  garner_reconstruct<kEncW, GE>(base + 2 * sub, plane, P, x);
+  add_words(xl, x[0], -1);
+  add_words(xh, x[0], 1);
+  if (!plan->lossless) {
+    // floored midpoints: (A 2^f_a)(B 2^f_b) - S1 lies in (-K(2^a + 2^b), K(2^a + 2^b) + K)
+    const int ba = plan->bits_a, bb = plan->bits_b;
+    add_shifted(xl, K, ba, -1);
+    add_shifted(xl, K, bb, -1);
+    add_shifted(xh, K, ba, 1);
+    add_shifted(xh, K, bb, 1);
+    add_shifted(xh, K, 0, 1);
+  }
+  Bits l, h, unused;
+  outward_bits(xl, Q, l, unused);
+  outward_bits(xh, Q, unused, h);
+  lo[m * N + n] = l;
+  hi[m * N + n] = h;
+}
+
 int g_sm_count[64];
 
 int sm_count() {
@@ -1017,8 +1225,8 @@ static int planner_blocks(long long n) {
   return (int)(b < 1 ? 1 : (b > cap ? cap : b));
 }
 
-cudaError_t launch_plan(int op, const void* A, long long nA, int la, const void* B, long long nB, int lb, int lc,
-                        long long K, int nprimes_fixed, DevPlan* plan, cudaStream_t s) {
+cudaError_t launch_plan(int op, const void* A, const void* A2, long long nA, int la, const void* B, const void* B2,
+                        long long nB, int lb, int lc, long long K, int nprimes_fixed, DevPlan* plan, cudaStream_t s) {
   PlanArgs pa{op, K, nprimes_fixed, la, lb, lc};
   if (nprimes_fixed) nA = nB = 0;  // only the finalisation is needed
   const int ba = planner_blocks(nA), bb = planner_blocks(nB);
@@ -1028,13 +1236,15 @@ cudaError_t launch_plan(int op, const void* A, long long nA, int la, const void*
   else if (op == RG_OP_LIMBS)
     plan_limbs_kernel<<<ba + bb, 256, 0, s>>>(static_cast<const int64_t*>(A), nA, la,
                                               static_cast<const int64_t*>(B), nB, lb, ba, plan, pa);
-  else if (op == RG_OP_ENCLOSE)
-    plan_float_kernel<unsigned long long><<<ba + bb, 256, 0, s>>>(static_cast<const unsigned long long*>(A), nA,
-                                                                  static_cast<const unsigned long long*>(B), nB, ba,
-                                                                  plan, pa);
-  else
-    plan_float_kernel<uint32_t><<<ba + bb, 256, 0, s>>>(static_cast<const uint32_t*>(A), nA,
-                                                        static_cast<const uint32_t*>(B), nB, ba, plan, pa);
+  else if (op == RG_OP_ENCLOSE || op == RG_OP_INTERVAL) {
+    using U = unsigned long long;
+    plan_float_kernel<U><<<ba + bb, 256, 0, s>>>(static_cast<const U*>(A), static_cast<const U*>(A2), nA,
+                                                 static_cast<const U*>(B), static_cast<const U*>(B2), nB, ba, plan, pa);
+  } else {
+    plan_float_kernel<uint32_t><<<ba + bb, 256, 0, s>>>(static_cast<const uint32_t*>(A), static_cast<const uint32_t*>(A2),
+                                                        nA, static_cast<const uint32_t*>(B),
+                                                        static_cast<const uint32_t*>(B2), nB, ba, plan, pa);
+  }
   return cudaGetLastError();
 }
 
@@ -1057,9 +1267,24 @@ static unsigned split_grid(long long items) {
   return (unsigned)(b < 1 ? 1 : (b > cap ? cap : b));
 }
 
-cudaError_t launch_split(int op, const void* A, const void* B, int la, int lb, long long batch, long long Mb,
-                         long long N, long long K, long long lda, long long ldb, void* RA, void* RB, DevPlan* plan,
-                         int i64_planes, bool transb, cudaStream_t st) {
+static IvSide make_iv_side(const void* Xm, const void* Xr, __half* Y, long long R, long long C, long long ldy,
+                           int vec) {
+  IvSide s;
+  s.Xm = Xm;
+  s.Xr = Xr;
+  s.Y = Y;
+  s.R = R;
+  s.C = C;
+  s.ldy = ldy;
+  s.sub = R * ldy;
+  s.plane = 3 * s.sub;
+  s.items = R * (ldy / vec);
+  return s;
+}
+
+cudaError_t launch_split(int op, const void* A, const void* A2, const void* B, const void* B2, int la, int lb,
+                         long long batch, long long Mb, long long N, long long K, long long lda, long long ldb,
+                         void* RA, void* RB, DevPlan* plan, int i64_planes, bool transb, cudaStream_t st) {
   __half* ra = static_cast<__half*>(RA);
   __half* rb = static_cast<__half*>(RB);
   // The products of a batch lie back to back, so each side is one matrix of
@@ -1067,6 +1292,15 @@ cudaError_t launch_split(int op, const void* A, const void* B, int la, int lb, l
   // RB [P][N][ldb], laid out like A.
   const long long M = batch * Mb;
   const long long brows = batch * (transb ? N : K), bcols = transb ? K : N;
+  if (op == RG_OP_INTERVAL || op == RG_OP_INTERVAL_F32) {
+    constexpr int V = 4;
+    const IvSide sa = make_iv_side(A, A2, ra, M, K, lda, V), sb = make_iv_side(B, B2, rb, brows, bcols, ldb, V);
+    if (op == RG_OP_INTERVAL)
+      return launch_dependent(split_interval_kernel<unsigned long long, V>, split_grid(sa.items + sb.items), 256, 0,
+                              st, sa, sb, (const DevPlan*)plan);
+    return launch_dependent(split_interval_kernel<uint32_t, V>, split_grid(sa.items + sb.items), 256, 0, st, sa, sb,
+                            (const DevPlan*)plan);
+  }
   if (op == RG_OP_ENCLOSE || op == RG_OP_ENCLOSE_F32) {
     constexpr int V = 8;
     const SplitSide sa = make_side(A, ra, M, K, lda, 1, V), sb = make_side(B, rb, brows, bcols, ldb, 1, V);
@@ -1101,10 +1335,17 @@ cudaError_t launch_split(int op, const void* A, const void* B, int la, int lb, l
   return cudaGetLastError();
 }
 
-cudaError_t launch_garner(int op, const void* RC, long long ldc, long long plane, long long M, long long N,
-                          long long K, int lc, DevPlan* plan, void* out0, void* out1, cudaStream_t st) {
+cudaError_t launch_garner(int op, const void* RC, long long ldc, long long plane, long long sub, long long M,
+                          long long N, long long K, int lc, DevPlan* plan, void* out0, void* out1, cudaStream_t st) {
   const uint8_t* rc = static_cast<const uint8_t*>(RC);
   auto blocks_for = [&](int ge) { return dim3((unsigned)((M * ((N + ge - 1) / ge) + 127) / 128)); };
+  if (op == RG_OP_INTERVAL)
+    return launch_dependent(garner_interval_kernel<unsigned long long>, blocks_for(1), 128, 0, st, rc, ldc, plane, sub,
+                            M, N, K, plan, static_cast<unsigned long long*>(out0),
+                            static_cast<unsigned long long*>(out1));
+  if (op == RG_OP_INTERVAL_F32)
+    return launch_dependent(garner_interval_kernel<uint32_t>, blocks_for(1), 128, 0, st, rc, ldc, plane, sub, M, N, K,
+                            plan, static_cast<uint32_t*>(out0), static_cast<uint32_t*>(out1));
   if (op == RG_OP_ENCLOSE)
     return launch_dependent(garner_enclose_kernel<unsigned long long>, blocks_for(GarnerGE<kEncW>::value), 128, 0, st,
                             rc, ldc, plane, M, N, K, plan, static_cast<unsigned long long*>(out0),

@@ -36,8 +36,9 @@ struct DevPlan {
   int maxbits_a, maxbits_b;               // limb operands: max bit length of |x|
   int maxe_a, maxe_b;                     // fp64: max of max(biased exponent, 1) over nonzero entries
   int inv_mine_a, inv_mine_b;             // fp64: 4096 - min of that exponent (0 = no nonzero entry)
-  int nonfinite;                          // fp64: an inf or nan entry was seen
-  int pad1[7];
+  int nonfinite;                          // floating point: an inf or nan entry was seen
+  int neg_radius;                         // intervals: a radius entry below zero was seen
+  int pad1[6];
   // diagnostics of a bounded wait that expired (which role, which wait)
   int timeout_where;
   int pad2[15];

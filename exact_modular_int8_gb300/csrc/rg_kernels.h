@@ -12,10 +12,11 @@ namespace rg {
 cudaError_t upload_tables();
 
 // Planner: reductions over A and B into the plan block (the host zeroes it
-// first); the last block derives the prime count, chunk counts and fp64
-// scales.  With nprimes_fixed > 0 only that derivation runs.
-cudaError_t launch_plan(int op, const void* A, long long nA, int la, const void* B, long long nB, int lb, int lc,
-                        long long K, int nprimes_fixed, DevPlan* plan, cudaStream_t s);
+// first); the last block derives the prime count, chunk counts and
+// floating-point scales.  With nprimes_fixed > 0 only that derivation runs.
+// A2, B2: the radii of interval operands (same sizes as A, B), else null.
+cudaError_t launch_plan(int op, const void* A, const void* A2, long long nA, int la, const void* B, const void* B2,
+                        long long nB, int lb, int lc, long long K, int nprimes_fixed, DevPlan* plan, cudaStream_t s);
 
 // Residue split of A [M][K] into RA [pmax][M][lda] and of B [K][N] into
 // RB [pmax][K][ldb] (fp16 balanced residues), for the plan's prime count.
@@ -24,9 +25,12 @@ cudaError_t launch_plan(int op, const void* A, long long nA, int la, const void*
 // transb: B is given transposed, [N][K], and RB becomes [pmax][N][ldb].
 // batch: A and B hold `batch` products back to back ([batch][M][K] and
 // [batch][K][N]); the residue planes become [pmax][batch][..][..].
-cudaError_t launch_split(int op, const void* A, const void* B, int la, int lb, long long batch, long long M,
-                         long long N, long long K, long long lda, long long ldb, void* RA, void* RB, DevPlan* plan,
-                         int i64_planes, bool transb, cudaStream_t st);
+// Intervals (A2, B2 the radii): three planes per prime and operand,
+// RA [pmax][3][batch * M][lda] holding (Am, |Am|, Ar) and RB likewise
+// (Bm, Br, |Bm| + Br).
+cudaError_t launch_split(int op, const void* A, const void* A2, const void* B, const void* B2, int la, int lb,
+                         long long batch, long long M, long long N, long long K, long long lda, long long ldb,
+                         void* RA, void* RB, DevPlan* plan, int i64_planes, bool transb, cudaStream_t st);
 
 // Per-prime tensor-core product RC[p] = RA[p] * RB[p] mod q_p (uint8).
 // derive_i64: the prime count is derived here from max |A|, max |B| (or
@@ -39,8 +43,10 @@ cudaError_t launch_gemm(const void* RA, long long lda, const void* RB, long long
                         cudaStream_t st, int fault, unsigned long long wait_ns, bool derive_i64, bool b_kmajor);
 
 // Balanced Garner: RC [P][M][ldc] -> int64 limbs C [M][N][lc] (op I64/LIMBS),
-// or the outward pair (lo, hi) as binary64 bit patterns (op ENCLOSE).
-cudaError_t launch_garner(int op, const void* RC, long long ldc, long long plane, long long M, long long N,
-                          long long K, int lc, DevPlan* plan, void* out0, void* out1, cudaStream_t st);
+// or the outward pair (lo, hi) as IEEE bit patterns (ops ENCLOSE[_F32]).  For
+// the interval ops RC holds three planes per prime, `sub` bytes apart: the
+// midpoint and the two radius products.
+cudaError_t launch_garner(int op, const void* RC, long long ldc, long long plane, long long sub, long long M,
+                          long long N, long long K, int lc, DevPlan* plan, void* out0, void* out1, cudaStream_t st);
 
 }  // namespace rg

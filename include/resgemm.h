@@ -51,6 +51,7 @@ extern "C" {
 #define RG_ERR_WORKSPACE 5  /* workspace too small */
 #define RG_ERR_CUDA 6       /* a CUDA runtime or driver call failed */
 #define RG_ERR_TIMEOUT 7    /* a bounded wait inside a kernel expired; the kernel stopped early */
+#define RG_ERR_RADIUS 8     /* an interval radius entry is negative */
 
 /* Flags. */
 #define RG_FLAG_SYNC 1u /* synchronise the stream before returning; return the device status */
@@ -64,6 +65,8 @@ extern "C" {
 #define RG_OP_ENCLOSE 2
 #define RG_OP_STAGE 3
 #define RG_OP_ENCLOSE_F32 4
+#define RG_OP_INTERVAL 5
+#define RG_OP_INTERVAL_F32 6
 
 /* Limits. */
 #define RG_MAX_K 131072 /* K <= 2^17 ("exact-solve" and "enclosure-gemm", Requirements and limits) */
@@ -150,6 +153,31 @@ int enclose_gemm_f32(const float* A, const float* B, float* lo, float* hi, int64
                      unsigned flags, void* ws, size_t ws_bytes, void* stream);
 
 /*
+ * Outward enclosure of the product of interval matrices in midpoint-radius
+ * form, <Am, Ar> [M][K] times <Bm, Br> [K][N] (radii >= 0), by Rump's bound:
+ * the midpoint S = Am * Bm and the radius R = |Am| * Br + Ar * (|Bm| + Br)
+ * are formed as exact integers (three products on the residue engine, one
+ * launch), and lo is the largest value of the format <= S - R, hi the
+ * smallest >= S + R.  Every point product A * B with A in <Am, Ar>, B in
+ * <Bm, Br> lies in [lo, hi]; the only overestimation is the bound's own
+ * ("enclosure-gemm", Usage: mm_interval; Method: Rump's midpoint-radius bound
+ * with its products and radius formed as exact integers).
+ *
+ * One scale covers an operand's midpoints and radii.  At a coarsened point
+ * (lossless = 0 in rg_get_plan) midpoints are floored and radius magnitudes
+ * rounded up, and the midpoint's flooring bound is added outward as for
+ * enclose_gemm_f64.  The residue range must hold bits_a + bits_b +
+ * ceil(log2 K) + 2 bits (bound_bits in rg_get_plan).  RG_FLAG_TRANS_B gives
+ * Bm and Br as [N][K].  Workspace: RG_OP_INTERVAL (RG_OP_INTERVAL_F32).
+ * Errors: RG_ERR_RADIUS (a negative radius: a set sign bit on a nonzero
+ * entry), RG_ERR_NONFINITE, and the errors of enclose_gemm_f64.
+ */
+int interval_gemm_f64(const double* Am, const double* Ar, const double* Bm, const double* Br, double* lo, double* hi,
+                      int64_t M, int64_t N, int64_t K, unsigned flags, void* ws, size_t ws_bytes, void* stream);
+int interval_gemm_f32(const float* Am, const float* Ar, const float* Bm, const float* Br, float* lo, float* hi,
+                      int64_t M, int64_t N, int64_t K, unsigned flags, void* ws, size_t ws_bytes, void* stream);
+
+/*
  * Batched forms: `batch` independent products of one shape, each operand's
  * products stored back to back: A [batch][M][K], B [batch][K][N] (with
  * RG_FLAG_TRANS_B [batch][N][K]; limbs add a last dimension as above),
@@ -170,6 +198,12 @@ int enclose_gemm_f64_batched(const double* A, const double* B, double* lo, doubl
                              int64_t N, int64_t K, unsigned flags, void* ws, size_t ws_bytes, void* stream);
 int enclose_gemm_f32_batched(const float* A, const float* B, float* lo, float* hi, int64_t batch, int64_t M,
                              int64_t N, int64_t K, unsigned flags, void* ws, size_t ws_bytes, void* stream);
+int interval_gemm_f64_batched(const double* Am, const double* Ar, const double* Bm, const double* Br, double* lo,
+                              double* hi, int64_t batch, int64_t M, int64_t N, int64_t K, unsigned flags, void* ws,
+                              size_t ws_bytes, void* stream);
+int interval_gemm_f32_batched(const float* Am, const float* Ar, const float* Bm, const float* Br, float* lo,
+                              float* hi, int64_t batch, int64_t M, int64_t N, int64_t K, unsigned flags, void* ws,
+                              size_t ws_bytes, void* stream);
 
 /*
  * The per-prime tensor-core stage alone, on caller-provided residues:
