@@ -109,7 +109,7 @@ struct PlanArgs {
 };
 
 struct LocalPlan {
-  int status, P, bits_a, bits_b, T, f_a, f_b, lossless, nchunk_a, nchunk_b;
+  int status, P, bits_a, bits_b, T, f_a, f_b, lossless, nword_a, nword_b;
 };
 
 __device__ int primes_for_bound(int T) {  // fewest primes with P > 2^(T+1); 0 if none
@@ -122,18 +122,19 @@ __device__ int primes_for_bound(int T) {  // fewest primes with P > 2^(T+1); 0 i
 __device__ LocalPlan finalize_plan(DevPlan* plan, const PlanArgs& a) {
   LocalPlan p = {};
   const int ck = ceil_log2_i64(a.K);
-  auto full_chunks = [](int L) { return (64 * L + kChunkBits - 1) / kChunkBits; };
+  // 32-bit words holding an entry of `bits` magnitude bits with its sign, at most the limbs' 2L
+  auto words_for = [](int bits, int L) { return min((bits + 1 + 31) / 32, 2 * L); };
   if (a.op == RG_OP_I64) {
     const unsigned long long ma = __ldcg(&plan->maxmag_a), mb = __ldcg(&plan->maxmag_b);
     p.bits_a = bitlen64(ma);
     p.bits_b = bitlen64(mb);
     p.T = p.bits_a + p.bits_b + ck;
     if (a.nprimes_fixed) {
-      p.nchunk_a = p.nchunk_b = full_chunks(1);
+      p.nword_a = p.nword_b = 2;
     } else {
-      // entries with |x| <= 2^23 are exact fp32 values: no chunks (nchunk 0)
-      p.nchunk_a = ma <= (1ull << 23) ? 0 : (p.bits_a + 1 + kChunkBits - 1) / kChunkBits;
-      p.nchunk_b = mb <= (1ull << 23) ? 0 : (p.bits_b + 1 + kChunkBits - 1) / kChunkBits;
+      // entries with |x| <= 2^23 are exact fp32 values: no words (nword 0)
+      p.nword_a = ma <= (1ull << 23) ? 0 : words_for(p.bits_a, 1);
+      p.nword_b = mb <= (1ull << 23) ? 0 : words_for(p.bits_b, 1);
       // exact range check: K * max|A| * max|B| <= 2^63 - 1, with 64x64 -> 128
       // products only
       const unsigned long long ab_hi = __umul64hi(ma, mb), ab = ma * mb;
@@ -145,11 +146,11 @@ __device__ LocalPlan finalize_plan(DevPlan* plan, const PlanArgs& a) {
     p.bits_b = __ldcg(&plan->maxbits_b);
     p.T = p.bits_a + p.bits_b + ck;
     if (a.nprimes_fixed) {
-      p.nchunk_a = full_chunks(a.la);
-      p.nchunk_b = full_chunks(a.lb);
+      p.nword_a = 2 * a.la;
+      p.nword_b = 2 * a.lb;
     } else {
-      p.nchunk_a = p.bits_a <= 23 ? 0 : min((p.bits_a + 1 + kChunkBits - 1) / kChunkBits, full_chunks(a.la));
-      p.nchunk_b = p.bits_b <= 23 ? 0 : min((p.bits_b + 1 + kChunkBits - 1) / kChunkBits, full_chunks(a.lb));
+      p.nword_a = p.bits_a <= 23 ? 0 : words_for(p.bits_a, a.la);
+      p.nword_b = p.bits_b <= 23 ? 0 : words_for(p.bits_b, a.lb);
       if (p.T > RG_MAX_BOUND_BITS || p.T > 64 * a.lc - 1) p.status = RG_ERR_RANGE;
     }
   } else {  // RG_OP_ENCLOSE[_F32], RG_OP_INTERVAL[_F32]
@@ -216,8 +217,8 @@ __device__ void planner_finish(DevPlan* plan, const PlanArgs& a) {
     plan->f_a = lp.f_a;
     plan->f_b = lp.f_b;
     plan->lossless = lp.lossless;
-    plan->nchunk_a = lp.nchunk_a;
-    plan->nchunk_b = lp.nchunk_b;
+    plan->nword_a = lp.nword_a;
+    plan->nword_b = lp.nword_b;
     if (lp.status) set_status(&plan->status, lp.status);
   }
   __syncthreads();
@@ -291,10 +292,15 @@ __global__ void __launch_bounds__(256) plan_limbs_kernel(const int64_t* __restri
   const long long n = sd.isA ? nA : nB;
   const int L = sd.isA ? la : lb;
   int m = 0;
-  for (long long i = sd.b0 * blockDim.x + threadIdx.x; i < n; i += sd.stride) {
-    const int b = limb_magnitude_bits(X + i * L, L);
-    m = b > m ? b : m;
+  long long i = sd.b0 * blockDim.x + threadIdx.x;
+  for (; i + 3 * sd.stride < n; i += 4 * sd.stride) {  // four independent entries in flight
+    const int b0 = limb_magnitude_bits(X + i * L, L);
+    const int b1 = limb_magnitude_bits(X + (i + sd.stride) * L, L);
+    const int b2 = limb_magnitude_bits(X + (i + 2 * sd.stride) * L, L);
+    const int b3 = limb_magnitude_bits(X + (i + 3 * sd.stride) * L, L);
+    m = max(m, max(max(b0, b1), max(b2, b3)));
   }
+  for (; i < n; i += sd.stride) m = max(m, limb_magnitude_bits(X + i * L, L));
   m = block_max_i32(m);
   if (threadIdx.x == 0 && m) atomicMax(sd.isA ? &plan->maxbits_a : &plan->maxbits_b, m);
   planner_finish(plan, pa);
@@ -375,96 +381,157 @@ __global__ void __launch_bounds__(256) plan_float_kernel(const Bits* __restrict_
 // Residue split ("exact-solve", Method: residues for every prime at once,
 // reduction by a precomputed reciprocal instead of hardware modulo)
 //
-// Every entry x is written as sum_c a_c 2^(12c) with 12-bit chunks a_c (the
-// top chunk signed), so x mod q == sum_c a_c w_{q,c} (mod q) with the
-// balanced weights w_{q,c} = 2^(12c) mod q.  With |a_c| < 2^12, |w| <= 125 and
-// at most 22 chunks the sum stays below 2^24 and is formed exactly in fp32;
-// one reciprocal-based reduction then yields the balanced residue, written as
-// fp16 (exact for |r| <= 125).  Columns from C up to the padded row length
-// are written as zeros.  Grid-stride over the items of A, then of B.
+// Integers: an entry x whose two's complement fits nw little-endian 32-bit
+// words equals U - [x < 0] 2^(32 nw), U those words read as unsigned, so over
+// the bytes b_j of U
+//   x mod q == sum_j b_j (2^(8j) mod q) - [x < 0] (2^(32 nw) mod q)   (mod q).
+// The byte weights are balanced (|w| <= 125) and packed four to a word, so a
+// word costs one dp4a (unsigned data bytes times signed weights).  At most 8
+// words keep the sum below 2^20, an exact fp32, and one reciprocal reduction
+// gives the balanced residue.  Entries with |x| <= 2^23 skip the bytes: x is
+// itself an exact fp32.
+//
+// Floating point: |x| 2^f = t 2^sh, t the significand (or, at a coarsened
+// point, the floored scaled magnitude with sh = 0), so
+//   x 2^f mod q == +-(t mod q)(2^sh mod q)   (mod q),
+// with 2^sh mod q from a per-block table; the product of two balanced
+// residues is below 2^14 and is reduced once more.
+//
+// Residues are written as fp16 (exact for |r| <= 125).  Columns from C up to
+// the padded row length are written as zeros.  Grid-stride over the items
+// (VEC consecutive entries of one row) of A, then of B.
 // ---------------------------------------------------------------------------
 
 struct SplitSide {
-  const void* X;   // int64 [R][C], limbs [R][C][L] or binary64 [R][C]
+  const void* X;   // int64 [R][C], limbs [R][C][L] or floating point [R][C]
   __half* Y;       // [pmax][R][ldy]
   long long R, C, ldy, plane;  // plane = R * ldy
   int L;           // limbs per entry (integer kinds)
   long long items; // R * ldy / VEC
 };
 
-// 12 bits starting at bit `pos` (a compile-time constant after unrolling) of
-// the sign-extended two's-complement value held in registers x[0..L).
-template <int LMAX>
-__device__ __forceinline__ unsigned chunk_bits(const unsigned long long (&x)[LMAX], int L, int pos) {
-  const int w = pos >> 6, off = pos & 63;
-  // sign word of the top limb x[L-1], selected with masks so that every
-  // register index stays a compile-time constant
-  unsigned long long sign = 0ull;
-#pragma unroll
-  for (int k = 0; k < LMAX; ++k)
-    sign |= (unsigned long long)((long long)x[k] >> 63) & (0ull - (unsigned long long)(k == L - 1));
-  const unsigned long long lo = (w < LMAX && w < L) ? x[w < LMAX ? w : 0] : sign;
-  unsigned long long v = lo >> off;
-  if (off > 64 - kChunkBits) {
-    const unsigned long long hi = (w + 1 < LMAX && w + 1 < L) ? x[w + 1 < LMAX ? w + 1 : 0] : sign;
-    v |= hi << (64 - off);
-  }
-  return (unsigned)(v & 0xFFFu);
+constexpr float kMagic = 12582912.0f;   // 1.5 * 2^23
+constexpr int kMagicBits = 0x4B400000;  // its bit pattern
+
+// Exact int -> float for |v| < 2^22 (and back) without the conversion unit:
+// the integer sits in the low mantissa bits of kMagic + v.
+__device__ __forceinline__ float int_to_float_exact(int v) { return __int_as_float(kMagicBits + v) - kMagic; }
+__device__ __forceinline__ int float_bits_offset(float v) { return __float_as_int(v + kMagic); }  // = kMagicBits + v
+
+// c + the four bytes of a (unsigned) dotted with the four bytes of b (signed).
+__device__ __forceinline__ int dp4a_us(uint32_t a, int b, int c) {
+  int d;
+  asm("dp4a.u32.s32 %0, %1, %2, %3;" : "=r"(d) : "r"(a), "r"(b), "r"(c));
+  return d;
 }
 
-// Writes the balanced residues of VEC entries for every prime.  nch == 0:
-// cf[e][0] holds the entry itself (|x| <= 2^23, exact in fp32).  Otherwise
-// s = sum_c cf[e][c] w_{q,c}; with at most 16 chunks |s| < 2^23 as well, so the
-// reduction needs no correction step.
-template <int VEC, int NCH>
-__device__ __forceinline__ void emit_residues(const float (&cf)[VEC][NCH], int nch, int P, __half* y,
-                                              long long plane) {
-  static_assert(VEC % 2 == 0, "residues are written as half2 pairs");
-  for (int p = 0; p < P; ++p) {
-    const float q = c_tab.qf[p], iq = c_tab.invq[p];
-    float r[VEC];
-    if (nch == 0) {
+// Per-prime constants of a split block, read with 16-byte shared loads.
+struct alignas(16) PrimeRec {
+  int w[kMaxWords];  // packed byte weights of words 0..7
+  float q, iq;       // q and fl(1/q)
+  int pad[2];
+};
+
+// Every prime's record (and, if ws is given, its word-string weights); none
+// of it depends on the predecessor kernel, so it is read before waiting.
+__device__ __forceinline__ void load_prime_recs(PrimeRec* rec, int (*ws)[kMaxWords + 1]) {
+  for (int i = threadIdx.x; i < kNumPrimes * kMaxWords; i += blockDim.x)
+    rec[i / kMaxWords].w[i % kMaxWords] = c_tab.wbyte[i / kMaxWords][i % kMaxWords];
+  for (int p = threadIdx.x; p < kNumPrimes; p += blockDim.x) {
+    rec[p].q = c_tab.qf[p];
+    rec[p].iq = c_tab.invq[p];
+  }
+  if (ws)
+    for (int i = threadIdx.x; i < kNumPrimes * (kMaxWords + 1); i += blockDim.x)
+      ws[i / (kMaxWords + 1)][i % (kMaxWords + 1)] = c_tab.wword[i / (kMaxWords + 1)][i % (kMaxWords + 1)];
+}
+
+// The first NW packed byte weights of a record (NW = 1, 2, 4 or 8).
+template <int NW>
+__device__ __forceinline__ void load_weights(const PrimeRec& r, int (&wv)[NW]) {
+  if constexpr (NW == 1) {
+    wv[0] = r.w[0];
+  } else if constexpr (NW == 2) {
+    const int2 v = *reinterpret_cast<const int2*>(r.w);
+    wv[0] = v.x;
+    wv[1] = v.y;
+  } else {
 #pragma unroll
-      for (int e = 0; e < VEC; ++e) r[e] = bal_mod_small(cf[e][0], q, iq);
+    for (int k = 0; k < NW; k += 4) {
+      const int4 v = *reinterpret_cast<const int4*>(r.w + k);
+      wv[k] = v.x;
+      wv[k + 1] = v.y;
+      wv[k + 2] = v.z;
+      wv[k + 3] = v.w;
+    }
+  }
+}
+
+template <int VEC>
+__device__ __forceinline__ void store_residues(const float (&r)[VEC], __half* dst) {
+  static_assert(VEC == 2 || VEC == 4 || VEC == 8, "residues are written as half2 pairs");
+  __half2 h[VEC / 2];
+#pragma unroll
+  for (int e = 0; e < VEC / 2; ++e) h[e] = __floats2half2_rn(r[2 * e], r[2 * e + 1]);
+  if constexpr (VEC == 8)
+    *reinterpret_cast<uint4*>(dst) = *reinterpret_cast<const uint4*>(h);
+  else if constexpr (VEC == 4)
+    *reinterpret_cast<uint2*>(dst) = *reinterpret_cast<const uint2*>(h);
+  else
+    *reinterpret_cast<__half2*>(dst) = h[0];
+}
+
+// Residues of VEC integer entries for every prime: nw == 0 takes the exact
+// fp32 values xf, otherwise the first nw words wd with the signs neg.
+template <int VEC, int NW>
+__device__ __forceinline__ void emit_int_residues(const uint32_t (&wd)[VEC][NW], const bool (&neg)[VEC],
+                                                  const float (&xf)[VEC], int nw, int P, const PrimeRec* rec,
+                                                  const int (*ws)[kMaxWords + 1], __half* y, long long plane) {
+  for (int p = 0; p < P; ++p) {
+    const PrimeRec& R = rec[p];
+    const float q = R.q, iq = R.iq;
+    float r[VEC];
+    if (nw == 0) {
+#pragma unroll
+      for (int e = 0; e < VEC; ++e) r[e] = bal_mod_small(xf[e], q, iq);
     } else {
+      int wv[NW];
+      load_weights<NW>(R, wv);
+#pragma unroll
+      for (int w = 0; w < NW; ++w) wv[w] = w < nw ? wv[w] : 0;  // words past nw weigh nothing
+      const int sg = ws[p][nw];
 #pragma unroll
       for (int e = 0; e < VEC; ++e) {
-        float s = 0.0f;
+        int acc = neg[e] ? -sg : 0;
 #pragma unroll
-        for (int c = 0; c < NCH; ++c)
-          if (c < nch) s = __fmaf_rn(cf[e][c], c_tab.chunk_w[p][c], s);
-        r[e] = NCH <= 16 ? bal_mod_small(s, q, iq) : bal_mod(s, q, iq);
+        for (int w = 0; w < NW; ++w) acc = dp4a_us(wd[e][w], wv[w], acc);
+        r[e] = bal_mod_small(int_to_float_exact(acc), q, iq);  // |acc| < 2^20
       }
     }
-    __half2 h[VEC / 2];
-#pragma unroll
-    for (int e = 0; e < VEC / 2; ++e) h[e] = __floats2half2_rn(r[2 * e], r[2 * e + 1]);
-    __half* dst = y + (long long)p * plane;
-    if constexpr (VEC == 8) {
-      *reinterpret_cast<uint4*>(dst) = *reinterpret_cast<const uint4*>(h);
-    } else if constexpr (VEC == 4) {
-      *reinterpret_cast<uint2*>(dst) = *reinterpret_cast<const uint2*>(h);
-    } else {
-      *reinterpret_cast<__half2*>(dst) = h[0];
-    }
+    store_residues<VEC>(r, y + (long long)p * plane);
   }
 }
 
 // Integer operands: int64 (L = 1) or limbs (L <= LMAX).  VEC consecutive
 // columns per item; their VEC * L words are contiguous and are read with
 // 16-byte loads when they lie fully inside the row and are aligned.
-template <int VEC, int NCH, int LMAX>
+template <int VEC, int LMAX>
 __global__ void __launch_bounds__(256) split_int_kernel(SplitSide sa, SplitSide sb, const DevPlan* plan) {
+  constexpr int NW = 2 * LMAX;
+  __shared__ PrimeRec rec[kNumPrimes];
+  __shared__ int ws[kNumPrimes][kMaxWords + 1];
+  load_prime_recs(rec, ws);
+  __syncthreads();
   wait_for_predecessor();
   if (plan->status) return;
   const int P = plan->P;
-  const int nch_a = plan->nchunk_a, nch_b = plan->nchunk_b;
+  const int nw_a = plan->nword_a, nw_b = plan->nword_b;
   const long long total = sa.items + sb.items;
   for (long long it = (long long)blockIdx.x * blockDim.x + threadIdx.x; it < total;
        it += (long long)gridDim.x * blockDim.x) {
     const bool isA = it < sa.items;
     const SplitSide& s = isA ? sa : sb;
-    const int nch = isA ? nch_a : nch_b;
+    const int nw = isA ? nw_a : nw_b;
     const long long item = isA ? it : it - sa.items;
     const long long per_row = s.ldy / VEC;
     const long long row = item / per_row;
@@ -486,38 +553,38 @@ __global__ void __launch_bounds__(256) split_int_kernel(SplitSide sa, SplitSide 
 #pragma unroll
         for (int k = 0; k < LMAX; ++k) xw[e][k] = (col0 + e < s.C && k < L) ? __ldg(X + e * L + k) : 0ull;
     }
-    float cf[VEC][NCH];
-    if (nch == 0) {  // |x| <= 2^23: the low word is the value
+    uint32_t wd[VEC][NW];
+    bool neg[VEC];
+    float xf[VEC];
 #pragma unroll
-      for (int e = 0; e < VEC; ++e) {
-        cf[e][0] = (float)(long long)xw[e][0];
+    for (int e = 0; e < VEC; ++e) {
+      unsigned long long top = 0ull;  // the top limb, selected with masks (no dynamic register index)
 #pragma unroll
-        for (int c = 1; c < NCH; ++c) cf[e][c] = 0.0f;
-      }
-    } else {
+      for (int k = 0; k < LMAX; ++k) top |= xw[e][k] & (0ull - (unsigned long long)(k == L - 1));
+      neg[e] = (long long)top < 0;
+      xf[e] = (float)(int)(long long)xw[e][0];  // used only when |x| <= 2^23
 #pragma unroll
-      for (int e = 0; e < VEC; ++e) {
-#pragma unroll
-        for (int c = 0; c < NCH; ++c) {
-          const unsigned a = chunk_bits<LMAX>(xw[e], L, c * kChunkBits);
-          const int v = (c == nch - 1) ? (int)((a ^ 0x800u) - 0x800u) : (int)a;  // top chunk signed
-          cf[e][c] = c < nch ? (float)v : 0.0f;
-        }
+      for (int k = 0; k < LMAX; ++k) {
+        wd[e][2 * k] = (uint32_t)xw[e][k];
+        wd[e][2 * k + 1] = (uint32_t)(xw[e][k] >> 32);
       }
     }
-    emit_residues<VEC, NCH>(cf, nch, P, s.Y + row * s.ldy + col0, s.plane);
+    emit_int_residues<VEC, NW>(wd, neg, xf, nw, P, rec, ws, s.Y + row * s.ldy + col0, s.plane);
   }
   allow_dependents();
 }
 
 // int64 operands without a planner pass: every entry's residues are written
 // for `P` primes (the most the bound can need, or the caller's count), the
-// chunk count is decided per warp from the warp's largest |x|, and max |A|,
+// word count is decided per warp from the warp's largest |x|, and max |A|,
 // max |B| are reduced on the side for the GEMM kernel to derive the prime count
 // and check the range.  Saves one read of A and B and one kernel launch.
 template <int VEC>
 __global__ void __launch_bounds__(256) split_i64_kernel(SplitSide sa, SplitSide sb, DevPlan* plan, int P) {
-  constexpr int NCH = 6;
+  __shared__ PrimeRec rec[kNumPrimes];
+  __shared__ int ws[kNumPrimes][kMaxWords + 1];
+  load_prime_recs(rec, ws);
+  __syncthreads();
   wait_for_predecessor();
   const int lane = threadIdx.x & 31;
   const long long total = sa.items + sb.items;
@@ -533,48 +600,40 @@ __global__ void __launch_bounds__(256) split_i64_kernel(SplitSide sa, SplitSide 
     const long long row = item / per_row;
     const long long col0 = (item - row * per_row) * VEC;
     const unsigned long long* X = static_cast<const unsigned long long*>(s.X) + row * s.C + col0;
-    unsigned long long xw[VEC][1];
+    unsigned long long xw[VEC];
     if (valid && col0 + VEC <= s.C && ((reinterpret_cast<uintptr_t>(X) & 15u) == 0)) {
 #pragma unroll
       for (int t = 0; t < VEC / 2; ++t) {
         const ulonglong2 v = __ldg(reinterpret_cast<const ulonglong2*>(X) + t);
-        xw[2 * t][0] = v.x;
-        xw[2 * t + 1][0] = v.y;
+        xw[2 * t] = v.x;
+        xw[2 * t + 1] = v.y;
       }
     } else {
 #pragma unroll
-      for (int e = 0; e < VEC; ++e) xw[e][0] = (valid && col0 + e < s.C) ? __ldg(X + e) : 0ull;
+      for (int e = 0; e < VEC; ++e) xw[e] = (valid && col0 + e < s.C) ? __ldg(X + e) : 0ull;
     }
     unsigned long long m = 0;
 #pragma unroll
-    for (int e = 0; e < VEC; ++e) m = max(m, abs_u64(xw[e][0]));
+    for (int e = 0; e < VEC; ++e) m = max(m, abs_u64(xw[e]));
     if (isA) max_a = max(max_a, m);
     else max_b = max(max_b, m);
-    // chunk count for the whole warp: none when every |x| <= 2^23
+    // words for the whole warp: none when every |x| <= 2^23, else the fewest
+    // holding every entry's two's complement
     const int bits = __reduce_max_sync(0xffffffffu, (unsigned)bitlen64(m));
-    const int nch = (bits <= 23 || (bits == 24 && __all_sync(0xffffffffu, m <= (1ull << 23))))
-                        ? 0 : (bits + 1 + kChunkBits - 1) / kChunkBits;
+    const int nw = (bits <= 23 || (bits == 24 && __all_sync(0xffffffffu, m <= (1ull << 23)))) ? 0
+                   : bits + 1 <= 32 ? 1 : 2;
     if (!valid) continue;
-    float cf[VEC][NCH];
-    if (nch == 0) {
+    uint32_t wd[VEC][2];
+    bool neg[VEC];
+    float xf[VEC];
 #pragma unroll
-      for (int e = 0; e < VEC; ++e) {
-        cf[e][0] = (float)(long long)xw[e][0];
-#pragma unroll
-        for (int c = 1; c < NCH; ++c) cf[e][c] = 0.0f;
-      }
-    } else {
-#pragma unroll
-      for (int e = 0; e < VEC; ++e) {
-#pragma unroll
-        for (int c = 0; c < NCH; ++c) {
-          const unsigned a = chunk_bits<1>(xw[e], 1, c * kChunkBits);
-          const int v = (c == nch - 1) ? (int)((a ^ 0x800u) - 0x800u) : (int)a;
-          cf[e][c] = c < nch ? (float)v : 0.0f;
-        }
-      }
+    for (int e = 0; e < VEC; ++e) {
+      neg[e] = (long long)xw[e] < 0;
+      xf[e] = (float)(int)(long long)xw[e];
+      wd[e][0] = (uint32_t)xw[e];
+      wd[e][1] = (uint32_t)(xw[e] >> 32);
     }
-    emit_residues<VEC, NCH>(cf, nch, P, s.Y + row * s.ldy + col0, s.plane);
+    emit_int_residues<VEC, 2>(wd, neg, xf, nw, P, rec, ws, s.Y + row * s.ldy + col0, s.plane);
   }
   max_a = block_max_u64(max_a);
   max_b = block_max_u64(max_b);
@@ -585,49 +644,69 @@ __global__ void __launch_bounds__(256) split_i64_kernel(SplitSide sa, SplitSide 
   allow_dependents();
 }
 
-// |x| * 2^f for a floating-point x, from its bit pattern: at a lossless point
-// |x| 2^f = t * 2^(12 c0) exactly (lost = false); at a coarsened point
-// t = floor(|x| 2^f), c0 = 0, and lost tells whether any bit was dropped.
+// |x| * 2^f for a floating-point x, from its bit pattern, as t * 2^sh: at a
+// lossless point t is the significand and sh >= 0 (lost = false); at a
+// coarsened point t = floor(|x| 2^f), sh = 0, and lost tells whether any bit
+// was dropped.
 template <typename Bits>
 __device__ __forceinline__ void scaled_magnitude(Bits v, int f, bool& neg, unsigned long long& t, bool& lost,
-                                                 int& c0) {
+                                                 int& sh) {
   using F = FloatFormat<Bits>;
   const int be = (int)((v >> F::kFracBits) & F::kExpMask);
   neg = (v & F::kSign) != 0;
   const unsigned long long hidden = 1ull << F::kFracBits;
   const unsigned long long m = ((unsigned long long)v & (hidden - 1ull)) | (be ? hidden : 0ull);
-  int sh = (be > 1 ? be : 1) - F::kLsbBias + f;  // |x| * 2^f = m * 2^sh
+  sh = (be > 1 ? be : 1) - F::kLsbBias + f;  // |x| * 2^f = m * 2^sh
   if (m == 0 || sh >= 0) {
     if (m == 0) sh = 0;
-    c0 = sh / kChunkBits;
-    t = m << (sh % kChunkBits);
+    t = m;
     lost = false;
   } else {
     const int r = -sh;
     t = r >= 64 ? 0ull : m >> r;
     lost = r >= 64 ? true : (m & ((1ull << r) - 1ull)) != 0ull;
-    c0 = 0;
+    sh = 0;
   }
 }
 
-// Floating-point operands: X' = x * 2^f = +-m * 2^sh with
-// sh = max(be,1) - min(be',1) >= 0 when lossless; the significand (53 bits for
-// binary64, 24 for binary32) shifted by sh % 12 is cut into NC chunks starting
-// at chunk index sh / 12.  No floating-point instruction reads x.
+// Words of t dotted with a prime's byte weights, reduced: t mod q, balanced.
+template <int NWF>
+__device__ __forceinline__ float residue_of_words(unsigned long long t, const int (&wv)[NWF], float q, float iq) {
+  int acc = dp4a_us((uint32_t)t, wv[0], 0);
+  if constexpr (NWF == 2) acc = dp4a_us((uint32_t)(t >> 32), wv[1], acc);
+  return bal_mod_small(int_to_float_exact(acc), q, iq);  // |acc| <= 8 * 255 * 125 < 2^22
+}
+
+// 2^s mod q for the primes and shifts a split block needs, as fp16 (exact).
+__device__ float g_pow2[kNumPrimes][kPow2Span];
+
+__device__ __forceinline__ void load_pow2(__half* pw, int P, int cols) {
+  for (int i = threadIdx.x; i < P * cols; i += blockDim.x) {
+    const int p = i / cols, c = i - p * cols;
+    pw[p * kPow2Span + c] = __float2half_rn(g_pow2[p][c]);
+  }
+}
+
+// Shifts a floating-point split can meet: sh < max(bits_a, bits_b) <= 255.
+__device__ __forceinline__ int pow2_cols(const DevPlan* plan) {
+  const int b = max(plan->bits_a, plan->bits_b);
+  return b < 1 ? 1 : (b > kPow2Span ? kPow2Span : b);
+}
+
+// Floating-point operands.  No floating-point instruction reads x.
 template <typename Bits, int VEC>
 __global__ void __launch_bounds__(256) split_float_kernel(SplitSide sa, SplitSide sb, const DevPlan* plan) {
   using F = FloatFormat<Bits>;
-  // the significand shifted left by up to 11 bits spans NC chunks: 6 (binary64) or 3 (binary32)
-  constexpr int kSpan = F::kFracBits + 1 + kChunkBits - 1;
-  constexpr int NC = (kSpan + kChunkBits - 1) / kChunkBits;
+  constexpr int NWF = F::kFracBits + 2 > 32 ? 2 : 1;  // words of t (the floored magnitude may gain a bit)
   constexpr int PER = 16 / sizeof(Bits);
-  __shared__ float w_s[kNumPrimes][kMaxChunks];
+  __shared__ PrimeRec rec[kNumPrimes];
+  __shared__ __half pw[kNumPrimes * kPow2Span];
+  load_prime_recs(rec, nullptr);
   wait_for_predecessor();
   if (plan->status) return;
   const int P = plan->P;
   const int fa = plan->f_a, fb = plan->f_b;
-  for (int i = threadIdx.x; i < P * kMaxChunks; i += blockDim.x)
-    w_s[i / kMaxChunks][i % kMaxChunks] = c_tab.chunk_w[i / kMaxChunks][i % kMaxChunks];
+  load_pow2(pw, P, pow2_cols(plan));
   __syncthreads();
   const long long total = sa.items + sb.items;
   for (long long it = (long long)blockIdx.x * blockDim.x + threadIdx.x; it < total;
@@ -651,33 +730,30 @@ __global__ void __launch_bounds__(256) split_float_kernel(SplitSide sa, SplitSid
 #pragma unroll
       for (int e = 0; e < VEC; ++e) xv[e] = col0 + e < s.C ? __ldg(X + e) : (Bits)0;
     }
-    float cf[VEC][NC];
-    int c0[VEC];
+    unsigned long long tv[VEC];
+    int shv[VEC];
+    bool negv[VEC];
 #pragma unroll
     for (int e = 0; e < VEC; ++e) {
-      bool neg, lost;
-      unsigned long long t;
-      scaled_magnitude<Bits>(xv[e], f, neg, t, lost, c0[e]);
-      if (neg && lost) ++t;  // floor of a negative value rounds away from zero
-      const float sg = neg ? -1.0f : 1.0f;
-#pragma unroll
-      for (int c = 0; c < NC; ++c) cf[e][c] = sg * (float)(unsigned)((t >> (kChunkBits * c)) & 0xFFFu);
+      bool lost;
+      scaled_magnitude<Bits>(xv[e], f, negv[e], tv[e], lost, shv[e]);
+      if (negv[e] && lost) ++tv[e];  // floor of a negative value rounds away from zero
     }
     __half* y = s.Y + row * s.ldy + col0;
     for (int p = 0; p < P; ++p) {
-      const float q = c_tab.qf[p], iq = c_tab.invq[p];
+      const PrimeRec& R = rec[p];
+      const float q = R.q, iq = R.iq;
+      int wv[NWF];
+      load_weights<NWF>(R, wv);
+      const __half* pwp = pw + p * kPow2Span;
       float r[VEC];
 #pragma unroll
       for (int e = 0; e < VEC; ++e) {
-        float acc = 0.0f;
-#pragma unroll
-        for (int c = 0; c < NC; ++c) acc = __fmaf_rn(cf[e][c], w_s[p][c0[e] + c], acc);
-        r[e] = bal_mod_small(acc, q, iq);  // |acc| <= NC * 4095 * 125 < 2^23
+        const float rt = residue_of_words<NWF>(tv[e], wv, q, iq);
+        const float rr = bal_mod_small(rt * __half2float(pwp[shv[e]]), q, iq);  // |rt * 2^sh mod q| < 2^14
+        r[e] = negv[e] ? -rr : rr;
       }
-      __half2 h[VEC / 2];
-#pragma unroll
-      for (int e = 0; e < VEC / 2; ++e) h[e] = __floats2half2_rn(r[2 * e], r[2 * e + 1]);
-      *reinterpret_cast<uint4*>(y + (long long)p * s.plane) = *reinterpret_cast<const uint4*>(h);
+      store_residues<VEC>(r, y + (long long)p * s.plane);
     }
   }
   allow_dependents();
@@ -704,17 +780,17 @@ struct IvSide {
 template <typename Bits, int VEC>
 __global__ void __launch_bounds__(256) split_interval_kernel(IvSide sa, IvSide sb, const DevPlan* plan) {
   using F = FloatFormat<Bits>;
-  constexpr int kSpan = F::kFracBits + 1 + kChunkBits - 1;
-  constexpr int NC = (kSpan + kChunkBits - 1) / kChunkBits;
+  constexpr int NWF = F::kFracBits + 2 > 32 ? 2 : 1;
   constexpr int PER = 16 / sizeof(Bits);
-  static_assert(VEC == 4 && (VEC * sizeof(Bits)) % 16 == 0, "four entries per item, whole 16-byte loads");
-  __shared__ float w_s[kNumPrimes][kMaxChunks];
+  static_assert((VEC * sizeof(Bits)) % 16 == 0, "whole 16-byte loads");
+  __shared__ PrimeRec rec[kNumPrimes];
+  __shared__ __half pw[kNumPrimes * kPow2Span];
+  load_prime_recs(rec, nullptr);
   wait_for_predecessor();
   if (plan->status) return;
   const int P = plan->P;
   const int fa = plan->f_a, fb = plan->f_b;
-  for (int i = threadIdx.x; i < P * kMaxChunks; i += blockDim.x)
-    w_s[i / kMaxChunks][i % kMaxChunks] = c_tab.chunk_w[i / kMaxChunks][i % kMaxChunks];
+  load_pow2(pw, P, pow2_cols(plan));
   __syncthreads();
   const long long total = sa.items + sb.items;
   for (long long it = (long long)blockIdx.x * blockDim.x + threadIdx.x; it < total;
@@ -746,53 +822,39 @@ __global__ void __launch_bounds__(256) split_interval_kernel(IvSide sa, IvSide s
         }
       }
     }
-    float cm[VEC][NC], cr[VEC][NC];
-    int c0m[VEC], c0r[VEC];
+    unsigned long long tm[VEC], tr[VEC];
+    int shm[VEC], shr[VEC];
     bool negm[VEC], lostm[VEC];
 #pragma unroll
     for (int e = 0; e < VEC; ++e) {
-      unsigned long long t;
       bool neg, lost;
-      scaled_magnitude<Bits>(xm[e], f, negm[e], t, lostm[e], c0m[e]);
-      if (negm[e] && lostm[e]) ++t;  // |floor(x 2^f)|
-      const float sg = negm[e] ? -1.0f : 1.0f;
-#pragma unroll
-      for (int c = 0; c < NC; ++c) cm[e][c] = sg * (float)(unsigned)((t >> (kChunkBits * c)) & 0xFFFu);
-      scaled_magnitude<Bits>(xr[e], f, neg, t, lost, c0r[e]);  // radii are >= 0 (the planner checked)
-      if (lost) ++t;                                             // ceil(r 2^f)
-#pragma unroll
-      for (int c = 0; c < NC; ++c) cr[e][c] = (float)(unsigned)((t >> (kChunkBits * c)) & 0xFFFu);
+      scaled_magnitude<Bits>(xm[e], f, negm[e], tm[e], lostm[e], shm[e]);
+      if (negm[e] && lostm[e]) ++tm[e];  // |floor(x 2^f)|
+      scaled_magnitude<Bits>(xr[e], f, neg, tr[e], lost, shr[e]);  // radii are >= 0 (the planner checked)
+      if (lost) ++tr[e];                                            // ceil(r 2^f)
     }
     __half* y = s.Y + row * s.ldy + col0;
     for (int p = 0; p < P; ++p) {
-      const float q = c_tab.qf[p], iq = c_tab.invq[p];
+      const PrimeRec& R = rec[p];
+      const float q = R.q, iq = R.iq;
+      int wv[NWF];
+      load_weights<NWF>(R, wv);
+      const __half* pwp = pw + p * kPow2Span;
       float r0[VEC], r1[VEC], r2[VEC];
 #pragma unroll
       for (int e = 0; e < VEC; ++e) {
-        float am = 0.0f, ar = 0.0f;
-#pragma unroll
-        for (int c = 0; c < NC; ++c) {
-          am = __fmaf_rn(cm[e][c], w_s[p][c0m[e] + c], am);
-          ar = __fmaf_rn(cr[e][c], w_s[p][c0r[e] + c], ar);
-        }
-        const float rm = bal_mod_small(am, q, iq);  // |am|, |ar| <= NC * 4095 * 125 < 2^23
-        const float rr = bal_mod_small(ar, q, iq);
-        const float rabs = negm[e] ? -rm : bal_mod_small(rm + (lostm[e] ? 1.0f : 0.0f), q, iq);  // ceil |x| 2^f
+        const float am = bal_mod_small(residue_of_words<NWF>(tm[e], wv, q, iq) * __half2float(pwp[shm[e]]), q, iq);
+        const float rr = bal_mod_small(residue_of_words<NWF>(tr[e], wv, q, iq) * __half2float(pwp[shr[e]]), q, iq);
+        const float rm = negm[e] ? -am : am;                                           // floor(x 2^f)
+        const float rabs = negm[e] ? am : bal_mod_small(am + (lostm[e] ? 1.0f : 0.0f), q, iq);  // ceil |x| 2^f
         r0[e] = rm;
         r1[e] = isA ? rabs : rr;
         r2[e] = isA ? rr : bal_mod_small(rabs + rr, q, iq);
       }
       __half* yp = y + (long long)p * s.plane;
-      __half2 h[VEC / 2];
-#pragma unroll
-      for (int e = 0; e < VEC / 2; ++e) h[e] = __floats2half2_rn(r0[2 * e], r0[2 * e + 1]);
-      *reinterpret_cast<uint2*>(yp) = *reinterpret_cast<const uint2*>(h);
-#pragma unroll
-      for (int e = 0; e < VEC / 2; ++e) h[e] = __floats2half2_rn(r1[2 * e], r1[2 * e + 1]);
-      *reinterpret_cast<uint2*>(yp + s.sub) = *reinterpret_cast<const uint2*>(h);
-#pragma unroll
-      for (int e = 0; e < VEC / 2; ++e) h[e] = __floats2half2_rn(r2[2 * e], r2[2 * e + 1]);
-      *reinterpret_cast<uint2*>(yp + 2 * s.sub) = *reinterpret_cast<const uint2*>(h);
+      store_residues<VEC>(r0, yp);
+      store_residues<VEC>(r1, yp + s.sub);
+      store_residues<VEC>(r2, yp + 2 * s.sub);
     }
   }
   allow_dependents();
@@ -819,13 +881,6 @@ struct GarnerGE {
 };
 
 constexpr int kGarnerBatch = 8;
-constexpr float kMagic = 12582912.0f;     // 1.5 * 2^23
-constexpr int kMagicBits = 0x4B400000;    // its bit pattern
-
-// Exact conversions without the conversion unit, for |v| < 2^22: the integer
-// sits in the low mantissa bits of kMagic + v.
-__device__ __forceinline__ float int_to_float_exact(int v) { return __int_as_float(kMagicBits + v) - kMagic; }
-__device__ __forceinline__ int float_bits_offset(float v) { return __float_as_int(v + kMagic); }  // = kMagicBits + v
 
 // x (W 32-bit words, two's complement, mod 2^(32W)) += D * Q_i, for the words
 // that can be significant once digits up to `last` are in (|x| < 2^(8(last+1)-1)).
@@ -1215,13 +1270,14 @@ cudaError_t upload_tables() {
   std::lock_guard<std::mutex> lock(mu);
   if (done[dev]) return cudaSuccess;
   e = cudaMemcpyToSymbol(c_tab, &host_tables(), sizeof(Tables));
+  if (e == cudaSuccess) e = cudaMemcpyToSymbol(g_pow2, host_pow2().v, sizeof(Pow2Table));
   if (e == cudaSuccess) done[dev] = true;
   return e;
 }
 
 static int planner_blocks(long long n) {
   long long b = (n + 256LL * 8 - 1) / (256LL * 8);
-  long long cap = sm_count();  // few blocks: each one ends with atomics on the plan block
+  long long cap = 4LL * sm_count();  // enough loads in flight; each block ends with a few atomics on the plan
   return (int)(b < 1 ? 1 : (b > cap ? cap : b));
 }
 
@@ -1319,17 +1375,17 @@ cudaError_t launch_split(int op, const void* A, const void* A2, const void* B, c
   if (L <= 1) {
     constexpr int V = 8;
     const SplitSide sa = make_side(A, ra, M, K, lda, la, V), sb = make_side(B, rb, brows, bcols, ldb, lb, V);
-    return launch_dependent(split_int_kernel<V, 6, 1>, split_grid(sa.items + sb.items), 256, 0, st, sa, sb,
+    return launch_dependent(split_int_kernel<V, 1>, split_grid(sa.items + sb.items), 256, 0, st, sa, sb,
                             (const DevPlan*)plan);
   } else if (L <= 2) {
-    constexpr int V = 4;
+    constexpr int V = 8;
     const SplitSide sa = make_side(A, ra, M, K, lda, la, V), sb = make_side(B, rb, brows, bcols, ldb, lb, V);
-    return launch_dependent(split_int_kernel<V, 11, 2>, split_grid(sa.items + sb.items), 256, 0, st, sa, sb,
+    return launch_dependent(split_int_kernel<V, 2>, split_grid(sa.items + sb.items), 256, 0, st, sa, sb,
                             (const DevPlan*)plan);
   } else {
-    constexpr int V = 2;
+    constexpr int V = 4;
     const SplitSide sa = make_side(A, ra, M, K, lda, la, V), sb = make_side(B, rb, brows, bcols, ldb, lb, V);
-    return launch_dependent(split_int_kernel<V, 22, 4>, split_grid(sa.items + sb.items), 256, 0, st, sa, sb,
+    return launch_dependent(split_int_kernel<V, 4>, split_grid(sa.items + sb.items), 256, 0, st, sa, sb,
                             (const DevPlan*)plan);
   }
   return cudaGetLastError();

@@ -11,8 +11,8 @@
 namespace rg {
 
 constexpr int kNumPrimes = RG_NUM_PRIMES;  // odd primes 3..251, largest first
-constexpr int kChunkBits = 12;             // operand split into 12-bit chunks
-constexpr int kMaxChunks = 24;             // covers 256-bit operands (22) with slack
+constexpr int kMaxWords = 8;               // 32-bit words of a 256-bit operand
+constexpr int kPow2Span = 256;             // 2^s mod q tabulated for s < 256
 constexpr int kGarnerWords = 14;           // ceil(53 / 4) int8x4 words per Garner row
 constexpr int kQWords = 11;                // 32-bit words of the mixed-radix weights Q_i
 constexpr int kMaxLimbsOut = RG_MAX_LIMBS_OUT;
@@ -28,7 +28,7 @@ struct DevPlan {
   int bound_bits;         // bits_a + bits_b + ceil(log2 K)
   int f_a, f_b;           // fp64 scale exponents
   int lossless;           // fp64: 1 if the scaling is exact
-  int nchunk_a, nchunk_b; // 12-bit chunks the split reads per entry
+  int nword_a, nword_b;   // 32-bit words the split reads per integer entry (0: the entry is an exact fp32)
   unsigned blocks_done;   // planner blocks finished (the last one derives the plan)
   int pad0[5];
   // reductions written by the planner kernels
@@ -50,7 +50,11 @@ struct Tables {
   int q[kNumPrimes];                          // q_0 = 251 > q_1 > ... > q_52 = 3
   float qf[kNumPrimes];                       // q as float
   float invq[kNumPrimes];                     // fl(1/q)
-  float chunk_w[kNumPrimes][kMaxChunks];      // balanced 2^(12c) mod q, as float
+  // Residue split: byte j of a little-endian word string weighs 2^(8j) mod q
+  // (balanced), packed four to an int32 (byte 4w + b in bits 8b..8b+7 of
+  // wbyte[.][w]); a string of k words as a whole weighs 2^(32k) mod q.
+  int wbyte[kNumPrimes][kMaxWords];
+  int wword[kNumPrimes][kMaxWords + 1];
   int log2P[kNumPrimes + 1];                  // floor(log2(q_0 * ... * q_{n-1})), n = 0..53
   // Balanced Garner: v_i = bal( ginv[i] * r_i + sum_{j<i} gd[i][j] * v_j  mod q_i )
   // with ginv[i] = bal(Q_i^-1 mod q_i), gd[i][j] = bal(-(Q_j mod q_i) * Q_i^-1 mod q_i),
@@ -63,6 +67,13 @@ struct Tables {
 
 // Host side: the tables (built once) and the primes.
 const Tables& host_tables();
+
+// 2^s mod q (balanced) for every prime and s < 256, kept in global memory
+// (too large for the constant bank beside Tables).
+struct Pow2Table {
+  float v[kNumPrimes][kPow2Span];
+};
+const Pow2Table& host_pow2();
 
 // ---------------------------------------------------------------------------
 // Device helpers

@@ -44,7 +44,13 @@ void build(Tables& t) {
     int q = t.q[i];
     t.qf[i] = (float)q;
     t.invq[i] = 1.0f / (float)q;
-    for (int c = 0; c < kMaxChunks; ++c) t.chunk_w[i][c] = (float)balanced(mod_pow(2, kChunkBits * c, q), q);
+    for (int w = 0; w < kMaxWords; ++w) {
+      uint32_t packed = 0;
+      for (int b = 0; b < 4; ++b)
+        packed |= (uint32_t)(uint8_t)(int8_t)balanced(mod_pow(2, 8 * (4 * w + b), q), q) << (8 * b);
+      t.wbyte[i][w] = (int)packed;
+    }
+    for (int k = 0; k <= kMaxWords; ++k) t.wword[i][k] = balanced(mod_pow(2, 32 * k, q), q);
   }
 
   // floor(log2) of the running product, with an exact multi-word product.
@@ -102,6 +108,17 @@ const Tables& host_tables() {
   static Tables t;
   static std::once_flag once;
   std::call_once(once, [] { build(t); });
+  return t;
+}
+
+const Pow2Table& host_pow2() {
+  static Pow2Table t;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    const Tables& b = host_tables();
+    for (int i = 0; i < kNumPrimes; ++i)
+      for (int e = 0; e < kPow2Span; ++e) t.v[i][e] = (float)balanced(mod_pow(2, e, b.q[i]), b.q[i]);
+  });
   return t;
 }
 
