@@ -70,7 +70,7 @@ class Layout(ctypes.Structure):
 class PlanInfo(ctypes.Structure):
     _fields_ = [("status", ctypes.c_int), ("nprimes", ctypes.c_int), ("bits_a", ctypes.c_int),
                 ("bits_b", ctypes.c_int), ("bound_bits", ctypes.c_int), ("f_a", ctypes.c_int),
-                ("f_b", ctypes.c_int), ("lossless", ctypes.c_int)]
+                ("f_b", ctypes.c_int), ("lossless", ctypes.c_int), ("splits", ctypes.c_int)]
 
     def as_dict(self):
         return {k: getattr(self, k) for k, _ in self._fields_}

@@ -58,7 +58,7 @@ int pmax_for(int op, long long K, int la, int lb, int nprimes) {
 struct Layout {
   size_t plan, ra, rb, rc, a, b, c, c2, total;
   long long lda, ldb, ldc;
-  int pmax;
+  int pmax, splits;  // splits: K slices RC has room for
 };
 
 bool is_interval(int op) { return op == RG_OP_INTERVAL || op == RG_OP_INTERVAL_F32; }
@@ -100,12 +100,13 @@ bool make_layout(int op, long long batch, long long M, long long N, long long K,
   int pmax = pmax_for(op, K, la, lb, nprimes);
   L->pmax = pmax;
   const size_t planes = (size_t)pmax * planes_per_product(op) * batch;
+  L->splits = gemm_max_splits((long long)planes_per_product(op) * batch, M, N, K);
   L->ra = off;
   off = align_up(off + planes * M * L->lda * 2, kAlign);
   L->rb = off;
   off = align_up(off + planes * (transb ? N : K) * L->ldb * 2, kAlign);
   L->rc = off;
-  off = align_up(off + planes * M * L->ldc, kAlign);
+  off = align_up(off + planes * M * L->ldc * L->splits, kAlign);
   if (flags & RG_FLAG_HOST) {
     size_t ea = elem_bytes(op, la), eb = elem_bytes(op, lb), ec = elem_bytes(op, lc);
     const size_t arrays = arrays_per_operand(op);
@@ -216,7 +217,7 @@ int run(int op, const void* A, const void* A2, int la, const void* B, const void
                       transb, s));
   int fault = g_fault.exchange(0);
   RG_TRY(launch_gemm(w + L.ra, L.lda, w + L.rb, L.ldb, w + L.rc, L.ldc, L.pmax, (int)gemm_batch, i64 ? nprimes : 0,
-                     M, N, K, plan, s, fault, g_wait_ns.load(), i64, transb));
+                     M, N, K, plan, s, fault, g_wait_ns.load(), i64, transb, L.splits));
   // Garner sees the batch as batch * M rows of each plane; an interval's
   // three product planes lie batch * M rows apart
   const long long sub = batch * M * L.ldc;
@@ -318,7 +319,7 @@ int res_gemm_stage(const uint16_t* RA, int64_t lda, const uint16_t* RB, int64_t 
   RG_TRY(cudaMemsetAsync(plan, 0, sizeof(DevPlan), s));
   int fault = g_fault.exchange(0);
   RG_TRY(launch_gemm(RA, lda, RB, ldb, RC, ldc, nprimes, 1, nprimes, M, N, K, plan, s, fault, g_wait_ns.load(), false,
-                     transb));
+                     transb, 1));
   return finish(ws, s, flags);
 }
 
@@ -369,6 +370,7 @@ int rg_get_plan(const void* ws, void* stream, rg_plan_info* out) {
   out->f_a = p.f_a;
   out->f_b = p.f_b;
   out->lossless = p.lossless;
+  out->splits = p.splits > 0 ? p.splits : 1;
   return RG_OK;
 }
 

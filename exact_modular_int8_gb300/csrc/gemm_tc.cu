@@ -67,6 +67,8 @@ struct GemmParams {
   int mt, nt;
   int kb_total;
   int batch;       // independent products per prime; plane = prime * batch + product
+  int planes;      // residue planes of one K slice of RC (pmax * batch)
+  int max_splits;  // K slices the output buffer has room for (1: no split-K)
   int P_fixed;     // 0: read (or derive) the prime count from the plan
   int derive_i64;  // derive the int64 plan from max |A|, max |B|
   int ceil_log2_k;
@@ -287,6 +289,51 @@ __device__ __forceinline__ TileCoord tile_coord(int t, int mt, int nt, int batch
   return c;
 }
 
+// Split-K: when there are too few tiles for the persistent CTAs, K is cut
+// into S slices of whole 1024-K chunks; a unit is one tile of one slice, and
+// each unit's residues go to its slice's planes of RC (summed mod q by
+// slice_sum_kernel afterwards).  S minimises the time in chunk units:
+// (waves of units) x (chunks per unit), plus, for S > 1, the summing pass (a
+// launch, about half a chunk, and S slices of one byte per output, about
+// tiles / 512 chunks per slice at HBM rate).  Every CTA derives the same S,
+// the smallest on ties, and CTA 0 records it in the plan.
+struct Unit {
+  TileCoord tc;
+  int s, kb_lo, kb_hi, nc;  // slice, k-block range, 1024-K chunks
+};
+
+struct Splits {
+  int S, kbs;  // slices and k-blocks per slice
+};
+
+__device__ __forceinline__ Splits choose_splits(const GemmParams& gp, int tiles, int workers, DevPlan* plan) {
+  const int nkc = (gp.kb_total + KC_BLOCKS - 1) / KC_BLOCKS;
+  int best = 1;
+  long long best_cost = -1;
+  for (int S = 1; S <= gp.max_splits && S <= nkc; ++S) {
+    const int cps = (nkc + S - 1) / S;
+    if ((nkc + cps - 1) / cps != S) continue;  // a slice would be empty
+    const long long waves = ((long long)tiles * S + workers - 1) / workers;
+    const long long cost = waves * cps * 512 + (S > 1 ? 256 + (long long)S * tiles : 0);  // in 1/512 chunk
+    if (best_cost < 0 || cost < best_cost) {
+      best_cost = cost;
+      best = S;
+    }
+  }
+  if (blockIdx.x == 0 && threadIdx.x == 0) plan->splits = best;
+  return Splits{best, (nkc + best - 1) / best * KC_BLOCKS};
+}
+
+__device__ __forceinline__ Unit unit_of(int u, int tiles, int mt, int nt, int batch, const Splits& sp, int kb_total) {
+  Unit r;
+  r.s = u / tiles;
+  r.tc = tile_coord(u - r.s * tiles, mt, nt, batch);
+  r.kb_lo = r.s * sp.kbs;
+  r.kb_hi = min(r.kb_lo + sp.kbs, kb_total);
+  r.nc = (r.kb_hi - r.kb_lo + KC_BLOCKS - 1) / KC_BLOCKS;
+  return r;
+}
+
 // ---------------------------------------------------------------------------
 // The kernel
 // ---------------------------------------------------------------------------
@@ -301,8 +348,9 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
   wait_for_predecessor();
   const int P = launch_primes(gp, plan);
   if (P == 0) return;
-  const int total = P * gp.batch * gp.mt * gp.nt;
-  const int nc_tile = (gp.kb_total + KC_BLOCKS - 1) / KC_BLOCKS;
+  const int tiles = P * gp.batch * gp.mt * gp.nt;
+  const Splits sp = choose_splits(gp, tiles, (int)gridDim.x, plan);
+  const int total = tiles * sp.S;
 
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint8_t* stage_base = smem;
@@ -352,8 +400,9 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       uint32_t issued_phase[STAGES] = {};
       bool ok = true;
       for (int t = blockIdx.x; t < total && ok; t += gridDim.x) {
-        TileCoord tc = tile_coord(t, gp.mt, gp.nt, gp.batch);
-        for (int kb = 0; kb < gp.kb_total; ++kb) {
+        const Unit u = unit_of(t, tiles, gp.mt, gp.nt, gp.batch, sp, gp.kb_total);
+        const TileCoord& tc = u.tc;
+        for (int kb = u.kb_lo; kb < u.kb_hi; ++kb) {
           if (!wait_bounded(smem_u32(&empty[stage]), phase ^ 1u, ctl, 1)) {
             ok = false;
             break;
@@ -393,7 +442,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       uint32_t phase = 0, acc_iter = 0;
       bool ok = true, any = false;
       for (int t = blockIdx.x; t < total && ok; t += gridDim.x) {
-        for (int c = 0; c < nc_tile && ok; ++c) {
+        const Unit u = unit_of(t, tiles, gp.mt, gp.nt, gp.batch, sp, gp.kb_total);
+        for (int c = 0; c < u.nc && ok; ++c) {
           const uint32_t b = acc_iter & 1u, aph = (acc_iter >> 1) & 1u;
           if (!wait_bounded(smem_u32(&tempty[b]), aph ^ 1u, ctl, 2)) {
             ok = false;
@@ -401,8 +451,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
           }
           tc_fence_after();
           const uint32_t d = tmem_base + b * BN;
-          const int kb0 = c * KC_BLOCKS;
-          const int kb1 = min(kb0 + KC_BLOCKS, gp.kb_total);
+          const int kb0 = u.kb_lo + c * KC_BLOCKS;
+          const int kb1 = min(kb0 + KC_BLOCKS, u.kb_hi);
           for (int kb = kb0; kb < kb1; ++kb) {
             if (!wait_bounded(smem_u32(&full[stage]), phase, ctl, 3)) {
               ok = false;
@@ -450,7 +500,10 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     bool ok = true;
     const uint32_t out_s = smem_u32(out_base);
     for (int t = blockIdx.x; t < total && ok; t += gridDim.x) {
-      TileCoord tc = tile_coord(t, gp.mt, gp.nt, gp.batch);
+      const Unit u = unit_of(t, tiles, gp.mt, gp.nt, gp.batch, sp, gp.kb_total);
+      const TileCoord& tc = u.tc;
+      const int nc_tile = u.nc;
+      const int out_plane = u.s * gp.planes + tc.p;
       const float q = gp.qf[tc.pr], iq = gp.invq[tc.pr];
       bool first_write = true;
       for (int c = 0; c < nc_tile; ++c) {
@@ -507,8 +560,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
           fence_proxy_async_smem();
           epilogue_bar();
           if (et == 0) {
-            tma_store_3d(&tmC, out_s, tc.n * BN, tc.m * BM, tc.p);
-            if (tc.n * BN + 128 < gp.N) tma_store_3d(&tmC, out_s + OUT_HALF, tc.n * BN + 128, tc.m * BM, tc.p);
+            tma_store_3d(&tmC, out_s, tc.n * BN, tc.m * BM, out_plane);
+            if (tc.n * BN + 128 < gp.N) tma_store_3d(&tmC, out_s + OUT_HALF, tc.n * BN + 128, tc.m * BM, out_plane);
             bulk_commit();
           }
         }
@@ -632,8 +685,9 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
   const int P = launch_primes(gp, plan);  // the same decision in both CTAs of the pair
   if (P == 0) return;
   const int mt2 = (gp.M + 255) / 256;
-  const int total = P * gp.batch * mt2 * gp.nt;
-  const int nc_tile = (gp.kb_total + KC_BLOCKS - 1) / KC_BLOCKS;
+  const int tiles = P * gp.batch * mt2 * gp.nt;
+  const Splits sp = choose_splits(gp, tiles, (int)(gridDim.x >> 1), plan);
+  const int total = tiles * sp.S;
   const uint32_t rank = cluster_rank();
   const int cid = blockIdx.x >> 1, ncl = gridDim.x >> 1;
 
@@ -683,8 +737,9 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       uint32_t phase = 0;
       bool ok = true;
       for (int t = cid; t < total && ok; t += ncl) {
-        TileCoord tc = tile_coord(t, mt2, gp.nt, gp.batch);
-        for (int kb = 0; kb < gp.kb_total; ++kb) {
+        const Unit u = unit_of(t, tiles, mt2, gp.nt, gp.batch, sp, gp.kb_total);
+        const TileCoord& tc = u.tc;
+        for (int kb = u.kb_lo; kb < u.kb_hi; ++kb) {
           if (!wait_bounded_cluster(smem_u32(&empty[stage]), phase ^ 1u, ctl, 11)) {
             ok = false;
             break;
@@ -716,7 +771,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       uint32_t phase = 0, acc_iter = 0;
       bool ok = true, any = false;
       for (int t = cid; t < total && ok; t += ncl) {
-        for (int c = 0; c < nc_tile && ok; ++c) {
+        const Unit u = unit_of(t, tiles, mt2, gp.nt, gp.batch, sp, gp.kb_total);
+        for (int c = 0; c < u.nc && ok; ++c) {
           const uint32_t b = acc_iter & 1u, aph = (acc_iter >> 1) & 1u;
           if (!wait_bounded_cluster(smem_u32(&tempty[b]), aph ^ 1u, ctl, 12)) {
             ok = false;
@@ -724,8 +780,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
           }
           tc_fence_after();
           const uint32_t d = tmem_base + b * BN;
-          const int kb0 = c * KC_BLOCKS;
-          const int kb1 = min(kb0 + KC_BLOCKS, gp.kb_total);
+          const int kb0 = u.kb_lo + c * KC_BLOCKS;
+          const int kb1 = min(kb0 + KC_BLOCKS, u.kb_hi);
           for (int kb = kb0; kb < kb1; ++kb) {
             if (!wait_bounded_cluster(smem_u32(&full[stage]), phase, ctl, 13)) {
               ok = false;
@@ -774,7 +830,10 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     const uint32_t out_s = smem_u32(out_base);
     const uint32_t tempty_leader[2] = {mapa_shared(smem_u32(&tempty[0]), 0), mapa_shared(smem_u32(&tempty[1]), 0)};
     for (int t = cid; t < total && ok; t += ncl) {
-      TileCoord tc = tile_coord(t, mt2, gp.nt, gp.batch);
+      const Unit u = unit_of(t, tiles, mt2, gp.nt, gp.batch, sp, gp.kb_total);
+      const TileCoord& tc = u.tc;
+      const int nc_tile = u.nc;
+      const int out_plane = u.s * gp.planes + tc.p;
       const float q = gp.qf[tc.pr], iq = gp.invq[tc.pr];
       const int row0 = tc.m * 256 + (int)rank * 128;
       bool first_write = true;
@@ -829,8 +888,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
           fence_proxy_async_smem();
           epilogue_bar();
           if (et == 0 && row0 < gp.M) {
-            tma_store_3d(&tmC, out_s, tc.n * BN, row0, tc.p);
-            if (tc.n * BN + 128 < gp.N) tma_store_3d(&tmC, out_s + OUT_HALF, tc.n * BN + 128, row0, tc.p);
+            tma_store_3d(&tmC, out_s, tc.n * BN, row0, out_plane);
+            if (tc.n * BN + 128 < gp.N) tma_store_3d(&tmC, out_s + OUT_HALF, tc.n * BN + 128, row0, out_plane);
             bulk_commit();
           }
         }
@@ -888,6 +947,48 @@ bool make_map_3d(CUtensorMap* m, CUtensorMapDataType dt, int esize, const void* 
   return r == CUDA_SUCCESS;
 }
 
+// Sums the K slices of the product residues into slice 0:
+// RC[0][p] = (RC[0][p] + ... + RC[S-1][p]) mod q, q the prime of plane p, for
+// the planes of the primes in use.  16 bytes per thread and slice; the bytes
+// are summed in 16-bit lanes (S <= 16 residues of at most 250 each).
+struct PrimeQ {
+  int q[kNumPrimes];
+};
+
+__global__ void __launch_bounds__(256) slice_sum_kernel(uint8_t* __restrict__ RC, long long slice_bytes,
+                                                        long long plane_bytes, int batch, PrimeQ qs,
+                                                        const DevPlan* plan) {
+  wait_for_predecessor();
+  if (plan->status) return;
+  const int S = plan->splits;
+  if (S <= 1) return;
+  const long long n16 = (long long)plan->P * batch * plane_bytes / 16;
+  for (long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x; i < n16;
+       i += (long long)gridDim.x * blockDim.x) {
+    const long long off = i * 16;
+    const int q = qs.q[(int)(off / plane_bytes) / batch];
+    uint32_t even[4] = {0, 0, 0, 0}, odd[4] = {0, 0, 0, 0};
+    for (int sl = 0; sl < S; ++sl) {
+      const uint4 v = *reinterpret_cast<const uint4*>(RC + sl * slice_bytes + off);
+      const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+      for (int k = 0; k < 4; ++k) {
+        even[k] += w[k] & 0x00FF00FFu;
+        odd[k] += (w[k] >> 8) & 0x00FF00FFu;
+      }
+    }
+    uint32_t out[4];
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+      const uint32_t b0 = (even[k] & 0xFFFFu) % q, b2 = (even[k] >> 16) % q;
+      const uint32_t b1 = (odd[k] & 0xFFFFu) % q, b3 = (odd[k] >> 16) % q;
+      out[k] = b0 | (b1 << 8) | (b2 << 16) | (b3 << 24);
+    }
+    *reinterpret_cast<uint4*>(RC + off) = make_uint4(out[0], out[1], out[2], out[3]);
+  }
+  allow_dependents();
+}
+
 int g_gemm_ready[64];
 std::atomic<int> g_gemm_variant{0};  // 0 automatic, 1 single-CTA, 2 CTA pair
 
@@ -895,7 +996,8 @@ std::atomic<int> g_gemm_variant{0};  // 0 automatic, 1 single-CTA, 2 CTA pair
 
 cudaError_t launch_gemm(const void* RA, long long lda, const void* RB, long long ldb, void* RC, long long ldc,
                         int pmax, int batch, int P_fixed, long long M, long long N, long long K, DevPlan* plan,
-                        cudaStream_t st, int fault, unsigned long long wait_ns, bool derive_i64, bool b_kmajor) {
+                        cudaStream_t st, int fault, unsigned long long wait_ns, bool derive_i64, bool b_kmajor,
+                        int max_splits) {
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
@@ -924,7 +1026,8 @@ cudaError_t launch_gemm(const void* RA, long long lda, const void* RB, long long
                                (uint64_t)ldb * 2, (uint64_t)N * ldb * 2, BK, pair ? 128 : BN)
                  : make_map_3d(&mb, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, RB, (uint64_t)N, (uint64_t)K, planes,
                                (uint64_t)ldb * 2, (uint64_t)K * ldb * 2, 64, BK)) ||
-      !make_map_3d(&mc, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, RC, (uint64_t)N, (uint64_t)M, planes, (uint64_t)ldc,
+      !make_map_3d(&mc, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, RC, (uint64_t)N, (uint64_t)M,
+                   planes * (uint64_t)max_splits, (uint64_t)ldc,
                    (uint64_t)M * ldc, 128, 128))
     return cudaErrorInvalidValue;
   GemmParams gp;
@@ -935,6 +1038,8 @@ cudaError_t launch_gemm(const void* RA, long long lda, const void* RB, long long
   gp.nt = (int)((N + BN - 1) / BN);
   gp.kb_total = (int)((K + BK - 1) / BK);
   gp.batch = batch;
+  gp.planes = (int)planes;
+  gp.max_splits = max_splits;
   gp.P_fixed = P_fixed;
   gp.derive_i64 = derive_i64 ? 1 : 0;
   gp.ceil_log2_k = 0;
@@ -947,14 +1052,26 @@ cudaError_t launch_gemm(const void* RA, long long lda, const void* RB, long long
     gp.invq[i] = t.invq[i];
   }
   for (int i = 0; i <= kNumPrimes; ++i) gp.log2P[i] = t.log2P[i];
+  auto slice_sum = [&]() -> cudaError_t {
+    if (max_splits <= 1) return cudaSuccess;
+    PrimeQ qs;
+    for (int i = 0; i < kNumPrimes; ++i) qs.q[i] = t.q[i];
+    const long long plane_bytes = M * ldc, n16 = (long long)planes * plane_bytes / 16;
+    long long blocks = (n16 + 255) / 256;
+    if (blocks > 4LL * sms[dev]) blocks = 4LL * sms[dev];
+    return launch_dependent(slice_sum_kernel, dim3((unsigned)(blocks < 1 ? 1 : blocks)), dim3(256), 0, st,
+                            static_cast<uint8_t*>(RC), (long long)planes * plane_bytes, plane_bytes, batch, qs,
+                            (const DevPlan*)plan);
+  };
   if (!pair) {
-    const long long tiles = (long long)planes * gp.mt * gp.nt;
+    const long long tiles = (long long)planes * gp.mt * gp.nt * max_splits;
     int grid = (int)(tiles < sms[dev] ? tiles : sms[dev]);
     if (grid < 1) grid = 1;
-    return b_kmajor ? launch_dependent(residue_gemm_kernel<true>, dim3(grid), dim3(NUM_THREADS), SMEM_BYTES, st, ma,
-                                       mb, mc, gp, plan)
-                    : launch_dependent(residue_gemm_kernel<false>, dim3(grid), dim3(NUM_THREADS), SMEM_BYTES, st, ma,
-                                       mb, mc, gp, plan);
+    e = b_kmajor ? launch_dependent(residue_gemm_kernel<true>, dim3(grid), dim3(NUM_THREADS), SMEM_BYTES, st, ma, mb,
+                                    mc, gp, plan)
+                 : launch_dependent(residue_gemm_kernel<false>, dim3(grid), dim3(NUM_THREADS), SMEM_BYTES, st, ma, mb,
+                                    mc, gp, plan);
+    return e != cudaSuccess ? e : slice_sum();
   }
   cudaLaunchConfig_t cfg = {};
   cfg.blockDim = dim3(NUM_THREADS);
@@ -979,13 +1096,25 @@ cudaError_t launch_gemm(const void* RA, long long lda, const void* RB, long long
       n = sms[dev] / 2;
     max_pairs[dev] = n;
   }
-  const long long tiles2 = (long long)planes * ((M + 255) / 256) * gp.nt;
+  const long long tiles2 = (long long)planes * ((M + 255) / 256) * gp.nt * max_splits;
   long long clusters = max_pairs[dev];
   if (tiles2 < clusters) clusters = tiles2;
   if (clusters < 1) clusters = 1;
   cfg.gridDim = dim3((unsigned)(2 * clusters));
-  return b_kmajor ? cudaLaunchKernelEx(&cfg, residue_gemm_pair_kernel<true>, ma, mb, mc, gp, plan)
-                  : cudaLaunchKernelEx(&cfg, residue_gemm_pair_kernel<false>, ma, mb, mc, gp, plan);
+  e = b_kmajor ? cudaLaunchKernelEx(&cfg, residue_gemm_pair_kernel<true>, ma, mb, mc, gp, plan)
+               : cudaLaunchKernelEx(&cfg, residue_gemm_pair_kernel<false>, ma, mb, mc, gp, plan);
+  return e != cudaSuccess ? e : slice_sum();
+}
+
+int gemm_max_splits(long long gemm_batch, long long M, long long N, long long K) {
+  const long long nkc = (K + (long long)KC_BLOCKS * BK - 1) / ((long long)KC_BLOCKS * BK);
+  // tiles with a single prime, of the larger (CTA-pair) kind; 160 bounds the
+  // persistent workers of any launch on this part
+  const long long tiles = gemm_batch * ((M + 255) / 256) * ((N + BN - 1) / BN);
+  long long want = (160 + tiles - 1) / tiles;
+  if (want > kMaxSplits) want = kMaxSplits;
+  if (want > nkc) want = nkc;
+  return (int)(want < 1 ? 1 : want);
 }
 
 }  // namespace rg

@@ -30,7 +30,8 @@ struct DevPlan {
   int lossless;           // fp64: 1 if the scaling is exact
   int nword_a, nword_b;   // 32-bit words the split reads per integer entry (0: the entry is an exact fp32)
   unsigned blocks_done;   // planner blocks finished (the last one derives the plan)
-  int pad0[5];
+  int splits;             // K slices the GEMM used (1: none)
+  int pad0[4];
   // reductions written by the planner kernels
   unsigned long long maxmag_a, maxmag_b;  // int64 operands: max |x|
   int maxbits_a, maxbits_b;               // limb operands: max bit length of |x|

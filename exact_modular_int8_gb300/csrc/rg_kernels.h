@@ -38,9 +38,17 @@ cudaError_t launch_split(int op, const void* A, const void* A2, const void* B, c
 // b_kmajor: RB is [pmax][N][ldb] (K contiguous) instead of [pmax][K][ldb].
 // batch: every prime's planes hold `batch` independent products
 // (RA [pmax][batch][M][lda], RB and RC likewise).
+// max_splits: RC has room for that many K slices ([max_splits][pmax * batch]
+// [M][ldc]); the kernel may split K across them when there are too few tiles,
+// and a second kernel then sums the slices into slice 0.
 cudaError_t launch_gemm(const void* RA, long long lda, const void* RB, long long ldb, void* RC, long long ldc,
                         int pmax, int batch, int P_fixed, long long M, long long N, long long K, DevPlan* plan,
-                        cudaStream_t st, int fault, unsigned long long wait_ns, bool derive_i64, bool b_kmajor);
+                        cudaStream_t st, int fault, unsigned long long wait_ns, bool derive_i64, bool b_kmajor,
+                        int max_splits);
+
+// K slices worth room in RC for a product of this shape (1: never split).
+constexpr int kMaxSplits = 16;
+int gemm_max_splits(long long gemm_batch, long long M, long long N, long long K);
 
 // Balanced Garner: RC [P][M][ldc] -> int64 limbs C [M][N][lc] (op I64/LIMBS),
 // or the outward pair (lo, hi) as IEEE bit patterns (ops ENCLOSE[_F32]).  For

@@ -295,6 +295,7 @@ typedef struct {
   int f_a;      /* fp64 only: A' = A * 2^f_a */
   int f_b;
   int lossless; /* fp64 only: 1 if both operands scaled exactly */
+  int splits;   /* K slices the per-prime GEMM used (1: none; more when there were too few output tiles) */
 } rg_plan_info;
 int rg_get_plan(const void* ws, void* stream, rg_plan_info* out);
 
