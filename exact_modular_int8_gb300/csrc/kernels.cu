@@ -432,18 +432,25 @@ struct alignas(16) PrimeRec {
   int pad[2];
 };
 
+// The records of every prime, built on the host and uploaded with the
+// constant tables; kept in global memory so that a block copies them to
+// shared memory with coalesced 16-byte loads (the constant bank serialises
+// loads whose addresses differ across a warp).
+struct SplitTables {
+  PrimeRec rec[kNumPrimes];
+  int ws[kNumPrimes][kMaxWords + 1];
+};
+__device__ SplitTables g_split;
+
 // Every prime's record (and, if ws is given, its word-string weights); none
 // of it depends on the predecessor kernel, so it is read before waiting.
 __device__ __forceinline__ void load_prime_recs(PrimeRec* rec, int (*ws)[kMaxWords + 1]) {
-  for (int i = threadIdx.x; i < kNumPrimes * kMaxWords; i += blockDim.x)
-    rec[i / kMaxWords].w[i % kMaxWords] = c_tab.wbyte[i / kMaxWords][i % kMaxWords];
-  for (int p = threadIdx.x; p < kNumPrimes; p += blockDim.x) {
-    rec[p].q = c_tab.qf[p];
-    rec[p].iq = c_tab.invq[p];
-  }
+  constexpr int kRecVec = (int)(sizeof(PrimeRec) * kNumPrimes / 16);
+  for (int i = threadIdx.x; i < kRecVec; i += blockDim.x)
+    reinterpret_cast<uint4*>(rec)[i] = reinterpret_cast<const uint4*>(g_split.rec)[i];
   if (ws)
     for (int i = threadIdx.x; i < kNumPrimes * (kMaxWords + 1); i += blockDim.x)
-      ws[i / (kMaxWords + 1)][i % (kMaxWords + 1)] = c_tab.wword[i / (kMaxWords + 1)][i % (kMaxWords + 1)];
+      (&ws[0][0])[i] = (&g_split.ws[0][0])[i];
 }
 
 // The first NW packed byte weights of a record (NW = 1, 2, 4 or 8).
@@ -1271,6 +1278,18 @@ cudaError_t upload_tables() {
   if (done[dev]) return cudaSuccess;
   e = cudaMemcpyToSymbol(c_tab, &host_tables(), sizeof(Tables));
   if (e == cudaSuccess) e = cudaMemcpyToSymbol(g_pow2, host_pow2().v, sizeof(Pow2Table));
+  if (e == cudaSuccess) {
+    static SplitTables st;  // built from the host tables
+    const Tables& t = host_tables();
+    for (int p = 0; p < kNumPrimes; ++p) {
+      for (int w = 0; w < kMaxWords; ++w) st.rec[p].w[w] = t.wbyte[p][w];
+      st.rec[p].q = t.qf[p];
+      st.rec[p].iq = t.invq[p];
+      st.rec[p].pad[0] = st.rec[p].pad[1] = 0;
+      for (int k = 0; k <= kMaxWords; ++k) st.ws[p][k] = t.wword[p][k];
+    }
+    e = cudaMemcpyToSymbol(g_split, &st, sizeof(SplitTables));
+  }
   if (e == cudaSuccess) done[dev] = true;
   return e;
 }
