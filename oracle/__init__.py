@@ -342,3 +342,48 @@ def interval_py(Am, Ar, Bm, Br, dtype=np.float64):
             lo[i][j] = rnd(S - R)[0]
             hi[i][j] = rnd(S + R)[1]
     return lo, hi
+
+
+# ---------------------------------------------------------------------------
+# Exact rational solve ("exact-solve" page, Correctness: an exact
+# Fraction Gaussian-elimination oracle on small systems)
+# ---------------------------------------------------------------------------
+
+
+def solve_fraction(A, b):
+    """The exact solution X of A X = b over the rationals, as a nested list
+    [n][c] of Fraction, or None when A is singular.  Gauss-Jordan elimination
+    in Fraction arithmetic, pivoting on the first nonzero entry of each column."""
+    A = [[Fraction(int(v)) for v in row] for row in np.asarray(A)]
+    B = np.asarray(b)
+    if B.ndim == 1:
+        B = B[:, None]
+    Bf = [[Fraction(int(v)) for v in row] for row in B]
+    n = len(A)
+    c = len(Bf[0]) if n else 0
+    M = [A[i] + Bf[i] for i in range(n)]
+    for k in range(n):
+        piv = next((r for r in range(k, n) if M[r][k] != 0), None)
+        if piv is None:
+            return None
+        M[k], M[piv] = M[piv], M[k]
+        inv = 1 / M[k][k]
+        M[k] = [v * inv for v in M[k]]
+        for r in range(n):
+            if r != k and M[r][k] != 0:
+                f = M[r][k]
+                M[r] = [vr - f * vk for vr, vk in zip(M[r], M[k])]
+    return [[M[i][n + j] for j in range(c)] for i in range(n)]
+
+
+def solution_as_integers(X):
+    """(N, d): integer numerators [n][c] and the least common denominator d of
+    a rational solution, the form in which the integer identity A N == d b is
+    checked."""
+    d = 1
+    for row in X:
+        for v in row:
+            d = d * v.denominator // math.gcd(d, v.denominator)
+    N = [[int(v * d) for v in row] for row in X]
+    return N, d
+
