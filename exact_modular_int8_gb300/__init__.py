@@ -19,6 +19,7 @@ from __future__ import annotations
 
 import ctypes
 import hashlib
+from fractions import Fraction
 import os
 import threading
 
@@ -36,6 +37,7 @@ RG_ERR_WORKSPACE = 5
 RG_ERR_CUDA = 6
 RG_ERR_TIMEOUT = 7
 RG_ERR_RADIUS = 8
+RG_ERR_SINGULAR = 9
 RG_FLAG_SYNC = 1
 RG_FLAG_HOST = 2
 RG_FLAG_TRANS_B = 4
@@ -50,7 +52,8 @@ EXPORTED = (
     "rg_inject_fault", "res_gemm_i64_noalloc", "rg_noalloc_scratch_bytes", "rg_set_gemm_variant",
     "res_gemm_i64_batched", "res_gemm_limbs_batched", "enclose_gemm_f64_batched", "rg_workspace_bytes_batched",
     "rg_workspace_layout_batched", "enclose_gemm_f32", "enclose_gemm_f32_batched", "interval_gemm_f64",
-    "interval_gemm_f32", "interval_gemm_f64_batched", "interval_gemm_f32_batched",
+    "interval_gemm_f32", "interval_gemm_f64_batched", "interval_gemm_f32_batched", "rg_solve_i64",
+    "rg_solution_free", "rg_rational_reconstruct",
 )
 
 
@@ -74,6 +77,11 @@ class PlanInfo(ctypes.Structure):
 
     def as_dict(self):
         return {k: getattr(self, k) for k, _ in self._fields_}
+
+
+class Solution(ctypes.Structure):
+    _fields_ = [("n", ctypes.c_int64), ("c", ctypes.c_int64), ("limbs", ctypes.c_int64),
+                ("values", ctypes.POINTER(ctypes.c_int64)), ("steps", ctypes.c_int64), ("primes", ctypes.c_int)]
 
 
 _lib = None
@@ -132,6 +140,12 @@ def library():
             lib.rg_inject_fault.restype = None
             lib.rg_set_gemm_variant.argtypes = [ci]
             lib.rg_set_gemm_variant.restype = ci
+            lib.rg_solve_i64.argtypes = [vp, vp, i64, i64, cu, vp, ctypes.POINTER(Solution)]
+            lib.rg_solve_i64.restype = ci
+            lib.rg_solution_free.argtypes = [ctypes.POINTER(Solution)]
+            lib.rg_solution_free.restype = None
+            lib.rg_rational_reconstruct.argtypes = [vp, ci, vp, ci, ci, ci, vp, vp, ci]
+            lib.rg_rational_reconstruct.restype = ci
             _lib = lib
     return _lib
 
@@ -477,3 +491,74 @@ def res_gemm_i64_noalloc(A: torch.Tensor, B: torch.Tensor, nprimes: int = 0, syn
                RG_FLAG_SYNC if sync else 0, torch.cuda.current_stream(A.device).cuda_stream)
     _check(rc, "res_gemm_i64_noalloc")
     return C
+
+
+# ---------------------------------------------------------------------------
+# exact solve ("exact-solve", Usage: solve)
+# ---------------------------------------------------------------------------
+
+
+def _limbs_to_int(vals) -> int:
+    """Little-endian two's-complement int64 limbs -> Python int."""
+    v = 0
+    for i, x in enumerate(vals):
+        v |= (int(x) & 0xFFFFFFFFFFFFFFFF) << (64 * i)
+    if vals and int(vals[-1]) < 0:
+        v -= 1 << (64 * len(vals))
+    return v
+
+
+def _int_to_limbs(v: int, limbs: int):
+    u = v & ((1 << (64 * limbs)) - 1)
+    return [((u >> (64 * i)) & 0xFFFFFFFFFFFFFFFF) - ((1 << 64) if (u >> (64 * i + 63)) & 1 else 0)
+            for i in range(limbs)]
+
+
+def solve(A: torch.Tensor, b: torch.Tensor, info: dict | None = None):
+    """The exact solution X of A X = b over the rationals, as a nested list [n][c] of
+    fractions.Fraction (c = 1 for a 1-D b), or None if A is singular.  A [n, n] and b are
+    int64 (CUDA tensors, or CPU tensors staged through the device).  `info`, if given,
+    receives the lift's step and prime counts."""
+    if A.dtype != torch.int64 or b.dtype != torch.int64 or A.dim() != 2 or A.shape[0] != A.shape[1]:
+        raise ValueError("A [n, n] and b [n] or [n, c] int64 expected")
+    b2 = b.reshape(-1, 1) if b.dim() == 1 else b
+    if b2.dim() != 2 or b2.shape[0] != A.shape[0]:
+        raise ValueError("b must have n rows")
+    A, b2 = A.contiguous(), b2.contiguous()
+    dev, flags = _call_ctx(A, b2)
+    n, c = A.shape[0], b2.shape[1]
+    sol = Solution()
+    with torch.cuda.device(dev):
+        rc = library().rg_solve_i64(A.data_ptr(), b2.data_ptr(), n, c, flags,
+                                    torch.cuda.current_stream(dev).cuda_stream, ctypes.byref(sol))
+    if rc == RG_ERR_SINGULAR:
+        return None
+    _check(rc, "rg_solve_i64")
+    try:
+        L = sol.limbs
+        vals = [sol.values[i] for i in range((n * c + 1) * L)]
+    finally:
+        library().rg_solution_free(ctypes.byref(sol))
+    d = _limbs_to_int(vals[n * c * L:])
+    if info is not None:
+        info.update(steps=int(sol.steps), primes=int(sol.primes), denominator=d)
+    return [[Fraction(_limbs_to_int(vals[(i * c + j) * L:(i * c + j + 1) * L]), d) for j in range(c)]
+            for i in range(n)]
+
+
+def rational_reconstruct(x: int, m: int, nbits: int, dbits: int):
+    """(N, D) with D x == N (mod m), |N| <= 2^nbits, 0 < D <= 2^dbits, in lowest terms,
+    by the library's host reconstruction; None if there is none."""
+    xl = max(1, (x.bit_length() + 63) // 64)
+    ml = max(1, (m.bit_length() + 63) // 64)
+    limbs = max(nbits, dbits) // 64 + 2
+    X = (ctypes.c_int64 * xl)(*_int_to_limbs(x, xl))
+    Mv = (ctypes.c_int64 * ml)(*_int_to_limbs(m, ml))
+    num = (ctypes.c_int64 * limbs)()
+    den = (ctypes.c_int64 * limbs)()
+    rc = library().rg_rational_reconstruct(X, xl, Mv, ml, nbits, dbits, num, den, limbs)
+    if rc == RG_ERR_RANGE:
+        return None
+    _check(rc, "rg_rational_reconstruct")
+    return _limbs_to_int(list(num)), _limbs_to_int(list(den))
+

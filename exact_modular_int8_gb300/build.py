@@ -1,6 +1,6 @@
 """Build libresgemm.so (the C-ABI library) in-tree with nvcc for sm_103a.
 
-Every translation unit under csrc/ is compiled in parallel and linked into
+Every translation unit under csrc/ (.cu, and host-only .cpp) is compiled in parallel and linked into
 ``_build/libresgemm.so`` next to this file.  A unit is rebuilt when it, a
 header it includes, or this script is newer than its object file.
 """
@@ -38,7 +38,7 @@ def _stale(target, deps):
 def build(verbose: bool = False, ptxas_info: bool = False) -> str:
     """Compile and link; return the library path."""
     os.makedirs(BUILD, exist_ok=True)
-    sources = sorted(glob.glob(os.path.join(CSRC, "*.cu")))
+    sources = sorted(glob.glob(os.path.join(CSRC, "*.cu")) + glob.glob(os.path.join(CSRC, "*.cpp")))
     headers = _headers()
     extra = ["-Xptxas", "-v"] if ptxas_info else []
 

@@ -390,6 +390,7 @@ const char* rg_strerror(int code) {
     case RG_ERR_CUDA: return "CUDA error";
     case RG_ERR_TIMEOUT: return "a bounded wait inside a kernel expired";
     case RG_ERR_RADIUS: return "an interval radius entry is negative";
+    case RG_ERR_SINGULAR: return "the matrix is singular modulo every prime below 256";
     default: return "unknown status";
   }
 }

@@ -1,0 +1,285 @@
+// bigint.cpp -- host multi-precision arithmetic for the exact solve's
+// rational reconstruction: schoolbook products, long division (Knuth's
+// algorithm D on 64-bit limbs), Euclid's gcd and the extended-Euclid
+// rational reconstruction.
+#include "bigint.h"
+
+#include <algorithm>
+
+namespace rg {
+namespace big {
+
+using u128 = unsigned __int128;
+
+void trim(Nat& a) {
+  while (!a.v.empty() && a.v.back() == 0) a.v.pop_back();
+}
+
+bool is_zero(const Nat& a) { return a.v.empty(); }
+
+int cmp(const Nat& a, const Nat& b) {
+  if (a.v.size() != b.v.size()) return a.v.size() < b.v.size() ? -1 : 1;
+  for (size_t i = a.v.size(); i-- > 0;)
+    if (a.v[i] != b.v[i]) return a.v[i] < b.v[i] ? -1 : 1;
+  return 0;
+}
+
+size_t bit_length(const Nat& a) {
+  if (a.v.empty()) return 0;
+  return 64 * (a.v.size() - 1) + (64 - __builtin_clzll(a.v.back()));
+}
+
+Nat from_u64(uint64_t x) {
+  Nat r;
+  if (x) r.v.push_back(x);
+  return r;
+}
+
+Nat pow2(size_t e) {
+  Nat r;
+  r.v.assign(e / 64 + 1, 0);
+  r.v[e / 64] = 1ull << (e % 64);
+  return r;
+}
+
+Nat add(const Nat& a, const Nat& b) {
+  const Nat& x = a.v.size() >= b.v.size() ? a : b;
+  const Nat& y = a.v.size() >= b.v.size() ? b : a;
+  Nat r;
+  r.v.resize(x.v.size() + 1);
+  Limb carry = 0;
+  for (size_t i = 0; i < x.v.size(); ++i) {
+    const u128 t = (u128)x.v[i] + (i < y.v.size() ? y.v[i] : 0) + carry;
+    r.v[i] = (Limb)t;
+    carry = (Limb)(t >> 64);
+  }
+  r.v[x.v.size()] = carry;
+  trim(r);
+  return r;
+}
+
+Nat sub(const Nat& a, const Nat& b) {
+  Nat r;
+  r.v.resize(a.v.size());
+  Limb borrow = 0;
+  for (size_t i = 0; i < a.v.size(); ++i) {
+    const Limb y = i < b.v.size() ? b.v[i] : 0;
+    const Limb t = a.v[i] - y - borrow;
+    borrow = (a.v[i] < y || (a.v[i] == y && borrow)) ? 1 : 0;
+    r.v[i] = t;
+  }
+  trim(r);
+  return r;
+}
+
+Nat mul(const Nat& a, const Nat& b) {
+  Nat r;
+  if (a.v.empty() || b.v.empty()) return r;
+  r.v.assign(a.v.size() + b.v.size(), 0);
+  for (size_t i = 0; i < a.v.size(); ++i) {
+    Limb carry = 0;
+    const Limb ai = a.v[i];
+    for (size_t j = 0; j < b.v.size(); ++j) {
+      const u128 t = (u128)ai * b.v[j] + r.v[i + j] + carry;
+      r.v[i + j] = (Limb)t;
+      carry = (Limb)(t >> 64);
+    }
+    r.v[i + b.v.size()] = carry;
+  }
+  trim(r);
+  return r;
+}
+
+void divmod(const Nat& a, const Nat& b, Nat* q, Nat* r) {
+  if (cmp(a, b) < 0) {
+    if (q) q->v.clear();
+    if (r) *r = a;
+    return;
+  }
+  const size_t n = b.v.size(), m = a.v.size() - n;
+  if (n == 1) {  // one-limb divisor
+    Nat qq;
+    qq.v.assign(a.v.size(), 0);
+    u128 rem = 0;
+    for (size_t i = a.v.size(); i-- > 0;) {
+      const u128 cur = (rem << 64) | a.v[i];
+      qq.v[i] = (Limb)(cur / b.v[0]);
+      rem = cur % b.v[0];
+    }
+    trim(qq);
+    if (q) *q = qq;
+    if (r) *r = from_u64((uint64_t)rem);
+    return;
+  }
+  // Knuth, The Art of Computer Programming vol. 2, 4.3.1, algorithm D.
+  const int s = __builtin_clzll(b.v[n - 1]);
+  std::vector<Limb> vn(n), un(a.v.size() + 1);
+  for (size_t i = n; i-- > 1;) vn[i] = (b.v[i] << s) | (s ? b.v[i - 1] >> (64 - s) : 0);
+  vn[0] = b.v[0] << s;
+  un[a.v.size()] = s ? a.v[a.v.size() - 1] >> (64 - s) : 0;
+  for (size_t i = a.v.size(); i-- > 1;) un[i] = (a.v[i] << s) | (s ? a.v[i - 1] >> (64 - s) : 0);
+  un[0] = a.v[0] << s;
+  Nat qq;
+  qq.v.assign(m + 1, 0);
+  for (size_t j = m + 1; j-- > 0;) {
+    const u128 num = ((u128)un[j + n] << 64) | un[j + n - 1];
+    u128 qhat = num / vn[n - 1], rhat = num % vn[n - 1];
+    while (qhat >> 64 || qhat * vn[n - 2] > ((rhat << 64) | un[j + n - 2])) {
+      --qhat;
+      rhat += vn[n - 1];
+      if (rhat >> 64) break;
+    }
+    // un[j .. j+n] -= qhat * vn
+    Limb borrow = 0, carry = 0;
+    for (size_t i = 0; i < n; ++i) {
+      const u128 p = qhat * vn[i] + carry;
+      carry = (Limb)(p >> 64);
+      const Limb lo = (Limb)p;
+      const Limb t = un[i + j] - lo - borrow;
+      borrow = (un[i + j] < lo || (un[i + j] == lo && borrow)) ? 1 : 0;
+      un[i + j] = t;
+    }
+    const Limb top = un[j + n];
+    const Limb t = top - carry - borrow;
+    const bool negative = top < carry || (top == carry && borrow);
+    un[j + n] = t;
+    if (negative) {  // qhat was one too large: add vn back
+      --qhat;
+      Limb c = 0;
+      for (size_t i = 0; i < n; ++i) {
+        const u128 sum = (u128)un[i + j] + vn[i] + c;
+        un[i + j] = (Limb)sum;
+        c = (Limb)(sum >> 64);
+      }
+      un[j + n] += c;
+    }
+    qq.v[j] = (Limb)qhat;
+  }
+  trim(qq);
+  if (q) *q = qq;
+  if (r) {
+    Nat rr;
+    rr.v.resize(n);
+    for (size_t i = 0; i < n; ++i) rr.v[i] = (un[i] >> s) | (s ? un[i + 1] << (64 - s) : 0);
+    trim(rr);
+    *r = rr;
+  }
+}
+
+Nat mod(const Nat& a, const Nat& b) {
+  Nat r;
+  divmod(a, b, nullptr, &r);
+  return r;
+}
+
+Nat gcd(Nat a, Nat b) {
+  while (!is_zero(b)) {
+    Nat r = mod(a, b);
+    a = std::move(b);
+    b = std::move(r);
+  }
+  return a;
+}
+
+Int add(const Int& a, const Int& b) {
+  Int r;
+  if (a.neg == b.neg) {
+    r.mag = add(a.mag, b.mag);
+    r.neg = a.neg && !is_zero(r.mag);
+    return r;
+  }
+  const int c = cmp(a.mag, b.mag);
+  if (c == 0) return r;
+  if (c > 0) {
+    r.mag = sub(a.mag, b.mag);
+    r.neg = a.neg;
+  } else {
+    r.mag = sub(b.mag, a.mag);
+    r.neg = b.neg;
+  }
+  return r;
+}
+
+Int sub(const Int& a, const Int& b) {
+  Int nb = b;
+  nb.neg = !b.neg && !is_zero(b.mag);
+  return add(a, nb);
+}
+
+Int mul(const Int& a, const Nat& b) {
+  Int r;
+  r.mag = mul(a.mag, b);
+  r.neg = a.neg && !is_zero(r.mag);
+  return r;
+}
+
+Int from_words(const uint32_t* w, int nw) {
+  Int r;
+  const bool neg = nw > 0 && (w[nw - 1] >> 31) != 0;
+  // magnitude = two's complement negation when negative
+  std::vector<uint32_t> m(w, w + nw);
+  if (neg) {
+    uint64_t carry = 1;
+    for (int i = 0; i < nw; ++i) {
+      const uint64_t t = (uint64_t)(uint32_t)~m[i] + carry;
+      m[i] = (uint32_t)t;
+      carry = t >> 32;
+    }
+  }
+  r.mag.v.assign((nw + 1) / 2, 0);
+  for (int i = 0; i < nw; ++i) r.mag.v[i / 2] |= (Limb)m[i] << (32 * (i % 2));
+  trim(r.mag);
+  r.neg = neg && !is_zero(r.mag);
+  return r;
+}
+
+bool to_limbs(const Int& a, int64_t* out, int limbs) {
+  // the magnitude must leave the sign bit free: |a| < 2^(64 limbs - 1), or
+  // a == -2^(64 limbs - 1)
+  const size_t bl = bit_length(a.mag);
+  if (bl > (size_t)64 * limbs) return false;
+  std::vector<Limb> v(limbs, 0);
+  for (size_t i = 0; i < a.mag.v.size(); ++i) v[i] = a.mag.v[i];
+  if (!a.neg) {
+    if (bl == (size_t)64 * limbs) return false;
+  } else {
+    Limb carry = 1;
+    for (int i = 0; i < limbs; ++i) {
+      const u128 t = (u128)(Limb)~v[i] + carry;
+      v[i] = (Limb)t;
+      carry = (Limb)(t >> 64);
+    }
+    if (!((v[limbs - 1] >> 63) & 1)) return false;
+  }
+  for (int i = 0; i < limbs; ++i) out[i] = (int64_t)v[i];
+  return true;
+}
+
+bool rational_reconstruct(const Nat& X, const Nat& M, const Nat& nbound, const Nat& dbound, Int* N, Nat* D) {
+  // Extended Euclid on (M, X) with the cofactor of X, stopped at the first
+  // remainder <= nbound (Wang's reconstruction).
+  Nat r0 = M, r1 = X;
+  Int t0, t1;
+  t1.mag = from_u64(1);
+  while (cmp(r1, nbound) > 0) {
+    Nat q, r;
+    divmod(r0, r1, &q, &r);
+    Int t = sub(t0, mul(t1, q));
+    r0 = std::move(r1);
+    r1 = std::move(r);
+    t0 = std::move(t1);
+    t1 = std::move(t);
+  }
+  if (is_zero(t1.mag) || cmp(t1.mag, dbound) > 0) return false;
+  Int n;
+  n.mag = r1;
+  n.neg = t1.neg && !is_zero(r1);  // N / D with D = |t1|
+  const Nat g = gcd(r1, t1.mag);
+  if (cmp(g, from_u64(1)) != 0) return false;
+  *N = n;
+  *D = t1.mag;
+  return true;
+}
+
+}  // namespace big
+}  // namespace rg

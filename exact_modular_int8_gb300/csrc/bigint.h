@@ -1,0 +1,52 @@
+// bigint.h -- host multi-precision integers for the exact solve's rational
+// reconstruction (internal).  Little-endian 64-bit limbs; naturals carry no
+// leading zero limb (zero is the empty vector).
+#pragma once
+#include <cstdint>
+#include <vector>
+
+namespace rg {
+namespace big {
+
+using Limb = uint64_t;
+
+struct Nat {
+  std::vector<Limb> v;
+};
+
+struct Int {  // sign and magnitude; zero is never negative
+  bool neg = false;
+  Nat mag;
+};
+
+void trim(Nat& a);
+bool is_zero(const Nat& a);
+int cmp(const Nat& a, const Nat& b);
+size_t bit_length(const Nat& a);
+Nat from_u64(uint64_t x);
+Nat pow2(size_t e);
+
+Nat add(const Nat& a, const Nat& b);
+Nat sub(const Nat& a, const Nat& b);  // requires a >= b
+Nat mul(const Nat& a, const Nat& b);
+// q = a / b, r = a % b (b != 0).
+void divmod(const Nat& a, const Nat& b, Nat* q, Nat* r);
+Nat mod(const Nat& a, const Nat& b);
+Nat gcd(Nat a, Nat b);
+
+Int add(const Int& a, const Int& b);
+Int sub(const Int& a, const Int& b);
+Int mul(const Int& a, const Nat& b);
+
+// Two's-complement words (little-endian 32-bit) -> Int.
+Int from_words(const uint32_t* w, int nw);
+// Int -> `limbs` little-endian two's-complement int64 limbs; false if it does not fit.
+bool to_limbs(const Int& a, int64_t* out, int limbs);
+
+// Rational reconstruction: the N, D with D X == N (mod M), |N| <= nbound,
+// 0 < D <= dbound, for 0 <= X < M and 2 nbound dbound < M (then unique, in
+// lowest terms).  False if there is none.
+bool rational_reconstruct(const Nat& X, const Nat& M, const Nat& nbound, const Nat& dbound, Int* N, Nat* D);
+
+}  // namespace big
+}  // namespace rg

@@ -11,11 +11,17 @@
 #include <mutex>
 
 #include "rg_common.cuh"
+#include "rg_garner.cuh"
 #include "rg_kernels.h"
 
 namespace rg {
 
 __constant__ Tables c_tab;
+
+// Garner reads the library's own prime tables.
+struct MainTab {
+  __device__ static __forceinline__ const Tables& t() { return c_tab; }
+};
 
 namespace {
 
@@ -409,14 +415,6 @@ struct SplitSide {
   int L;           // limbs per entry (integer kinds)
   long long items; // R * ldy / VEC
 };
-
-constexpr float kMagic = 12582912.0f;   // 1.5 * 2^23
-constexpr int kMagicBits = 0x4B400000;  // its bit pattern
-
-// Exact int -> float for |v| < 2^22 (and back) without the conversion unit:
-// the integer sits in the low mantissa bits of kMagic + v.
-__device__ __forceinline__ float int_to_float_exact(int v) { return __int_as_float(kMagicBits + v) - kMagic; }
-__device__ __forceinline__ int float_bits_offset(float v) { return __float_as_int(v + kMagic); }  // = kMagicBits + v
 
 // c + the four bytes of a (unsigned) dotted with the four bytes of b (signed).
 __device__ __forceinline__ int dp4a_us(uint32_t a, int b, int c) {
@@ -868,132 +866,10 @@ __global__ void __launch_bounds__(256) split_interval_kernel(IvSide sa, IvSide s
 }
 
 // ---------------------------------------------------------------------------
-// Balanced Garner ("exact-solve" and "enclosure-gemm", Method: balanced-Garner
-// mixed-radix digits).  With Q_i = q_0 ... q_{i-1} the digits
-//   v_i = bal( (r_i - sum_{j<i} v_j Q_j) Q_i^-1  mod q_i ),  |v_i| <= (q_i-1)/2,
-// give x = sum_i v_i Q_i, the unique representative with |x| <= (P-1)/2.
-// Each digit costs one int8x4 dot product per four earlier digits and one
-// reciprocal reduction, and is added into x at once: after digit i,
-// |x| < Q_{i+1} / 2 < 2^(8(i+1) - 1), so only the low i/4 + 2 words of x can
-// differ from its sign extension and only those are updated.  Residues are
-// fetched eight primes at a time, so the loads of a batch are in flight
-// together; the loop stops at the plan's prime count.
+// Garner kernels ("exact-solve" and "enclosure-gemm", Method: balanced-Garner
+// mixed-radix digits); the reconstruction itself is garner_reconstruct in
+// rg_garner.cuh.
 // ---------------------------------------------------------------------------
-
-// Output elements per thread: four (one 32-bit residue load per prime) for
-// narrow results, two for wide ones to bound register use.
-template <int W>
-struct GarnerGE {
-  static constexpr int value = W <= 4 ? 4 : 2;
-};
-
-constexpr int kGarnerBatch = 8;
-
-// x (W 32-bit words, two's complement, mod 2^(32W)) += D * Q_i, for the words
-// that can be significant once digits up to `last` are in (|x| < 2^(8(last+1)-1)).
-template <int W>
-__device__ __forceinline__ void add_scaled_weight(uint32_t (&x)[W], int D, int i, int last) {
-  if constexpr (W == 2) {
-    const unsigned long long Qi = ((unsigned long long)c_tab.Qw[i][1] << 32) | c_tab.Qw[i][0];
-    const unsigned long long x64 = (((unsigned long long)x[1] << 32) | x[0]) + (unsigned long long)(long long)D * Qi;
-    x[0] = (uint32_t)x64;
-    x[1] = (uint32_t)(x64 >> 32);
-  } else {
-    long long carry = 0;
-#pragma unroll
-    for (int k = 0; k < W; ++k) {
-      if (k < last / 4 + 2) {
-        const long long qk = k < kQWords ? (long long)c_tab.Qw[i][k < kQWords ? k : 0] : 0ll;
-        const long long t = (long long)x[k] + qk * D + carry;
-        x[k] = (uint32_t)t;
-        carry = t >> 32;
-      }
-    }
-  }
-}
-
-// x[e] (W 32-bit words, two's complement) = the reconstructed integers of the
-// GE residue vectors starting at rc (plane = distance between primes).
-// Digits are combined in pairs, D = v_i + q_i v_{i+1} (|D| < 2^15, exact in
-// fp32), so the wide accumulation runs once per two primes.
-template <int W, int GE>
-__device__ __forceinline__ void garner_reconstruct(const uint8_t* __restrict__ rc, long long plane, int P,
-                                                   uint32_t (&x)[GE][W]) {
-  uint32_t V[GE][kGarnerWords];
-  float pend[GE];  // the even digit of the current pair, as float
-#pragma unroll
-  for (int e = 0; e < GE; ++e) {
-#pragma unroll
-    for (int w = 0; w < kGarnerWords; ++w) V[e][w] = 0u;
-#pragma unroll
-    for (int k = 0; k < W; ++k) x[e][k] = 0u;
-    pend[e] = 0.0f;
-  }
-#pragma unroll
-  for (int i0 = 0; i0 < kNumPrimes; i0 += kGarnerBatch) {
-    if (i0 >= P) break;
-    uint32_t rw[kGarnerBatch];
-#pragma unroll
-    for (int j = 0; j < kGarnerBatch; ++j) {
-      const int i = i0 + j;
-      static_assert(GE == 1 || GE == 2 || GE == 4, "one, two or four adjacent entries");
-      if constexpr (GE == 4)
-        rw[j] = (i < P) ? __ldg(reinterpret_cast<const uint32_t*>(rc + (long long)i * plane)) : 0u;
-      else if constexpr (GE == 2)
-        rw[j] = (i < P) ? (uint32_t)__ldg(reinterpret_cast<const unsigned short*>(rc + (long long)i * plane)) : 0u;
-      else
-        rw[j] = (i < P) ? (uint32_t)__ldg(rc + (long long)i * plane) : 0u;
-    }
-#pragma unroll
-    for (int j = 0; j < kGarnerBatch; ++j) {
-      const int i = i0 + j;
-      if (i >= kNumPrimes || i >= P) break;
-      const float q = c_tab.qf[i], iq = c_tab.invq[i];
-      const int gi = c_tab.ginv[i];
-      // byte selector that inserts a new low byte at position i % 4
-      constexpr unsigned kSel[4] = {0x3214u, 0x3240u, 0x3410u, 0x4210u};
-#pragma unroll
-      for (int e = 0; e < GE; ++e) {
-        // s = Q_i^-1 r_i - sum_{j<i} (Q_j Q_i^-1 mod q_i) v_j, |s| < 2^20
-        int acc = gi * (int)((rw[j] >> (8 * e)) & 0xFFu);
-#pragma unroll
-        for (int w = 0; w < kGarnerWords; ++w)
-          if (4 * w < i) acc = __dp4a((int)V[e][w], c_tab.gd_packed[i][w], acc);
-        const float vf = bal_mod_small(int_to_float_exact(acc), q, iq);
-        const int vb = float_bits_offset(vf);
-        V[e][i / 4] = __byte_perm(V[e][i / 4], (uint32_t)vb, kSel[i % 4]);
-        if ((i & 1) == 0) {
-          pend[e] = vf;
-          if (i + 1 >= P) {  // unpaired last digit
-            if (W > 2 && (i % 4) == 0 && i > 0 && i / 4 + 1 < W)
-              x[e][i / 4 + 1] = (uint32_t)((int)x[e][i / 4] >> 31);
-            add_scaled_weight<W>(x[e], vb - kMagicBits, i, i);
-          }
-        } else {
-          const float D = __fmaf_rn(vf, c_tab.qf[i - 1], pend[e]);  // v_{i-1} + q_{i-1} v_i
-          if (W > 2 && ((i - 1) % 4) == 0 && i > 1 && (i - 1) / 4 + 1 < W)
-            x[e][(i - 1) / 4 + 1] = (uint32_t)((int)x[e][(i - 1) / 4] >> 31);
-          add_scaled_weight<W>(x[e], float_bits_offset(D) - kMagicBits, i - 1, i);
-        }
-      }
-    }
-  }
-  if constexpr (W == 2) return;  // the 64-bit form is complete
-  // sign-extend from the last significant word (branch-free, so x stays in
-  // registers: every index is a compile-time constant)
-  const int top = (P - 1) / 4 + 2;
-#pragma unroll
-  for (int e = 0; e < GE; ++e) {
-    uint32_t sign = 0u;
-#pragma unroll
-    for (int k = 0; k < W; ++k) {
-      const uint32_t at_top = 0u - (uint32_t)(k == top - 1);
-      const uint32_t above = 0u - (uint32_t)(k >= top);
-      sign = (sign & ~at_top) | ((uint32_t)((int)x[e][k] >> 31) & at_top);
-      x[e][k] = (x[e][k] & ~above) | (sign & above);
-    }
-  }
-}
 
 template <int LC>
 __global__ void __launch_bounds__(128) garner_int_kernel(const uint8_t* __restrict__ RC, long long ldc,
@@ -1009,7 +885,7 @@ __global__ void __launch_bounds__(128) garner_int_kernel(const uint8_t* __restri
   const long long m = item / per_row;
   const long long n0 = (item - m * per_row) * GE;
   uint32_t x[GE][W];
-  garner_reconstruct<W, GE>(RC + m * ldc + n0, plane, P, x);
+  garner_reconstruct<W, GE, MainTab>(RC + m * ldc + n0, plane, P, x);
   int64_t* out = C + (m * N + n0) * LC;
   if (n0 + GE <= N && ((reinterpret_cast<uintptr_t>(out) & 15u) == 0)) {
     // GE * LC consecutive int64: 16-byte stores
@@ -1138,7 +1014,7 @@ __global__ void __launch_bounds__(128) garner_enclose_kernel(const uint8_t* __re
   const long long m = item / per_row;
   const long long n0 = (item - m * per_row) * GE;
   uint32_t x[GE][kEncW];
-  garner_reconstruct<kEncW, GE>(RC + m * ldc + n0, plane, P, x);
+  garner_reconstruct<kEncW, GE, MainTab>(RC + m * ldc + n0, plane, P, x);
   Bits l[GE], h[GE];
   if (plan->lossless) {
 #pragma unroll
@@ -1222,13 +1098,13 @@ __global__ void __launch_bounds__(128) garner_interval_kernel(const uint8_t* __r
   const long long m = item / N, n = item - m * N;
   const uint8_t* base = RC + m * ldc + n;
   uint32_t x[GE][kEncW], xl[kEncW], xh[kEncW];
-  garner_reconstruct<kEncW, GE>(base, plane, P, x);
+  garner_reconstruct<kEncW, GE, MainTab>(base, plane, P, x);
 #pragma unroll
   for (int k = 0; k < kEncW; ++k) xl[k] = xh[k] = x[0][k];
-  garner_reconstruct<kEncW, GE>(base + sub, plane, P, x);
+  garner_reconstruct<kEncW, GE, MainTab>(base + sub, plane, P, x);
   add_words(xl, x[0], -1);
   add_words(xh, x[0], 1);
-  garner_reconstruct<kEncW, GE>(base + 2 * sub, plane, P, x);
+  garner_reconstruct<kEncW, GE, MainTab>(base + 2 * sub, plane, P, x);
   add_words(xl, x[0], -1);
   add_words(xh, x[0], 1);
   if (!plan->lossless) {

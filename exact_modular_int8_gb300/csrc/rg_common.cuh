@@ -68,6 +68,9 @@ struct Tables {
 
 // Host side: the tables (built once) and the primes.
 const Tables& host_tables();
+// The same tables for another sequence of distinct odd primes below 256
+// (count <= 53), e.g. the subset a solve can use.
+void build_tables_for(const int* qs, int count, Tables* out);
 
 // 2^s mod q (balanced) for every prime and s < 256, kept in global memory
 // (too large for the constant bank beside Tables).
@@ -105,6 +108,14 @@ __device__ __forceinline__ float bal_mod_small(float s, float q, float invq) {
 }
 
 __device__ __forceinline__ void set_status(int* status, int code) { atomicCAS(status, 0, code); }
+
+constexpr float kMagic = 12582912.0f;   // 1.5 * 2^23
+constexpr int kMagicBits = 0x4B400000;  // its bit pattern
+
+// Exact int -> float for |v| < 2^22 (and back) without the conversion unit:
+// the integer sits in the low mantissa bits of kMagic + v.
+__device__ __forceinline__ float int_to_float_exact(int v) { return __int_as_float(kMagicBits + v) - kMagic; }
+__device__ __forceinline__ int float_bits_offset(float v) { return __float_as_int(v + kMagic); }  // = kMagicBits + v
 
 // Programmatic dependent launch: a kernel launched with programmatic stream
 // serialisation may start while its predecessor finishes; it must wait here

@@ -1,0 +1,665 @@
+// solve.cu -- exact rational solution of an integer system A X = B on the
+// residue engine ("exact-solve" page, Method):
+//   1. A^-1 mod q for every prime q < 256 at once, by Gauss-Jordan
+//      elimination over all primes (one launch per elimination step);
+//   2. Dixon's p-adic lift with the modulus P = the product of the primes that
+//      do not divide det(A): X_i = A^-1 R_i mod P (per prime, then balanced
+//      Garner into the wide base-P digit), R_{i+1} = (R_i - A X_i) / P formed
+//      in one 64-bit limb as (R_i - A X_i) P^-1 mod 2^64 (P odd);
+//   3. on the host, rational reconstruction of one component for the common
+//      denominator, then one modular product per numerator.
+#include <cuda_runtime.h>
+
+#include <algorithm>
+#include <cmath>
+#include <cstring>
+#include <thread>
+#include <vector>
+
+#include "bigint.h"
+#include "rg_garner.cuh"
+#include "rg_kernels.h"
+
+namespace rg {
+namespace {
+
+// Tables of the prime sequence a solve lifts with (a subset of the residue
+// base), uploaded once the inverse shows which primes divide det(A).
+__constant__ Tables c_sol;
+__constant__ Tables c_all;  // the full base, for the inverse
+
+struct SolTab {
+  __device__ static __forceinline__ const Tables& t() { return c_sol; }
+};
+
+constexpr int kMaxSolveN = 8192;
+constexpr int kW = 11;  // 32-bit words of a base-P digit (|x| < P / 2 < 2^333)
+
+// ---------------------------------------------------------------------------
+// Norms and range: row and column sums of squares of A, column sums of
+// squares of B (fp64, for the Hadamard bounds) and max |A|.
+// ---------------------------------------------------------------------------
+__global__ void __launch_bounds__(256) norms_kernel(const int64_t* __restrict__ A, const int64_t* __restrict__ B,
+                                                    int n, int c, double* rows, double* cols, double* bcols,
+                                                    unsigned long long* maxabs) {
+  const int warp = (blockIdx.x * blockDim.x + threadIdx.x) >> 5, lane = threadIdx.x & 31;
+  // one warp per row of A
+  if (warp < n) {
+    double s = 0.0;
+    unsigned long long m = 0;
+    for (int k = lane; k < n; k += 32) {
+      const long long v = A[(long long)warp * n + k];
+      const double d = (double)v;
+      s = fma(d, d, s);
+      const unsigned long long a = v < 0 ? 0ull - (unsigned long long)v : (unsigned long long)v;
+      m = a > m ? a : m;
+    }
+    for (int o = 16; o; o >>= 1) {
+      s += __shfl_xor_sync(0xffffffffu, s, o);
+      const unsigned long long t = __shfl_xor_sync(0xffffffffu, m, o);
+      m = t > m ? t : m;
+    }
+    if (lane == 0) {
+      rows[warp] = s;
+      atomicMax(maxabs, m);
+    }
+  }
+  // one thread per column of A, then of B
+  const int t = blockIdx.x * blockDim.x + threadIdx.x;
+  if (t < n) {
+    double s = 0.0;
+    for (int i = 0; i < n; ++i) {
+      const double d = (double)A[(long long)i * n + t];
+      s = fma(d, d, s);
+    }
+    cols[t] = s;
+  } else if (t < n + c) {
+    double s = 0.0;
+    for (int i = 0; i < n; ++i) {
+      const double d = (double)B[(long long)i * c + (t - n)];
+      s = fma(d, d, s);
+    }
+    bcols[t - n] = s;
+  }
+}
+
+// ---------------------------------------------------------------------------
+// Batched modular inverse ("exact-solve", Method: A^-1 mod q for every prime
+// by Gauss-Jordan, one grid per elimination step spanning all primes).
+// M[p] is A mod q_p in [0, q), n x n bytes, inverted in place: at step k the
+// pivot row is the first row >= k with a nonzero in column k; it is swapped
+// up, scaled by the pivot's inverse (its own column entry becoming that
+// inverse), and every other row i subtracts f_i times it, f_i its old column
+// entry (the column entry itself becoming -f_i times the inverse).  The row
+// swaps become column swaps of the result, undone at the end.  A prime with
+// no pivot at some step divides det(A) and is marked singular.
+// ---------------------------------------------------------------------------
+
+// x mod q in [0, q) for an int64 x, by the split's byte weights (wbyte,
+// wword of the full base, prime index p).
+__device__ __forceinline__ int residue_i64(long long x, int p) {
+  const unsigned long long u = (unsigned long long)x;
+  int acc = x < 0 ? -c_all.wword[p][2] : 0;
+  asm("dp4a.u32.s32 %0, %1, %2, %0;" : "+r"(acc) : "r"((uint32_t)u), "r"(c_all.wbyte[p][0]));
+  asm("dp4a.u32.s32 %0, %1, %2, %0;" : "+r"(acc) : "r"((uint32_t)(u >> 32)), "r"(c_all.wbyte[p][1]));
+  const float q = c_all.qf[p];
+  float r = bal_mod_small(int_to_float_exact(acc), q, c_all.invq[p]);  // |acc| < 2^20
+  return (int)(r < 0.0f ? r + q : r);
+}
+
+// M[p] = diag(A, I) mod q_p, of order nE = n rounded up to 16 (the padding
+// keeps every row a whole number of 16-byte vectors; the inverse of diag(A, I)
+// is diag(A^-1, I), and the same primes divide both determinants).
+__global__ void __launch_bounds__(256) gj_init_kernel(const int64_t* __restrict__ A, int n, int nE,
+                                                      uint8_t* __restrict__ M) {
+  const long long nn = (long long)nE * nE;
+  for (long long e = (long long)blockIdx.x * blockDim.x + threadIdx.x; e < nn; e += (long long)gridDim.x * blockDim.x) {
+    const int i = (int)(e / nE), j = (int)(e - (long long)i * nE);
+    const long long x = (i < n && j < n) ? A[(long long)i * n + j] : (i == j ? 1 : 0);
+    for (int p = 0; p < kNumPrimes; ++p) M[p * nn + e] = (uint8_t)residue_i64(x, p);
+  }
+}
+
+// (a * b) mod q for a, b in [0, q), q < 256.
+__device__ __forceinline__ int mulmod(int a, int b, float q, float iq) {
+  float r = bal_mod_small((float)(a * b), q, iq);
+  return (int)(r < 0.0f ? r + q : r);
+}
+
+__device__ __forceinline__ int invmod(int a, int q) {  // a^(q-2) mod q, a != 0
+  int r = 1, b = a, e = q - 2;
+  while (e) {
+    if (e & 1) r = r * b % q;
+    b = b * b % q;
+    e >>= 1;
+  }
+  return r;
+}
+
+// One block per prime: pivot search, row swap, saved column, scaled pivot row.
+__global__ void __launch_bounds__(256) gj_pivot_kernel(uint8_t* __restrict__ M, uint8_t* __restrict__ F, int n, int k,
+                                                       int* __restrict__ perm, int* __restrict__ sing,
+                                                       int* __restrict__ pinv) {
+  wait_for_predecessor();
+  const int p = blockIdx.x;
+  if (sing[p]) return;
+  const long long nn = (long long)n * n;
+  uint8_t* Mp = M + p * nn;
+  __shared__ int s_piv;
+  if (threadIdx.x == 0) s_piv = n;
+  __syncthreads();
+  int mine = n;
+  for (int r = k + threadIdx.x; r < n; r += blockDim.x)
+    if (Mp[(long long)r * n + k]) {
+      mine = r;
+      break;
+    }
+  if (mine < n) atomicMin(&s_piv, mine);
+  __syncthreads();
+  const int r = s_piv;
+  if (r == n) {  // no pivot: q_p divides det(A)
+    if (threadIdx.x == 0) sing[p] = 1;
+    return;
+  }
+  if (r != k)
+    for (int j = threadIdx.x; j < n; j += blockDim.x) {
+      const uint8_t a = Mp[(long long)k * n + j];
+      Mp[(long long)k * n + j] = Mp[(long long)r * n + j];
+      Mp[(long long)r * n + j] = a;
+    }
+  __syncthreads();
+  const int q = c_all.q[p];
+  const int inv = invmod(Mp[(long long)k * n + k], q);
+  for (int i = threadIdx.x; i < n; i += blockDim.x) F[(long long)p * n + i] = Mp[(long long)i * n + k];
+  __syncthreads();
+  const float qf = c_all.qf[p], iq = c_all.invq[p];
+  for (int j = threadIdx.x; j < n; j += blockDim.x) {
+    const int a = j == k ? 1 : Mp[(long long)k * n + j];
+    Mp[(long long)k * n + j] = (uint8_t)mulmod(a, inv, qf, iq);
+  }
+  if (threadIdx.x == 0) {
+    perm[p * n + k] = r;
+    pinv[p] = inv;
+  }
+  allow_dependents();
+}
+
+// Every other row i: M[i][j] -= F[i] * M[k][j] (column k taken as 0 first).
+// 16 bytes of one row per thread; grid.y = prime.
+__global__ void __launch_bounds__(256) gj_elim_kernel(uint8_t* __restrict__ M, const uint8_t* __restrict__ F, int n,
+                                                      int k, const int* __restrict__ sing) {
+  wait_for_predecessor();
+  const int p = blockIdx.y;
+  if (sing[p]) return;
+  const long long nn = (long long)n * n;
+  const int per_row = n / 16;
+  const long long items = (long long)n * per_row;
+  uint8_t* Mp = M + p * nn;
+  const float qf = c_all.qf[p], iq = c_all.invq[p];
+  const int q = c_all.q[p];
+  for (long long it = (long long)blockIdx.x * blockDim.x + threadIdx.x; it < items;
+       it += (long long)gridDim.x * blockDim.x) {
+    const int i = (int)(it / per_row), j0 = (int)(it - (long long)i * per_row) * 16;
+    if (i == k) continue;
+    const int f = F[(long long)p * n + i];
+    if (f == 0) continue;
+    const int nf = q - f;
+    uint4 rowv = *reinterpret_cast<const uint4*>(Mp + (long long)i * n + j0);
+    const uint4 piv = *reinterpret_cast<const uint4*>(Mp + (long long)k * n + j0);
+    uint8_t* rb = reinterpret_cast<uint8_t*>(&rowv);
+    const uint8_t* pb = reinterpret_cast<const uint8_t*>(&piv);
+#pragma unroll
+    for (int b = 0; b < 16; ++b) {
+      const int a = (j0 + b == k) ? 0 : rb[b];
+      float r = bal_mod_small((float)(a + nf * pb[b]), qf, iq);  // < 2^16
+      rb[b] = (uint8_t)(r < 0.0f ? r + qf : r);
+    }
+    *reinterpret_cast<uint4*>(Mp + (long long)i * n + j0) = rowv;
+  }
+  allow_dependents();
+}
+
+// Undo the column swaps and write the balanced int8 inverse planes of the
+// lift's primes: Binv[s][i][j] = bal(M[map[s]][i][sigma(j)]) for i, j < n,
+// rows of nE bytes (zero past n).  The padded block stays the identity, so
+// sigma maps the first n columns among themselves.
+struct PrimeMap {
+  int idx[kNumPrimes];
+};
+
+__global__ void __launch_bounds__(256) gj_finish_kernel(const uint8_t* __restrict__ M, const int* __restrict__ perm,
+                                                        int n, int nE, PrimeMap map, int8_t* __restrict__ Binv) {
+  extern __shared__ int sigma[];
+  const int s = blockIdx.y, p = map.idx[s];
+  if (threadIdx.x == 0) {
+    for (int j = 0; j < nE; ++j) sigma[j] = j;
+    for (int k = nE - 1; k >= 0; --k) {
+      const int r = perm[p * nE + k];
+      const int t = sigma[k];
+      sigma[k] = sigma[r];
+      sigma[r] = t;
+    }
+  }
+  __syncthreads();
+  const long long nn = (long long)nE * nE;
+  const int q = c_all.q[p], h = (q - 1) / 2;
+  for (long long e = (long long)blockIdx.x * blockDim.x + threadIdx.x; e < (long long)n * nE;
+       e += (long long)gridDim.x * blockDim.x) {
+    const int i = (int)(e / nE), j = (int)(e - (long long)i * nE);
+    int v = 0;
+    if (j < n) {
+      v = M[p * nn + (long long)i * nE + sigma[j]];
+      v = v > h ? v - q : v;
+    }
+    Binv[(long long)s * n * nE + e] = (int8_t)v;
+  }
+}
+
+// ---------------------------------------------------------------------------
+// The lift ("exact-solve", Method: Dixon's lift on the residue engine).
+// ---------------------------------------------------------------------------
+
+// Rr[s][t][k] = bal(R[k][t] mod q_s) (int8), rows of length ld (zero padded).
+__global__ void __launch_bounds__(256) lift_residue_kernel(const int64_t* __restrict__ R, int n, int c, int ld, int E,
+                                                           int8_t* __restrict__ Rr) {
+  wait_for_predecessor();
+  for (long long e = (long long)blockIdx.x * blockDim.x + threadIdx.x; e < (long long)c * ld;
+       e += (long long)gridDim.x * blockDim.x) {
+    const int t = (int)(e / ld), k = (int)(e - (long long)t * ld);
+    const long long x = k < n ? R[(long long)k * c + t] : 0;
+    const unsigned long long u = (unsigned long long)x;
+    for (int s = 0; s < E; ++s) {
+      int acc = x < 0 ? -c_sol.wword[s][2] : 0;
+      asm("dp4a.u32.s32 %0, %1, %2, %0;" : "+r"(acc) : "r"((uint32_t)u), "r"(c_sol.wbyte[s][0]));
+      asm("dp4a.u32.s32 %0, %1, %2, %0;" : "+r"(acc) : "r"((uint32_t)(u >> 32)), "r"(c_sol.wbyte[s][1]));
+      Rr[((long long)s * c + t) * ld + k] = (int8_t)bal_mod_small(int_to_float_exact(acc), c_sol.qf[s], c_sol.invq[s]);
+    }
+  }
+  allow_dependents();
+}
+
+// RC[s][i][t] = (Binv[s][i][:] . Rr[s][t][:]) mod q_s in [0, q): one warp per
+// (prime, row), 16 int8 per lane and step, dp4a; |sum| <= n 125^2 < 2^31.
+__global__ void __launch_bounds__(256) lift_gemv_kernel(const int8_t* __restrict__ Binv, const int8_t* __restrict__ Rr,
+                                                        int n, int c, int ld, int E, uint8_t* __restrict__ RC) {
+  wait_for_predecessor();
+  const long long warp = ((long long)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+  const int lane = threadIdx.x & 31;
+  if (warp >= (long long)E * n) return;
+  const int s = (int)(warp / n), i = (int)(warp - (long long)s * n);
+  const int8_t* brow = Binv + ((long long)s * n + i) * ld;
+  const int q = c_sol.q[s];
+  for (int t = 0; t < c; ++t) {
+    const int8_t* rv = Rr + ((long long)s * c + t) * ld;
+    int acc = 0;
+    for (int k = lane * 16; k < ld; k += 32 * 16) {
+      const int4 a = *reinterpret_cast<const int4*>(brow + k);
+      const int4 b = *reinterpret_cast<const int4*>(rv + k);
+      acc = __dp4a(a.x, b.x, acc);
+      acc = __dp4a(a.y, b.y, acc);
+      acc = __dp4a(a.z, b.z, acc);
+      acc = __dp4a(a.w, b.w, acc);
+    }
+    for (int o = 16; o; o >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, o);
+    if (lane == 0) {
+      int r = acc % q;
+      RC[((long long)s * n + i) * c + t] = (uint8_t)(r < 0 ? r + q : r);
+    }
+  }
+  allow_dependents();
+}
+
+// The base-P digit X_i of every component (balanced Garner over the lift's
+// primes), kept for the reconstruction, and its low 64 bits for the update.
+__global__ void __launch_bounds__(128) lift_digit_kernel(const uint8_t* __restrict__ RC, int n, int c, int E,
+                                                         uint32_t* __restrict__ digit,
+                                                         unsigned long long* __restrict__ xlow) {
+  wait_for_predecessor();
+  const long long e = (long long)blockIdx.x * blockDim.x + threadIdx.x;
+  if (e < (long long)n * c) {
+    uint32_t x[1][kW];
+    garner_reconstruct<kW, 1, SolTab>(RC + e, (long long)n * c, E, x);
+#pragma unroll
+    for (int w = 0; w < kW; ++w) digit[e * kW + w] = x[0][w];
+    xlow[e] = ((unsigned long long)x[0][1] << 32) | x[0][0];
+  }
+  allow_dependents();
+}
+
+// R[i][t] = (R[i][t] - sum_k A[i][k] Xlow[k][t]) * P^-1 mod 2^64: the exact
+// quotient (R - A X) / P, which fits one signed limb.  One warp per row.
+__global__ void __launch_bounds__(256) lift_update_kernel(const int64_t* __restrict__ A, int n, int c,
+                                                          const unsigned long long* __restrict__ xlow,
+                                                          unsigned long long pinv64, int64_t* __restrict__ R) {
+  wait_for_predecessor();
+  const long long warp = ((long long)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+  const int lane = threadIdx.x & 31;
+  if (warp < n) {
+    const int64_t* arow = A + warp * n;
+    for (int t = 0; t < c; ++t) {
+      unsigned long long acc = 0;
+      for (int k = lane; k < n; k += 32) acc += (unsigned long long)arow[k] * xlow[(long long)k * c + t];
+      for (int o = 16; o; o >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, o);
+      if (lane == 0) {
+        const unsigned long long r = (unsigned long long)R[warp * c + t];
+        R[warp * c + t] = (int64_t)((r - acc) * pinv64);
+      }
+    }
+  }
+  allow_dependents();
+}
+
+// ---------------------------------------------------------------------------
+// Host side
+// ---------------------------------------------------------------------------
+
+struct DevBuf {  // stream-ordered device allocation
+  void* p = nullptr;
+  cudaStream_t s = nullptr;
+  cudaError_t alloc(size_t bytes, cudaStream_t st) {
+    s = st;
+    return cudaMallocAsync(&p, bytes ? bytes : 16, st);
+  }
+  ~DevBuf() {
+    if (p) cudaFreeAsync(p, s);
+  }
+};
+
+#define SOLVE_TRY(x)                             \
+  do {                                           \
+    cudaError_t e_ = (x);                        \
+    if (e_ != cudaSuccess) return RG_ERR_CUDA;   \
+  } while (0)
+
+unsigned long long inverse_mod_2_64(unsigned long long a) {  // a odd; Newton iteration
+  unsigned long long x = a;  // correct to 3 bits
+  for (int i = 0; i < 6; ++i) x *= 2 - a * x;
+  return x;
+}
+
+int sm_count_host() {
+  int dev = 0, n = 0;
+  cudaGetDevice(&dev);
+  cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
+  return n > 0 ? n : 148;
+}
+
+unsigned grid_for(long long items, int per_block = 256) {
+  long long b = (items + per_block - 1) / per_block;
+  const long long cap = 8LL * sm_count_host();
+  return (unsigned)std::max(1LL, std::min(b, cap));
+}
+
+}  // namespace
+}  // namespace rg
+
+using namespace rg;
+
+extern "C" void rg_solution_free(rg_solution* s) {
+  if (!s) return;
+  delete[] s->values;
+  s->values = nullptr;
+}
+
+extern "C" int rg_solve_i64(const int64_t* A_in, const int64_t* B_in, int64_t n64, int64_t c64, unsigned flags,
+                            void* stream, rg_solution* out) {
+  if (!A_in || !B_in || !out) return RG_ERR_ARG;
+  std::memset(out, 0, sizeof(*out));
+  if (n64 < 1 || c64 < 1 || c64 > (1 << 20)) return RG_ERR_ARG;
+  if (n64 > kMaxSolveN) return RG_ERR_RANGE;
+  const int n = (int)n64, c = (int)c64;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  SOLVE_TRY(upload_tables());
+  {
+    static bool uploaded[64];
+    int dev = 0;
+    SOLVE_TRY(cudaGetDevice(&dev));
+    if (dev < 0 || dev >= 64) return RG_ERR_CUDA;
+    if (!uploaded[dev]) {
+      SOLVE_TRY(cudaMemcpyToSymbol(c_all, &host_tables(), sizeof(Tables)));
+      uploaded[dev] = true;
+    }
+  }
+  const size_t nn = (size_t)n * n;
+  DevBuf dA, dB;
+  const int64_t* A = A_in;
+  const int64_t* B = B_in;
+  if (flags & RG_FLAG_HOST) {
+    SOLVE_TRY(dA.alloc(nn * 8, st));
+    SOLVE_TRY(dB.alloc((size_t)n * c * 8, st));
+    SOLVE_TRY(cudaMemcpyAsync(dA.p, A_in, nn * 8, cudaMemcpyHostToDevice, st));
+    SOLVE_TRY(cudaMemcpyAsync(dB.p, B_in, (size_t)n * c * 8, cudaMemcpyHostToDevice, st));
+    A = static_cast<const int64_t*>(dA.p);
+    B = static_cast<const int64_t*>(dB.p);
+  }
+
+  // 1. norms and the range check (one host synchronisation)
+  DevBuf dn;
+  SOLVE_TRY(dn.alloc(((size_t)2 * n + c) * 8 + 8, st));
+  double* rows = static_cast<double*>(dn.p);
+  double* cols = rows + n;
+  double* bcols = cols + n;
+  unsigned long long* maxabs = reinterpret_cast<unsigned long long*>(bcols + c);
+  SOLVE_TRY(cudaMemsetAsync(maxabs, 0, 8, st));
+  norms_kernel<<<(unsigned)((std::max((long long)n * 32, (long long)n + c) + 255) / 256), 256, 0, st>>>(
+      A, B, n, c, rows, cols, bcols, maxabs);
+  SOLVE_TRY(cudaGetLastError());
+  std::vector<double> hn((size_t)2 * n + c + 1);
+  SOLVE_TRY(cudaMemcpyAsync(hn.data(), dn.p, hn.size() * 8, cudaMemcpyDeviceToHost, st));
+  SOLVE_TRY(cudaStreamSynchronize(st));
+  unsigned long long amax;
+  std::memcpy(&amax, &hn[2 * n + c], 8);
+  if (amax == 0) return RG_ERR_SINGULAR;
+  if ((unsigned __int128)amax * (unsigned __int128)n >= ((unsigned __int128)1 << 63)) return RG_ERR_RANGE;
+  // Hadamard bounds (in bits, rounded up with a margin for the fp64 sums):
+  // |det A| <= prod of row (or column) norms; by Cramer's rule each numerator
+  // is the determinant of A with one column replaced by a column of B.
+  double row_bits = 0.0, col_bits = 0.0, min_col = 1e300, bmax = 0.0;
+  bool zero_line = false;
+  for (int i = 0; i < n; ++i) {
+    if (hn[i] <= 0.0 || hn[n + i] <= 0.0) zero_line = true;
+    row_bits += 0.5 * std::log2(std::max(hn[i], 1.0));
+    col_bits += 0.5 * std::log2(std::max(hn[n + i], 1.0));
+    min_col = std::min(min_col, 0.5 * std::log2(std::max(hn[n + i], 1.0)));
+  }
+  if (zero_line) return RG_ERR_SINGULAR;
+  for (int t = 0; t < c; ++t) bmax = std::max(bmax, 0.5 * std::log2(std::max(hn[2 * n + t], 1.0)));
+  const double margin = 4.0 + 1e-9 * n;
+  const double dbits = std::min(row_bits, col_bits) + margin;
+  double nbits_rows = 0.0;  // replacing column t: row norms grow to sqrt(|a_i|^2 + b_i^2) <= |a_i| + |b|
+  for (int i = 0; i < n; ++i) nbits_rows += 0.5 * std::log2(std::max(hn[i], 1.0) + std::exp2(2.0 * bmax));
+  const double nbits = std::min(nbits_rows, col_bits - min_col + bmax) + margin;
+
+  // 2. batched inverse, on diag(A, I) of order nE = n rounded up to 16
+  const int nE = (n + 15) / 16 * 16, ld = nE;
+  const size_t nnE = (size_t)nE * nE;
+  DevBuf dM, dF, dperm, dsing, dpinv;
+  SOLVE_TRY(dM.alloc((size_t)kNumPrimes * nnE, st));
+  SOLVE_TRY(dF.alloc((size_t)kNumPrimes * nE, st));
+  SOLVE_TRY(dperm.alloc((size_t)kNumPrimes * nE * 4, st));
+  SOLVE_TRY(dsing.alloc(kNumPrimes * 4, st));
+  SOLVE_TRY(dpinv.alloc(kNumPrimes * 4, st));
+  uint8_t* M = static_cast<uint8_t*>(dM.p);
+  uint8_t* F = static_cast<uint8_t*>(dF.p);
+  int* perm = static_cast<int*>(dperm.p);
+  int* sing = static_cast<int*>(dsing.p);
+  int* pinv = static_cast<int*>(dpinv.p);
+  SOLVE_TRY(cudaMemsetAsync(sing, 0, kNumPrimes * 4, st));
+  gj_init_kernel<<<grid_for((long long)nnE), 256, 0, st>>>(A, n, nE, M);
+  SOLVE_TRY(cudaGetLastError());
+  const long long elim_items = (long long)nE * (nE / 16);
+  const dim3 elim_grid(std::max(1u, std::min((unsigned)((elim_items + 255) / 256), 4u * sm_count_host())),
+                       kNumPrimes);
+  for (int k = 0; k < nE; ++k) {
+    SOLVE_TRY(launch_dependent(gj_pivot_kernel, dim3(kNumPrimes), dim3(256), 0, st, M, F, nE, k, perm, sing, pinv));
+    SOLVE_TRY(launch_dependent(gj_elim_kernel, elim_grid, dim3(256), 0, st, M, (const uint8_t*)F, nE, k,
+                               (const int*)sing));
+  }
+  int hsing[kNumPrimes];
+  SOLVE_TRY(cudaMemcpyAsync(hsing, sing, sizeof(hsing), cudaMemcpyDeviceToHost, st));
+  SOLVE_TRY(cudaStreamSynchronize(st));
+  const Tables& T = host_tables();
+  std::vector<int> qs;
+  PrimeMap map{};
+  for (int p = 0; p < kNumPrimes; ++p)
+    if (!hsing[p]) {
+      map.idx[qs.size()] = p;
+      qs.push_back(T.q[p]);
+    }
+  const int E = (int)qs.size();
+  if (E == 0) return RG_ERR_SINGULAR;  // singular modulo every prime below 256
+  Tables sol;
+  build_tables_for(qs.data(), E, &sol);
+  SOLVE_TRY(cudaMemcpyToSymbolAsync(c_sol, &sol, sizeof(Tables), 0, cudaMemcpyHostToDevice, st));
+  DevBuf dBinv;
+  SOLVE_TRY(dBinv.alloc((size_t)E * n * ld, st));
+  int8_t* Binv = static_cast<int8_t*>(dBinv.p);
+  gj_finish_kernel<<<dim3(grid_for((long long)n * ld), E), 256, (size_t)nE * 4, st>>>(M, perm, n, nE, map, Binv);
+  SOLVE_TRY(cudaGetLastError());
+
+  // 3. the lift
+  double log2P = 0.0;
+  big::Nat Pn = big::from_u64(1);
+  for (int q : qs) {
+    log2P += std::log2((double)q);
+    Pn = big::mul(Pn, big::from_u64((uint64_t)q));
+  }
+  const int steps = std::max(1, (int)std::ceil((1.0 + nbits + dbits) / log2P));
+  unsigned long long P64 = 1;
+  for (int q : qs) P64 *= (unsigned long long)q;  // P mod 2^64
+  const unsigned long long pinv64 = inverse_mod_2_64(P64);
+  DevBuf dR, dRr, dRC, dX, dlow;
+  SOLVE_TRY(dR.alloc((size_t)n * c * 8, st));
+  SOLVE_TRY(dRr.alloc((size_t)E * c * ld, st));
+  SOLVE_TRY(dRC.alloc((size_t)E * n * c, st));
+  SOLVE_TRY(dX.alloc((size_t)steps * n * c * kW * 4, st));
+  SOLVE_TRY(dlow.alloc((size_t)n * c * 8, st));
+  int64_t* R = static_cast<int64_t*>(dR.p);
+  SOLVE_TRY(cudaMemcpyAsync(R, B, (size_t)n * c * 8, cudaMemcpyDeviceToDevice, st));
+  uint32_t* X = static_cast<uint32_t*>(dX.p);
+  for (int i = 0; i < steps; ++i) {
+    SOLVE_TRY(launch_dependent(lift_residue_kernel, dim3(grid_for((long long)c * ld)), dim3(256), 0, st,
+                               (const int64_t*)R, n, c, ld, E, static_cast<int8_t*>(dRr.p)));
+    SOLVE_TRY(launch_dependent(lift_gemv_kernel, dim3((unsigned)(((long long)E * n * 32 + 255) / 256)), dim3(256), 0,
+                               st, (const int8_t*)Binv, (const int8_t*)dRr.p, n, c, ld, E,
+                               static_cast<uint8_t*>(dRC.p)));
+    SOLVE_TRY(launch_dependent(lift_digit_kernel, dim3((unsigned)(((long long)n * c + 127) / 128)), dim3(128), 0, st,
+                               (const uint8_t*)dRC.p, n, c, E, X + (size_t)i * n * c * kW,
+                               static_cast<unsigned long long*>(dlow.p)));
+    SOLVE_TRY(launch_dependent(lift_update_kernel, dim3((unsigned)(((long long)n * 32 + 255) / 256)), dim3(256), 0, st,
+                               A, n, c, (const unsigned long long*)dlow.p, pinv64, R));
+  }
+  std::vector<uint32_t> hX((size_t)steps * n * c * kW);
+  SOLVE_TRY(cudaMemcpyAsync(hX.data(), X, hX.size() * 4, cudaMemcpyDeviceToHost, st));
+  SOLVE_TRY(cudaStreamSynchronize(st));
+
+  // 4. rational reconstruction on the host
+  const big::Nat Pm = [&] {
+    big::Nat r = big::from_u64(1);
+    for (int i = 0; i < steps; ++i) r = big::mul(r, Pn);
+    return r;
+  }();
+  const big::Nat nbound = big::pow2((size_t)std::ceil(nbits));
+  const big::Nat dbound = big::pow2((size_t)std::ceil(dbits));
+  big::Nat half;
+  big::divmod(Pm, big::from_u64(2), &half, nullptr);
+  const long long comps = (long long)n * c;
+  // X_k = sum_i x_i P^i in [0, P^m)
+  auto value_of = [&](long long k) {
+    big::Int x = big::from_words(&hX[((size_t)(steps - 1) * comps + k) * kW], kW);
+    for (int i = steps - 2; i >= 0; --i) {
+      x = big::mul(x, Pn);
+      x = big::add(x, big::from_words(&hX[((size_t)i * comps + k) * kW], kW));
+    }
+    if (x.neg) x.mag = big::sub(Pm, x.mag);
+    return x.mag;
+  };
+  std::vector<big::Nat> Xv(comps);
+  const int nthreads = std::max(1, std::min((int)std::thread::hardware_concurrency(), 64));
+  auto parallel = [&](auto&& fn) {
+    std::vector<std::thread> th;
+    for (int w = 0; w < nthreads; ++w)
+      th.emplace_back([&, w] {
+        for (long long k = w; k < comps; k += nthreads) fn(k);
+      });
+    for (auto& t : th) t.join();
+  };
+  parallel([&](long long k) { Xv[k] = value_of(k); });
+  big::Nat D = big::from_u64(1);
+  std::vector<big::Int> Nv(comps);
+  bool ok = false;
+  for (int attempt = 0; attempt < 64 && !ok; ++attempt) {
+    std::vector<char> fits(comps, 1);
+    parallel([&](long long k) {
+      big::Nat y = big::mod(big::mul(D, Xv[k]), Pm);
+      big::Int v;
+      if (big::cmp(y, half) > 0) {
+        v.mag = big::sub(Pm, y);
+        v.neg = !big::is_zero(v.mag);
+      } else {
+        v.mag = y;
+      }
+      fits[k] = big::cmp(v.mag, nbound) <= 0;
+      Nv[k] = v;
+    });
+    long long bad = -1;
+    for (long long k = 0; k < comps; ++k)
+      if (!fits[k]) {
+        bad = k;
+        break;
+      }
+    if (bad < 0) {
+      ok = true;
+      break;
+    }
+    // the denominator of component `bad` joins the common one
+    big::Int Nk;
+    big::Nat Dk;
+    if (!big::rational_reconstruct(Xv[bad], Pm, nbound, dbound, &Nk, &Dk)) return RG_ERR_RANGE;
+    const big::Nat g = big::gcd(D, Dk);
+    big::Nat Dk_g;
+    big::divmod(Dk, g, &Dk_g, nullptr);
+    D = big::mul(D, Dk_g);
+  }
+  if (!ok) return RG_ERR_RANGE;
+  // the numerators and the denominator as limbs
+  size_t maxbits = big::bit_length(D);
+  for (const auto& v : Nv) maxbits = std::max(maxbits, big::bit_length(v.mag));
+  const int limbs = (int)(maxbits / 64 + 1);
+  out->n = n;
+  out->c = c;
+  out->limbs = limbs;
+  out->steps = steps;
+  out->primes = E;
+  out->values = new int64_t[(size_t)(comps + 1) * limbs];
+  for (long long k = 0; k < comps; ++k)
+    if (!big::to_limbs(Nv[k], out->values + (size_t)k * limbs, limbs)) {
+      rg_solution_free(out);
+      return RG_ERR_RANGE;
+    }
+  big::Int Di;
+  Di.mag = D;
+  if (!big::to_limbs(Di, out->values + (size_t)comps * limbs, limbs)) {
+    rg_solution_free(out);
+    return RG_ERR_RANGE;
+  }
+  return RG_OK;
+}
+
+extern "C" int rg_rational_reconstruct(const int64_t* x, int xl, const int64_t* m, int ml, int nbits, int dbits,
+                                       int64_t* num, int64_t* den, int limbs) {
+  if (!x || !m || !num || !den || xl < 1 || ml < 1 || limbs < 1 || nbits < 0 || dbits < 0) return RG_ERR_ARG;
+  big::Nat X, M;
+  X.v.assign((const uint64_t*)x, (const uint64_t*)x + xl);
+  M.v.assign((const uint64_t*)m, (const uint64_t*)m + ml);
+  big::trim(X);
+  big::trim(M);
+  if (big::is_zero(M) || big::cmp(X, M) >= 0) return RG_ERR_ARG;
+  big::Int N;
+  big::Nat D;
+  if (!big::rational_reconstruct(X, M, big::pow2(nbits), big::pow2(dbits), &N, &D)) return RG_ERR_RANGE;
+  big::Int Di;
+  Di.mag = D;
+  if (!big::to_limbs(N, num, limbs) || !big::to_limbs(Di, den, limbs)) return RG_ERR_RANGE;
+  return RG_OK;
+}

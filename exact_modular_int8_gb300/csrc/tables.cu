@@ -27,20 +27,13 @@ int balanced(int r, int q) {  // r in [0, q) -> [-(q-1)/2, (q-1)/2]
   return r > (q - 1) / 2 ? r - q : r;
 }
 
-void build(Tables& t) {
+// Tables for the prime sequence qs[0..E) (distinct odd primes below 256, in
+// the order the residues are combined); entries past E stay zero.
+void build_for(const int* qs, int E, Tables& t) {
   std::memset(&t, 0, sizeof(t));
-  // odd primes below 256, descending
-  bool composite[256] = {};
-  int n = 0;
-  int asc[kNumPrimes];
-  for (int i = 2; i < 256; ++i) {
-    if (composite[i]) continue;
-    for (int j = i * i; j < 256; j += i) composite[j] = true;
-    if (i != 2) asc[n++] = i;
-  }
-  for (int i = 0; i < kNumPrimes; ++i) t.q[i] = asc[kNumPrimes - 1 - i];
+  for (int i = 0; i < E; ++i) t.q[i] = qs[i];
 
-  for (int i = 0; i < kNumPrimes; ++i) {
+  for (int i = 0; i < E; ++i) {
     int q = t.q[i];
     t.qf[i] = (float)q;
     t.invq[i] = 1.0f / (float)q;
@@ -56,7 +49,7 @@ void build(Tables& t) {
   // floor(log2) of the running product, with an exact multi-word product.
   uint32_t big[16] = {1};
   t.log2P[0] = 0;
-  for (int n2 = 1; n2 <= kNumPrimes; ++n2) {
+  for (int n2 = 1; n2 <= E; ++n2) {
     uint64_t carry = 0;
     for (int w = 0; w < 16; ++w) {
       uint64_t v = (uint64_t)big[w] * (uint64_t)t.q[n2 - 1] + carry;
@@ -73,7 +66,7 @@ void build(Tables& t) {
   // Mixed-radix weights Q_i as words.
   {
     uint32_t q_words[kQWords] = {1};
-    for (int i = 0; i < kNumPrimes; ++i) {
+    for (int i = 0; i < E; ++i) {
       for (int w = 0; w < kQWords; ++w) t.Qw[i][w] = q_words[w];
       uint64_t carry = 0;
       for (int w = 0; w < kQWords; ++w) {
@@ -85,7 +78,7 @@ void build(Tables& t) {
   }
 
   // Garner constants.
-  for (int i = 0; i < kNumPrimes; ++i) {
+  for (int i = 0; i < E; ++i) {
     int q = t.q[i];
     long long Qi = 1;  // Q_i mod q
     for (int j = 0; j < i; ++j) Qi = Qi * t.q[j] % q;
@@ -102,14 +95,33 @@ void build(Tables& t) {
   }
 }
 
+// The residue base: the odd primes below 256, largest first.
+void canonical_primes(int (&qs)[kNumPrimes]) {
+  bool composite[256] = {};
+  int n = 0;
+  int asc[kNumPrimes];
+  for (int i = 2; i < 256; ++i) {
+    if (composite[i]) continue;
+    for (int j = i * i; j < 256; j += i) composite[j] = true;
+    if (i != 2) asc[n++] = i;
+  }
+  for (int i = 0; i < kNumPrimes; ++i) qs[i] = asc[kNumPrimes - 1 - i];
+}
+
 }  // namespace
 
 const Tables& host_tables() {
   static Tables t;
   static std::once_flag once;
-  std::call_once(once, [] { build(t); });
+  std::call_once(once, [] {
+    int qs[kNumPrimes];
+    canonical_primes(qs);
+    build_for(qs, kNumPrimes, t);
+  });
   return t;
 }
+
+void build_tables_for(const int* qs, int count, Tables* out) { build_for(qs, count, *out); }
 
 const Pow2Table& host_pow2() {
   static Pow2Table t;

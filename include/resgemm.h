@@ -52,6 +52,7 @@ extern "C" {
 #define RG_ERR_CUDA 6       /* a CUDA runtime or driver call failed */
 #define RG_ERR_TIMEOUT 7    /* a bounded wait inside a kernel expired; the kernel stopped early */
 #define RG_ERR_RADIUS 8     /* an interval radius entry is negative */
+#define RG_ERR_SINGULAR 9   /* rg_solve_i64: A is singular modulo every prime below 256 */
 
 /* Flags. */
 #define RG_FLAG_SYNC 1u /* synchronise the stream before returning; return the device status */
@@ -298,6 +299,53 @@ typedef struct {
   int splits;   /* K slices the per-prime GEMM used (1: none; more when there were too few output tiles) */
 } rg_plan_info;
 int rg_get_plan(const void* ws, void* stream, rg_plan_info* out);
+
+/*
+ * Exact rational solution of A X = B for integer A [n][n] and B [n][c]
+ * (row-major int64; device pointers, or host pointers with RG_FLAG_HOST)
+ * ("exact-solve", Method).
+ *  1. A^-1 mod q for all 53 primes at once by Gauss-Jordan elimination on the
+ *     GPU, one launch per elimination step over all primes; the primes that
+ *     divide det(A) are dropped.
+ *  2. Dixon's p-adic lift with P = the product of the remaining primes:
+ *     X_i = A^-1 R_i mod P per prime, then balanced Garner into the base-P
+ *     digit; R_{i+1} = (R_i - A X_i) P^-1 mod 2^64, exact in one limb; as
+ *     many steps as make P^m exceed twice the product of the Hadamard bounds
+ *     of numerator and denominator.
+ *  3. On the host: rational reconstruction of a component for the common
+ *     denominator, then one modular product per numerator.
+ * On success `out` holds the numerators N [n][c] and the least common
+ * denominator d > 0 (X = N / d exactly), as `limbs` little-endian
+ * two's-complement int64 limbs each, in a host array the library allocates
+ * and rg_solution_free releases.  Requires n * max|A| < 2^63 (so the residual
+ * stays one limb) and n <= 8192.  The call synchronises `stream`.  It is not
+ * safe to run two solves at once on one device (one constant table holds the
+ * lift's primes).
+ * Errors: RG_ERR_ARG, RG_ERR_RANGE (n or the entries out of range),
+ * RG_ERR_SINGULAR (A is singular modulo every prime below 256: singular over
+ * the rationals, unless det(A) is divisible by all 53 primes), RG_ERR_CUDA.
+ */
+typedef struct {
+  int64_t n, c;     /* shape of the solution */
+  int64_t limbs;    /* int64 limbs per value */
+  int64_t* values;  /* (n * c + 1) * limbs: the numerators row-major, then d */
+  int64_t steps;    /* lift steps m */
+  int primes;       /* primes in the lift modulus P */
+} rg_solution;
+int rg_solve_i64(const int64_t* A, const int64_t* B, int64_t n, int64_t c, unsigned flags, void* stream,
+                 rg_solution* out);
+void rg_solution_free(rg_solution* s);
+
+/*
+ * Rational reconstruction on the host (the solve's last step, exposed for
+ * testing): N, D with D X == N (mod M), |N| <= 2^nbits, 0 < D <= 2^dbits, in
+ * lowest terms, for 0 <= X < M given as xl and ml little-endian 64-bit limbs.
+ * Writes `limbs` two's-complement limbs each to num and den.  Returns
+ * RG_ERR_RANGE if no such pair exists or it does not fit, RG_ERR_ARG on bad
+ * arguments.  Unique when 2^(nbits + dbits + 1) < M.
+ */
+int rg_rational_reconstruct(const int64_t* x, int xl, const int64_t* m, int ml, int nbits, int dbits, int64_t* num,
+                            int64_t* den, int limbs);
 
 /* Synchronise `stream` and return the device status of the last call that
  * used `ws` (RG_OK, RG_ERR_RANGE, RG_ERR_NONFINITE, RG_ERR_LOSSY,

@@ -1,0 +1,127 @@
+"""GPU exact solve (rg_solve_i64 / solve; "exact-solve", Method: batched
+modular inverse, Dixon lift on the residue engine, rational reconstruction)
+against the Fraction Gaussian-elimination oracle on small systems and the
+integer identity A N == d b on larger ones ("exact-solve", Correctness)."""
+import math
+from fractions import Fraction
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from tests.gpu_util import dev, rg  # noqa: F401
+
+pytestmark = pytest.mark.gpu
+
+
+def nonsingular(n, lo, hi, seed):
+    rng = np.random.default_rng(seed)
+    while True:
+        A = rng.integers(lo, hi, size=(n, n), dtype=np.int64)
+        if oracle.solve_fraction(A[: min(n, 12), : min(n, 12)], np.ones((min(n, 12), 1), dtype=np.int64)) is not None:
+            return A
+
+
+def integer_identity(A, X, b):
+    """A N == d b with N, d the integer form of X, in Python integers."""
+    N, d = oracle.solution_as_integers(X)
+    n, c = len(N), len(N[0])
+    Ai = [[int(v) for v in row] for row in A]
+    for i in range(n):
+        for j in range(c):
+            if sum(Ai[i][k] * N[k][j] for k in range(n)) != d * int(b[i][j]):
+                return False
+    return True
+
+
+@pytest.mark.parametrize("n,c,seed", [(1, 1, 0), (3, 2, 1), (7, 1, 2), (16, 3, 3), (20, 1, 4)])
+def test_against_fraction_oracle(rg, n, c, seed):
+    rng = np.random.default_rng(seed + 100)
+    A = nonsingular(n, -(2**20), 2**20, seed)
+    b = rng.integers(-(2**30), 2**30, size=(n, c), dtype=np.int64)
+    X = rg.solve(dev(A), dev(b))
+    assert X == oracle.solve_fraction(A, b)
+
+
+@pytest.mark.parametrize("n,seed", [(33, 5), (100, 6), (257, 7)])
+def test_planted_integer_solution(rg, n, seed):
+    rng = np.random.default_rng(seed)
+    A = rng.integers(-(2**24), 2**24, size=(n, n), dtype=np.int64)
+    x = rng.integers(-(2**20), 2**20, size=(n, 2), dtype=np.int64)
+    b = np.array([[sum(int(A[i, k]) * int(x[k, j]) for k in range(n)) for j in range(2)] for i in range(n)],
+                 dtype=object)
+    assert all(abs(int(v)) < 2**63 for v in b.ravel())
+    info = {}
+    X = rg.solve(dev(A), dev(b.astype(np.int64)), info=info)
+    assert X == [[Fraction(int(v)) for v in row] for row in x]
+    assert info["denominator"] == 1 and info["steps"] >= 1
+
+
+def test_rational_solution_integer_identity(rg):
+    n = 128
+    rng = np.random.default_rng(8)
+    A = rng.integers(-(2**23), 2**23, size=(n, n), dtype=np.int64)
+    b = rng.integers(-(2**23), 2**23, size=(n, 1), dtype=np.int64)
+    info = {}
+    X = rg.solve(dev(A), dev(b), info=info)
+    assert integer_identity(A, X, b)
+    d = info["denominator"]
+    assert math.lcm(*[v.denominator for row in X for v in row]) == d  # the least common denominator
+
+
+def test_pascal_order_30(rg):
+    """The pages' example: the order-30 Pascal system (condition ~1e32) has an exact integer solution."""
+    n = 30
+    P = np.array([[math.comb(i + j, i) for j in range(n)] for i in range(n)], dtype=object)
+    assert max(int(v) for v in P.ravel()) * n < 2**63
+    b = np.ones((n, 1), dtype=np.int64)
+    X = rg.solve(dev(P.astype(np.int64)), dev(b))
+    assert all(v.denominator == 1 for row in X for v in row)
+    assert integer_identity(P, X, b)
+    assert X == oracle.solve_fraction(P, b)
+
+
+def test_scaled_hilbert_dense_denominators(rg):
+    n = 9
+    L = math.lcm(*range(1, 2 * n))
+    H = np.array([[L // (i + j + 1) for j in range(n)] for i in range(n)], dtype=np.int64)
+    b = np.eye(n, 2, dtype=np.int64)
+    X = rg.solve(dev(H), dev(b))
+    assert X == oracle.solve_fraction(H, b)
+    assert max(v.denominator for row in X for v in row) > 1
+
+
+def test_primes_dividing_det_are_dropped(rg):
+    """Every entry a multiple of 3 * 5 * 7: det(A) is divisible by 105^n, so the lift runs without those primes."""
+    n = 24
+    rng = np.random.default_rng(9)
+    A = 105 * rng.integers(-1000, 1000, size=(n, n), dtype=np.int64)
+    b = rng.integers(-1000, 1000, size=(n, 1), dtype=np.int64)
+    info = {}
+    X = rg.solve(dev(A), dev(b), info=info)
+    assert info["primes"] <= 50
+    assert integer_identity(A, X, b)
+
+
+def test_host_tensors_and_vector_b(rg):
+    n = 12
+    A = nonsingular(n, -99, 100, 10)
+    b = np.arange(n, dtype=np.int64) - 5
+    X = rg.solve(torch.from_numpy(A), torch.from_numpy(b))
+    assert X == oracle.solve_fraction(A, b[:, None])
+
+
+def test_singular_returns_none(rg):
+    A = np.array([[1, 2, 3], [2, 4, 6], [7, 1, 1]], dtype=np.int64)
+    assert rg.solve(dev(A), dev(np.ones((3, 1), dtype=np.int64))) is None
+    Z = np.zeros((4, 4), dtype=np.int64)
+    assert rg.solve(dev(Z), dev(np.ones((4, 1), dtype=np.int64))) is None
+
+
+def test_range_error(rg):
+    n = 4
+    A = np.full((n, n), 2**62, dtype=np.int64)  # n * max|A| = 2^64
+    with pytest.raises(rg.ResGemmError) as e:
+        rg.solve(dev(A), dev(np.ones((n, 1), dtype=np.int64)))
+    assert e.value.code == rg.RG_ERR_RANGE
