@@ -43,6 +43,8 @@ def parse_args():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default="exact24_1024")
     ap.add_argument("--no-extras", action="store_true", help="skip e2e, cpu baseline, int8 probe and 4096^3 stage")
+    ap.add_argument("--solve", type=int, default=0, metavar="N",
+                    help="instead, time the exact solve of an N x N system with 24-bit entries")
     return ap.parse_args()
 
 
@@ -274,10 +276,48 @@ def job_throughput(total_ms_max: float, steps: int, macs: int, world: int):
     return value, total_ms_max / steps
 
 
+def run_solve(args):
+    """Wall time of the exact rational solve (the call synchronises), with its phases, and
+    the integer identity A N == d b checked on the result."""
+    import numpy as np
+    import torch
+
+    import exact_modular_int8_gb300 as rg
+    from workloads import solve_system
+
+    n = args.solve
+    A, b = solve_system(n)
+    dA, db = torch.from_numpy(A).cuda(), torch.from_numpy(b).cuda()
+    for _ in range(max(1, args.warmup)):
+        rg.solve_integers(dA, db)
+    times, infos = [], []
+    for _ in range(args.steps):
+        info = {}
+        t0 = time.perf_counter()
+        N, d = rg.solve_integers(dA, db, info=info)
+        times.append(time.perf_counter() - t0)
+        infos.append(info)
+    ok = all(sum(int(A[i, k]) * N[k][0] for k in range(n)) == d * int(b[i, 0]) for i in range(n))
+    mean = lambda key: sum(x[key] for x in infos) / len(infos)  # noqa: E731
+    line = {"metric": "exact rational solve wall time (A x = b, b one column; numerators and common denominator "
+                      "as Python ints)", "value": 1e3 * sum(times) / len(times),
+            "unit": "ms", "n_gpus": 1, "steps": args.steps, "warmup": max(1, args.warmup),
+            "higher_is_better": False, "dtype": "int64", "data": "synthetic",
+            "config": {"workload": f"solve24_{n}", "n": n, "c": 1, "entries": "int64 uniform in [-2^23, 2^23)"},
+            "phases_ms": {"inverse": mean("ms_inverse"), "lift": mean("ms_lift"),
+                          "reconstruct": mean("ms_reconstruct")},
+            "lift_steps": infos[-1]["steps"], "primes": infos[-1]["primes"],
+            "denominator_bits": d.bit_length(), "identity_A_N_eq_d_b": ok}
+    print(json.dumps(line), flush=True)
+
+
 def main():
     args = parse_args()
     if args.impl == "reference":
         run_reference(args)
+        return
+    if args.solve:
+        run_solve(args)
         return
     import numpy as np
     import torch

@@ -81,7 +81,8 @@ class PlanInfo(ctypes.Structure):
 
 class Solution(ctypes.Structure):
     _fields_ = [("n", ctypes.c_int64), ("c", ctypes.c_int64), ("limbs", ctypes.c_int64),
-                ("values", ctypes.POINTER(ctypes.c_int64)), ("steps", ctypes.c_int64), ("primes", ctypes.c_int)]
+                ("values", ctypes.POINTER(ctypes.c_int64)), ("steps", ctypes.c_int64), ("primes", ctypes.c_int),
+                ("ms_inverse", ctypes.c_double), ("ms_lift", ctypes.c_double), ("ms_reconstruct", ctypes.c_double)]
 
 
 _lib = None
@@ -514,11 +515,11 @@ def _int_to_limbs(v: int, limbs: int):
             for i in range(limbs)]
 
 
-def solve(A: torch.Tensor, b: torch.Tensor, info: dict | None = None):
-    """The exact solution X of A X = b over the rationals, as a nested list [n][c] of
-    fractions.Fraction (c = 1 for a 1-D b), or None if A is singular.  A [n, n] and b are
-    int64 (CUDA tensors, or CPU tensors staged through the device).  `info`, if given,
-    receives the lift's step and prime counts."""
+def solve_integers(A: torch.Tensor, b: torch.Tensor, info: dict | None = None):
+    """The exact solution of A X = b in integer form (N, d): numerators N [n][c] (Python
+    ints) and the least common denominator d > 0, X = N / d; None if A is singular.  A [n, n]
+    and b [n] or [n, c] are int64 (CUDA tensors, or CPU tensors staged through the device).
+    `info`, if given, receives the lift's step and prime counts and the phase times."""
     if A.dtype != torch.int64 or b.dtype != torch.int64 or A.dim() != 2 or A.shape[0] != A.shape[1]:
         raise ValueError("A [n, n] and b [n] or [n, c] int64 expected")
     b2 = b.reshape(-1, 1) if b.dim() == 1 else b
@@ -535,15 +536,27 @@ def solve(A: torch.Tensor, b: torch.Tensor, info: dict | None = None):
         return None
     _check(rc, "rg_solve_i64")
     try:
-        L = sol.limbs
-        vals = [sol.values[i] for i in range((n * c + 1) * L)]
+        nb = 8 * sol.limbs
+        raw = ctypes.string_at(sol.values, (n * c + 1) * nb)
     finally:
         library().rg_solution_free(ctypes.byref(sol))
-    d = _limbs_to_int(vals[n * c * L:])
+    vals = [int.from_bytes(raw[k * nb:(k + 1) * nb], "little", signed=True) for k in range(n * c + 1)]
+    d = vals[-1]
     if info is not None:
-        info.update(steps=int(sol.steps), primes=int(sol.primes), denominator=d)
-    return [[Fraction(_limbs_to_int(vals[(i * c + j) * L:(i * c + j + 1) * L]), d) for j in range(c)]
-            for i in range(n)]
+        info.update(steps=int(sol.steps), primes=int(sol.primes), denominator=d, ms_inverse=sol.ms_inverse,
+                    ms_lift=sol.ms_lift, ms_reconstruct=sol.ms_reconstruct)
+    return [vals[i * c:(i + 1) * c] for i in range(n)], d
+
+
+def solve(A: torch.Tensor, b: torch.Tensor, info: dict | None = None):
+    """The exact solution X of A X = b over the rationals, as a nested list [n][c] of
+    fractions.Fraction (c = 1 for a 1-D b), or None if A is singular ("exact-solve", Usage:
+    solve).  See solve_integers for the arguments."""
+    r = solve_integers(A, b, info)
+    if r is None:
+        return None
+    N, d = r
+    return [[Fraction(v, d) for v in row] for row in N]
 
 
 def rational_reconstruct(x: int, m: int, nbits: int, dbits: int):

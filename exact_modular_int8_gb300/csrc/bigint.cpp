@@ -255,12 +255,208 @@ bool to_limbs(const Int& a, int64_t* out, int limbs) {
   return true;
 }
 
+Reducer make_reducer(const Nat& M) {
+  Reducer R;
+  R.M = M;
+  const size_t n = M.v.size();
+  R.shift = __builtin_clzll(M.v[n - 1]);
+  R.vn.resize(n);
+  for (size_t i = n; i-- > 1;) R.vn[i] = (M.v[i] << R.shift) | (R.shift ? M.v[i - 1] >> (64 - R.shift) : 0);
+  R.vn[0] = M.v[0] << R.shift;
+  return R;
+}
+
+void mul_into(const Limb* a, size_t na, const Limb* b, size_t nb, std::vector<Limb>& out) {
+  out.assign(na + nb, 0);
+  for (size_t i = 0; i < na; ++i) {
+    Limb carry = 0;
+    const Limb ai = a[i];
+    Limb* o = out.data() + i;
+    for (size_t j = 0; j < nb; ++j) {
+      const u128 t = (u128)ai * b[j] + o[j] + carry;
+      o[j] = (Limb)t;
+      carry = (Limb)(t >> 64);
+    }
+    o[nb] = carry;
+  }
+}
+
+void reduce(const Reducer& R, const Limb* a, size_t na, std::vector<Limb>& un, Nat* r) {
+  while (na > 0 && a[na - 1] == 0) --na;
+  const size_t n = R.vn.size();
+  if (na < n || (na == n && [&] {
+        for (size_t i = n; i-- > 0;)
+          if (a[i] != R.M.v[i]) return a[i] < R.M.v[i];
+        return false;
+      }())) {
+    r->v.assign(a, a + na);
+    return;
+  }
+  const int s = R.shift;
+  const std::vector<Limb>& vn = R.vn;
+  un.assign(na + 1, 0);
+  un[na] = s ? a[na - 1] >> (64 - s) : 0;
+  for (size_t i = na; i-- > 1;) un[i] = (a[i] << s) | (s ? a[i - 1] >> (64 - s) : 0);
+  un[0] = a[0] << s;
+  if (n == 1) {
+    u128 rem = 0;
+    for (size_t i = na + 1; i-- > 0;) rem = ((rem << 64) | un[i]) % vn[0];
+    r->v.assign(1, (Limb)(rem >> s));
+    trim(*r);
+    return;
+  }
+  for (size_t j = na - n + 1; j-- > 0;) {  // Knuth's algorithm D, remainder only
+    const u128 num = ((u128)un[j + n] << 64) | un[j + n - 1];
+    u128 qhat = num / vn[n - 1], rhat = num % vn[n - 1];
+    while (qhat >> 64 || qhat * vn[n - 2] > ((rhat << 64) | un[j + n - 2])) {
+      --qhat;
+      rhat += vn[n - 1];
+      if (rhat >> 64) break;
+    }
+    Limb borrow = 0, carry = 0;
+    for (size_t i = 0; i < n; ++i) {
+      const u128 p = qhat * vn[i] + carry;
+      carry = (Limb)(p >> 64);
+      const Limb lo = (Limb)p;
+      const Limb t = un[i + j] - lo - borrow;
+      borrow = (un[i + j] < lo || (un[i + j] == lo && borrow)) ? 1 : 0;
+      un[i + j] = t;
+    }
+    const Limb top = un[j + n];
+    const bool negative = top < carry || (top == carry && borrow);
+    un[j + n] = top - carry - borrow;
+    if (negative) {
+      Limb c = 0;
+      for (size_t i = 0; i < n; ++i) {
+        const u128 sum = (u128)un[i + j] + vn[i] + c;
+        un[i + j] = (Limb)sum;
+        c = (Limb)(sum >> 64);
+      }
+      un[j + n] += c;
+    }
+  }
+  r->v.resize(n);
+  for (size_t i = 0; i < n; ++i) r->v[i] = (un[i] >> s) | (s ? un[i + 1] << (64 - s) : 0);
+  trim(*r);
+}
+
+void mul_add_into(std::vector<Limb>& acc, const Limb* m, size_t nm, const Limb* z, size_t nz,
+                  std::vector<Limb>& scratch) {
+  size_t na = acc.size();
+  while (na > 0 && acc[na - 1] == 0) --na;
+  scratch.assign(std::max(na + nm, nz) + 1, 0);
+  for (size_t i = 0; i < na; ++i) {
+    Limb carry = 0;
+    const Limb ai = acc[i];
+    Limb* o = scratch.data() + i;
+    for (size_t j = 0; j < nm; ++j) {
+      const u128 t = (u128)ai * m[j] + o[j] + carry;
+      o[j] = (Limb)t;
+      carry = (Limb)(t >> 64);
+    }
+    o[nm] = carry;
+  }
+  Limb carry = 0;
+  for (size_t i = 0; i < scratch.size(); ++i) {
+    const u128 t = (u128)scratch[i] + (i < nz ? z[i] : 0) + carry;
+    scratch[i] = (Limb)t;
+    carry = (Limb)(t >> 64);
+  }
+  acc.swap(scratch);
+}
+
+namespace {
+
+// a * x for a natural x and a one-limb a.
+Nat mul_limb(const Nat& x, Limb a) {
+  Nat r;
+  if (!a || x.v.empty()) return r;
+  r.v.resize(x.v.size() + 1);
+  Limb carry = 0;
+  for (size_t i = 0; i < x.v.size(); ++i) {
+    const u128 t = (u128)x.v[i] * a + carry;
+    r.v[i] = (Limb)t;
+    carry = (Limb)(t >> 64);
+  }
+  r.v[x.v.size()] = carry;
+  trim(r);
+  return r;
+}
+
+// a * x + b * y for signed one-limb coefficients.
+Int lincomb(const Int& x, long long a, const Int& y, long long b) {
+  Int px, py;
+  px.mag = mul_limb(x.mag, (Limb)(a < 0 ? -(unsigned long long)a : (unsigned long long)a));
+  px.neg = (x.neg != (a < 0)) && !is_zero(px.mag);
+  py.mag = mul_limb(y.mag, (Limb)(b < 0 ? -(unsigned long long)b : (unsigned long long)b));
+  py.neg = (y.neg != (b < 0)) && !is_zero(py.mag);
+  return add(px, py);
+}
+
+// The 62 bits of x starting at bit s (x < 2^(s + 62)).
+uint64_t bits_at(const Nat& x, size_t s) {
+  const size_t w = s / 64, o = s % 64;
+  uint64_t lo = w < x.v.size() ? x.v[w] >> o : 0;
+  if (o && w + 1 < x.v.size()) lo |= x.v[w + 1] << (64 - o);
+  return lo & ((1ull << 62) - 1);
+}
+
+}  // namespace
+
 bool rational_reconstruct(const Nat& X, const Nat& M, const Nat& nbound, const Nat& dbound, Int* N, Nat* D) {
   // Extended Euclid on (M, X) with the cofactor of X, stopped at the first
   // remainder <= nbound (Wang's reconstruction).
   Nat r0 = M, r1 = X;
   Int t0, t1;
   t1.mag = from_u64(1);
+  // Lehmer's method (Knuth, TAOCP vol. 2, 4.5.2, algorithm L): the quotient
+  // sequence of the leading 62 bits, accepted while the bracketing quotients
+  // (u + A) / (v + C) and (u + B) / (v + D) agree, is the full numbers'
+  // sequence; its 2x2 matrix is then applied once.  Run only while r1 stays
+  // more than 64 bits above the bound: one batch shrinks r1 by less than
+  // 2^63, so no remainder of a batch reaches the stopping point.
+  const size_t stop_bits = bit_length(nbound) + 64;
+  while (bit_length(r1) > stop_bits) {
+    const size_t b0 = bit_length(r0);
+    const size_t sh = b0 > 62 ? b0 - 62 : 0;
+    long long u = (long long)bits_at(r0, sh), v = (long long)bits_at(r1, sh);
+    long long A = 1, B = 0, C = 0, Dc = 1;
+    while (true) {
+      const __int128 d1 = (__int128)v + C, d2 = (__int128)v + Dc;
+      if (d1 <= 0 || d2 <= 0) break;
+      const __int128 q1 = ((__int128)u + A) / d1, q2 = ((__int128)u + B) / d2;
+      if (q1 != q2) break;
+      const long long q = (long long)q1;
+      long long T = A - q * C;
+      A = C;
+      C = T;
+      T = B - q * Dc;
+      B = Dc;
+      Dc = T;
+      T = u - q * v;
+      u = v;
+      v = T;
+    }
+    if (B == 0) {  // no usable leading quotient: one full-precision step
+      Nat q, r;
+      divmod(r0, r1, &q, &r);
+      Int t = sub(t0, mul(t1, q));
+      r0 = std::move(r1);
+      r1 = std::move(r);
+      t0 = std::move(t1);
+      t1 = std::move(t);
+    } else {
+      Int R0, R1;
+      R0.mag = r0;
+      R1.mag = r1;
+      Int n0 = lincomb(R0, A, R1, B), n1 = lincomb(R0, C, R1, Dc);
+      Int s0 = lincomb(t0, A, t1, B), s1 = lincomb(t0, C, t1, Dc);
+      r0 = std::move(n0.mag);
+      r1 = std::move(n1.mag);
+      t0 = std::move(s0);
+      t1 = std::move(s1);
+    }
+  }
   while (cmp(r1, nbound) > 0) {
     Nat q, r;
     divmod(r0, r1, &q, &r);

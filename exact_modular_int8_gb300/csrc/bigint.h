@@ -43,6 +43,23 @@ Int from_words(const uint32_t* w, int nw);
 // Int -> `limbs` little-endian two's-complement int64 limbs; false if it does not fit.
 bool to_limbs(const Int& a, int64_t* out, int limbs);
 
+// Repeated reduction modulo one fixed M > 0 (normalised once for long
+// division), with caller-owned scratch so that no call allocates once the
+// buffers have grown.
+struct Reducer {
+  Nat M;
+  std::vector<Limb> vn;  // M shifted so its top limb has its top bit set
+  int shift = 0;
+};
+Reducer make_reducer(const Nat& M);
+// out = (a[0..na) * b[0..nb)) as limbs (length na + nb, not trimmed).
+void mul_into(const Limb* a, size_t na, const Limb* b, size_t nb, std::vector<Limb>& out);
+// r = a mod R.M for a given as na limbs; un is scratch.
+void reduce(const Reducer& R, const Limb* a, size_t na, std::vector<Limb>& un, Nat* r);
+// acc = acc * m + z in place (m and z as limb arrays; acc grows as needed).
+void mul_add_into(std::vector<Limb>& acc, const Limb* m, size_t nm, const Limb* z, size_t nz,
+                  std::vector<Limb>& scratch);
+
 // Rational reconstruction: the N, D with D X == N (mod M), |N| <= nbound,
 // 0 < D <= dbound, for 0 <= X < M and 2 nbound dbound < M (then unique, in
 // lowest terms).  False if there is none.

@@ -11,6 +11,7 @@
 #include <cuda_runtime.h>
 
 #include <algorithm>
+#include <chrono>
 #include <cmath>
 #include <cstring>
 #include <thread>
@@ -409,6 +410,11 @@ extern "C" int rg_solve_i64(const int64_t* A_in, const int64_t* B_in, int64_t n6
   if (n64 > kMaxSolveN) return RG_ERR_RANGE;
   const int n = (int)n64, c = (int)c64;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
+  using clock = std::chrono::steady_clock;
+  const auto t0 = clock::now();
+  auto ms_since = [](clock::time_point a) {
+    return std::chrono::duration<double, std::milli>(clock::now() - a).count();
+  };
   SOLVE_TRY(upload_tables());
   {
     static bool uploaded[64];
@@ -518,6 +524,9 @@ extern "C" int rg_solve_i64(const int64_t* A_in, const int64_t* B_in, int64_t n6
   SOLVE_TRY(cudaGetLastError());
 
   // 3. the lift
+  SOLVE_TRY(cudaStreamSynchronize(st));
+  const double ms_inverse = ms_since(t0);
+  const auto t1 = clock::now();
   double log2P = 0.0;
   big::Nat Pn = big::from_u64(1);
   for (int q : qs) {
@@ -552,6 +561,8 @@ extern "C" int rg_solve_i64(const int64_t* A_in, const int64_t* B_in, int64_t n6
   std::vector<uint32_t> hX((size_t)steps * n * c * kW);
   SOLVE_TRY(cudaMemcpyAsync(hX.data(), X, hX.size() * 4, cudaMemcpyDeviceToHost, st));
   SOLVE_TRY(cudaStreamSynchronize(st));
+  const double ms_lift = ms_since(t1);
+  const auto t2 = clock::now();
 
   // 4. rational reconstruction on the host
   const big::Nat Pm = [&] {
@@ -564,64 +575,107 @@ extern "C" int rg_solve_i64(const int64_t* A_in, const int64_t* B_in, int64_t n6
   big::Nat half;
   big::divmod(Pm, big::from_u64(2), &half, nullptr);
   const long long comps = (long long)n * c;
-  // X_k = sum_i x_i P^i in [0, P^m)
-  auto value_of = [&](long long k) {
-    big::Int x = big::from_words(&hX[((size_t)(steps - 1) * comps + k) * kW], kW);
-    for (int i = steps - 2; i >= 0; --i) {
-      x = big::mul(x, Pn);
-      x = big::add(x, big::from_words(&hX[((size_t)i * comps + k) * kW], kW));
-    }
-    if (x.neg) x.mag = big::sub(Pm, x.mag);
-    return x.mag;
+  const size_t pl = Pn.v.size();  // limbs of P (<= 6)
+  // X_k = sum_i x_i P^i mod P^m, from the balanced digits normalised to
+  // [0, P) by borrow propagation (a final borrow is a multiple of P^m), then
+  // Horner's rule on naturals, allocation-free per component.
+  struct Scratch {
+    std::vector<big::Limb> acc, tmp, un, prod;
+    std::vector<big::Limb> z;  // normalised digits, m x pl limbs
   };
+  auto value_of = [&](long long k, Scratch& S) {
+    S.z.assign((size_t)steps * pl, 0);
+    int borrow = 0;
+    for (int i = 0; i < steps; ++i) {
+      big::Int x = big::from_words(&hX[((size_t)i * comps + k) * kW], kW);
+      if (borrow) x = big::sub(x, big::Int{false, big::from_u64(1)});
+      borrow = x.neg ? 1 : 0;
+      const big::Nat zi = x.neg ? big::sub(Pn, x.mag) : x.mag;
+      std::copy(zi.v.begin(), zi.v.end(), S.z.begin() + (size_t)i * pl);
+    }
+    S.acc.clear();
+    for (int i = steps - 1; i >= 0; --i) big::mul_add_into(S.acc, Pn.v.data(), pl, &S.z[(size_t)i * pl], pl, S.tmp);
+    big::Nat X;
+    X.v = S.acc;
+    big::trim(X);
+    return X;
+  };
+  const big::Reducer red = big::make_reducer(Pm);
   std::vector<big::Nat> Xv(comps);
   const int nthreads = std::max(1, std::min((int)std::thread::hardware_concurrency(), 64));
-  auto parallel = [&](auto&& fn) {
+  std::vector<Scratch> scratch(nthreads + 4);
+  auto parallel_from = [&](long long first, auto&& fn) {
     std::vector<std::thread> th;
     for (int w = 0; w < nthreads; ++w)
       th.emplace_back([&, w] {
-        for (long long k = w; k < comps; k += nthreads) fn(k);
+        for (long long k = first + w; k < comps; k += nthreads) fn(k, scratch[w]);
       });
     for (auto& t : th) t.join();
   };
-  parallel([&](long long k) { Xv[k] = value_of(k); });
+  auto parallel = [&](auto&& fn) { parallel_from(0, fn); };
+  // The denominators of a few components, reconstructed concurrently with
+  // the remaining components' values, give the common denominator D: their
+  // lcm divides det A, and a factor cancelled in one component's fraction
+  // rarely cancels in all of them.
+  const long long sample = std::min<long long>(comps, std::max(1, std::min(4, nthreads / 2)));
+  for (long long k = 0; k < sample; ++k) Xv[k] = value_of(k, scratch[k]);
+  std::vector<big::Nat> Ds(sample);
+  std::vector<char> rec_ok(sample, 0);
+  {
+    std::vector<std::thread> th;
+    for (long long k = 0; k < sample; ++k)
+      th.emplace_back([&, k] {
+        big::Int Nk;
+        rec_ok[k] = big::rational_reconstruct(Xv[k], Pm, nbound, dbound, &Nk, &Ds[k]);
+      });
+    const int rest = std::max(1, nthreads - (int)sample);
+    for (int w = 0; w < rest; ++w)
+      th.emplace_back([&, w] {
+        for (long long k = sample + w; k < comps; k += rest) Xv[k] = value_of(k, scratch[sample + w]);
+      });
+    for (auto& t : th) t.join();
+  }
   big::Nat D = big::from_u64(1);
+  for (long long k = 0; k < sample; ++k) {
+    if (!rec_ok[k]) return RG_ERR_RANGE;
+    big::Nat t;
+    big::divmod(Ds[k], big::gcd(D, Ds[k]), &t, nullptr);
+    D = big::mul(D, t);
+  }
+  // N_k = D X_k mod P^m, balanced, for every k.  A component whose N_k
+  // exceeds the numerator bound has a denominator not dividing D: its own
+  // reconstruction extends D by the missing factor t, and the numerators
+  // already found scale by t (each stays <= |det A_k| since D still divides
+  // det A).
   std::vector<big::Int> Nv(comps);
-  bool ok = false;
-  for (int attempt = 0; attempt < 64 && !ok; ++attempt) {
-    std::vector<char> fits(comps, 1);
-    parallel([&](long long k) {
-      big::Nat y = big::mod(big::mul(D, Xv[k]), Pm);
-      big::Int v;
-      if (big::cmp(y, half) > 0) {
-        v.mag = big::sub(Pm, y);
-        v.neg = !big::is_zero(v.mag);
-      } else {
-        v.mag = y;
-      }
-      fits[k] = big::cmp(v.mag, nbound) <= 0;
-      Nv[k] = v;
-    });
-    long long bad = -1;
-    for (long long k = 0; k < comps; ++k)
-      if (!fits[k]) {
-        bad = k;
-        break;
-      }
-    if (bad < 0) {
-      ok = true;
-      break;
+  std::vector<char> fits(comps, 0);
+  auto numerator = [&](long long k, Scratch& S) {
+    big::mul_into(D.v.data(), D.v.size(), Xv[k].v.data(), Xv[k].v.size(), S.prod);
+    big::Nat y;
+    big::reduce(red, S.prod.data(), S.prod.size(), S.un, &y);
+    big::Int v;
+    if (big::cmp(y, half) > 0) {
+      v.mag = big::sub(Pm, y);
+      v.neg = !big::is_zero(v.mag);
+    } else {
+      v.mag = y;
     }
-    // the denominator of component `bad` joins the common one
+    fits[k] = big::cmp(v.mag, nbound) <= 0;
+    Nv[k] = v;
+  };
+  parallel(numerator);
+  for (long long k = 0; k < comps; ++k) {
+    if (fits[k]) continue;
     big::Int Nk;
     big::Nat Dk;
-    if (!big::rational_reconstruct(Xv[bad], Pm, nbound, dbound, &Nk, &Dk)) return RG_ERR_RANGE;
-    const big::Nat g = big::gcd(D, Dk);
-    big::Nat Dk_g;
-    big::divmod(Dk, g, &Dk_g, nullptr);
-    D = big::mul(D, Dk_g);
+    if (!big::rational_reconstruct(Xv[k], Pm, nbound, dbound, &Nk, &Dk)) return RG_ERR_RANGE;
+    big::Nat t;
+    big::divmod(Dk, big::gcd(D, Dk), &t, nullptr);
+    D = big::mul(D, t);
+    for (long long j = 0; j < k; ++j) Nv[j] = big::mul(Nv[j], t);
+    parallel_from(k, numerator);  // the rest, against the new D
+    if (!fits[k]) return RG_ERR_RANGE;
   }
-  if (!ok) return RG_ERR_RANGE;
   // the numerators and the denominator as limbs
   size_t maxbits = big::bit_length(D);
   for (const auto& v : Nv) maxbits = std::max(maxbits, big::bit_length(v.mag));
@@ -631,6 +685,8 @@ extern "C" int rg_solve_i64(const int64_t* A_in, const int64_t* B_in, int64_t n6
   out->limbs = limbs;
   out->steps = steps;
   out->primes = E;
+  out->ms_inverse = ms_inverse;
+  out->ms_lift = ms_lift;
   out->values = new int64_t[(size_t)(comps + 1) * limbs];
   for (long long k = 0; k < comps; ++k)
     if (!big::to_limbs(Nv[k], out->values + (size_t)k * limbs, limbs)) {
@@ -643,6 +699,7 @@ extern "C" int rg_solve_i64(const int64_t* A_in, const int64_t* B_in, int64_t n6
     rg_solution_free(out);
     return RG_ERR_RANGE;
   }
+  out->ms_reconstruct = ms_since(t2);
   return RG_OK;
 }
 

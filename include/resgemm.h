@@ -331,6 +331,9 @@ typedef struct {
   int64_t* values;  /* (n * c + 1) * limbs: the numerators row-major, then d */
   int64_t steps;    /* lift steps m */
   int primes;       /* primes in the lift modulus P */
+  double ms_inverse;      /* wall time of the batched inverse (incl. norms and range check) */
+  double ms_lift;         /* wall time of the lift, digits copied to the host */
+  double ms_reconstruct;  /* wall time of the host reconstruction */
 } rg_solution;
 int rg_solve_i64(const int64_t* A, const int64_t* B, int64_t n, int64_t c, unsigned flags, void* stream,
                  rg_solution* out);

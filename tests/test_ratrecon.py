@@ -48,3 +48,19 @@ def test_no_fraction_within_the_bounds(lib):
     rng = random.Random(5)
     n, d, m, x = planted(rng, 60, 60, 127)
     assert lib.rational_reconstruct(x, m, 10, 10) is None
+
+
+def test_many_sizes_around_the_lehmer_boundary(lib):
+    """Moduli from 65 to 5000 bits, bounds from 0 to half the modulus: the leading-digit
+    batches and the single-step tail must together stop at the first small remainder."""
+    rng = random.Random(11)
+    for _ in range(300):
+        mbits = rng.randrange(65, 5000)
+        nbits = rng.randrange(0, mbits // 2)
+        dbits = rng.randrange(0, mbits - nbits - 2)
+        n, d, m, x = planted(rng, max(nbits, 1), max(dbits, 1), mbits)
+        r = lib.rational_reconstruct(x, m, nbits, dbits)
+        if abs(n) <= 2**nbits and d <= 2**dbits:
+            assert r == (n, d)
+        else:
+            assert r is None or (abs(r[0]) <= 2**nbits and 0 < r[1] <= 2**dbits and (r[1] * x - r[0]) % m == 0)

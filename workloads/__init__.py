@@ -97,3 +97,13 @@ def sample_rows(M, seed, n=64):
     """Seeded distinct row indices used to check large outputs row by row."""
     rng = np.random.default_rng(seed + 1000)
     return np.sort(rng.choice(M, size=min(n, M), replace=False)).astype(np.int64)
+
+
+def solve_system(n, c=1, bits=24, seed=6):
+    """A [n, n] and b [n, c] int64 with entries uniform in [-2^(bits-1), 2^(bits-1)): the
+    "exact-solve" page's measured systems (24-bit integer entries), seeded."""
+    rng = np.random.default_rng(seed + n)
+    A = rng.integers(-(2 ** (bits - 1)), 2 ** (bits - 1), size=(n, n), dtype=np.int64)
+    b = rng.integers(-(2 ** (bits - 1)), 2 ** (bits - 1), size=(n, c), dtype=np.int64)
+    return A, b
+
