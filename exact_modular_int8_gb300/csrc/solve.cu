@@ -228,20 +228,26 @@ struct PrimeMap {
   int idx[kNumPrimes];
 };
 
-__global__ void __launch_bounds__(256) gj_finish_kernel(const uint8_t* __restrict__ M, const int* __restrict__ perm,
-                                                        int n, int nE, PrimeMap map, int8_t* __restrict__ Binv) {
-  extern __shared__ int sigma[];
-  const int s = blockIdx.y, p = map.idx[s];
-  if (threadIdx.x == 0) {
-    for (int j = 0; j < nE; ++j) sigma[j] = j;
+// sigma[s] = the column order that undoes prime map[s]'s row swaps (the
+// swaps applied to the identity in reverse order); one block per prime.
+__global__ void gj_sigma_kernel(const int* __restrict__ perm, int nE, PrimeMap map, int* __restrict__ sigma_all) {
+  const int s = blockIdx.x, p = map.idx[s];
+  int* sigma = sigma_all + (long long)s * nE;
+  for (int j = threadIdx.x; j < nE; j += blockDim.x) sigma[j] = j;
+  __syncthreads();
+  if (threadIdx.x == 0)
     for (int k = nE - 1; k >= 0; --k) {
       const int r = perm[p * nE + k];
       const int t = sigma[k];
       sigma[k] = sigma[r];
       sigma[r] = t;
     }
-  }
-  __syncthreads();
+}
+
+__global__ void __launch_bounds__(256) gj_finish_kernel(const uint8_t* __restrict__ M, const int* __restrict__ sigma_all,
+                                                        int n, int nE, PrimeMap map, int8_t* __restrict__ Binv) {
+  const int s = blockIdx.y, p = map.idx[s];
+  const int* sigma = sigma_all + (long long)s * nE;
   const long long nn = (long long)nE * nE;
   const int q = c_all.q[p], h = (q - 1) / 2;
   for (long long e = (long long)blockIdx.x * blockDim.x + threadIdx.x; e < (long long)n * nE;
@@ -260,21 +266,22 @@ __global__ void __launch_bounds__(256) gj_finish_kernel(const uint8_t* __restric
 // The lift ("exact-solve", Method: Dixon's lift on the residue engine).
 // ---------------------------------------------------------------------------
 
-// Rr[s][t][k] = bal(R[k][t] mod q_s) (int8), rows of length ld (zero padded).
-__global__ void __launch_bounds__(256) lift_residue_kernel(const int64_t* __restrict__ R, int n, int c, int ld, int E,
+// Rr[s][t][k] = bal(R[k][t] mod q_s) (int8), rows of length ld (zero
+// padded); one thread per (entry, prime), the prime index s = blockIdx.y
+// uniform across the block.
+__global__ void __launch_bounds__(256) lift_residue_kernel(const int64_t* __restrict__ R, int n, int c, int ld,
                                                            int8_t* __restrict__ Rr) {
   wait_for_predecessor();
+  const int s = blockIdx.y;
   for (long long e = (long long)blockIdx.x * blockDim.x + threadIdx.x; e < (long long)c * ld;
        e += (long long)gridDim.x * blockDim.x) {
     const int t = (int)(e / ld), k = (int)(e - (long long)t * ld);
     const long long x = k < n ? R[(long long)k * c + t] : 0;
     const unsigned long long u = (unsigned long long)x;
-    for (int s = 0; s < E; ++s) {
-      int acc = x < 0 ? -c_sol.wword[s][2] : 0;
-      asm("dp4a.u32.s32 %0, %1, %2, %0;" : "+r"(acc) : "r"((uint32_t)u), "r"(c_sol.wbyte[s][0]));
-      asm("dp4a.u32.s32 %0, %1, %2, %0;" : "+r"(acc) : "r"((uint32_t)(u >> 32)), "r"(c_sol.wbyte[s][1]));
-      Rr[((long long)s * c + t) * ld + k] = (int8_t)bal_mod_small(int_to_float_exact(acc), c_sol.qf[s], c_sol.invq[s]);
-    }
+    int acc = x < 0 ? -c_sol.wword[s][2] : 0;
+    asm("dp4a.u32.s32 %0, %1, %2, %0;" : "+r"(acc) : "r"((uint32_t)u), "r"(c_sol.wbyte[s][0]));
+    asm("dp4a.u32.s32 %0, %1, %2, %0;" : "+r"(acc) : "r"((uint32_t)(u >> 32)), "r"(c_sol.wbyte[s][1]));
+    Rr[((long long)s * c + t) * ld + k] = (int8_t)bal_mod_small(int_to_float_exact(acc), c_sol.qf[s], c_sol.invq[s]);
   }
   allow_dependents();
 }
@@ -517,10 +524,14 @@ extern "C" int rg_solve_i64(const int64_t* A_in, const int64_t* B_in, int64_t n6
   Tables sol;
   build_tables_for(qs.data(), E, &sol);
   SOLVE_TRY(cudaMemcpyToSymbolAsync(c_sol, &sol, sizeof(Tables), 0, cudaMemcpyHostToDevice, st));
-  DevBuf dBinv;
+  DevBuf dBinv, dsigma;
   SOLVE_TRY(dBinv.alloc((size_t)E * n * ld, st));
+  SOLVE_TRY(dsigma.alloc((size_t)E * nE * 4, st));
   int8_t* Binv = static_cast<int8_t*>(dBinv.p);
-  gj_finish_kernel<<<dim3(grid_for((long long)n * ld), E), 256, (size_t)nE * 4, st>>>(M, perm, n, nE, map, Binv);
+  int* sigma = static_cast<int*>(dsigma.p);
+  gj_sigma_kernel<<<E, 256, 0, st>>>(perm, nE, map, sigma);
+  SOLVE_TRY(cudaGetLastError());
+  gj_finish_kernel<<<dim3(grid_for((long long)n * ld), E), 256, 0, st>>>(M, sigma, n, nE, map, Binv);
   SOLVE_TRY(cudaGetLastError());
 
   // 3. the lift
@@ -547,8 +558,9 @@ extern "C" int rg_solve_i64(const int64_t* A_in, const int64_t* B_in, int64_t n6
   SOLVE_TRY(cudaMemcpyAsync(R, B, (size_t)n * c * 8, cudaMemcpyDeviceToDevice, st));
   uint32_t* X = static_cast<uint32_t*>(dX.p);
   for (int i = 0; i < steps; ++i) {
-    SOLVE_TRY(launch_dependent(lift_residue_kernel, dim3(grid_for((long long)c * ld)), dim3(256), 0, st,
-                               (const int64_t*)R, n, c, ld, E, static_cast<int8_t*>(dRr.p)));
+    SOLVE_TRY(launch_dependent(lift_residue_kernel,
+                               dim3(std::max(1u, std::min((unsigned)(((long long)c * ld + 255) / 256), 64u)), E),
+                               dim3(256), 0, st, (const int64_t*)R, n, c, ld, static_cast<int8_t*>(dRr.p)));
     SOLVE_TRY(launch_dependent(lift_gemv_kernel, dim3((unsigned)(((long long)E * n * 32 + 255) / 256)), dim3(256), 0,
                                st, (const int8_t*)Binv, (const int8_t*)dRr.p, n, c, ld, E,
                                static_cast<uint8_t*>(dRC.p)));
