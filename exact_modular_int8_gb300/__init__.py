@@ -53,7 +53,7 @@ EXPORTED = (
     "res_gemm_i64_batched", "res_gemm_limbs_batched", "enclose_gemm_f64_batched", "rg_workspace_bytes_batched",
     "rg_workspace_layout_batched", "enclose_gemm_f32", "enclose_gemm_f32_batched", "interval_gemm_f64",
     "interval_gemm_f32", "interval_gemm_f64_batched", "interval_gemm_f32_batched", "rg_solve_i64",
-    "rg_solution_free", "rg_rational_reconstruct",
+    "rg_solution_free", "rg_rational_reconstruct", "rg_set_crt_mode",
 )
 
 
@@ -73,7 +73,7 @@ class Layout(ctypes.Structure):
 class PlanInfo(ctypes.Structure):
     _fields_ = [("status", ctypes.c_int), ("nprimes", ctypes.c_int), ("bits_a", ctypes.c_int),
                 ("bits_b", ctypes.c_int), ("bound_bits", ctypes.c_int), ("f_a", ctypes.c_int),
-                ("f_b", ctypes.c_int), ("lossless", ctypes.c_int), ("splits", ctypes.c_int)]
+                ("f_b", ctypes.c_int), ("lossless", ctypes.c_int), ("splits", ctypes.c_int), ("crt_rn", ctypes.c_int)]
 
     def as_dict(self):
         return {k: getattr(self, k) for k, _ in self._fields_}
@@ -141,6 +141,8 @@ def library():
             lib.rg_inject_fault.restype = None
             lib.rg_set_gemm_variant.argtypes = [ci]
             lib.rg_set_gemm_variant.restype = ci
+            lib.rg_set_crt_mode.argtypes = [ci]
+            lib.rg_set_crt_mode.restype = ci
             lib.rg_solve_i64.argtypes = [vp, vp, i64, i64, cu, vp, ctypes.POINTER(Solution)]
             lib.rg_solve_i64.restype = ci
             lib.rg_solution_free.argtypes = [ctypes.POINTER(Solution)]

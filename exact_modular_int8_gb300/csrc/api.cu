@@ -371,6 +371,7 @@ int rg_get_plan(const void* ws, void* stream, rg_plan_info* out) {
   out->f_b = p.f_b;
   out->lossless = p.lossless;
   out->splits = p.splits > 0 ? p.splits : 1;
+  out->crt_rn = p.crt_rn;
   return RG_OK;
 }
 

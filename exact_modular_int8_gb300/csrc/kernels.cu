@@ -8,6 +8,7 @@
 #include <cuda_fp16.h>
 
 #include <cstdint>
+#include <atomic>
 #include <mutex>
 
 #include "rg_common.cuh"
@@ -112,10 +113,11 @@ struct PlanArgs {
   int op;
   long long K;
   int nprimes_fixed, la, lb, lc;
+  int allow_rn;  // the wide outputs may use round-to-nearest CRT
 };
 
 struct LocalPlan {
-  int status, P, bits_a, bits_b, T, f_a, f_b, lossless, nword_a, nword_b;
+  int status, P, bits_a, bits_b, T, f_a, f_b, lossless, nword_a, nword_b, crt_rn;
 };
 
 __device__ int primes_for_bound(int T) {  // fewest primes with P > 2^(T+1); 0 if none
@@ -198,7 +200,21 @@ __device__ LocalPlan finalize_plan(DevPlan* plan, const PlanArgs& a) {
     p.lossless = ba == bits_a0 && bb == bits_b0;
   }
   if (p.status) return p;
-  p.P = a.nprimes_fixed ? a.nprimes_fixed : primes_for_bound(p.T);
+  if (a.nprimes_fixed) {
+    p.P = a.nprimes_fixed;
+  } else {
+    p.P = primes_for_bound(p.T);
+    // on request the wide outputs reconstruct by round-to-nearest CRT, which
+    // wants one more bit of headroom (P > 4 |x|); where 53 primes cannot give
+    // it, balanced Garner reconstructs from the usual prime count
+    if (a.op != RG_OP_I64 && a.allow_rn) {
+      const int prn = primes_for_bound(p.T + 1);
+      if (prn) {
+        p.P = prn;
+        p.crt_rn = 1;
+      }
+    }
+  }
   if (p.P == 0) p.status = RG_ERR_RANGE;
   return p;
 }
@@ -225,6 +241,7 @@ __device__ void planner_finish(DevPlan* plan, const PlanArgs& a) {
     plan->lossless = lp.lossless;
     plan->nword_a = lp.nword_a;
     plan->nword_b = lp.nword_b;
+    plan->crt_rn = lp.crt_rn;
     if (lp.status) set_status(&plan->status, lp.status);
   }
   __syncthreads();
@@ -876,16 +893,22 @@ __global__ void __launch_bounds__(128) garner_int_kernel(const uint8_t* __restri
                                                          long long plane, long long M, long long N, DevPlan* plan,
                                                          int64_t* __restrict__ C) {
   constexpr int W = 2 * LC, GE = GarnerGE<W>::value;
+  __shared__ CrtRn crt;
   wait_for_predecessor();
   if (plan->status) return;
   const int P = plan->P;
+  const bool rn = plan->crt_rn != 0;
+  if (rn) crt_rn_tables<MainTab>(crt, P);
   const long long per_row = (N + GE - 1) / GE;
   const long long item = (long long)blockIdx.x * blockDim.x + threadIdx.x;
   if (item >= M * per_row) return;
   const long long m = item / per_row;
   const long long n0 = (item - m * per_row) * GE;
   uint32_t x[GE][W];
-  garner_reconstruct<W, GE, MainTab>(RC + m * ldc + n0, plane, P, x);
+  if (rn)
+    crt_rn_reconstruct<W, GE, MainTab>(RC + m * ldc + n0, plane, P, crt, x);
+  else
+    garner_reconstruct<W, GE, MainTab>(RC + m * ldc + n0, plane, P, x);
   int64_t* out = C + (m * N + n0) * LC;
   if (n0 + GE <= N && ((reinterpret_cast<uintptr_t>(out) & 15u) == 0)) {
     // GE * LC consecutive int64: 16-byte stores
@@ -1004,17 +1027,23 @@ __global__ void __launch_bounds__(128) garner_enclose_kernel(const uint8_t* __re
                                                              Bits* __restrict__ hi) {
   constexpr int GE = GarnerGE<kEncW>::value;
   static_assert(GE == 2, "the bound stores below write GE entries as one vector");
+  __shared__ CrtRn crt;
   wait_for_predecessor();
   if (plan->status) return;
   const int P = plan->P;
   const int Q = plan->f_a + plan->f_b;
+  const bool rn = plan->crt_rn != 0;
+  if (rn) crt_rn_tables<MainTab>(crt, P);
   const long long per_row = (N + GE - 1) / GE;
   const long long item = (long long)blockIdx.x * blockDim.x + threadIdx.x;
   if (item >= M * per_row) return;
   const long long m = item / per_row;
   const long long n0 = (item - m * per_row) * GE;
   uint32_t x[GE][kEncW];
-  garner_reconstruct<kEncW, GE, MainTab>(RC + m * ldc + n0, plane, P, x);
+  if (rn)
+    crt_rn_reconstruct<kEncW, GE, MainTab>(RC + m * ldc + n0, plane, P, crt, x);
+  else
+    garner_reconstruct<kEncW, GE, MainTab>(RC + m * ldc + n0, plane, P, x);
   Bits l[GE], h[GE];
   if (plan->lossless) {
 #pragma unroll
@@ -1089,22 +1118,31 @@ __global__ void __launch_bounds__(128) garner_interval_kernel(const uint8_t* __r
                                                               long long N, long long K, DevPlan* plan,
                                                               Bits* __restrict__ lo, Bits* __restrict__ hi) {
   constexpr int GE = 1;
+  __shared__ CrtRn crt;
   wait_for_predecessor();
   if (plan->status) return;
   const int P = plan->P;
   const int Q = plan->f_a + plan->f_b;
+  const bool rn = plan->crt_rn != 0;
+  if (rn) crt_rn_tables<MainTab>(crt, P);
   const long long item = (long long)blockIdx.x * blockDim.x + threadIdx.x;
   if (item >= M * N) return;
   const long long m = item / N, n = item - m * N;
   const uint8_t* base = RC + m * ldc + n;
+  auto reconstruct = [&](const uint8_t* at, uint32_t (&v)[GE][kEncW]) {
+    if (rn)
+      crt_rn_reconstruct<kEncW, GE, MainTab>(at, plane, P, crt, v);
+    else
+      garner_reconstruct<kEncW, GE, MainTab>(at, plane, P, v);
+  };
   uint32_t x[GE][kEncW], xl[kEncW], xh[kEncW];
-  garner_reconstruct<kEncW, GE, MainTab>(base, plane, P, x);
+  reconstruct(base, x);
 #pragma unroll
   for (int k = 0; k < kEncW; ++k) xl[k] = xh[k] = x[0][k];
-  garner_reconstruct<kEncW, GE, MainTab>(base + sub, plane, P, x);
+  reconstruct(base + sub, x);
   add_words(xl, x[0], -1);
   add_words(xh, x[0], 1);
-  garner_reconstruct<kEncW, GE, MainTab>(base + 2 * sub, plane, P, x);
+  reconstruct(base + 2 * sub, x);
   add_words(xl, x[0], -1);
   add_words(xh, x[0], 1);
   if (!plan->lossless) {
@@ -1124,6 +1162,7 @@ __global__ void __launch_bounds__(128) garner_interval_kernel(const uint8_t* __r
 }
 
 int g_sm_count[64];
+std::atomic<int> g_crt_mode{0};  // 0: balanced Garner, 1: round-to-nearest CRT where the plan allows
 
 int sm_count() {
   int dev = 0;
@@ -1178,7 +1217,7 @@ static int planner_blocks(long long n) {
 
 cudaError_t launch_plan(int op, const void* A, const void* A2, long long nA, int la, const void* B, const void* B2,
                         long long nB, int lb, int lc, long long K, int nprimes_fixed, DevPlan* plan, cudaStream_t s) {
-  PlanArgs pa{op, K, nprimes_fixed, la, lb, lc};
+  PlanArgs pa{op, K, nprimes_fixed, la, lb, lc, g_crt_mode.load() == 1 ? 1 : 0};
   if (nprimes_fixed) nA = nB = 0;  // only the finalisation is needed
   const int ba = planner_blocks(nA), bb = planner_blocks(nB);
   if (op == RG_OP_I64)
@@ -1317,3 +1356,8 @@ cudaError_t launch_garner(int op, const void* RC, long long ldc, long long plane
 }
 
 }  // namespace rg
+
+extern "C" int rg_set_crt_mode(int mode) {
+  if (mode < 0 || mode > 1) return -1;
+  return rg::g_crt_mode.exchange(mode);
+}

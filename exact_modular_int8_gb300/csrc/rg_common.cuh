@@ -31,7 +31,8 @@ struct DevPlan {
   int nword_a, nword_b;   // 32-bit words the split reads per integer entry (0: the entry is an exact fp32)
   unsigned blocks_done;   // planner blocks finished (the last one derives the plan)
   int splits;             // K slices the GEMM used (1: none)
-  int pad0[4];
+  int crt_rn;             // 1: reconstruct by round-to-nearest CRT (P > 4 |x| guaranteed), 0: balanced Garner
+  int pad0[3];
   // reductions written by the planner kernels
   unsigned long long maxmag_a, maxmag_b;  // int64 operands: max |x|
   int maxbits_a, maxbits_b;               // limb operands: max bit length of |x|

@@ -140,3 +140,141 @@ __device__ __forceinline__ void garner_reconstruct(const uint8_t* __restrict__ r
 
 }  // namespace
 }  // namespace rg
+
+namespace rg {
+namespace {
+
+// ---------------------------------------------------------------------------
+// CRT with a round-to-nearest quotient ("Accelerating Multiple-Precision LU
+// Decomposition with Ozaki Scheme II", CRT reconstruction of the centred
+// representative by round-to-nearest).  With M_i = P / q_i and
+// y_i = bal(M_i^-1 mod q_i), the digits s_i = bal(r_i y_i mod q_i) give
+// S = sum_i s_i M_i == x (mod P), and S / P = sum_i s_i / q_i = k + x / P.
+// When |x| < P / 4 the quotient k is the nearest integer to the fp32 sum of
+// s_i / q_i (|s_i / q_i| <= 1/2, so 53 terms carry an error far below 1/4),
+// and x = S - k P exactly.  O(P W) work per output instead of Garner's O(P^2);
+// S and k P are formed modulo 2^(32 W), which holds x.
+// ---------------------------------------------------------------------------
+constexpr int kCrtWords = 11;   // P < 2^334
+constexpr int kCrtStride = 12;  // words per table row (16-byte aligned rows)
+
+struct CrtRn {
+  uint32_t M[kNumPrimes][kCrtStride];  // M_i = P / q_i
+  uint32_t Pw[kCrtStride];             // P
+  uint32_t Cw[kCrtStride];             // 128 * sum_i M_i (the digits are summed offset by +128)
+  float y[kNumPrimes];                 // bal(M_i^-1 mod q_i)
+};
+
+// Block-wide: the tables for the first P primes of TAB.  Ends with a barrier.
+template <typename TAB>
+__device__ __forceinline__ void crt_rn_tables(CrtRn& T, int P) {
+  for (int i = threadIdx.x; i <= P; i += blockDim.x) {
+    uint32_t w[kCrtWords];
+#pragma unroll
+    for (int k = 0; k < kCrtWords; ++k) w[k] = k == 0 ? 1u : 0u;
+    const int qi = i < P ? TAB::t().q[i] : 1;
+    int mmod = 1;  // M_i mod q_i
+    for (int j = 0; j < P; ++j) {
+      if (j == i) continue;
+      const uint32_t qj = (uint32_t)TAB::t().q[j];
+      unsigned long long carry = 0;
+#pragma unroll
+      for (int k = 0; k < kCrtWords; ++k) {
+        const unsigned long long t = (unsigned long long)w[k] * qj + carry;
+        w[k] = (uint32_t)t;
+        carry = t >> 32;
+      }
+      if (i < P) mmod = mmod * (int)(qj % (uint32_t)qi) % qi;
+    }
+    uint32_t* dst = i < P ? T.M[i] : T.Pw;
+#pragma unroll
+    for (int k = 0; k < kCrtStride; ++k) dst[k] = k < kCrtWords ? w[k] : 0u;
+    if (i < P) {
+      int inv = 1, b = mmod, e = qi - 2;  // Fermat: mmod^(q-2)
+      while (e) {
+        if (e & 1) inv = inv * b % qi;
+        b = b * b % qi;
+        e >>= 1;
+      }
+      T.y[i] = (float)(inv > (qi - 1) / 2 ? inv - qi : inv);
+    }
+  }
+  __syncthreads();
+  if (threadIdx.x == 0) {  // 128 * sum_i M_i, normalised to 32-bit words
+    unsigned long long carry = 0;
+    for (int k = 0; k < kCrtWords; ++k) {
+      unsigned long long t = carry;
+      for (int i = 0; i < P; ++i) t += (unsigned long long)T.M[i][k] << 7;
+      T.Cw[k] = (uint32_t)t;
+      carry = t >> 32;
+    }
+    T.Cw[kCrtWords] = 0;
+  }
+  __syncthreads();
+}
+
+// x[e] (W words, two's complement) = the centred integers of the GE residue
+// vectors (residues in [0, q)) starting at rc, plane bytes apart.
+template <int W, int GE, typename TAB>
+__device__ __forceinline__ void crt_rn_reconstruct(const uint8_t* __restrict__ rc, long long plane, int P,
+                                                   const CrtRn& T, uint32_t (&x)[GE][W]) {
+  constexpr int NW = W < kCrtWords ? W : kCrtWords;  // words that can differ from the sign
+  static_assert(GE == 1 || GE == 2 || GE == 4, "one, two or four adjacent entries");
+  unsigned long long acc[GE][NW];  // sum_i (s_i + 128) M_i, words not yet normalised (< 2^46)
+  float kf[GE];
+#pragma unroll
+  for (int e = 0; e < GE; ++e) {
+    kf[e] = 0.0f;
+#pragma unroll
+    for (int w = 0; w < NW; ++w) acc[e][w] = 0;
+  }
+#pragma unroll 1
+  for (int i0 = 0; i0 < P; i0 += kGarnerBatch) {
+    uint32_t rw[kGarnerBatch];
+#pragma unroll
+    for (int j = 0; j < kGarnerBatch; ++j) {
+      const int i = i0 + j;
+      if constexpr (GE == 4)
+        rw[j] = (i < P) ? __ldg(reinterpret_cast<const uint32_t*>(rc + (long long)i * plane)) : 0u;
+      else if constexpr (GE == 2)
+        rw[j] = (i < P) ? (uint32_t)__ldg(reinterpret_cast<const unsigned short*>(rc + (long long)i * plane)) : 0u;
+      else
+        rw[j] = (i < P) ? (uint32_t)__ldg(rc + (long long)i * plane) : 0u;
+    }
+#pragma unroll
+    for (int j = 0; j < kGarnerBatch; ++j) {
+      const int i = i0 + j;
+      if (i >= P) break;
+      const float q = TAB::t().qf[i], iq = TAB::t().invq[i], y = T.y[i];
+      uint32_t m[NW];
+#pragma unroll
+      for (int w = 0; w < NW; ++w) m[w] = T.M[i][w];
+#pragma unroll
+      for (int e = 0; e < GE; ++e) {
+        const float r = int_to_float_exact((int)((rw[j] >> (8 * e)) & 0xFFu));
+        const float s = bal_mod_small(r * y, q, iq);  // |r y| <= 250 * 125
+        kf[e] = __fmaf_rn(s, iq, kf[e]);
+        const uint32_t sp = (uint32_t)(float_bits_offset(s) - kMagicBits + 128);  // s + 128 in [3, 253]
+#pragma unroll
+        for (int w = 0; w < NW; ++w) acc[e][w] += (unsigned long long)sp * m[w];
+      }
+    }
+  }
+#pragma unroll
+  for (int e = 0; e < GE; ++e) {
+    const long long k = (long long)(float_bits_offset(kf[e]) - kMagicBits);  // nearest integer (|k| <= 27)
+    long long carry = 0;
+#pragma unroll
+    for (int w = 0; w < NW; ++w) {
+      const long long t = (long long)acc[e][w] - (long long)T.Cw[w] - k * (long long)T.Pw[w] + carry;
+      x[e][w] = (uint32_t)t;
+      carry = t >> 32;  // arithmetic shift: the next word's borrow or carry
+    }
+    const uint32_t sign = (uint32_t)((int)x[e][NW - 1] >> 31);
+#pragma unroll
+    for (int w = NW; w < W; ++w) x[e][w] = sign;
+  }
+}
+
+}  // namespace
+}  // namespace rg

@@ -297,6 +297,7 @@ typedef struct {
   int f_b;
   int lossless; /* fp64 only: 1 if both operands scaled exactly */
   int splits;   /* K slices the per-prime GEMM used (1: none; more when there were too few output tiles) */
+  int crt_rn;   /* 1: reconstructed by round-to-nearest CRT (the plan kept P > 4 |result|); 0: balanced Garner */
 } rg_plan_info;
 int rg_get_plan(const void* ws, void* stream, rg_plan_info* out);
 
@@ -349,6 +350,16 @@ void rg_solution_free(rg_solution* s);
  */
 int rg_rational_reconstruct(const int64_t* x, int xl, const int64_t* m, int ml, int nbits, int dbits, int64_t* num,
                             int64_t* den, int limbs);
+
+/* Reconstruction of the wide outputs (limbs, enclosures, intervals): 0 =
+ * balanced Garner (the default), 1 = CRT by round-to-nearest quotient
+ * ("Accelerating Multiple-Precision LU Decomposition with Ozaki Scheme II")
+ * where the plan can keep P > 4 |result| (one more bit of headroom, so
+ * sometimes one more prime), Garner otherwise.  On GB300 the second takes
+ * about twice as long for 38 primes, so it is not the default.  Returns the
+ * previous mode, or -1 for an invalid one.  The int64 path always uses
+ * Garner. */
+int rg_set_crt_mode(int mode);
 
 /* Synchronise `stream` and return the device status of the last call that
  * used `ws` (RG_OK, RG_ERR_RANGE, RG_ERR_NONFINITE, RG_ERR_LOSSY,
