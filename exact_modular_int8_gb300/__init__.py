@@ -53,7 +53,7 @@ EXPORTED = (
     "res_gemm_i64_batched", "res_gemm_limbs_batched", "enclose_gemm_f64_batched", "rg_workspace_bytes_batched",
     "rg_workspace_layout_batched", "enclose_gemm_f32", "enclose_gemm_f32_batched", "interval_gemm_f64",
     "interval_gemm_f32", "interval_gemm_f64_batched", "interval_gemm_f32_batched", "rg_solve_i64",
-    "rg_solution_free", "rg_rational_reconstruct", "rg_set_crt_mode",
+    "rg_solution_free", "rg_rational_reconstruct", "rg_set_crt_mode", "rg_set_stage_events",
 )
 
 
@@ -149,6 +149,8 @@ def library():
             lib.rg_solution_free.restype = None
             lib.rg_rational_reconstruct.argtypes = [vp, ci, vp, ci, ci, ci, vp, vp, ci]
             lib.rg_rational_reconstruct.restype = ci
+            lib.rg_set_stage_events.argtypes = [ctypes.POINTER(ctypes.c_void_p), ci]
+            lib.rg_set_stage_events.restype = ci
             _lib = lib
     return _lib
 
@@ -440,6 +442,24 @@ def get_plan(ws: torch.Tensor | None = None, device=None) -> dict:
         _check(library().rg_get_plan(w.data_ptr(), torch.cuda.current_stream(dev).cuda_stream, ctypes.byref(info)),
                "rg_get_plan")
     return info.as_dict()
+
+
+def set_stage_events(events) -> None:
+    """Record four CUDA events around the stages of every later call (before
+    the first kernel, before and after the GEMM, after the reconstruction);
+    None removes the hook.  `events` are torch.cuda.Event objects (timing
+    enabled) that stay alive while the hook is set."""
+    lib = library()
+    if events is None:
+        _check(lib.rg_set_stage_events(None, 0), "rg_set_stage_events")
+        return
+    evs = list(events)
+    if len(evs) != 4:
+        raise ValueError("four events expected")
+    for e in evs:
+        e.record()  # creates the CUDA event behind a lazily created torch event
+    arr = (ctypes.c_void_p * 4)(*[e.cuda_event for e in evs])
+    _check(lib.rg_set_stage_events(arr, 4), "rg_set_stage_events")
 
 
 def status(ws: torch.Tensor | None = None, device=None) -> int:

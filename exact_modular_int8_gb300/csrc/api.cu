@@ -21,6 +21,16 @@ constexpr size_t kAlign = 4096;
 
 std::atomic<unsigned long long> g_wait_ns{1000000000ull};
 std::atomic<int> g_fault{0};
+// Stage timing events (rg_set_stage_events): recorded on the call's stream
+// before the first kernel, before the GEMM, after the GEMM and after Garner.
+std::mutex g_ev_mu;
+cudaEvent_t g_ev[4] = {nullptr, nullptr, nullptr, nullptr};
+bool g_ev_on = false;
+
+cudaError_t record_stage(int i, cudaStream_t s) {
+  std::lock_guard<std::mutex> lk(g_ev_mu);
+  return g_ev_on ? cudaEventRecord(g_ev[i], s) : cudaSuccess;
+}
 
 size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 long long round_up(long long x, long long a) { return (x + a - 1) / a * a; }
@@ -209,6 +219,7 @@ int run(int op, const void* A, const void* A2, int la, const void* B, const void
   // int64: the split reduces max |A|, max |B| itself and the GEMM derives the
   // plan; the other operations run the planner kernel first
   const bool i64 = op == RG_OP_I64;
+  RG_TRY(record_stage(0, s));
   if (!i64)
     RG_TRY(launch_plan(op, dA, dA2, batch * M * K, la1, dB, dB2, batch * K * N, lb1, lc1, K,
                        is_enclose(op) ? 0 : nprimes, plan, s));
@@ -216,13 +227,16 @@ int run(int op, const void* A, const void* A2, int la, const void* B, const void
   RG_TRY(launch_split(op, dA, dA2, dB, dB2, la1, lb1, batch, M, N, K, L.lda, L.ldb, w + L.ra, w + L.rb, plan, L.pmax,
                       transb, s));
   int fault = g_fault.exchange(0);
+  RG_TRY(record_stage(1, s));
   RG_TRY(launch_gemm(w + L.ra, L.lda, w + L.rb, L.ldb, w + L.rc, L.ldc, L.pmax, (int)gemm_batch, i64 ? nprimes : 0,
                      M, N, K, plan, s, fault, g_wait_ns.load(), i64, transb, L.splits));
   // Garner sees the batch as batch * M rows of each plane; an interval's
   // three product planes lie batch * M rows apart
   const long long sub = batch * M * L.ldc;
+  RG_TRY(record_stage(2, s));
   RG_TRY(launch_garner(op, w + L.rc, L.ldc, planes_per_product(op) * sub, sub, batch * M, N, K,
                        op == RG_OP_LIMBS ? lc : 1, plan, dC, dC2, s));
+  RG_TRY(record_stage(3, s));
   if (flags & RG_FLAG_HOST) {
     RG_TRY(cudaMemcpyAsync(C, dC, out_bytes, cudaMemcpyDeviceToHost, s));
     if (is_enclose(op)) RG_TRY(cudaMemcpyAsync(C2, dC2, out_bytes, cudaMemcpyDeviceToHost, s));
@@ -399,6 +413,17 @@ const char* rg_strerror(int code) {
 uint64_t rg_set_wait_limit_ns(uint64_t ns) { return g_wait_ns.exchange(ns ? ns : 1000000000ull); }
 
 void rg_inject_fault(int kind) { g_fault.store(kind); }
+
+int rg_set_stage_events(void* const* events, int n) {
+  if (n != 0 && (n != 4 || !events)) return RG_ERR_ARG;
+  if (n == 4)
+    for (int i = 0; i < 4; ++i)
+      if (!events[i]) return RG_ERR_ARG;
+  std::lock_guard<std::mutex> lk(g_ev_mu);
+  for (int i = 0; i < 4; ++i) g_ev[i] = n ? static_cast<cudaEvent_t>(events[i]) : nullptr;
+  g_ev_on = n == 4;
+  return RG_OK;
+}
 
 }  // extern "C"
 

@@ -250,12 +250,19 @@ __device__ __forceinline__ float partial_residue(float x, float q, float iq) {
 __device__ __forceinline__ void final_residues(const uint32_t (&r)[32], const uint32_t (&carry)[8], bool add_carry,
                                                float q, float iq, uint32_t (&packed)[8]) {
   const float magic = 12582912.0f, two23 = 8388608.0f;
+  // One rounding suffices when |x / q| < 2^22, true for every |x| < 2^24 once
+  // q >= 5: t = rint(x fl(1/q)) is within 1/2 + 1/q of x / q, so
+  // |x - t q| < q and one conditional add gives [0, q).  For q = 3 (large
+  // unreduced residues from the stage entry point) the partial reduction
+  // runs first.
+  const bool one_round = q > 4.0f;
 #pragma unroll
   for (int w = 0; w < 8; ++w) {
     uint32_t b[4];
 #pragma unroll
     for (int k = 0; k < 4; ++k) {
-      float v = partial_residue(__uint_as_float(r[4 * w + k]), q, iq);
+      float v = __uint_as_float(r[4 * w + k]);
+      if (!one_round) v = partial_residue(v, q, iq);
       const float t = __fadd_rn(__fmaf_rn(v, iq, magic), -magic);
       v = __fmaf_rn(-t, q, v);
       v = v < 0.0f ? v + q : v;
@@ -287,6 +294,60 @@ __device__ __forceinline__ TileCoord tile_coord(int t, int mt, int nt, int batch
   c.n = r / mt;  // consecutive CTAs share a B column block
   c.m = r - c.n * mt;
   return c;
+}
+
+// After tcgen05.wait::ld: ties the loaded registers to this point, so that no
+// use of them is scheduled before the wait.
+__device__ __forceinline__ void pin32(uint32_t (&r)[32]) {
+#pragma unroll
+  for (int i = 0; i < 32; ++i) asm volatile("" : "+r"(r[i]));
+}
+
+__device__ __forceinline__ void prefetch_tmap(const CUtensorMap* m) {
+  asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(m)) : "memory");
+}
+
+
+// 32 accumulator columns (from col) of this thread's row: mode 0 writes the
+// partial residues back to tensor memory for the next chunk; modes 1 and 2
+// write residue bytes to the staging halves, mode 2 adding the bytes the
+// carry chunk left there when add_carry is set.
+__device__ __forceinline__ void reduce32(uint32_t (&r)[32], uint32_t taddr_col, int col, int row, int mode,
+                                         bool add_carry, float q, float iq, uint8_t* out_base) {
+  if (mode == 0) {
+#pragma unroll
+    for (int i = 0; i < 32; ++i) r[i] = __float_as_uint(partial_residue(__uint_as_float(r[i]), q, iq));
+    tmem_st32(taddr_col, r);
+    return;
+  }
+  const int half = col >> 7;
+  const int j0 = (col & 127) >> 4;
+  uint8_t* hbase = out_base + half * OUT_HALF;
+  uint4* p0 = reinterpret_cast<uint4*>(hbase + sw128_off(row, j0));
+  uint4* p1 = reinterpret_cast<uint4*>(hbase + sw128_off(row, j0 + 1));
+  uint32_t carry[8] = {0, 0, 0, 0, 0, 0, 0, 0};
+  if (add_carry) {
+    const uint4 c0 = *p0, c1 = *p1;
+    carry[0] = c0.x; carry[1] = c0.y; carry[2] = c0.z; carry[3] = c0.w;
+    carry[4] = c1.x; carry[5] = c1.y; carry[6] = c1.z; carry[7] = c1.w;
+  }
+  uint32_t packed[8];
+  final_residues(r, carry, add_carry, q, iq, packed);
+  *p0 = make_uint4(packed[0], packed[1], packed[2], packed[3]);
+  *p1 = make_uint4(packed[4], packed[5], packed[6], packed[7]);
+}
+
+// This thread's 128 accumulator columns from col_begin, 32 at a time.
+__device__ __forceinline__ void drain128(uint32_t taddr, int col_begin, int row, int mode, bool add_carry, float q,
+                                         float iq, uint8_t* out_base) {
+#pragma unroll 1
+  for (int col = col_begin; col < col_begin + 128; col += 32) {
+    uint32_t r[32];
+    tmem_ld32(taddr + col, r);
+    tmem_wait_ld();
+    pin32(r);
+    reduce32(r, taddr + col, col, row, mode, add_carry, q, iq, out_base);
+  }
 }
 
 // Split-K: when there are too few tiles for the persistent CTAs, K is cut
@@ -324,6 +385,24 @@ __device__ __forceinline__ Splits choose_splits(const GemmParams& gp, int tiles,
   return Splits{best, (nkc + best - 1) / best * KC_BLOCKS};
 }
 
+// The launch's prime count and K slicing, read from the plan by thread 0 and
+// passed on through shared memory (sh, three ints): all threads of every CTA
+// reading the plan's line at once would queue thousands of L2 requests on it.
+// Ends with a block barrier.
+__device__ __forceinline__ void read_plan_once(const GemmParams& gp, DevPlan* plan, int tiles_per_prime, int workers,
+                                               int* sh, int& P, Splits& sp) {
+  if (threadIdx.x == 0) {
+    const int p = launch_primes(gp, plan);
+    const Splits s = p ? choose_splits(gp, p * tiles_per_prime, workers, plan) : Splits{1, gp.kb_total};
+    sh[0] = p;
+    sh[1] = s.S;
+    sh[2] = s.kbs;
+  }
+  __syncthreads();
+  P = sh[0];
+  sp = Splits{sh[1], sh[2]};
+}
+
 __device__ __forceinline__ Unit unit_of(int u, int tiles, int mt, int nt, int batch, const Splits& sp, int kb_total) {
   Unit r;
   r.s = u / tiles;
@@ -345,12 +424,6 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                         const __grid_constant__ CUtensorMap tmC, const __grid_constant__ GemmParams gp,
                         DevPlan* plan) {
   extern __shared__ uint8_t smem_raw[];
-  wait_for_predecessor();
-  const int P = launch_primes(gp, plan);
-  if (P == 0) return;
-  const int tiles = P * gp.batch * gp.mt * gp.nt;
-  const Splits sp = choose_splits(gp, tiles, (int)gridDim.x, plan);
-  const int total = tiles * sp.S;
 
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint8_t* stage_base = smem;
@@ -380,6 +453,9 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     mbar_init(smem_u32(drain), 1);
     *abort_flag = 0;
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    prefetch_tmap(&tmA);
+    prefetch_tmap(&tmB);
+    prefetch_tmap(&tmC);
   }
   if (warp == 1) {
     asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(tmem_slot)),
@@ -390,6 +466,17 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
+
+  // Everything above uses only this CTA's shared and tensor memory and so
+  // overlaps the predecessor's tail; the plan is read after the wait.  A call
+  // that has already failed (P = 0) gets no units and goes to the teardown.
+  wait_for_predecessor();
+  __shared__ int s_plan[3];
+  int P;
+  Splits sp;
+  read_plan_once(gp, plan, gp.batch * gp.mt * gp.nt, (int)gridDim.x, s_plan, P, sp);
+  const int tiles = P * gp.batch * gp.mt * gp.nt;
+  const int total = P ? tiles * sp.S : 0;
 
   if (warp == 0) {
     // ------------------------------------------------------------ producer
@@ -525,33 +612,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
           epilogue_bar();
           first_write = false;
         }
-#pragma unroll 1
-        for (int col = col_begin; col < col_begin + BN / 2; col += 32) {
-          uint32_t r[32];
-          tmem_ld32(taddr + col, r);
-          tmem_wait_ld();
-          if (mode == 0) {
-#pragma unroll
-            for (int i = 0; i < 32; ++i) r[i] = __float_as_uint(partial_residue(__uint_as_float(r[i]), q, iq));
-            tmem_st32(taddr + col, r);
-          } else {
-            const int half = col >> 7;
-            const int j0 = (col & 127) >> 4;
-            uint8_t* hbase = out_base + half * OUT_HALF;
-            uint4* p0 = reinterpret_cast<uint4*>(hbase + sw128_off(row, j0));
-            uint4* p1 = reinterpret_cast<uint4*>(hbase + sw128_off(row, j0 + 1));
-            uint32_t carry[8] = {0, 0, 0, 0, 0, 0, 0, 0};
-            if (mode == 2 && nc_tile >= 2) {
-              uint4 c0 = *p0, c1 = *p1;
-              carry[0] = c0.x; carry[1] = c0.y; carry[2] = c0.z; carry[3] = c0.w;
-              carry[4] = c1.x; carry[5] = c1.y; carry[6] = c1.z; carry[7] = c1.w;
-            }
-            uint32_t packed[8];
-            final_residues(r, carry, mode == 2 && nc_tile >= 2, q, iq, packed);
-            *p0 = make_uint4(packed[0], packed[1], packed[2], packed[3]);
-            *p1 = make_uint4(packed[4], packed[5], packed[6], packed[7]);
-          }
-        }
+        drain128(taddr, col_begin, row, mode, mode == 2 && nc_tile >= 2, q, iq, out_base);
         if (mode == 0) tmem_wait_st();
         tc_fence_before();
         __syncwarp();
@@ -681,13 +742,6 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                              const __grid_constant__ CUtensorMap tmC, const __grid_constant__ GemmParams gp,
                              DevPlan* plan) {
   extern __shared__ uint8_t smem_raw[];
-  wait_for_predecessor();
-  const int P = launch_primes(gp, plan);  // the same decision in both CTAs of the pair
-  if (P == 0) return;
-  const int mt2 = (gp.M + 255) / 256;
-  const int tiles = P * gp.batch * mt2 * gp.nt;
-  const Splits sp = choose_splits(gp, tiles, (int)(gridDim.x >> 1), plan);
-  const int total = tiles * sp.S;
   const uint32_t rank = cluster_rank();
   const int cid = blockIdx.x >> 1, ncl = gridDim.x >> 1;
 
@@ -719,6 +773,9 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     mbar_init(smem_u32(drain), 1);
     *abort_flag = 0;
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    prefetch_tmap(&tmA);
+    prefetch_tmap(&tmB);
+    prefetch_tmap(&tmC);
   }
   if (warp == 1) {  // one warp in each CTA allocates for the pair
     asm volatile("tcgen05.alloc.cta_group::2.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(tmem_slot)),
@@ -729,6 +786,17 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
   cluster_sync();  // barriers of both CTAs are initialised before any remote arrival
   tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
+
+  // As in the single-CTA kernel: the setup above overlaps the predecessor's
+  // tail, and a failed call (P = 0, the same in both CTAs) gets no units.
+  wait_for_predecessor();
+  const int mt2 = (gp.M + 255) / 256;
+  __shared__ int s_plan[3];
+  int P;
+  Splits sp;
+  read_plan_once(gp, plan, gp.batch * mt2 * gp.nt, (int)(gridDim.x >> 1), s_plan, P, sp);
+  const int tiles = P * gp.batch * mt2 * gp.nt;
+  const int total = P ? tiles * sp.S : 0;
 
   if (warp == 0) {
     // ------------------------------------------------------------ producer (both CTAs)
@@ -853,33 +921,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
           epilogue_bar();
           first_write = false;
         }
-#pragma unroll 1
-        for (int col = col_begin; col < col_begin + BN / 2; col += 32) {
-          uint32_t r[32];
-          tmem_ld32(taddr + col, r);
-          tmem_wait_ld();
-          if (mode == 0) {
-#pragma unroll
-            for (int i = 0; i < 32; ++i) r[i] = __float_as_uint(partial_residue(__uint_as_float(r[i]), q, iq));
-            tmem_st32(taddr + col, r);
-          } else {
-            const int half = col >> 7;
-            const int j0 = (col & 127) >> 4;
-            uint8_t* hbase = out_base + half * OUT_HALF;
-            uint4* p0 = reinterpret_cast<uint4*>(hbase + sw128_off(row, j0));
-            uint4* p1 = reinterpret_cast<uint4*>(hbase + sw128_off(row, j0 + 1));
-            uint32_t carry[8] = {0, 0, 0, 0, 0, 0, 0, 0};
-            if (mode == 2 && nc_tile >= 2) {
-              const uint4 c0 = *p0, c1 = *p1;
-              carry[0] = c0.x; carry[1] = c0.y; carry[2] = c0.z; carry[3] = c0.w;
-              carry[4] = c1.x; carry[5] = c1.y; carry[6] = c1.z; carry[7] = c1.w;
-            }
-            uint32_t packed[8];
-            final_residues(r, carry, mode == 2 && nc_tile >= 2, q, iq, packed);
-            *p0 = make_uint4(packed[0], packed[1], packed[2], packed[3]);
-            *p1 = make_uint4(packed[4], packed[5], packed[6], packed[7]);
-          }
-        }
+        drain128(taddr, col_begin, row, mode, mode == 2 && nc_tile >= 2, q, iq, out_base);
         if (mode == 0) tmem_wait_st();
         tc_fence_before();
         __syncwarp();

@@ -381,6 +381,18 @@ const char* rg_strerror(int code);
 uint64_t rg_set_wait_limit_ns(uint64_t ns);
 void rg_inject_fault(int kind);
 
+/* Measurement hook: with n = 4, every later GEMM call (res_gemm_i64/limbs,
+ * enclose_gemm_*, interval_gemm_*, batched or not) records events[0] on its
+ * stream before its first kernel, events[1] before the per-prime GEMM,
+ * events[2] after it (split-K summation included) and events[3] after the
+ * reconstruction kernel, so that the caller can time each stage inside a
+ * real call with cudaEventElapsedTime.  events are cudaEvent_t handles the
+ * caller created and keeps alive while the hook is set.  The records
+ * serialise the stages (no overlap of one kernel's start with the previous
+ * one's end).  n = 0 removes the hook.  Process-wide; returns RG_OK, or
+ * RG_ERR_ARG for another n or a null handle. */
+int rg_set_stage_events(void* const* events, int n);
+
 /* Test hook: which tensor-core kernel runs the per-prime stage.  0 = choose
  * by shape (the CTA-pair kernel when M > 128), 1 = single-CTA kernel,
  * 2 = CTA-pair kernel.  Returns the previous choice, or -1 for an invalid

@@ -125,6 +125,15 @@ def test_argument_errors_need_no_device(rg):
     assert lib.res_gemm_stage(p, 2**17 + 8, p, 64, p, 16, 1, 2, 2, 2**17 + 1, 0, wsp, 4096, None) == rg.RG_ERR_RANGE
 
 
+def test_stage_events_hook_arguments(rg):
+    lib = rg.library()
+    nulls = (ctypes.c_void_p * 4)()
+    assert lib.rg_set_stage_events(None, 3) == rg.RG_ERR_ARG
+    assert lib.rg_set_stage_events(None, 4) == rg.RG_ERR_ARG
+    assert lib.rg_set_stage_events(nulls, 4) == rg.RG_ERR_ARG
+    assert lib.rg_set_stage_events(None, 0) == rg.RG_OK
+
+
 def test_wait_limit_roundtrip(rg):
     lib = rg.library()
     old = lib.rg_set_wait_limit_ns(12345)

@@ -159,3 +159,24 @@ def _log2_prod(rg, n):
     for q in rg.primes()[:n]:
         prod *= q
     return prod.bit_length() - 1
+
+
+def test_stage_events_time_a_real_call(rg):
+    """The stage-event hook records four ordered events inside a call and leaves its result unchanged."""
+    w = WORKLOADS["exact24_64"]
+    A, B = w.generate()
+    ref = oracle.matmul_i64(A, B, lc=1)[:, :, 0]
+    evs = [torch.cuda.Event(enable_timing=True) for _ in range(4)]
+    rg.set_stage_events(evs)
+    try:
+        C = host(rg.res_gemm_i64(dev(A), dev(B)))
+    finally:
+        rg.set_stage_events(None)
+    torch.cuda.synchronize()
+    assert np.array_equal(C, ref)
+    spans = [evs[i].elapsed_time(evs[i + 1]) for i in range(3)]
+    assert all(t > 0 for t in spans), spans
+    # with the hook removed the events are not recorded again
+    rg.res_gemm_i64(dev(A), dev(B))
+    torch.cuda.synchronize()
+    assert [evs[i].elapsed_time(evs[i + 1]) for i in range(3)] == spans
