@@ -602,6 +602,38 @@ __global__ void __launch_bounds__(256) split_int_kernel(SplitSide sa, SplitSide 
 // max |B| are reduced on the side for the GEMM kernel to derive the prime count
 // and check the range.  Saves one read of A and B and one kernel launch.
 template <int VEC>
+struct I64Item {
+  unsigned long long x[VEC];
+};
+
+// The VEC int64 entries of item `it` (zeros past the row's end or the last item).
+template <int VEC>
+__device__ __forceinline__ I64Item<VEC> load_i64_item(const SplitSide& sa, const SplitSide& sb, long long it,
+                                                      long long total) {
+  I64Item<VEC> v;
+  const bool valid = it < total;
+  const bool isA = it < sa.items;
+  const SplitSide& s = isA ? sa : sb;
+  const long long item = isA ? it : it - sa.items;
+  const long long per_row = s.ldy / VEC;
+  const long long row = item / per_row;
+  const long long col0 = (item - row * per_row) * VEC;
+  const unsigned long long* X = static_cast<const unsigned long long*>(s.X) + row * s.C + col0;
+  if (valid && col0 + VEC <= s.C && ((reinterpret_cast<uintptr_t>(X) & 15u) == 0)) {
+#pragma unroll
+    for (int t = 0; t < VEC / 2; ++t) {
+      const ulonglong2 w = __ldg(reinterpret_cast<const ulonglong2*>(X) + t);
+      v.x[2 * t] = w.x;
+      v.x[2 * t + 1] = w.y;
+    }
+  } else {
+#pragma unroll
+    for (int e = 0; e < VEC; ++e) v.x[e] = (valid && col0 + e < s.C) ? __ldg(X + e) : 0ull;
+  }
+  return v;
+}
+
+template <int VEC>
 __global__ void __launch_bounds__(256) split_i64_kernel(SplitSide sa, SplitSide sb, DevPlan* plan, int P) {
   __shared__ PrimeRec rec[kNumPrimes];
   __shared__ int ws[kNumPrimes][kMaxWords + 1];
@@ -612,7 +644,14 @@ __global__ void __launch_bounds__(256) split_i64_kernel(SplitSide sa, SplitSide 
   const long long total = sa.items + sb.items;
   const long long stride = (long long)gridDim.x * blockDim.x;
   unsigned long long max_a = 0, max_b = 0;
-  for (long long base = (long long)blockIdx.x * blockDim.x + (threadIdx.x & ~31); base < total; base += stride) {
+  // grid-stride over warp-aligned items; the next item's words are loaded
+  // while the current one is reduced, so reads, arithmetic and residue
+  // stores overlap
+  long long base = (long long)blockIdx.x * blockDim.x + (threadIdx.x & ~31);
+  I64Item<VEC> next = load_i64_item<VEC>(sa, sb, base + lane, total);
+  for (; base < total; base += stride) {
+    const I64Item<VEC> cur = next;
+    if (base + stride < total) next = load_i64_item<VEC>(sa, sb, base + stride + lane, total);
     const long long it = base + lane;
     const bool valid = it < total;
     const bool isA = it < sa.items;
@@ -621,22 +660,9 @@ __global__ void __launch_bounds__(256) split_i64_kernel(SplitSide sa, SplitSide 
     const long long per_row = s.ldy / VEC;
     const long long row = item / per_row;
     const long long col0 = (item - row * per_row) * VEC;
-    const unsigned long long* X = static_cast<const unsigned long long*>(s.X) + row * s.C + col0;
-    unsigned long long xw[VEC];
-    if (valid && col0 + VEC <= s.C && ((reinterpret_cast<uintptr_t>(X) & 15u) == 0)) {
-#pragma unroll
-      for (int t = 0; t < VEC / 2; ++t) {
-        const ulonglong2 v = __ldg(reinterpret_cast<const ulonglong2*>(X) + t);
-        xw[2 * t] = v.x;
-        xw[2 * t + 1] = v.y;
-      }
-    } else {
-#pragma unroll
-      for (int e = 0; e < VEC; ++e) xw[e] = (valid && col0 + e < s.C) ? __ldg(X + e) : 0ull;
-    }
     unsigned long long m = 0;
 #pragma unroll
-    for (int e = 0; e < VEC; ++e) m = max(m, abs_u64(xw[e]));
+    for (int e = 0; e < VEC; ++e) m = max(m, abs_u64(cur.x[e]));
     if (isA) max_a = max(max_a, m);
     else max_b = max(max_b, m);
     // words for the whole warp: none when every |x| <= 2^23, else the fewest
@@ -650,10 +676,10 @@ __global__ void __launch_bounds__(256) split_i64_kernel(SplitSide sa, SplitSide 
     float xf[VEC];
 #pragma unroll
     for (int e = 0; e < VEC; ++e) {
-      neg[e] = (long long)xw[e] < 0;
-      xf[e] = (float)(int)(long long)xw[e];
-      wd[e][0] = (uint32_t)xw[e];
-      wd[e][1] = (uint32_t)(xw[e] >> 32);
+      neg[e] = (long long)cur.x[e] < 0;
+      xf[e] = (float)(int)(long long)cur.x[e];
+      wd[e][0] = (uint32_t)cur.x[e];
+      wd[e][1] = (uint32_t)(cur.x[e] >> 32);
     }
     emit_int_residues<VEC, 2>(wd, neg, xf, nw, P, rec, ws, s.Y + row * s.ldy + col0, s.plane);
   }
@@ -1251,11 +1277,15 @@ static SplitSide make_side(const void* X, __half* Y, long long R, long long C, l
   return s;
 }
 
-static unsigned split_grid(long long items) {
+static unsigned split_grid(long long items, int blocks_per_sm = 8) {
   long long b = (items + 255) / 256;
-  const long long cap = 8LL * sm_count();
+  const long long cap = (long long)blocks_per_sm * sm_count();
   return (unsigned)(b < 1 ? 1 : (b > cap ? cap : b));
 }
+
+// Blocks per SM of the int64 split: few enough that each thread walks several
+// items and its prefetch overlaps the reduction of the current one.
+constexpr int kSplitI64BlocksPerSm = 3;
 
 static IvSide make_iv_side(const void* Xm, const void* Xr, __half* Y, long long R, long long C, long long ldy,
                            int vec) {
@@ -1304,7 +1334,8 @@ cudaError_t launch_split(int op, const void* A, const void* A2, const void* B, c
   if (op == RG_OP_I64) {
     constexpr int V = 8;
     const SplitSide sa = make_side(A, ra, M, K, lda, 1, V), sb = make_side(B, rb, brows, bcols, ldb, 1, V);
-    return launch_dependent(split_i64_kernel<V>, split_grid(sa.items + sb.items), 256, 0, st, sa, sb, plan, i64_planes);
+    return launch_dependent(split_i64_kernel<V>, split_grid(sa.items + sb.items, kSplitI64BlocksPerSm), 256, 0, st, sa,
+                            sb, plan, i64_planes);
   }
   if (L <= 1) {
     constexpr int V = 8;
