@@ -431,6 +431,7 @@ struct SplitSide {
   long long R, C, ldy, plane;  // plane = R * ldy
   int L;           // limbs per entry (integer kinds)
   long long items; // R * ldy / VEC
+  RowDiv rd;       // division by the items per row, ldy / VEC
 };
 
 // c + the four bytes of a (unsigned) dotted with the four bytes of b (signed).
@@ -556,7 +557,7 @@ __global__ void __launch_bounds__(256) split_int_kernel(SplitSide sa, SplitSide 
     const int nw = isA ? nw_a : nw_b;
     const long long item = isA ? it : it - sa.items;
     const long long per_row = s.ldy / VEC;
-    const long long row = item / per_row;
+    const long long row = div_row(item, s.rd);
     const long long col0 = (item - row * per_row) * VEC;
     const int L = s.L;
     const unsigned long long* X = static_cast<const unsigned long long*>(s.X) + (row * s.C + col0) * L;
@@ -616,7 +617,7 @@ __device__ __forceinline__ I64Item<VEC> load_i64_item(const SplitSide& sa, const
   const SplitSide& s = isA ? sa : sb;
   const long long item = isA ? it : it - sa.items;
   const long long per_row = s.ldy / VEC;
-  const long long row = item / per_row;
+  const long long row = div_row(item, s.rd);
   const long long col0 = (item - row * per_row) * VEC;
   const unsigned long long* X = static_cast<const unsigned long long*>(s.X) + row * s.C + col0;
   if (valid && col0 + VEC <= s.C && ((reinterpret_cast<uintptr_t>(X) & 15u) == 0)) {
@@ -658,7 +659,7 @@ __global__ void __launch_bounds__(256) split_i64_kernel(SplitSide sa, SplitSide 
     const SplitSide& s = isA ? sa : sb;
     const long long item = isA ? it : it - sa.items;
     const long long per_row = s.ldy / VEC;
-    const long long row = item / per_row;
+    const long long row = div_row(item, s.rd);
     const long long col0 = (item - row * per_row) * VEC;
     unsigned long long m = 0;
 #pragma unroll
@@ -764,7 +765,7 @@ __global__ void __launch_bounds__(256) split_float_kernel(SplitSide sa, SplitSid
     const int f = isA ? fa : fb;
     const long long item = isA ? it : it - sa.items;
     const long long per_row = s.ldy / VEC;
-    const long long row = item / per_row;
+    const long long row = div_row(item, s.rd);
     const long long col0 = (item - row * per_row) * VEC;
     const Bits* X = static_cast<const Bits*>(s.X) + row * s.C + col0;
     Bits xv[VEC];
@@ -823,6 +824,7 @@ struct IvSide {
   __half* Y;        // [pmax][3][R][ldy]
   long long R, C, ldy, sub, plane;  // sub = R * ldy (plane to plane), plane = 3 * sub (prime to prime)
   long long items;  // R * ldy / VEC
+  RowDiv rd;        // division by the items per row, ldy / VEC
 };
 
 template <typename Bits, int VEC>
@@ -848,7 +850,7 @@ __global__ void __launch_bounds__(256) split_interval_kernel(IvSide sa, IvSide s
     const int f = isA ? fa : fb;
     const long long item = isA ? it : it - sa.items;
     const long long per_row = s.ldy / VEC;
-    const long long row = item / per_row;
+    const long long row = div_row(item, s.rd);
     const long long col0 = (item - row * per_row) * VEC;
     Bits xm[VEC], xr[VEC];
     {
@@ -916,8 +918,8 @@ __global__ void __launch_bounds__(256) split_interval_kernel(IvSide sa, IvSide s
 
 template <int LC>
 __global__ void __launch_bounds__(128) garner_int_kernel(const uint8_t* __restrict__ RC, long long ldc,
-                                                         long long plane, long long M, long long N, DevPlan* plan,
-                                                         int64_t* __restrict__ C) {
+                                                         long long plane, long long M, long long N, RowDiv rd,
+                                                         DevPlan* plan, int64_t* __restrict__ C) {
   constexpr int W = 2 * LC, GE = GarnerGE<W>::value;
   __shared__ CrtRn crt;
   wait_for_predecessor();
@@ -928,7 +930,7 @@ __global__ void __launch_bounds__(128) garner_int_kernel(const uint8_t* __restri
   const long long per_row = (N + GE - 1) / GE;
   const long long item = (long long)blockIdx.x * blockDim.x + threadIdx.x;
   if (item >= M * per_row) return;
-  const long long m = item / per_row;
+  const long long m = div_row(item, rd);  // item / per_row
   const long long n0 = (item - m * per_row) * GE;
   uint32_t x[GE][W];
   if (rn)
@@ -1049,8 +1051,8 @@ __device__ __forceinline__ void add_shifted(uint32_t (&x)[kEncW], long long v, i
 template <typename Bits>
 __global__ void __launch_bounds__(128) garner_enclose_kernel(const uint8_t* __restrict__ RC, long long ldc,
                                                              long long plane, long long M, long long N,
-                                                             long long K, DevPlan* plan, Bits* __restrict__ lo,
-                                                             Bits* __restrict__ hi) {
+                                                             long long K, RowDiv rd, DevPlan* plan,
+                                                             Bits* __restrict__ lo, Bits* __restrict__ hi) {
   constexpr int GE = GarnerGE<kEncW>::value;
   static_assert(GE == 2, "the bound stores below write GE entries as one vector");
   __shared__ CrtRn crt;
@@ -1063,7 +1065,7 @@ __global__ void __launch_bounds__(128) garner_enclose_kernel(const uint8_t* __re
   const long long per_row = (N + GE - 1) / GE;
   const long long item = (long long)blockIdx.x * blockDim.x + threadIdx.x;
   if (item >= M * per_row) return;
-  const long long m = item / per_row;
+  const long long m = div_row(item, rd);  // item / per_row
   const long long n0 = (item - m * per_row) * GE;
   uint32_t x[GE][kEncW];
   if (rn)
@@ -1141,7 +1143,7 @@ __device__ __forceinline__ void add_words(uint32_t (&x)[kEncW], const uint32_t (
 template <typename Bits>
 __global__ void __launch_bounds__(128) garner_interval_kernel(const uint8_t* __restrict__ RC, long long ldc,
                                                               long long plane, long long sub, long long M,
-                                                              long long N, long long K, DevPlan* plan,
+                                                              long long N, long long K, RowDiv rd, DevPlan* plan,
                                                               Bits* __restrict__ lo, Bits* __restrict__ hi) {
   constexpr int GE = 1;
   __shared__ CrtRn crt;
@@ -1153,7 +1155,7 @@ __global__ void __launch_bounds__(128) garner_interval_kernel(const uint8_t* __r
   if (rn) crt_rn_tables<MainTab>(crt, P);
   const long long item = (long long)blockIdx.x * blockDim.x + threadIdx.x;
   if (item >= M * N) return;
-  const long long m = item / N, n = item - m * N;
+  const long long m = div_row(item, rd), n = item - m * N;  // item / N
   const uint8_t* base = RC + m * ldc + n;
   auto reconstruct = [&](const uint8_t* at, uint32_t (&v)[GE][kEncW]) {
     if (rn)
@@ -1274,6 +1276,7 @@ static SplitSide make_side(const void* X, __half* Y, long long R, long long C, l
   s.plane = R * ldy;
   s.L = L;
   s.items = R * (ldy / vec);
+  s.rd = make_rowdiv(ldy / vec);
   return s;
 }
 
@@ -1299,6 +1302,7 @@ static IvSide make_iv_side(const void* Xm, const void* Xr, __half* Y, long long 
   s.sub = R * ldy;
   s.plane = 3 * s.sub;
   s.items = R * (ldy / vec);
+  s.rd = make_rowdiv(ldy / vec);
   return s;
 }
 
@@ -1362,26 +1366,28 @@ cudaError_t launch_garner(int op, const void* RC, long long ldc, long long plane
   auto blocks_for = [&](int ge) { return dim3((unsigned)((M * ((N + ge - 1) / ge) + 127) / 128)); };
   if (op == RG_OP_INTERVAL)
     return launch_dependent(garner_interval_kernel<unsigned long long>, blocks_for(1), 128, 0, st, rc, ldc, plane, sub,
-                            M, N, K, plan, static_cast<unsigned long long*>(out0),
+                            M, N, K, make_rowdiv(N), plan, static_cast<unsigned long long*>(out0),
                             static_cast<unsigned long long*>(out1));
   if (op == RG_OP_INTERVAL_F32)
     return launch_dependent(garner_interval_kernel<uint32_t>, blocks_for(1), 128, 0, st, rc, ldc, plane, sub, M, N, K,
-                            plan, static_cast<uint32_t*>(out0), static_cast<uint32_t*>(out1));
+                            make_rowdiv(N), plan, static_cast<uint32_t*>(out0), static_cast<uint32_t*>(out1));
+  const RowDiv rd_enc = make_rowdiv((N + GarnerGE<kEncW>::value - 1) / GarnerGE<kEncW>::value);
   if (op == RG_OP_ENCLOSE)
     return launch_dependent(garner_enclose_kernel<unsigned long long>, blocks_for(GarnerGE<kEncW>::value), 128, 0, st,
-                            rc, ldc, plane, M, N, K, plan, static_cast<unsigned long long*>(out0),
+                            rc, ldc, plane, M, N, K, rd_enc, plan, static_cast<unsigned long long*>(out0),
                             static_cast<unsigned long long*>(out1));
   if (op == RG_OP_ENCLOSE_F32)
     return launch_dependent(garner_enclose_kernel<uint32_t>, blocks_for(GarnerGE<kEncW>::value), 128, 0, st, rc, ldc,
-                            plane, M, N, K, plan, static_cast<uint32_t*>(out0), static_cast<uint32_t*>(out1));
+                            plane, M, N, K, rd_enc, plan, static_cast<uint32_t*>(out0), static_cast<uint32_t*>(out1));
   int64_t* C = static_cast<int64_t*>(out0);
+  auto rowdiv_for = [&](int ge) { return make_rowdiv((N + ge - 1) / ge); };
   switch (lc) {
-    case 1: return launch_dependent(garner_int_kernel<1>, blocks_for(GarnerGE<2>::value), 128, 0, st, rc, ldc, plane, M, N, plan, C);
-    case 2: return launch_dependent(garner_int_kernel<2>, blocks_for(GarnerGE<4>::value), 128, 0, st, rc, ldc, plane, M, N, plan, C);
-    case 3: return launch_dependent(garner_int_kernel<3>, blocks_for(GarnerGE<6>::value), 128, 0, st, rc, ldc, plane, M, N, plan, C);
-    case 4: return launch_dependent(garner_int_kernel<4>, blocks_for(GarnerGE<8>::value), 128, 0, st, rc, ldc, plane, M, N, plan, C);
-    case 5: return launch_dependent(garner_int_kernel<5>, blocks_for(GarnerGE<10>::value), 128, 0, st, rc, ldc, plane, M, N, plan, C);
-    case 6: return launch_dependent(garner_int_kernel<6>, blocks_for(GarnerGE<12>::value), 128, 0, st, rc, ldc, plane, M, N, plan, C);
+    case 1: return launch_dependent(garner_int_kernel<1>, blocks_for(GarnerGE<2>::value), 128, 0, st, rc, ldc, plane, M, N, rowdiv_for(GarnerGE<2>::value), plan, C);
+    case 2: return launch_dependent(garner_int_kernel<2>, blocks_for(GarnerGE<4>::value), 128, 0, st, rc, ldc, plane, M, N, rowdiv_for(GarnerGE<4>::value), plan, C);
+    case 3: return launch_dependent(garner_int_kernel<3>, blocks_for(GarnerGE<6>::value), 128, 0, st, rc, ldc, plane, M, N, rowdiv_for(GarnerGE<6>::value), plan, C);
+    case 4: return launch_dependent(garner_int_kernel<4>, blocks_for(GarnerGE<8>::value), 128, 0, st, rc, ldc, plane, M, N, rowdiv_for(GarnerGE<8>::value), plan, C);
+    case 5: return launch_dependent(garner_int_kernel<5>, blocks_for(GarnerGE<10>::value), 128, 0, st, rc, ldc, plane, M, N, rowdiv_for(GarnerGE<10>::value), plan, C);
+    case 6: return launch_dependent(garner_int_kernel<6>, blocks_for(GarnerGE<12>::value), 128, 0, st, rc, ldc, plane, M, N, rowdiv_for(GarnerGE<12>::value), plan, C);
     default: return cudaErrorInvalidValue;
   }
 }

@@ -127,6 +127,39 @@ __device__ __forceinline__ void wait_for_predecessor() { asm volatile("griddepco
 // main work, so an early dependent never competes with unfinished work).
 __device__ __forceinline__ void allow_dependents() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
 
+// Division by a row length fixed for a launch, n / d for 0 <= n, by one
+// multiply-high and shifts (Granlund and Montgomery, "Division by invariant
+// integers using multiplication", unsigned N-bit division with a rounded-up
+// 33-bit multiplier): with l = ceil(log2 d) and m = floor(2^32 (2^l - d) / d) + 1,
+// t = mulhi(m, n) gives n / d = (t + ((n - t) >> min(l, 1))) >> max(l - 1, 0) for
+// every n < 2^32.  Larger n, or d >= 2^31, divide in 64 bits.
+struct RowDiv {
+  long long d;
+  uint32_t magic;
+  uint32_t sh1, sh2;
+  int fast;
+};
+
+inline RowDiv make_rowdiv(long long d) {
+  RowDiv r{d > 0 ? d : 1, 0u, 0u, 0u, 0};
+  if (d <= 0 || d >= (1LL << 31)) return r;
+  int l = 0;
+  while ((1LL << l) < d) ++l;
+  r.magic = (uint32_t)(((1ULL << 32) * ((1ULL << l) - (unsigned long long)d)) / (unsigned long long)d + 1ULL);
+  r.sh1 = l > 0 ? 1u : 0u;
+  r.sh2 = l > 0 ? (uint32_t)(l - 1) : 0u;
+  r.fast = 1;
+  return r;
+}
+
+__device__ __forceinline__ long long div_row(long long n, const RowDiv& r) {
+  if (r.fast && (unsigned long long)n < (1ULL << 32)) {
+    const uint32_t nn = (uint32_t)n, t = __umulhi(r.magic, nn);
+    return (long long)((t + ((nn - t) >> r.sh1)) >> r.sh2);
+  }
+  return n / r.d;
+}
+
 // Launches `kernel` with programmatic stream serialisation.
 template <typename... KArgs, typename... Args>
 inline cudaError_t launch_dependent(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t st,
