@@ -247,34 +247,57 @@ __device__ __forceinline__ float partial_residue(float x, float q, float iq) {
 // (|r| < 2^23, see the split kernel's reduction), giving the balanced residue,
 // moved to [0, q).  Bytes enter and leave the float domain through
 // the low mantissa bits of 2^23.
-__device__ __forceinline__ void final_residues(const uint32_t (&r)[32], const uint32_t (&carry)[8], bool add_carry,
-                                               float q, float iq, uint32_t (&packed)[8]) {
+// Residue bytes of 32 accumulator values (|x| < 2^24, exact integers in
+// fp32), in [0, q), packed four to a word; with CARRY the bytes in `carry`
+// are added mod q.  ONE_ROUND: one rounding suffices when |x / q| < 2^22,
+// true for every |x| < 2^24 once q >= 5: t = rint(x fl(1/q)) is within
+// 1/2 + 1/q of x / q, so |x - t q| < q and one conditional add gives [0, q).
+// For q = 3 (large unreduced residues from the stage entry point) the
+// partial reduction runs first.  Straight-line code over the 32 values, so
+// that their dependency chains interleave.
+template <bool ONE_ROUND, bool CARRY>
+__device__ __forceinline__ void final_residues_t(const uint32_t (&r)[32], const uint32_t (&carry)[8], float q,
+                                                 float iq, uint32_t (&packed)[8]) {
   const float magic = 12582912.0f, two23 = 8388608.0f;
-  // One rounding suffices when |x / q| < 2^22, true for every |x| < 2^24 once
-  // q >= 5: t = rint(x fl(1/q)) is within 1/2 + 1/q of x / q, so
-  // |x - t q| < q and one conditional add gives [0, q).  For q = 3 (large
-  // unreduced residues from the stage entry point) the partial reduction
-  // runs first.
-  const bool one_round = q > 4.0f;
+  float v[32];
+#pragma unroll
+  for (int i = 0; i < 32; ++i) {
+    v[i] = __uint_as_float(r[i]);
+    if constexpr (!ONE_ROUND) v[i] = partial_residue(v[i], q, iq);
+  }
+#pragma unroll
+  for (int i = 0; i < 32; ++i) {
+    const float t = __fadd_rn(__fmaf_rn(v[i], iq, magic), -magic);
+    v[i] = __fmaf_rn(-t, q, v[i]);
+    v[i] = v[i] < 0.0f ? v[i] + q : v[i];
+  }
+  if constexpr (CARRY) {
+#pragma unroll
+    for (int i = 0; i < 32; ++i) {
+      // 0x4B0000cc is the float 2^23 + c for the carry byte c
+      const float c = __uint_as_float(__byte_perm(carry[i >> 2], 0x4B000000u, 0x7540u + (uint32_t)(i & 3))) - two23;
+      v[i] = v[i] + c;
+      v[i] = v[i] >= q ? v[i] - q : v[i];
+    }
+  }
 #pragma unroll
   for (int w = 0; w < 8; ++w) {
     uint32_t b[4];
 #pragma unroll
-    for (int k = 0; k < 4; ++k) {
-      float v = __uint_as_float(r[4 * w + k]);
-      if (!one_round) v = partial_residue(v, q, iq);
-      const float t = __fadd_rn(__fmaf_rn(v, iq, magic), -magic);
-      v = __fmaf_rn(-t, q, v);
-      v = v < 0.0f ? v + q : v;
-      if (add_carry) {
-        // 0x4B0000cc is the float 2^23 + c for the carry byte c
-        const float c = __uint_as_float(__byte_perm(carry[w], 0x4B000000u, 0x7540u + (uint32_t)k)) - two23;
-        v = v + c;
-        v = v >= q ? v - q : v;
-      }
-      b[k] = __float_as_uint(v + two23);  // low byte = v
-    }
+    for (int k = 0; k < 4; ++k) b[k] = __float_as_uint(v[4 * w + k] + two23);  // low byte = v
     packed[w] = __byte_perm(__byte_perm(b[0], b[1], 0x0040u), __byte_perm(b[2], b[3], 0x0040u), 0x5410u);
+  }
+}
+
+__device__ __forceinline__ void final_residues(const uint32_t (&r)[32], const uint32_t (&carry)[8], bool add_carry,
+                                               float q, float iq, uint32_t (&packed)[8]) {
+  const bool one_round = q > 4.0f;  // uniform: one prime per tile
+  if (one_round) {
+    if (add_carry) final_residues_t<true, true>(r, carry, q, iq, packed);
+    else final_residues_t<true, false>(r, carry, q, iq, packed);
+  } else {
+    if (add_carry) final_residues_t<false, true>(r, carry, q, iq, packed);
+    else final_residues_t<false, false>(r, carry, q, iq, packed);
   }
 }
 
