@@ -235,7 +235,7 @@ int run(int op, const void* A, const void* A2, int la, const void* B, const void
   const long long sub = batch * M * L.ldc;
   RG_TRY(record_stage(2, s));
   RG_TRY(launch_garner(op, w + L.rc, L.ldc, planes_per_product(op) * sub, sub, batch * M, N, K,
-                       op == RG_OP_LIMBS ? lc : 1, plan, dC, dC2, s));
+                       op == RG_OP_LIMBS ? lc : 1, L.pmax, plan, dC, dC2, s));
   RG_TRY(record_stage(3, s));
   if (flags & RG_FLAG_HOST) {
     RG_TRY(cudaMemcpyAsync(C, dC, out_bytes, cudaMemcpyDeviceToHost, s));

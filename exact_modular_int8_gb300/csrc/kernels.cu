@@ -916,7 +916,8 @@ __global__ void __launch_bounds__(256) split_interval_kernel(IvSide sa, IvSide s
 // rg_garner.cuh.
 // ---------------------------------------------------------------------------
 
-template <int LC>
+// MAXP: a compile-time bound on the prime count (the workspace's pmax).
+template <int LC, int MAXP>
 __global__ void __launch_bounds__(128) garner_int_kernel(const uint8_t* __restrict__ RC, long long ldc,
                                                          long long plane, long long M, long long N, RowDiv rd,
                                                          DevPlan* plan, int64_t* __restrict__ C) {
@@ -925,6 +926,10 @@ __global__ void __launch_bounds__(128) garner_int_kernel(const uint8_t* __restri
   wait_for_predecessor();
   if (plan->status) return;
   const int P = plan->P;
+  if (P > MAXP) {  // the planner keeps P within the workspace's planes
+    if (blockIdx.x == 0 && threadIdx.x == 0) set_status(&plan->status, RG_ERR_RANGE);
+    return;
+  }
   const bool rn = plan->crt_rn != 0;
   if (rn) crt_rn_tables<MainTab>(crt, P);
   const long long per_row = (N + GE - 1) / GE;
@@ -936,7 +941,7 @@ __global__ void __launch_bounds__(128) garner_int_kernel(const uint8_t* __restri
   if (rn)
     crt_rn_reconstruct<W, GE, MainTab>(RC + m * ldc + n0, plane, P, crt, x);
   else
-    garner_reconstruct<W, GE, MainTab>(RC + m * ldc + n0, plane, P, x);
+    garner_reconstruct<W, GE, MainTab, MAXP>(RC + m * ldc + n0, plane, P, x);
   int64_t* out = C + (m * N + n0) * LC;
   if (n0 + GE <= N && ((reinterpret_cast<uintptr_t>(out) & 15u) == 0)) {
     // GE * LC consecutive int64: 16-byte stores
@@ -1360,8 +1365,12 @@ cudaError_t launch_split(int op, const void* A, const void* A2, const void* B, c
   return cudaGetLastError();
 }
 
+// Prime bound of the register-lean integer Garner kernels.
+constexpr int kGarnerSmallP = 12;
+
 cudaError_t launch_garner(int op, const void* RC, long long ldc, long long plane, long long sub, long long M,
-                          long long N, long long K, int lc, DevPlan* plan, void* out0, void* out1, cudaStream_t st) {
+                          long long N, long long K, int lc, int pmax, DevPlan* plan, void* out0, void* out1,
+                          cudaStream_t st) {
   const uint8_t* rc = static_cast<const uint8_t*>(RC);
   auto blocks_for = [&](int ge) { return dim3((unsigned)((M * ((N + ge - 1) / ge) + 127) / 128)); };
   if (op == RG_OP_INTERVAL)
@@ -1381,13 +1390,20 @@ cudaError_t launch_garner(int op, const void* RC, long long ldc, long long plane
                             plane, M, N, K, rd_enc, plan, static_cast<uint32_t*>(out0), static_cast<uint32_t*>(out1));
   int64_t* C = static_cast<int64_t*>(out0);
   auto rowdiv_for = [&](int ge) { return make_rowdiv((N + ge - 1) / ge); };
+  // the packed digits of at most kGarnerSmallP primes fit in 3 registers per
+  // entry, against 14 for all 53
+  const bool small = pmax <= kGarnerSmallP;
+  auto go = [&](auto k_small, auto k_all, int ge) {
+    return launch_dependent(small ? k_small : k_all, blocks_for(ge), 128, 0, st, rc, ldc, plane, M, N, rowdiv_for(ge),
+                            plan, C);
+  };
   switch (lc) {
-    case 1: return launch_dependent(garner_int_kernel<1>, blocks_for(GarnerGE<2>::value), 128, 0, st, rc, ldc, plane, M, N, rowdiv_for(GarnerGE<2>::value), plan, C);
-    case 2: return launch_dependent(garner_int_kernel<2>, blocks_for(GarnerGE<4>::value), 128, 0, st, rc, ldc, plane, M, N, rowdiv_for(GarnerGE<4>::value), plan, C);
-    case 3: return launch_dependent(garner_int_kernel<3>, blocks_for(GarnerGE<6>::value), 128, 0, st, rc, ldc, plane, M, N, rowdiv_for(GarnerGE<6>::value), plan, C);
-    case 4: return launch_dependent(garner_int_kernel<4>, blocks_for(GarnerGE<8>::value), 128, 0, st, rc, ldc, plane, M, N, rowdiv_for(GarnerGE<8>::value), plan, C);
-    case 5: return launch_dependent(garner_int_kernel<5>, blocks_for(GarnerGE<10>::value), 128, 0, st, rc, ldc, plane, M, N, rowdiv_for(GarnerGE<10>::value), plan, C);
-    case 6: return launch_dependent(garner_int_kernel<6>, blocks_for(GarnerGE<12>::value), 128, 0, st, rc, ldc, plane, M, N, rowdiv_for(GarnerGE<12>::value), plan, C);
+    case 1: return go(garner_int_kernel<1, kGarnerSmallP>, garner_int_kernel<1, kNumPrimes>, GarnerGE<2>::value);
+    case 2: return go(garner_int_kernel<2, kGarnerSmallP>, garner_int_kernel<2, kNumPrimes>, GarnerGE<4>::value);
+    case 3: return go(garner_int_kernel<3, kGarnerSmallP>, garner_int_kernel<3, kNumPrimes>, GarnerGE<6>::value);
+    case 4: return go(garner_int_kernel<4, kGarnerSmallP>, garner_int_kernel<4, kNumPrimes>, GarnerGE<8>::value);
+    case 5: return go(garner_int_kernel<5, kGarnerSmallP>, garner_int_kernel<5, kNumPrimes>, GarnerGE<10>::value);
+    case 6: return go(garner_int_kernel<6, kGarnerSmallP>, garner_int_kernel<6, kNumPrimes>, GarnerGE<12>::value);
     default: return cudaErrorInvalidValue;
   }
 }

@@ -57,39 +57,43 @@ __device__ __forceinline__ void add_scaled_weight(uint32_t (&x)[W], int D, int i
 // x[e] (W 32-bit words, two's complement) = the reconstructed integers of the
 // GE residue vectors starting at rc (plane = distance between primes).
 // Digits are combined in pairs, D = v_i + q_i v_{i+1} (|D| < 2^15, exact in
-// fp32), so the wide accumulation runs once per two primes.
-template <int W, int GE, typename TAB>
+// fp32), so the wide accumulation runs once per two primes.  MAXP bounds P
+// at compile time (the packed digits take (MAXP + 3) / 4 registers per entry).
+template <int W, int GE, typename TAB, int MAXP = kNumPrimes>
 __device__ __forceinline__ void garner_reconstruct(const uint8_t* __restrict__ rc, long long plane, int P,
                                                    uint32_t (&x)[GE][W]) {
-  uint32_t V[GE][kGarnerWords];
+  static_assert(MAXP >= 1 && MAXP <= kNumPrimes, "prime bound");
+  constexpr int kWords = (MAXP + 3) / 4;
+  uint32_t V[GE][kWords];
   float pend[GE];  // the even digit of the current pair, as float
 #pragma unroll
   for (int e = 0; e < GE; ++e) {
 #pragma unroll
-    for (int w = 0; w < kGarnerWords; ++w) V[e][w] = 0u;
+    for (int w = 0; w < kWords; ++w) V[e][w] = 0u;
 #pragma unroll
     for (int k = 0; k < W; ++k) x[e][k] = 0u;
     pend[e] = 0.0f;
   }
 #pragma unroll
-  for (int i0 = 0; i0 < kNumPrimes; i0 += kGarnerBatch) {
+  for (int i0 = 0; i0 < MAXP; i0 += kGarnerBatch) {
     if (i0 >= P) break;
     uint32_t rw[kGarnerBatch];
 #pragma unroll
     for (int j = 0; j < kGarnerBatch; ++j) {
       const int i = i0 + j;
       static_assert(GE == 1 || GE == 2 || GE == 4, "one, two or four adjacent entries");
+      const bool in = i < P && i < MAXP;
       if constexpr (GE == 4)
-        rw[j] = (i < P) ? __ldg(reinterpret_cast<const uint32_t*>(rc + (long long)i * plane)) : 0u;
+        rw[j] = in ? __ldg(reinterpret_cast<const uint32_t*>(rc + (long long)i * plane)) : 0u;
       else if constexpr (GE == 2)
-        rw[j] = (i < P) ? (uint32_t)__ldg(reinterpret_cast<const unsigned short*>(rc + (long long)i * plane)) : 0u;
+        rw[j] = in ? (uint32_t)__ldg(reinterpret_cast<const unsigned short*>(rc + (long long)i * plane)) : 0u;
       else
-        rw[j] = (i < P) ? (uint32_t)__ldg(rc + (long long)i * plane) : 0u;
+        rw[j] = in ? (uint32_t)__ldg(rc + (long long)i * plane) : 0u;
     }
 #pragma unroll
     for (int j = 0; j < kGarnerBatch; ++j) {
       const int i = i0 + j;
-      if (i >= kNumPrimes || i >= P) break;
+      if (i >= MAXP || i >= P) break;
       const float q = TAB::t().qf[i], iq = TAB::t().invq[i];
       const int gi = TAB::t().ginv[i];
       // byte selector that inserts a new low byte at position i % 4
@@ -99,7 +103,7 @@ __device__ __forceinline__ void garner_reconstruct(const uint8_t* __restrict__ r
         // s = Q_i^-1 r_i - sum_{j<i} (Q_j Q_i^-1 mod q_i) v_j, |s| < 2^20
         int acc = gi * (int)((rw[j] >> (8 * e)) & 0xFFu);
 #pragma unroll
-        for (int w = 0; w < kGarnerWords; ++w)
+        for (int w = 0; w < kWords; ++w)
           if (4 * w < i) acc = __dp4a((int)V[e][w], TAB::t().gd_packed[i][w], acc);
         const float vf = bal_mod_small(int_to_float_exact(acc), q, iq);
         const int vb = float_bits_offset(vf);

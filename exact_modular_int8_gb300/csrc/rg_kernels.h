@@ -53,8 +53,10 @@ int gemm_max_splits(long long gemm_batch, long long M, long long N, long long K)
 // Balanced Garner: RC [P][M][ldc] -> int64 limbs C [M][N][lc] (op I64/LIMBS),
 // or the outward pair (lo, hi) as IEEE bit patterns (ops ENCLOSE[_F32]).  For
 // the interval ops RC holds three planes per prime, `sub` bytes apart: the
-// midpoint and the two radius products.
+// midpoint and the two radius products.  pmax bounds the plan's prime count
+// (the planes the workspace holds).
 cudaError_t launch_garner(int op, const void* RC, long long ldc, long long plane, long long sub, long long M,
-                          long long N, long long K, int lc, DevPlan* plan, void* out0, void* out1, cudaStream_t st);
+                          long long N, long long K, int lc, int pmax, DevPlan* plan, void* out0, void* out1,
+                          cudaStream_t st);
 
 }  // namespace rg
