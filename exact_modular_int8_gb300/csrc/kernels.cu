@@ -718,22 +718,42 @@ __device__ __forceinline__ void scaled_magnitude(Bits v, int f, bool& neg, unsig
   }
 }
 
-// Words of t dotted with a prime's byte weights, reduced: t mod q, balanced.
-template <int NWF>
-__device__ __forceinline__ float residue_of_words(unsigned long long t, const int (&wv)[NWF], float q, float iq) {
-  int acc = dp4a_us((uint32_t)t, wv[0], 0);
-  if constexpr (NWF == 2) acc = dp4a_us((uint32_t)(t >> 32), wv[1], acc);
-  return bal_mod_small(int_to_float_exact(acc), q, iq);  // |acc| <= 8 * 255 * 125 < 2^22
-}
+// Byte weights of 2^(8k + s) mod q (ShiftWeights), uploaded with the tables.
+__device__ uint2 g_wsh[kNumPrimes][kPow2Span];
 
-// 2^s mod q for the primes and shifts a split block needs, as fp16 (exact).
-__device__ float g_pow2[kNumPrimes][kPow2Span];
+// Dynamic shared memory of the floating-point splits: the shifted byte
+// weights of P primes and `cols` shifts, [P][cols], when they fit in
+// kWshEntries (a plan's usual size: tens of primes, tens of shifts);
+// larger plans read the global table through L1 instead.  The plan is only
+// known on the device, so the launch reserves the fixed kWshBytes.
+constexpr int kWshEntries = 2048;
+constexpr size_t kWshBytes = sizeof(uint2) * kWshEntries;
 
-__device__ __forceinline__ void load_pow2(__half* pw, int P, int cols) {
+// Stages the table for P primes and `cols` shifts in shared memory if it
+// fits; false if the block must read the global table.
+__device__ __forceinline__ bool stage_wsh(uint2* wsh, int P, int cols) {
+  if (P * cols > kWshEntries) return false;
   for (int i = threadIdx.x; i < P * cols; i += blockDim.x) {
     const int p = i / cols, c = i - p * cols;
-    pw[p * kPow2Span + c] = __float2half_rn(g_pow2[p][c]);
+    wsh[i] = g_wsh[p][c];
   }
+  return true;
+}
+
+// The weights of prime p and shift sh: staged ([P][cols]) or global.
+template <bool STAGED>
+__device__ __forceinline__ uint2 wsh_get(const uint2* wsh, int cols, int p, int sh) {
+  if constexpr (STAGED) return wsh[p * cols + sh];
+  else return __ldg(&g_wsh[p][sh]);
+}
+
+// Balanced residue of t * 2^s from the bytes of t and the shifted byte weights
+// w of s: one dot product per word, one reduction (|acc| <= 8 * 255 * 125 < 2^21).
+template <int NWF>
+__device__ __forceinline__ float shifted_residue(unsigned long long t, uint2 w, float q, float iq) {
+  int acc = dp4a_us((uint32_t)t, (int)w.x, 0);
+  if constexpr (NWF == 2) acc = dp4a_us((uint32_t)(t >> 32), (int)w.y, acc);
+  return bal_mod_small(int_to_float_exact(acc), q, iq);
 }
 
 // Shifts a floating-point split can meet: sh < max(bits_a, bits_b) <= 255.
@@ -742,21 +762,14 @@ __device__ __forceinline__ int pow2_cols(const DevPlan* plan) {
   return b < 1 ? 1 : (b > kPow2Span ? kPow2Span : b);
 }
 
-// Floating-point operands.  No floating-point instruction reads x.
-template <typename Bits, int VEC>
-__global__ void __launch_bounds__(256) split_float_kernel(SplitSide sa, SplitSide sb, const DevPlan* plan) {
+// The split's main loop (weights staged in shared memory or read from the
+// global table).
+template <typename Bits, int VEC, bool STAGED>
+__device__ __forceinline__ void split_float_loop(const SplitSide& sa, const SplitSide& sb, int P, int fa, int fb,
+                                                 const PrimeRec* rec, const uint2* wsh, int cols) {
   using F = FloatFormat<Bits>;
   constexpr int NWF = F::kFracBits + 2 > 32 ? 2 : 1;  // words of t (the floored magnitude may gain a bit)
   constexpr int PER = 16 / sizeof(Bits);
-  __shared__ PrimeRec rec[kNumPrimes];
-  __shared__ __half pw[kNumPrimes * kPow2Span];
-  load_prime_recs(rec, nullptr);
-  wait_for_predecessor();
-  if (plan->status) return;
-  const int P = plan->P;
-  const int fa = plan->f_a, fb = plan->f_b;
-  load_pow2(pw, P, pow2_cols(plan));
-  __syncthreads();
   const long long total = sa.items + sb.items;
   for (long long it = (long long)blockIdx.x * blockDim.x + threadIdx.x; it < total;
        it += (long long)gridDim.x * blockDim.x) {
@@ -792,19 +805,34 @@ __global__ void __launch_bounds__(256) split_float_kernel(SplitSide sa, SplitSid
     for (int p = 0; p < P; ++p) {
       const PrimeRec& R = rec[p];
       const float q = R.q, iq = R.iq;
-      int wv[NWF];
-      load_weights<NWF>(R, wv);
-      const __half* pwp = pw + p * kPow2Span;
       float r[VEC];
 #pragma unroll
       for (int e = 0; e < VEC; ++e) {
-        const float rt = residue_of_words<NWF>(tv[e], wv, q, iq);
-        const float rr = bal_mod_small(rt * __half2float(pwp[shv[e]]), q, iq);  // |rt * 2^sh mod q| < 2^14
+        const float rr = shifted_residue<NWF>(tv[e], wsh_get<STAGED>(wsh, cols, p, shv[e]), q, iq);
         r[e] = negv[e] ? -rr : rr;
       }
       store_residues<VEC>(r, y + (long long)p * s.plane);
     }
   }
+}
+
+// Floating-point operands.  No floating-point instruction reads x.
+template <typename Bits, int VEC>
+__global__ void __launch_bounds__(256) split_float_kernel(SplitSide sa, SplitSide sb, const DevPlan* plan) {
+  __shared__ PrimeRec rec[kNumPrimes];
+  extern __shared__ uint2 wsh[];
+  load_prime_recs(rec, nullptr);
+  wait_for_predecessor();
+  if (plan->status) return;
+  const int P = plan->P;
+  const int fa = plan->f_a, fb = plan->f_b;
+  const int cols = pow2_cols(plan);
+  const bool staged = stage_wsh(wsh, P, cols);
+  __syncthreads();
+  if (staged)
+    split_float_loop<Bits, VEC, true>(sa, sb, P, fa, fb, rec, wsh, cols);
+  else
+    split_float_loop<Bits, VEC, false>(sa, sb, P, fa, fb, rec, wsh, cols);
   allow_dependents();
 }
 
@@ -827,21 +855,13 @@ struct IvSide {
   RowDiv rd;        // division by the items per row, ldy / VEC
 };
 
-template <typename Bits, int VEC>
-__global__ void __launch_bounds__(256) split_interval_kernel(IvSide sa, IvSide sb, const DevPlan* plan) {
+template <typename Bits, int VEC, bool STAGED>
+__device__ __forceinline__ void split_interval_loop(const IvSide& sa, const IvSide& sb, int P, int fa, int fb,
+                                                    const PrimeRec* rec, const uint2* wsh, int cols) {
   using F = FloatFormat<Bits>;
   constexpr int NWF = F::kFracBits + 2 > 32 ? 2 : 1;
   constexpr int PER = 16 / sizeof(Bits);
   static_assert((VEC * sizeof(Bits)) % 16 == 0, "whole 16-byte loads");
-  __shared__ PrimeRec rec[kNumPrimes];
-  __shared__ __half pw[kNumPrimes * kPow2Span];
-  load_prime_recs(rec, nullptr);
-  wait_for_predecessor();
-  if (plan->status) return;
-  const int P = plan->P;
-  const int fa = plan->f_a, fb = plan->f_b;
-  load_pow2(pw, P, pow2_cols(plan));
-  __syncthreads();
   const long long total = sa.items + sb.items;
   for (long long it = (long long)blockIdx.x * blockDim.x + threadIdx.x; it < total;
        it += (long long)gridDim.x * blockDim.x) {
@@ -887,14 +907,11 @@ __global__ void __launch_bounds__(256) split_interval_kernel(IvSide sa, IvSide s
     for (int p = 0; p < P; ++p) {
       const PrimeRec& R = rec[p];
       const float q = R.q, iq = R.iq;
-      int wv[NWF];
-      load_weights<NWF>(R, wv);
-      const __half* pwp = pw + p * kPow2Span;
       float r0[VEC], r1[VEC], r2[VEC];
 #pragma unroll
       for (int e = 0; e < VEC; ++e) {
-        const float am = bal_mod_small(residue_of_words<NWF>(tm[e], wv, q, iq) * __half2float(pwp[shm[e]]), q, iq);
-        const float rr = bal_mod_small(residue_of_words<NWF>(tr[e], wv, q, iq) * __half2float(pwp[shr[e]]), q, iq);
+        const float am = shifted_residue<NWF>(tm[e], wsh_get<STAGED>(wsh, cols, p, shm[e]), q, iq);
+        const float rr = shifted_residue<NWF>(tr[e], wsh_get<STAGED>(wsh, cols, p, shr[e]), q, iq);
         const float rm = negm[e] ? -am : am;                                           // floor(x 2^f)
         const float rabs = negm[e] ? am : bal_mod_small(am + (lostm[e] ? 1.0f : 0.0f), q, iq);  // ceil |x| 2^f
         r0[e] = rm;
@@ -907,6 +924,24 @@ __global__ void __launch_bounds__(256) split_interval_kernel(IvSide sa, IvSide s
       store_residues<VEC>(r2, yp + 2 * s.sub);
     }
   }
+}
+
+template <typename Bits, int VEC>
+__global__ void __launch_bounds__(256) split_interval_kernel(IvSide sa, IvSide sb, const DevPlan* plan) {
+  __shared__ PrimeRec rec[kNumPrimes];
+  extern __shared__ uint2 wsh[];
+  load_prime_recs(rec, nullptr);
+  wait_for_predecessor();
+  if (plan->status) return;
+  const int P = plan->P;
+  const int fa = plan->f_a, fb = plan->f_b;
+  const int cols = pow2_cols(plan);
+  const bool staged = stage_wsh(wsh, P, cols);
+  __syncthreads();
+  if (staged)
+    split_interval_loop<Bits, VEC, true>(sa, sb, P, fa, fb, rec, wsh, cols);
+  else
+    split_interval_loop<Bits, VEC, false>(sa, sb, P, fa, fb, rec, wsh, cols);
   allow_dependents();
 }
 
@@ -1225,7 +1260,7 @@ cudaError_t upload_tables() {
   std::lock_guard<std::mutex> lock(mu);
   if (done[dev]) return cudaSuccess;
   e = cudaMemcpyToSymbol(c_tab, &host_tables(), sizeof(Tables));
-  if (e == cudaSuccess) e = cudaMemcpyToSymbol(g_pow2, host_pow2().v, sizeof(Pow2Table));
+  if (e == cudaSuccess) e = cudaMemcpyToSymbol(g_wsh, host_shift_weights().w, sizeof(ShiftWeights));
   if (e == cudaSuccess) {
     static SplitTables st;  // built from the host tables
     const Tables& t = host_tables();
@@ -1311,6 +1346,31 @@ static IvSide make_iv_side(const void* Xm, const void* Xr, __half* Y, long long 
   return s;
 }
 
+// The floating-point splits' dynamic shared memory (kWshBytes) exceeds the
+// default 48 KB limit; raised once per device.
+static cudaError_t allow_wsh_smem() {
+  static std::mutex mu;
+  static bool done[64];
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+  std::lock_guard<std::mutex> lock(mu);
+  if (done[dev]) return cudaSuccess;
+  const int bytes = (int)kWshBytes;
+  e = cudaFuncSetAttribute(split_interval_kernel<unsigned long long, 4>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           bytes);
+  if (e == cudaSuccess)
+    e = cudaFuncSetAttribute(split_interval_kernel<uint32_t, 4>, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+  if (e == cudaSuccess)
+    e = cudaFuncSetAttribute(split_float_kernel<unsigned long long, 8>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             bytes);
+  if (e == cudaSuccess)
+    e = cudaFuncSetAttribute(split_float_kernel<uint32_t, 8>, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+  if (e == cudaSuccess) done[dev] = true;
+  return e;
+}
+
 cudaError_t launch_split(int op, const void* A, const void* A2, const void* B, const void* B2, int la, int lb,
                          long long batch, long long Mb, long long N, long long K, long long lda, long long ldb,
                          void* RA, void* RB, DevPlan* plan, int i64_planes, bool transb, cudaStream_t st) {
@@ -1321,22 +1381,26 @@ cudaError_t launch_split(int op, const void* A, const void* A2, const void* B, c
   // RB [P][N][ldb], laid out like A.
   const long long M = batch * Mb;
   const long long brows = batch * (transb ? N : K), bcols = transb ? K : N;
+  if (op == RG_OP_INTERVAL || op == RG_OP_INTERVAL_F32 || op == RG_OP_ENCLOSE || op == RG_OP_ENCLOSE_F32) {
+    cudaError_t e = allow_wsh_smem();
+    if (e != cudaSuccess) return e;
+  }
   if (op == RG_OP_INTERVAL || op == RG_OP_INTERVAL_F32) {
     constexpr int V = 4;
     const IvSide sa = make_iv_side(A, A2, ra, M, K, lda, V), sb = make_iv_side(B, B2, rb, brows, bcols, ldb, V);
     if (op == RG_OP_INTERVAL)
-      return launch_dependent(split_interval_kernel<unsigned long long, V>, split_grid(sa.items + sb.items), 256, 0,
-                              st, sa, sb, (const DevPlan*)plan);
-    return launch_dependent(split_interval_kernel<uint32_t, V>, split_grid(sa.items + sb.items), 256, 0, st, sa, sb,
-                            (const DevPlan*)plan);
+      return launch_dependent(split_interval_kernel<unsigned long long, V>, split_grid(sa.items + sb.items), 256,
+                              kWshBytes, st, sa, sb, (const DevPlan*)plan);
+    return launch_dependent(split_interval_kernel<uint32_t, V>, split_grid(sa.items + sb.items), 256, kWshBytes, st,
+                            sa, sb, (const DevPlan*)plan);
   }
   if (op == RG_OP_ENCLOSE || op == RG_OP_ENCLOSE_F32) {
     constexpr int V = 8;
     const SplitSide sa = make_side(A, ra, M, K, lda, 1, V), sb = make_side(B, rb, brows, bcols, ldb, 1, V);
     if (op == RG_OP_ENCLOSE)
-      return launch_dependent(split_float_kernel<unsigned long long, V>, split_grid(sa.items + sb.items), 256, 0, st,
-                              sa, sb, (const DevPlan*)plan);
-    return launch_dependent(split_float_kernel<uint32_t, V>, split_grid(sa.items + sb.items), 256, 0, st, sa, sb,
+      return launch_dependent(split_float_kernel<unsigned long long, V>, split_grid(sa.items + sb.items), 256,
+                              kWshBytes, st, sa, sb, (const DevPlan*)plan);
+    return launch_dependent(split_float_kernel<uint32_t, V>, split_grid(sa.items + sb.items), 256, kWshBytes, st, sa, sb,
                             (const DevPlan*)plan);
   }
   const int L = la > lb ? la : lb;

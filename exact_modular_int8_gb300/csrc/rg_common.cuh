@@ -12,7 +12,7 @@ namespace rg {
 
 constexpr int kNumPrimes = RG_NUM_PRIMES;  // odd primes 3..251, largest first
 constexpr int kMaxWords = 8;               // 32-bit words of a 256-bit operand
-constexpr int kPow2Span = 256;             // 2^s mod q tabulated for s < 256
+constexpr int kPow2Span = 256;             // shifts s < 256 are tabulated
 constexpr int kGarnerWords = 14;           // ceil(53 / 4) int8x4 words per Garner row
 constexpr int kQWords = 11;                // 32-bit words of the mixed-radix weights Q_i
 constexpr int kMaxLimbsOut = RG_MAX_LIMBS_OUT;
@@ -73,12 +73,14 @@ const Tables& host_tables();
 // (count <= 53), e.g. the subset a solve can use.
 void build_tables_for(const int* qs, int count, Tables* out);
 
-// 2^s mod q (balanced) for every prime and s < 256, kept in global memory
-// (too large for the constant bank beside Tables).
-struct Pow2Table {
-  float v[kNumPrimes][kPow2Span];
+// Byte weights of shifted words: for every prime q, shift s < 256 and byte
+// position k < 8, bal(2^(8k + s) mod q) as an int8, four to a word (word 0:
+// k = 0..3, word 1: k = 4..7).  A dot product of an integer's bytes with the
+// words of shift s gives its residue times 2^s.  Kept in global memory.
+struct ShiftWeights {
+  uint32_t w[kNumPrimes][kPow2Span][2];
 };
-const Pow2Table& host_pow2();
+const ShiftWeights& host_shift_weights();
 
 // ---------------------------------------------------------------------------
 // Device helpers

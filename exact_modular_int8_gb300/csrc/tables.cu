@@ -123,13 +123,22 @@ const Tables& host_tables() {
 
 void build_tables_for(const int* qs, int count, Tables* out) { build_for(qs, count, *out); }
 
-const Pow2Table& host_pow2() {
-  static Pow2Table t;
+const ShiftWeights& host_shift_weights() {
+  static ShiftWeights t;
   static std::once_flag once;
   std::call_once(once, [] {
     const Tables& b = host_tables();
     for (int i = 0; i < kNumPrimes; ++i)
-      for (int e = 0; e < kPow2Span; ++e) t.v[i][e] = (float)balanced(mod_pow(2, e, b.q[i]), b.q[i]);
+      for (int s = 0; s < kPow2Span; ++s)
+        for (int word = 0; word < 2; ++word) {
+          uint32_t packed = 0;
+          for (int j = 0; j < 4; ++j) {
+            const int k = 4 * word + j;
+            const int v = balanced(mod_pow(2, 8 * k + s, b.q[i]), b.q[i]);  // |v| <= 125
+            packed |= (uint32_t)(uint8_t)(int8_t)v << (8 * j);
+          }
+          t.w[i][s][word] = packed;
+        }
   });
   return t;
 }
