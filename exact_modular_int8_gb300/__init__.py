@@ -251,6 +251,16 @@ def _prepare(A, B, sync, transb):
     return A, B, dev, flags
 
 
+def _output(out, shape, dtype, like: torch.Tensor, host: bool, what: str) -> torch.Tensor:
+    """A new result tensor, or the caller's `out` after checking that the kernels may write it whole."""
+    if out is None:
+        return torch.empty(shape, dtype=dtype, device=like.device, pin_memory=host)
+    if (not isinstance(out, torch.Tensor) or tuple(out.shape) != tuple(shape) or out.dtype != dtype
+            or out.device != like.device or not out.is_contiguous()):
+        raise ValueError(f"{what}: out must be a contiguous {dtype} tensor of shape {tuple(shape)} on {like.device}")
+    return out
+
+
 def res_gemm_i64(A: torch.Tensor, B: torch.Tensor, nprimes: int = 0, sync: bool = True, out=None,
                  ws: torch.Tensor | None = None, transb: bool = False) -> torch.Tensor:
     """Exact C = A @ B for int64 matrices (CUDA tensors, or CPU tensors staged through the device).
@@ -263,7 +273,7 @@ def res_gemm_i64(A: torch.Tensor, B: torch.Tensor, nprimes: int = 0, sync: bool 
     A, B, dev, flags = _prepare(A, B, sync, transb)
     host = bool(flags & RG_FLAG_HOST)
     shape = (batch, M, N) if batched else (M, N)
-    C = out if out is not None else torch.empty(shape, dtype=torch.int64, device=A.device, pin_memory=host)
+    C = _output(out, shape, torch.int64, A, host, "res_gemm_i64")
     with torch.cuda.device(dev):
         need = workspace_bytes(RG_OP_I64, M, N, K, nprimes=nprimes, host=host, transb=transb, batch=batch)
         if need == 0:
@@ -287,7 +297,7 @@ def res_gemm_limbs(A: torch.Tensor, B: torch.Tensor, lc: int, nprimes: int = 0, 
     A, B, dev, flags = _prepare(A, B, sync, transb)
     host = bool(flags & RG_FLAG_HOST)
     shape = (batch, M, N, lc) if batched else (M, N, lc)
-    C = out if out is not None else torch.empty(shape, dtype=torch.int64, device=A.device, pin_memory=host)
+    C = _output(out, shape, torch.int64, A, host, "res_gemm_limbs")
     with torch.cuda.device(dev):
         need = workspace_bytes(RG_OP_LIMBS, M, N, K, la, lb, lc, nprimes, host=host, transb=transb, batch=batch)
         if need == 0:
@@ -301,10 +311,11 @@ def res_gemm_limbs(A: torch.Tensor, B: torch.Tensor, lc: int, nprimes: int = 0, 
 
 
 def enclose_gemm(A: torch.Tensor, B: torch.Tensor, sync: bool = True, ws: torch.Tensor | None = None,
-                 transb: bool = False):
+                 transb: bool = False, out=None):
     """(lo, hi) with lo <= A @ B <= hi entrywise in exact arithmetic, in the operands' format
     (float64 or float32).  With transb, B is given as [N, K] and the bracket is of A @ B.T.
-    A [b, M, K] and B [b, K, N] run as one batched call sharing one plan."""
+    A [b, M, K] and B [b, K, N] run as one batched call sharing one plan.  `out` may give the
+    (lo, hi) pair to write."""
     if A.dtype != B.dtype or A.dtype not in (torch.float64, torch.float32):
         raise ValueError("float64 or float32 operands of one dtype expected")
     sh = _shapes(A, B, transb, 0)
@@ -316,9 +327,11 @@ def enclose_gemm(A: torch.Tensor, B: torch.Tensor, sync: bool = True, ws: torch.
     A, B, dev, flags = _prepare(A, B, sync, transb)
     pin = bool(flags & RG_FLAG_HOST)
     shape = (batch, M, N) if batched else (M, N)
-    lo = torch.empty(shape, dtype=A.dtype, device=A.device, pin_memory=pin)
-    hi = torch.empty(shape, dtype=A.dtype, device=A.device, pin_memory=pin)
     name = "enclose_gemm_f32" if f32 else "enclose_gemm_f64"
+    if out is not None and (not isinstance(out, (tuple, list)) or len(out) != 2):
+        raise ValueError(f"{name}: out must be a (lo, hi) pair")
+    lo = _output(None if out is None else out[0], shape, A.dtype, A, pin, name)
+    hi = _output(None if out is None else out[1], shape, A.dtype, A, pin, name)
     with torch.cuda.device(dev):
         need = workspace_bytes(op, M, N, K, host=pin, transb=transb, batch=batch)
         if need == 0:
@@ -332,11 +345,11 @@ def enclose_gemm(A: torch.Tensor, B: torch.Tensor, sync: bool = True, ws: torch.
 
 
 def enclose_gemm_f64(A: torch.Tensor, B: torch.Tensor, sync: bool = True, ws: torch.Tensor | None = None,
-                     transb: bool = False):
+                     transb: bool = False, out=None):
     """enclose_gemm for float64 operands (float64 bounds)."""
     if A.dtype != torch.float64 or B.dtype != torch.float64:
         raise ValueError("float64 operands expected")
-    return enclose_gemm(A, B, sync, ws, transb)
+    return enclose_gemm(A, B, sync, ws, transb, out)
 
 
 def enclose_gemm_f32(A: torch.Tensor, B: torch.Tensor, sync: bool = True, ws: torch.Tensor | None = None,

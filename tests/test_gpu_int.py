@@ -180,3 +180,24 @@ def test_stage_events_time_a_real_call(rg):
     rg.res_gemm_i64(dev(A), dev(B))
     torch.cuda.synchronize()
     assert [evs[i].elapsed_time(evs[i + 1]) for i in range(3)] == spans
+
+
+def test_out_tensor_is_checked_and_written(rg):
+    A, B = int_matrices(33, 20, 17, -1000, 1000, 5)
+    dA, dB = dev(A), dev(B)
+    out = torch.full((33, 20), 7, dtype=torch.int64, device="cuda")
+    C = rg.res_gemm_i64(dA, dB, out=out)
+    assert C.data_ptr() == out.data_ptr() and np.array_equal(host(out), A @ B)
+    for bad in (torch.empty((33, 21), dtype=torch.int64, device="cuda"),
+                torch.empty((33, 20), dtype=torch.int32, device="cuda"),
+                torch.empty((20, 33), dtype=torch.int64, device="cuda").t(),
+                torch.empty((33, 20), dtype=torch.int64)):
+        with pytest.raises(ValueError):
+            rg.res_gemm_i64(dA, dB, out=bad)
+    lo = torch.empty((33, 20), dtype=torch.float64, device="cuda")
+    hi = torch.empty_like(lo)
+    Af, Bf = A.astype(np.float64), B.astype(np.float64)
+    rlo, rhi = rg.enclose_gemm_f64(dev(Af), dev(Bf), out=(lo, hi))
+    assert rlo.data_ptr() == lo.data_ptr() and np.array_equal(host(lo), Af @ Bf) and np.array_equal(host(hi), Af @ Bf)
+    with pytest.raises(ValueError):
+        rg.enclose_gemm_f64(dev(Af), dev(Bf), out=(lo,))
