@@ -17,7 +17,9 @@ Helpers: width_ulps, digest, get_plan, workspace_bytes.
 """
 from __future__ import annotations
 
+import contextlib
 import ctypes
+import functools
 import hashlib
 from fractions import Fraction
 import os
@@ -168,9 +170,13 @@ def _layout_flags(host, transb):
     return (RG_FLAG_HOST if host else 0) | (RG_FLAG_TRANS_B if transb else 0)
 
 
+@functools.lru_cache(maxsize=512)
+def _ws_bytes(op, batch, M, N, K, la, lb, lc, nprimes, flags) -> int:
+    return int(library().rg_workspace_bytes_batched(op, batch, M, N, K, la, lb, lc, nprimes, flags))
+
+
 def workspace_bytes(op, M, N, K, la=1, lb=1, lc=1, nprimes=0, host=False, transb=False, batch=1) -> int:
-    return int(library().rg_workspace_bytes_batched(op, batch, M, N, K, la, lb, lc, nprimes,
-                                                    _layout_flags(host, transb)))
+    return _ws_bytes(op, batch, M, N, K, la, lb, lc, nprimes, _layout_flags(host, transb))
 
 
 def workspace_layout(op, M, N, K, la=1, lb=1, lc=1, nprimes=0, host=False, transb=False, batch=1) -> Layout:
@@ -219,6 +225,11 @@ def _call_ctx(A, B):
     if dev.type == "cpu":
         return torch.device("cuda", torch.cuda.current_device()), RG_FLAG_HOST
     raise ValueError(f"unsupported device {dev}")
+
+
+def _on(dev):
+    """The device context of a call: none when `dev` is already the current device."""
+    return contextlib.nullcontext() if dev.index == torch.cuda.current_device() else torch.cuda.device(dev)
 
 
 def _check(rc, where):
@@ -274,7 +285,7 @@ def res_gemm_i64(A: torch.Tensor, B: torch.Tensor, nprimes: int = 0, sync: bool 
     host = bool(flags & RG_FLAG_HOST)
     shape = (batch, M, N) if batched else (M, N)
     C = _output(out, shape, torch.int64, A, host, "res_gemm_i64")
-    with torch.cuda.device(dev):
+    with _on(dev):
         need = workspace_bytes(RG_OP_I64, M, N, K, nprimes=nprimes, host=host, transb=transb, batch=batch)
         if need == 0:
             raise ResGemmError(RG_ERR_ARG, "res_gemm_i64")
@@ -298,7 +309,7 @@ def res_gemm_limbs(A: torch.Tensor, B: torch.Tensor, lc: int, nprimes: int = 0, 
     host = bool(flags & RG_FLAG_HOST)
     shape = (batch, M, N, lc) if batched else (M, N, lc)
     C = _output(out, shape, torch.int64, A, host, "res_gemm_limbs")
-    with torch.cuda.device(dev):
+    with _on(dev):
         need = workspace_bytes(RG_OP_LIMBS, M, N, K, la, lb, lc, nprimes, host=host, transb=transb, batch=batch)
         if need == 0:
             raise ResGemmError(RG_ERR_ARG, "res_gemm_limbs")
@@ -332,7 +343,7 @@ def enclose_gemm(A: torch.Tensor, B: torch.Tensor, sync: bool = True, ws: torch.
         raise ValueError(f"{name}: out must be a (lo, hi) pair")
     lo = _output(None if out is None else out[0], shape, A.dtype, A, pin, name)
     hi = _output(None if out is None else out[1], shape, A.dtype, A, pin, name)
-    with torch.cuda.device(dev):
+    with _on(dev):
         need = workspace_bytes(op, M, N, K, host=pin, transb=transb, batch=batch)
         if need == 0:
             raise ResGemmError(RG_ERR_ARG, name)
@@ -397,7 +408,7 @@ def interval_gemm(Am: torch.Tensor, Ar: torch.Tensor, Bm: torch.Tensor, Br: torc
     lo = torch.empty(shape, dtype=Am.dtype, device=Am.device, pin_memory=pin)
     hi = torch.empty(shape, dtype=Am.dtype, device=Am.device, pin_memory=pin)
     name = "interval_gemm_f32" if f32 else "interval_gemm_f64"
-    with torch.cuda.device(dev):
+    with _on(dev):
         need = workspace_bytes(op, M, N, K, host=pin, transb=transb, batch=batch)
         if need == 0:
             raise ResGemmError(RG_ERR_ARG, name)
@@ -437,7 +448,7 @@ def res_gemm_stage(RA: torch.Tensor, RB: torch.Tensor, nprimes: int, M: int, N: 
         RC = torch.empty((nprimes, M, ldc), dtype=torch.uint8, device=RA.device)
     dev = RA.device
     flags = (RG_FLAG_SYNC if sync else 0) | (RG_FLAG_TRANS_B if transb else 0)
-    with torch.cuda.device(dev):
+    with _on(dev):
         w = workspace(4096, dev)
         rc = library().res_gemm_stage(RA.data_ptr(), lda, RB.data_ptr(), ldb, RC.data_ptr(), RC.shape[-1], nprimes,
                                       M, N, K, flags, w.data_ptr(), w.numel(),
@@ -451,7 +462,7 @@ def get_plan(ws: torch.Tensor | None = None, device=None) -> dict:
     dev = torch.device("cuda", torch.cuda.current_device()) if device is None else torch.device(device)
     w = ws if ws is not None else workspace(4096, dev)
     info = PlanInfo()
-    with torch.cuda.device(dev):
+    with _on(dev):
         _check(library().rg_get_plan(w.data_ptr(), torch.cuda.current_stream(dev).cuda_stream, ctypes.byref(info)),
                "rg_get_plan")
     return info.as_dict()
@@ -478,7 +489,7 @@ def set_stage_events(events) -> None:
 def status(ws: torch.Tensor | None = None, device=None) -> int:
     dev = torch.device("cuda", torch.cuda.current_device()) if device is None else torch.device(device)
     w = ws if ws is not None else workspace(4096, dev)
-    with torch.cuda.device(dev):
+    with _on(dev):
         return int(library().rg_status(w.data_ptr(), torch.cuda.current_stream(dev).cuda_stream))
 
 
@@ -564,7 +575,7 @@ def solve_integers(A: torch.Tensor, b: torch.Tensor, info: dict | None = None):
     dev, flags = _call_ctx(A, b2)
     n, c = A.shape[0], b2.shape[1]
     sol = Solution()
-    with torch.cuda.device(dev):
+    with _on(dev):
         rc = library().rg_solve_i64(A.data_ptr(), b2.data_ptr(), n, c, flags,
                                     torch.cuda.current_stream(dev).cuda_stream, ctypes.byref(sol))
     if rc == RG_ERR_SINGULAR:

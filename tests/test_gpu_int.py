@@ -201,3 +201,28 @@ def test_out_tensor_is_checked_and_written(rg):
     assert rlo.data_ptr() == lo.data_ptr() and np.array_equal(host(lo), Af @ Bf) and np.array_equal(host(hi), Af @ Bf)
     with pytest.raises(ValueError):
         rg.enclose_gemm_f64(dev(Af), dev(Bf), out=(lo,))
+
+
+@pytest.mark.parametrize("pin_in,pin_out", [(True, True), (False, True), (True, False), (False, False)])
+def test_host_buffers_pinned_or_pageable(rg, pin_in, pin_out):
+    """Pinned host buffers are used in place (int64 operands, every output), pageable ones are
+    staged; all four mixes give the exact product, as does the enclosure (operands always staged)."""
+    A, B = int_matrices(130, 70, 300, -(2**23), 2**23, 23)
+    hA, hB = torch.from_numpy(A), torch.from_numpy(B)
+    if pin_in:
+        hA, hB = hA.pin_memory(), hB.pin_memory()
+    out = torch.empty((130, 70), dtype=torch.int64)
+    if pin_out:
+        out = out.pin_memory()
+    C = rg.res_gemm_i64(hA, hB, out=out)
+    assert C.data_ptr() == out.data_ptr() and np.array_equal(C.numpy(), A @ B)
+    Af, Bf = (A >> 8).astype(np.float64), (B >> 8).astype(np.float64)
+    fA, fB = torch.from_numpy(Af), torch.from_numpy(Bf)
+    if pin_in:
+        fA, fB = fA.pin_memory(), fB.pin_memory()
+    lo, hi = torch.empty((130, 70), dtype=torch.float64), torch.empty((130, 70), dtype=torch.float64)
+    if pin_out:
+        lo, hi = lo.pin_memory(), hi.pin_memory()
+    rlo, rhi = rg.enclose_gemm_f64(fA, fB, out=(lo, hi))
+    ref = Af @ Bf  # products of 15-bit integers summed over 300 terms: exact in float64
+    assert np.array_equal(rlo.numpy(), ref) and np.array_equal(rhi.numpy(), ref)
