@@ -56,9 +56,11 @@ __device__ __forceinline__ void add_scaled_weight(uint32_t (&x)[W], int D, int i
 
 // x[e] (W 32-bit words, two's complement) = the reconstructed integers of the
 // GE residue vectors starting at rc (plane = distance between primes).
-// Digits are combined in pairs, D = v_i + q_i v_{i+1} (|D| < 2^15, exact in
-// fp32), so the wide accumulation runs once per two primes.  MAXP bounds P
-// at compile time (the packed digits take (MAXP + 3) / 4 registers per entry).
+// Digits are combined four at a time, D = v_i + q_i v_{i+1} + q_i q_{i+1}
+// (v_{i+2} + q_{i+2} v_{i+3}), |D| <= (q_i q_{i+1} q_{i+2} q_{i+3} - 1) / 2 < 2^31:
+// the pairs in fp32 (|pair| < 2^15), the quad in int32, so the wide
+// accumulation runs once per four primes.  MAXP bounds P at compile time (the
+// packed digits take (MAXP + 3) / 4 registers per entry).
 template <int W, int GE, typename TAB, int MAXP = kNumPrimes>
 __device__ __forceinline__ void garner_reconstruct(const uint8_t* __restrict__ rc, long long plane, int P,
                                                    uint32_t (&x)[GE][W]) {
@@ -66,6 +68,7 @@ __device__ __forceinline__ void garner_reconstruct(const uint8_t* __restrict__ r
   constexpr int kWords = (MAXP + 3) / 4;
   uint32_t V[GE][kWords];
   float pend[GE];  // the even digit of the current pair, as float
+  int dq[GE];      // the first pair of the current quad
 #pragma unroll
   for (int e = 0; e < GE; ++e) {
 #pragma unroll
@@ -73,6 +76,7 @@ __device__ __forceinline__ void garner_reconstruct(const uint8_t* __restrict__ r
 #pragma unroll
     for (int k = 0; k < W; ++k) x[e][k] = 0u;
     pend[e] = 0.0f;
+    dq[e] = 0;
   }
 #pragma unroll
   for (int i0 = 0; i0 < MAXP; i0 += kGarnerBatch) {
@@ -108,18 +112,31 @@ __device__ __forceinline__ void garner_reconstruct(const uint8_t* __restrict__ r
         const float vf = bal_mod_small(int_to_float_exact(acc), q, iq);
         const int vb = float_bits_offset(vf);
         V[e][i / 4] = __byte_perm(V[e][i / 4], (uint32_t)vb, kSel[i % 4]);
+        const int s0 = i & ~3;  // the quad's first prime
+        int d = 0;              // the quad's value, when it is added now
+        bool add = false;
         if ((i & 1) == 0) {
           pend[e] = vf;
-          if (i + 1 >= P) {  // unpaired last digit
-            if (W > 2 && (i % 4) == 0 && i > 0 && i / 4 + 1 < W)
-              x[e][i / 4 + 1] = (uint32_t)((int)x[e][i / 4] >> 31);
-            add_scaled_weight<W, TAB>(x[e], vb - kMagicBits, i, i);
+          if (i + 1 >= P) {  // the last digit opens a pair: v_i, or the first pair plus q_{i-2} q_{i-1} v_i
+            d = (i & 2) ? dq[e] + TAB::t().q[i - 2] * TAB::t().q[i - 1] * (vb - kMagicBits) : vb - kMagicBits;
+            add = true;
           }
         } else {
-          const float D = __fmaf_rn(vf, TAB::t().qf[i - 1], pend[e]);  // v_{i-1} + q_{i-1} v_i
-          if (W > 2 && ((i - 1) % 4) == 0 && i > 1 && (i - 1) / 4 + 1 < W)
-            x[e][(i - 1) / 4 + 1] = (uint32_t)((int)x[e][(i - 1) / 4] >> 31);
-          add_scaled_weight<W, TAB>(x[e], float_bits_offset(D) - kMagicBits, i - 1, i);
+          const int pair = float_bits_offset(__fmaf_rn(vf, TAB::t().qf[i - 1], pend[e])) - kMagicBits;
+          if ((i & 2) == 0) {  // the quad's first pair
+            dq[e] = pair;
+            if (i + 1 >= P) {
+              d = pair;
+              add = true;
+            }
+          } else {
+            d = dq[e] + TAB::t().q[i - 3] * TAB::t().q[i - 2] * pair;
+            add = true;
+          }
+        }
+        if (add) {
+          if (W > 2 && s0 > 0 && s0 / 4 + 1 < W) x[e][s0 / 4 + 1] = (uint32_t)((int)x[e][s0 / 4] >> 31);
+          add_scaled_weight<W, TAB>(x[e], d, s0, i);
         }
       }
     }
