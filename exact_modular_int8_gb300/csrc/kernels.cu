@@ -285,26 +285,65 @@ __global__ void __launch_bounds__(256) plan_i64_kernel(const int64_t* __restrict
 }
 
 // Bit length of |x| for multi-limb x (two's complement, signed top limb).
-__device__ __forceinline__ int limb_magnitude_bits(const int64_t* x, int L) {
-  unsigned long long w[RG_MAX_LIMBS_IN];
-  const bool neg = x[L - 1] < 0;
-  unsigned long long carry = 1;
+// Bit length of |x| for an L-limb two's-complement integer held in w.
+template <int L>
+__device__ __forceinline__ int limb_magnitude_bits(const unsigned long long (&w)[L]) {
+  const bool neg = (long long)w[L - 1] < 0;
+  unsigned long long carry = 1, m[L];
 #pragma unroll
-  for (int i = 0; i < RG_MAX_LIMBS_IN; ++i) {
-    if (i < L) {
-      unsigned long long v = (unsigned long long)x[i];
-      if (neg) {
-        v = ~v + carry;
-        carry = (v == 0 && carry) ? 1 : 0;
-      }
-      w[i] = v;
+  for (int i = 0; i < L; ++i) {
+    unsigned long long v = w[i];
+    if (neg) {
+      v = ~v + carry;
+      carry = (v == 0 && carry) ? 1 : 0;
     }
+    m[i] = v;
   }
   int b = 0;
 #pragma unroll
-  for (int i = 0; i < RG_MAX_LIMBS_IN; ++i)
-    if (i < L && w[i]) b = 64 * i + bitlen64(w[i]);
+  for (int i = 0; i < L; ++i)
+    if (m[i]) b = 64 * i + bitlen64(m[i]);
   return b;
+}
+
+// VEC: 16-byte loads (L even and the base 16-byte aligned, which the caller checks).
+template <int L, bool VEC>
+__device__ __forceinline__ void load_limbs(const int64_t* __restrict__ x, unsigned long long (&w)[L]) {
+  if constexpr (VEC) {
+    static_assert(L % 2 == 0, "pairs of limbs");
+#pragma unroll
+    for (int i = 0; i < L; i += 2) {
+      const ulonglong2 v = __ldg(reinterpret_cast<const ulonglong2*>(x) + i / 2);
+      w[i] = v.x;
+      w[i + 1] = v.y;
+    }
+  } else {
+#pragma unroll
+    for (int i = 0; i < L; ++i) w[i] = (unsigned long long)__ldg(x + i);
+  }
+}
+
+// max bit length over n L-limb entries of X, strided as the planner side says;
+// four entries' limbs are loaded before any is examined.
+template <int L, bool VEC>
+__device__ __forceinline__ int scan_limbs(const int64_t* __restrict__ X, long long n, const PlannerSide& sd) {
+  int m = 0;
+  long long i = sd.b0 * blockDim.x + threadIdx.x;
+  for (; i + 3 * sd.stride < n; i += 4 * sd.stride) {
+    unsigned long long w0[L], w1[L], w2[L], w3[L];
+    load_limbs<L, VEC>(X + i * L, w0);
+    load_limbs<L, VEC>(X + (i + sd.stride) * L, w1);
+    load_limbs<L, VEC>(X + (i + 2 * sd.stride) * L, w2);
+    load_limbs<L, VEC>(X + (i + 3 * sd.stride) * L, w3);
+    m = max(m, max(max(limb_magnitude_bits<L>(w0), limb_magnitude_bits<L>(w1)),
+                   max(limb_magnitude_bits<L>(w2), limb_magnitude_bits<L>(w3))));
+  }
+  for (; i < n; i += sd.stride) {
+    unsigned long long w[L];
+    load_limbs<L, VEC>(X + i * L, w);
+    m = max(m, limb_magnitude_bits<L>(w));
+  }
+  return m;
 }
 
 __global__ void __launch_bounds__(256) plan_limbs_kernel(const int64_t* __restrict__ A, long long nA, int la,
@@ -314,16 +353,15 @@ __global__ void __launch_bounds__(256) plan_limbs_kernel(const int64_t* __restri
   const int64_t* X = sd.isA ? A : B;
   const long long n = sd.isA ? nA : nB;
   const int L = sd.isA ? la : lb;
+  // even limb counts read 16 bytes at a time when the base is 16-byte aligned
+  const bool aligned = (reinterpret_cast<uintptr_t>(X) & 15u) == 0;
   int m = 0;
-  long long i = sd.b0 * blockDim.x + threadIdx.x;
-  for (; i + 3 * sd.stride < n; i += 4 * sd.stride) {  // four independent entries in flight
-    const int b0 = limb_magnitude_bits(X + i * L, L);
-    const int b1 = limb_magnitude_bits(X + (i + sd.stride) * L, L);
-    const int b2 = limb_magnitude_bits(X + (i + 2 * sd.stride) * L, L);
-    const int b3 = limb_magnitude_bits(X + (i + 3 * sd.stride) * L, L);
-    m = max(m, max(max(b0, b1), max(b2, b3)));
+  switch (L) {
+    case 1: m = scan_limbs<1, false>(X, n, sd); break;
+    case 2: m = aligned ? scan_limbs<2, true>(X, n, sd) : scan_limbs<2, false>(X, n, sd); break;
+    case 3: m = scan_limbs<3, false>(X, n, sd); break;
+    default: m = aligned ? scan_limbs<4, true>(X, n, sd) : scan_limbs<4, false>(X, n, sd); break;
   }
-  for (; i < n; i += sd.stride) m = max(m, limb_magnitude_bits(X + i * L, L));
   m = block_max_i32(m);
   if (threadIdx.x == 0 && m) atomicMax(sd.isA ? &plan->maxbits_a : &plan->maxbits_b, m);
   planner_finish(plan, pa);
@@ -358,9 +396,7 @@ __device__ __forceinline__ void scan_float(const Bits* __restrict__ X, long long
     exponent_stats<Bits>(v, emax, einv, bad);
     if (radius && (v & F::kSign) && (Bits)(v << 1) != 0) negr = 1;
   };
-#pragma unroll 4
-  for (long long i = sd.b0 * blockDim.x + threadIdx.x; i < nv; i += sd.stride) {
-    const uint4 v = __ldg(X4 + i);
+  auto chunk = [&](const uint4& v) {
     if constexpr (PER == 4) {
       one(v.x);
       one(v.y);
@@ -370,7 +406,17 @@ __device__ __forceinline__ void scan_float(const Bits* __restrict__ X, long long
       one(((unsigned long long)v.y << 32) | v.x);
       one(((unsigned long long)v.w << 32) | v.z);
     }
+  };
+  long long i = sd.b0 * blockDim.x + threadIdx.x;
+  for (; i + 3 * sd.stride < nv; i += 4 * sd.stride) {  // four 16-byte loads in flight before any work
+    const uint4 v0 = __ldg(X4 + i), v1 = __ldg(X4 + i + sd.stride), v2 = __ldg(X4 + i + 2 * sd.stride),
+                v3 = __ldg(X4 + i + 3 * sd.stride);
+    chunk(v0);
+    chunk(v1);
+    chunk(v2);
+    chunk(v3);
   }
+  for (; i < nv; i += sd.stride) chunk(__ldg(X4 + i));
   for (long long i = PER * nv + sd.b0 * blockDim.x + threadIdx.x; i < n; i += sd.stride) one(__ldg(X + i));
 }
 
@@ -1279,7 +1325,9 @@ cudaError_t upload_tables() {
 
 static int planner_blocks(long long n) {
   long long b = (n + 256LL * 8 - 1) / (256LL * 8);
-  long long cap = 4LL * sm_count();  // enough loads in flight; each block ends with a few atomics on the plan
+  // two blocks per SM and side: with four 16-byte loads in flight per thread
+  // that covers HBM latency, and every block ends with atomics on the plan
+  long long cap = 2LL * sm_count();
   return (int)(b < 1 ? 1 : (b > cap ? cap : b));
 }
 
