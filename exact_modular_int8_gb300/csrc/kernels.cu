@@ -462,9 +462,9 @@ __global__ void __launch_bounds__(256) plan_float_kernel(const Bits* __restrict_
 //
 // Floating point: |x| 2^f = t 2^sh, t the significand (or, at a coarsened
 // point, the floored scaled magnitude with sh = 0), so
-//   x 2^f mod q == +-(t mod q)(2^sh mod q)   (mod q),
-// with 2^sh mod q from a per-block table; the product of two balanced
-// residues is below 2^14 and is reduced once more.
+//   x 2^f mod q == +-(t 2^sh mod q)   (mod q),
+// and t 2^sh mod q is the dot product of t's bytes with the byte weights
+// bal(2^(8k + sh) mod q) of its shift (ShiftWeights), reduced once.
 //
 // Residues are written as fp16 (exact for |r| <= 125).  Columns from C up to
 // the padded row length are written as zeros.  Grid-stride over the items
