@@ -80,3 +80,29 @@ def test_range_errors(rg):
     with pytest.raises(rg.ResGemmError) as e:  # needs 259 bits, 2 limbs hold 127
         rg.res_gemm_limbs(dev(A), dev(B), 2)
     assert e.value.code == rg.RG_ERR_RANGE
+
+
+@pytest.mark.parametrize("la,lb", [(2, 2), (4, 4), (2, 4)])
+def test_operands_off_16_byte_alignment(rg, la, lb):
+    """Operands starting 8 bytes past a 16-byte boundary take the scalar-load paths of the planner and the split."""
+    rng = np.random.default_rng(la + 10 * lb)
+    M, N, K = 37, 41, 53
+    full = dict(low=-(2**63), high=2**63 - 1, endpoint=True, dtype=np.int64)
+
+    def operand(shape, limbs):
+        # 128-bit values in `limbs` limbs (upper limbs sign-extend), so the product stays within the 332-bit gate
+        x = rng.integers(size=shape + (2,), **full)
+        ext = np.repeat((x[..., 1:2] < 0).astype(np.int64) * -1, limbs - 2, axis=-1)
+        return np.concatenate([x, ext], axis=-1) if limbs > 2 else x
+
+    A = operand((M, K), la)
+    B = operand((K, N), lb)
+    bufA = torch.empty(A.size + 1, dtype=torch.int64, device="cuda")
+    bufB = torch.empty(B.size + 1, dtype=torch.int64, device="cuda")
+    dA = bufA[1:].view(M, K, la)
+    dB = bufB[1:].view(K, N, lb)
+    dA.copy_(torch.from_numpy(A))
+    dB.copy_(torch.from_numpy(B))
+    assert dA.data_ptr() % 16 == 8 and dB.data_ptr() % 16 == 8
+    C = host(rg.res_gemm_limbs(dA, dB, 6))
+    assert np.array_equal(C, oracle.matmul_limbs(A, B, 6))
