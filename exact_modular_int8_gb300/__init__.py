@@ -371,15 +371,29 @@ def enclose_gemm_f32(A: torch.Tensor, B: torch.Tensor, sync: bool = True, ws: to
     return enclose_gemm(A, B, sync, ws, transb)
 
 
-def mm_enclose(A: torch.Tensor, B: torch.Tensor):
+def _enclose_info(A: torch.Tensor) -> dict:
+    """The regime of the last enclosure on A's device ("enclosure-gemm", Method: the lossless
+    one-step bracket, or a coarsened fixed point whose flooring bound is added outward)."""
+    dev = A.device if A.device.type == "cuda" else None
+    plan = get_plan(device=dev)
+    lossless = bool(plan["lossless"])
+    return {"regime": "lossless" if lossless else "coarsened", "lossless": lossless, "nprimes": plan["nprimes"],
+            "scale_exponents": (plan["f_a"], plan["f_b"]), "bound_bits": plan["bound_bits"]}
+
+
+def mm_enclose(A: torch.Tensor, B: torch.Tensor, return_info: bool = False):
     """lo <= A @ B <= hi entrywise, exactly, for float64 or float32 operands
-    ("enclosure-gemm", Usage: mm_enclose)."""
-    return enclose_gemm(A, B)
+    ("enclosure-gemm", Usage: mm_enclose).  With return_info, also a dict naming the regime
+    (lossless, or coarsened with the flooring bound added outward) and the plan's prime count and
+    scale exponents."""
+    lo, hi = enclose_gemm(A, B)
+    return (lo, hi, _enclose_info(A)) if return_info else (lo, hi)
 
 
-def mm_enclose_nt(A: torch.Tensor, Bt: torch.Tensor):
+def mm_enclose_nt(A: torch.Tensor, Bt: torch.Tensor, return_info: bool = False):
     """The bracket of A @ Bt.T without a transposed copy ("enclosure-gemm", Usage: mm_enclose_nt)."""
-    return enclose_gemm(A, Bt, transb=True)
+    lo, hi = enclose_gemm(A, Bt, transb=True)
+    return (lo, hi, _enclose_info(A)) if return_info else (lo, hi)
 
 
 def interval_gemm(Am: torch.Tensor, Ar: torch.Tensor, Bm: torch.Tensor, Br: torch.Tensor, sync: bool = True,
@@ -426,12 +440,13 @@ def mm_interval(A_mid: torch.Tensor, A_rad: torch.Tensor, B_mid: torch.Tensor, B
     return interval_gemm(A_mid, A_rad, B_mid, B_rad)
 
 
-def bmm_enclose(A: torch.Tensor, B: torch.Tensor):
+def bmm_enclose(A: torch.Tensor, B: torch.Tensor, return_info: bool = False):
     """Brackets of the batch A [b, M, K] @ B [b, K, N] with one shared plan
     ("enclosure-gemm", Usage: bmm_enclose)."""
     if A.dim() != 3 or B.dim() != 3:
         raise ValueError("A [b,M,K] and B [b,K,N] expected")
-    return enclose_gemm(A, B)
+    lo, hi = enclose_gemm(A, B)
+    return (lo, hi, _enclose_info(A)) if return_info else (lo, hi)
 
 
 def res_gemm_stage(RA: torch.Tensor, RB: torch.Tensor, nprimes: int, M: int, N: int, K: int, RC=None,

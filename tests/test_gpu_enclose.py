@@ -144,3 +144,22 @@ def test_host_buffers_and_digest(rg):
     lo2, hi2 = rg.enclose_gemm_f64(torch.from_numpy(A), torch.from_numpy(B))
     assert lo2.device.type == "cpu"
     assert rg.digest(lo1, hi1) == rg.digest(lo2, hi2)
+
+
+def test_return_info_reports_the_regime(rg):
+    """return_info names the regime ("enclosure-gemm", Method: lossless one-step bracket, or coarsened)."""
+    B = np.ones((4, 1))
+    wide = np.array([[1e300, 1.0, -1e300, 2.0**-60]], dtype=np.float64)
+    lo, hi, info = rg.mm_enclose(dev(wide), dev(B), return_info=True)
+    assert info["regime"] == "coarsened" and not info["lossless"]
+    rlo, rhi = oracle.enclose_f64(wide, B)
+    check_contains(host(lo), host(hi), rlo, rhi)
+    narrow = np.array([[2.0**100, 1.0, -(2.0**100), 3 * 2.0**-60]], dtype=np.float64)
+    lo, hi, info = rg.mm_enclose_nt(dev(narrow), dev(B.T.copy()), return_info=True)
+    assert info["regime"] == "lossless" and info["lossless"] and info["nprimes"] >= 1
+    rlo, rhi = oracle.enclose_f64(narrow, B)
+    assert np.array_equal(host(lo), rlo) and np.array_equal(host(hi), rhi)
+    lo, hi = rg.bmm_enclose(dev(narrow[None]), dev(B[None]))
+    assert np.array_equal(host(lo)[0], rlo)
+    lo, hi, info = rg.bmm_enclose(dev(narrow[None]), dev(B[None]), return_info=True)
+    assert info["lossless"]
