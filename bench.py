@@ -116,7 +116,15 @@ def workload_description(w):
         return f"int64 uniform in [{w.lo}, {w.hi})"
     if w.kind == "limbs":
         return f"signed {64 * w.limbs}-bit integers as {w.limbs} int64 limbs, uniform"
+    if w.kind == "normal32":
+        return "float32 i.i.d. standard normal (the float64 draw rounded)"
+    if w.kind == "interval":
+        return "float64 intervals: midpoints standard normal, radii uniform in [0, 2^-20) x |midpoint|"
     return "float64 i.i.d. standard normal"
+
+
+def workload_dtype(w):
+    return {"normal": "f64", "interval": "f64", "normal32": "f32"}.get(w.kind, "int64")
 
 
 # ---------------------------------------------------------------------------
@@ -131,6 +139,10 @@ def oracle_call(w, A, B, rows):
         return oracle.matmul_i64(A, B, lc=1 if w.out_limbs == 1 else w.out_limbs, rows=rows)
     if w.kind == "limbs":
         return oracle.matmul_limbs(A, B, w.out_limbs, rows=rows)
+    if w.kind == "normal32":
+        return oracle.enclose_f32(A, B, rows=rows)
+    if w.kind == "interval":
+        return oracle.interval(A[0], A[1], B[0], B[1], rows=rows)
     return oracle.enclose_f64(A, B, rows=rows)
 
 
@@ -196,7 +208,7 @@ def run_reference(args):
     line = {
         "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": args.gpus, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": t * 1e3, "higher_is_better": True, "scaling": "weak",
-        "vs_baseline": None, "dtype": "int64" if w.kind != "normal" else "f64", "data": "synthetic",
+        "vs_baseline": None, "dtype": workload_dtype(w), "data": "synthetic",
         "config": {"workload": w.name, "M": w.M, "N": w.N, "K": w.K, "entries": workload_description(w),
                    "seed": w.seed, "step": f"{rows} output rows per step (bounded sample)"},
         "cpu_baseline": {"value": value, "unit": UNIT, "cores": oracle.threads_used(), "kind": "oracle",
@@ -341,7 +353,9 @@ def main():
             return rg.res_gemm_i64(dA, dB, sync=False, out=out)
         if w.kind == "limbs":
             return rg.res_gemm_limbs(dA, dB, w.out_limbs, sync=False, out=out)
-        return rg.enclose_gemm_f64(dA, dB, sync=False, out=out)
+        if w.kind == "interval":  # A, B hold (midpoint, radius) stacked
+            return rg.interval_gemm(dA[0], dA[1], dB[0], dB[1], sync=False, out=out)
+        return rg.enclose_gemm(dA, dB, sync=False, out=out)
 
     flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
     out = None
@@ -403,29 +417,34 @@ def main():
     # with L2 flushed before each launch (inputs cold in HBM)
     P = plan["nprimes"]
     peaks, peak_src = load_peaks()
-    op = {"int": rg.RG_OP_I64, "limbs": rg.RG_OP_LIMBS, "normal": rg.RG_OP_ENCLOSE}[w.kind]
+    op = {"int": rg.RG_OP_I64, "limbs": rg.RG_OP_LIMBS, "normal": rg.RG_OP_ENCLOSE, "normal32": rg.RG_OP_ENCLOSE_F32,
+          "interval": rg.RG_OP_INTERVAL}[w.kind]
+    products = 3 if w.kind == "interval" else 1  # an interval product is three exact products
     la = lb = w.limbs if w.kind == "limbs" else 1
     lc = w.out_limbs if w.kind == "limbs" else 1
     L = rg.workspace_layout(op, w.M, w.N, w.K, la, lb, lc)
     ws = rg.workspace(rg.workspace_bytes(op, w.M, w.N, w.K, la, lb, lc), dev)
-    ra = ws[L.ra:L.ra + P * w.M * L.lda * 2].view(torch.float16).view(P, w.M, L.lda)
-    rb = ws[L.rb:L.rb + P * w.K * L.ldb * 2].view(torch.float16).view(P, w.K, L.ldb)
-    rc = torch.empty((P, w.M, L.ldc), dtype=torch.uint8, device=dev)
+    # the alone timing runs the first planes of the workspace as one stage call
+    # (an interval call's 3P planes are capped at the 53 the stage accepts)
+    Pa = min(P * products, len(rg.primes()))
+    ra = ws[L.ra:L.ra + Pa * w.M * L.lda * 2].view(torch.float16).view(Pa, w.M, L.lda)
+    rb = ws[L.rb:L.rb + Pa * w.K * L.ldb * 2].view(torch.float16).view(Pa, w.K, L.ldb)
+    rc = torch.empty((Pa, w.M, L.ldc), dtype=torch.uint8, device=dev)
     for _ in range(3):
-        rg.res_gemm_stage(ra, rb, P, w.M, w.N, w.K, RC=rc, sync=False)
+        rg.res_gemm_stage(ra, rb, Pa, w.M, w.N, w.K, RC=rc, sync=False)
     gt = []
     for _ in range(args.steps):
         flush.fill_(1.0)
         e0 = torch.cuda.Event(enable_timing=True)
         e1 = torch.cuda.Event(enable_timing=True)
         e0.record(stream)
-        rg.res_gemm_stage(ra, rb, P, w.M, w.N, w.K, RC=rc, sync=False)
+        rg.res_gemm_stage(ra, rb, Pa, w.M, w.N, w.K, RC=rc, sync=False)
         e1.record(stream)
         gt.append((e0, e1))
     torch.cuda.synchronize(dev)
     gemm_alone_ms = sum(a.elapsed_time(b) for a, b in gt) / len(gt)
     gemm_ms = stages_ms["gemm"]
-    gemm_flops = 2.0 * w.macs * P
+    gemm_flops = 2.0 * w.macs * P * products
     achieved = gemm_flops / (gemm_ms * 1e-3) / 1e12
     peak = float(peaks["bf16_tflops"])  # fp16 and bf16 share the nominal dense rate
     traffic = gemm_traffic_record(os.path.join(ROOT, "exact_modular_int8_gb300", "csrc", "gemm_tc.cu"))
@@ -439,12 +458,12 @@ def main():
                 "peak_source": f"{peak_src} bf16 dense burst (MEASURED_PEAKS.json); fp16 nominal rate equals bf16",
                 "algorithmic_flops_per_launch": gemm_flops, "avg_launch_ms": gemm_ms,
                 "avg_launch": "inside the timed call, events on its stream between the stages",
-                "alone_cold_inputs_ms": gemm_alone_ms, "primes": P}
+                "alone_cold_inputs_ms": gemm_alone_ms, "alone_planes": Pa, "primes": P, "products_per_prime": products}
 
     line = {
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
         "warmup": max(args.warmup, 3), "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak",
-        "vs_baseline": None, "dtype": "int64" if w.kind != "normal" else "f64", "data": "synthetic",
+        "vs_baseline": None, "dtype": workload_dtype(w), "data": "synthetic",
         "config": {"workload": w.name, "M": w.M, "N": w.N, "K": w.K, "entries": workload_description(w),
                    "seed": w.seed, "nprimes": f"planned on the device: {P}",
                    "l2": "flushed between timed steps (512 MiB write outside the timed events)"},
@@ -482,9 +501,12 @@ def measure_e2e(rg, w, A, B, args, dev):
         out = torch.empty((w.M, w.N, w.out_limbs), dtype=torch.int64).pin_memory()
         fn = lambda: rg.res_gemm_limbs(hA, hB, w.out_limbs, out=out)
         d2h = out.numel() * 8
-    else:
-        fn = lambda: rg.enclose_gemm_f64(hA, hB)
+    elif w.kind == "interval":
+        fn = lambda: rg.interval_gemm(hA[0], hA[1], hB[0], hB[1])
         d2h = 2 * w.M * w.N * 8
+    else:
+        fn = lambda: rg.enclose_gemm(hA, hB)
+        d2h = 2 * w.M * w.N * A.itemsize
     for _ in range(3):
         fn()
     torch.cuda.synchronize(dev)

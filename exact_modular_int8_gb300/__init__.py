@@ -397,7 +397,7 @@ def mm_enclose_nt(A: torch.Tensor, Bt: torch.Tensor, return_info: bool = False):
 
 
 def interval_gemm(Am: torch.Tensor, Ar: torch.Tensor, Bm: torch.Tensor, Br: torch.Tensor, sync: bool = True,
-                  ws: torch.Tensor | None = None, transb: bool = False):
+                  ws: torch.Tensor | None = None, transb: bool = False, out=None):
     """(lo, hi) enclosing every product A @ B with A in <Am, Ar>, B in <Bm, Br> (midpoint, radius >= 0),
     by Rump's bound formed exactly and rounded outward once, in the operands' format (float64 or
     float32).  transb gives Bm and Br as [N, K]; a leading batch dimension shares one plan."""
@@ -419,9 +419,11 @@ def interval_gemm(Am: torch.Tensor, Ar: torch.Tensor, Bm: torch.Tensor, Br: torc
     flags |= (RG_FLAG_SYNC if sync else 0) | (RG_FLAG_TRANS_B if transb else 0)
     pin = bool(flags & RG_FLAG_HOST)
     shape = (batch, M, N) if batched else (M, N)
-    lo = torch.empty(shape, dtype=Am.dtype, device=Am.device, pin_memory=pin)
-    hi = torch.empty(shape, dtype=Am.dtype, device=Am.device, pin_memory=pin)
     name = "interval_gemm_f32" if f32 else "interval_gemm_f64"
+    if out is not None and (not isinstance(out, (tuple, list)) or len(out) != 2):
+        raise ValueError(f"{name}: out must be a (lo, hi) pair")
+    lo = _output(None if out is None else out[0], shape, Am.dtype, Am, pin, name)
+    hi = _output(None if out is None else out[1], shape, Am.dtype, Am, pin, name)
     with _on(dev):
         need = workspace_bytes(op, M, N, K, host=pin, transb=transb, batch=batch)
         if need == 0:

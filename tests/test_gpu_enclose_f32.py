@@ -109,3 +109,17 @@ def test_mixed_dtypes_rejected(rg):
     with pytest.raises(ValueError):
         rg.mm_enclose(torch.ones((4, 4), dtype=torch.float32, device="cuda"),
                       torch.ones((4, 4), dtype=torch.float64, device="cuda"))
+
+
+def test_enclose_f32_workload_sampled_rows(rg):
+    """The bench's float32 enclosure workload at full size (1024 x 4096 x 1024): sample rows bit for bit."""
+    from workloads import WORKLOADS, sample_rows
+
+    w = WORKLOADS["enclose_f32"]
+    A, B = w.generate()
+    lo, hi = rg.enclose_gemm_f32(dev(A), dev(B))
+    assert rg.get_plan()["lossless"] == 1
+    rows = sample_rows(w.M, w.seed, n=16)
+    rlo, rhi = oracle.enclose_f32(A, B, rows=rows)
+    assert np.array_equal(host(lo)[rows].view(np.uint32), rlo.view(np.uint32))
+    assert np.array_equal(host(hi)[rows].view(np.uint32), rhi.view(np.uint32))

@@ -102,3 +102,16 @@ def test_negative_radius_rejected(rg):
     with pytest.raises(rg.ResGemmError) as e:
         rg.mm_interval(*(dev(x) for x in (Am, Ar, Bm, Br)))
     assert e.value.code == rg.RG_ERR_RADIUS
+
+
+def test_interval_normal_workload_sampled_rows(rg):
+    """The bench's interval workload at full size (1024 x 4096 x 1024): seeded sample rows bit for bit."""
+    from workloads import WORKLOADS, sample_rows
+
+    w = WORKLOADS["interval_normal"]
+    A, B = w.generate()
+    lo, hi = rg.interval_gemm(dev(A[0]), dev(A[1]), dev(B[0]), dev(B[1]))
+    assert rg.get_plan()["lossless"] == 1
+    rows = sample_rows(w.M, w.seed, n=16)
+    rlo, rhi = oracle.interval(A[0], A[1], B[0], B[1], rows=rows)
+    assert np.array_equal(host(lo)[rows], rlo) and np.array_equal(host(hi)[rows], rhi)

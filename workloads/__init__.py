@@ -21,7 +21,7 @@ class Workload:
     """One named synthetic workload: shapes, entry distribution and seed."""
 
     name: str
-    kind: str  # "int", "limbs" or "normal"
+    kind: str  # "int", "limbs", "normal" (float64), "normal32" (float32) or "interval"
     M: int
     N: int
     K: int
@@ -39,6 +39,11 @@ class Workload:
             return limb_matrices(self.M, self.N, self.K, self.limbs, self.seed)
         if self.kind == "normal":
             return normal_matrices(self.M, self.N, self.K, self.seed)
+        if self.kind == "normal32":
+            A, B = normal_matrices(self.M, self.N, self.K, self.seed)
+            return A.astype(np.float32), B.astype(np.float32)
+        if self.kind == "interval":
+            return interval_matrices(self.M, self.N, self.K, self.seed)
         raise ValueError(self.kind)
 
     @property
@@ -53,6 +58,9 @@ class Workload:
 #  enclose_normal : fp64 standard normal, M=1024, K=4096, N=1024, seed 3
 #  longk_int8     : M=N=512, K=131072, entries in [-128, 128), seed 4
 #  exact24_4096   : 4096^3, entries in [-2^23, 2^23), seed 5 (GEMM-stage scale)
+#  enclose_f32    : enclose_normal's shape and draw, rounded to float32
+#  interval_normal: enclose_normal's shape; midpoints standard normal, radii
+#                   uniform in [0, 2^-20) times |midpoint|, seed 7
 WORKLOADS = {
     "exact24_64": Workload("exact24_64", "int", 64, 64, 64, 0, -(2**23), 2**23),
     "exact24_1024": Workload("exact24_1024", "int", 1024, 1024, 1024, 1, -(2**23), 2**23),
@@ -60,6 +68,8 @@ WORKLOADS = {
     "enclose_normal": Workload("enclose_normal", "normal", 1024, 1024, 4096, 3),
     "longk_int8": Workload("longk_int8", "int", 512, 512, 131072, 4, -128, 128),
     "exact24_4096": Workload("exact24_4096", "int", 4096, 4096, 4096, 5, -(2**23), 2**23),
+    "enclose_f32": Workload("enclose_f32", "normal32", 1024, 1024, 4096, 3),
+    "interval_normal": Workload("interval_normal", "interval", 1024, 1024, 4096, 7),
 }
 
 
@@ -91,6 +101,17 @@ def normal_matrices(M, N, K, seed):
     A = rng.standard_normal((M, K))
     B = rng.standard_normal((K, N))
     return A, B
+
+
+def interval_matrices(M, N, K, seed):
+    """Interval operands as stacked (midpoint, radius) float64 arrays, A [2,M,K] and B [2,K,N]:
+    midpoints i.i.d. standard normal, radii uniform in [0, 2^-20) times the midpoint's magnitude."""
+    rng = np.random.default_rng(seed)
+    Am = rng.standard_normal((M, K))
+    Bm = rng.standard_normal((K, N))
+    Ar = rng.random((M, K)) * 2.0**-20 * np.abs(Am)
+    Br = rng.random((K, N)) * 2.0**-20 * np.abs(Bm)
+    return np.stack([Am, Ar]), np.stack([Bm, Br])
 
 
 def sample_rows(M, seed, n=64):
