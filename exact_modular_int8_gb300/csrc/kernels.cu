@@ -8,6 +8,7 @@
 #include <cuda_fp16.h>
 
 #include <cstdint>
+#include <type_traits>
 #include <atomic>
 #include <mutex>
 
@@ -950,25 +951,38 @@ __device__ __forceinline__ void split_interval_loop(const IvSide& sa, const IvSi
       if (lost) ++tr[e];                                            // ceil(r 2^f)
     }
     __half* y = s.Y + row * s.ldy + col0;
-    for (int p = 0; p < P; ++p) {
-      const PrimeRec& R = rec[p];
-      const float q = R.q, iq = R.iq;
-      float r0[VEC], r1[VEC], r2[VEC];
+    // A writes (Am, |Am|, Ar), B writes (Bm, Br, |Bm| + Br); the side is
+    // uniform over an item, so each side has its own loop
+    auto planes = [&](auto side_a) {
+      constexpr bool IS_A = decltype(side_a)::value;
+      for (int p = 0; p < P; ++p) {
+        const PrimeRec& R = rec[p];
+        const float q = R.q, iq = R.iq;
+        float r0[VEC], r1[VEC], r2[VEC];
 #pragma unroll
-      for (int e = 0; e < VEC; ++e) {
-        const float am = shifted_residue<NWF>(tm[e], wsh_get<STAGED>(wsh, cols, p, shm[e]), q, iq);
-        const float rr = shifted_residue<NWF>(tr[e], wsh_get<STAGED>(wsh, cols, p, shr[e]), q, iq);
-        const float rm = negm[e] ? -am : am;                                           // floor(x 2^f)
-        const float rabs = negm[e] ? am : bal_mod_small(am + (lostm[e] ? 1.0f : 0.0f), q, iq);  // ceil |x| 2^f
-        r0[e] = rm;
-        r1[e] = isA ? rabs : rr;
-        r2[e] = isA ? rr : bal_mod_small(rabs + rr, q, iq);
+        for (int e = 0; e < VEC; ++e) {
+          const float am = shifted_residue<NWF>(tm[e], wsh_get<STAGED>(wsh, cols, p, shm[e]), q, iq);
+          const float rr = shifted_residue<NWF>(tr[e], wsh_get<STAGED>(wsh, cols, p, shr[e]), q, iq);
+          const float rabs = negm[e] ? am : bal_mod_small(am + (lostm[e] ? 1.0f : 0.0f), q, iq);  // ceil |x| 2^f
+          r0[e] = negm[e] ? -am : am;  // floor(x 2^f)
+          if constexpr (IS_A) {
+            r1[e] = rabs;
+            r2[e] = rr;
+          } else {
+            r1[e] = rr;
+            r2[e] = bal_mod_small(rabs + rr, q, iq);
+          }
+        }
+        __half* yp = y + (long long)p * s.plane;
+        store_residues<VEC>(r0, yp);
+        store_residues<VEC>(r1, yp + s.sub);
+        store_residues<VEC>(r2, yp + 2 * s.sub);
       }
-      __half* yp = y + (long long)p * s.plane;
-      store_residues<VEC>(r0, yp);
-      store_residues<VEC>(r1, yp + s.sub);
-      store_residues<VEC>(r2, yp + 2 * s.sub);
-    }
+    };
+    if (isA)
+      planes(std::true_type{});
+    else
+      planes(std::false_type{});
   }
 }
 
