@@ -655,6 +655,10 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     if (et == 0) bulk_wait0();
   }
 
+  // the role branches leave single lanes working while the rest of their warp
+  // runs ahead: reconverge every warp, so that the block barrier below sees
+  // whole warps and the memory is freed only after the last tensor-memory read
+  __syncwarp();
   tc_fence_before();
   __syncthreads();
   allow_dependents();
@@ -964,6 +968,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     if (et == 0) bulk_wait0();
   }
 
+  __syncwarp();  // whole warps again before the abort check and the barriers below
   if (*abort_flag) {
     // an aborted role may leave copies in flight that signal either CTA:
     // give them time to land before the pair leaves
