@@ -1011,13 +1011,19 @@ __global__ void __launch_bounds__(256) split_interval_kernel(IvSide sa, IvSide s
 // rg_garner.cuh.
 // ---------------------------------------------------------------------------
 
+__device__ CrtTables g_crt;  // round-to-nearest CRT tables of every prime count
+
+__device__ __forceinline__ CrtView crt_view(int P) { return CrtView{g_crt.M[P], g_crt.Pw[P], g_crt.Cw[P], g_crt.y[P]}; }
+
 // MAXP: a compile-time bound on the prime count (the workspace's pmax).
+// rn_free: reconstruct by round-to-nearest CRT whenever the planned primes
+// already exceed 4 |result| (the bound's prime count for one more bit is no
+// larger than P), at no extra prime; otherwise as the plan says.
 template <int LC, int MAXP>
 __global__ void __launch_bounds__(128) garner_int_kernel(const uint8_t* __restrict__ RC, long long ldc,
                                                          long long plane, long long M, long long N, RowDiv rd,
-                                                         DevPlan* plan, int64_t* __restrict__ C) {
+                                                         DevPlan* plan, int64_t* __restrict__ C, int rn_free) {
   constexpr int W = 2 * LC, GE = GarnerGE<W>::value;
-  __shared__ CrtRn crt;
   wait_for_predecessor();
   if (plan->status) return;
   const int P = plan->P;
@@ -1025,8 +1031,16 @@ __global__ void __launch_bounds__(128) garner_int_kernel(const uint8_t* __restri
     if (blockIdx.x == 0 && threadIdx.x == 0) set_status(&plan->status, RG_ERR_RANGE);
     return;
   }
-  const bool rn = plan->crt_rn != 0;
-  if (rn) crt_rn_tables<MainTab>(crt, P);
+  const bool plan_rn = plan->crt_rn != 0;
+  bool rn = plan_rn;
+  if (!rn && rn_free) {
+    const int prn = primes_for_bound(plan->bound_bits + 1);
+    rn = prn != 0 && prn <= P;
+  }
+  // recorded for rg_get_plan; every block takes the same decision from the
+  // same plan fields, so a block that reads the flag already set agrees
+  if (rn && !plan_rn && blockIdx.x == 0 && threadIdx.x == 0) plan->crt_rn = 1;
+  const CrtView crt = crt_view(P);
   const long long per_row = (N + GE - 1) / GE;
   const long long item = (long long)blockIdx.x * blockDim.x + threadIdx.x;
   if (item >= M * per_row) return;
@@ -1155,13 +1169,12 @@ __global__ void __launch_bounds__(128) garner_enclose_kernel(const uint8_t* __re
                                                              Bits* __restrict__ lo, Bits* __restrict__ hi) {
   constexpr int GE = GarnerGE<kEncW>::value;
   static_assert(GE == 2, "the bound stores below write GE entries as one vector");
-  __shared__ CrtRn crt;
   wait_for_predecessor();
   if (plan->status) return;
   const int P = plan->P;
   const int Q = plan->f_a + plan->f_b;
   const bool rn = plan->crt_rn != 0;
-  if (rn) crt_rn_tables<MainTab>(crt, P);
+  const CrtView crt = crt_view(P);
   const long long per_row = (N + GE - 1) / GE;
   const long long item = (long long)blockIdx.x * blockDim.x + threadIdx.x;
   if (item >= M * per_row) return;
@@ -1246,13 +1259,12 @@ __global__ void __launch_bounds__(128) garner_interval_kernel(const uint8_t* __r
                                                               long long N, long long K, RowDiv rd, DevPlan* plan,
                                                               Bits* __restrict__ lo, Bits* __restrict__ hi) {
   constexpr int GE = 1;
-  __shared__ CrtRn crt;
   wait_for_predecessor();
   if (plan->status) return;
   const int P = plan->P;
   const int Q = plan->f_a + plan->f_b;
   const bool rn = plan->crt_rn != 0;
-  if (rn) crt_rn_tables<MainTab>(crt, P);
+  const CrtView crt = crt_view(P);
   const long long item = (long long)blockIdx.x * blockDim.x + threadIdx.x;
   if (item >= M * N) return;
   const long long m = div_row(item, rd), n = item - m * N;  // item / N
@@ -1290,7 +1302,9 @@ __global__ void __launch_bounds__(128) garner_interval_kernel(const uint8_t* __r
 }
 
 int g_sm_count[64];
-std::atomic<int> g_crt_mode{0};  // 0: balanced Garner, 1: round-to-nearest CRT where the plan allows
+// 0: balanced Garner; 1: round-to-nearest CRT for the wide outputs where the
+// plan can keep P > 4 |x|, and for int64 where its primes already do
+std::atomic<int> g_crt_mode{0};
 
 int sm_count() {
   int dev = 0;
@@ -1321,6 +1335,7 @@ cudaError_t upload_tables() {
   if (done[dev]) return cudaSuccess;
   e = cudaMemcpyToSymbol(c_tab, &host_tables(), sizeof(Tables));
   if (e == cudaSuccess) e = cudaMemcpyToSymbol(g_wsh, host_shift_weights().w, sizeof(ShiftWeights));
+  if (e == cudaSuccess) e = cudaMemcpyToSymbol(g_crt, &host_crt_tables(), sizeof(CrtTables));
   if (e == cudaSuccess) {
     static SplitTables st;  // built from the host tables
     const Tables& t = host_tables();
@@ -1519,9 +1534,10 @@ cudaError_t launch_garner(int op, const void* RC, long long ldc, long long plane
   // the packed digits of at most kGarnerSmallP primes fit in 3 registers per
   // entry, against 14 for all 53
   const bool small = pmax <= kGarnerSmallP;
+  const int rn_free = op == RG_OP_I64 && g_crt_mode.load() == 1 ? 1 : 0;
   auto go = [&](auto k_small, auto k_all, int ge) {
     return launch_dependent(small ? k_small : k_all, blocks_for(ge), 128, 0, st, rc, ldc, plane, M, N, rowdiv_for(ge),
-                            plan, C);
+                            plan, C, rn_free);
   };
   switch (lc) {
     case 1: return go(garner_int_kernel<1, kGarnerSmallP>, garner_int_kernel<1, kNumPrimes>, GarnerGE<2>::value);

@@ -82,6 +82,22 @@ struct ShiftWeights {
 };
 const ShiftWeights& host_shift_weights();
 
+// CRT with a round-to-nearest quotient, for the first P primes of the
+// library's order and every P = 1..53: M[P][i] = (q_0 ... q_{P-1}) / q_i and
+// Pw[P] = q_0 ... q_{P-1} as little-endian 32-bit words (kCrtWords significant,
+// rows padded to kCrtStride), Cw[P] = 128 * sum_i M[P][i], and
+// y[P][i] = bal(M[P][i]^-1 mod q_i).  Built once on the host, read from global
+// memory by the kernels.
+constexpr int kCrtWords = 11;   // q_0 ... q_52 < 2^334
+constexpr int kCrtStride = 12;  // words per row (16-byte aligned rows)
+struct CrtTables {
+  uint32_t M[kNumPrimes + 1][kNumPrimes][kCrtStride];
+  uint32_t Pw[kNumPrimes + 1][kCrtStride];
+  uint32_t Cw[kNumPrimes + 1][kCrtStride];
+  float y[kNumPrimes + 1][kNumPrimes];
+};
+const CrtTables& host_crt_tables();
+
 // ---------------------------------------------------------------------------
 // Device helpers
 // ---------------------------------------------------------------------------

@@ -176,69 +176,19 @@ namespace {
 // and x = S - k P exactly.  O(P W) work per output instead of Garner's O(P^2);
 // S and k P are formed modulo 2^(32 W), which holds x.
 // ---------------------------------------------------------------------------
-constexpr int kCrtWords = 11;   // P < 2^334
-constexpr int kCrtStride = 12;  // words per table row (16-byte aligned rows)
-
-struct CrtRn {
-  uint32_t M[kNumPrimes][kCrtStride];  // M_i = P / q_i
-  uint32_t Pw[kCrtStride];             // P
-  uint32_t Cw[kCrtStride];             // 128 * sum_i M_i (the digits are summed offset by +128)
-  float y[kNumPrimes];                 // bal(M_i^-1 mod q_i)
+// The tables of one prime count P (CrtTables rows in global memory).
+struct CrtView {
+  const uint32_t (*M)[kCrtStride];  // M[i] = P / q_i
+  const uint32_t* Pw;               // P
+  const uint32_t* Cw;               // 128 * sum_i M_i (the digits are summed offset by +128)
+  const float* y;                   // bal(M_i^-1 mod q_i)
 };
-
-// Block-wide: the tables for the first P primes of TAB.  Ends with a barrier.
-template <typename TAB>
-__device__ __forceinline__ void crt_rn_tables(CrtRn& T, int P) {
-  for (int i = threadIdx.x; i <= P; i += blockDim.x) {
-    uint32_t w[kCrtWords];
-#pragma unroll
-    for (int k = 0; k < kCrtWords; ++k) w[k] = k == 0 ? 1u : 0u;
-    const int qi = i < P ? TAB::t().q[i] : 1;
-    int mmod = 1;  // M_i mod q_i
-    for (int j = 0; j < P; ++j) {
-      if (j == i) continue;
-      const uint32_t qj = (uint32_t)TAB::t().q[j];
-      unsigned long long carry = 0;
-#pragma unroll
-      for (int k = 0; k < kCrtWords; ++k) {
-        const unsigned long long t = (unsigned long long)w[k] * qj + carry;
-        w[k] = (uint32_t)t;
-        carry = t >> 32;
-      }
-      if (i < P) mmod = mmod * (int)(qj % (uint32_t)qi) % qi;
-    }
-    uint32_t* dst = i < P ? T.M[i] : T.Pw;
-#pragma unroll
-    for (int k = 0; k < kCrtStride; ++k) dst[k] = k < kCrtWords ? w[k] : 0u;
-    if (i < P) {
-      int inv = 1, b = mmod, e = qi - 2;  // Fermat: mmod^(q-2)
-      while (e) {
-        if (e & 1) inv = inv * b % qi;
-        b = b * b % qi;
-        e >>= 1;
-      }
-      T.y[i] = (float)(inv > (qi - 1) / 2 ? inv - qi : inv);
-    }
-  }
-  __syncthreads();
-  if (threadIdx.x == 0) {  // 128 * sum_i M_i, normalised to 32-bit words
-    unsigned long long carry = 0;
-    for (int k = 0; k < kCrtWords; ++k) {
-      unsigned long long t = carry;
-      for (int i = 0; i < P; ++i) t += (unsigned long long)T.M[i][k] << 7;
-      T.Cw[k] = (uint32_t)t;
-      carry = t >> 32;
-    }
-    T.Cw[kCrtWords] = 0;
-  }
-  __syncthreads();
-}
 
 // x[e] (W words, two's complement) = the centred integers of the GE residue
 // vectors (residues in [0, q)) starting at rc, plane bytes apart.
 template <int W, int GE, typename TAB>
 __device__ __forceinline__ void crt_rn_reconstruct(const uint8_t* __restrict__ rc, long long plane, int P,
-                                                   const CrtRn& T, uint32_t (&x)[GE][W]) {
+                                                   const CrtView& T, uint32_t (&x)[GE][W]) {
   constexpr int NW = W < kCrtWords ? W : kCrtWords;  // words that can differ from the sign
   static_assert(GE == 1 || GE == 2 || GE == 4, "one, two or four adjacent entries");
   unsigned long long acc[GE][NW];  // sum_i (s_i + 128) M_i, words not yet normalised (< 2^46)
@@ -266,10 +216,10 @@ __device__ __forceinline__ void crt_rn_reconstruct(const uint8_t* __restrict__ r
     for (int j = 0; j < kGarnerBatch; ++j) {
       const int i = i0 + j;
       if (i >= P) break;
-      const float q = TAB::t().qf[i], iq = TAB::t().invq[i], y = T.y[i];
+      const float q = TAB::t().qf[i], iq = TAB::t().invq[i], y = __ldg(T.y + i);
       uint32_t m[NW];
 #pragma unroll
-      for (int w = 0; w < NW; ++w) m[w] = T.M[i][w];
+      for (int w = 0; w < NW; ++w) m[w] = __ldg(&T.M[i][w]);
 #pragma unroll
       for (int e = 0; e < GE; ++e) {
         const float r = int_to_float_exact((int)((rw[j] >> (8 * e)) & 0xFFu));
@@ -287,7 +237,7 @@ __device__ __forceinline__ void crt_rn_reconstruct(const uint8_t* __restrict__ r
     long long carry = 0;
 #pragma unroll
     for (int w = 0; w < NW; ++w) {
-      const long long t = (long long)acc[e][w] - (long long)T.Cw[w] - k * (long long)T.Pw[w] + carry;
+      const long long t = (long long)acc[e][w] - (long long)__ldg(T.Cw + w) - k * (long long)__ldg(T.Pw + w) + carry;
       x[e][w] = (uint32_t)t;
       carry = t >> 32;  // arithmetic shift: the next word's borrow or carry
     }

@@ -143,6 +143,49 @@ const ShiftWeights& host_shift_weights() {
   return t;
 }
 
+const CrtTables& host_crt_tables() {
+  static CrtTables t;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    const Tables& b = host_tables();
+    // w (kCrtWords little-endian words) *= f, for f < 2^32
+    auto mul_small = [](uint32_t (&w)[kCrtWords], uint32_t f) {
+      unsigned long long carry = 0;
+      for (int k = 0; k < kCrtWords; ++k) {
+        const unsigned long long v = (unsigned long long)w[k] * f + carry;
+        w[k] = (uint32_t)v;
+        carry = v >> 32;
+      }
+    };
+    for (int P = 1; P <= kNumPrimes; ++P) {
+      unsigned long long csum[kCrtWords] = {};  // 128 * sum_i M_i, word by word before the carries
+      for (int i = 0; i <= P; ++i) {  // i = P: the whole product
+        uint32_t w[kCrtWords] = {1u};
+        int mmod = 1;  // M_i mod q_i
+        for (int j = 0; j < P; ++j) {
+          if (j == i) continue;
+          mul_small(w, (uint32_t)b.q[j]);
+          if (i < P) mmod = mmod * (b.q[j] % b.q[i]) % b.q[i];
+        }
+        uint32_t* dst = i < P ? t.M[P][i] : t.Pw[P];
+        for (int k = 0; k < kCrtStride; ++k) dst[k] = k < kCrtWords ? w[k] : 0u;
+        if (i < P) {
+          t.y[P][i] = (float)balanced(mod_pow(mmod, b.q[i] - 2, b.q[i]), b.q[i]);  // Fermat: q_i prime
+          for (int k = 0; k < kCrtWords; ++k) csum[k] += (unsigned long long)w[k] << 7;
+        }
+      }
+      unsigned long long carry = 0;
+      for (int k = 0; k < kCrtWords; ++k) {
+        const unsigned long long v = csum[k] + carry;  // csum[k] < 53 * 2^39
+        t.Cw[P][k] = (uint32_t)v;
+        carry = v >> 32;
+      }
+      t.Cw[P][kCrtWords] = 0;
+    }
+  });
+  return t;
+}
+
 }  // namespace rg
 
 extern "C" int rg_prime(int i) {

@@ -138,3 +138,13 @@ def test_wait_limit_roundtrip(rg):
     lib = rg.library()
     old = lib.rg_set_wait_limit_ns(12345)
     assert lib.rg_set_wait_limit_ns(old) == 12345
+
+
+def test_crt_mode_range(rg):
+    """Modes 0 (default) and 1 are accepted and return the previous mode; others are refused."""
+    lib = rg.library()
+    old = lib.rg_set_crt_mode(1)
+    assert old in (0, 1)
+    assert lib.rg_set_crt_mode(0) == 1
+    assert lib.rg_set_crt_mode(2) == -1 and lib.rg_set_crt_mode(-1) == -1
+    assert lib.rg_set_crt_mode(old) == 0

@@ -1,7 +1,7 @@
 """The two reconstructions of the wide outputs: round-to-nearest CRT (on
 request, when the plan can keep P > 4 |x|) and balanced Garner (the default;
-always for the int64 path, a caller-fixed prime count, and products at the
-332-bit capacity).  Extreme
+always for a caller-fixed prime count and for products at the 332-bit
+capacity).  The int64 path's two reconstructions are tested in test_gpu_crt_i64.py.  Extreme
 same-sign operands put the result at its bound, where the rounded quotient
 has the least margin."""
 import numpy as np
