@@ -1059,8 +1059,55 @@ __global__ void __launch_bounds__(256) slice_sum_kernel(uint8_t* __restrict__ RC
   allow_dependents();
 }
 
-int g_gemm_ready[64];
 std::atomic<int> g_gemm_variant{0};  // 0 automatic, 1 single-CTA, 2 CTA pair
+
+// Per device, set up once under a lock: the kernels' shared-memory limits, the
+// SM count and how many CTA pairs can be resident at once.
+struct GemmDevice {
+  int sms = 0, max_pairs = 0;
+};
+
+cudaError_t gemm_device(int dev, GemmDevice& out) {
+  static std::mutex mu;
+  static GemmDevice devs[64];
+  std::lock_guard<std::mutex> lock(mu);
+  GemmDevice& d = devs[dev];
+  if (!d.sms) {
+    for (auto k : {residue_gemm_kernel<false>, residue_gemm_kernel<true>}) {
+      cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
+      if (e != cudaSuccess) return e;
+    }
+    for (auto k : {residue_gemm_pair_kernel<false>, residue_gemm_pair_kernel<true>}) {
+      cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM2_BYTES);
+      if (e != cudaSuccess) return e;
+    }
+    int sms = 0;
+    cudaError_t e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    if (e != cudaSuccess) return e;
+    if (sms < 2) return cudaErrorInvalidDevice;
+    // not every SM can be paired within its GPC
+    cudaLaunchConfig_t cfg = {};
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = 2;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    cfg.blockDim = dim3(NUM_THREADS);
+    cfg.dynamicSmemBytes = SMEM2_BYTES;
+    cfg.gridDim = dim3((unsigned)(sms & ~1));
+    int n = 0;
+    if (cudaOccupancyMaxActiveClusters(&n, residue_gemm_pair_kernel<false>, &cfg) != cudaSuccess || n < 1) {
+      cudaGetLastError();  // the query's own failure is not the call's
+      n = sms / 2;
+    }
+    d.max_pairs = n;
+    d.sms = sms;
+  }
+  out = d;
+  return cudaSuccess;
+}
 
 }  // namespace
 
@@ -1072,19 +1119,9 @@ cudaError_t launch_gemm(const void* RA, long long lda, const void* RB, long long
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
   if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
-  static int sms[64];
-  if (!g_gemm_ready[dev]) {
-    for (auto k : {residue_gemm_kernel<false>, residue_gemm_kernel<true>}) {
-      e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
-      if (e != cudaSuccess) return e;
-    }
-    for (auto k : {residue_gemm_pair_kernel<false>, residue_gemm_pair_kernel<true>}) {
-      e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM2_BYTES);
-      if (e != cudaSuccess) return e;
-    }
-    cudaDeviceGetAttribute(&sms[dev], cudaDevAttrMultiProcessorCount, dev);
-    g_gemm_ready[dev] = 1;
-  }
+  GemmDevice gd;
+  e = gemm_device(dev, gd);
+  if (e != cudaSuccess) return e;
   // the pair kernel loads A in 128-row halves of a 256-row tile
   const int variant = g_gemm_variant.load();
   const bool pair = variant == 2 || (variant == 0 && M > BM);
@@ -1128,14 +1165,14 @@ cudaError_t launch_gemm(const void* RA, long long lda, const void* RB, long long
     for (int i = 0; i < kNumPrimes; ++i) qs.q[i] = t.q[i];
     const long long plane_bytes = M * ldc, n16 = (long long)planes * plane_bytes / 16;
     long long blocks = (n16 + 255) / 256;
-    if (blocks > 4LL * sms[dev]) blocks = 4LL * sms[dev];
+    if (blocks > 4LL * gd.sms) blocks = 4LL * gd.sms;
     return launch_dependent(slice_sum_kernel, dim3((unsigned)(blocks < 1 ? 1 : blocks)), dim3(256), 0, st,
                             static_cast<uint8_t*>(RC), (long long)planes * plane_bytes, plane_bytes, batch, qs,
                             (const DevPlan*)plan);
   };
   if (!pair) {
     const long long tiles = (long long)planes * gp.mt * gp.nt * max_splits;
-    int grid = (int)(tiles < sms[dev] ? tiles : sms[dev]);
+    int grid = (int)(tiles < gd.sms ? tiles : gd.sms);
     if (grid < 1) grid = 1;
     e = b_kmajor ? launch_dependent(residue_gemm_kernel<true>, dim3(grid), dim3(NUM_THREADS), SMEM_BYTES, st, ma, mb,
                                     mc, gp, plan)
@@ -1156,18 +1193,10 @@ cudaError_t launch_gemm(const void* RA, long long lda, const void* RB, long long
   attr[1].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 2;
-  // persistent: as many pairs as can be resident at once (not every SM can
-  // be paired within its GPC), never more than there are tiles
-  static int max_pairs[64];
-  if (!max_pairs[dev]) {
-    int n = 0;
-    cfg.gridDim = dim3((unsigned)(sms[dev] & ~1));
-    if (cudaOccupancyMaxActiveClusters(&n, residue_gemm_pair_kernel<false>, &cfg) != cudaSuccess || n < 1)
-      n = sms[dev] / 2;
-    max_pairs[dev] = n;
-  }
+  // persistent: as many pairs as can be resident at once, never more than
+  // there are tiles
   const long long tiles2 = (long long)planes * ((M + 255) / 256) * gp.nt * max_splits;
-  long long clusters = max_pairs[dev];
+  long long clusters = gd.max_pairs;
   if (tiles2 < clusters) clusters = tiles2;
   if (clusters < 1) clusters = 1;
   cfg.gridDim = dim3((unsigned)(2 * clusters));

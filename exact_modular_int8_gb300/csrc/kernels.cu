@@ -1301,7 +1301,7 @@ __global__ void __launch_bounds__(128) garner_interval_kernel(const uint8_t* __r
   hi[m * N + n] = h;
 }
 
-int g_sm_count[64];
+std::atomic<int> g_sm_count[64];  // per device, 0 until read
 // 0: balanced Garner; 1: round-to-nearest CRT for the wide outputs where the
 // plan can keep P > 4 |x|, and for int64 where its primes already do
 std::atomic<int> g_crt_mode{0};
@@ -1310,12 +1310,12 @@ int sm_count() {
   int dev = 0;
   cudaGetDevice(&dev);
   if (dev < 0 || dev >= 64) return 148;
-  if (!g_sm_count[dev]) {
-    int n = 0;
-    cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
-    g_sm_count[dev] = n > 0 ? n : 148;
+  int n = g_sm_count[dev].load(std::memory_order_relaxed);
+  if (!n) {  // threads that race here all store the same count
+    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n < 1) n = 148;
+    g_sm_count[dev].store(n, std::memory_order_relaxed);
   }
-  return g_sm_count[dev];
+  return n;
 }
 
 }  // namespace

@@ -14,6 +14,7 @@
 #include <chrono>
 #include <cmath>
 #include <cstring>
+#include <mutex>
 #include <thread>
 #include <vector>
 
@@ -424,10 +425,12 @@ extern "C" int rg_solve_i64(const int64_t* A_in, const int64_t* B_in, int64_t n6
   };
   SOLVE_TRY(upload_tables());
   {
+    static std::mutex mu;
     static bool uploaded[64];
     int dev = 0;
     SOLVE_TRY(cudaGetDevice(&dev));
     if (dev < 0 || dev >= 64) return RG_ERR_CUDA;
+    std::lock_guard<std::mutex> lock(mu);
     if (!uploaded[dev]) {
       SOLVE_TRY(cudaMemcpyToSymbol(c_all, &host_tables(), sizeof(Tables)));
       uploaded[dev] = true;

@@ -226,3 +226,44 @@ def test_host_buffers_pinned_or_pageable(rg, pin_in, pin_out):
     rlo, rhi = rg.enclose_gemm_f64(fA, fB, out=(lo, hi))
     ref = Af @ Bf  # products of 15-bit integers summed over 300 terms: exact in float64
     assert np.array_equal(rlo.numpy(), ref) and np.array_equal(rhi.numpy(), ref)
+
+
+_CONCURRENT = r"""
+import sys, threading
+import numpy as np, torch
+sys.path.insert(0, sys.argv[1])
+import exact_modular_int8_gb300 as rg
+import oracle
+from workloads import int_matrices
+cases = [int_matrices(150 + 40 * i, 130 + 30 * i, 300, -(2**22), 2**22, 40 + i) for i in range(4)]
+out, err = [None] * 4, []
+start = threading.Barrier(4)
+def run(i):
+    try:
+        s = torch.cuda.Stream()
+        with torch.cuda.stream(s):
+            A, B = (torch.from_numpy(x).cuda() for x in cases[i])
+            start.wait()
+            out[i] = rg.res_gemm_i64(A, B).cpu().numpy()
+    except Exception as e:  # reported below
+        err.append(repr(e))
+ts = [threading.Thread(target=run, args=(i,)) for i in range(4)]
+for t in ts: t.start()
+for t in ts: t.join()
+assert not err, err
+for i, (A, B) in enumerate(cases):
+    assert np.array_equal(out[i], oracle.matmul_i64(A, B, lc=1)[:, :, 0]), i
+print("concurrent ok")
+"""
+
+
+def test_concurrent_first_calls_from_host_threads(rg):
+    """Four host threads make their first calls at once, each on its own stream (so its own
+    workspace), in a fresh process: the per-device setup is taken once, and every product is exact."""
+    import os
+    import subprocess
+    import sys
+    root = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+    r = subprocess.run([sys.executable, "-c", _CONCURRENT, root], capture_output=True, text=True, timeout=600,
+                       cwd=root)
+    assert r.returncode == 0 and "concurrent ok" in r.stdout, r.stdout[-2000:] + r.stderr[-2000:]
