@@ -133,24 +133,7 @@ __device__ LocalPlan finalize_plan(DevPlan* plan, const PlanArgs& a) {
   const int ck = ceil_log2_i64(a.K);
   // 32-bit words holding an entry of `bits` magnitude bits with its sign, at most the limbs' 2L
   auto words_for = [](int bits, int L) { return min((bits + 1 + 31) / 32, 2 * L); };
-  if (a.op == RG_OP_I64) {
-    const unsigned long long ma = __ldcg(&plan->maxmag_a), mb = __ldcg(&plan->maxmag_b);
-    p.bits_a = bitlen64(ma);
-    p.bits_b = bitlen64(mb);
-    p.T = p.bits_a + p.bits_b + ck;
-    if (a.nprimes_fixed) {
-      p.nword_a = p.nword_b = 2;
-    } else {
-      // entries with |x| <= 2^23 are exact fp32 values: no words (nword 0)
-      p.nword_a = ma <= (1ull << 23) ? 0 : words_for(p.bits_a, 1);
-      p.nword_b = mb <= (1ull << 23) ? 0 : words_for(p.bits_b, 1);
-      // exact range check: K * max|A| * max|B| <= 2^63 - 1, with 64x64 -> 128
-      // products only
-      const unsigned long long ab_hi = __umul64hi(ma, mb), ab = ma * mb;
-      const unsigned long long k = (unsigned long long)a.K;
-      if (ab_hi != 0 || __umul64hi(ab, k) != 0 || ab * k > 0x7FFFFFFFFFFFFFFFull) p.status = RG_ERR_RANGE;
-    }
-  } else if (a.op == RG_OP_LIMBS) {
+  if (a.op == RG_OP_LIMBS) {
     p.bits_a = __ldcg(&plan->maxbits_a);
     p.bits_b = __ldcg(&plan->maxbits_b);
     p.T = p.bits_a + p.bits_b + ck;
@@ -208,7 +191,7 @@ __device__ LocalPlan finalize_plan(DevPlan* plan, const PlanArgs& a) {
     // on request the wide outputs reconstruct by round-to-nearest CRT, which
     // wants one more bit of headroom (P > 4 |x|); where 53 primes cannot give
     // it, balanced Garner reconstructs from the usual prime count
-    if (a.op != RG_OP_I64 && a.allow_rn) {
+    if (a.allow_rn) {
       const int prn = primes_for_bound(p.T + 1);
       if (prn) {
         p.P = prn;
@@ -263,29 +246,6 @@ __device__ __forceinline__ PlannerSide planner_side(int nbA) {
   return s;
 }
 
-// max |x| of int64 A and B; 16-byte loads when aligned, scalar tail.
-__global__ void __launch_bounds__(256) plan_i64_kernel(const int64_t* __restrict__ A, long long nA,
-                                                       const int64_t* __restrict__ B, long long nB, int nbA,
-                                                       DevPlan* plan, PlanArgs pa) {
-  const PlannerSide sd = planner_side(nbA);
-  const unsigned long long* X = reinterpret_cast<const unsigned long long*>(sd.isA ? A : B);
-  const long long n = sd.isA ? nA : nB;
-  const long long nv = (reinterpret_cast<uintptr_t>(X) & 15u) == 0 ? n / 2 : 0;
-  const ulonglong2* X2 = reinterpret_cast<const ulonglong2*>(X);
-  unsigned long long m = 0;
-#pragma unroll 4
-  for (long long i = sd.b0 * blockDim.x + threadIdx.x; i < nv; i += sd.stride) {
-    const ulonglong2 v = __ldg(X2 + i);
-    m = max(m, max(abs_u64(v.x), abs_u64(v.y)));
-  }
-  for (long long i = 2 * nv + sd.b0 * blockDim.x + threadIdx.x; i < n; i += sd.stride)
-    m = max(m, abs_u64(__ldg(X + i)));
-  m = block_max_u64(m);
-  if (threadIdx.x == 0 && m) atomicMax(sd.isA ? &plan->maxmag_a : &plan->maxmag_b, m);
-  planner_finish(plan, pa);
-}
-
-// Bit length of |x| for multi-limb x (two's complement, signed top limb).
 // Bit length of |x| for an L-limb two's-complement integer held in w.
 template <int L>
 __device__ __forceinline__ int limb_magnitude_bits(const unsigned long long (&w)[L]) {
@@ -1366,9 +1326,8 @@ cudaError_t launch_plan(int op, const void* A, const void* A2, long long nA, int
   if (nprimes_fixed) nA = nB = 0;  // only the finalisation is needed
   const int ba = planner_blocks(nA), bb = planner_blocks(nB);
   if (op == RG_OP_I64)
-    plan_i64_kernel<<<ba + bb, 256, 0, s>>>(static_cast<const int64_t*>(A), nA, static_cast<const int64_t*>(B), nB,
-                                            ba, plan, pa);
-  else if (op == RG_OP_LIMBS)
+    return cudaErrorInvalidValue;  // int64 plans in its split and GEMM kernels, with no planner pass
+  if (op == RG_OP_LIMBS)
     plan_limbs_kernel<<<ba + bb, 256, 0, s>>>(static_cast<const int64_t*>(A), nA, la,
                                               static_cast<const int64_t*>(B), nB, lb, ba, plan, pa);
   else if (op == RG_OP_ENCLOSE || op == RG_OP_INTERVAL) {
