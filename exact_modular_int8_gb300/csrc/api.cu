@@ -7,6 +7,7 @@
 // RG_FLAG_SYNC / RG_FLAG_HOST calls, rg_status() and rg_get_plan() wait for the
 // device.
 #include <atomic>
+#include <climits>
 #include <mutex>
 #include <cstdint>
 #include <cstring>
@@ -95,6 +96,10 @@ bool make_layout(int op, long long batch, long long M, long long N, long long K,
                             lc > RG_MAX_LIMBS_OUT))
     return false;
   if (op != RG_OP_LIMBS) la = lb = lc = 1;
+  // shapes the kernels index in 32 bits (rows, columns, products) and the
+  // longest exact-sum K; with these and the tile bound below, every size in
+  // the layout stays below 2^61
+  if (M > INT32_MAX || N > INT32_MAX || batch > INT32_MAX || K > RG_MAX_K) return false;
   std::memset(L, 0, sizeof(*L));
   const bool transb = (flags & RG_FLAG_TRANS_B) != 0;
   L->lda = round_up(K, 8);
@@ -108,6 +113,10 @@ bool make_layout(int op, long long batch, long long M, long long N, long long K,
     return true;
   }
   int pmax = pmax_for(op, K, la, lb, nprimes);
+  // the persistent GEMM numbers its tiles (plane, row block, column block)
+  // in int: at most 2^31 - 1 of the single-CTA kind (the larger count)
+  const __int128 tiles = (__int128)pmax * planes_per_product(op) * batch * ((M + 127) / 128) * ((N + 255) / 256);
+  if (tiles > INT32_MAX) return false;
   L->pmax = pmax;
   const size_t planes = (size_t)pmax * planes_per_product(op) * batch;
   L->splits = gemm_max_splits((long long)planes_per_product(op) * batch, M, N, K);
@@ -186,9 +195,7 @@ int run(int op, const void* A, const void* A2, int la, const void* B, const void
   Layout L;
   if (!make_layout(op, batch, M, N, K, la, lb, lc, nprimes, flags, &L)) return RG_ERR_ARG;
   if (ws_bytes < L.total) return RG_ERR_WORKSPACE;
-  // the persistent GEMM numbers its tiles (plane, row block, column block) in int
   const long long gemm_batch = batch * planes_per_product(op);
-  if ((long long)L.pmax * gemm_batch * ((M + 127) / 128) * ((N + 255) / 256) > (1LL << 31) - 1) return RG_ERR_ARG;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   uint8_t* w = static_cast<uint8_t*>(ws);
   DevPlan* plan = reinterpret_cast<DevPlan*>(w + L.plan);
@@ -339,6 +346,8 @@ int res_gemm_stage(const uint16_t* RA, int64_t lda, const uint16_t* RB, int64_t 
                    void* stream) {
   if (!RA || !RB || !RC || !ws || (flags & RG_FLAG_HOST)) return RG_ERR_ARG;
   if (M <= 0 || N <= 0 || K <= 0 || nprimes < 1 || nprimes > kNumPrimes) return RG_ERR_ARG;
+  if (M > INT32_MAX || N > INT32_MAX) return RG_ERR_ARG;
+  if ((__int128)nprimes * ((M + 127) / 128) * ((N + 255) / 256) > INT32_MAX) return RG_ERR_ARG;  // int tile numbers
   const bool transb = (flags & RG_FLAG_TRANS_B) != 0;
   if (lda < K || lda % 8 || ldc < N || ldc % 16) return RG_ERR_ARG;
   if (transb ? (ldb < K || ldb % 8) : (ldb < N || ldb % 64)) return RG_ERR_ARG;

@@ -258,7 +258,11 @@ size_t rg_noalloc_scratch_bytes(void);
  * la, lb, lc are the limb counts (1 for RG_OP_I64 / RG_OP_ENCLOSE[_F32]); nprimes
  * is the value the call will pass (0 = plan on the device).  flags must
  * match the call's RG_FLAG_HOST and RG_FLAG_TRANS_B bits.  Returns 0 for
- * invalid arguments.  An empty problem needs the 4 KiB plan block only.
+ * invalid arguments, including shapes the kernels cannot index: M, N or
+ * batch above 2^31 - 1, K above 2^17, or more than 2^31 - 1 GEMM tiles
+ * (primes x products x ceil(M / 128) x ceil(N / 256)); the entry points
+ * return RG_ERR_ARG (RG_ERR_RANGE for K) for the same shapes.  An empty
+ * problem needs the 4 KiB plan block only.
  */
 size_t rg_workspace_bytes(int op, int64_t M, int64_t N, int64_t K, int la, int lb, int lc, int nprimes,
                           unsigned flags);

@@ -93,6 +93,20 @@ def test_workspace_sizes(rg):
     assert rg.workspace_bytes(rg.RG_OP_LIMBS, 4, 4, 4, la=2, lb=2, lc=7) == 0
 
 
+def test_workspace_query_refuses_shapes_the_kernels_cannot_index(rg):
+    """Shapes past 32-bit rows, columns or batch, K past 2^17, or more than 2^31 - 1 GEMM tiles get 0
+    (an invalid problem), never a size wrapped modulo 2^64."""
+    big = 2**31 - 1
+    assert rg.workspace_bytes(rg.RG_OP_I64, 2**31, 8, 8) == 0
+    assert rg.workspace_bytes(rg.RG_OP_I64, 8, 2**40, 8) == 0
+    assert rg.workspace_bytes(rg.RG_OP_I64, 8, 8, 2**17 + 1) == 0
+    assert rg.workspace_bytes(rg.RG_OP_I64, 8, 8, 8, batch=2**31) == 0
+    assert rg.workspace_bytes(rg.RG_OP_INTERVAL, big, big, 64, batch=big) == 0  # about 2^85 tiles
+    assert rg.workspace_bytes(rg.RG_OP_I64, 2**22, 2**22, 8) == 0  # 9 primes x 2^15 x 2^14 tiles > 2^31
+    n = rg.workspace_bytes(rg.RG_OP_I64, 2**18, 2**18, 8)  # 9 x 2048 x 1024 tiles: valid; C's 9 planes take 620 GB
+    assert n > 9 * 2**36 and n < 2**40
+
+
 def test_argument_errors_need_no_device(rg):
     lib = rg.library()
     buf = (ctypes.c_int64 * 16)()
@@ -123,6 +137,13 @@ def test_argument_errors_need_no_device(rg):
     assert lib.res_gemm_stage(p, 8, p, 64, p, 16, 0, 2, 2, 2, 0, wsp, 4096, None) == rg.RG_ERR_ARG
     assert lib.res_gemm_stage(p, 8, p, 32, p, 16, 1, 2, 2, 2, 0, wsp, 4096, None) == rg.RG_ERR_ARG
     assert lib.res_gemm_stage(p, 2**17 + 8, p, 64, p, 16, 1, 2, 2, 2**17 + 1, 0, wsp, 4096, None) == rg.RG_ERR_RANGE
+    # shapes past the kernels' 32-bit tile numbering
+    assert lib.res_gemm_stage(p, 8, p, 2**31 + 64, p, 2**31 + 16, 1, 2, 2**31, 2, 0, wsp, 4096, None) == rg.RG_ERR_ARG
+    assert lib.res_gemm_stage(p, 8, p, 2**21, p, 2**21, 53, 2**21, 2**21, 2, 0, wsp, 4096, None) == rg.RG_ERR_ARG
+    assert lib.res_gemm_i64(p, p, p, 2**31, 2, 2, 0, 0, wsp, 4096, None) == rg.RG_ERR_ARG
+    assert lib.res_gemm_i64(p, p, p, 2**22, 2**22, 8, 0, 0, wsp, 1 << 62, None) == rg.RG_ERR_ARG
+    assert lib.interval_gemm_f64_batched(p, p, p, p, p, p, 2**31 - 1, 2**31 - 1, 2**31 - 1, 64, 0, wsp, 1 << 62,
+                                         None) == rg.RG_ERR_ARG
 
 
 def test_stage_events_hook_arguments(rg):
