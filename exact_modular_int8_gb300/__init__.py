@@ -179,6 +179,15 @@ def workspace_bytes(op, M, N, K, la=1, lb=1, lc=1, nprimes=0, host=False, transb
     return _ws_bytes(op, batch, M, N, K, la, lb, lc, nprimes, _layout_flags(host, transb))
 
 
+def _need(op, M, N, K, where, **kw) -> int:
+    """The call's workspace size; a shape the library refuses raises as the C entry point would
+    (RG_ERR_RANGE for K above 2^17, RG_ERR_ARG otherwise)."""
+    need = workspace_bytes(op, M, N, K, **kw)
+    if need == 0:
+        raise ResGemmError(RG_ERR_RANGE if K > MAX_K else RG_ERR_ARG, where)
+    return need
+
+
 def workspace_layout(op, M, N, K, la=1, lb=1, lc=1, nprimes=0, host=False, transb=False, batch=1) -> Layout:
     out = Layout()
     rc = library().rg_workspace_layout_batched(op, batch, M, N, K, la, lb, lc, nprimes, _layout_flags(host, transb),
@@ -286,9 +295,7 @@ def res_gemm_i64(A: torch.Tensor, B: torch.Tensor, nprimes: int = 0, sync: bool 
     shape = (batch, M, N) if batched else (M, N)
     C = _output(out, shape, torch.int64, A, host, "res_gemm_i64")
     with _on(dev):
-        need = workspace_bytes(RG_OP_I64, M, N, K, nprimes=nprimes, host=host, transb=transb, batch=batch)
-        if need == 0:
-            raise ResGemmError(RG_ERR_ARG, "res_gemm_i64")
+        need = _need(RG_OP_I64, M, N, K, "res_gemm_i64", nprimes=nprimes, host=host, transb=transb, batch=batch)
         w = ws if ws is not None else workspace(need, dev)
         rc = library().res_gemm_i64_batched(A.data_ptr(), B.data_ptr(), C.data_ptr(), batch, M, N, K, nprimes, flags,
                                             w.data_ptr(), w.numel(), torch.cuda.current_stream(dev).cuda_stream)
@@ -310,9 +317,8 @@ def res_gemm_limbs(A: torch.Tensor, B: torch.Tensor, lc: int, nprimes: int = 0, 
     shape = (batch, M, N, lc) if batched else (M, N, lc)
     C = _output(out, shape, torch.int64, A, host, "res_gemm_limbs")
     with _on(dev):
-        need = workspace_bytes(RG_OP_LIMBS, M, N, K, la, lb, lc, nprimes, host=host, transb=transb, batch=batch)
-        if need == 0:
-            raise ResGemmError(RG_ERR_ARG, "res_gemm_limbs")
+        need = _need(RG_OP_LIMBS, M, N, K, "res_gemm_limbs", la=la, lb=lb, lc=lc, nprimes=nprimes, host=host,
+                     transb=transb, batch=batch)
         w = ws if ws is not None else workspace(need, dev)
         rc = library().res_gemm_limbs_batched(A.data_ptr(), la, B.data_ptr(), lb, C.data_ptr(), lc, batch, M, N, K,
                                               nprimes, flags, w.data_ptr(), w.numel(),
@@ -344,9 +350,7 @@ def enclose_gemm(A: torch.Tensor, B: torch.Tensor, sync: bool = True, ws: torch.
     lo = _output(None if out is None else out[0], shape, A.dtype, A, pin, name)
     hi = _output(None if out is None else out[1], shape, A.dtype, A, pin, name)
     with _on(dev):
-        need = workspace_bytes(op, M, N, K, host=pin, transb=transb, batch=batch)
-        if need == 0:
-            raise ResGemmError(RG_ERR_ARG, name)
+        need = _need(op, M, N, K, name, host=pin, transb=transb, batch=batch)
         w = ws if ws is not None else workspace(need, dev)
         rc = getattr(library(), name + "_batched")(A.data_ptr(), B.data_ptr(), lo.data_ptr(), hi.data_ptr(), batch,
                                                    M, N, K, flags, w.data_ptr(), w.numel(),
@@ -425,9 +429,7 @@ def interval_gemm(Am: torch.Tensor, Ar: torch.Tensor, Bm: torch.Tensor, Br: torc
     lo = _output(None if out is None else out[0], shape, Am.dtype, Am, pin, name)
     hi = _output(None if out is None else out[1], shape, Am.dtype, Am, pin, name)
     with _on(dev):
-        need = workspace_bytes(op, M, N, K, host=pin, transb=transb, batch=batch)
-        if need == 0:
-            raise ResGemmError(RG_ERR_ARG, name)
+        need = _need(op, M, N, K, name, host=pin, transb=transb, batch=batch)
         w = ws if ws is not None else workspace(need, dev)
         rc = getattr(library(), name + "_batched")(Am.data_ptr(), Ar.data_ptr(), Bm.data_ptr(), Br.data_ptr(),
                                                    lo.data_ptr(), hi.data_ptr(), batch, M, N, K, flags,

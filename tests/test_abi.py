@@ -169,3 +169,14 @@ def test_crt_mode_range(rg):
     assert lib.rg_set_crt_mode(0) == 1
     assert lib.rg_set_crt_mode(2) == -1 and lib.rg_set_crt_mode(-1) == -1
     assert lib.rg_set_crt_mode(old) == 0
+
+
+def test_binding_reports_refused_shapes_like_the_entry_points(rg):
+    """The binding sizes the workspace first; a refused shape raises the code the C entry point returns."""
+    with pytest.raises(rg.ResGemmError) as e:
+        rg._need(rg.RG_OP_I64, 8, 8, rg.MAX_K + 1, "res_gemm_i64")
+    assert e.value.code == rg.RG_ERR_RANGE
+    with pytest.raises(rg.ResGemmError) as e:
+        rg._need(rg.RG_OP_ENCLOSE, 2**31, 8, 8, "enclose_gemm")
+    assert e.value.code == rg.RG_ERR_ARG
+    assert rg._need(rg.RG_OP_I64, 8, 8, rg.MAX_K, "res_gemm_i64") == rg.workspace_bytes(rg.RG_OP_I64, 8, 8, rg.MAX_K)
