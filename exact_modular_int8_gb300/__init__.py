@@ -55,7 +55,7 @@ EXPORTED = (
     "res_gemm_i64_batched", "res_gemm_limbs_batched", "enclose_gemm_f64_batched", "rg_workspace_bytes_batched",
     "rg_workspace_layout_batched", "enclose_gemm_f32", "enclose_gemm_f32_batched", "interval_gemm_f64",
     "interval_gemm_f32", "interval_gemm_f64_batched", "interval_gemm_f32_batched", "rg_solve_i64",
-    "rg_solution_free", "rg_rational_reconstruct", "rg_set_crt_mode", "rg_set_stage_events",
+    "rg_solution_free", "rg_rational_reconstruct", "rg_big_gcd", "rg_set_crt_mode", "rg_set_stage_events",
 )
 
 
@@ -151,6 +151,8 @@ def library():
             lib.rg_solution_free.restype = None
             lib.rg_rational_reconstruct.argtypes = [vp, ci, vp, ci, ci, ci, vp, vp, ci]
             lib.rg_rational_reconstruct.restype = ci
+            lib.rg_big_gcd.argtypes = [vp, ci, vp, ci, vp, ci]
+            lib.rg_big_gcd.restype = ci
             lib.rg_set_stage_events.argtypes = [ctypes.POINTER(ctypes.c_void_p), ci]
             lib.rg_set_stage_events.restype = ci
             _lib = lib
@@ -622,6 +624,18 @@ def solve(A: torch.Tensor, b: torch.Tensor, info: dict | None = None):
         return None
     N, d = r
     return [[Fraction(v, d) for v in row] for row in N]
+
+
+def big_gcd(a: int, b: int) -> int:
+    """gcd of two naturals by the library's host big-integer code (the solve's reconstruction uses it)."""
+    al, bl = max(1, (a.bit_length() + 63) // 64), max(1, (b.bit_length() + 63) // 64)
+    gl = min(al, bl)
+    mask = (1 << 64) - 1
+    A = (ctypes.c_uint64 * al)(*[(a >> (64 * i)) & mask for i in range(al)])
+    B = (ctypes.c_uint64 * bl)(*[(b >> (64 * i)) & mask for i in range(bl)])
+    G = (ctypes.c_uint64 * gl)()
+    _check(library().rg_big_gcd(A, al, B, bl, G, gl), "rg_big_gcd")
+    return sum(int(G[i]) << (64 * i) for i in range(gl))
 
 
 def rational_reconstruct(x: int, m: int, nbits: int, dbits: int):

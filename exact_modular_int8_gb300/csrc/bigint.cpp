@@ -1,7 +1,8 @@
 // bigint.cpp -- host multi-precision arithmetic for the exact solve's
 // rational reconstruction: schoolbook products, long division (Knuth's
-// algorithm D on 64-bit limbs), Euclid's gcd and the extended-Euclid
-// rational reconstruction.
+// algorithm D on 64-bit limbs), and Lehmer's gcd and extended-Euclid
+// rational reconstruction, each batch of leading-digit quotients applied to
+// the full numbers in one in-place pass.
 #include "bigint.h"
 
 #include <algorithm>
@@ -170,15 +171,6 @@ Nat mod(const Nat& a, const Nat& b) {
   Nat r;
   divmod(a, b, nullptr, &r);
   return r;
-}
-
-Nat gcd(Nat a, Nat b) {
-  while (!is_zero(b)) {
-    Nat r = mod(a, b);
-    a = std::move(b);
-    b = std::move(r);
-  }
-  return a;
 }
 
 Int add(const Int& a, const Int& b) {
@@ -367,32 +359,6 @@ void mul_add_into(std::vector<Limb>& acc, const Limb* m, size_t nm, const Limb* 
 
 namespace {
 
-// a * x for a natural x and a one-limb a.
-Nat mul_limb(const Nat& x, Limb a) {
-  Nat r;
-  if (!a || x.v.empty()) return r;
-  r.v.resize(x.v.size() + 1);
-  Limb carry = 0;
-  for (size_t i = 0; i < x.v.size(); ++i) {
-    const u128 t = (u128)x.v[i] * a + carry;
-    r.v[i] = (Limb)t;
-    carry = (Limb)(t >> 64);
-  }
-  r.v[x.v.size()] = carry;
-  trim(r);
-  return r;
-}
-
-// a * x + b * y for signed one-limb coefficients.
-Int lincomb(const Int& x, long long a, const Int& y, long long b) {
-  Int px, py;
-  px.mag = mul_limb(x.mag, (Limb)(a < 0 ? -(unsigned long long)a : (unsigned long long)a));
-  px.neg = (x.neg != (a < 0)) && !is_zero(px.mag);
-  py.mag = mul_limb(y.mag, (Limb)(b < 0 ? -(unsigned long long)b : (unsigned long long)b));
-  py.neg = (y.neg != (b < 0)) && !is_zero(py.mag);
-  return add(px, py);
-}
-
 // The 62 bits of x starting at bit s (x < 2^(s + 62)).
 uint64_t bits_at(const Nat& x, size_t s) {
   const size_t w = s / 64, o = s % 64;
@@ -401,7 +367,119 @@ uint64_t bits_at(const Nat& x, size_t s) {
   return lo & ((1ull << 62) - 1);
 }
 
+// Lehmer's method (Knuth, TAOCP vol. 2, 4.5.2, algorithm L) for x >= y: the
+// quotient sequence of the leading 62 bits (x's top 62 and y's bits at the
+// same place), accepted while the bracketing quotients (u + A) / (v + C) and
+// (u + B) / (v + D) agree, is the full numbers' sequence.  Returns the 2x2
+// matrix of those steps: (A x + B y, C x + D y) are the remainders they reach.
+// B == 0 when not even the first quotient is certain (y far below x).
+struct Lehmer {
+  long long A, B, C, D;
+};
+Lehmer lehmer_matrix(const Nat& x, const Nat& y) {
+  const size_t b0 = bit_length(x);
+  const size_t sh = b0 > 62 ? b0 - 62 : 0;
+  long long u = (long long)bits_at(x, sh), v = (long long)bits_at(y, sh);
+  long long A = 1, B = 0, C = 0, D = 1;
+  while (true) {
+    const __int128 d1 = (__int128)v + C, d2 = (__int128)v + D;
+    if (d1 <= 0 || d2 <= 0) break;
+    const __int128 q1 = ((__int128)u + A) / d1, q2 = ((__int128)u + B) / d2;
+    if (q1 != q2) break;
+    const long long q = (long long)q1;
+    long long T = A - q * C;
+    A = C;
+    C = T;
+    T = B - q * D;
+    B = D;
+    D = T;
+    T = u - q * v;
+    u = v;
+    v = T;
+  }
+  return Lehmer{A, B, C, D};
+}
+
+// (x, y) <- (A x + B y, C x + D y) in one pass and in place, for a Lehmer
+// matrix applied to two remainders: each row's entries have opposite signs
+// (or one is zero) and magnitudes below 2^62, so every limb's A x_i + B y_i
+// lies below 2^126 and, with its carry, fits a signed 128-bit accumulator;
+// the images are the next two remainders, nonnegative and no longer than x.
+void apply_matrix(Nat& x, Nat& y, long long A, long long B, long long C, long long D) {
+  const size_t n = std::max(x.v.size(), y.v.size());
+  x.v.resize(n, 0);
+  y.v.resize(n, 0);
+  __int128 c1 = 0, c2 = 0;
+  for (size_t i = 0; i < n; ++i) {
+    const __int128 xi = (__int128)x.v[i], yi = (__int128)y.v[i];
+    const __int128 t1 = (__int128)A * xi + (__int128)B * yi + c1;
+    const __int128 t2 = (__int128)C * xi + (__int128)D * yi + c2;
+    x.v[i] = (Limb)t1;
+    y.v[i] = (Limb)t2;
+    c1 = t1 >> 64;  // arithmetic: a borrow carries as -1
+    c2 = t2 >> 64;
+  }
+  trim(x);
+  trim(y);
+}
+
+// The same matrix on the cofactors of those remainders, (t0, t1) <- (A t0 +
+// B t1, C t0 + D t1), in one pass and in place.  Consecutive cofactors of
+// Euclid's sequence alternate in sign, as do the entries of each row, so
+// A t0 and B t1 never have opposite signs: the new magnitude is
+// |A| |t0| + |B| |t1| (below 2^127 per limb with its carry) and the sign is
+// that of either nonzero term.
+void apply_matrix_cofactors(Int& t0, Int& t1, long long A, long long B, long long C, long long D) {
+  auto mag = [](long long v) { return (unsigned long long)(v < 0 ? -(unsigned long long)v : (unsigned long long)v); };
+  auto sign_of = [](long long a, const Int& x, long long b, const Int& y) {
+    if (a != 0 && !is_zero(x.mag)) return (a < 0) != x.neg;
+    return (b < 0) != y.neg;
+  };
+  const bool n0 = sign_of(A, t0, B, t1), n1 = sign_of(C, t0, D, t1);
+  const unsigned __int128 a = mag(A), b = mag(B), c = mag(C), d = mag(D);
+  const size_t n = std::max(t0.mag.v.size(), t1.mag.v.size());
+  t0.mag.v.resize(n + 1, 0);
+  t1.mag.v.resize(n + 1, 0);
+  unsigned __int128 c0 = 0, c1 = 0;
+  for (size_t i = 0; i <= n; ++i) {
+    const unsigned __int128 x = t0.mag.v[i], y = t1.mag.v[i];
+    const unsigned __int128 u0 = a * x + b * y + c0, u1 = c * x + d * y + c1;
+    t0.mag.v[i] = (Limb)u0;
+    t1.mag.v[i] = (Limb)u1;
+    c0 = u0 >> 64;
+    c1 = u1 >> 64;
+  }
+  if (c0) t0.mag.v.push_back((Limb)c0);
+  if (c1) t1.mag.v.push_back((Limb)c1);
+  trim(t0.mag);
+  trim(t1.mag);
+  t0.neg = n0 && !is_zero(t0.mag);
+  t1.neg = n1 && !is_zero(t1.mag);
+}
+
 }  // namespace
+
+Nat gcd(Nat a, Nat b) {
+  if (cmp(a, b) < 0) std::swap(a, b);
+  // Lehmer batches while b is wider than two limbs (each replaces about 30
+  // single steps by one pass over the numbers), then Euclid's single steps
+  while (b.v.size() > 2) {
+    const Lehmer m = lehmer_matrix(a, b);
+    if (m.B == 0) {
+      Nat r = mod(a, b);
+      a = std::move(b);
+      b = std::move(r);
+    } else {
+      apply_matrix(a, b, m.A, m.B, m.C, m.D);
+    }
+  }
+  while (!is_zero(b)) {
+    Nat r = mod(a, b);
+    a = std::move(b);
+    b = std::move(r);
+  }
+  return a;
+}
 
 bool rational_reconstruct(const Nat& X, const Nat& M, const Nat& nbound, const Nat& dbound, Int* N, Nat* D) {
   // Extended Euclid on (M, X) with the cofactor of X, stopped at the first
@@ -409,34 +487,14 @@ bool rational_reconstruct(const Nat& X, const Nat& M, const Nat& nbound, const N
   Nat r0 = M, r1 = X;
   Int t0, t1;
   t1.mag = from_u64(1);
-  // Lehmer's method (Knuth, TAOCP vol. 2, 4.5.2, algorithm L): the quotient
-  // sequence of the leading 62 bits, accepted while the bracketing quotients
-  // (u + A) / (v + C) and (u + B) / (v + D) agree, is the full numbers'
-  // sequence; its 2x2 matrix is then applied once.  Run only while r1 stays
-  // more than 64 bits above the bound: one batch shrinks r1 by less than
-  // 2^63, so no remainder of a batch reaches the stopping point.
+  // Lehmer batches (lehmer_matrix), each applied once to the remainders and
+  // the cofactors.  Run only while r1 stays more than 64 bits above the
+  // bound: one batch shrinks r1 by less than 2^63, so no remainder of a batch
+  // reaches the stopping point.
   const size_t stop_bits = bit_length(nbound) + 64;
   while (bit_length(r1) > stop_bits) {
-    const size_t b0 = bit_length(r0);
-    const size_t sh = b0 > 62 ? b0 - 62 : 0;
-    long long u = (long long)bits_at(r0, sh), v = (long long)bits_at(r1, sh);
-    long long A = 1, B = 0, C = 0, Dc = 1;
-    while (true) {
-      const __int128 d1 = (__int128)v + C, d2 = (__int128)v + Dc;
-      if (d1 <= 0 || d2 <= 0) break;
-      const __int128 q1 = ((__int128)u + A) / d1, q2 = ((__int128)u + B) / d2;
-      if (q1 != q2) break;
-      const long long q = (long long)q1;
-      long long T = A - q * C;
-      A = C;
-      C = T;
-      T = B - q * Dc;
-      B = Dc;
-      Dc = T;
-      T = u - q * v;
-      u = v;
-      v = T;
-    }
+    const Lehmer lm = lehmer_matrix(r0, r1);
+    const long long A = lm.A, B = lm.B, C = lm.C, Dc = lm.D;
     if (B == 0) {  // no usable leading quotient: one full-precision step
       Nat q, r;
       divmod(r0, r1, &q, &r);
@@ -446,15 +504,8 @@ bool rational_reconstruct(const Nat& X, const Nat& M, const Nat& nbound, const N
       t0 = std::move(t1);
       t1 = std::move(t);
     } else {
-      Int R0, R1;
-      R0.mag = r0;
-      R1.mag = r1;
-      Int n0 = lincomb(R0, A, R1, B), n1 = lincomb(R0, C, R1, Dc);
-      Int s0 = lincomb(t0, A, t1, B), s1 = lincomb(t0, C, t1, Dc);
-      r0 = std::move(n0.mag);
-      r1 = std::move(n1.mag);
-      t0 = std::move(s0);
-      t1 = std::move(s1);
+      apply_matrix(r0, r1, A, B, C, Dc);
+      apply_matrix_cofactors(t0, t1, A, B, C, Dc);
     }
   }
   while (cmp(r1, nbound) > 0) {

@@ -735,3 +735,16 @@ extern "C" int rg_rational_reconstruct(const int64_t* x, int xl, const int64_t* 
   if (!big::to_limbs(N, num, limbs) || !big::to_limbs(Di, den, limbs)) return RG_ERR_RANGE;
   return RG_OK;
 }
+
+extern "C" int rg_big_gcd(const uint64_t* a, int al, const uint64_t* b, int bl, uint64_t* g, int gl) {
+  if (!a || !b || !g || al < 1 || bl < 1 || gl < 1) return RG_ERR_ARG;
+  big::Nat A, B;
+  A.v.assign(a, a + al);
+  B.v.assign(b, b + bl);
+  big::trim(A);
+  big::trim(B);
+  const big::Nat G = big::gcd(A, B);
+  if ((int)G.v.size() > gl) return RG_ERR_RANGE;
+  for (int i = 0; i < gl; ++i) g[i] = i < (int)G.v.size() ? G.v[i] : 0;
+  return RG_OK;
+}

@@ -355,6 +355,14 @@ void rg_solution_free(rg_solution* s);
 int rg_rational_reconstruct(const int64_t* x, int xl, const int64_t* m, int ml, int nbits, int dbits, int64_t* num,
                             int64_t* den, int limbs);
 
+/*
+ * gcd(a, b) of naturals given as al and bl little-endian 64-bit limbs, by the
+ * host big-integer code the solve's reconstruction uses (exposed for
+ * testing; gcd(0, 0) = 0).  Writes gl limbs to g.  RG_ERR_RANGE if the gcd
+ * needs more than gl limbs, RG_ERR_ARG on bad arguments.
+ */
+int rg_big_gcd(const uint64_t* a, int al, const uint64_t* b, int bl, uint64_t* g, int gl);
+
 /* Reconstruction of the results: 0 = balanced Garner (the default); 1 = CRT
  * with a round-to-nearest quotient ("Accelerating Multiple-Precision LU
  * Decomposition with Ozaki Scheme II") for the wide outputs (limbs,

@@ -64,3 +64,27 @@ def test_many_sizes_around_the_lehmer_boundary(lib):
             assert r == (n, d)
         else:
             assert r is None or (abs(r[0]) <= 2**nbits and 0 < r[1] <= 2**dbits and (r[1] * x - r[0]) % m == 0)
+
+
+@pytest.mark.parametrize("bits", [1, 63, 64, 65, 128, 129, 200, 1000, 5000, 15000, 30000])
+def test_gcd_against_python(lib, bits):
+    """The host gcd (Lehmer batches over two limbs, Euclid below) against math.gcd, with planted
+    common factors of every size and operands of unequal length."""
+    rng = random.Random(bits)
+    for _ in range(8):
+        g = rng.getrandbits(rng.randrange(1, bits + 1)) | 1
+        a = g * rng.getrandbits(bits)
+        b = g * rng.getrandbits(max(1, bits - rng.randrange(0, bits // 2 + 1)))
+        assert lib.big_gcd(a, b) == math.gcd(a, b)
+        assert lib.big_gcd(b, a) == math.gcd(a, b)
+
+
+def test_gcd_special_cases(lib):
+    fib = [0, 1]
+    while fib[-1].bit_length() < 4000:  # consecutive Fibonacci numbers: every quotient is 1
+        fib.append(fib[-1] + fib[-2])
+    cases = [(0, 0), (0, 7), (7, 0), (1, 1), (2**4000, 2**1234), (2**4000 + 1, 2**4000 + 1),
+             (fib[-1], fib[-2]), (fib[-1] * 3, fib[-2] * 3), (12345 * (2**3000 + 7), 2**3000 + 7),
+             (2**3000 + 7, 5), (3**2000, 3**1500 * 2**100), ((1 << 5000) - 1, (1 << 3000) - 1)]
+    for a, b in cases:
+        assert lib.big_gcd(a, b) == math.gcd(a, b), (a.bit_length(), b.bit_length())
