@@ -11,6 +11,7 @@
 #include <cuda_runtime.h>
 
 #include <algorithm>
+#include <atomic>
 #include <chrono>
 #include <cmath>
 #include <cstring>
@@ -632,22 +633,27 @@ extern "C" int rg_solve_i64(const int64_t* A_in, const int64_t* B_in, int64_t n6
   // the remaining components' values, give the common denominator D: their
   // lcm divides det A, and a factor cancelled in one component's fraction
   // rarely cancels in all of them.
+  // Each sampling thread forms its component's value and reconstructs it,
+  // then joins the other threads on the remaining values, which every
+  // thread takes one at a time from a shared counter.
   const long long sample = std::min<long long>(comps, std::max(1, std::min(4, nthreads / 2)));
-  for (long long k = 0; k < sample; ++k) Xv[k] = value_of(k, scratch[k]);
   std::vector<big::Nat> Ds(sample);
   std::vector<char> rec_ok(sample, 0);
   {
+    std::atomic<long long> next{sample};
+    auto values = [&](Scratch& S) {
+      for (long long k = next.fetch_add(1); k < comps; k = next.fetch_add(1)) Xv[k] = value_of(k, S);
+    };
     std::vector<std::thread> th;
     for (long long k = 0; k < sample; ++k)
       th.emplace_back([&, k] {
+        Xv[k] = value_of(k, scratch[k]);
         big::Int Nk;
         rec_ok[k] = big::rational_reconstruct(Xv[k], Pm, nbound, dbound, &Nk, &Ds[k]);
+        values(scratch[k]);
       });
     const int rest = std::max(1, nthreads - (int)sample);
-    for (int w = 0; w < rest; ++w)
-      th.emplace_back([&, w] {
-        for (long long k = sample + w; k < comps; k += rest) Xv[k] = value_of(k, scratch[sample + w]);
-      });
+    for (int w = 0; w < rest; ++w) th.emplace_back([&, w] { values(scratch[sample + w]); });
     for (auto& t : th) t.join();
   }
   big::Nat D = big::from_u64(1);
