@@ -54,27 +54,31 @@ def build(force: bool = False) -> str:
 def _load():
     global _lib
     if _lib is None:
-        lib = ctypes.CDLL(build())
-        i64p = ctypes.POINTER(ctypes.c_int64)
-        dp = ctypes.POINTER(ctypes.c_double)
-        ci = ctypes.c_int
-        lib.oracle_matmul_i64.argtypes = [i64p, i64p, i64p, ci, ci, ci, ci, i64p, ci, ci]
-        lib.oracle_matmul_i64.restype = ctypes.c_long
-        lib.oracle_matmul_limbs.argtypes = [i64p, ci, i64p, ci, i64p, ci, ci, ci, ci, i64p, ci, ci]
-        lib.oracle_matmul_limbs.restype = ctypes.c_long
-        lib.oracle_enclose_f64.argtypes = [dp, dp, dp, dp, ci, ci, ci, i64p, ci, ci]
-        lib.oracle_enclose_f64.restype = ci
-        fp = ctypes.POINTER(ctypes.c_float)
-        lib.oracle_enclose_f32.argtypes = [fp, fp, fp, fp, ci, ci, ci, i64p, ci, ci]
-        lib.oracle_enclose_f32.restype = ci
-        lib.oracle_interval_f64.argtypes = [dp, dp, dp, dp, dp, dp, ci, ci, ci, i64p, ci, ci]
-        lib.oracle_interval_f64.restype = ci
-        lib.oracle_interval_f32.argtypes = [fp, fp, fp, fp, fp, fp, ci, ci, ci, i64p, ci, ci]
-        lib.oracle_interval_f32.restype = ci
-        lib.oracle_threads.argtypes = [ci]
-        lib.oracle_threads.restype = ci
-        _lib = lib
+        _lib = _configure(ctypes.CDLL(build()))
     return _lib
+
+
+def _configure(lib):
+    """Declare the C oracle's entry points on a loaded library (this build, or a test's copy)."""
+    i64p = ctypes.POINTER(ctypes.c_int64)
+    dp = ctypes.POINTER(ctypes.c_double)
+    ci = ctypes.c_int
+    lib.oracle_matmul_i64.argtypes = [i64p, i64p, i64p, ci, ci, ci, ci, i64p, ci, ci]
+    lib.oracle_matmul_i64.restype = ctypes.c_long
+    lib.oracle_matmul_limbs.argtypes = [i64p, ci, i64p, ci, i64p, ci, ci, ci, ci, i64p, ci, ci]
+    lib.oracle_matmul_limbs.restype = ctypes.c_long
+    lib.oracle_enclose_f64.argtypes = [dp, dp, dp, dp, ci, ci, ci, i64p, ci, ci]
+    lib.oracle_enclose_f64.restype = ci
+    fp = ctypes.POINTER(ctypes.c_float)
+    lib.oracle_enclose_f32.argtypes = [fp, fp, fp, fp, ci, ci, ci, i64p, ci, ci]
+    lib.oracle_enclose_f32.restype = ci
+    lib.oracle_interval_f64.argtypes = [dp, dp, dp, dp, dp, dp, ci, ci, ci, i64p, ci, ci]
+    lib.oracle_interval_f64.restype = ci
+    lib.oracle_interval_f32.argtypes = [fp, fp, fp, fp, fp, fp, ci, ci, ci, i64p, ci, ci]
+    lib.oracle_interval_f32.restype = ci
+    lib.oracle_threads.argtypes = [ci]
+    lib.oracle_threads.restype = ci
+    return lib
 
 
 def default_threads() -> int:
