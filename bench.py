@@ -469,8 +469,9 @@ def main():
                    "l2": "flushed between timed steps (512 MiB write outside the timed events)"},
         "roofline": roofline,
         "stages_ms": stages_ms,
-        # our kernels per call: split, GEMM, Garner, plus the planner for limbs and fp64
-        "gpu_launches": (3 if w.kind == "int" else 4) * args.steps * world,
+        # our kernels per call: split, GEMM and Garner, the planner for every kind but int64, and the
+        # slice sum when the layout lets the GEMM split K
+        "gpu_launches": ((3 if w.kind == "int" else 4) + (1 if L.splits > 1 else 0)) * args.steps * world,
         "clocks": clock_info,
     }
 

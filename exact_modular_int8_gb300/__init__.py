@@ -69,7 +69,8 @@ class ResGemmError(RuntimeError):
 
 class Layout(ctypes.Structure):
     _fields_ = [("ra", ctypes.c_size_t), ("rb", ctypes.c_size_t), ("rc", ctypes.c_size_t),
-                ("lda", ctypes.c_int64), ("ldb", ctypes.c_int64), ("ldc", ctypes.c_int64), ("pmax", ctypes.c_int)]
+                ("lda", ctypes.c_int64), ("ldb", ctypes.c_int64), ("ldc", ctypes.c_int64), ("pmax", ctypes.c_int),
+                ("splits", ctypes.c_int)]
 
 
 class PlanInfo(ctypes.Structure):

@@ -390,6 +390,7 @@ int rg_workspace_layout_batched(int op, int64_t batch, int64_t M, int64_t N, int
   out->ldb = L.ldb;
   out->ldc = L.ldc;
   out->pmax = L.pmax;
+  out->splits = L.splits > 0 ? L.splits : 1;
   return RG_OK;
 }
 

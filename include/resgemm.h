@@ -278,11 +278,14 @@ size_t rg_workspace_bytes_batched(int op, int64_t batch, int64_t M, int64_t N, i
  *   rc: uint8 product residues, [pmax][M][ldc] (ldc = N rounded up to 16)
  * Residue planes follow the prime order q_0 = 251, q_1 = 241, ...; a batched
  * call stores each prime's planes for all products back to back
- * ([pmax][batch][M][lda] and so on). */
+ * ([pmax][batch][M][lda] and so on).  splits: the K slices rc has room for
+ * (more than one lets the GEMM split long K over idle SMs; the slices are then
+ * summed mod q into the first by one extra kernel launch per call). */
 typedef struct {
   size_t ra, rb, rc;
   int64_t lda, ldb, ldc;
   int pmax;
+  int splits;
 } rg_layout;
 int rg_workspace_layout(int op, int64_t M, int64_t N, int64_t K, int la, int lb, int lc, int nprimes,
                         unsigned flags, rg_layout* out);

@@ -93,6 +93,16 @@ def test_workspace_sizes(rg):
     assert rg.workspace_bytes(rg.RG_OP_LIMBS, 4, 4, 4, la=2, lb=2, lc=7) == 0
 
 
+def test_layout_reports_k_slices(rg):
+    """rc holds as many K slices as the GEMM may use: one for a single 1024-K chunk, one per chunk
+    while the tiles alone cannot fill the GPU, at most 16."""
+    assert rg.workspace_layout(rg.RG_OP_I64, 1024, 1024, 1024).splits == 1
+    assert rg.workspace_layout(rg.RG_OP_ENCLOSE, 1024, 1024, 4096).splits == 4  # 16 pair tiles, 4 chunks
+    assert rg.workspace_layout(rg.RG_OP_I64, 512, 512, 131072).splits == 16  # 4 pair tiles, 128 chunks
+    assert rg.workspace_layout(rg.RG_OP_I64, 4096, 4096, 4096).splits == 1  # 256 pair tiles fill the GPU
+    assert rg.workspace_layout(rg.RG_OP_I64, 0, 8, 8).splits == 1  # an empty problem
+
+
 def test_workspace_query_refuses_shapes_the_kernels_cannot_index(rg):
     """Shapes past 32-bit rows, columns or batch, K past 2^17, or more than 2^31 - 1 GEMM tiles get 0
     (an invalid problem), never a size wrapped modulo 2^64."""
