@@ -158,10 +158,12 @@ int* status_word() {
   return words[dev];
 }
 
-int finish(void* ws, cudaStream_t s, unsigned flags) {
+// The status word of the call: read into `host_word` when the caller gives
+// one (any host int, pinned or not), else into this thread's pinned word.
+int finish(void* ws, cudaStream_t s, unsigned flags, int* host_word = nullptr) {
   if (!(flags & (RG_FLAG_SYNC | RG_FLAG_HOST))) return RG_OK;
   int fallback = 0;
-  int* st = status_word();
+  int* st = host_word ? host_word : status_word();
   if (!st) st = &fallback;
   DevPlan* plan = static_cast<DevPlan*>(ws);
   if (cudaMemcpyAsync(st, &plan->status, sizeof(int), cudaMemcpyDeviceToHost, s) != cudaSuccess) return RG_ERR_CUDA;
@@ -177,10 +179,11 @@ int finish(void* ws, cudaStream_t s, unsigned flags) {
 
 // Shared driver for every entry point; `batch` products of the same shape
 // share one plan (one prime count, one pair of scale exponents).  A2 and B2
-// are the radii of interval operands (null otherwise).
+// are the radii of interval operands (null otherwise).  `status_host`, if
+// given, is the host int the final status read lands in (see finish()).
 int run(int op, const void* A, const void* A2, int la, const void* B, const void* B2, int lb, void* C, void* C2,
         int lc, long long batch, long long M, long long N, long long K, int nprimes, unsigned flags, void* ws,
-        size_t ws_bytes, void* stream) {
+        size_t ws_bytes, void* stream, int* status_host = nullptr) {
   if (!ws || (reinterpret_cast<uintptr_t>(ws) & 255u) != 0) return RG_ERR_ARG;
   if (batch < 0 || M < 0 || N < 0 || K < 0 || nprimes < 0 || nprimes > kNumPrimes) return RG_ERR_ARG;
   // an empty problem reads no operand, and writes outputs only if it has entries
@@ -213,7 +216,7 @@ int run(int op, const void* A, const void* A2, int la, const void* B, const void
         if (is_enclose(op)) RG_TRY(cudaMemsetAsync(C2, 0, out_bytes, s));
       }
     }
-    return finish(ws, s, flags);
+    return finish(ws, s, flags, status_host);
   }
   RG_TRY(upload_tables());
   const void* dA = A;
@@ -267,7 +270,7 @@ int run(int op, const void* A, const void* A2, int la, const void* B, const void
     RG_TRY(cudaMemcpyAsync(C, dC, out_bytes, cudaMemcpyDeviceToHost, s));
     if (is_enclose(op)) RG_TRY(cudaMemcpyAsync(C2, dC2, out_bytes, cudaMemcpyDeviceToHost, s));
   }
-  return finish(ws, s, flags);
+  return finish(ws, s, flags, status_host);
 }
 
 }  // namespace
@@ -497,12 +500,19 @@ extern "C" size_t rg_noalloc_scratch_bytes(void) { return kNoAllocScratchBytes; 
 
 extern "C" int res_gemm_i64_noalloc(const int64_t* A, const int64_t* B, int64_t* C, int64_t M, int64_t N, int64_t K,
                                     int nprimes, unsigned flags, void* stream) {
+  // the argument checks of res_gemm_i64, in its order, before the layout
+  if (M < 0 || N < 0 || K < 0 || nprimes < 0 || nprimes > kNumPrimes) return RG_ERR_ARG;
+  if ((M && N && K && (!A || !B)) || (M && N && !C)) return RG_ERR_ARG;
+  if (K > RG_MAX_K) return RG_ERR_RANGE;
   Layout L;
   if (!make_layout(RG_OP_I64, 1, M, N, K, 1, 1, 1, nprimes, flags, &L)) return RG_ERR_ARG;
   if (L.total > kNoAllocScratchBytes) return RG_ERR_WORKSPACE;  // before any device work
   void* ws = nullptr;
   int rc = noalloc_scratch(&ws);
   if (rc != RG_OK) return rc;
+  // the closing status read lands in this stack word: the pinned per-thread
+  // word of the other entry points is allocated on first use
+  int status = 0;
   return run(RG_OP_I64, A, nullptr, 1, B, nullptr, 1, C, nullptr, 1, 1, M, N, K, nprimes,
-             flags, ws, kNoAllocScratchBytes, stream);
+             flags, ws, kNoAllocScratchBytes, stream, &status);
 }

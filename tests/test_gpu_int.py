@@ -1,8 +1,9 @@
 """GPU parity of the exact int64 path (res_gemm_i64) against the CPU oracle.
 
 Bit-exact comparison, element by element: in full on the small and 1024^3
-workloads and on ragged shapes that span several tiles and a tail, on seeded
-sample rows for the long-K workload at full size, plus closed forms.
+workloads, the long-K workload and the 4096^3 workload (planned and all 53
+primes), and on ragged shapes that span several tiles and a tail, plus closed
+forms.
 """
 import numpy as np
 import pytest
@@ -10,7 +11,7 @@ import torch
 
 import oracle
 from tests.gpu_util import balanced_mod, dev, host, rg, stage_buffers  # noqa: F401
-from workloads import WORKLOADS, int_matrices, sample_rows
+from workloads import WORKLOADS, int_matrices
 
 pytestmark = pytest.mark.gpu
 
@@ -102,14 +103,33 @@ def test_fixed_prime_count(rg, nprimes):
     assert np.array_equal(C, A @ B)
 
 
-def test_longk_int8_sampled_rows(rg):
+def test_longk_int8_full(rg):
+    # K = 2^17, the longest exact sum ("enclosure-gemm", Requirements and limits)
     w = WORKLOADS["longk_int8"]
     A, B = w.generate()
     C = host(rg.res_gemm_i64(dev(A), dev(B)))
-    rows = sample_rows(w.M, w.seed)
-    ref = oracle.matmul_i64(A, B, lc=1, rows=rows)[:, :, 0]
-    assert np.array_equal(C[rows], ref)
+    ref = oracle.matmul_i64(A, B, lc=1)[:, :, 0]
+    assert np.array_equal(C, ref)
     assert rg.get_plan()["nprimes"] == 5
+
+
+@pytest.fixture(scope="module")
+def exact24_4096():
+    """The 4096^3 workload and its oracle product (computed once for the module)."""
+    w = WORKLOADS["exact24_4096"]
+    A, B = w.generate()
+    return A, B, oracle.matmul_i64(A, B, lc=1)[:, :, 0]
+
+
+@pytest.mark.parametrize("nprimes,expect", [(0, 8), (53, 53)], ids=["planned", "all_53_primes"])
+def test_exact24_4096_full(rg, exact24_4096, nprimes, expect):
+    # the square workload the GEMM-stage throughput is quoted on, every entry,
+    # with the planned prime count and with the whole prime set (CRT uniqueness:
+    # the same integers)
+    A, B, ref = exact24_4096
+    C = rg.res_gemm_i64(dev(A), dev(B), nprimes=nprimes)
+    assert rg.get_plan()["nprimes"] == expect
+    assert np.array_equal(host(C), ref)
 
 
 def test_longk_closed_form(rg):

@@ -5,7 +5,7 @@ import torch
 
 import oracle
 from tests.gpu_util import dev, host, rg  # noqa: F401
-from workloads import WORKLOADS, limb_matrices, sample_rows
+from workloads import WORKLOADS, limb_matrices
 
 pytestmark = pytest.mark.gpu
 
@@ -51,16 +51,26 @@ def test_small_values_in_wide_limbs(rg):
     assert rg.get_plan()["nprimes"] <= 5
 
 
-def test_wide128_2048_sampled_rows(rg):
+@pytest.fixture(scope="module")
+def wide128_2048():
+    """The 2048^3 signed 128-bit workload and its 6-limb oracle product (computed once)."""
     w = WORKLOADS["wide128_2048"]
     A, B = w.generate()
-    C = host(rg.res_gemm_limbs(dev(A), dev(B), w.out_limbs))
-    rows = sample_rows(w.M, w.seed)
-    ref = oracle.matmul_limbs(A, B, w.out_limbs, rows=rows)
-    assert np.array_equal(C[rows], ref)
+    return w, A, B, oracle.matmul_limbs(A, B, w.out_limbs)
+
+
+@pytest.mark.parametrize("nprimes,expect", [(0, 38), (53, 53)], ids=["planned", "all_53_primes"])
+def test_wide128_2048_full(rg, wide128_2048, nprimes, expect):
+    # every entry, with the planned prime count and with the full prime set
+    # the workload prescribes (the same integers by CRT uniqueness)
+    w, A, B, ref = wide128_2048
+    C = host(rg.res_gemm_limbs(dev(A), dev(B), w.out_limbs, nprimes=nprimes))
+    assert np.array_equal(C, ref)
     plan = rg.get_plan()
-    # max |x| of values uniform in [-2^127, 2^127) has bit length 127
-    assert plan["bits_a"] == 127 and plan["bits_b"] == 127 and plan["bound_bits"] == 127 + 127 + 11
+    assert plan["nprimes"] == expect
+    if not nprimes:
+        # max |x| of values uniform in [-2^127, 2^127) has bit length 127
+        assert plan["bits_a"] == 127 and plan["bits_b"] == 127 and plan["bound_bits"] == 127 + 127 + 11
 
 
 @pytest.mark.parametrize("nprimes", [42, 43, 52, 53])
