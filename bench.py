@@ -3,8 +3,9 @@
 
 A step is one call of the whole path (device planner, residue split, per-prime
 tensor-core GEMM, balanced Garner) on one synthetic problem already resident in
-HBM.  The default workload is the exact int64 product M = N = K = 1024 with
-entries uniform in [-2^23, 2^23) (seed 1).  The metric is effective
+HBM.  The default workload is the exact int64 product M = N = K = 4096 with
+entries uniform in [-2^23, 2^23) (seed 5), the square product the per-prime
+GEMM stage's tensor-core fraction is quoted on.  The metric is effective
 2*M*N*K / time, in TOPS (10^12 integer operations per second).
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME]
@@ -41,8 +42,9 @@ def parse_args():
     ap.add_argument("--steps", type=int, default=20)
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
-    ap.add_argument("--workload", default="exact24_1024")
-    ap.add_argument("--no-extras", action="store_true", help="skip e2e, cpu baseline, int8 probe and 4096^3 stage")
+    ap.add_argument("--workload", default="exact24_4096")
+    ap.add_argument("--no-extras", action="store_true",
+                    help="skip e2e, cpu baseline, the tensor-rate probes and the secondary workloads")
     ap.add_argument("--solve", type=int, default=0, metavar="N",
                     help="instead, time the exact solve of an N x N system with 24-bit entries")
     return ap.parse_args()
@@ -190,7 +192,7 @@ def run_reference(args):
 
     w = WORKLOADS[args.workload]
     A, B = w.generate()
-    rows, _, dt = time_oracle(w, A, B, 5.0)  # size one step to about five seconds (or one whole pass)
+    rows, _, dt = time_oracle(w, A, B, 2.0)  # size one step to about two seconds (or one whole pass)
     import numpy as np
 
     sel = np.arange(rows, dtype=np.int64) if rows < w.M else None
@@ -350,9 +352,9 @@ def main():
 
     def call(out=None):
         if w.kind == "int":
-            return rg.res_gemm_i64(dA, dB, sync=False, out=out)
+            return rg.res_gemm_i64(dA, dB, nprimes=w.nprimes, sync=False, out=out)
         if w.kind == "limbs":
-            return rg.res_gemm_limbs(dA, dB, w.out_limbs, sync=False, out=out)
+            return rg.res_gemm_limbs(dA, dB, w.out_limbs, nprimes=w.nprimes, sync=False, out=out)
         if w.kind == "interval":  # A, B hold (midpoint, radius) stacked
             return rg.interval_gemm(dA[0], dA[1], dB[0], dB[1], sync=False, out=out)
         return rg.enclose_gemm(dA, dB, sync=False, out=out)
@@ -422,8 +424,8 @@ def main():
     products = 3 if w.kind == "interval" else 1  # an interval product is three exact products
     la = lb = w.limbs if w.kind == "limbs" else 1
     lc = w.out_limbs if w.kind == "limbs" else 1
-    L = rg.workspace_layout(op, w.M, w.N, w.K, la, lb, lc)
-    ws = rg.workspace(rg.workspace_bytes(op, w.M, w.N, w.K, la, lb, lc), dev)
+    L = rg.workspace_layout(op, w.M, w.N, w.K, la, lb, lc, nprimes=w.nprimes)
+    ws = rg.workspace(rg.workspace_bytes(op, w.M, w.N, w.K, la, lb, lc, nprimes=w.nprimes), dev)
     # the alone timing runs the first planes of the workspace as one stage call
     # (an interval call's 3P planes are capped at the 53 the stage accepts)
     Pa = min(P * products, len(rg.primes()))
@@ -465,7 +467,8 @@ def main():
         "warmup": max(args.warmup, 3), "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": workload_dtype(w), "data": "synthetic",
         "config": {"workload": w.name, "M": w.M, "N": w.N, "K": w.K, "entries": workload_description(w),
-                   "seed": w.seed, "nprimes": f"planned on the device: {P}",
+                   "seed": w.seed,
+                   "nprimes": f"fixed by the caller: {P}" if w.nprimes else f"planned on the device: {P}",
                    "l2": "flushed between timed steps (512 MiB write outside the timed events)"},
         "roofline": roofline,
         "stages_ms": stages_ms,
@@ -477,10 +480,22 @@ def main():
 
     if rank == 0 and world == 1 and not args.no_extras:
         line["e2e"] = measure_e2e(rg, w, A, B, args, dev)
-        line["int8_library_tops"] = int8_probe(torch, dev)
-        if line["int8_library_tops"]:
-            line["roofline"]["frac_of_int8_library_peak"] = achieved / line["int8_library_tops"]
-        line["gemm_stage_4096"] = gemm_stage_4096(rg, torch, dev, flush, peak)
+        rates = rate_probes(rg, torch, dev)
+        line["tensor_rates"] = rates
+        int8 = rates.get("mma_sync_s8_tops")
+        if int8:
+            # the metric's INT8 roofline: the warp-level s8 MMA, the only integer
+            # tensor-core instruction on sm_103a; the residue GEMM runs on the fp16
+            # pipe instead, so this fraction can exceed 1
+            line["roofline"]["int8_peak"] = int8
+            line["roofline"]["int8_peak_instruction"] = "mma.sync.aligned.m16n8k32.row.col.s32.s8.s8.s32"
+            line["roofline"]["frac_of_int8_peak"] = achieved / int8
+        f16 = rates.get("tcgen05_f16_tflops")
+        if f16:
+            # context: the instruction's own measured rate, from shared-memory operands with no data movement
+            line["roofline"]["f16_instruction_peak"] = f16
+            line["roofline"]["frac_of_f16_instruction_peak"] = achieved / f16
+        line["secondary"] = secondary_workloads(rg, torch, dev, flush, w, dA, dB, out, peak, args)
         line["cpu_baseline"] = cpu_baseline(w, A, B)
     if rank == 0:
         print(json.dumps(line), flush=True)
@@ -496,11 +511,11 @@ def measure_e2e(rg, w, A, B, args, dev):
     hB = torch.from_numpy(B).pin_memory()
     if w.kind == "int":
         out = torch.empty((w.M, w.N), dtype=torch.int64).pin_memory()
-        fn = lambda: rg.res_gemm_i64(hA, hB, out=out)
+        fn = lambda: rg.res_gemm_i64(hA, hB, nprimes=w.nprimes, out=out)
         d2h = out.numel() * 8
     elif w.kind == "limbs":
         out = torch.empty((w.M, w.N, w.out_limbs), dtype=torch.int64).pin_memory()
-        fn = lambda: rg.res_gemm_limbs(hA, hB, w.out_limbs, out=out)
+        fn = lambda: rg.res_gemm_limbs(hA, hB, w.out_limbs, nprimes=w.nprimes, out=out)
         d2h = out.numel() * 8
     elif w.kind == "interval":
         fn = lambda: rg.interval_gemm(hA[0], hA[1], hB[0], hB[1])
@@ -520,93 +535,111 @@ def measure_e2e(rg, w, A, B, args, dev):
             "api": "exact_modular_int8_gb300 call on pinned host tensors (C ABI with RG_FLAG_HOST)"}
 
 
-def int8_probe(torch, dev):
-    """INT8 tensor-core rate of the library path on this GPU (torch._int_mm, 8192^3)."""
+def _time_events(torch, dev, fn, reps, flush=None):
+    """Per-launch milliseconds of fn() over `reps` launches, each bracketed by events on the
+    current stream (L2 flushed before each when `flush` is given)."""
+    ev = []
+    for _ in range(reps):
+        if flush is not None:
+            flush.fill_(1.0)
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        e0.record()
+        fn()
+        e1.record()
+        ev.append((e0, e1))
+    torch.cuda.synchronize(dev)
+    return [a.elapsed_time(b) for a, b in ev]
+
+
+def rate_probes(rg, torch, dev):
+    """Peak rates of the tensor-core instructions a residue product could run on, measured
+    here: the warp-level INT8 MMA (the metric's INT8 roofline), tcgen05 kind::f16 (what the
+    residue GEMM uses) and kind::f8f6f4 E4M3 (what an FP8 digit split would use); plus the
+    INT8 library GEMM (torch._int_mm, 8192^3) for context.  Best of five launches after three
+    warm-ups, CUDA events on the launching stream; SM clocks sampled over the probes."""
+    out = {}
+    clocks = ClockSampler(dev.index)
+    clocks.start()
+    for key, kind, iters in (("mma_sync_s8_tops", rg.RG_PROBE_MMA_S8, 20000),
+                             ("tcgen05_f16_tflops", rg.RG_PROBE_TCGEN05_F16, 8192),
+                             ("tcgen05_e4m3_tflops", rg.RG_PROBE_TCGEN05_E4M3, 8192)):
+        ops = [0.0]
+
+        def launch(kind=kind, iters=iters, ops=ops):
+            ops[0] = rg.probe_mma_rate(kind, iters)
+
+        for _ in range(3):
+            launch()
+        ms = _time_events(torch, dev, launch, 5)
+        if rg.status() != rg.RG_OK:
+            out[key] = None
+            continue
+        out[key] = ops[0] / (min(ms) * 1e-3) / 1e12
+        out[key.rsplit("_", 1)[0] + "_ms"] = min(ms)
+    out["clocks"] = clocks.stop()
+    if out.get("tcgen05_f16_tflops") and out.get("tcgen05_e4m3_tflops"):
+        # an FP8 balanced base-17 digit split needs three E4M3 sub-products per fp16 one
+        out["e4m3_over_f16"] = out["tcgen05_e4m3_tflops"] / out["tcgen05_f16_tflops"]
+        out["fp8_digit_split_speedup"] = out["e4m3_over_f16"] / 3.0
     try:
         n = 8192
         a = torch.randint(-128, 128, (n, n), dtype=torch.int8, device=dev)
         b = torch.randint(-128, 128, (n, n), dtype=torch.int8, device=dev)
         for _ in range(2):
             torch._int_mm(a, b)
-        torch.cuda.synchronize(dev)
-        best = None
-        for _ in range(5):
-            e0 = torch.cuda.Event(enable_timing=True)
-            e1 = torch.cuda.Event(enable_timing=True)
-            e0.record()
-            torch._int_mm(a, b)
-            e1.record()
-            torch.cuda.synchronize(dev)
-            ms = e0.elapsed_time(e1)
-            best = ms if best is None or ms < best else best
-        return 2.0 * n**3 / (best * 1e-3) / 1e12
+        out["int8_library_tops"] = 2.0 * n**3 / (min(_time_events(torch, dev, lambda: torch._int_mm(a, b), 5)) *
+                                                 1e-3) / 1e12
+        del a, b
     except Exception:  # noqa: BLE001 - a missing library kernel only removes a context figure
-        return None
+        out["int8_library_tops"] = None
+    return out
 
 
-def gemm_stage_4096(rg, torch, dev, flush, peak):
-    """The per-prime GEMM stage at 4096^3 with 8 primes (24-bit entries, seed 5)."""
-    from workloads import WORKLOADS
-
-    w = WORKLOADS["exact24_4096"]
-    A, B = w.generate()
-    dA, dB = torch.from_numpy(A).to(dev), torch.from_numpy(B).to(dev)
-    rg.res_gemm_i64(dA, dB)
-    P = rg.get_plan()["nprimes"]
-    L = rg.workspace_layout(rg.RG_OP_I64, w.M, w.N, w.K)
-    ws = rg.workspace(rg.workspace_bytes(rg.RG_OP_I64, w.M, w.N, w.K), dev)
-    ra = ws[L.ra:L.ra + P * w.M * L.lda * 2].view(torch.float16).view(P, w.M, L.lda)
-    rb = ws[L.rb:L.rb + P * w.K * L.ldb * 2].view(torch.float16).view(P, w.K, L.ldb)
-    rc = torch.empty((P, w.M, L.ldc), dtype=torch.uint8, device=dev)
-    for _ in range(3):
-        rg.res_gemm_stage(ra, rb, P, w.M, w.N, w.K, RC=rc, sync=False)
-    ev = []
-    for _ in range(10):
-        flush.fill_(1.0)
-        e0 = torch.cuda.Event(enable_timing=True)
-        e1 = torch.cuda.Event(enable_timing=True)
-        e0.record()
-        rg.res_gemm_stage(ra, rb, P, w.M, w.N, w.K, RC=rc, sync=False)
-        e1.record()
-        ev.append((e0, e1))
-    torch.cuda.synchronize(dev)
-    ms = sum(a.elapsed_time(b) for a, b in ev) / len(ev)
-    tf = 2.0 * w.macs * P / (ms * 1e-3) / 1e12
-    # whole call at this size
-    for _ in range(2):
-        rg.res_gemm_i64(dA, dB, sync=False)
-    torch.cuda.synchronize(dev)
-    e0 = torch.cuda.Event(enable_timing=True)
-    e1 = torch.cuda.Event(enable_timing=True)
-    flush.fill_(1.0)
-    e0.record()
-    for _ in range(5):
-        rg.res_gemm_i64(dA, dB, sync=False)
-    e1.record()
-    torch.cuda.synchronize(dev)
-    call_ms = e0.elapsed_time(e1) / 5
-    # batched-prime scaling: the same call with all 53 primes (the result is the same integers)
-    P53 = len(rg.primes())
-    ref = rg.res_gemm_i64(dA, dB, sync=False)
-    out53 = rg.res_gemm_i64(dA, dB, nprimes=P53)
-    stages53 = []
-    for _ in range(3):
+def _stage_times(rg, torch, dev, flush, fn, reps):
+    """Mean per-stage milliseconds (split, GEMM, Garner) of fn() with the stage-event hook."""
+    st = []
+    for _ in range(reps):
         flush.fill_(1.0)
         evs = [torch.cuda.Event(enable_timing=True) for _ in range(4)]
         rg.set_stage_events(evs)
-        rg.res_gemm_i64(dA, dB, nprimes=P53, sync=False, out=out53)
+        fn()
         rg.set_stage_events(None)
-        stages53.append(evs)
+        st.append(evs)
     torch.cuda.synchronize(dev)
-    if rg.status() != rg.RG_OK or not torch.equal(out53, ref):
-        raise SystemExit("the 53-prime call differs from the planned one")
-    st53 = {n: sum(e[i].elapsed_time(e[i + 1]) for e in stages53) / len(stages53)
+    return {n: sum(e[i].elapsed_time(e[i + 1]) for e in st) / len(st)
             for i, n in enumerate(("split_ms", "gemm_ms", "garner_ms"))}
-    tf53 = 2.0 * w.macs * P53 / (st53["gemm_ms"] * 1e-3) / 1e12
-    return {"primes": P, "gemm_ms": ms, "gemm_tflops": tf, "frac_of_fp16_peak": tf / peak,
-            "call_ms": call_ms, "call_effective_tops": 2.0 * w.macs / (call_ms * 1e-3) / 1e12,
-            "all_53_primes": {**st53, "gemm_tflops": tf53, "frac_of_fp16_peak": tf53 / peak,
-                              "call_ms": sum(st53.values())}}
+
+
+def secondary_workloads(rg, torch, dev, flush, w, dA, dB, ref, peak, args):
+    """Context figures beside the headline line, each call timed alone with L2 flushed before
+    it: the 1024^3 exact product (the latency-bound size), and, for an int64 headline, the same
+    call on all 53 primes (batched-prime scaling; its integers must equal the planned call's)."""
+    from workloads import WORKLOADS
+
+    res = {}
+    reps = max(args.steps, 10)
+    if w.name != "exact24_1024":
+        s = WORKLOADS["exact24_1024"]
+        A, B = s.generate()
+        sA, sB = torch.from_numpy(A).to(dev), torch.from_numpy(B).to(dev)
+        o = rg.res_gemm_i64(sA, sB)
+        ms = _time_events(torch, dev, lambda: rg.res_gemm_i64(sA, sB, sync=False, out=o), reps, flush)
+        stages = _stage_times(rg, torch, dev, flush, lambda: rg.res_gemm_i64(sA, sB, sync=False, out=o), reps)
+        P = rg.get_plan()["nprimes"]
+        res["exact24_1024"] = {"call_ms": sum(ms) / len(ms), "call_effective_tops": 2.0 * s.macs / (
+            sum(ms) / len(ms) * 1e-3) / 1e12, **stages, "primes": P,
+            "gemm_frac_of_fp16_peak": 2.0 * s.macs * P / (stages["gemm_ms"] * 1e-3) / 1e12 / peak}
+    if w.kind == "int" and not w.nprimes:
+        P53 = len(rg.primes())
+        o53 = rg.res_gemm_i64(dA, dB, nprimes=P53)
+        if rg.status() != rg.RG_OK or not torch.equal(o53, ref):
+            raise SystemExit("the 53-prime call differs from the planned one")
+        ms = _time_events(torch, dev, lambda: rg.res_gemm_i64(dA, dB, nprimes=P53, sync=False, out=o53), 3, flush)
+        st = _stage_times(rg, torch, dev, flush, lambda: rg.res_gemm_i64(dA, dB, nprimes=P53, sync=False, out=o53), 3)
+        tf = 2.0 * w.macs * P53 / (st["gemm_ms"] * 1e-3) / 1e12
+        res["all_53_primes"] = {**st, "call_ms": sum(ms) / len(ms), "gemm_tflops": tf, "frac_of_fp16_peak": tf / peak}
+    return res
 
 
 if __name__ == "__main__":

@@ -45,6 +45,7 @@ RG_FLAG_HOST = 2
 RG_FLAG_TRANS_B = 4
 RG_OP_I64, RG_OP_LIMBS, RG_OP_ENCLOSE, RG_OP_STAGE, RG_OP_ENCLOSE_F32 = 0, 1, 2, 3, 4
 RG_OP_INTERVAL, RG_OP_INTERVAL_F32 = 5, 6
+RG_PROBE_MMA_S8, RG_PROBE_TCGEN05_F16, RG_PROBE_TCGEN05_E4M3 = 0, 1, 2
 MAX_K = 131072
 NUM_PRIMES = 53
 
@@ -56,6 +57,7 @@ EXPORTED = (
     "rg_workspace_layout_batched", "enclose_gemm_f32", "enclose_gemm_f32_batched", "interval_gemm_f64",
     "interval_gemm_f32", "interval_gemm_f64_batched", "interval_gemm_f32_batched", "rg_solve_i64",
     "rg_solution_free", "rg_rational_reconstruct", "rg_big_gcd", "rg_set_crt_mode", "rg_set_stage_events",
+    "rg_probe_mma_rate",
 )
 
 
@@ -156,6 +158,12 @@ def library():
             lib.rg_big_gcd.restype = ci
             lib.rg_set_stage_events.argtypes = [ctypes.POINTER(ctypes.c_void_p), ci]
             lib.rg_set_stage_events.restype = ci
+            lib.rg_probe_mma_rate.argtypes = [ci, ci, ci, vp, sz, vp, ctypes.POINTER(ctypes.c_double)]
+            lib.rg_probe_mma_rate.restype = ci
+            lib.res_gemm_i64_noalloc.argtypes = [vp, vp, vp, i64, i64, i64, ci, cu, vp]
+            lib.res_gemm_i64_noalloc.restype = ci
+            lib.rg_noalloc_scratch_bytes.argtypes = []
+            lib.rg_noalloc_scratch_bytes.restype = sz
             _lib = lib
     return _lib
 
@@ -508,6 +516,19 @@ def set_stage_events(events) -> None:
     _check(lib.rg_set_stage_events(arr, 4), "rg_set_stage_events")
 
 
+def probe_mma_rate(kind: int, iters: int, blocks: int = 0, ws: torch.Tensor | None = None) -> float:
+    """Enqueue one launch of a tensor-core rate probe (RG_PROBE_*) on the current stream of
+    the current device; returns the operations (2 x multiply-adds) it performs.  Time it with
+    events around the call; read its status afterwards with status(ws)."""
+    dev = torch.device("cuda", torch.cuda.current_device())
+    w = ws if ws is not None else workspace(4096, dev)
+    ops = ctypes.c_double(0.0)
+    _check(library().rg_probe_mma_rate(int(kind), int(blocks), int(iters), w.data_ptr(), w.numel(),
+                                       torch.cuda.current_stream(dev).cuda_stream, ctypes.byref(ops)),
+           "rg_probe_mma_rate")
+    return ops.value
+
+
 def status(ws: torch.Tensor | None = None, device=None) -> int:
     dev = torch.device("cuda", torch.cuda.current_device()) if device is None else torch.device(device)
     w = ws if ws is not None else workspace(4096, dev)
@@ -542,22 +563,23 @@ def digest(lo: torch.Tensor, hi: torch.Tensor) -> str:
 
 def res_gemm_i64_noalloc(A: torch.Tensor, B: torch.Tensor, nprimes: int = 0, sync: bool = True,
                          out=None) -> torch.Tensor:
-    """res_gemm_i64 on the library's fixed static scratch: for callers that cannot
-    allocate device memory (the output is allocated here only when `out` is None)."""
+    """res_gemm_i64 on the library's fixed static scratch, for callers that cannot
+    allocate device memory when they call.  A [M,K] and B [K,N] are int64 CUDA tensors; the
+    result is allocated here only when `out` is None, and a given `out` must be a contiguous
+    int64 [M,N] tensor on A's device.  Non-contiguous operands are copied first (an
+    allocation), and the copies stay referenced until the call has returned; with
+    sync=False the caller must keep A and B alive until the stream has run the call."""
     if A.dtype != torch.int64 or B.dtype != torch.int64 or A.dim() != 2 or B.dim() != 2 or A.shape[1] != B.shape[0]:
         raise ValueError("A [M,K] and B [K,N] int64 expected")
     if A.device.type != "cuda" or B.device != A.device:
         raise ValueError("device tensors on one GPU expected")
     M, K = A.shape
     N = B.shape[1]
-    C = out if out is not None else torch.empty((M, N), dtype=torch.int64, device=A.device)
-    f = library().res_gemm_i64_noalloc
-    f.argtypes = [ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int64, ctypes.c_int64, ctypes.c_int64,
-                  ctypes.c_int, ctypes.c_uint, ctypes.c_void_p]
-    f.restype = ctypes.c_int
-    with torch.cuda.device(A.device):
-        rc = f(A.contiguous().data_ptr(), B.contiguous().data_ptr(), C.data_ptr(), M, N, K, nprimes,
-               RG_FLAG_SYNC if sync else 0, torch.cuda.current_stream(A.device).cuda_stream)
+    A, B, dev, flags = _prepare(A, B, sync, False)
+    C = _output(out, (M, N), torch.int64, A, False, "res_gemm_i64_noalloc")
+    with _on(dev):
+        rc = library().res_gemm_i64_noalloc(A.data_ptr(), B.data_ptr(), C.data_ptr(), M, N, K, nprimes, flags,
+                                            torch.cuda.current_stream(dev).cuda_stream)
     _check(rc, "res_gemm_i64_noalloc")
     return C
 

@@ -21,7 +21,15 @@
  *    copies) and the library stages them through the workspace.
  *  - The caller owns every buffer, including the workspace `ws` of
  *    `ws_bytes` bytes (device memory, 256-byte aligned), sized by
- *    rg_workspace_bytes().  The library allocates no device memory.
+ *    rg_workspace_bytes().  The product entry points allocate no device
+ *    memory.  Two exceptions elsewhere in the library: rg_solve_i64 takes
+ *    its device buffers from cudaMallocAsync on its stream (and frees them
+ *    there), and the module holds one fixed 64 MiB static device array, the
+ *    scratch of res_gemm_i64_noalloc, on every GPU that loads it.
+ *  - A synchronising call reads its closing status into a pinned host word
+ *    that the library allocates (cudaHostAlloc) once per host thread and
+ *    device, on that thread's first synchronising call;
+ *    res_gemm_i64_noalloc reads it into a stack word instead.
  *  - All work is ordered on `stream` (a cudaStream_t; NULL = legacy default
  *    stream).  Without RG_FLAG_SYNC a call only enqueues work: it returns
  *    RG_OK once the arguments are accepted, and errors found on the device
@@ -232,13 +240,16 @@ int res_gemm_stage(const uint16_t* RA, int64_t lda, const uint16_t* RB, int64_t 
  * cudaMalloc's implicit synchronisation is not allowed, and code whose only
  * device memory is the buffers it was handed.
  *
- * Arguments and results are those of res_gemm_i64 (the caller still passes
- * A, B and C).  The scratch is one fixed static device array of
- * rg_noalloc_scratch_bytes() bytes (64 MiB) inside the library, which every
- * GPU that loads the library holds until the process exits.  A problem whose
- * scratch (rg_workspace_bytes(RG_OP_I64, ...)) exceeds it returns
- * RG_ERR_WORKSPACE before any device work.  No cudaMalloc, cudaFree or other
- * allocating routine is called.
+ * Arguments, results and status codes are those of res_gemm_i64 (the
+ * caller still passes A, B and C; K > 2^17 gives RG_ERR_RANGE).  The scratch
+ * is one fixed static device array of rg_noalloc_scratch_bytes() bytes
+ * (64 MiB) inside the library, which every GPU that loads the library holds
+ * until the process exits.  A problem whose scratch
+ * (rg_workspace_bytes(RG_OP_I64, ...)) exceeds it returns RG_ERR_WORKSPACE
+ * before any device work.  No cudaMalloc, cudaFree, cudaHostAlloc or other
+ * allocating routine is called: with RG_FLAG_SYNC or RG_FLAG_HOST the
+ * closing status is copied into a host stack word and the stream is
+ * synchronised.
  *
  * The first call on each device looks up the array's device address (and
  * copies the constant tables), so make that first call before any stream
@@ -326,9 +337,11 @@ int rg_get_plan(const void* ws, void* stream, rg_plan_info* out);
  * denominator d > 0 (X = N / d exactly), as `limbs` little-endian
  * two's-complement int64 limbs each, in a host array the library allocates
  * and rg_solution_free releases.  Requires n * max|A| < 2^63 (so the residual
- * stays one limb) and n <= 8192.  The call synchronises `stream`.  It is not
- * safe to run two solves at once on one device (one constant table holds the
- * lift's primes).
+ * stays one limb) and n <= 8192.  The call synchronises `stream`.  Unlike the
+ * product entry points it takes no workspace: its device buffers come from
+ * cudaMallocAsync on `stream` and are freed there before it returns.  It is
+ * not safe to run two solves at once on one device (one constant table holds
+ * the lift's primes).
  * Errors: RG_ERR_ARG, RG_ERR_RANGE (n or the entries out of range),
  * RG_ERR_SINGULAR (A is singular modulo every prime below 256: singular over
  * the rationals, unless det(A) is divisible by all 53 primes), RG_ERR_CUDA.
@@ -416,6 +429,34 @@ int rg_set_stage_events(void* const* events, int n);
  * 2 = CTA-pair kernel.  Returns the previous choice, or -1 for an invalid
  * value.  Not thread-safe; for tests and measurements only. */
 int rg_set_gemm_variant(int variant);
+
+/* Measurement: one launch of a peak-rate probe of a tensor-core instruction,
+ * enqueued on `stream` for the caller to time with events.  No page has a
+ * counterpart: the probes give the denominators the per-prime GEMM is
+ * reported against ("enclosure-gemm", Method: one INT8 tensor-core GEMM per
+ * prime, hence a "% of INT8 tensor-core roofline"), and the rate of the FP8
+ * instruction that a balanced base-17 digit split of the residues would use
+ * ("Accelerating Multiple-Precision LU Decomposition with Ozaki Scheme II",
+ * FP8 encoding).  Not part of the product path.
+ *   kind  RG_PROBE_MMA_S8: warp-level mma.sync m16n8k32 s8 x s8 -> s32 from
+ *           registers, eight independent accumulators per warp, 8 warps per
+ *           block (blocks = 0: four per SM);
+ *         RG_PROBE_TCGEN05_F16 / RG_PROBE_TCGEN05_E4M3: tcgen05.mma
+ *           cta_group::1 kind::f16 (fp16) / kind::f8f6f4 (E4M3), M = 128,
+ *           N = 256, operands in shared memory, fp32 accumulator in tensor
+ *           memory, one CTA per SM (blocks = 0: the SM count).
+ *   iters  rounds per warp or CTA (1 .. 2^24): 8 MMAs per round for
+ *          mma.sync, 4 for tcgen05 (K = 64 fp16 or 128 E4M3 per round).
+ *   ws     device memory of >= 256 bytes, 256-byte aligned, caller-owned;
+ *          the probe's status (RG_ERR_TIMEOUT if the tcgen05 probe's bounded
+ *          wait expired) is read from it with rg_status(ws, stream).
+ * *ops_per_launch receives 2 x the multiply-adds one launch performs.
+ * Returns RG_OK once enqueued, RG_ERR_ARG or RG_ERR_CUDA. */
+#define RG_PROBE_MMA_S8 0
+#define RG_PROBE_TCGEN05_F16 1
+#define RG_PROBE_TCGEN05_E4M3 2
+int rg_probe_mma_rate(int kind, int blocks, int iters, void* ws, size_t ws_bytes, void* stream,
+                      double* ops_per_launch);
 
 #ifdef __cplusplus
 }

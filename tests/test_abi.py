@@ -190,3 +190,13 @@ def test_binding_reports_refused_shapes_like_the_entry_points(rg):
         rg._need(rg.RG_OP_ENCLOSE, 2**31, 8, 8, "enclose_gemm")
     assert e.value.code == rg.RG_ERR_ARG
     assert rg._need(rg.RG_OP_I64, 8, 8, rg.MAX_K, "res_gemm_i64") == rg.workspace_bytes(rg.RG_OP_I64, 8, 8, rg.MAX_K)
+
+
+def test_probe_rejects_bad_arguments_before_the_device(rg):
+    lib = rg.library()
+    ops = ctypes.c_double(0.0)
+    # no workspace, or an unknown probe kind with no workspace: refused before any CUDA call
+    assert lib.rg_probe_mma_rate(rg.RG_PROBE_MMA_S8, 0, 10, None, 4096, None, ctypes.byref(ops)) == rg.RG_ERR_ARG
+    assert lib.rg_probe_mma_rate(7, 0, 10, None, 4096, None, ctypes.byref(ops)) == rg.RG_ERR_ARG
+    assert lib.rg_probe_mma_rate(rg.RG_PROBE_MMA_S8, 0, 10, 256, 4096, None, None) == rg.RG_ERR_ARG
+    assert lib.rg_probe_mma_rate(rg.RG_PROBE_MMA_S8, 0, 10, 256, 128, None, ctypes.byref(ops)) == rg.RG_ERR_ARG

@@ -41,7 +41,7 @@ def test_reference_arm_prints_one_contract_line():
     assert len(lines) == 1
     d = json.loads(lines[0])
     assert d["impl"] == "reference" and d["n_gpus"] == 1 and d["steps"] == 1 and d["higher_is_better"] is True
-    assert d["value"] > 0 and d["unit"] == "TOPS" and d["config"]["workload"] == "exact24_1024"
+    assert d["value"] > 0 and d["unit"] == "TOPS" and d["config"]["workload"] == "exact24_4096"
     cb = d["cpu_baseline"]
     assert cb["kind"] == "oracle" and cb["cores"] >= 1 and cb["value"] == d["value"] and cb["sample"]
     e = d["e2e"]

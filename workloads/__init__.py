@@ -30,6 +30,7 @@ class Workload:
     hi: int = 0
     limbs: int = 1  # limbs per entry for kind == "limbs"
     out_limbs: int = 1  # limbs of the exact result
+    nprimes: int = 0  # primes the call is asked to use (0: as many as the bound needs)
 
     def generate(self):
         """Return (A, B) as numpy arrays."""
@@ -55,6 +56,7 @@ class Workload:
 #  exact24_64     : 64^3, entries uniform in [-2^23, 2^23), seed 0
 #  exact24_1024   : 1024^3, same distribution, seed 1 (|C| < 2^57)
 #  wide128_2048   : 2048^3, signed 128-bit entries (2 limbs), seed 2, 6-limb result
+#  wide128_2048_p53: the same problem on the full set of 53 primes
 #  enclose_normal : fp64 standard normal, M=1024, K=4096, N=1024, seed 3
 #  longk_int8     : M=N=512, K=131072, entries in [-128, 128), seed 4
 #  exact24_4096   : 4096^3, entries in [-2^23, 2^23), seed 5 (GEMM-stage scale)
@@ -65,6 +67,7 @@ WORKLOADS = {
     "exact24_64": Workload("exact24_64", "int", 64, 64, 64, 0, -(2**23), 2**23),
     "exact24_1024": Workload("exact24_1024", "int", 1024, 1024, 1024, 1, -(2**23), 2**23),
     "wide128_2048": Workload("wide128_2048", "limbs", 2048, 2048, 2048, 2, limbs=2, out_limbs=6),
+    "wide128_2048_p53": Workload("wide128_2048_p53", "limbs", 2048, 2048, 2048, 2, limbs=2, out_limbs=6, nprimes=53),
     "enclose_normal": Workload("enclose_normal", "normal", 1024, 1024, 4096, 3),
     "longk_int8": Workload("longk_int8", "int", 512, 512, 131072, 4, -128, 128),
     "exact24_4096": Workload("exact24_4096", "int", 4096, 4096, 4096, 5, -(2**23), 2**23),
