@@ -13,6 +13,11 @@
 //                          would use (page "Accelerating Multiple-Precision LU
 //                          Decomposition with Ozaki Scheme II", FP8 balanced
 //                          base-17 encoding).
+//   RG_PROBE_TCGEN05_F16_BMN, _PAIR, _PAIR_BMN, _PAIR_BMN_SYNC: kind::f16 in
+//                          the forms the residue GEMM uses: B MN-major, the
+//                          CTA-pair instruction (cta_group::2, M = 256), and
+//                          the pair's issue loop (a wait on a completed
+//                          barrier and a commit every four MMAs).
 //
 // Not part of the product path.  The INT8 rate is the denominator of the
 // "% of INT8 tensor-core roofline" reported for the per-prime GEMM; the
@@ -122,14 +127,37 @@ __device__ __forceinline__ void probe_umma(uint32_t d, uint64_t a, uint64_t b, u
         : "memory");
 }
 
-// KIND 0: kind::f16, 1: kind::f8f6f4 (E4M3)
 template <int KIND>
+__device__ __forceinline__ void probe_umma_pair(uint32_t d, uint64_t a, uint64_t b, uint32_t idesc, uint32_t acc) {
+  static_assert(KIND == 0, "the pair probe runs kind::f16");
+  asm volatile(
+      "{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n tcgen05.mma.cta_group::2.kind::f16 [%0], %1, %2, %3, p;\n}\n" ::"r"(
+          d),
+      "l"(a), "l"(b), "r"(idesc), "r"(acc)
+      : "memory");
+}
+
+__device__ __forceinline__ void probe_cluster_sync() {
+  asm volatile("barrier.cluster.arrive.release.aligned;\nbarrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+
+// KIND 0: kind::f16, 1: kind::f8f6f4 (E4M3).  BMN: B is read MN-major (64-column
+// slabs 8 KB apart, as the residue GEMM stages an N-major B).  PAIR: clusters
+// of two CTAs, the first issuing cta_group::2 MMAs with M = 256 (each CTA
+// holds 128 rows of A and 128 columns of B).  SYNC: every round also waits on
+// an already completed barrier and commits to another, as the GEMM's issue
+// loop does per k-block.
+template <int KIND, bool BMN = false, bool PAIR = false, bool SYNC = false>
 __global__ void __launch_bounds__(128, 1) probe_tcgen05_kernel(int iters, unsigned long long limit_ns, DevPlan* plan) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint32_t* words = reinterpret_cast<uint32_t*>(smem);
   uint64_t* bar = reinterpret_cast<uint64_t*>(smem + kTcA + kTcB);
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bar + 1);
+  uint64_t* bar_ready = bar + 1;  // SYNC: completed once at set-up
+  uint64_t* bar_commit = bar + 2;  // SYNC: receives a commit every round
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bar + 3);
+  uint32_t rank = 0;
+  if constexpr (PAIR) asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(rank));
   // finite operand values: fp16 pairs in +-[1, 2), or E4M3 bytes with the
   // exponent's low bit clear (never the all-ones exponent and mantissa of NaN)
   for (int i = threadIdx.x; i < (kTcA + kTcB) / 4; i += blockDim.x) {
@@ -139,25 +167,65 @@ __global__ void __launch_bounds__(128, 1) probe_tcgen05_kernel(int iters, unsign
   asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
   if (threadIdx.x == 0) {
     asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(su32(bar)) : "memory");
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(su32(bar_ready)) : "memory");
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(su32(bar_commit)) : "memory");
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(su32(bar_ready)) : "memory");  // phase 0 done
   }
-  if (threadIdx.x < 32) {
-    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(su32(tmem_slot)),
-                 "r"((uint32_t)kTcN));
-    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;");
+  if (threadIdx.x < 32) {  // one warp of each CTA allocates (for the pair, jointly)
+    if constexpr (PAIR) {
+      asm volatile("tcgen05.alloc.cta_group::2.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(su32(tmem_slot)),
+                   "r"((uint32_t)kTcN));
+      asm volatile("tcgen05.relinquish_alloc_permit.cta_group::2.sync.aligned;");
+    } else {
+      asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(su32(tmem_slot)),
+                   "r"((uint32_t)kTcN));
+      asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;");
+    }
   }
   asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
   __syncthreads();
+  if constexpr (PAIR) probe_cluster_sync();
   asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
   const uint32_t tmem = *tmem_slot;
-  if (threadIdx.x == 0) {
-    const uint64_t a = probe_desc(su32(smem)), b = probe_desc(su32(smem + kTcA));
+  if (threadIdx.x == 0 && rank == 0) {
+    const uint64_t a = probe_desc(su32(smem));
+    // B: K-major rows (32 bytes per K step), or MN-major 64-column slabs 8 KB
+    // apart (16 K rows = 2048 bytes per K step)
+    const uint64_t b = BMN ? ((probe_desc(su32(smem + kTcA)) & ~(0x3FFFull << 16)) | ((uint64_t)(8192 >> 4) << 16))
+                           : probe_desc(su32(smem + kTcA));
+    constexpr uint32_t b_step = BMN ? 128 : 2;
+    constexpr uint32_t idesc =
+        (kTcIdesc & ~(0x1Fu << 24)) | ((uint32_t)((PAIR ? 2 * kTcM : kTcM) >> 4) << 24) | (BMN ? (1u << 16) : 0u);
     for (int it = 0; it < iters; ++it) {
+      if constexpr (SYNC) {
+        if (!probe_try_wait(su32(bar_ready), 0)) atomicCAS(&plan->status, 0, RG_ERR_TIMEOUT);  // never: phase 0 done
+        asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+      }
 #pragma unroll
-      for (int kk = 0; kk < 4; ++kk) probe_umma<KIND>(tmem, a + 2 * kk, b + 2 * kk, (it | kk) ? 1u : 0u);
+      for (int kk = 0; kk < 4; ++kk) {
+        if constexpr (PAIR)
+          probe_umma_pair<KIND>(tmem, a + 2 * kk, b + b_step * kk, idesc, (it | kk) ? 1u : 0u);
+        else
+          probe_umma<KIND>(tmem, a + 2 * kk, b + b_step * kk, (it | kk) ? 1u : 0u);
+      }
+      if constexpr (SYNC) {
+        if constexpr (PAIR)
+          asm volatile("tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
+                           su32(bar_commit))
+                       : "memory");
+        else
+          asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
+                           su32(bar_commit))
+                       : "memory");
+      }
     }
-    asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(su32(bar))
-                 : "memory");
+    if constexpr (PAIR)
+      asm volatile("tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(su32(bar))
+                   : "memory");
+    else
+      asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(su32(bar))
+                   : "memory");
     if (!probe_wait(su32(bar), limit_ns)) {
       atomicCAS(&plan->status, 0, RG_ERR_TIMEOUT);
       probe_wait(su32(bar), limit_ns);  // the issued MMAs must end before the memory is freed
@@ -166,10 +234,34 @@ __global__ void __launch_bounds__(128, 1) probe_tcgen05_kernel(int iters, unsign
   __syncwarp();
   asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
   __syncthreads();
+  if constexpr (PAIR) probe_cluster_sync();  // the first CTA's MMAs read both CTAs' memory
   if (threadIdx.x < 32) {
     asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
-    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"((uint32_t)kTcN));
+    if constexpr (PAIR)
+      asm volatile("tcgen05.dealloc.cta_group::2.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"((uint32_t)kTcN));
+    else
+      asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"((uint32_t)kTcN));
   }
+}
+
+template <typename K>
+cudaError_t launch_probe(K kernel, int blocks, bool pair, cudaStream_t s, int iters, unsigned long long limit_ns,
+                         DevPlan* plan) {
+  cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kTcSmem);
+  if (e != cudaSuccess) return e;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)blocks);
+  cfg.blockDim = dim3(128);
+  cfg.dynamicSmemBytes = kTcSmem;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = pair ? 2 : 1;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kernel, iters, limit_ns, plan);
 }
 
 }  // namespace
@@ -195,14 +287,34 @@ extern "C" int rg_probe_mma_rate(int kind, int blocks, int iters, void* ws, size
       break;
     }
     case RG_PROBE_TCGEN05_F16:
-    case RG_PROBE_TCGEN05_E4M3: {
-      const int nb = blocks ? blocks : sms;
-      const bool f16 = kind == RG_PROBE_TCGEN05_F16;
-      auto k = f16 ? probe_tcgen05_kernel<0> : probe_tcgen05_kernel<1>;
-      if (cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, kTcSmem) != cudaSuccess)
-        return RG_ERR_CUDA;
-      k<<<nb, 128, kTcSmem, s>>>(iters, limit_ns, plan);
-      *ops_per_launch = 2.0 * nb * (double)iters * 4 * kTcM * kTcN * (f16 ? 16.0 : 32.0);
+    case RG_PROBE_TCGEN05_E4M3:
+    case RG_PROBE_TCGEN05_F16_BMN:
+    case RG_PROBE_TCGEN05_F16_PAIR:
+    case RG_PROBE_TCGEN05_F16_PAIR_BMN:
+    case RG_PROBE_TCGEN05_F16_PAIR_BMN_SYNC: {
+      const bool pair = kind >= RG_PROBE_TCGEN05_F16_PAIR;
+      const int nb = blocks ? blocks : (pair ? (sms & ~1) : sms);
+      if (pair && (nb & 1)) return RG_ERR_ARG;
+      cudaError_t e;
+      switch (kind) {
+        case RG_PROBE_TCGEN05_F16: e = launch_probe(probe_tcgen05_kernel<0>, nb, false, s, iters, limit_ns, plan); break;
+        case RG_PROBE_TCGEN05_E4M3: e = launch_probe(probe_tcgen05_kernel<1>, nb, false, s, iters, limit_ns, plan); break;
+        case RG_PROBE_TCGEN05_F16_BMN:
+          e = launch_probe(probe_tcgen05_kernel<0, true>, nb, false, s, iters, limit_ns, plan);
+          break;
+        case RG_PROBE_TCGEN05_F16_PAIR:
+          e = launch_probe(probe_tcgen05_kernel<0, false, true>, nb, true, s, iters, limit_ns, plan);
+          break;
+        case RG_PROBE_TCGEN05_F16_PAIR_BMN:
+          e = launch_probe(probe_tcgen05_kernel<0, true, true>, nb, true, s, iters, limit_ns, plan);
+          break;
+        default:
+          e = launch_probe(probe_tcgen05_kernel<0, true, true, true>, nb, true, s, iters, limit_ns, plan);
+          break;
+      }
+      if (e != cudaSuccess) return RG_ERR_CUDA;
+      // per CTA and round: four MMAs of 128 rows (a pair's M = 256 instruction covers both CTAs' rows)
+      *ops_per_launch = 2.0 * nb * (double)iters * 4 * kTcM * kTcN * (kind == RG_PROBE_TCGEN05_E4M3 ? 32.0 : 16.0);
       break;
     }
     default:

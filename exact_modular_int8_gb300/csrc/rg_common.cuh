@@ -98,6 +98,25 @@ struct CrtTables {
 };
 const CrtTables& host_crt_tables();
 
+// CRT by idempotent sums, for results that fit in int64 ("Accelerating
+// Multiple-Precision LU Decomposition with Ozaki Scheme II", CRT with a
+// round-to-nearest quotient, taken here on the unreduced residues): for the
+// first P primes (P <= kIdemMaxP) and their product P, E_i = (P / q_i) *
+// ((P / q_i)^-1 mod q_i) mod P is 1 modulo q_i and 0 modulo every other
+// prime, so S = sum_i r_i E_i == x (mod P) for residues r_i in [0, q_i), and
+// x = S - round(S / P) P when |x| < P / 4.  Rows hold E_i mod 2^64 (two
+// words), f_i = round(2^20 E_i / P) and P mod 2^64.
+constexpr int kIdemMaxP = 12;
+constexpr int kIdemFracBits = 20;
+struct IdemTables {
+  uint32_t elo[kIdemMaxP + 1][kIdemMaxP];
+  uint32_t ehi[kIdemMaxP + 1][kIdemMaxP];
+  uint32_t f[kIdemMaxP + 1][kIdemMaxP];
+  uint32_t plo[kIdemMaxP + 1];
+  uint32_t phi[kIdemMaxP + 1];
+};
+const IdemTables& host_idem_tables();
+
 // ---------------------------------------------------------------------------
 // Device helpers
 // ---------------------------------------------------------------------------

@@ -186,6 +186,32 @@ const CrtTables& host_crt_tables() {
   return t;
 }
 
+const IdemTables& host_idem_tables() {
+  static IdemTables t;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    const Tables& b = host_tables();
+    typedef unsigned __int128 u128;  // the product of 12 primes below 256 is below 2^96
+    std::memset(&t, 0, sizeof(t));
+    for (int P = 1; P <= kIdemMaxP; ++P) {
+      u128 prod = 1;
+      for (int j = 0; j < P; ++j) prod *= (u128)b.q[j];
+      for (int i = 0; i < P; ++i) {
+        const int q = b.q[i];
+        const u128 m = prod / (u128)q;
+        const int inv = mod_pow((int)(m % (u128)q), q - 2, q);  // Fermat: q prime
+        const u128 e = m * (u128)inv % prod;                     // m * inv < 2^104
+        t.elo[P][i] = (uint32_t)e;
+        t.ehi[P][i] = (uint32_t)(e >> 32);
+        t.f[P][i] = (uint32_t)(((e << kIdemFracBits) + prod / 2) / prod);  // e * 2^20 < 2^116
+      }
+      t.plo[P] = (uint32_t)prod;
+      t.phi[P] = (uint32_t)(prod >> 32);
+    }
+  });
+  return t;
+}
+
 }  // namespace rg
 
 extern "C" int rg_prime(int i) {

@@ -315,7 +315,8 @@ typedef struct {
   int f_b;
   int lossless; /* fp64 only: 1 if both operands scaled exactly */
   int splits;   /* K slices the per-prime GEMM used (1: none; more when there were too few output tiles) */
-  int crt_rn;   /* 1: reconstructed by round-to-nearest CRT (the plan kept P > 4 |result|); 0: balanced Garner */
+  int crt_rn;   /* 0: balanced Garner; 1: round-to-nearest CRT on balanced digits; 2: CRT by idempotent
+                 * sums (both with P > 4 |result|; see rg_set_crt_mode) */
 } rg_plan_info;
 int rg_get_plan(const void* ws, void* stream, rg_plan_info* out);
 
@@ -379,17 +380,23 @@ int rg_rational_reconstruct(const int64_t* x, int xl, const int64_t* m, int ml, 
  */
 int rg_big_gcd(const uint64_t* a, int al, const uint64_t* b, int bl, uint64_t* g, int gl);
 
-/* Reconstruction of the results: 0 = balanced Garner (the default); 1 = CRT
- * with a round-to-nearest quotient ("Accelerating Multiple-Precision LU
- * Decomposition with Ozaki Scheme II") for the wide outputs (limbs,
- * enclosures, intervals) where the plan can keep P > 4 |result| (one more bit
- * of headroom, so sometimes one more prime), and for int64 where its planned
- * primes already exceed 4 |result|; Garner otherwise.  On GB300 Garner is the
- * faster of the two (38 primes, 128-bit, 2048^2 outputs: 264 against 317 us;
- * 8 primes, int64, 1024^2 outputs: 12.5 against 14.3 us), so mode 1 is not
- * the default.
- * rg_get_plan's crt_rn reports the choice a call made.  Returns the previous
- * mode, or -1 for an invalid one. */
+/* Reconstruction of the results.  Mode 0 (the default): one-limb results
+ * (res_gemm_i64, res_gemm_limbs with lc = 1) whose planned primes already
+ * exceed 4 |result| (no extra prime), with at most 12 primes, by CRT with
+ * idempotent sums: S = sum_i r_i E_i over the unreduced residues, E_i the
+ * CRT idempotent of q_i, and the result S - round(S / P) P formed modulo
+ * 2^64 (four integer multiply-adds per prime and entry); everything else by
+ * balanced Garner.  Mode 1: CRT with a round-to-nearest quotient on balanced
+ * digits ("Accelerating Multiple-Precision LU Decomposition with Ozaki Scheme
+ * II") for the wide outputs (limbs, enclosures, intervals) where the plan can
+ * keep P > 4 |result| (one more bit of headroom, so sometimes one more
+ * prime), and for int64 where its planned primes already exceed 4 |result|;
+ * Garner otherwise.  Mode 2: balanced Garner for every result.  On GB300
+ * Garner is faster than mode 1's digits (38 primes, 128-bit, 2048^2 outputs:
+ * 264 against 317 us; 8 primes, int64, 1024^2 outputs: 12.5 against 14.3 us).
+ * rg_get_plan's crt_rn reports the choice a call made (0 Garner, 1 balanced
+ * digits, 2 idempotent sums).  Returns the previous mode, or -1 for an
+ * invalid one. */
 int rg_set_crt_mode(int mode);
 
 /* Synchronise `stream` and return the device status of the last call that
@@ -443,10 +450,19 @@ int rg_set_gemm_variant(int variant);
  *           block (blocks = 0: four per SM);
  *         RG_PROBE_TCGEN05_F16 / RG_PROBE_TCGEN05_E4M3: tcgen05.mma
  *           cta_group::1 kind::f16 (fp16) / kind::f8f6f4 (E4M3), M = 128,
- *           N = 256, operands in shared memory, fp32 accumulator in tensor
- *           memory, one CTA per SM (blocks = 0: the SM count).
+ *           N = 256, operands in shared memory (both K-major), fp32
+ *           accumulator in tensor memory, one CTA per SM (blocks = 0: the SM
+ *           count);
+ *         RG_PROBE_TCGEN05_F16_BMN: the same with B read MN-major;
+ *         RG_PROBE_TCGEN05_F16_PAIR / _PAIR_BMN: cta_group::2 (clusters of
+ *           two CTAs, M = 256, N = 256), B K-major / MN-major; blocks must
+ *           be even (0: the SM count rounded down to even);
+ *         RG_PROBE_TCGEN05_F16_PAIR_BMN_SYNC: the pair form with the residue
+ *           GEMM's per-k-block issue loop (a barrier wait and a commit every
+ *           four MMAs), without data movement.
  *   iters  rounds per warp or CTA (1 .. 2^24): 8 MMAs per round for
- *          mma.sync, 4 for tcgen05 (K = 64 fp16 or 128 E4M3 per round).
+ *          mma.sync, 4 for tcgen05 (K = 64 fp16 or 128 E4M3 per round;
+ *          *ops_per_launch counts 128 rows per CTA for the pair forms too).
  *   ws     device memory of >= 256 bytes, 256-byte aligned, caller-owned;
  *          the probe's status (RG_ERR_TIMEOUT if the tcgen05 probe's bounded
  *          wait expired) is read from it with rg_status(ws, stream).
@@ -455,6 +471,10 @@ int rg_set_gemm_variant(int variant);
 #define RG_PROBE_MMA_S8 0
 #define RG_PROBE_TCGEN05_F16 1
 #define RG_PROBE_TCGEN05_E4M3 2
+#define RG_PROBE_TCGEN05_F16_BMN 3
+#define RG_PROBE_TCGEN05_F16_PAIR 4
+#define RG_PROBE_TCGEN05_F16_PAIR_BMN 5
+#define RG_PROBE_TCGEN05_F16_PAIR_BMN_SYNC 6
 int rg_probe_mma_rate(int kind, int blocks, int iters, void* ws, size_t ws_bytes, void* stream,
                       double* ops_per_launch);
 

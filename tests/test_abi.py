@@ -172,12 +172,13 @@ def test_wait_limit_roundtrip(rg):
 
 
 def test_crt_mode_range(rg):
-    """Modes 0 (default) and 1 are accepted and return the previous mode; others are refused."""
+    """Modes 0 (default), 1 and 2 are accepted and return the previous mode; others are refused."""
     lib = rg.library()
     old = lib.rg_set_crt_mode(1)
     assert old in (0, 1)
     assert lib.rg_set_crt_mode(0) == 1
-    assert lib.rg_set_crt_mode(2) == -1 and lib.rg_set_crt_mode(-1) == -1
+    assert lib.rg_set_crt_mode(2) == 0 and lib.rg_set_crt_mode(0) == 2
+    assert lib.rg_set_crt_mode(3) == -1 and lib.rg_set_crt_mode(-1) == -1
     assert lib.rg_set_crt_mode(old) == 0
 
 

@@ -79,7 +79,7 @@ def test_fixed_prime_count_uses_garner(rg):
     assert np.array_equal(C_rn, C_g) and np.array_equal(C_rn, oracle.matmul_limbs(A, B, 6))
 
 
-def test_default_is_garner(rg):
+def test_default_is_garner_for_wide_results(rg):
     rg.library().rg_set_crt_mode(0)
     rng = np.random.default_rng(5)
     full = dict(low=-(2**63), high=2**63 - 1, endpoint=True, dtype=np.int64)

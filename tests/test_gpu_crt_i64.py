@@ -1,10 +1,11 @@
-"""The int64 path's two reconstructions.  By default it reconstructs by
-balanced Garner; in mode 1 of rg_set_crt_mode, by round-to-nearest CRT
-whenever its planned primes already exceed 4 |C| (the prime count for a bound
-one bit larger is no larger), and by Garner otherwise.  Operands at
-their extremes put |C| at its bound, where the rounded quotient has the least
-margin ("Accelerating Multiple-Precision LU Decomposition with Ozaki Scheme
-II", CRT by round-to-nearest; "exact-solve", balanced Garner)."""
+"""The int64 path's three reconstructions.  Whenever its planned primes
+already exceed 4 |C| (the prime count for a bound one bit larger is no
+larger), it reconstructs by idempotent sums with a rounded quotient by
+default (mode 0 of rg_set_crt_mode, up to 12 primes), by round-to-nearest CRT
+on balanced digits in mode 1, and by balanced Garner otherwise and in mode 2.
+Operands at their extremes put |C| at its bound, where the rounded quotient
+has the least margin ("Accelerating Multiple-Precision LU Decomposition with
+Ozaki Scheme II", CRT by round-to-nearest; "exact-solve", balanced Garner)."""
 import numpy as np
 import pytest
 
@@ -63,37 +64,55 @@ def test_result_at_its_bound(rg, mode, sign, b, K):
     T = 2 * b + int(np.ceil(np.log2(K)))
     ps = rg.primes()
     P = primes_for_bound(ps, T)
+    headroom = primes_for_bound(ps, T + 1) <= P
     C = host(rg.res_gemm_i64(dev(A), dev(B)))
     plan = rg.get_plan()
     assert plan["status"] == 0 and plan["bound_bits"] == T and plan["nprimes"] == P
-    assert plan["crt_rn"] == (1 if primes_for_bound(ps, T + 1) <= P else 0)
+    assert plan["crt_rn"] == (1 if headroom else 0)
     assert np.array_equal(C, want)
     mode(0)
+    C0 = host(rg.res_gemm_i64(dev(A), dev(B)))
+    assert rg.get_plan()["crt_rn"] == (2 if headroom and P <= 12 else 0)
+    assert np.array_equal(C0, want)
+    mode(2)
     C2 = host(rg.res_gemm_i64(dev(A), dev(B)))
     assert rg.get_plan()["crt_rn"] == 0
     assert np.array_equal(C2, want)
 
 
-def test_headline_workload_both_modes(rg, mode):
-    """1024^3, 24-bit entries: 8 primes give the extra bit for free; both reconstructions agree."""
+def test_headline_workload_all_modes(rg, mode):
+    """1024^3, 24-bit entries: 8 primes give the extra bit for free; the three reconstructions agree."""
     w = WORKLOADS["exact24_1024"]
     A, B = w.generate()
     dA, dB = dev(A), dev(B)
-    C0 = rg.res_gemm_i64(dA, dB)
+    C1 = rg.res_gemm_i64(dA, dB)
     plan = rg.get_plan()
     assert plan["nprimes"] == 8 and plan["crt_rn"] == 1
     mode(0)
+    C0 = rg.res_gemm_i64(dA, dB)
+    assert rg.get_plan()["crt_rn"] == 2
+    mode(2)
     C2 = rg.res_gemm_i64(dA, dB)
     assert rg.get_plan()["crt_rn"] == 0
-    assert bool((C0 == C2).all())
+    assert bool((C0 == C2).all()) and bool((C1 == C2).all())
 
 
-def test_caller_fixed_prime_count(rg, mode):
-    """53 fixed primes hold far more than 4 |C| for 27-bit entries (|C| < 70 * 2^54): round-to-nearest CRT, exact."""
-    rng = np.random.default_rng(11)
-    A = rng.integers(-(2**27), 2**27, size=(33, 70), dtype=np.int64)
-    B = rng.integers(-(2**27), 2**27, size=(70, 45), dtype=np.int64)
-    C = host(rg.res_gemm_i64(dev(A), dev(B), nprimes=53))
+@pytest.mark.parametrize("P", list(range(1, 13)))
+def test_idempotent_sums_every_prime_count(rg, mode, P):
+    """Caller-fixed prime counts 1..12, with the a-priori bound T as large as the headroom rule
+    allows (P >= 2^(T+2)) and results close to 2^T in both signs: the rounded quotient's margin
+    is at its thinnest, and mode 0 takes idempotent sums there."""
+    ps = rg.primes()
+    prod = 1
+    for q in ps[:P]:
+        prod *= q
+    T = min(prod.bit_length() - 3, 62)
+    ta, tb = (T + 1) // 2, T // 2
+    a, b = 2**ta - 1, 2**tb - 1  # bits_a + bits_b = T, |a b| close to 2^T
+    A = np.array([[a], [-a], [a // 3], [1], [0]], dtype=np.int64)
+    B = np.array([[b, -b, 1, 0]], dtype=np.int64)
+    mode(0)
+    C = host(rg.res_gemm_i64(dev(A), dev(B), nprimes=P))
     plan = rg.get_plan()
-    assert plan["nprimes"] == 53 and plan["crt_rn"] == 1
+    assert plan["bound_bits"] == T and plan["crt_rn"] == 2
     assert np.array_equal(C, oracle.matmul_i64(A, B, lc=1)[:, :, 0])
