@@ -974,14 +974,20 @@ __global__ void __launch_bounds__(256) split_interval_kernel(IvSide sa, IvSide s
 __device__ CrtTables g_crt;  // round-to-nearest CRT tables of every prime count
 __constant__ IdemTables c_idem;  // idempotent-sum CRT tables, prime counts 1..kIdemMaxP
 
-// x[e] = the int64 results of GE = 4 adjacent entries from their residues r_i
+// x[e] = the int64 results of four adjacent entries from their residues r_i
 // in [0, q_i) (one 32-bit word per prime, `plane` bytes apart), for exactly PP
 // primes, by the idempotent sum S = sum_i r_i E_i and the rounded quotient
-// k = round(S / P) (tables in IdemTables).  Exact when |x| < P / 4: the
-// quotient is formed as sum_i r_i f_i with f_i = round(2^20 E_i / P), within
-// PP * 250 * 2^-21 < 0.0015 of S / P (and below 2^32), while S / P lies within
-// 1/4 of k.  S and k P are formed modulo 2^64, which holds x.  Four integer
-// multiply-adds per prime and entry, no modular reduction.
+// k = round(S / P) (tables in IdemTables); S and k P are formed modulo 2^64,
+// which holds the result x = S - k P.  The quotient is estimated as
+// sum_i r_i f_i with f_i = round(2^20 E_i / P), within PP * 250 * 2^-21 <
+// 0.0015 of S / P (and below 2^32 - 2^19).  S / P lies within |x| / P of the
+// true quotient, and |x| <= (P - 1) / 2, so the estimate rounds to the true
+// quotient or to a neighbour:
+//  - PP >= 9: P > 2^70 and |x| < 2^63, so |x| / P < 2^-7 and it is the true one;
+//  - PP <= 8: P < 2^63, so the three candidates are told apart exactly: the
+//    result is the one in [-(P - 1) / 2, (P - 1) / 2] (a wrong one lies at
+//    least P / 2 + 1/2 from zero, also after wrapping modulo 2^64).
+// Four integer multiply-adds per prime and entry, no modular reduction.
 template <int PP>
 __device__ __forceinline__ void idem_reconstruct4(const uint8_t* __restrict__ rc, long long plane,
                                                   unsigned long long (&x)[4]) {
@@ -998,53 +1004,85 @@ __device__ __forceinline__ void idem_reconstruct4(const uint8_t* __restrict__ rc
       const uint32_t r = __byte_perm(rw[i], 0u, 0x4440u + (uint32_t)e);  // byte e, zero-extended
       lo[e] += (unsigned long long)r * elo;                                // < 12 * 250 * 2^32 < 2^44
       hi[e] += r * ehi;                                                    // modulo 2^32
-      kq[e] += r * f;                                                      // < 12 * 250 * 2^20 < 2^32 - 2^19
+      kq[e] += r * f;                                                      // < 12 * 250 * 2^20
     }
   }
   const unsigned long long P64 = ((unsigned long long)c_idem.phi[PP] << 32) | c_idem.plo[PP];
 #pragma unroll
   for (int e = 0; e < 4; ++e) {
-    const uint32_t k = (kq[e] + (1u << (kIdemFracBits - 1))) >> kIdemFracBits;  // round(S / P)
-    x[e] = lo[e] + ((unsigned long long)hi[e] << 32) - (unsigned long long)k * P64;
+    const uint32_t k = (kq[e] + (1u << (kIdemFracBits - 1))) >> kIdemFracBits;
+    unsigned long long v = lo[e] + ((unsigned long long)hi[e] << 32) - (unsigned long long)k * P64;
+    if constexpr (PP <= 8) {
+      const unsigned long long h = P64 >> 1;  // (P - 1) / 2, P odd
+      if (v + h > 2 * h) {                    // v outside [-h, h]: the quotient was off by one
+        const unsigned long long up = v - P64;  // quotient + 1
+        v = (up + h <= 2 * h) ? up : v + P64;
+      }
+    }
+    x[e] = v;
   }
 }
 
-// Runs idem_reconstruct4 with the prime count P (1..kIdemMaxP) as a
-// compile-time constant, so every table entry is an immediate constant operand.
-__device__ __forceinline__ void idem_reconstruct4_p(int P, const uint8_t* __restrict__ rc, long long plane,
-                                                    unsigned long long (&x)[4]) {
+// Int64 results (one limb) of up to kIdemMaxP primes by idempotent sums
+// (idem_reconstruct4), four adjacent entries per thread; the prime count is
+// dispatched to a compile-time constant, so every table entry is an
+// immediate constant operand.  Exact for every int64 result the plan (or the
+// caller's prime count) allows; rg_get_plan reports crt_rn = 2.
+__global__ void __launch_bounds__(128) crt_idem_kernel(const uint8_t* __restrict__ RC, long long ldc, long long plane,
+                                                       long long M, long long N, RowDiv rd, DevPlan* plan,
+                                                       int64_t* __restrict__ C) {
+  wait_for_predecessor();
+  if (plan->status) return;
+  const int P = plan->P;
+  if (P < 1 || P > kIdemMaxP) {  // the launch is chosen for pmax <= kIdemMaxP
+    if (blockIdx.x == 0 && threadIdx.x == 0) set_status(&plan->status, RG_ERR_RANGE);
+    return;
+  }
+  if (blockIdx.x == 0 && threadIdx.x == 0) plan->crt_rn = 2;
+  const long long per_row = (N + 3) / 4;
+  const long long item = (long long)blockIdx.x * blockDim.x + threadIdx.x;
+  if (item >= M * per_row) return;
+  const long long m = div_row(item, rd);  // item / per_row
+  const long long n0 = (item - m * per_row) * 4;
+  const uint8_t* rc = RC + m * ldc + n0;
+  unsigned long long v[4];
   switch (P) {
-    case 1: idem_reconstruct4<1>(rc, plane, x); break;
-    case 2: idem_reconstruct4<2>(rc, plane, x); break;
-    case 3: idem_reconstruct4<3>(rc, plane, x); break;
-    case 4: idem_reconstruct4<4>(rc, plane, x); break;
-    case 5: idem_reconstruct4<5>(rc, plane, x); break;
-    case 6: idem_reconstruct4<6>(rc, plane, x); break;
-    case 7: idem_reconstruct4<7>(rc, plane, x); break;
-    case 8: idem_reconstruct4<8>(rc, plane, x); break;
-    case 9: idem_reconstruct4<9>(rc, plane, x); break;
-    case 10: idem_reconstruct4<10>(rc, plane, x); break;
-    case 11: idem_reconstruct4<11>(rc, plane, x); break;
-    default: idem_reconstruct4<12>(rc, plane, x); break;
+    case 1: idem_reconstruct4<1>(rc, plane, v); break;
+    case 2: idem_reconstruct4<2>(rc, plane, v); break;
+    case 3: idem_reconstruct4<3>(rc, plane, v); break;
+    case 4: idem_reconstruct4<4>(rc, plane, v); break;
+    case 5: idem_reconstruct4<5>(rc, plane, v); break;
+    case 6: idem_reconstruct4<6>(rc, plane, v); break;
+    case 7: idem_reconstruct4<7>(rc, plane, v); break;
+    case 8: idem_reconstruct4<8>(rc, plane, v); break;
+    case 9: idem_reconstruct4<9>(rc, plane, v); break;
+    case 10: idem_reconstruct4<10>(rc, plane, v); break;
+    case 11: idem_reconstruct4<11>(rc, plane, v); break;
+    default: idem_reconstruct4<12>(rc, plane, v); break;
+  }
+  int64_t* out = C + m * N + n0;
+  if (n0 + 4 <= N && ((reinterpret_cast<uintptr_t>(out) & 15u) == 0)) {
+    *reinterpret_cast<ulonglong2*>(out) = make_ulonglong2(v[0], v[1]);
+    *reinterpret_cast<ulonglong2*>(out + 2) = make_ulonglong2(v[2], v[3]);
+  } else {
+#pragma unroll
+    for (int e = 0; e < 4; ++e)
+      if (n0 + e < N) out[e] = (int64_t)v[e];
   }
 }
-static_assert(kIdemMaxP == 12, "idem_reconstruct4_p dispatches prime counts 1..12");
+static_assert(kIdemMaxP == 12, "crt_idem_kernel dispatches prime counts 1..12");
 
 __device__ __forceinline__ CrtView crt_view(int P) { return CrtView{g_crt.M[P], g_crt.Pw[P], g_crt.Cw[P], g_crt.y[P]}; }
 
 // MAXP: a compile-time bound on the prime count (the workspace's pmax).
-// crt_mode (rg_set_crt_mode): when the planned primes already exceed
-// 4 |result| (the bound's prime count for one more bit is no larger than P),
-// mode 0 reconstructs one-limb results by idempotent sums (P <= kIdemMaxP)
-// and mode 1 int64 results by round-to-nearest CRT on balanced digits, at no
-// extra prime; otherwise, and in mode 2, as the plan says (Garner unless the
-// planner chose round-to-nearest CRT).
+// rn_free: reconstruct by round-to-nearest CRT whenever the planned primes
+// already exceed 4 |result| (the bound's prime count for one more bit is no
+// larger than P), at no extra prime; otherwise as the plan says.
 template <int LC, int MAXP>
 __global__ void __launch_bounds__(128) garner_int_kernel(const uint8_t* __restrict__ RC, long long ldc,
                                                          long long plane, long long M, long long N, RowDiv rd,
-                                                         DevPlan* plan, int64_t* __restrict__ C, int crt_mode) {
+                                                         DevPlan* plan, int64_t* __restrict__ C, int rn_free) {
   constexpr int W = 2 * LC, GE = GarnerGE<W>::value;
-  static_assert(LC != 1 || GE == 4, "the one-limb kernels reconstruct four entries per thread");
   wait_for_predecessor();
   if (plan->status) return;
   const int P = plan->P;
@@ -1052,19 +1090,15 @@ __global__ void __launch_bounds__(128) garner_int_kernel(const uint8_t* __restri
     if (blockIdx.x == 0 && threadIdx.x == 0) set_status(&plan->status, RG_ERR_RANGE);
     return;
   }
-  // the planner's choice (1); 2 is this kernel's own record of idempotent sums,
-  // which the test below re-derives
-  const bool plan_rn = plan->crt_rn == 1;
-  bool rn = plan_rn, idem = false;
-  if (!rn && crt_mode != 2) {
+  const bool plan_rn = plan->crt_rn != 0;
+  bool rn = plan_rn;
+  if (!rn && rn_free) {
     const int prn = primes_for_bound(plan->bound_bits + 1);
-    const bool headroom = prn != 0 && prn <= P;  // P > 4 |result|
-    idem = LC == 1 && crt_mode == 0 && headroom && P <= kIdemMaxP;
-    rn = crt_mode == 1 && headroom;
+    rn = prn != 0 && prn <= P;
   }
   // recorded for rg_get_plan; every block takes the same decision from the
   // same plan fields, so a block that reads the flag already set agrees
-  if ((rn || idem) && !plan_rn && blockIdx.x == 0 && threadIdx.x == 0) plan->crt_rn = idem ? 2 : 1;
+  if (rn && !plan_rn && blockIdx.x == 0 && threadIdx.x == 0) plan->crt_rn = 1;
   const CrtView crt = crt_view(P);
   const long long per_row = (N + GE - 1) / GE;
   const long long item = (long long)blockIdx.x * blockDim.x + threadIdx.x;
@@ -1072,23 +1106,10 @@ __global__ void __launch_bounds__(128) garner_int_kernel(const uint8_t* __restri
   const long long m = div_row(item, rd);  // item / per_row
   const long long n0 = (item - m * per_row) * GE;
   uint32_t x[GE][W];
-  if constexpr (LC == 1) {
-    if (idem) {
-      unsigned long long v[4];
-      idem_reconstruct4_p(P, RC + m * ldc + n0, plane, v);
-#pragma unroll
-      for (int e = 0; e < GE; ++e) {
-        x[e][0] = (uint32_t)v[e];
-        x[e][1] = (uint32_t)(v[e] >> 32);
-      }
-    }
-  }
-  if (!idem) {
-    if (rn)
-      crt_rn_reconstruct<W, GE, MainTab>(RC + m * ldc + n0, plane, P, crt, x);
-    else
-      garner_reconstruct<W, GE, MainTab, MAXP>(RC + m * ldc + n0, plane, P, x);
-  }
+  if (rn)
+    crt_rn_reconstruct<W, GE, MainTab>(RC + m * ldc + n0, plane, P, crt, x);
+  else
+    garner_reconstruct<W, GE, MainTab, MAXP>(RC + m * ldc + n0, plane, P, x);
   int64_t* out = C + (m * N + n0) * LC;
   if (n0 + GE <= N && ((reinterpret_cast<uintptr_t>(out) & 15u) == 0)) {
     // GE * LC consecutive int64: 16-byte stores
@@ -1572,13 +1593,15 @@ cudaError_t launch_garner(int op, const void* RC, long long ldc, long long plane
   // the packed digits of at most kGarnerSmallP primes fit in 3 registers per
   // entry, against 14 for all 53
   const bool small = pmax <= kGarnerSmallP;
-  // the int64 path takes mode 1's round-to-nearest CRT when its primes allow it;
-  // modes 0 and 2 apply to every one-limb result
   const int mode = g_crt_mode.load();
-  const int crt_mode = mode == 1 ? (op == RG_OP_I64 ? 1 : 2) : mode;
+  // mode 0: one-limb results of at most kIdemMaxP primes by idempotent sums
+  if (mode == 0 && lc == 1 && pmax >= 1 && pmax <= kIdemMaxP)
+    return launch_dependent(crt_idem_kernel, blocks_for(4), 128, 0, st, rc, ldc, plane, M, N, rowdiv_for(4), plan, C);
+  // mode 1: int64 by round-to-nearest CRT on balanced digits when its primes allow it
+  const int rn_free = op == RG_OP_I64 && mode == 1 ? 1 : 0;
   auto go = [&](auto k_small, auto k_all, int ge) {
     return launch_dependent(small ? k_small : k_all, blocks_for(ge), 128, 0, st, rc, ldc, plane, M, N, rowdiv_for(ge),
-                            plan, C, crt_mode);
+                            plan, C, rn_free);
   };
   switch (lc) {
     case 1: return go(garner_int_kernel<1, kGarnerSmallP>, garner_int_kernel<1, kNumPrimes>, GarnerGE<2>::value);

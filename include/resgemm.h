@@ -381,14 +381,15 @@ int rg_rational_reconstruct(const int64_t* x, int xl, const int64_t* m, int ml, 
 int rg_big_gcd(const uint64_t* a, int al, const uint64_t* b, int bl, uint64_t* g, int gl);
 
 /* Reconstruction of the results.  Mode 0 (the default): one-limb results
- * (res_gemm_i64, res_gemm_limbs with lc = 1) whose planned primes already
- * exceed 4 |result| (no extra prime), with at most 12 primes, by CRT with
- * idempotent sums: S = sum_i r_i E_i over the unreduced residues, E_i the
- * CRT idempotent of q_i, and the result S - round(S / P) P formed modulo
- * 2^64 (four integer multiply-adds per prime and entry); everything else by
- * balanced Garner.  Mode 1: CRT with a round-to-nearest quotient on balanced
- * digits ("Accelerating Multiple-Precision LU Decomposition with Ozaki Scheme
- * II") for the wide outputs (limbs, enclosures, intervals) where the plan can
+ * (res_gemm_i64, res_gemm_limbs with lc = 1) of at most 12 primes (every
+ * int64 product the library plans, and caller-fixed counts up to 12) by CRT
+ * with idempotent sums: S = sum_i r_i E_i over the unreduced residues, E_i
+ * the CRT idempotent of q_i, and the result S - k P formed modulo 2^64 with
+ * k the rounded estimate of S / P, or a neighbour of it when that leaves the
+ * symmetric range (four integer multiply-adds per prime and entry);
+ * everything else by balanced Garner.  Mode 1: CRT with a round-to-nearest
+ * quotient on balanced digits ("Accelerating Multiple-Precision LU
+ * Decomposition with Ozaki Scheme II") for the wide outputs (limbs, enclosures, intervals) where the plan can
  * keep P > 4 |result| (one more bit of headroom, so sometimes one more
  * prime), and for int64 where its planned primes already exceed 4 |result|;
  * Garner otherwise.  Mode 2: balanced Garner for every result.  On GB300

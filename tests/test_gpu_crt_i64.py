@@ -1,11 +1,13 @@
-"""The int64 path's three reconstructions.  Whenever its planned primes
-already exceed 4 |C| (the prime count for a bound one bit larger is no
-larger), it reconstructs by idempotent sums with a rounded quotient by
-default (mode 0 of rg_set_crt_mode, up to 12 primes), by round-to-nearest CRT
-on balanced digits in mode 1, and by balanced Garner otherwise and in mode 2.
-Operands at their extremes put |C| at its bound, where the rounded quotient
-has the least margin ("Accelerating Multiple-Precision LU Decomposition with
-Ozaki Scheme II", CRT by round-to-nearest; "exact-solve", balanced Garner)."""
+"""The int64 path's three reconstructions.  By default (mode 0 of
+rg_set_crt_mode) one-limb results of up to 12 primes are reconstructed by
+idempotent sums with a rounded quotient, with the neighbouring quotients tried
+when the result falls outside the symmetric range; mode 1 takes
+round-to-nearest CRT on balanced digits whenever the planned primes already
+exceed 4 |C| (the prime count for a bound one bit larger is no larger), and
+Garner otherwise; mode 2 takes balanced Garner.  Operands at their extremes
+put |C| at its bound, where the rounded quotient has the least margin
+("Accelerating Multiple-Precision LU Decomposition with Ozaki Scheme II", CRT
+by round-to-nearest; "exact-solve", balanced Garner)."""
 import numpy as np
 import pytest
 
@@ -72,7 +74,7 @@ def test_result_at_its_bound(rg, mode, sign, b, K):
     assert np.array_equal(C, want)
     mode(0)
     C0 = host(rg.res_gemm_i64(dev(A), dev(B)))
-    assert rg.get_plan()["crt_rn"] == (2 if headroom and P <= 12 else 0)
+    assert rg.get_plan()["crt_rn"] == 2
     assert np.array_equal(C0, want)
     mode(2)
     C2 = host(rg.res_gemm_i64(dev(A), dev(B)))
@@ -116,3 +118,24 @@ def test_idempotent_sums_every_prime_count(rg, mode, P):
     plan = rg.get_plan()
     assert plan["bound_bits"] == T and plan["crt_rn"] == 2
     assert np.array_equal(C, oracle.matmul_i64(A, B, lc=1)[:, :, 0])
+
+
+@pytest.mark.parametrize("P", [1, 2, 3, 5, 8])
+def test_idempotent_sums_with_the_callers_guarantee_only(rg, mode, P):
+    """A caller-fixed prime count below the a-priori bound: entries near 2^40 whose products cancel
+    to results anywhere in the symmetric range, up to +-(P - 1) / 2, where the rounded quotient
+    is as likely to be off by one as not and the range test picks the result."""
+    ps = rg.primes()
+    prod = 1
+    for q in ps[:P]:
+        prod *= q
+    h = (prod - 1) // 2
+    big = 2**40
+    vals = [h, -h, h - 1, -(h - 1), 0, 1, -1, h // 2, -(h // 3)]
+    A = np.array([[v + big, -big] for v in vals], dtype=np.int64)
+    B = np.array([[1], [1]], dtype=np.int64)  # C = v
+    mode(0)
+    C = host(rg.res_gemm_i64(dev(A), dev(B), nprimes=P))
+    assert rg.get_plan()["crt_rn"] == 2
+    assert np.array_equal(C, oracle.matmul_i64(A, B, lc=1)[:, :, 0])
+    assert np.array_equal(C[:, 0], np.array(vals, dtype=np.int64))
