@@ -532,7 +532,8 @@ def measure_e2e(rg, w, A, B, args, dev):
     dt = (time.perf_counter() - t0) / args.steps
     return {"value": 2.0 * w.macs / dt / 1e12, "unit": UNIT, "h2d_bytes_per_step": int(A.nbytes + B.nbytes),
             "d2h_bytes_per_step": int(d2h), "ms_per_step": dt * 1e3,
-            "api": "exact_modular_int8_gb300 call on pinned host tensors (C ABI with RG_FLAG_HOST)"}
+            "api": "exact_modular_int8_gb300 call on pinned host tensors (C ABI with RG_FLAG_HOST; large int64 "
+                   "products pipeline A's row blocks and C's over the link)"}
 
 
 def _time_events(torch, dev, fn, reps, flush=None):

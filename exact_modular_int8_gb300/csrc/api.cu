@@ -177,13 +177,131 @@ int finish(void* ws, cudaStream_t s, unsigned flags, int* host_word = nullptr) {
     if (e_ != cudaSuccess) return RG_ERR_CUDA; \
   } while (0)
 
+// ---------------------------------------------------------------------------
+// Host-buffer int64 products large enough for the CPU-GPU link to dominate:
+// A is copied in row blocks on a copy stream while the blocks already on the
+// device are split, multiplied and reconstructed on the call's stream, and
+// every block of C goes back on a second copy stream as soon as it is done
+// (copies in opposite directions share the link).  B is copied and split
+// once; each A block reuses one block-sized region of residue planes.
+// ---------------------------------------------------------------------------
+constexpr int kPipeMaxBlocks = 8;
+constexpr size_t kPipeMinBytes = size_t(32) << 20;  // operands and result; below this one block wins
+
+struct HostPipe {
+  std::mutex mu;  // one pipelined call per device at a time (the copy streams and events are shared)
+  bool ready = false;
+  cudaStream_t h2d = nullptr, d2h = nullptr;
+  cudaEvent_t start = nullptr, b = nullptr, done = nullptr, a[kPipeMaxBlocks] = {}, c[kPipeMaxBlocks] = {};
+};
+HostPipe g_pipe[64];
+std::mutex g_pipe_init_mu;
+
+// The copy streams and events of the current device, created on first use.
+HostPipe* host_pipe() {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return nullptr;
+  HostPipe& p = g_pipe[dev];
+  std::lock_guard<std::mutex> lk(g_pipe_init_mu);
+  if (!p.ready) {
+    const unsigned ef = cudaEventDisableTiming;
+    bool ok = cudaStreamCreateWithFlags(&p.h2d, cudaStreamNonBlocking) == cudaSuccess &&
+              cudaStreamCreateWithFlags(&p.d2h, cudaStreamNonBlocking) == cudaSuccess &&
+              cudaEventCreateWithFlags(&p.start, ef) == cudaSuccess &&
+              cudaEventCreateWithFlags(&p.b, ef) == cudaSuccess && cudaEventCreateWithFlags(&p.done, ef) == cudaSuccess;
+    for (int j = 0; ok && j < kPipeMaxBlocks; ++j)
+      ok = cudaEventCreateWithFlags(&p.a[j], ef) == cudaSuccess && cudaEventCreateWithFlags(&p.c[j], ef) == cudaSuccess;
+    if (!ok) return nullptr;  // the call fails; a later call retries the creation
+    p.ready = true;
+  }
+  return &p;
+}
+
+// Row blocks of a pipelined host-buffer int64 call: at least two, one per
+// 1024 rows up to kPipeMaxBlocks, whole 256-row pair tiles each; false when
+// the problem is too small to gain from the overlap.
+bool pipeline_shape(long long M, long long N, long long K, int* nb, long long* mb) {
+  const unsigned __int128 bytes = ((unsigned __int128)M * K + (unsigned __int128)K * N + (unsigned __int128)M * N) * 8;
+  if (M < 512 || bytes < kPipeMinBytes) return false;
+  long long n = M / 1024;
+  n = n < 2 ? 2 : (n > kPipeMaxBlocks ? kPipeMaxBlocks : n);
+  const long long rows = ((M + n - 1) / n + 255) / 256 * 256;
+  if (rows >= M) return false;
+  *mb = rows;
+  *nb = (int)((M + rows - 1) / rows);
+  return *nb >= 2 && *nb <= kPipeMaxBlocks;
+}
+
+// The pipelined host-buffer int64 call (see HostPipe); the workspace is the
+// host layout `L` (staging for A, B and C, residue planes for all M rows, of
+// which one block's rows are used).
+int run_i64_host_pipelined(const void* A, const void* B, void* C, long long M, long long N, long long K, int nprimes,
+                           unsigned flags, const Layout& L, uint8_t* w, cudaStream_t s, int nb, long long mb) {
+  HostPipe* hp = host_pipe();
+  if (!hp) return RG_ERR_CUDA;
+  std::lock_guard<std::mutex> lk(hp->mu);
+  const bool transb = (flags & RG_FLAG_TRANS_B) != 0;
+  DevPlan* plan = reinterpret_cast<DevPlan*>(w + L.plan);
+  int64_t* dA = reinterpret_cast<int64_t*>(w + L.a);
+  int64_t* dB = reinterpret_cast<int64_t*>(w + L.b);
+  int64_t* dC = reinterpret_cast<int64_t*>(w + L.c);
+  const int64_t* hA = static_cast<const int64_t*>(A);
+  int64_t* hC = static_cast<int64_t*>(C);
+  RG_TRY(upload_tables());
+  RG_TRY(cudaMemsetAsync(plan, 0, sizeof(DevPlan), s));
+  // the copies start once the call's stream has reached this call
+  RG_TRY(cudaEventRecord(hp->start, s));
+  RG_TRY(cudaStreamWaitEvent(hp->h2d, hp->start, 0));
+  RG_TRY(cudaStreamWaitEvent(hp->d2h, hp->start, 0));
+  RG_TRY(cudaMemcpyAsync(dB, B, (size_t)K * N * 8, cudaMemcpyHostToDevice, hp->h2d));
+  RG_TRY(cudaEventRecord(hp->b, hp->h2d));
+  for (int j = 0; j < nb; ++j) {
+    const long long m0 = j * mb, mj = M - m0 < mb ? M - m0 : mb;
+    RG_TRY(cudaMemcpyAsync(dA + m0 * K, hA + m0 * K, (size_t)mj * K * 8, cudaMemcpyHostToDevice, hp->h2d));
+    RG_TRY(cudaEventRecord(hp->a[j], hp->h2d));
+  }
+  RG_TRY(cudaStreamWaitEvent(s, hp->b, 0));
+  int fault = g_fault.exchange(0);
+  for (int j = 0; j < nb; ++j) {
+    const long long m0 = j * mb, mj = M - m0 < mb ? M - m0 : mb;
+    RG_TRY(cudaStreamWaitEvent(s, hp->a[j], 0));
+    // the first block's split also takes B (and max |B|); the GEMM of every
+    // block derives its prime count from the reductions so far, and Garner
+    // reads that count, so each block is exact on its own
+    RG_TRY(launch_split(RG_OP_I64, dA + m0 * K, nullptr, j == 0 ? dB : nullptr, nullptr, 1, 1, 1, mj, N, K, L.lda,
+                        L.ldb, w + L.ra, w + L.rb, plan, L.pmax, transb, s));
+    RG_TRY(launch_gemm(w + L.ra, L.lda, w + L.rb, L.ldb, w + L.rc, L.ldc, L.pmax, 1, nprimes, mj, N, K, plan, s,
+                       j == 0 ? fault : 0, g_wait_ns.load(), true, transb, L.splits));
+    RG_TRY(launch_garner(RG_OP_I64, w + L.rc, L.ldc, mj * L.ldc, mj * L.ldc, mj, N, K, 1, L.pmax, plan, dC + m0 * N,
+                         nullptr, s));
+    RG_TRY(cudaEventRecord(hp->c[j], s));
+  }
+  // results go back after all the work is enqueued (a copy into pageable
+  // memory returns only when it is done)
+  for (int j = 0; j < nb; ++j) {
+    const long long m0 = j * mb, mj = M - m0 < mb ? M - m0 : mb;
+    RG_TRY(cudaStreamWaitEvent(hp->d2h, hp->c[j], 0));
+    RG_TRY(cudaMemcpyAsync(hC + m0 * N, dC + m0 * N, (size_t)mj * N * 8, cudaMemcpyDeviceToHost, hp->d2h));
+  }
+  RG_TRY(cudaEventRecord(hp->done, hp->d2h));
+  RG_TRY(cudaStreamWaitEvent(s, hp->done, 0));
+  return finish(w, s, flags);
+}
+
+bool stage_events_on() {
+  std::lock_guard<std::mutex> lk(g_ev_mu);
+  return g_ev_on;
+}
+
 // Shared driver for every entry point; `batch` products of the same shape
 // share one plan (one prime count, one pair of scale exponents).  A2 and B2
 // are the radii of interval operands (null otherwise).  `status_host`, if
 // given, is the host int the final status read lands in (see finish()).
+// `pipeline`: large host-buffer int64 products may take the pipelined path
+// (which creates copy streams and events on first use).
 int run(int op, const void* A, const void* A2, int la, const void* B, const void* B2, int lb, void* C, void* C2,
         int lc, long long batch, long long M, long long N, long long K, int nprimes, unsigned flags, void* ws,
-        size_t ws_bytes, void* stream, int* status_host = nullptr) {
+        size_t ws_bytes, void* stream, int* status_host = nullptr, bool pipeline = true) {
   if (!ws || (reinterpret_cast<uintptr_t>(ws) & 255u) != 0) return RG_ERR_ARG;
   if (batch < 0 || M < 0 || N < 0 || K < 0 || nprimes < 0 || nprimes > kNumPrimes) return RG_ERR_ARG;
   // an empty problem reads no operand, and writes outputs only if it has entries
@@ -217,6 +335,12 @@ int run(int op, const void* A, const void* A2, int la, const void* B, const void
       }
     }
     return finish(ws, s, flags, status_host);
+  }
+  if (pipeline && op == RG_OP_I64 && batch == 1 && (flags & RG_FLAG_HOST) && !stage_events_on()) {
+    int nb = 0;
+    long long mb = 0;
+    if (pipeline_shape(M, N, K, &nb, &mb))
+      return run_i64_host_pipelined(A, B, C, M, N, K, nprimes, flags, L, w, s, nb, mb);
   }
   RG_TRY(upload_tables());
   const void* dA = A;
@@ -514,5 +638,5 @@ extern "C" int res_gemm_i64_noalloc(const int64_t* A, const int64_t* B, int64_t*
   // word of the other entry points is allocated on first use
   int status = 0;
   return run(RG_OP_I64, A, nullptr, 1, B, nullptr, 1, C, nullptr, 1, 1, M, N, K, nprimes,
-             flags, ws, kNoAllocScratchBytes, stream, &status);
+             flags, ws, kNoAllocScratchBytes, stream, &status, /*pipeline=*/false);
 }

@@ -1542,7 +1542,9 @@ cudaError_t launch_split(int op, const void* A, const void* A2, const void* B, c
   const int L = la > lb ? la : lb;
   if (op == RG_OP_I64) {
     constexpr int V = 8;
-    const SplitSide sa = make_side(A, ra, M, K, lda, 1, V), sb = make_side(B, rb, brows, bcols, ldb, 1, V);
+    const SplitSide sa = make_side(A, ra, M, K, lda, 1, V);
+    SplitSide sb = make_side(B, rb, brows, bcols, ldb, 1, V);
+    if (!B) sb.items = 0;  // A alone: B's residues are already in RB
     return launch_dependent(split_i64_kernel<V>, split_grid(sa.items + sb.items, kSplitI64BlocksPerSm), 256, 0, st, sa,
                             sb, plan, i64_planes);
   }

@@ -25,6 +25,8 @@ cudaError_t launch_plan(int op, const void* A, const void* A2, long long nA, int
 // transb: B is given transposed, [N][K], and RB becomes [pmax][N][ldb].
 // batch: A and B hold `batch` products back to back ([batch][M][K] and
 // [batch][K][N]); the residue planes become [pmax][batch][..][..].
+// int64 only: B == nullptr splits A alone (B's residues already in RB; max |B|
+// already in the plan).
 // Intervals (A2, B2 the radii): three planes per prime and operand,
 // RA [pmax][3][batch * M][lda] holding (Am, |Am|, Ar) and RB likewise
 // (Bm, Br, |Bm| + Br).

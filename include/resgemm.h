@@ -18,7 +18,12 @@
  *    little-endian 64-bit limbs, two's complement, signed top limb.
  *  - Pointers are device pointers, unless RG_FLAG_HOST is set; then A, B and
  *    the outputs are host pointers (pinned memory gives asynchronous
- *    copies) and the library stages them through the workspace.
+ *    copies) and the library stages them through the workspace.  A
+ *    single (unbatched) res_gemm_i64 call with at least 512 rows and 32 MiB
+ *    of operands and result moves A and C in row blocks on two copy streams
+ *    of its own (created on a device's first such call), overlapping the
+ *    link with the blocks' kernels; such calls on one device run one at a
+ *    time.
  *  - The caller owns every buffer, including the workspace `ws` of
  *    `ws_bytes` bytes (device memory, 256-byte aligned), sized by
  *    rg_workspace_bytes().  The product entry points allocate no device

@@ -86,3 +86,38 @@ def test_interval(rg):
     rlo, rhi = oracle.interval(A[0], A[1], B[0], B[1], rows=rows)
     assert np.array_equal(lo.numpy()[rows].view(np.uint64), rlo.view(np.uint64))
     assert np.array_equal(hi.numpy()[rows].view(np.uint64), rhi.view(np.uint64))
+
+
+@pytest.fixture(scope="module")
+def pipelined_case():
+    """2500 x 1000 x 3000 int64 (104 MB of operands and result): A goes over the link in two row
+    blocks of 1280 and 1220 rows.  The first block's entries are small and the second's full
+    24-bit, so the two blocks plan different prime counts (7 and 8)."""
+    M, N, K = 2500, 1000, 3000
+    A, B = int_matrices(M, N, K, -(2**23), 2**23, 63)
+    A[:1280] //= 2**13
+    return A, B, oracle.matmul_i64(A, B, lc=1)[:, :, 0]
+
+
+@pytest.mark.parametrize("pin,transb", [(True, False), (False, False), (True, True)])
+def test_int64_pipelined_row_blocks(rg, pipelined_case, pin, transb):
+    A, B, ref = pipelined_case
+    Bx = np.ascontiguousarray(B.T) if transb else B
+    out = torch.empty(ref.shape, dtype=torch.int64)
+    if pin:
+        out = out.pin_memory()
+    for _ in range(2):  # twice: the copy streams and events are reused
+        out.fill_(-1)
+        C = rg.res_gemm_i64(pinned(A, pin), pinned(Bx, pin), out=out, transb=transb)
+        assert np.array_equal(C.numpy(), ref)
+    assert rg.get_plan()["nprimes"] == 8
+
+
+def test_int64_pipelined_four_blocks_ragged(rg):
+    # 4100 rows: blocks of 1280, 1280, 1280 and 260 rows (36 MB)
+    M, N, K = 4100, 512, 512
+    A, B = int_matrices(M, N, K, -(2**23), 2**23, 64)
+    C = rg.res_gemm_i64(pinned(A, True), pinned(B, True))
+    assert np.array_equal(C.numpy(), host(rg.res_gemm_i64(dev(A), dev(B))))
+    rows = spread_rows(M)
+    assert np.array_equal(C.numpy()[rows], oracle.matmul_i64(A, B, lc=1, rows=rows)[:, :, 0])
