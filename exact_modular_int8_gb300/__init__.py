@@ -109,7 +109,7 @@ def library():
             vp, i64, ci, cu, sz = ctypes.c_void_p, ctypes.c_int64, ctypes.c_int, ctypes.c_uint, ctypes.c_size_t
             lib.res_gemm_i64.argtypes = [vp, vp, vp, i64, i64, i64, ci, cu, vp, sz, vp]
             lib.res_gemm_limbs.argtypes = [vp, ci, vp, ci, vp, ci, i64, i64, i64, ci, cu, vp, sz, vp]
-            lib.enclose_gemm_f64.argtypes = [vp, vp, vp, vp, i64, i64, i64, cu, vp, sz, vp]
+            lib.enclose_gemm_f64.argtypes = [vp, vp, vp, vp, i64, i64, i64, cu, ctypes.POINTER(ci), vp, sz, vp]
             lib.res_gemm_stage.argtypes = [vp, i64, vp, i64, vp, i64, ci, i64, i64, i64, cu, vp, sz, vp]
             lib.res_gemm_i64_batched.argtypes = [vp, vp, vp, i64, i64, i64, i64, ci, cu, vp, sz, vp]
             lib.res_gemm_limbs_batched.argtypes = [vp, ci, vp, ci, vp, ci, i64, i64, i64, i64, ci, cu, vp, sz, vp]

@@ -413,8 +413,20 @@ int res_gemm_limbs(const int64_t* A, int la, const int64_t* B, int lb, int64_t* 
 }
 
 int enclose_gemm_f64(const double* A, const double* B, double* lo, double* hi, int64_t M, int64_t N, int64_t K,
-                     unsigned flags, void* ws, size_t ws_bytes, void* stream) {
-  return run(RG_OP_ENCLOSE, A, nullptr, 1, B, nullptr, 1, lo, hi, 1, 1, M, N, K, 0, flags, ws, ws_bytes, stream);
+                     unsigned flags, int* info, void* ws, size_t ws_bytes, void* stream) {
+  if (info) flags |= RG_FLAG_SYNC;  // the regime is known once the call has run
+  const int rc = run(RG_OP_ENCLOSE, A, nullptr, 1, B, nullptr, 1, lo, hi, 1, 1, M, N, K, 0, flags, ws, ws_bytes, stream);
+  if (rc != RG_OK || !info) return rc;
+  int lossless = 1;
+  if (M && N && K) {  // an empty product is exactly zero: lossless
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    const DevPlan* plan = static_cast<const DevPlan*>(ws);
+    if (cudaMemcpyAsync(&lossless, &plan->lossless, sizeof(int), cudaMemcpyDeviceToHost, s) != cudaSuccess ||
+        cudaStreamSynchronize(s) != cudaSuccess)
+      return RG_ERR_CUDA;
+  }
+  *info = lossless ? 0 : 1;
+  return RG_OK;
 }
 
 int enclose_gemm_f32(const float* A, const float* B, float* lo, float* hi, int64_t M, int64_t N, int64_t K,

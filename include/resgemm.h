@@ -146,11 +146,15 @@ int res_gemm_limbs(const int64_t* A, int la, const int64_t* B, int lb, int64_t* 
  * K(2^bits_a + 2^bits_b) + K) bounding the induced error is added to S before
  * each endpoint is rounded outward: a valid, looser bracket, reported by
  * rg_get_plan() with lossless = 0 ("enclosure-gemm", Method).
+ * info: null, or a host int that receives the regime on success: 0 when both
+ * operands scaled exactly (the tightest bracket), 1 when they were coarsened
+ * (return_info's "regime" in "enclosure-gemm", Usage).  A non-null info
+ * implies RG_FLAG_SYNC.
  * Errors: RG_ERR_NONFINITE (an inf or nan entry), RG_ERR_RANGE (K > 2^17),
  * and the errors of res_gemm_i64.
  */
 int enclose_gemm_f64(const double* A, const double* B, double* lo, double* hi, int64_t M, int64_t N, int64_t K,
-                     unsigned flags, void* ws, size_t ws_bytes, void* stream);
+                     unsigned flags, int* info, void* ws, size_t ws_bytes, void* stream);
 
 /*
  * enclose_gemm_f64 for binary32 operands, with binary32 bounds: lo and hi are

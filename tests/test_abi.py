@@ -141,7 +141,7 @@ def test_argument_errors_need_no_device(rg):
     assert lib.res_gemm_limbs(p, 5, p, 1, p, 2, 2, 2, 2, 0, 0, wsp, 4096, None) == rg.RG_ERR_ARG
     assert lib.res_gemm_limbs(p, 1, p, 1, p, 7, 2, 2, 2, 0, 0, wsp, 4096, None) == rg.RG_ERR_ARG
     # enclosure needs both outputs
-    assert lib.enclose_gemm_f64(p, p, p, None, 2, 2, 2, 0, wsp, 4096, None) == rg.RG_ERR_ARG
+    assert lib.enclose_gemm_f64(p, p, p, None, 2, 2, 2, 0, None, wsp, 4096, None) == rg.RG_ERR_ARG
     # stage: leading dimensions and prime count
     assert lib.res_gemm_stage(p, 7, p, 64, p, 16, 1, 2, 2, 2, 0, wsp, 4096, None) == rg.RG_ERR_ARG
     assert lib.res_gemm_stage(p, 8, p, 64, p, 16, 0, 2, 2, 2, 0, wsp, 4096, None) == rg.RG_ERR_ARG

@@ -163,3 +163,25 @@ def test_return_info_reports_the_regime(rg):
     assert np.array_equal(host(lo)[0], rlo)
     lo, hi, info = rg.bmm_enclose(dev(narrow[None]), dev(B[None]), return_info=True)
     assert info["lossless"]
+
+
+def test_entry_point_reports_the_regime_in_info(rg):
+    """enclose_gemm_f64's info out-argument: 0 for a lossless scaling, 1 for a coarsened one; the bounds
+    equal the binding's (which reads the regime from the plan instead)."""
+    import ctypes
+
+    lib = rg.library()
+    B = np.ones((4, 1))
+    for A, want in ((np.array([[1e300, 1.0, -1e300, 2.0**-60]]), 1),
+                    (np.array([[2.0**100, 1.0, -(2.0**100), 3 * 2.0**-60]]), 0)):
+        dA, dB = dev(A), dev(B)
+        lo = torch.empty((1, 1), dtype=torch.float64, device="cuda")
+        hi = torch.empty_like(lo)
+        ws = rg.workspace(rg.workspace_bytes(rg.RG_OP_ENCLOSE, 1, 1, 4), torch.device("cuda", 0))
+        info = ctypes.c_int(-1)
+        rc = lib.enclose_gemm_f64(dA.data_ptr(), dB.data_ptr(), lo.data_ptr(), hi.data_ptr(), 1, 1, 4, 0,
+                                  ctypes.byref(info), ws.data_ptr(), ws.numel(),
+                                  torch.cuda.current_stream().cuda_stream)
+        assert rc == rg.RG_OK and info.value == want
+        rlo, rhi = rg.enclose_gemm_f64(dA, dB)
+        assert torch.equal(lo, rlo) and torch.equal(hi, rhi)
