@@ -315,7 +315,20 @@ int run(int op, const void* A, const void* A2, int la, const void* B, const void
   if (M > (1LL << 31) - 1 || N > (1LL << 31) - 1 || batch > (1LL << 31) - 1) return RG_ERR_ARG;
   Layout L;
   if (!make_layout(op, batch, M, N, K, la, lb, lc, nprimes, flags, &L)) return RG_ERR_ARG;
-  if (ws_bytes < L.total) return RG_ERR_WORKSPACE;
+  if (ws_bytes < L.total) {
+    // floating point: a smaller workspace holds planes for fewer primes, and
+    // the plan coarsens the scaling to fit them (reported as not lossless)
+    if (!is_enclose(op) || empty) return RG_ERR_WORKSPACE;
+    int p = L.pmax - 1;
+    for (; p >= 1; --p) {
+      Layout Lp;
+      if (make_layout(op, batch, M, N, K, la, lb, lc, p, flags, &Lp) && Lp.total <= ws_bytes) {
+        L = Lp;
+        break;
+      }
+    }
+    if (p < 1) return RG_ERR_WORKSPACE;
+  }
   const long long gemm_batch = batch * planes_per_product(op);
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   uint8_t* w = static_cast<uint8_t*>(ws);
@@ -375,7 +388,7 @@ int run(int op, const void* A, const void* A2, int la, const void* B, const void
   RG_TRY(record_stage(0, s));
   if (!i64)
     RG_TRY(launch_plan(op, dA, dA2, batch * M * K, la1, dB, dB2, batch * K * N, lb1, lc1, K,
-                       is_enclose(op) ? 0 : nprimes, plan, s));
+                       is_enclose(op) ? 0 : nprimes, L.pmax, plan, s));
   const bool transb = (flags & RG_FLAG_TRANS_B) != 0;
   RG_TRY(launch_split(op, dA, dA2, dB, dB2, la1, lb1, batch, M, N, K, L.lda, L.ldb, w + L.ra, w + L.rb, plan, L.pmax,
                       transb, s));

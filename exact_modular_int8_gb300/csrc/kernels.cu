@@ -115,6 +115,7 @@ struct PlanArgs {
   long long K;
   int nprimes_fixed, la, lb, lc;
   int allow_rn;  // the wide outputs may use round-to-nearest CRT
+  int pcap;      // floating point: the most primes the workspace's planes hold
 };
 
 struct LocalPlan {
@@ -165,10 +166,15 @@ __device__ LocalPlan finalize_plan(DevPlan* plan, const PlanArgs& a) {
     // finest binary point holding every entry exactly: |A * 2^f_a| < 2^bits_a
     const int bits_a0 = ea ? ea - mina + sig : 0, bits_b0 = eb ? eb - minb + sig : 0;
     // coarsened until each operand fits 256-bit two's complement and the
-    // product fits the residue range (enclosure-gemm, Method): the larger
-    // operand gives up bits first
+    // product fits the residue range (enclosure-gemm, Method), here the range
+    // of the primes the workspace holds: the larger operand gives up bits first
+    const int cap_bits = min(RG_MAX_BOUND_BITS, c_tab.log2P[a.pcap] - 1);
+    if (cap_bits - ck - extra < 2) {  // not one bit per operand
+      p.status = RG_ERR_WORKSPACE;
+      return p;
+    }
     int ba = min(bits_a0, 255), bb = min(bits_b0, 255);
-    int excess = ba + bb + ck + extra - RG_MAX_BOUND_BITS;
+    int excess = ba + bb + ck + extra - cap_bits;
     if (excess > 0) {
       const int d = min(excess, abs(ba - bb));
       if (ba >= bb) ba -= d; else bb -= d;
@@ -193,7 +199,7 @@ __device__ LocalPlan finalize_plan(DevPlan* plan, const PlanArgs& a) {
     // it, balanced Garner reconstructs from the usual prime count
     if (a.allow_rn) {
       const int prn = primes_for_bound(p.T + 1);
-      if (prn) {
+      if (prn && prn <= a.pcap) {  // within the workspace's planes
         p.P = prn;
         p.crt_rn = 1;
       }
@@ -1421,8 +1427,10 @@ static int planner_blocks(long long n) {
 }
 
 cudaError_t launch_plan(int op, const void* A, const void* A2, long long nA, int la, const void* B, const void* B2,
-                        long long nB, int lb, int lc, long long K, int nprimes_fixed, DevPlan* plan, cudaStream_t s) {
-  PlanArgs pa{op, K, nprimes_fixed, la, lb, lc, g_crt_mode.load() == 1 ? 1 : 0};
+                        long long nB, int lb, int lc, long long K, int nprimes_fixed, int pcap, DevPlan* plan,
+                        cudaStream_t s) {
+  if (pcap < 1 || pcap > kNumPrimes) return cudaErrorInvalidValue;
+  PlanArgs pa{op, K, nprimes_fixed, la, lb, lc, g_crt_mode.load() == 1 ? 1 : 0, pcap};
   if (nprimes_fixed) nA = nB = 0;  // only the finalisation is needed
   const int ba = planner_blocks(nA), bb = planner_blocks(nB);
   if (op == RG_OP_I64)

@@ -15,8 +15,12 @@ cudaError_t upload_tables();
 // first); the last block derives the prime count, chunk counts and
 // floating-point scales.  With nprimes_fixed > 0 only that derivation runs.
 // A2, B2: the radii of interval operands (same sizes as A, B), else null.
+// pcap: the most primes the workspace holds planes for; the floating-point
+// plans coarsen their scaling to fit them (RG_ERR_WORKSPACE if not one bit per
+// operand is left).
 cudaError_t launch_plan(int op, const void* A, const void* A2, long long nA, int la, const void* B, const void* B2,
-                        long long nB, int lb, int lc, long long K, int nprimes_fixed, DevPlan* plan, cudaStream_t s);
+                        long long nB, int lb, int lc, long long K, int nprimes_fixed, int pcap, DevPlan* plan,
+                        cudaStream_t s);
 
 // Residue split of A [M][K] into RA [pmax][M][lda] and of B [K][N] into
 // RB [pmax][K][ldb] (fp16 balanced residues), for the plan's prime count.

@@ -283,6 +283,17 @@ size_t rg_noalloc_scratch_bytes(void);
  * (primes x products x ceil(M / 128) x ceil(N / 256)); the entry points
  * return RG_ERR_ARG (RG_ERR_RANGE for K) for the same shapes.  An empty
  * problem needs the 4 KiB plan block only.
+ * The floating-point operations (RG_OP_ENCLOSE[_F32], RG_OP_INTERVAL[_F32])
+ * plan on the device, so with nprimes = 0 the size covers all 53 primes.
+ * Their entry points also accept a smaller workspace, down to the size this
+ * function gives for nprimes = 1: the call then uses the largest prime count
+ * p whose size (nprimes = p) fits, and the plan coarsens the scaling to fit p
+ * primes where it needs more (a valid, looser bracket; rg_get_plan reports
+ * lossless = 0).  A workspace sized for the prime count a first call reports
+ * (rg_get_plan's nprimes) gives later calls on operands of the same binary
+ * range the same bits, as the page's working-memory model P (MK + KN) has it
+ * ("enclosure-gemm", Requirements and limits).  When not one bit per operand
+ * is left the call fails with RG_ERR_WORKSPACE.
  */
 size_t rg_workspace_bytes(int op, int64_t M, int64_t N, int64_t K, int la, int lb, int lc, int nprimes,
                           unsigned flags);

@@ -185,3 +185,33 @@ def test_entry_point_reports_the_regime_in_info(rg):
         assert rc == rg.RG_OK and info.value == want
         rlo, rhi = rg.enclose_gemm_f64(dA, dB)
         assert torch.equal(lo, rlo) and torch.equal(hi, rhi)
+
+
+def test_smaller_workspace_caps_the_primes(rg):
+    """A workspace for fewer primes than the lossless plan needs gives a coarsened, valid bracket; one
+    sized for the count a first call reports gives the same bits as the full workspace."""
+    A, B = normal_matrices(64, 48, 256, 21)
+    dA, dB = dev(A), dev(B)
+    lo, hi = rg.enclose_gemm_f64(dA, dB)
+    full = rg.get_plan()
+    assert full["lossless"] == 1
+    P = full["nprimes"]
+    d0 = torch.device("cuda", 0)
+    exact = torch.empty(rg.workspace_bytes(rg.RG_OP_ENCLOSE, 64, 48, 256, nprimes=P), dtype=torch.uint8, device=d0)
+    lo2, hi2 = rg.enclose_gemm_f64(dA, dB, ws=exact)
+    assert torch.equal(lo2, lo) and torch.equal(hi2, hi)
+    assert rg.get_plan(ws=exact)["nprimes"] == P and rg.get_plan(ws=exact)["lossless"] == 1
+    small = torch.empty(rg.workspace_bytes(rg.RG_OP_ENCLOSE, 64, 48, 256, nprimes=P - 6), dtype=torch.uint8,
+                        device=d0)
+    lo3, hi3 = rg.enclose_gemm_f64(dA, dB, ws=small)
+    plan = rg.get_plan(ws=small)
+    assert plan["lossless"] == 0 and plan["nprimes"] <= P - 6
+    rlo, rhi = oracle.enclose_f64(A, B)
+    check_contains(host(lo3), host(hi3), rlo, rhi)
+    tiny = torch.empty(rg.workspace_bytes(rg.RG_OP_ENCLOSE, 64, 48, 256, nprimes=1), dtype=torch.uint8, device=d0)
+    with pytest.raises(rg.ResGemmError) as e:  # 7 bits of residue range cannot hold K = 256
+        rg.enclose_gemm_f64(dA, dB, ws=tiny)
+    assert e.value.code == rg.RG_ERR_WORKSPACE
+    with pytest.raises(rg.ResGemmError) as e:
+        rg.enclose_gemm_f64(dA, dB, ws=tiny[:4096])
+    assert e.value.code == rg.RG_ERR_WORKSPACE
