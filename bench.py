@@ -472,9 +472,12 @@ def main():
                    "l2": "flushed between timed steps (512 MiB write outside the timed events)"},
         "roofline": roofline,
         "stages_ms": stages_ms,
-        # our kernels per call: split, GEMM and Garner, the planner for every kind but int64, and the
-        # slice sum when the layout lets the GEMM split K
-        "gpu_launches": ((3 if w.kind == "int" else 4) + (1 if L.splits > 1 else 0)) * args.steps * world,
+        # our kernels per call: split, GEMM and reconstruction, the planner for every kind but int64, the
+        # int64 split's plane fix-up pass when its planes are large (16 MiB of A and B residues or more), and
+        # the slice sum when the layout lets the GEMM split K
+        "gpu_launches": ((3 if w.kind == "int" else 4) + (1 if L.splits > 1 else 0) +
+                         (1 if w.kind == "int" and not w.nprimes and (w.M + w.N) * w.K * 2 >= (16 << 20) else 0))
+        * args.steps * world,
         "clocks": clock_info,
     }
 

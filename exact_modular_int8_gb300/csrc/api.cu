@@ -18,6 +18,10 @@ namespace {
 using namespace rg;
 
 constexpr size_t kPlanBytes = 4096;
+// One residue plane of A and B (fp16) from which the int64 split writes the
+// previous call's plane count instead of the most an int64 product can need:
+// below it the saved writes are worth less than the fix-up pass's launch.
+constexpr size_t kPlaneHintMinBytes = size_t(16) << 20;
 constexpr size_t kAlign = 4096;
 
 std::atomic<unsigned long long> g_wait_ns{1000000000ull};
@@ -390,12 +394,18 @@ int run(int op, const void* A, const void* A2, int la, const void* B, const void
     RG_TRY(launch_plan(op, dA, dA2, batch * M * K, la1, dB, dB2, batch * K * N, lb1, lc1, K,
                        is_enclose(op) ? 0 : nprimes, L.pmax, plan, s));
   const bool transb = (flags & RG_FLAG_TRANS_B) != 0;
+  // planner-free int64 with large planes: the split writes as many planes as
+  // the previous call on this workspace used, and a fix-up pass adds any that
+  // this call needs beyond them (see kPlaneHintOffset)
+  uint32_t* plane_hint = reinterpret_cast<uint32_t*>(w + L.plan + kPlaneHintOffset);
+  const bool use_hint =
+      i64 && nprimes == 0 && (unsigned __int128)batch * (M + N) * K * 2 >= (unsigned __int128)kPlaneHintMinBytes;
   RG_TRY(launch_split(op, dA, dA2, dB, dB2, la1, lb1, batch, M, N, K, L.lda, L.ldb, w + L.ra, w + L.rb, plan, L.pmax,
-                      transb, s));
+                      transb, s, use_hint ? plane_hint : nullptr));
   int fault = g_fault.exchange(0);
   RG_TRY(record_stage(1, s));
   RG_TRY(launch_gemm(w + L.ra, L.lda, w + L.rb, L.ldb, w + L.rc, L.ldc, L.pmax, (int)gemm_batch, i64 ? nprimes : 0,
-                     M, N, K, plan, s, fault, g_wait_ns.load(), i64, transb, L.splits));
+                     M, N, K, plan, s, fault, g_wait_ns.load(), i64, transb, L.splits, i64 ? plane_hint : nullptr));
   // Garner sees the batch as batch * M rows of each plane; an interval's
   // three product planes lie batch * M rows apart
   const long long sub = batch * M * L.ldc;

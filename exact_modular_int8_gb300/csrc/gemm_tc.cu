@@ -74,6 +74,7 @@ struct GemmParams {
   int ceil_log2_k;
   int fault;
   unsigned long long wait_ns;
+  uint32_t* plane_hint;  // derive_i64: where to record the prime count for the next call's split (or null)
   float qf[kNumPrimes];
   float invq[kNumPrimes];
   int log2P[kNumPrimes + 1];  // floor(log2(q_0 ... q_{n-1}))
@@ -107,6 +108,7 @@ __device__ int launch_primes(const GemmParams& gp, DevPlan* plan) {
     plan->bits_b = bits_b;
     plan->bound_bits = T;
     if (range) atomicCAS(&plan->status, 0, RG_ERR_RANGE);
+    else if (gp.plane_hint && !gp.P_fixed) *gp.plane_hint = kPlaneHintTag | (uint32_t)P;
   }
   return range ? 0 : P;
 }
@@ -1114,7 +1116,7 @@ cudaError_t gemm_device(int dev, GemmDevice& out) {
 cudaError_t launch_gemm(const void* RA, long long lda, const void* RB, long long ldb, void* RC, long long ldc,
                         int pmax, int batch, int P_fixed, long long M, long long N, long long K, DevPlan* plan,
                         cudaStream_t st, int fault, unsigned long long wait_ns, bool derive_i64, bool b_kmajor,
-                        int max_splits) {
+                        int max_splits, uint32_t* plane_hint) {
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
@@ -1153,6 +1155,7 @@ cudaError_t launch_gemm(const void* RA, long long lda, const void* RB, long long
   while ((1LL << gp.ceil_log2_k) < K) ++gp.ceil_log2_k;
   gp.fault = fault;
   gp.wait_ns = wait_ns;
+  gp.plane_hint = derive_i64 ? plane_hint : nullptr;
   const Tables& t = host_tables();
   for (int i = 0; i < kNumPrimes; ++i) {
     gp.qf[i] = t.qf[i];

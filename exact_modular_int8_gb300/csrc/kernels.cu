@@ -522,8 +522,9 @@ __device__ __forceinline__ void store_residues(const float (&r)[VEC], __half* ds
 template <int VEC, int NW>
 __device__ __forceinline__ void emit_int_residues(const uint32_t (&wd)[VEC][NW], const bool (&neg)[VEC],
                                                   const float (&xf)[VEC], int nw, int P, const PrimeRec* rec,
-                                                  const int (*ws)[kMaxWords + 1], __half* y, long long plane) {
-  for (int p = 0; p < P; ++p) {
+                                                  const int (*ws)[kMaxWords + 1], __half* y, long long plane,
+                                                  int p0 = 0) {
+  for (int p = p0; p < P; ++p) {
     const PrimeRec& R = rec[p];
     const float q = R.q, iq = R.iq;
     float r[VEC];
@@ -647,13 +648,63 @@ __device__ __forceinline__ I64Item<VEC> load_i64_item(const SplitSide& sa, const
   return v;
 }
 
+// The residue-plane count a planner-free int64 split writes: `pmax`, or the
+// prime count the previous call on this workspace used (its GEMM records it,
+// tagged, in the plan block beyond the part each call clears) when that is
+// smaller.  A later fix-up pass writes whatever planes the call turns out to
+// need beyond it, so the count only saves writes and never decides a result.
+__device__ __forceinline__ int i64_planes_written(const uint32_t* hint, int pmax) {
+  if (!hint) return pmax;
+  const uint32_t h = __ldcg(hint);
+  const int p = (int)(h & 0xFFFFu);
+  return (h & 0xFFFF0000u) == kPlaneHintTag && p >= 1 && p < pmax ? p : pmax;
+}
+
+// Residues of the VEC int64 entries of `cur` (item `it`) for the primes
+// [p0, p1); the word count is decided per warp from the warp's largest |x|
+// (none when every |x| <= 2^23), m receives this item's largest |x|.
 template <int VEC>
-__global__ void __launch_bounds__(256) split_i64_kernel(SplitSide sa, SplitSide sb, DevPlan* plan, int P) {
+__device__ __forceinline__ void emit_i64_item(const SplitSide& sa, const SplitSide& sb, const I64Item<VEC>& cur,
+                                              long long it, long long total, int p0, int p1, const PrimeRec* rec,
+                                              const int (*ws)[kMaxWords + 1], unsigned long long& m, bool& isA) {
+  const bool valid = it < total;
+  isA = it < sa.items;
+  const SplitSide& s = isA ? sa : sb;
+  const long long item = isA ? it : it - sa.items;
+  const long long per_row = s.ldy / VEC;
+  const long long row = div_row(item, s.rd);
+  const long long col0 = (item - row * per_row) * VEC;
+  m = 0;
+#pragma unroll
+  for (int e = 0; e < VEC; ++e) m = max(m, abs_u64(cur.x[e]));
+  // words for the whole warp: none when every |x| <= 2^23, else the fewest
+  // holding every entry's two's complement
+  const int bits = __reduce_max_sync(0xffffffffu, (unsigned)bitlen64(m));
+  const int nw = (bits <= 23 || (bits == 24 && __all_sync(0xffffffffu, m <= (1ull << 23)))) ? 0
+                 : bits + 1 <= 32 ? 1 : 2;
+  if (!valid) return;
+  uint32_t wd[VEC][2];
+  bool neg[VEC];
+  float xf[VEC];
+#pragma unroll
+  for (int e = 0; e < VEC; ++e) {
+    neg[e] = (long long)cur.x[e] < 0;
+    xf[e] = (float)(int)(long long)cur.x[e];
+    wd[e][0] = (uint32_t)cur.x[e];
+    wd[e][1] = (uint32_t)(cur.x[e] >> 32);
+  }
+  emit_int_residues<VEC, 2>(wd, neg, xf, nw, p1, rec, ws, s.Y + row * s.ldy + col0, s.plane, p0);
+}
+
+template <int VEC>
+__global__ void __launch_bounds__(256) split_i64_kernel(SplitSide sa, SplitSide sb, DevPlan* plan, int P,
+                                                        const uint32_t* hint) {
   __shared__ PrimeRec rec[kNumPrimes];
   __shared__ int ws[kNumPrimes][kMaxWords + 1];
   load_prime_recs(rec, ws);
   __syncthreads();
   wait_for_predecessor();
+  const int planes = i64_planes_written(hint, P);
   const int lane = threadIdx.x & 31;
   const long long total = sa.items + sb.items;
   const long long stride = (long long)gridDim.x * blockDim.x;
@@ -666,42 +717,56 @@ __global__ void __launch_bounds__(256) split_i64_kernel(SplitSide sa, SplitSide 
   for (; base < total; base += stride) {
     const I64Item<VEC> cur = next;
     if (base + stride < total) next = load_i64_item<VEC>(sa, sb, base + stride + lane, total);
-    const long long it = base + lane;
-    const bool valid = it < total;
-    const bool isA = it < sa.items;
-    const SplitSide& s = isA ? sa : sb;
-    const long long item = isA ? it : it - sa.items;
-    const long long per_row = s.ldy / VEC;
-    const long long row = div_row(item, s.rd);
-    const long long col0 = (item - row * per_row) * VEC;
-    unsigned long long m = 0;
-#pragma unroll
-    for (int e = 0; e < VEC; ++e) m = max(m, abs_u64(cur.x[e]));
+    unsigned long long m;
+    bool isA;
+    emit_i64_item<VEC>(sa, sb, cur, base + lane, total, 0, planes, rec, ws, m, isA);
     if (isA) max_a = max(max_a, m);
     else max_b = max(max_b, m);
-    // words for the whole warp: none when every |x| <= 2^23, else the fewest
-    // holding every entry's two's complement
-    const int bits = __reduce_max_sync(0xffffffffu, (unsigned)bitlen64(m));
-    const int nw = (bits <= 23 || (bits == 24 && __all_sync(0xffffffffu, m <= (1ull << 23)))) ? 0
-                   : bits + 1 <= 32 ? 1 : 2;
-    if (!valid) continue;
-    uint32_t wd[VEC][2];
-    bool neg[VEC];
-    float xf[VEC];
-#pragma unroll
-    for (int e = 0; e < VEC; ++e) {
-      neg[e] = (long long)cur.x[e] < 0;
-      xf[e] = (float)(int)(long long)cur.x[e];
-      wd[e][0] = (uint32_t)cur.x[e];
-      wd[e][1] = (uint32_t)(cur.x[e] >> 32);
-    }
-    emit_int_residues<VEC, 2>(wd, neg, xf, nw, P, rec, ws, s.Y + row * s.ldy + col0, s.plane);
   }
   max_a = block_max_u64(max_a);
   max_b = block_max_u64(max_b);
   if (threadIdx.x == 0) {
     if (max_a) atomicMax(&plan->maxmag_a, max_a);
     if (max_b) atomicMax(&plan->maxmag_b, max_b);
+  }
+  allow_dependents();
+}
+
+// After a split that wrote fewer than pmax planes: derives the call's prime
+// count from the split's reductions, as the GEMM will (fewest primes with
+// product > 2^(T+1), T = bits(max|A|) + bits(max|B|) + ceil(log2 K), within
+// the int64 range), and writes the planes from the split's count up to it.
+// Returns at once when the split's planes suffice, or when the range check
+// fails (the GEMM records the error).
+template <int VEC>
+__global__ void __launch_bounds__(256) split_i64_fixup_kernel(SplitSide sa, SplitSide sb, DevPlan* plan, int pmax,
+                                                              const uint32_t* hint, long long K, int ceil_log2_k) {
+  __shared__ PrimeRec rec[kNumPrimes];
+  __shared__ int ws[kNumPrimes][kMaxWords + 1];
+  wait_for_predecessor();
+  if (plan->status) return;
+  const int planes = i64_planes_written(hint, pmax);
+  const unsigned long long ma = __ldcg(&plan->maxmag_a), mb = __ldcg(&plan->maxmag_b);
+  const int T = bitlen64(ma) + bitlen64(mb) + ceil_log2_k;
+  const unsigned long long ab = ma * mb;
+  if (__umul64hi(ma, mb) != 0 || __umul64hi(ab, (unsigned long long)K) != 0 ||
+      ab * (unsigned long long)K > 0x7FFFFFFFFFFFFFFFull)
+    return;
+  const int P = min(primes_for_bound(T), pmax);
+  if (P <= planes) {  // the usual case: every block leaves at once (the decision is the same in all)
+    allow_dependents();
+    return;
+  }
+  load_prime_recs(rec, ws);
+  __syncthreads();
+  const int lane = threadIdx.x & 31;
+  const long long total = sa.items + sb.items;
+  const long long stride = (long long)gridDim.x * blockDim.x;
+  for (long long base = (long long)blockIdx.x * blockDim.x + (threadIdx.x & ~31); base < total; base += stride) {
+    const I64Item<VEC> cur = load_i64_item<VEC>(sa, sb, base + lane, total);
+    unsigned long long m;
+    bool isA;
+    emit_i64_item<VEC>(sa, sb, cur, base + lane, total, planes, P, rec, ws, m, isA);
   }
   allow_dependents();
 }
@@ -1517,7 +1582,8 @@ static cudaError_t allow_wsh_smem() {
 
 cudaError_t launch_split(int op, const void* A, const void* A2, const void* B, const void* B2, int la, int lb,
                          long long batch, long long Mb, long long N, long long K, long long lda, long long ldb,
-                         void* RA, void* RB, DevPlan* plan, int i64_planes, bool transb, cudaStream_t st) {
+                         void* RA, void* RB, DevPlan* plan, int i64_planes, bool transb, cudaStream_t st,
+                         const uint32_t* plane_hint) {
   __half* ra = static_cast<__half*>(RA);
   __half* rb = static_cast<__half*>(RB);
   // The products of a batch lie back to back, so each side is one matrix of
@@ -1553,8 +1619,13 @@ cudaError_t launch_split(int op, const void* A, const void* A2, const void* B, c
     const SplitSide sa = make_side(A, ra, M, K, lda, 1, V);
     SplitSide sb = make_side(B, rb, brows, bcols, ldb, 1, V);
     if (!B) sb.items = 0;  // A alone: B's residues are already in RB
-    return launch_dependent(split_i64_kernel<V>, split_grid(sa.items + sb.items, kSplitI64BlocksPerSm), 256, 0, st, sa,
-                            sb, plan, i64_planes);
+    const unsigned grid = split_grid(sa.items + sb.items, kSplitI64BlocksPerSm);
+    cudaError_t e = launch_dependent(split_i64_kernel<V>, grid, 256, 0, st, sa, sb, plan, i64_planes, plane_hint);
+    if (e != cudaSuccess || !plane_hint) return e;
+    int ck = 0;
+    while ((1LL << ck) < K) ++ck;
+    return launch_dependent(split_i64_fixup_kernel<V>, grid, 256, 0, st, sa, sb, plan, i64_planes,
+                            (const uint32_t*)plane_hint, K, ck);
   }
   if (L <= 1) {
     constexpr int V = 8;

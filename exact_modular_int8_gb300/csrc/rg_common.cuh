@@ -47,6 +47,14 @@ struct DevPlan {
 };
 static_assert(sizeof(DevPlan) <= 256, "plan block");
 
+// A word of the workspace's plan block beyond the DevPlan that each call
+// clears: the planner-free int64 path's GEMM records there the prime count
+// it used (tagged), and the next call's split writes only that many residue
+// planes when it is below the most an int64 product can need (a fix-up pass
+// adds any planes the call then needs).
+constexpr size_t kPlaneHintOffset = 256;
+constexpr uint32_t kPlaneHintTag = 0x52470000u;
+
 // Constant tables for the split and Garner kernels, computed on the host once.
 struct Tables {
   int q[kNumPrimes];                          // q_0 = 251 > q_1 > ... > q_52 = 3

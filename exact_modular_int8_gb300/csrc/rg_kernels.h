@@ -34,9 +34,13 @@ cudaError_t launch_plan(int op, const void* A, const void* A2, long long nA, int
 // Intervals (A2, B2 the radii): three planes per prime and operand,
 // RA [pmax][3][batch * M][lda] holding (Am, |Am|, Ar) and RB likewise
 // (Bm, Br, |Bm| + Br).
+// plane_hint (int64 only, may be null): the workspace's plane-count word; the
+// split then writes only as many planes as the previous call used and a
+// fix-up pass adds the planes this call needs beyond them.
 cudaError_t launch_split(int op, const void* A, const void* A2, const void* B, const void* B2, int la, int lb,
                          long long batch, long long M, long long N, long long K, long long lda, long long ldb,
-                         void* RA, void* RB, DevPlan* plan, int i64_planes, bool transb, cudaStream_t st);
+                         void* RA, void* RB, DevPlan* plan, int i64_planes, bool transb, cudaStream_t st,
+                         const uint32_t* plane_hint = nullptr);
 
 // Per-prime tensor-core product RC[p] = RA[p] * RB[p] mod q_p (uint8).
 // derive_i64: the prime count is derived here from max |A|, max |B| (or
@@ -50,8 +54,10 @@ cudaError_t launch_split(int op, const void* A, const void* A2, const void* B, c
 cudaError_t launch_gemm(const void* RA, long long lda, const void* RB, long long ldb, void* RC, long long ldc,
                         int pmax, int batch, int P_fixed, long long M, long long N, long long K, DevPlan* plan,
                         cudaStream_t st, int fault, unsigned long long wait_ns, bool derive_i64, bool b_kmajor,
-                        int max_splits);
+                        int max_splits, uint32_t* plane_hint = nullptr);
 
+// plane_hint (derive_i64 only, may be null): receives the prime count used,
+// tagged, for the next call's split.
 // K slices worth room in RC for a product of this shape (1: never split).
 constexpr int kMaxSplits = 16;
 int gemm_max_splits(long long gemm_batch, long long M, long long N, long long K);

@@ -287,3 +287,39 @@ def test_concurrent_first_calls_from_host_threads(rg):
     r = subprocess.run([sys.executable, "-c", _CONCURRENT, root], capture_output=True, text=True, timeout=600,
                        cwd=root)
     assert r.returncode == 0 and "concurrent ok" in r.stdout, r.stdout[-2000:] + r.stderr[-2000:]
+
+
+def test_plane_count_hint_and_fixup(rg):
+    """Large planner-free int64 calls write as many residue planes as the previous call on the same
+    workspace used (a tagged word in the plan block), and a fix-up pass adds the planes a call needs
+    beyond them; so every sequence of calls stays exact, whatever the word holds."""
+    M = N = K = 2048  # (M + N) K fp16 residues: 16 MiB per plane, the size from which the count is reused
+    A24, B24 = int_matrices(M, N, K, -(2**23), 2**23, 31)
+    A8, B8 = int_matrices(M, N, K, -128, 128, 32)
+    ref24 = oracle.matmul_i64(A24, B24, lc=1)[:, :, 0]
+    ref8 = oracle.matmul_i64(A8, B8, lc=1)[:, :, 0]
+    ws = torch.empty(rg.workspace_bytes(rg.RG_OP_I64, M, N, K), dtype=torch.uint8, device="cuda")
+    word = ws[256:260].view(torch.int32)
+    tag = 0x52470000
+    # a word claiming one plane: the split writes one, the fix-up the other seven
+    word.fill_(tag | 1)
+    C = host(rg.res_gemm_i64(dev(A24), dev(B24), ws=ws))
+    assert np.array_equal(C, ref24)
+    assert rg.get_plan(ws=ws)["nprimes"] == 8 and int(word.item()) == tag | 8
+    # fewer primes next: the split writes 8 planes, of which the call uses 4
+    C = host(rg.res_gemm_i64(dev(A8), dev(B8), ws=ws))
+    assert np.array_equal(C, ref8)
+    P8 = rg.get_plan(ws=ws)["nprimes"]
+    assert P8 < 8 and int(word.item()) == tag | P8
+    # more primes again: the fix-up adds planes P8..7
+    C = host(rg.res_gemm_i64(dev(A24), dev(B24), ws=ws))
+    assert np.array_equal(C, ref24) and int(word.item()) == tag | 8
+    # a garbage word is ignored (all nine planes), and so is a count outside 1..8
+    for w in (0x12345678, tag | 0, tag | 9, tag | 40):
+        word.fill_(w)
+        C = host(rg.res_gemm_i64(dev(A24), dev(B24), ws=ws))
+        assert np.array_equal(C, ref24)
+    # a caller-fixed prime count neither reads nor writes the word
+    word.fill_(tag | 2)
+    C = host(rg.res_gemm_i64(dev(A8), dev(B8), nprimes=6, ws=ws))
+    assert np.array_equal(C, ref8) and int(word.item()) == tag | 2
