@@ -59,7 +59,7 @@ EXPORTED = (
     "rg_workspace_layout_batched", "enclose_gemm_f32", "enclose_gemm_f32_batched", "interval_gemm_f64",
     "interval_gemm_f32", "interval_gemm_f64_batched", "interval_gemm_f32_batched", "rg_solve_i64",
     "rg_solution_free", "rg_rational_reconstruct", "rg_big_gcd", "rg_set_crt_mode", "rg_set_stage_events",
-    "rg_probe_mma_rate",
+    "rg_probe_mma_rate", "rg_big_mulmod",
 )
 
 
@@ -158,6 +158,8 @@ def library():
             lib.rg_rational_reconstruct.restype = ci
             lib.rg_big_gcd.argtypes = [vp, ci, vp, ci, vp, ci]
             lib.rg_big_gcd.restype = ci
+            lib.rg_big_mulmod.argtypes = [vp, ci, vp, ci, vp, ci, vp, ci]
+            lib.rg_big_mulmod.restype = ci
             lib.rg_set_stage_events.argtypes = [ctypes.POINTER(ctypes.c_void_p), ci]
             lib.rg_set_stage_events.restype = ci
             lib.rg_probe_mma_rate.argtypes = [ci, ci, ci, vp, sz, vp, ctypes.POINTER(ctypes.c_double)]
@@ -661,6 +663,16 @@ def big_gcd(a: int, b: int) -> int:
     G = (ctypes.c_uint64 * gl)()
     _check(library().rg_big_gcd(A, al, B, bl, G, gl), "rg_big_gcd")
     return sum(int(G[i]) << (64 * i) for i in range(gl))
+
+
+def big_mulmod(a: int, b: int, m: int) -> int:
+    """(a b) mod m for naturals a, b < m by the library's host big-integer code (the solve's numerators use it)."""
+    n = max(1, (m.bit_length() + 63) // 64)
+    mask = (1 << 64) - 1
+    limbs = lambda x: (ctypes.c_uint64 * n)(*[(x >> (64 * i)) & mask for i in range(n)])  # noqa: E731
+    R = (ctypes.c_uint64 * n)()
+    _check(library().rg_big_mulmod(limbs(a), n, limbs(b), n, limbs(m), n, R, n), "rg_big_mulmod")
+    return sum(int(R[i]) << (64 * i) for i in range(n))
 
 
 def rational_reconstruct(x: int, m: int, nbits: int, dbits: int):

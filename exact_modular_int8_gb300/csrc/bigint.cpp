@@ -332,6 +332,180 @@ void reduce(const Reducer& R, const Limb* a, size_t na, std::vector<Limb>& un, N
   trim(*r);
 }
 
+namespace {
+
+// out[0 .. na + nb) = a * b, schoolbook (out need not be cleared).
+void school_mul(const Limb* a, size_t na, const Limb* b, size_t nb, Limb* out) {
+  std::fill(out, out + na + nb, Limb(0));
+  for (size_t i = 0; i < na; ++i) {
+    Limb carry = 0;
+    const Limb ai = a[i];
+    Limb* o = out + i;
+    for (size_t j = 0; j < nb; ++j) {
+      const u128 t = (u128)ai * b[j] + o[j] + carry;
+      o[j] = (Limb)t;
+      carry = (Limb)(t >> 64);
+    }
+    o[nb] = carry;
+  }
+}
+
+// r[0 .. n) += a[0 .. na) (na <= n); returns the carry out of r[n - 1].
+Limb add_to(Limb* r, size_t n, const Limb* a, size_t na) {
+  Limb carry = 0;
+  size_t i = 0;
+  for (; i < na; ++i) {
+    const u128 t = (u128)r[i] + a[i] + carry;
+    r[i] = (Limb)t;
+    carry = (Limb)(t >> 64);
+  }
+  for (; carry && i < n; ++i) {
+    const u128 t = (u128)r[i] + carry;
+    r[i] = (Limb)t;
+    carry = (Limb)(t >> 64);
+  }
+  return carry;
+}
+
+// r[0 .. n) -= a[0 .. na) (na <= n); returns the borrow out of r[n - 1].
+Limb sub_from(Limb* r, size_t n, const Limb* a, size_t na) {
+  Limb borrow = 0;
+  size_t i = 0;
+  for (; i < na; ++i) {
+    const Limb x = r[i], y = a[i];
+    const Limb d = x - y - borrow;
+    borrow = (x < y || (x == y && borrow)) ? 1 : 0;
+    r[i] = d;
+  }
+  for (; borrow && i < n; ++i) {
+    borrow = r[i] == 0 ? 1 : 0;
+    r[i] -= 1;
+  }
+  return borrow;
+}
+
+// out[0 .. na + nb) = a * b with na >= nb (Karatsuba on halves of the longer
+// factor when both are long; the longer split into nb-limb pieces when the
+// factors are far apart in length).
+void kmul(const Limb* a, size_t na, const Limb* b, size_t nb, Limb* out) {
+  if (na < nb) {
+    std::swap(a, b);
+    std::swap(na, nb);
+  }
+  if (nb < kKaratsubaLimbs) {
+    school_mul(a, na, b, nb, out);
+    return;
+  }
+  if (na >= 2 * nb) {  // pieces of nb limbs of a, each a balanced product
+    std::fill(out, out + na + nb, Limb(0));
+    std::vector<Limb> piece(2 * nb);
+    for (size_t off = 0; off < na; off += nb) {
+      const size_t len = std::min(nb, na - off);
+      kmul(a + off, len, b, nb, piece.data());
+      add_to(out + off, na + nb - off, piece.data(), len + nb);
+    }
+    return;
+  }
+  // a = a0 + a1 B^h, b = b0 + b1 B^h, h = ceil(na / 2) (so nb > h as na < 2 nb)
+  const size_t h = (na + 1) / 2, na1 = na - h, nb1 = nb - h;
+  // z0 = a0 b0 in out[0 .. 2h), z2 = a1 b1 in out[2h .. na + nb)
+  kmul(a, h, b, h, out);
+  kmul(a + h, na1, b + h, nb1, out + 2 * h);
+  // sa = a0 + a1, sb = b0 + b1 (h + 1 limbs each), z1 = sa sb - z0 - z2
+  std::vector<Limb> sa(h + 1, 0), sb(h + 1, 0), z1(2 * h + 2);
+  std::copy(a, a + h, sa.begin());
+  sa[h] = add_to(sa.data(), h, a + h, na1);
+  std::copy(b, b + h, sb.begin());
+  sb[h] = add_to(sb.data(), h, b + h, nb1);
+  kmul(sa.data(), h + 1, sb.data(), h + 1, z1.data());
+  sub_from(z1.data(), 2 * h + 2, out, 2 * h);
+  sub_from(z1.data(), 2 * h + 2, out + 2 * h, na1 + nb1);
+  size_t nz1 = 2 * h + 2;
+  while (nz1 > 0 && z1[nz1 - 1] == 0) --nz1;
+  add_to(out + h, na + nb - h, z1.data(), nz1);
+}
+
+}  // namespace
+
+void kmul_into(const Limb* a, size_t na, const Limb* b, size_t nb, std::vector<Limb>& out) {
+  out.assign(na + nb, 0);
+  if (!na || !nb) return;
+  kmul(a, na, b, nb, out.data());
+}
+
+void radix_value(const Limb* z, size_t cnt, size_t pl, const std::vector<Nat>& pw, std::vector<Limb>& out) {
+  if (cnt <= 16) {
+    out.clear();
+    std::vector<Limb> scratch;
+    for (size_t i = cnt; i-- > 0;) mul_add_into(out, pw[0].v.data(), pw[0].v.size(), z + i * pl, pl, scratch);
+    return;
+  }
+  size_t h = 1, k = 0;
+  while (2 * h < cnt) {
+    h *= 2;
+    ++k;
+  }
+  std::vector<Limb> lo, hi;
+  radix_value(z, h, pl, pw, lo);
+  radix_value(z + h * pl, cnt - h, pl, pw, hi);
+  size_t nh = hi.size(), nl = lo.size();
+  while (nh > 0 && hi[nh - 1] == 0) --nh;
+  while (nl > 0 && lo[nl - 1] == 0) --nl;
+  if (nh == 0) {
+    out.assign(lo.begin(), lo.begin() + nl);
+    return;
+  }
+  kmul_into(hi.data(), nh, pw[k].v.data(), pw[k].v.size(), out);
+  if (out.size() < nl + 1) out.resize(nl + 1, 0);
+  out.push_back(0);
+  add_to(out.data(), out.size(), lo.data(), nl);
+}
+
+Barrett make_barrett(const Nat& M) {
+  Barrett R;
+  R.M = M;
+  R.n = M.v.size();
+  Nat b2n;
+  b2n.v.assign(2 * R.n + 1, 0);
+  b2n.v[2 * R.n] = 1;
+  divmod(b2n, M, &R.mu, nullptr);
+  return R;
+}
+
+bool reduce_barrett(const Barrett& R, const Limb* a, size_t na, std::vector<Limb>& s1, std::vector<Limb>& s2,
+                    Nat* r) {
+  while (na > 0 && a[na - 1] == 0) --na;
+  const size_t n = R.n;
+  if (na > 2 * n) return false;
+  if (na < n) {
+    r->v.assign(a, a + na);
+    return true;
+  }
+  // q3 = floor(floor(a / B^(n-1)) mu / B^(n+1))
+  kmul_into(a + (n - 1), na - (n - 1), R.mu.v.data(), R.mu.v.size(), s1);
+  const size_t q3 = s1.size() > n + 1 ? s1.size() - (n + 1) : 0;
+  // r = (a - q3 M) mod B^(n+1)
+  if (q3)
+    kmul_into(s1.data() + (n + 1), q3, R.M.v.data(), n, s2);
+  else
+    s2.clear();
+  std::vector<Limb> rr(a, a + std::min(na, n + 1));
+  rr.resize(n + 1, 0);
+  sub_from(rr.data(), n + 1, s2.data(), std::min(s2.size(), n + 1));  // a borrow out of limb n is the wrap mod B^(n+1)
+  // at most two more subtractions of M
+  auto ge_m = [&]() {
+    if (rr[n] != 0) return true;
+    for (size_t i = n; i-- > 0;)
+      if (rr[i] != R.M.v[i]) return rr[i] > R.M.v[i];
+    return true;
+  };
+  for (int k = 0; k < 3 && ge_m(); ++k) sub_from(rr.data(), n + 1, R.M.v.data(), n);
+  if (ge_m()) return false;  // cannot happen for a < B^(2n)
+  r->v.assign(rr.begin(), rr.begin() + n);
+  trim(*r);
+  return true;
+}
+
 void mul_add_into(std::vector<Limb>& acc, const Limb* m, size_t nm, const Limb* z, size_t nz,
                   std::vector<Limb>& scratch) {
   size_t na = acc.size();

@@ -56,6 +56,30 @@ Reducer make_reducer(const Nat& M);
 void mul_into(const Limb* a, size_t na, const Limb* b, size_t nb, std::vector<Limb>& out);
 // r = a mod R.M for a given as na limbs; un is scratch.
 void reduce(const Reducer& R, const Limb* a, size_t na, std::vector<Limb>& un, Nat* r);
+// out = a * b by Karatsuba's method above kKaratsubaLimbs limbs per factor
+// (schoolbook below), out of length na + nb, not trimmed.
+constexpr size_t kKaratsubaLimbs = 32;
+void kmul_into(const Limb* a, size_t na, const Limb* b, size_t nb, std::vector<Limb>& out);
+
+// Repeated reduction modulo one fixed M > 0 by Barrett's method: with n the
+// limbs of M and mu = floor(B^(2n) / M) (B = 2^64), the quotient of any
+// x < B^(2n) is floor(floor(x / B^(n-1)) mu / B^(n+1)) minus at most 2, so
+// the remainder takes two products and at most two subtractions.
+struct Barrett {
+  Nat M;
+  Nat mu;
+  size_t n = 0;
+};
+Barrett make_barrett(const Nat& M);
+// r = a mod R.M for a of na limbs, a < B^(2n) (else false); s1, s2 are scratch.
+bool reduce_barrett(const Barrett& R, const Limb* a, size_t na, std::vector<Limb>& s1, std::vector<Limb>& s2, Nat* r);
+
+// out = sum_{i < cnt} z_i R^i for digits z_i of pl limbs each (z = cnt x pl
+// limbs) and R = pw[0], with pw[k] = R^(2^k) for every 2^k < cnt: the lower
+// and upper halves (at the largest power of two below cnt) recursively, then
+// one Karatsuba product by a power of R; Horner's rule below 16 digits.
+void radix_value(const Limb* z, size_t cnt, size_t pl, const std::vector<Nat>& pw, std::vector<Limb>& out);
+
 // acc = acc * m + z in place (m and z as limb arrays; acc grows as needed).
 void mul_add_into(std::vector<Limb>& acc, const Limb* m, size_t nm, const Limb* z, size_t nz,
                   std::vector<Limb>& scratch);

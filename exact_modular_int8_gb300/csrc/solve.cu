@@ -594,11 +594,13 @@ extern "C" int rg_solve_i64(const int64_t* A_in, const int64_t* B_in, int64_t n6
   const size_t pl = Pn.v.size();  // limbs of P (<= 6)
   // X_k = sum_i x_i P^i mod P^m, from the balanced digits normalised to
   // [0, P) by borrow propagation (a final borrow is a multiple of P^m), then
-  // Horner's rule on naturals, allocation-free per component.
+  // converted by halves with the powers P^(2^j) (big::radix_value).
   struct Scratch {
     std::vector<big::Limb> acc, tmp, un, prod;
     std::vector<big::Limb> z;  // normalised digits, m x pl limbs
   };
+  std::vector<big::Nat> pw(1, Pn);  // P^(2^j) for every 2^j below the step count
+  while (((size_t)1 << pw.size()) < (size_t)steps) pw.push_back(big::mul(pw.back(), pw.back()));
   auto value_of = [&](long long k, Scratch& S) {
     S.z.assign((size_t)steps * pl, 0);
     int borrow = 0;
@@ -609,14 +611,13 @@ extern "C" int rg_solve_i64(const int64_t* A_in, const int64_t* B_in, int64_t n6
       const big::Nat zi = x.neg ? big::sub(Pn, x.mag) : x.mag;
       std::copy(zi.v.begin(), zi.v.end(), S.z.begin() + (size_t)i * pl);
     }
-    S.acc.clear();
-    for (int i = steps - 1; i >= 0; --i) big::mul_add_into(S.acc, Pn.v.data(), pl, &S.z[(size_t)i * pl], pl, S.tmp);
+    big::radix_value(S.z.data(), (size_t)steps, pl, pw, S.acc);
     big::Nat X;
     X.v = S.acc;
     big::trim(X);
     return X;
   };
-  const big::Reducer red = big::make_reducer(Pm);
+  const big::Barrett bar = big::make_barrett(Pm);
   std::vector<big::Nat> Xv(comps);
   const int nthreads = std::max(1, std::min((int)std::thread::hardware_concurrency(), 64));
   std::vector<Scratch> scratch(nthreads + 4);
@@ -671,9 +672,13 @@ extern "C" int rg_solve_i64(const int64_t* A_in, const int64_t* B_in, int64_t n6
   std::vector<big::Int> Nv(comps);
   std::vector<char> fits(comps, 0);
   auto numerator = [&](long long k, Scratch& S) {
-    big::mul_into(D.v.data(), D.v.size(), Xv[k].v.data(), Xv[k].v.size(), S.prod);
+    // D X_k < (P^m)^2: a Karatsuba product, then Barrett's reduction modulo P^m
+    big::kmul_into(D.v.data(), D.v.size(), Xv[k].v.data(), Xv[k].v.size(), S.prod);
     big::Nat y;
-    big::reduce(red, S.prod.data(), S.prod.size(), S.un, &y);
+    if (!big::reduce_barrett(bar, S.prod.data(), S.prod.size(), S.un, S.tmp, &y)) {
+      fits[k] = 0;  // not reached: D <= dbound < P^m and X_k < P^m
+      return;
+    }
     big::Int v;
     if (big::cmp(y, half) > 0) {
       v.mag = big::sub(Pm, y);
@@ -739,6 +744,27 @@ extern "C" int rg_rational_reconstruct(const int64_t* x, int xl, const int64_t* 
   big::Int Di;
   Di.mag = D;
   if (!big::to_limbs(N, num, limbs) || !big::to_limbs(Di, den, limbs)) return RG_ERR_RANGE;
+  return RG_OK;
+}
+
+extern "C" int rg_big_mulmod(const uint64_t* a, int al, const uint64_t* b, int bl, const uint64_t* m, int ml,
+                             uint64_t* r, int rl) {
+  if (!a || !b || !m || !r || al < 1 || bl < 1 || ml < 1 || rl < 1) return RG_ERR_ARG;
+  big::Nat A, B, M;
+  A.v.assign(a, a + al);
+  B.v.assign(b, b + bl);
+  M.v.assign(m, m + ml);
+  big::trim(A);
+  big::trim(B);
+  big::trim(M);
+  if (big::is_zero(M) || big::cmp(A, M) >= 0 || big::cmp(B, M) >= 0) return RG_ERR_ARG;
+  const big::Barrett bar = big::make_barrett(M);
+  std::vector<big::Limb> prod, s1, s2;
+  big::kmul_into(A.v.data(), A.v.size(), B.v.data(), B.v.size(), prod);
+  big::Nat R;
+  if (!big::reduce_barrett(bar, prod.data(), prod.size(), s1, s2, &R)) return RG_ERR_RANGE;
+  if ((int)R.v.size() > rl) return RG_ERR_RANGE;
+  for (int i = 0; i < rl; ++i) r[i] = i < (int)R.v.size() ? R.v[i] : 0;
   return RG_OK;
 }
 

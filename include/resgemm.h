@@ -400,6 +400,16 @@ int rg_rational_reconstruct(const int64_t* x, int xl, const int64_t* m, int ml, 
  */
 int rg_big_gcd(const uint64_t* a, int al, const uint64_t* b, int bl, uint64_t* g, int gl);
 
+/*
+ * (a * b) mod m of naturals a, b < m given as little-endian 64-bit limbs, by
+ * the host big-integer code the solve's numerators use: a Karatsuba product
+ * and Barrett's reduction (exposed for testing).  Writes rl limbs to r.
+ * RG_ERR_RANGE if the result needs more than rl limbs, RG_ERR_ARG on bad
+ * arguments (m zero, a or b not below m).
+ */
+int rg_big_mulmod(const uint64_t* a, int al, const uint64_t* b, int bl, const uint64_t* m, int ml, uint64_t* r,
+                  int rl);
+
 /* Reconstruction of the results.  Mode 0 (the default): one-limb results
  * (res_gemm_i64, res_gemm_limbs with lc = 1) of at most 12 primes (every
  * int64 product the library plans, and caller-fixed counts up to 12) by CRT

@@ -58,9 +58,11 @@ def test_planted_integer_solution(rg, n, seed):
     assert info["denominator"] == 1 and info["steps"] >= 1
 
 
-def test_rational_solution_integer_identity(rg):
-    n = 128
-    rng = np.random.default_rng(8)
+@pytest.mark.parametrize("n", [128, 600])
+def test_rational_solution_integer_identity(rg, n):
+    # 600: about 100 lift steps, so the digits' conversion recurses several levels and the numerators'
+    # products run through Karatsuba's method and Barrett's reduction
+    rng = np.random.default_rng(8 + n)
     A = rng.integers(-(2**23), 2**23, size=(n, n), dtype=np.int64)
     b = rng.integers(-(2**23), 2**23, size=(n, 1), dtype=np.int64)
     info = {}

@@ -88,3 +88,17 @@ def test_gcd_special_cases(lib):
              (2**3000 + 7, 5), (3**2000, 3**1500 * 2**100), ((1 << 5000) - 1, (1 << 3000) - 1)]
     for a, b in cases:
         assert lib.big_gcd(a, b) == math.gcd(a, b), (a.bit_length(), b.bit_length())
+
+
+@pytest.mark.parametrize("mbits", [2, 63, 64, 65, 2000, 2048, 64 * 31 + 5, 64 * 33, 64 * 97, 64 * 300 + 17, 56000])
+def test_mulmod_karatsuba_and_barrett(lib, mbits):
+    """(a b) mod m by the Karatsuba product and Barrett's reduction the solve's numerators use, against
+    Python integers: one to 880 limbs (the size at n = 1024), unbalanced factors, and operands at the
+    edges (0, 1, m - 1, dense all-ones limbs)."""
+    rng = random.Random(mbits)
+    m = rng.getrandbits(mbits) | (1 << (mbits - 1)) | 1
+    cases = [(0, 0), (1, m - 1), (m - 1, m - 1), ((1 << (mbits - 1)) - 1, m - 1)]
+    cases += [(rng.randrange(m), rng.randrange(m)) for _ in range(4)]
+    cases += [(rng.randrange(m), rng.randrange(min(m, 1 << 64 * 40))) for _ in range(2)]  # unbalanced
+    for a, b in cases:
+        assert lib.big_mulmod(a, b, m) == a * b % m
