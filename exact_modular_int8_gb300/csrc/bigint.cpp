@@ -1,6 +1,7 @@
 // bigint.cpp -- host multi-precision arithmetic for the exact solve's
-// rational reconstruction: schoolbook products, long division (Knuth's
-// algorithm D on 64-bit limbs), and Lehmer's gcd and extended-Euclid
+// rational reconstruction: schoolbook and Karatsuba products, long division
+// (Knuth's algorithm D on 64-bit limbs), Barrett's reduction by a fixed
+// modulus, radix conversion by halves, and Lehmer's gcd and extended-Euclid
 // rational reconstruction, each batch of leading-digit quotients applied to
 // the full numbers in one in-place pass.
 #include "bigint.h"
