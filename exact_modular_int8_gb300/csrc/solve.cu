@@ -1,7 +1,8 @@
 // solve.cu -- exact rational solution of an integer system A X = B on the
 // residue engine ("exact-solve" page, Method):
 //   1. A^-1 mod q for every prime q < 256 at once, by Gauss-Jordan
-//      elimination over all primes (one launch per elimination step);
+//      elimination over all primes, blocked: per block of pivots, one panel
+//      factorisation in shared memory and one INT8 tensor-core update;
 //   2. Dixon's p-adic lift with the modulus P = the product of the primes that
 //      do not divide det(A): X_i = A^-1 R_i mod P (per prime, then balanced
 //      Garner into the wide base-P digit), R_{i+1} = (R_i - A X_i) / P formed
@@ -139,85 +140,325 @@ __device__ __forceinline__ int invmod(int a, int q) {  // a^(q-2) mod q, a != 0
   return r;
 }
 
-// One block per prime: pivot search, row swap, saved column, scaled pivot row.
-__global__ void __launch_bounds__(256) gj_pivot_kernel(uint8_t* __restrict__ M, uint8_t* __restrict__ F, int n, int k,
-                                                       int* __restrict__ perm, int* __restrict__ sing,
-                                                       int* __restrict__ pinv) {
-  wait_for_predecessor();
-  const int p = blockIdx.x;
-  if (sing[p]) return;
-  const long long nn = (long long)n * n;
-  uint8_t* Mp = M + p * nn;
-  __shared__ int s_piv;
-  if (threadIdx.x == 0) s_piv = n;
-  __syncthreads();
-  int mine = n;
-  for (int r = k + threadIdx.x; r < n; r += blockDim.x)
-    if (Mp[(long long)r * n + k]) {
-      mine = r;
-      break;
-    }
-  if (mine < n) atomicMin(&s_piv, mine);
-  __syncthreads();
-  const int r = s_piv;
-  if (r == n) {  // no pivot: q_p divides det(A)
-    if (threadIdx.x == 0) sing[p] = 1;
-    return;
-  }
-  if (r != k)
-    for (int j = threadIdx.x; j < n; j += blockDim.x) {
-      const uint8_t a = Mp[(long long)k * n + j];
-      Mp[(long long)k * n + j] = Mp[(long long)r * n + j];
-      Mp[(long long)r * n + j] = a;
-    }
-  __syncthreads();
-  const int q = c_all.q[p];
-  const int inv = invmod(Mp[(long long)k * n + k], q);
-  for (int i = threadIdx.x; i < n; i += blockDim.x) F[(long long)p * n + i] = Mp[(long long)i * n + k];
-  __syncthreads();
+// ---------------------------------------------------------------------------
+// Blocked Gauss-Jordan.  The pivots are taken in blocks J = [k0, k0 + b).  The
+// steps of the in-place elimination for one pivot k are: the first nonzero at
+// or below the diagonal of column k is the pivot, its row is swapped with row
+// k, row k is scaled by the pivot's inverse (its entry in column k becoming
+// that inverse), and every other row loses its multiple f of row k (its
+// entry in column k becoming -f / pivot).  For a column outside J, the b steps
+// of a block compose to one linear map: with Xs the column after the block's
+// row swaps, Xs_J its entries in the pivot rows, and W the panel (the columns
+// of J, all rows) after the b steps,
+//     X <- Xs with the pivot rows zeroed + W Xs_J.
+// W differs from the identity only in J's columns, so the map is a product of
+// inner dimension b per prime.  The panel kernel runs the b steps on the
+// panel alone, in shared memory; the update kernel forms the product with
+// the INT8 tensor-core MMA on balanced residues.  Both keep the unblocked
+// elimination's pivots, so the result and the recorded swaps are the same.
+// ---------------------------------------------------------------------------
+
+constexpr int kPanelThreads = 1024;
+constexpr int kSwapCols = 256;                // columns per chunk of the panel kernel's row-permutation pass
+constexpr int kSwapStride = kSwapCols + 4;    // an odd number of words: column reads across rows hit distinct banks
+constexpr size_t kPanelSmemLimit = 200u << 10;
+
+// Dynamic shared memory of the panel kernel for order nE and width b: the
+// panel (rows of b + 4 bytes, an odd number of words, so that one thread per
+// row reads without bank conflicts) or the permutation pass's row chunks,
+// whichever is larger, then the source-row index of every row.
+size_t panel_smem(int nE, int b) {
+  const size_t pan = (size_t)nE * (b + 4), chunk = (size_t)2 * b * kSwapStride;
+  return std::max(pan, chunk) + (size_t)nE * 2;
+}
+
+// The widest block (64, 32 or 16 pivots, at most nE) whose panel fits.
+int panel_width(int nE) {
+  for (int b : {64, 32, 16})
+    if (b <= nE && panel_smem(nE, b) <= kPanelSmemLimit) return b;
+  return 16;
+}
+
+// One block per prime.  Factors the panel of block [k0, k0 + B) (the b steps
+// above, on the columns of J only), writes it back (uint8 in [0, q)) and as
+// balanced int8 rows of kb bytes, Wb[p][i][t] (zero for t >= B), records the
+// pivot rows in perm, then applies the block's row swaps to the columns
+// outside J: the rows the swaps move out of J get their final contents, and
+// the pivot rows' contents go, balanced and transposed, to RT[p][j][t] (zero
+// in J's columns and for t >= B).  A prime without a pivot sets sing[p].
+template <int B>
+__global__ void __launch_bounds__(kPanelThreads) gj_panel_kernel(uint8_t* __restrict__ M, int nE, int k0, int kb,
+                                                                 int8_t* __restrict__ Wb, int8_t* __restrict__ RT,
+                                                                 int* __restrict__ perm, int* __restrict__ sing) {
+  extern __shared__ __align__(16) uint8_t sm[];
+  __shared__ uint8_t invtab[256];
+  __shared__ __align__(16) uint8_t spiv[B];
+  __shared__ int s_piv, s_nd;
+  __shared__ int s_disp[B];
+  constexpr int PS = B + 4;  // panel row stride
+  constexpr int WPR = B / 4;  // words per panel row
+  const int p = blockIdx.x, tid = threadIdx.x;
+  const int q = c_all.q[p], h = (q - 1) / 2;
   const float qf = c_all.qf[p], iq = c_all.invq[p];
-  for (int j = threadIdx.x; j < n; j += blockDim.x) {
-    const int a = j == k ? 1 : Mp[(long long)k * n + j];
-    Mp[(long long)k * n + j] = (uint8_t)mulmod(a, inv, qf, iq);
+  uint8_t* pan = sm;
+  const size_t pan_bytes = (size_t)nE * PS, chunk_bytes = (size_t)2 * B * kSwapStride;
+  const size_t body = pan_bytes > chunk_bytes ? pan_bytes : chunk_bytes;
+  uint16_t* src = reinterpret_cast<uint16_t*>(sm + body);  // row i holds original row src[i]
+  for (int a = tid; a < 256; a += kPanelThreads) invtab[a] = (a > 0 && a < q) ? (uint8_t)invmod(a, q) : 0;
+  for (int i = tid; i < nE; i += kPanelThreads) src[i] = (uint16_t)i;
+  if (tid == 0) {
+    s_piv = nE;
+    s_nd = 0;
   }
-  if (threadIdx.x == 0) {
-    perm[p * n + k] = r;
-    pinv[p] = inv;
+  wait_for_predecessor();
+  if (sing[p]) return;
+  uint8_t* Mp = M + (size_t)p * nE * nE;
+  constexpr int VPR = B / 16;  // 16-byte vectors per panel row in M
+  for (int e = tid; e < nE * VPR; e += kPanelThreads) {
+    const int i = e / VPR, v = e - i * VPR;
+    const uint4 w = *reinterpret_cast<const uint4*>(Mp + (size_t)i * nE + k0 + v * 16);
+    uint32_t* d = reinterpret_cast<uint32_t*>(pan + (size_t)i * PS + v * 16);
+    d[0] = w.x;
+    d[1] = w.y;
+    d[2] = w.z;
+    d[3] = w.w;
+  }
+  __syncthreads();
+  for (int t = 0; t < B; ++t) {
+    const int kc = k0 + t;
+    for (int i = kc + tid; i < nE; i += kPanelThreads)
+      if (pan[(size_t)i * PS + t]) {
+        atomicMin(&s_piv, i);
+        break;
+      }
+    __syncthreads();
+    const int r = s_piv;
+    if (r >= nE) {  // no pivot: q_p divides det(A) (the same value in every thread)
+      if (tid == 0) sing[p] = 1;
+      return;
+    }
+    if (r != kc) {
+      if (tid < WPR) {
+        uint32_t* x = reinterpret_cast<uint32_t*>(pan + (size_t)kc * PS) + tid;
+        uint32_t* y = reinterpret_cast<uint32_t*>(pan + (size_t)r * PS) + tid;
+        const uint32_t a = *x;
+        *x = *y;
+        *y = a;
+      } else if (tid == WPR) {
+        const uint16_t a = src[kc];
+        src[kc] = src[r];
+        src[r] = a;
+      }
+    }
+    __syncthreads();
+    if (tid < B) {
+      const int inv = invtab[pan[(size_t)kc * PS + t]];
+      const int a = tid == t ? 1 : pan[(size_t)kc * PS + tid];
+      spiv[tid] = (uint8_t)mulmod(a, inv, qf, iq);
+    }
+    if (tid == 0) {
+      perm[p * nE + kc] = r;
+      s_piv = nE;  // every thread has read it
+    }
+    __syncthreads();
+    const uint32_t* pv = reinterpret_cast<const uint32_t*>(spiv);
+    for (int i = tid; i < nE; i += kPanelThreads) {
+      uint32_t* row = reinterpret_cast<uint32_t*>(pan + (size_t)i * PS);
+      if (i == kc) {
+#pragma unroll
+        for (int w = 0; w < WPR; ++w) row[w] = pv[w];
+        continue;
+      }
+      const int f = pan[(size_t)i * PS + t];
+      if (f == 0) continue;
+      const int nf = q - f;
+#pragma unroll 4
+      for (int w = 0; w < WPR; ++w) {
+        const uint32_t x = row[w], y = pv[w];
+        uint32_t out = 0;
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          const int a = (4 * w + e == t) ? 0 : (int)((x >> (8 * e)) & 255u);
+          const float v = bal_mod_small((float)(a + nf * (int)((y >> (8 * e)) & 255u)), qf, iq);  // < 2^16
+          out |= (uint32_t)(int)(v < 0.0f ? v + qf : v) << (8 * e);
+        }
+        row[w] = out;
+      }
+    }
+    __syncthreads();
+  }
+  // the panel back into M, and balanced into Wb
+  for (int e = tid; e < nE * VPR; e += kPanelThreads) {
+    const int i = e / VPR, v = e - i * VPR;
+    const uint32_t* s = reinterpret_cast<const uint32_t*>(pan + (size_t)i * PS + v * 16);
+    *reinterpret_cast<uint4*>(Mp + (size_t)i * nE + k0 + v * 16) = make_uint4(s[0], s[1], s[2], s[3]);
+  }
+  int8_t* Wp = Wb + (size_t)p * nE * kb;
+  const int kw = kb / 4;
+  for (int e = tid; e < nE * kw; e += kPanelThreads) {
+    const int i = e / kw, w = e - i * kw;
+    uint32_t out = 0;
+    if (w < WPR) {
+      const uint32_t x = reinterpret_cast<const uint32_t*>(pan + (size_t)i * PS)[w];
+#pragma unroll
+      for (int b8 = 0; b8 < 4; ++b8) {
+        int v = (int)((x >> (8 * b8)) & 255u);
+        v = v > h ? v - q : v;
+        out |= (uint32_t)(uint8_t)(int8_t)v << (8 * b8);
+      }
+    }
+    *reinterpret_cast<uint32_t*>(Wp + (size_t)i * kb + 4 * w) = out;
+  }
+  // rows outside J that the swaps changed (at most one per swap)
+  for (int i = tid; i < nE; i += kPanelThreads)
+    if ((i < k0 || i >= k0 + B) && src[i] != i) {
+      const int u = atomicAdd(&s_nd, 1);
+      if (u < B) s_disp[u] = i;  // always: each swap moves at most one row outside J
+    }
+  __syncthreads();  // the panel is no longer needed: its space holds the row chunks below
+  const int nd = min(s_nd, B);
+  const int slots = B + nd;  // slot s < B: pivot row k0 + s; slot B + u: displaced row s_disp[u]
+  uint8_t* buf = sm;
+  int8_t* Rp = RT + (size_t)p * nE * kb;
+  for (int c0 = 0; c0 < nE; c0 += kSwapCols) {
+    const int cw = min(kSwapCols, nE - c0), cwords = cw / 4;  // cw is a multiple of 16
+    for (int e = tid; e < slots * cwords; e += kPanelThreads) {
+      const int s = e / cwords, w = e - s * cwords;
+      const int from = src[s < B ? k0 + s : s_disp[s - B]];
+      reinterpret_cast<uint32_t*>(buf + (size_t)s * kSwapStride)[w] =
+          reinterpret_cast<const uint32_t*>(Mp + (size_t)from * nE + c0)[w];
+    }
+    __syncthreads();
+    for (int e = tid; e < nd * cwords; e += kPanelThreads) {
+      const int u = e / cwords, w = e - u * cwords;
+      const int col = c0 + 4 * w;
+      if (col >= k0 && col < k0 + B) continue;  // the panel's columns already hold W
+      reinterpret_cast<uint32_t*>(Mp + (size_t)s_disp[u] * nE + c0)[w] =
+          reinterpret_cast<const uint32_t*>(buf + (size_t)(B + u) * kSwapStride)[w];
+    }
+    for (int e = tid; e < cw * kw; e += kPanelThreads) {
+      const int c = e / kw, w = e - c * kw;
+      const int col = c0 + c;
+      uint32_t out = 0;
+      if (w < WPR && (col < k0 || col >= k0 + B)) {
+#pragma unroll
+        for (int b8 = 0; b8 < 4; ++b8) {
+          int v = buf[(size_t)(4 * w + b8) * kSwapStride + c];
+          v = v > h ? v - q : v;
+          out |= (uint32_t)(uint8_t)(int8_t)v << (8 * b8);
+        }
+      }
+      *reinterpret_cast<uint32_t*>(Rp + (size_t)col * kb + 4 * w) = out;
+    }
+    __syncthreads();
   }
   allow_dependents();
 }
 
-// Every other row i: M[i][j] -= F[i] * M[k][j] (column k taken as 0 first).
-// 16 bytes of one row per thread; grid.y = prime.
-__global__ void __launch_bounds__(256) gj_elim_kernel(uint8_t* __restrict__ M, const uint8_t* __restrict__ F, int n,
-                                                      int k, const int* __restrict__ sing) {
+constexpr int kUpdTile = 128;                 // rows and columns of one update tile
+constexpr int kUpdThreads = 256;              // 8 warps, each 32 rows x 64 columns of the tile
+constexpr int kUpdOutStride = kUpdTile + 16;  // bytes per staged result row (36 words: the 2-byte stores of
+                                              // a warp's eight rows fall in distinct banks)
+
+size_t update_smem(int kb) { return (size_t)2 * kUpdTile * (kb + 16) + (size_t)kUpdTile * kUpdOutStride; }
+
+// d += a b for one m16n8k32 tile: signed 8-bit operands, 32-bit accumulators.
+__device__ __forceinline__ void mma_s8(int (&d)[4], const uint32_t (&a)[4], uint32_t b0, uint32_t b1) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k32.row.col.s32.s8.s8.s32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, {%0,%1,%2,%3};"
+      : "+r"(d[0]), "+r"(d[1]), "+r"(d[2]), "+r"(d[3])
+      : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+}
+
+// (a + b) mod q for four byte lanes, a and b in [0, q).
+__device__ __forceinline__ uint32_t add_mod4(uint32_t a, uint32_t b, uint32_t q4) {
+  const uint32_t c = __vsub4(q4, b);      // q - b, in [1, q]
+  const uint32_t ge = __vcmpgeu4(a, c);   // a + b >= q
+  return (ge & __vsub4(a, c)) | (~ge & __vadd4(a, b));
+}
+
+// The columns outside J of one 128 x 128 tile of one prime's matrix (grid.z =
+// prime): X[i][j] <- base + sum_t W[i][t] RT[j][t] mod q, base = 0 in the
+// pivot rows and X[i][j] elsewhere (the panel kernel has already permuted
+// the rows the swaps moved).  The product runs on balanced residues,
+// |sum| <= kb 125^2 < 2^23, reduced once into [0, q); one modular addition
+// then folds in the base.
+__global__ void __launch_bounds__(kUpdThreads) gj_update_kernel(uint8_t* __restrict__ M, int nE, int k0, int b,
+                                                                int kb, const int8_t* __restrict__ Wb,
+                                                                const int8_t* __restrict__ RT,
+                                                                const int* __restrict__ sing) {
+  extern __shared__ __align__(16) uint8_t sm[];
+  const int p = blockIdx.z;
+  const int i0 = blockIdx.y * kUpdTile, j0 = blockIdx.x * kUpdTile;
+  const int ls = kb + 16;  // operand row stride: the eight rows of a fragment load fall in distinct banks
+  int8_t* Ws = reinterpret_cast<int8_t*>(sm);
+  int8_t* Rs = Ws + kUpdTile * ls;
+  uint8_t* Cs = reinterpret_cast<uint8_t*>(Rs + kUpdTile * ls);
   wait_for_predecessor();
-  const int p = blockIdx.y;
-  if (sing[p]) return;
-  const long long nn = (long long)n * n;
-  const int per_row = n / 16;
-  const long long items = (long long)n * per_row;
-  uint8_t* Mp = M + p * nn;
-  const float qf = c_all.qf[p], iq = c_all.invq[p];
-  const int q = c_all.q[p];
-  for (long long it = (long long)blockIdx.x * blockDim.x + threadIdx.x; it < items;
-       it += (long long)gridDim.x * blockDim.x) {
-    const int i = (int)(it / per_row), j0 = (int)(it - (long long)i * per_row) * 16;
-    if (i == k) continue;
-    const int f = F[(long long)p * n + i];
-    if (f == 0) continue;
-    const int nf = q - f;
-    uint4 rowv = *reinterpret_cast<const uint4*>(Mp + (long long)i * n + j0);
-    const uint4 piv = *reinterpret_cast<const uint4*>(Mp + (long long)k * n + j0);
-    uint8_t* rb = reinterpret_cast<uint8_t*>(&rowv);
-    const uint8_t* pb = reinterpret_cast<const uint8_t*>(&piv);
+  if (sing[p] || (j0 >= k0 && j0 + kUpdTile <= k0 + b)) return;
+  const int8_t* Wp = Wb + (size_t)p * nE * kb;
+  const int8_t* Rp = RT + (size_t)p * nE * kb;
+  const int vr = kb / 16;
+  for (int e = threadIdx.x; e < kUpdTile * vr; e += kUpdThreads) {
+    const int r = e / vr, v = e - r * vr;
+    uint4 a = make_uint4(0u, 0u, 0u, 0u), c = a;
+    if (i0 + r < nE) a = *reinterpret_cast<const uint4*>(Wp + (size_t)(i0 + r) * kb + v * 16);
+    if (j0 + r < nE) c = *reinterpret_cast<const uint4*>(Rp + (size_t)(j0 + r) * kb + v * 16);
+    *reinterpret_cast<uint4*>(Ws + r * ls + v * 16) = a;
+    *reinterpret_cast<uint4*>(Rs + r * ls + v * 16) = c;
+  }
+  __syncthreads();
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, g = lane >> 2, c4 = (lane & 3) * 4;
+  const int wr = (warp & 3) * 32, wc = (warp >> 2) * 64;
+  int acc[2][8][4] = {};
+  for (int ks = 0; ks < kb; ks += 32) {
+    uint32_t a[2][4];
 #pragma unroll
-    for (int b = 0; b < 16; ++b) {
-      const int a = (j0 + b == k) ? 0 : rb[b];
-      float r = bal_mod_small((float)(a + nf * pb[b]), qf, iq);  // < 2^16
-      rb[b] = (uint8_t)(r < 0.0f ? r + qf : r);
+    for (int mi = 0; mi < 2; ++mi) {
+      const int8_t* ap = Ws + (wr + mi * 16 + g) * ls + ks + c4;
+      a[mi][0] = *reinterpret_cast<const uint32_t*>(ap);
+      a[mi][1] = *reinterpret_cast<const uint32_t*>(ap + 8 * ls);
+      a[mi][2] = *reinterpret_cast<const uint32_t*>(ap + 16);
+      a[mi][3] = *reinterpret_cast<const uint32_t*>(ap + 8 * ls + 16);
     }
-    *reinterpret_cast<uint4*>(Mp + (long long)i * n + j0) = rowv;
+#pragma unroll
+    for (int ni = 0; ni < 8; ++ni) {
+      const int8_t* bp = Rs + (wc + ni * 8 + g) * ls + ks + c4;
+      const uint32_t b0 = *reinterpret_cast<const uint32_t*>(bp), b1 = *reinterpret_cast<const uint32_t*>(bp + 16);
+#pragma unroll
+      for (int mi = 0; mi < 2; ++mi) mma_s8(acc[mi][ni], a[mi], b0, b1);
+    }
+  }
+  const int q = c_all.q[p];
+  const float qf = c_all.qf[p], iq = c_all.invq[p];
+  auto red = [&](int x) {
+    const float v = bal_mod_small((float)x, qf, iq);
+    return (uint32_t)(int)(v < 0.0f ? v + qf : v);
+  };
+#pragma unroll
+  for (int mi = 0; mi < 2; ++mi)
+#pragma unroll
+    for (int ni = 0; ni < 8; ++ni) {
+      const int row = wr + mi * 16 + g, col = wc + ni * 8 + (lane & 3) * 2;
+      *reinterpret_cast<uint16_t*>(Cs + row * kUpdOutStride + col) =
+          (uint16_t)(red(acc[mi][ni][0]) | red(acc[mi][ni][1]) << 8);
+      *reinterpret_cast<uint16_t*>(Cs + (row + 8) * kUpdOutStride + col) =
+          (uint16_t)(red(acc[mi][ni][2]) | red(acc[mi][ni][3]) << 8);
+    }
+  __syncthreads();
+  uint8_t* Mp = M + (size_t)p * nE * nE;
+  const uint32_t q4 = (uint32_t)q * 0x01010101u;
+  for (int e = threadIdx.x; e < kUpdTile * (kUpdTile / 16); e += kUpdThreads) {
+    const int r = e >> 3, v = e & 7;
+    const int i = i0 + r, j = j0 + v * 16;
+    if (i >= nE || j >= nE || (j >= k0 && j < k0 + b)) continue;
+    uint4 o = *reinterpret_cast<const uint4*>(Cs + r * kUpdOutStride + v * 16);
+    uint8_t* dst = Mp + (size_t)i * nE + j;
+    if (i < k0 || i >= k0 + b) {
+      const uint4 x = *reinterpret_cast<const uint4*>(dst);
+      o = make_uint4(add_mod4(o.x, x.x, q4), add_mod4(o.y, x.y, q4), add_mod4(o.z, x.z, q4), add_mod4(o.w, x.w, q4));
+    }
+    *reinterpret_cast<uint4*>(dst) = o;
   }
   allow_dependents();
 }
@@ -400,6 +641,26 @@ unsigned grid_for(long long items, int per_block = 256) {
   return (unsigned)std::max(1LL, std::min(b, cap));
 }
 
+// The panel kernels' dynamic shared memory above the default 48 KB, set once
+// per device.
+cudaError_t allow_panel_smem() {
+  static std::mutex mu;
+  static bool done[64];
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+  std::lock_guard<std::mutex> lock(mu);
+  if (done[dev]) return cudaSuccess;
+  const int bytes = (int)kPanelSmemLimit;
+  e = cudaFuncSetAttribute(gj_panel_kernel<64>, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+  if (e == cudaSuccess) e = cudaFuncSetAttribute(gj_panel_kernel<48>, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+  if (e == cudaSuccess) e = cudaFuncSetAttribute(gj_panel_kernel<32>, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+  if (e == cudaSuccess) e = cudaFuncSetAttribute(gj_panel_kernel<16>, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+  if (e == cudaSuccess) done[dev] = true;
+  return e;
+}
+
 }  // namespace
 }  // namespace rg
 
@@ -490,27 +751,42 @@ extern "C" int rg_solve_i64(const int64_t* A_in, const int64_t* B_in, int64_t n6
   // 2. batched inverse, on diag(A, I) of order nE = n rounded up to 16
   const int nE = (n + 15) / 16 * 16, ld = nE;
   const size_t nnE = (size_t)nE * nE;
-  DevBuf dM, dF, dperm, dsing, dpinv;
+  const int bw = panel_width(nE), kbw = (bw + 31) / 32 * 32;
+  DevBuf dM, dW, dRT, dperm, dsing;
   SOLVE_TRY(dM.alloc((size_t)kNumPrimes * nnE, st));
-  SOLVE_TRY(dF.alloc((size_t)kNumPrimes * nE, st));
+  SOLVE_TRY(dW.alloc((size_t)kNumPrimes * nE * kbw, st));
+  SOLVE_TRY(dRT.alloc((size_t)kNumPrimes * nE * kbw, st));
   SOLVE_TRY(dperm.alloc((size_t)kNumPrimes * nE * 4, st));
   SOLVE_TRY(dsing.alloc(kNumPrimes * 4, st));
-  SOLVE_TRY(dpinv.alloc(kNumPrimes * 4, st));
   uint8_t* M = static_cast<uint8_t*>(dM.p);
-  uint8_t* F = static_cast<uint8_t*>(dF.p);
+  int8_t* Wb = static_cast<int8_t*>(dW.p);
+  int8_t* RT = static_cast<int8_t*>(dRT.p);
   int* perm = static_cast<int*>(dperm.p);
   int* sing = static_cast<int*>(dsing.p);
-  int* pinv = static_cast<int*>(dpinv.p);
   SOLVE_TRY(cudaMemsetAsync(sing, 0, kNumPrimes * 4, st));
   gj_init_kernel<<<grid_for((long long)nnE), 256, 0, st>>>(A, n, nE, M);
   SOLVE_TRY(cudaGetLastError());
-  const long long elim_items = (long long)nE * (nE / 16);
-  const dim3 elim_grid(std::max(1u, std::min((unsigned)((elim_items + 255) / 256), 4u * sm_count_host())),
-                       kNumPrimes);
-  for (int k = 0; k < nE; ++k) {
-    SOLVE_TRY(launch_dependent(gj_pivot_kernel, dim3(kNumPrimes), dim3(256), 0, st, M, F, nE, k, perm, sing, pinv));
-    SOLVE_TRY(launch_dependent(gj_elim_kernel, elim_grid, dim3(256), 0, st, M, (const uint8_t*)F, nE, k,
-                               (const int*)sing));
+  SOLVE_TRY(allow_panel_smem());
+  const unsigned tiles = (unsigned)((nE + kUpdTile - 1) / kUpdTile);
+  for (int k0 = 0; k0 < nE; k0 += bw) {
+    const int b = std::min(bw, nE - k0), kb = (b + 31) / 32 * 32;  // b: a multiple of 16
+    const size_t smem = panel_smem(nE, b);
+    if (b == 64)
+      SOLVE_TRY(launch_dependent(gj_panel_kernel<64>, dim3(kNumPrimes), dim3(kPanelThreads), smem, st, M, nE, k0, kb,
+                                 Wb, RT, perm, sing));
+    else if (b == 48)
+      SOLVE_TRY(launch_dependent(gj_panel_kernel<48>, dim3(kNumPrimes), dim3(kPanelThreads), smem, st, M, nE, k0, kb,
+                                 Wb, RT, perm, sing));
+    else if (b == 32)
+      SOLVE_TRY(launch_dependent(gj_panel_kernel<32>, dim3(kNumPrimes), dim3(kPanelThreads), smem, st, M, nE, k0, kb,
+                                 Wb, RT, perm, sing));
+    else
+      SOLVE_TRY(launch_dependent(gj_panel_kernel<16>, dim3(kNumPrimes), dim3(kPanelThreads), smem, st, M, nE, k0, kb,
+                                 Wb, RT, perm, sing));
+    if (b < nE)
+      SOLVE_TRY(launch_dependent(gj_update_kernel, dim3(tiles, tiles, kNumPrimes), dim3(kUpdThreads),
+                                 update_smem(kb), st, M, nE, k0, b, kb, (const int8_t*)Wb, (const int8_t*)RT,
+                                 (const int*)sing));
   }
   int hsing[kNumPrimes];
   SOLVE_TRY(cudaMemcpyAsync(hsing, sing, sizeof(hsing), cudaMemcpyDeviceToHost, st));

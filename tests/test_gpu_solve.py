@@ -127,3 +127,40 @@ def test_range_error(rg):
     with pytest.raises(rg.ResGemmError) as e:
         rg.solve(dev(A), dev(np.ones((n, 1), dtype=np.int64)))
     assert e.value.code == rg.RG_ERR_RANGE
+
+
+def det_is_zero_mod(A, q):
+    """Whether q divides det(A), by Gaussian elimination over GF(q) (numpy, exact in int64)."""
+    M = np.mod(A, q).astype(np.int64)
+    n = len(M)
+    for k in range(n):
+        nz = np.nonzero(M[k:, k])[0]
+        if len(nz) == 0:
+            return True
+        r = k + nz[0]
+        M[[k, r]] = M[[r, k]]
+        inv = pow(int(M[k, k]), q - 2, q)
+        M[k] = M[k] * inv % q
+        f = M[k + 1:, k].copy()
+        M[k + 1:] = (M[k + 1:] - np.outer(f, M[k])) % q
+    return False
+
+
+def test_primes_dividing_det_found_in_later_pivot_blocks(rg):
+    """Rows made dependent modulo 3, 5 and 7 only (each is another row combination plus a multiple of q times a
+    random row), at positions that the elimination reaches in its second, third and fourth block of pivots: exactly
+    the primes dividing det(A) are dropped, and the solution is exact."""
+    n = 230
+    rng = np.random.default_rng(11)
+    A = rng.integers(-(2**20), 2**20, size=(n, n), dtype=np.int64)
+    for row, q, (a, b) in ((100, 3, (0, 1)), (170, 5, (2, 3)), (229, 7, (4, 5))):
+        A[row] = A[a] + A[b] + q * rng.integers(-1000, 1000, size=n)
+    b = rng.integers(-(2**20), 2**20, size=(n, 1), dtype=np.int64)
+    info = {}
+    X = rg.solve(dev(A), dev(b), info=info)
+    primes = [q for q in range(3, 256, 2) if all(q % d for d in range(3, int(q ** 0.5) + 1, 2))]
+    assert len(primes) == 53
+    kept = [q for q in primes if not det_is_zero_mod(A, q)]
+    assert 3 not in kept and 5 not in kept and 7 not in kept
+    assert info["primes"] == len(kept)
+    assert integer_identity(A, X, b)
