@@ -47,7 +47,7 @@ RG_OP_I64, RG_OP_LIMBS, RG_OP_ENCLOSE, RG_OP_STAGE, RG_OP_ENCLOSE_F32 = 0, 1, 2,
 RG_OP_INTERVAL, RG_OP_INTERVAL_F32 = 5, 6
 RG_PROBE_MMA_S8, RG_PROBE_TCGEN05_F16, RG_PROBE_TCGEN05_E4M3 = 0, 1, 2
 RG_PROBE_TCGEN05_F16_BMN, RG_PROBE_TCGEN05_F16_PAIR, RG_PROBE_TCGEN05_F16_PAIR_BMN = 3, 4, 5
-RG_PROBE_TCGEN05_F16_PAIR_BMN_SYNC = 6
+RG_PROBE_TCGEN05_F16_PAIR_BMN_SYNC, RG_PROBE_MMA_F16 = 6, 7
 MAX_K = 131072
 NUM_PRIMES = 53
 

@@ -13,6 +13,9 @@
 //                          would use (page "Accelerating Multiple-Precision LU
 //                          Decomposition with Ozaki Scheme II", FP8 balanced
 //                          base-17 encoding).
+//   RG_PROBE_MMA_F16       mma.sync.aligned.m16n8k16 f16 x f16 -> f32, the
+//                          warp-level fp16 MMA (the exact solve's elimination
+//                          update could hold its residues in either type).
 //   RG_PROBE_TCGEN05_F16_BMN, _PAIR, _PAIR_BMN, _PAIR_BMN_SYNC: kind::f16 in
 //                          the forms the residue GEMM uses: B MN-major, the
 //                          CTA-pair instruction (cta_group::2, M = 256), and
@@ -61,6 +64,27 @@ __global__ void __launch_bounds__(kProbeThreadsSync) probe_mma_s8_kernel(int ite
 #pragma unroll
   for (int j = 0; j < kSyncChains; ++j) s ^= c[j][0] ^ c[j][1] ^ c[j][2] ^ c[j][3];
   atomicXor(sink, s);
+}
+
+// The same loop with mma.sync m16n8k16 fp16 x fp16 -> fp32 (operands 1.0).
+__global__ void __launch_bounds__(kProbeThreadsSync) probe_mma_f16_kernel(int iters, int* sink) {
+  const uint32_t one2 = 0x3C003C00u;  // two fp16 ones
+  float c[kSyncChains][4];
+#pragma unroll
+  for (int j = 0; j < kSyncChains; ++j) c[j][0] = c[j][1] = c[j][2] = c[j][3] = 0.0f;
+  for (int it = 0; it < iters; ++it) {
+#pragma unroll
+    for (int j = 0; j < kSyncChains; ++j)
+      asm volatile(
+          "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
+          "{%0,%1,%2,%3};"
+          : "+f"(c[j][0]), "+f"(c[j][1]), "+f"(c[j][2]), "+f"(c[j][3])
+          : "r"(one2), "r"(one2), "r"(one2), "r"(one2), "r"(one2), "r"(one2));
+  }
+  float s = 0.0f;
+#pragma unroll
+  for (int j = 0; j < kSyncChains; ++j) s += c[j][0] + c[j][1] + c[j][2] + c[j][3];
+  atomicXor(sink, __float_as_int(s) + (int)(blockIdx.x * kProbeThreadsSync + threadIdx.x));
 }
 
 // ---------------------------------------------------------------------------
@@ -284,6 +308,12 @@ extern "C" int rg_probe_mma_rate(int kind, int blocks, int iters, void* ws, size
       const int nb = blocks ? blocks : 4 * sms;
       probe_mma_s8_kernel<<<nb, kProbeThreadsSync, 0, s>>>(iters, &plan->pad0[0]);
       *ops_per_launch = 2.0 * nb * (kProbeThreadsSync / 32) * (double)iters * kSyncChains * (16.0 * 8.0 * 32.0);
+      break;
+    }
+    case RG_PROBE_MMA_F16: {
+      const int nb = blocks ? blocks : 4 * sms;
+      probe_mma_f16_kernel<<<nb, kProbeThreadsSync, 0, s>>>(iters, &plan->pad0[0]);
+      *ops_per_launch = 2.0 * nb * (kProbeThreadsSync / 32) * (double)iters * kSyncChains * (16.0 * 8.0 * 16.0);
       break;
     }
     case RG_PROBE_TCGEN05_F16:

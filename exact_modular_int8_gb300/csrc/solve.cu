@@ -9,6 +9,7 @@
 //      in one 64-bit limb as (R_i - A X_i) P^-1 mod 2^64 (P odd);
 //   3. on the host, rational reconstruction of one component for the common
 //      denominator, then one modular product per numerator.
+#include <cuda_fp16.h>
 #include <cuda_runtime.h>
 
 #include <algorithm>
@@ -43,11 +44,12 @@ constexpr int kW = 11;  // 32-bit words of a base-P digit (|x| < P / 2 < 2^333)
 // Norms and range: row and column sums of squares of A, column sums of
 // squares of B (fp64, for the Hadamard bounds) and max |A|.
 // ---------------------------------------------------------------------------
+// One warp per row of A (its sum of squares and max |A|), then one thread per
+// column of B.
 __global__ void __launch_bounds__(256) norms_kernel(const int64_t* __restrict__ A, const int64_t* __restrict__ B,
-                                                    int n, int c, double* rows, double* cols, double* bcols,
+                                                    int n, int c, double* rows, double* bcols,
                                                     unsigned long long* maxabs) {
   const int warp = (blockIdx.x * blockDim.x + threadIdx.x) >> 5, lane = threadIdx.x & 31;
-  // one warp per row of A
   if (warp < n) {
     double s = 0.0;
     unsigned long long m = 0;
@@ -68,28 +70,46 @@ __global__ void __launch_bounds__(256) norms_kernel(const int64_t* __restrict__ 
       atomicMax(maxabs, m);
     }
   }
-  // one thread per column of A, then of B
   const int t = blockIdx.x * blockDim.x + threadIdx.x;
-  if (t < n) {
+  if (t < c) {
     double s = 0.0;
     for (int i = 0; i < n; ++i) {
-      const double d = (double)A[(long long)i * n + t];
+      const double d = (double)B[(long long)i * c + t];
       s = fma(d, d, s);
     }
-    cols[t] = s;
-  } else if (t < n + c) {
-    double s = 0.0;
-    for (int i = 0; i < n; ++i) {
-      const double d = (double)B[(long long)i * c + (t - n)];
-      s = fma(d, d, s);
-    }
-    bcols[t - n] = s;
+    bcols[t] = s;
   }
+}
+
+// Column sums of squares of A over the rows [y * rows_per, (y + 1) * rows_per)
+// of chunk y = blockIdx.y, one thread per column (a row of A is read by
+// consecutive threads): part[y][t].
+__global__ void __launch_bounds__(256) col_norms_part_kernel(const int64_t* __restrict__ A, int n, int rows_per,
+                                                             double* __restrict__ part) {
+  const int t = blockIdx.x * blockDim.x + threadIdx.x;
+  if (t >= n) return;
+  const int i0 = blockIdx.y * rows_per, i1 = min(n, i0 + rows_per);
+  double s = 0.0;
+  for (int i = i0; i < i1; ++i) {
+    const double d = (double)A[(long long)i * n + t];
+    s = fma(d, d, s);
+  }
+  part[(size_t)blockIdx.y * n + t] = s;
+}
+
+// cols[t] = the chunks' partial sums of column t, added in chunk order.
+__global__ void __launch_bounds__(256) col_norms_sum_kernel(const double* __restrict__ part, int n, int chunks,
+                                                            double* __restrict__ cols) {
+  const int t = blockIdx.x * blockDim.x + threadIdx.x;
+  if (t >= n) return;
+  double s = 0.0;
+  for (int y = 0; y < chunks; ++y) s += part[(size_t)y * n + t];
+  cols[t] = s;
 }
 
 // ---------------------------------------------------------------------------
 // Batched modular inverse ("exact-solve", Method: A^-1 mod q for every prime
-// by Gauss-Jordan, one grid per elimination step spanning all primes).
+// by Gauss-Jordan, each launch spanning all primes; here blocked, below).
 // M[p] is A mod q_p in [0, q), n x n bytes, inverted in place: at step k the
 // pivot row is the first row >= k with a nonzero in column k; it is swapped
 // up, scaled by the pivot's inverse (its own column entry becoming that
@@ -115,8 +135,11 @@ __device__ __forceinline__ int residue_i64(long long x, int p) {
 // keeps every row a whole number of 16-byte vectors; the inverse of diag(A, I)
 // is diag(A^-1, I), and the same primes divide both determinants).
 __global__ void __launch_bounds__(256) gj_init_kernel(const int64_t* __restrict__ A, int n, int nE,
-                                                      uint8_t* __restrict__ M) {
+                                                      uint8_t* __restrict__ M, int* __restrict__ rowsrc) {
   const long long nn = (long long)nE * nE;
+  for (long long e = (long long)blockIdx.x * blockDim.x + threadIdx.x; e < (long long)kNumPrimes * nE;
+       e += (long long)gridDim.x * blockDim.x)
+    rowsrc[e] = (int)(e % nE);
   for (long long e = (long long)blockIdx.x * blockDim.x + threadIdx.x; e < nn; e += (long long)gridDim.x * blockDim.x) {
     const int i = (int)(e / nE), j = (int)(e - (long long)i * nE);
     const long long x = (i < n && j < n) ? A[(long long)i * n + j] : (i == j ? 1 : 0);
@@ -172,31 +195,57 @@ size_t panel_smem(int nE, int b) {
   return std::max(pan, chunk) + (size_t)nE * 2;
 }
 
-// The widest block (64, 32 or 16 pivots, at most nE) whose panel fits.
-int panel_width(int nE) {
-  for (int b : {64, 32, 16})
-    if (b <= nE && panel_smem(nE, b) <= kPanelSmemLimit) return b;
-  return 16;
+// The panel kernel's shape for order nE: the block width B (its panel of
+// nE x (B + 4) bytes within kPanelSmemLimit), the sub-block S and the rows
+// per thread RPT = nE / 1024 rounded up, with RPT x S <= 32 entries held in
+// registers.
+struct PanelCfg {
+  int B, S, RPT;
+};
+PanelCfg panel_cfg(int nE) {
+  if (nE <= kPanelThreads) return {64, 16, 1};
+  if (nE <= 2 * kPanelThreads) return {64, 8, 2};
+  if (nE <= 4 * kPanelThreads) return {32, 8, 4};
+  return {16, 4, 8};
 }
 
-// One block per prime.  Factors the panel of block [k0, k0 + B) (the b steps
-// above, on the columns of J only), writes it back (uint8 in [0, q)) and as
-// balanced int8 rows of kb bytes, Wb[p][i][t] (zero for t >= B), records the
-// pivot rows in perm, then applies the block's row swaps to the columns
-// outside J: the rows the swaps move out of J get their final contents, and
-// the pivot rows' contents go, balanced and transposed, to RT[p][j][t] (zero
-// in J's columns and for t >= B).  A prime without a pivot sets sing[p].
-template <int B>
-__global__ void __launch_bounds__(kPanelThreads) gj_panel_kernel(uint8_t* __restrict__ M, int nE, int k0, int kb,
-                                                                 int8_t* __restrict__ Wb, int8_t* __restrict__ RT,
-                                                                 int* __restrict__ perm, int* __restrict__ sing) {
+// Reduction of |x| <= 2^23 into [0, q).
+__device__ __forceinline__ int red_q(int x, float qf, float iq) {
+  const float v = bal_mod_small((float)x, qf, iq);
+  return (int)(v < 0.0f ? v + qf : v);
+}
+
+// One block per prime.  Factors the panel of block [k0, k0 + b), b <= B a
+// multiple of 16 (the steps above, on J's columns only), writes it back
+// (uint8 in [0, q)) and as balanced fp16 rows of kb entries, Wb[p][i][t]
+// (zero for t >= b), then applies the block's row swaps to the columns outside J:
+// the rows the swaps move out of J get their final contents, and the pivot
+// rows' contents go, balanced and transposed, to RT[p][j][t] (zero in J's
+// columns and for t >= b).  rowsrc[p][i] follows the original row that row i
+// holds.  A prime without a pivot sets sing[p].
+//
+// The panel itself is factored in sub-blocks of S pivots by the same
+// composition: each thread holds the S sub-block entries of its RPT rows in
+// registers, unreduced during the sub-block's steps (each step adds at most
+// 250^2 in magnitude: |x| < 2^20 after 16), reducing only the entry that
+// decides the multiplier and the next pivot; then the other panel columns
+// take X <- Xs with the sub-block's pivot rows zeroed + W_S Xs_S by dp4a.
+template <int B, int S, int RPT>
+__global__ void __launch_bounds__(kPanelThreads) gj_panel_kernel(uint8_t* __restrict__ M, int nE, int k0, int b,
+                                                                 int kb, __half* __restrict__ Wb,
+                                                                 __half* __restrict__ RT, int* __restrict__ rowsrc,
+                                                                 int* __restrict__ sing) {
+  static_assert(S % 4 == 0 && B % S == 0 && 16 % S == 0, "sub-blocks of whole words dividing every panel width");
   extern __shared__ __align__(16) uint8_t sm[];
   __shared__ uint8_t invtab[256];
-  __shared__ __align__(16) uint8_t spiv[B];
-  __shared__ int s_piv, s_nd;
+  __shared__ __align__(16) int spiv[S];
+  __shared__ __align__(16) uint8_t Rt[B * S];  // [panel column][t]: a sub-block's pivot rows, transposed
+  __shared__ int s_piv[2];
+  __shared__ int s_nd;
   __shared__ int s_disp[B];
-  constexpr int PS = B + 4;  // panel row stride
-  constexpr int WPR = B / 4;  // words per panel row
+  __shared__ int s_rs[2 * B];
+  constexpr int PS = B + 4;  // panel row stride: an odd number of words
+  constexpr int SW = S / 4;
   const int p = blockIdx.x, tid = threadIdx.x;
   const int q = c_all.q[p], h = (q - 1) / 2;
   const float qf = c_all.qf[p], iq = c_all.invq[p];
@@ -207,15 +256,15 @@ __global__ void __launch_bounds__(kPanelThreads) gj_panel_kernel(uint8_t* __rest
   for (int a = tid; a < 256; a += kPanelThreads) invtab[a] = (a > 0 && a < q) ? (uint8_t)invmod(a, q) : 0;
   for (int i = tid; i < nE; i += kPanelThreads) src[i] = (uint16_t)i;
   if (tid == 0) {
-    s_piv = nE;
+    s_piv[0] = s_piv[1] = nE;
     s_nd = 0;
   }
   wait_for_predecessor();
   if (sing[p]) return;
   uint8_t* Mp = M + (size_t)p * nE * nE;
-  constexpr int VPR = B / 16;  // 16-byte vectors per panel row in M
-  for (int e = tid; e < nE * VPR; e += kPanelThreads) {
-    const int i = e / VPR, v = e - i * VPR;
+  const int vpr = b / 16;  // 16-byte vectors per panel row in M
+  for (int e = tid; e < nE * vpr; e += kPanelThreads) {
+    const int i = e / vpr, v = e - i * vpr;
     const uint4 w = *reinterpret_cast<const uint4*>(Mp + (size_t)i * nE + k0 + v * 16);
     uint32_t* d = reinterpret_cast<uint32_t*>(pan + (size_t)i * PS + v * 16);
     d[0] = w.x;
@@ -224,107 +273,163 @@ __global__ void __launch_bounds__(kPanelThreads) gj_panel_kernel(uint8_t* __rest
     d[3] = w.w;
   }
   __syncthreads();
-  for (int t = 0; t < B; ++t) {
-    const int kc = k0 + t;
-    for (int i = kc + tid; i < nE; i += kPanelThreads)
-      if (pan[(size_t)i * PS + t]) {
-        atomicMin(&s_piv, i);
-        break;
-      }
-    __syncthreads();
-    const int r = s_piv;
-    if (r >= nE) {  // no pivot: q_p divides det(A) (the same value in every thread)
-      if (tid == 0) sing[p] = 1;
-      return;
-    }
-    if (r != kc) {
-      if (tid < WPR) {
-        uint32_t* x = reinterpret_cast<uint32_t*>(pan + (size_t)kc * PS) + tid;
-        uint32_t* y = reinterpret_cast<uint32_t*>(pan + (size_t)r * PS) + tid;
-        const uint32_t a = *x;
-        *x = *y;
-        *y = a;
-      } else if (tid == WPR) {
-        const uint16_t a = src[kc];
-        src[kc] = src[r];
-        src[r] = a;
-      }
-    }
-    __syncthreads();
-    if (tid < B) {
-      const int inv = invtab[pan[(size_t)kc * PS + t]];
-      const int a = tid == t ? 1 : pan[(size_t)kc * PS + tid];
-      spiv[tid] = (uint8_t)mulmod(a, inv, qf, iq);
-    }
-    if (tid == 0) {
-      perm[p * nE + kc] = r;
-      s_piv = nE;  // every thread has read it
-    }
-    __syncthreads();
-    const uint32_t* pv = reinterpret_cast<const uint32_t*>(spiv);
-    for (int i = tid; i < nE; i += kPanelThreads) {
-      uint32_t* row = reinterpret_cast<uint32_t*>(pan + (size_t)i * PS);
-      if (i == kc) {
+  for (int c0 = 0; c0 < b; c0 += S) {  // sub-block: panel columns [c0, c0 + S), pivots k0 + c0 + tt
+    const int kc0 = k0 + c0;
+    int a[RPT][S];
+    int rid[RPT];  // the panel row each register slot holds; a row swap exchanges two slots' ids
 #pragma unroll
-        for (int w = 0; w < WPR; ++w) row[w] = pv[w];
-        continue;
+    for (int k = 0; k < RPT; ++k) {
+      const int row = tid + k * kPanelThreads;
+      rid[k] = row;
+#pragma unroll
+      for (int w = 0; w < SW; ++w) {
+        const uint32_t x = row < nE ? reinterpret_cast<const uint32_t*>(pan + (size_t)row * PS + c0)[w] : 0u;
+#pragma unroll
+        for (int e = 0; e < 4; ++e) a[k][4 * w + e] = (int)((x >> (8 * e)) & 255u);
       }
-      const int f = pan[(size_t)i * PS + t];
-      if (f == 0) continue;
-      const int nf = q - f;
-#pragma unroll 4
-      for (int w = 0; w < WPR; ++w) {
-        const uint32_t x = row[w], y = pv[w];
+      if (row >= kc0 && row < nE && a[k][0] != 0) atomicMin(&s_piv[c0 & 1], row);
+    }
+    __syncthreads();
+#pragma unroll
+    for (int tt = 0; tt < S; ++tt) {
+      const int tg = c0 + tt, kc = k0 + tg;
+      const int r = s_piv[tg & 1];
+      if (r >= nE) {  // no pivot: q_p divides det(A) (the same value in every thread)
+        if (tid == 0) sing[p] = 1;
+        return;
+      }
+#pragma unroll
+      for (int k = 0; k < RPT; ++k) {
+        rid[k] = rid[k] == kc ? r : (rid[k] == r ? kc : rid[k]);
+        if (rid[k] == kc) {  // the pivot row: reduced, scaled by the pivot's inverse
+          const int inv = invtab[red_q(a[k][tt], qf, iq)];
+#pragma unroll
+          for (int j = 0; j < S; ++j) {
+            const int v = j == tt ? inv : mulmod(red_q(a[k][j], qf, iq), inv, qf, iq);
+            a[k][j] = v;
+            spiv[j] = v;
+          }
+        }
+      }
+      if (r != kc) {
+        if (tid < b / 4 && (tid < c0 / 4 || tid >= c0 / 4 + SW)) {  // the panel's other columns
+          uint32_t* x = reinterpret_cast<uint32_t*>(pan + (size_t)kc * PS) + tid;
+          uint32_t* y = reinterpret_cast<uint32_t*>(pan + (size_t)r * PS) + tid;
+          const uint32_t t0 = *x;
+          *x = *y;
+          *y = t0;
+        } else if (tid == kPanelThreads - 1) {
+          const uint16_t t0 = src[kc];
+          src[kc] = src[r];
+          src[r] = t0;
+        }
+      }
+      if (tid == 0) s_piv[(tg + 1) & 1] = nE;  // read last before the previous step's end
+      __syncthreads();
+      // every other row loses f times the pivot row (its entry tt becoming -f * inverse); the
+      // next column's reduced entry names a pivot candidate for the next step
+#pragma unroll
+      for (int k = 0; k < RPT; ++k) {
+        const int row = rid[k];
+        if (row >= nE || row == kc) continue;
+        const int f = red_q(a[k][tt], qf, iq);
+        if (f) {
+          a[k][tt] = 0;
+#pragma unroll
+          for (int j = 0; j < S; ++j) a[k][j] -= f * spiv[j];
+        }
+        if (tt + 1 < S && row > kc && red_q(a[k][tt + 1], qf, iq) != 0) atomicMin(&s_piv[(tg + 1) & 1], row);
+      }
+      __syncthreads();
+    }
+    // the sub-block back into the panel, reduced, each slot into the row it holds
+#pragma unroll
+    for (int k = 0; k < RPT; ++k) {
+      const int row = rid[k];
+      if (row >= nE) continue;
+#pragma unroll
+      for (int w = 0; w < SW; ++w) {
+        uint32_t x = 0;
+#pragma unroll
+        for (int e = 0; e < 4; ++e) x |= (uint32_t)red_q(a[k][4 * w + e], qf, iq) << (8 * e);
+        reinterpret_cast<uint32_t*>(pan + (size_t)row * PS + c0)[w] = x;
+      }
+    }
+    if (b == S) break;  // no other panel columns
+    __syncthreads();
+    for (int e = tid; e < b * S; e += kPanelThreads) {
+      const int j = e / S, t = e - j * S;
+      Rt[e] = pan[(size_t)(kc0 + t) * PS + j];
+    }
+    __syncthreads();
+    // the other panel columns: X <- (0 in the sub-block's pivot rows, else X) + W_S Rt (sums < 16 * 250^2)
+#pragma unroll
+    for (int k = 0; k < RPT; ++k) {
+      const int row = tid + k * kPanelThreads;
+      if (row >= nE) continue;
+      uint32_t* prow = reinterpret_cast<uint32_t*>(pan + (size_t)row * PS);
+      uint32_t wv[SW];
+#pragma unroll
+      for (int u = 0; u < SW; ++u) wv[u] = prow[c0 / 4 + u];
+      const bool pivot_row = row >= kc0 && row < kc0 + S;
+      for (int w = 0; w < b / 4; ++w) {
+        if (w >= c0 / 4 && w < c0 / 4 + SW) continue;
+        const uint32_t base = pivot_row ? 0u : prow[w];
         uint32_t out = 0;
 #pragma unroll
         for (int e = 0; e < 4; ++e) {
-          const int a = (4 * w + e == t) ? 0 : (int)((x >> (8 * e)) & 255u);
-          const float v = bal_mod_small((float)(a + nf * (int)((y >> (8 * e)) & 255u)), qf, iq);  // < 2^16
-          out |= (uint32_t)(int)(v < 0.0f ? v + qf : v) << (8 * e);
+          const uint32_t* rt = reinterpret_cast<const uint32_t*>(Rt + (4 * w + e) * S);
+          int x = (int)((base >> (8 * e)) & 255u);
+#pragma unroll
+          for (int u = 0; u < SW; ++u) asm("dp4a.u32.u32 %0, %1, %2, %0;" : "+r"(x) : "r"(wv[u]), "r"(rt[u]));
+          out |= (uint32_t)red_q(x, qf, iq) << (8 * e);
         }
-        row[w] = out;
+        prow[w] = out;
       }
     }
     __syncthreads();
   }
+  __syncthreads();
   // the panel back into M, and balanced into Wb
-  for (int e = tid; e < nE * VPR; e += kPanelThreads) {
-    const int i = e / VPR, v = e - i * VPR;
+  for (int e = tid; e < nE * vpr; e += kPanelThreads) {
+    const int i = e / vpr, v = e - i * vpr;
     const uint32_t* s = reinterpret_cast<const uint32_t*>(pan + (size_t)i * PS + v * 16);
     *reinterpret_cast<uint4*>(Mp + (size_t)i * nE + k0 + v * 16) = make_uint4(s[0], s[1], s[2], s[3]);
   }
-  int8_t* Wp = Wb + (size_t)p * nE * kb;
-  const int kw = kb / 4;
-  for (int e = tid; e < nE * kw; e += kPanelThreads) {
-    const int i = e / kw, w = e - i * kw;
-    uint32_t out = 0;
-    if (w < WPR) {
-      const uint32_t x = reinterpret_cast<const uint32_t*>(pan + (size_t)i * PS)[w];
-#pragma unroll
-      for (int b8 = 0; b8 < 4; ++b8) {
-        int v = (int)((x >> (8 * b8)) & 255u);
-        v = v > h ? v - q : v;
-        out |= (uint32_t)(uint8_t)(int8_t)v << (8 * b8);
-      }
+  __half* Wp = Wb + (size_t)p * nE * kb;
+  const int kp = kb / 2;  // pairs of fp16 per row
+  for (int e = tid; e < nE * kp; e += kPanelThreads) {
+    const int i = e / kp, t = 2 * (e - i * kp);
+    __half2 out = __floats2half2_rn(0.0f, 0.0f);
+    if (t < b) {
+      int v0 = pan[(size_t)i * PS + t], v1 = pan[(size_t)i * PS + t + 1];
+      v0 = v0 > h ? v0 - q : v0;
+      v1 = v1 > h ? v1 - q : v1;
+      out = __floats2half2_rn((float)v0, (float)v1);  // |v| <= 125: exact
     }
-    *reinterpret_cast<uint32_t*>(Wp + (size_t)i * kb + 4 * w) = out;
+    *reinterpret_cast<__half2*>(Wp + (size_t)i * kb + t) = out;
   }
   // rows outside J that the swaps changed (at most one per swap)
   for (int i = tid; i < nE; i += kPanelThreads)
-    if ((i < k0 || i >= k0 + B) && src[i] != i) {
+    if ((i < k0 || i >= k0 + b) && src[i] != i) {
       const int u = atomicAdd(&s_nd, 1);
-      if (u < B) s_disp[u] = i;  // always: each swap moves at most one row outside J
+      if (u < b) s_disp[u] = i;  // always: each swap moves at most one row outside J
     }
   __syncthreads();  // the panel is no longer needed: its space holds the row chunks below
-  const int nd = min(s_nd, B);
-  const int slots = B + nd;  // slot s < B: pivot row k0 + s; slot B + u: displaced row s_disp[u]
+  const int nd = min(s_nd, b);
+  const int slots = b + nd;  // slot s < b: pivot row k0 + s; slot b + u: displaced row s_disp[u]
+  // the original row each row of M holds: rowsrc[i] <- rowsrc[src[i]] for the rows the swaps changed
+  int* rs = rowsrc + (size_t)p * nE;
+  for (int s = tid; s < slots; s += kPanelThreads) s_rs[s] = rs[src[s < b ? k0 + s : s_disp[s - b]]];
+  __syncthreads();
+  for (int s = tid; s < slots; s += kPanelThreads) rs[s < b ? k0 + s : s_disp[s - b]] = s_rs[s];
   uint8_t* buf = sm;
-  int8_t* Rp = RT + (size_t)p * nE * kb;
+  __half* Rp = RT + (size_t)p * nE * kb;
   for (int c0 = 0; c0 < nE; c0 += kSwapCols) {
     const int cw = min(kSwapCols, nE - c0), cwords = cw / 4;  // cw is a multiple of 16
     for (int e = tid; e < slots * cwords; e += kPanelThreads) {
       const int s = e / cwords, w = e - s * cwords;
-      const int from = src[s < B ? k0 + s : s_disp[s - B]];
+      const int from = src[s < b ? k0 + s : s_disp[s - b]];
       reinterpret_cast<uint32_t*>(buf + (size_t)s * kSwapStride)[w] =
           reinterpret_cast<const uint32_t*>(Mp + (size_t)from * nE + c0)[w];
     }
@@ -332,23 +437,21 @@ __global__ void __launch_bounds__(kPanelThreads) gj_panel_kernel(uint8_t* __rest
     for (int e = tid; e < nd * cwords; e += kPanelThreads) {
       const int u = e / cwords, w = e - u * cwords;
       const int col = c0 + 4 * w;
-      if (col >= k0 && col < k0 + B) continue;  // the panel's columns already hold W
+      if (col >= k0 && col < k0 + b) continue;  // the panel's columns already hold W
       reinterpret_cast<uint32_t*>(Mp + (size_t)s_disp[u] * nE + c0)[w] =
-          reinterpret_cast<const uint32_t*>(buf + (size_t)(B + u) * kSwapStride)[w];
+          reinterpret_cast<const uint32_t*>(buf + (size_t)(b + u) * kSwapStride)[w];
     }
-    for (int e = tid; e < cw * kw; e += kPanelThreads) {
-      const int c = e / kw, w = e - c * kw;
+    for (int e = tid; e < cw * kp; e += kPanelThreads) {
+      const int c = e / kp, t = 2 * (e - c * kp);
       const int col = c0 + c;
-      uint32_t out = 0;
-      if (w < WPR && (col < k0 || col >= k0 + B)) {
-#pragma unroll
-        for (int b8 = 0; b8 < 4; ++b8) {
-          int v = buf[(size_t)(4 * w + b8) * kSwapStride + c];
-          v = v > h ? v - q : v;
-          out |= (uint32_t)(uint8_t)(int8_t)v << (8 * b8);
-        }
+      __half2 out = __floats2half2_rn(0.0f, 0.0f);
+      if (t < b && (col < k0 || col >= k0 + b)) {
+        int v0 = buf[(size_t)t * kSwapStride + c], v1 = buf[(size_t)(t + 1) * kSwapStride + c];
+        v0 = v0 > h ? v0 - q : v0;
+        v1 = v1 > h ? v1 - q : v1;
+        out = __floats2half2_rn((float)v0, (float)v1);
       }
-      *reinterpret_cast<uint32_t*>(Rp + (size_t)col * kb + 4 * w) = out;
+      *reinterpret_cast<__half2*>(Rp + (size_t)col * kb + t) = out;
     }
     __syncthreads();
   }
@@ -360,13 +463,15 @@ constexpr int kUpdThreads = 256;              // 8 warps, each 32 rows x 64 colu
 constexpr int kUpdOutStride = kUpdTile + 16;  // bytes per staged result row (36 words: the 2-byte stores of
                                               // a warp's eight rows fall in distinct banks)
 
-size_t update_smem(int kb) { return (size_t)2 * kUpdTile * (kb + 16) + (size_t)kUpdTile * kUpdOutStride; }
+// Operand rows of kb fp16 plus 16 bytes: kb / 2 + 4 words, so that the eight rows of a fragment load (four
+// words each) fall in distinct banks.
+size_t update_smem(int kb) { return (size_t)2 * kUpdTile * (kb * 2 + 16) + (size_t)kUpdTile * kUpdOutStride; }
 
-// d += a b for one m16n8k32 tile: signed 8-bit operands, 32-bit accumulators.
-__device__ __forceinline__ void mma_s8(int (&d)[4], const uint32_t (&a)[4], uint32_t b0, uint32_t b1) {
+// d += a b for one m16n8k16 tile: fp16 operands, fp32 accumulators.
+__device__ __forceinline__ void mma_f16(float (&d)[4], const uint32_t (&a)[4], uint32_t b0, uint32_t b1) {
   asm volatile(
-      "mma.sync.aligned.m16n8k32.row.col.s32.s8.s8.s32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, {%0,%1,%2,%3};"
-      : "+r"(d[0]), "+r"(d[1]), "+r"(d[2]), "+r"(d[3])
+      "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, {%0,%1,%2,%3};"
+      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
       : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
 }
 
@@ -380,66 +485,67 @@ __device__ __forceinline__ uint32_t add_mod4(uint32_t a, uint32_t b, uint32_t q4
 // The columns outside J of one 128 x 128 tile of one prime's matrix (grid.z =
 // prime): X[i][j] <- base + sum_t W[i][t] RT[j][t] mod q, base = 0 in the
 // pivot rows and X[i][j] elsewhere (the panel kernel has already permuted
-// the rows the swaps moved).  The product runs on balanced residues,
-// |sum| <= kb 125^2 < 2^23, reduced once into [0, q); one modular addition
-// then folds in the base.
-__global__ void __launch_bounds__(kUpdThreads) gj_update_kernel(uint8_t* __restrict__ M, int nE, int k0, int b,
-                                                                int kb, const int8_t* __restrict__ Wb,
-                                                                const int8_t* __restrict__ RT,
+// the rows the swaps moved).  The product runs on the warp-level fp16 tensor
+// MMA with fp32 accumulation, exact here: the balanced residues (|r| <= 125)
+// are fp16 integers and |sum| <= 64 125^2 < 2^24.  One reduction into
+// [0, q), then one modular addition folds in the base.
+__global__ void __launch_bounds__(kUpdThreads, 2) gj_update_kernel(uint8_t* __restrict__ M, int nE, int k0, int b,
+                                                                int kb, const __half* __restrict__ Wb,
+                                                                const __half* __restrict__ RT,
                                                                 const int* __restrict__ sing) {
   extern __shared__ __align__(16) uint8_t sm[];
   const int p = blockIdx.z;
   const int i0 = blockIdx.y * kUpdTile, j0 = blockIdx.x * kUpdTile;
-  const int ls = kb + 16;  // operand row stride: the eight rows of a fragment load fall in distinct banks
-  int8_t* Ws = reinterpret_cast<int8_t*>(sm);
-  int8_t* Rs = Ws + kUpdTile * ls;
-  uint8_t* Cs = reinterpret_cast<uint8_t*>(Rs + kUpdTile * ls);
+  const int lw = kb / 2 + 4;  // operand row stride in 32-bit words
+  uint32_t* Ws = reinterpret_cast<uint32_t*>(sm);
+  uint32_t* Rs = Ws + kUpdTile * lw;
+  uint8_t* Cs = reinterpret_cast<uint8_t*>(Rs + kUpdTile * lw);
   wait_for_predecessor();
   if (sing[p] || (j0 >= k0 && j0 + kUpdTile <= k0 + b)) return;
-  const int8_t* Wp = Wb + (size_t)p * nE * kb;
-  const int8_t* Rp = RT + (size_t)p * nE * kb;
-  const int vr = kb / 16;
+  const __half* Wp = Wb + (size_t)p * nE * kb;
+  const __half* Rp = RT + (size_t)p * nE * kb;
+  const int vr = kb / 8;  // 16-byte vectors per operand row
   for (int e = threadIdx.x; e < kUpdTile * vr; e += kUpdThreads) {
     const int r = e / vr, v = e - r * vr;
     uint4 a = make_uint4(0u, 0u, 0u, 0u), c = a;
-    if (i0 + r < nE) a = *reinterpret_cast<const uint4*>(Wp + (size_t)(i0 + r) * kb + v * 16);
-    if (j0 + r < nE) c = *reinterpret_cast<const uint4*>(Rp + (size_t)(j0 + r) * kb + v * 16);
-    *reinterpret_cast<uint4*>(Ws + r * ls + v * 16) = a;
-    *reinterpret_cast<uint4*>(Rs + r * ls + v * 16) = c;
+    if (i0 + r < nE) a = *reinterpret_cast<const uint4*>(Wp + (size_t)(i0 + r) * kb + v * 8);
+    if (j0 + r < nE) c = *reinterpret_cast<const uint4*>(Rp + (size_t)(j0 + r) * kb + v * 8);
+    *reinterpret_cast<uint4*>(Ws + r * lw + v * 4) = a;
+    *reinterpret_cast<uint4*>(Rs + r * lw + v * 4) = c;
   }
   __syncthreads();
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, g = lane >> 2, c4 = (lane & 3) * 4;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, g = lane >> 2, c4 = lane & 3;
   const int wr = (warp & 3) * 32, wc = (warp >> 2) * 64;
-  int acc[2][8][4] = {};
-  for (int ks = 0; ks < kb; ks += 32) {
+  float acc[2][8][4] = {};
+  for (int ks = 0; ks < kb / 2; ks += 8) {  // 16 fp16 of K = 8 words
     uint32_t a[2][4];
 #pragma unroll
     for (int mi = 0; mi < 2; ++mi) {
-      const int8_t* ap = Ws + (wr + mi * 16 + g) * ls + ks + c4;
-      a[mi][0] = *reinterpret_cast<const uint32_t*>(ap);
-      a[mi][1] = *reinterpret_cast<const uint32_t*>(ap + 8 * ls);
-      a[mi][2] = *reinterpret_cast<const uint32_t*>(ap + 16);
-      a[mi][3] = *reinterpret_cast<const uint32_t*>(ap + 8 * ls + 16);
+      const uint32_t* ap = Ws + (wr + mi * 16 + g) * lw + ks + c4;
+      a[mi][0] = ap[0];
+      a[mi][1] = ap[8 * lw];
+      a[mi][2] = ap[4];
+      a[mi][3] = ap[8 * lw + 4];
     }
 #pragma unroll
     for (int ni = 0; ni < 8; ++ni) {
-      const int8_t* bp = Rs + (wc + ni * 8 + g) * ls + ks + c4;
-      const uint32_t b0 = *reinterpret_cast<const uint32_t*>(bp), b1 = *reinterpret_cast<const uint32_t*>(bp + 16);
+      const uint32_t* bp = Rs + (wc + ni * 8 + g) * lw + ks + c4;
+      const uint32_t b0 = bp[0], b1 = bp[4];
 #pragma unroll
-      for (int mi = 0; mi < 2; ++mi) mma_s8(acc[mi][ni], a[mi], b0, b1);
+      for (int mi = 0; mi < 2; ++mi) mma_f16(acc[mi][ni], a[mi], b0, b1);
     }
   }
   const int q = c_all.q[p];
   const float qf = c_all.qf[p], iq = c_all.invq[p];
-  auto red = [&](int x) {
-    const float v = bal_mod_small((float)x, qf, iq);
+  auto red = [&](float x) {
+    const float v = bal_mod_small(x, qf, iq);
     return (uint32_t)(int)(v < 0.0f ? v + qf : v);
   };
 #pragma unroll
   for (int mi = 0; mi < 2; ++mi)
 #pragma unroll
     for (int ni = 0; ni < 8; ++ni) {
-      const int row = wr + mi * 16 + g, col = wc + ni * 8 + (lane & 3) * 2;
+      const int row = wr + mi * 16 + g, col = wc + ni * 8 + c4 * 2;
       *reinterpret_cast<uint16_t*>(Cs + row * kUpdOutStride + col) =
           (uint16_t)(red(acc[mi][ni][0]) | red(acc[mi][ni][1]) << 8);
       *reinterpret_cast<uint16_t*>(Cs + (row + 8) * kUpdOutStride + col) =
@@ -463,45 +569,35 @@ __global__ void __launch_bounds__(kUpdThreads) gj_update_kernel(uint8_t* __restr
   allow_dependents();
 }
 
-// Undo the column swaps and write the balanced int8 inverse planes of the
-// lift's primes: Binv[s][i][j] = bal(M[map[s]][i][sigma(j)]) for i, j < n,
-// rows of nE bytes (zero past n).  The padded block stays the identity, so
-// sigma maps the first n columns among themselves.
+// The lift's primes, in order: map[s] = index of the s-th prime kept.
 struct PrimeMap {
   int idx[kNumPrimes];
 };
 
-// sigma[s] = the column order that undoes prime map[s]'s row swaps (the
-// swaps applied to the identity in reverse order); one block per prime.
-__global__ void gj_sigma_kernel(const int* __restrict__ perm, int nE, PrimeMap map, int* __restrict__ sigma_all) {
-  const int s = blockIdx.x, p = map.idx[s];
-  int* sigma = sigma_all + (long long)s * nE;
-  for (int j = threadIdx.x; j < nE; j += blockDim.x) sigma[j] = j;
-  __syncthreads();
-  if (threadIdx.x == 0)
-    for (int k = nE - 1; k >= 0; --k) {
-      const int r = perm[p * nE + k];
-      const int t = sigma[k];
-      sigma[k] = sigma[r];
-      sigma[r] = t;
-    }
-}
-
-__global__ void __launch_bounds__(256) gj_finish_kernel(const uint8_t* __restrict__ M, const int* __restrict__ sigma_all,
+// Undoes the row swaps, which act on the in-place result as column swaps,
+// and writes the balanced int8 inverse planes of the lift's primes: column c
+// of M[map[s]] is column rowsrc[c] of the inverse, Binv[s][i][rowsrc[c]] =
+// bal(M[map[s]][i][c]) for i < n, in rows of nE bytes (zero past n).  The
+// padded block keeps its identity rows in place, so rowsrc maps the first n
+// columns among themselves.  Each block stages whole rows in shared memory.
+__global__ void __launch_bounds__(256) gj_finish_kernel(const uint8_t* __restrict__ M, const int* __restrict__ rowsrc,
                                                         int n, int nE, PrimeMap map, int8_t* __restrict__ Binv) {
+  __shared__ __align__(16) int8_t out[kMaxSolveN];
   const int s = blockIdx.y, p = map.idx[s];
-  const int* sigma = sigma_all + (long long)s * nE;
-  const long long nn = (long long)nE * nE;
   const int q = c_all.q[p], h = (q - 1) / 2;
-  for (long long e = (long long)blockIdx.x * blockDim.x + threadIdx.x; e < (long long)n * nE;
-       e += (long long)gridDim.x * blockDim.x) {
-    const int i = (int)(e / nE), j = (int)(e - (long long)i * nE);
-    int v = 0;
-    if (j < n) {
-      v = M[p * nn + (long long)i * nE + sigma[j]];
-      v = v > h ? v - q : v;
+  const int* rs = rowsrc + (size_t)p * nE;
+  for (int j = n + threadIdx.x; j < nE; j += blockDim.x) out[j] = 0;
+  for (int i = blockIdx.x; i < n; i += gridDim.x) {
+    const uint8_t* row = M + ((size_t)p * nE + i) * nE;
+    for (int c = threadIdx.x; c < n; c += blockDim.x) {
+      const int v = row[c];
+      out[rs[c]] = (int8_t)(v > h ? v - q : v);
     }
-    Binv[(long long)s * n * nE + e] = (int8_t)v;
+    __syncthreads();
+    int8_t* dst = Binv + ((size_t)s * n + i) * nE;
+    for (int v = threadIdx.x; v < nE / 16; v += blockDim.x)
+      reinterpret_cast<uint4*>(dst)[v] = reinterpret_cast<const uint4*>(out)[v];
+    __syncthreads();
   }
 }
 
@@ -641,8 +737,8 @@ unsigned grid_for(long long items, int per_block = 256) {
   return (unsigned)std::max(1LL, std::min(b, cap));
 }
 
-// The panel kernels' dynamic shared memory above the default 48 KB, set once
-// per device.
+// The panel and update kernels' dynamic shared memory above the default
+// 48 KB, set once per device.
 cudaError_t allow_panel_smem() {
   static std::mutex mu;
   static bool done[64];
@@ -653,10 +749,12 @@ cudaError_t allow_panel_smem() {
   std::lock_guard<std::mutex> lock(mu);
   if (done[dev]) return cudaSuccess;
   const int bytes = (int)kPanelSmemLimit;
-  e = cudaFuncSetAttribute(gj_panel_kernel<64>, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
-  if (e == cudaSuccess) e = cudaFuncSetAttribute(gj_panel_kernel<48>, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
-  if (e == cudaSuccess) e = cudaFuncSetAttribute(gj_panel_kernel<32>, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
-  if (e == cudaSuccess) e = cudaFuncSetAttribute(gj_panel_kernel<16>, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+  const cudaFuncAttribute attr = cudaFuncAttributeMaxDynamicSharedMemorySize;
+  e = cudaFuncSetAttribute(gj_panel_kernel<64, 16, 1>, attr, bytes);
+  if (e == cudaSuccess) e = cudaFuncSetAttribute(gj_panel_kernel<64, 8, 2>, attr, bytes);
+  if (e == cudaSuccess) e = cudaFuncSetAttribute(gj_panel_kernel<32, 8, 4>, attr, bytes);
+  if (e == cudaSuccess) e = cudaFuncSetAttribute(gj_panel_kernel<16, 4, 8>, attr, bytes);
+  if (e == cudaSuccess) e = cudaFuncSetAttribute(gj_update_kernel, attr, (int)update_smem(64));
   if (e == cudaSuccess) done[dev] = true;
   return e;
 }
@@ -719,8 +817,17 @@ extern "C" int rg_solve_i64(const int64_t* A_in, const int64_t* B_in, int64_t n6
   double* bcols = cols + n;
   unsigned long long* maxabs = reinterpret_cast<unsigned long long*>(bcols + c);
   SOLVE_TRY(cudaMemsetAsync(maxabs, 0, 8, st));
-  norms_kernel<<<(unsigned)((std::max((long long)n * 32, (long long)n + c) + 255) / 256), 256, 0, st>>>(
-      A, B, n, c, rows, cols, bcols, maxabs);
+  const int rows_per = std::max(32, (n + 63) / 64), chunks = (n + rows_per - 1) / rows_per;
+  DevBuf dpart;
+  SOLVE_TRY(dpart.alloc((size_t)chunks * n * 8, st));
+  norms_kernel<<<(unsigned)((std::max((long long)n * 32, (long long)c) + 255) / 256), 256, 0, st>>>(A, B, n, c, rows,
+                                                                                                     bcols, maxabs);
+  SOLVE_TRY(cudaGetLastError());
+  col_norms_part_kernel<<<dim3((unsigned)((n + 255) / 256), (unsigned)chunks), 256, 0, st>>>(
+      A, n, rows_per, static_cast<double*>(dpart.p));
+  SOLVE_TRY(cudaGetLastError());
+  col_norms_sum_kernel<<<(unsigned)((n + 255) / 256), 256, 0, st>>>(static_cast<const double*>(dpart.p), n, chunks,
+                                                                     cols);
   SOLVE_TRY(cudaGetLastError());
   std::vector<double> hn((size_t)2 * n + c + 1);
   SOLVE_TRY(cudaMemcpyAsync(hn.data(), dn.p, hn.size() * 8, cudaMemcpyDeviceToHost, st));
@@ -751,41 +858,39 @@ extern "C" int rg_solve_i64(const int64_t* A_in, const int64_t* B_in, int64_t n6
   // 2. batched inverse, on diag(A, I) of order nE = n rounded up to 16
   const int nE = (n + 15) / 16 * 16, ld = nE;
   const size_t nnE = (size_t)nE * nE;
-  const int bw = panel_width(nE), kbw = (bw + 31) / 32 * 32;
-  DevBuf dM, dW, dRT, dperm, dsing;
+  const PanelCfg pc = panel_cfg(nE);
+  const int bw = pc.B, kbw = (bw + 31) / 32 * 32;
+  DevBuf dM, dW, dRT, drowsrc, dsing;
   SOLVE_TRY(dM.alloc((size_t)kNumPrimes * nnE, st));
-  SOLVE_TRY(dW.alloc((size_t)kNumPrimes * nE * kbw, st));
-  SOLVE_TRY(dRT.alloc((size_t)kNumPrimes * nE * kbw, st));
-  SOLVE_TRY(dperm.alloc((size_t)kNumPrimes * nE * 4, st));
+  SOLVE_TRY(dW.alloc((size_t)kNumPrimes * nE * kbw * 2, st));
+  SOLVE_TRY(dRT.alloc((size_t)kNumPrimes * nE * kbw * 2, st));
+  SOLVE_TRY(drowsrc.alloc((size_t)kNumPrimes * nE * 4, st));
   SOLVE_TRY(dsing.alloc(kNumPrimes * 4, st));
   uint8_t* M = static_cast<uint8_t*>(dM.p);
-  int8_t* Wb = static_cast<int8_t*>(dW.p);
-  int8_t* RT = static_cast<int8_t*>(dRT.p);
-  int* perm = static_cast<int*>(dperm.p);
+  __half* Wb = static_cast<__half*>(dW.p);
+  __half* RT = static_cast<__half*>(dRT.p);
+  int* rowsrc = static_cast<int*>(drowsrc.p);
   int* sing = static_cast<int*>(dsing.p);
   SOLVE_TRY(cudaMemsetAsync(sing, 0, kNumPrimes * 4, st));
-  gj_init_kernel<<<grid_for((long long)nnE), 256, 0, st>>>(A, n, nE, M);
+  gj_init_kernel<<<grid_for((long long)nnE), 256, 0, st>>>(A, n, nE, M, rowsrc);
   SOLVE_TRY(cudaGetLastError());
   SOLVE_TRY(allow_panel_smem());
   const unsigned tiles = (unsigned)((nE + kUpdTile - 1) / kUpdTile);
   for (int k0 = 0; k0 < nE; k0 += bw) {
     const int b = std::min(bw, nE - k0), kb = (b + 31) / 32 * 32;  // b: a multiple of 16
-    const size_t smem = panel_smem(nE, b);
-    if (b == 64)
-      SOLVE_TRY(launch_dependent(gj_panel_kernel<64>, dim3(kNumPrimes), dim3(kPanelThreads), smem, st, M, nE, k0, kb,
-                                 Wb, RT, perm, sing));
-    else if (b == 48)
-      SOLVE_TRY(launch_dependent(gj_panel_kernel<48>, dim3(kNumPrimes), dim3(kPanelThreads), smem, st, M, nE, k0, kb,
-                                 Wb, RT, perm, sing));
-    else if (b == 32)
-      SOLVE_TRY(launch_dependent(gj_panel_kernel<32>, dim3(kNumPrimes), dim3(kPanelThreads), smem, st, M, nE, k0, kb,
-                                 Wb, RT, perm, sing));
+    const size_t smem = panel_smem(nE, bw);
+    const dim3 pg(kNumPrimes), pt(kPanelThreads);
+    if (pc.RPT == 1)
+      SOLVE_TRY(launch_dependent(gj_panel_kernel<64, 16, 1>, pg, pt, smem, st, M, nE, k0, b, kb, Wb, RT, rowsrc, sing));
+    else if (pc.RPT == 2)
+      SOLVE_TRY(launch_dependent(gj_panel_kernel<64, 8, 2>, pg, pt, smem, st, M, nE, k0, b, kb, Wb, RT, rowsrc, sing));
+    else if (pc.RPT == 4)
+      SOLVE_TRY(launch_dependent(gj_panel_kernel<32, 8, 4>, pg, pt, smem, st, M, nE, k0, b, kb, Wb, RT, rowsrc, sing));
     else
-      SOLVE_TRY(launch_dependent(gj_panel_kernel<16>, dim3(kNumPrimes), dim3(kPanelThreads), smem, st, M, nE, k0, kb,
-                                 Wb, RT, perm, sing));
+      SOLVE_TRY(launch_dependent(gj_panel_kernel<16, 4, 8>, pg, pt, smem, st, M, nE, k0, b, kb, Wb, RT, rowsrc, sing));
     if (b < nE)
       SOLVE_TRY(launch_dependent(gj_update_kernel, dim3(tiles, tiles, kNumPrimes), dim3(kUpdThreads),
-                                 update_smem(kb), st, M, nE, k0, b, kb, (const int8_t*)Wb, (const int8_t*)RT,
+                                 update_smem(kb), st, M, nE, k0, b, kb, (const __half*)Wb, (const __half*)RT,
                                  (const int*)sing));
   }
   int hsing[kNumPrimes];
@@ -804,14 +909,10 @@ extern "C" int rg_solve_i64(const int64_t* A_in, const int64_t* B_in, int64_t n6
   Tables sol;
   build_tables_for(qs.data(), E, &sol);
   SOLVE_TRY(cudaMemcpyToSymbolAsync(c_sol, &sol, sizeof(Tables), 0, cudaMemcpyHostToDevice, st));
-  DevBuf dBinv, dsigma;
+  DevBuf dBinv;
   SOLVE_TRY(dBinv.alloc((size_t)E * n * ld, st));
-  SOLVE_TRY(dsigma.alloc((size_t)E * nE * 4, st));
   int8_t* Binv = static_cast<int8_t*>(dBinv.p);
-  int* sigma = static_cast<int*>(dsigma.p);
-  gj_sigma_kernel<<<E, 256, 0, st>>>(perm, nE, map, sigma);
-  SOLVE_TRY(cudaGetLastError());
-  gj_finish_kernel<<<dim3(grid_for((long long)n * ld), E), 256, 0, st>>>(M, sigma, n, nE, map, Binv);
+  gj_finish_kernel<<<dim3((unsigned)std::min(n, 128), E), 256, 0, st>>>(M, rowsrc, n, nE, map, Binv);
   SOLVE_TRY(cudaGetLastError());
 
   // 3. the lift

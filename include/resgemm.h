@@ -345,8 +345,9 @@ int rg_get_plan(const void* ws, void* stream, rg_plan_info* out);
  * (row-major int64; device pointers, or host pointers with RG_FLAG_HOST)
  * ("exact-solve", Method).
  *  1. A^-1 mod q for all 53 primes at once by Gauss-Jordan elimination on the
- *     GPU, one launch per elimination step over all primes; the primes that
- *     divide det(A) are dropped.
+ *     GPU, over all primes in each launch, blocked: per block of up to 64
+ *     pivots, one panel factorisation and one INT8 tensor-core update of the
+ *     other columns; the primes that divide det(A) are dropped.
  *  2. Dixon's p-adic lift with P = the product of the remaining primes:
  *     X_i = A^-1 R_i mod P per prime, then balanced Garner into the base-P
  *     digit; R_{i+1} = (R_i - A X_i) P^-1 mod 2^64, exact in one limb; as
@@ -490,7 +491,9 @@ int rg_set_gemm_variant(int variant);
  *           be even (0: the SM count rounded down to even);
  *         RG_PROBE_TCGEN05_F16_PAIR_BMN_SYNC: the pair form with the residue
  *           GEMM's per-k-block issue loop (a barrier wait and a commit every
- *           four MMAs), without data movement.
+ *           four MMAs), without data movement;
+ *         RG_PROBE_MMA_F16: warp-level mma.sync m16n8k16 f16 x f16 -> f32,
+ *           otherwise as RG_PROBE_MMA_S8.
  *   iters  rounds per warp or CTA (1 .. 2^24): 8 MMAs per round for
  *          mma.sync, 4 for tcgen05 (K = 64 fp16 or 128 E4M3 per round;
  *          *ops_per_launch counts 128 rows per CTA for the pair forms too).
@@ -506,6 +509,7 @@ int rg_set_gemm_variant(int variant);
 #define RG_PROBE_TCGEN05_F16_PAIR 4
 #define RG_PROBE_TCGEN05_F16_PAIR_BMN 5
 #define RG_PROBE_TCGEN05_F16_PAIR_BMN_SYNC 6
+#define RG_PROBE_MMA_F16 7
 int rg_probe_mma_rate(int kind, int blocks, int iters, void* ws, size_t ws_bytes, void* stream,
                       double* ops_per_launch);
 

@@ -198,6 +198,6 @@ def test_probe_rejects_bad_arguments_before_the_device(rg):
     ops = ctypes.c_double(0.0)
     # no workspace, or an unknown probe kind with no workspace: refused before any CUDA call
     assert lib.rg_probe_mma_rate(rg.RG_PROBE_MMA_S8, 0, 10, None, 4096, None, ctypes.byref(ops)) == rg.RG_ERR_ARG
-    assert lib.rg_probe_mma_rate(7, 0, 10, None, 4096, None, ctypes.byref(ops)) == rg.RG_ERR_ARG
+    assert lib.rg_probe_mma_rate(8, 0, 10, None, 4096, None, ctypes.byref(ops)) == rg.RG_ERR_ARG
     assert lib.rg_probe_mma_rate(rg.RG_PROBE_MMA_S8, 0, 10, 256, 4096, None, None) == rg.RG_ERR_ARG
     assert lib.rg_probe_mma_rate(rg.RG_PROBE_MMA_S8, 0, 10, 256, 128, None, ctypes.byref(ops)) == rg.RG_ERR_ARG

@@ -24,6 +24,7 @@ def test_probes_run_and_count_their_work(rg):
         (rg.RG_PROBE_TCGEN05_F16_PAIR, 64, 0, 2.0 * (sms & ~1) * 64 * 4 * 128 * 256 * 16),
         (rg.RG_PROBE_TCGEN05_F16_PAIR_BMN, 64, 2, 2.0 * 2 * 64 * 4 * 128 * 256 * 16),
         (rg.RG_PROBE_TCGEN05_F16_PAIR_BMN_SYNC, 64, 0, 2.0 * (sms & ~1) * 64 * 4 * 128 * 256 * 16),
+        (rg.RG_PROBE_MMA_F16, 100, 0, 2.0 * 4 * sms * 8 * 100 * 8 * 16 * 8 * 16),
     ]
     for kind, iters, blocks, want in cases:
         ops = rg.probe_mma_rate(kind, iters, blocks)
@@ -33,7 +34,7 @@ def test_probes_run_and_count_their_work(rg):
 
 
 def test_probe_arguments_are_checked(rg):
-    for kind, iters, blocks in ((7, 10, 0), (rg.RG_PROBE_MMA_S8, 0, 0), (rg.RG_PROBE_MMA_S8, 10, -1),
+    for kind, iters, blocks in ((8, 10, 0), (rg.RG_PROBE_MMA_S8, 0, 0), (rg.RG_PROBE_MMA_S8, 10, -1),
                                 (rg.RG_PROBE_TCGEN05_F16_PAIR, 10, 3)):
         with pytest.raises(rg.ResGemmError) as e:
             rg.probe_mma_rate(kind, iters, blocks)

@@ -164,3 +164,17 @@ def test_primes_dividing_det_found_in_later_pivot_blocks(rg):
     assert 3 not in kept and 5 not in kept and 7 not in kept
     assert info["primes"] == len(kept)
     assert integer_identity(A, X, b)
+
+
+@pytest.mark.parametrize("n", [1100, 2100, 4200])
+def test_planted_solution_at_every_panel_shape(rg, n):
+    """Orders past 1024, 2048 and 4096 rows, where the elimination's panel kernel holds 2, 4 and 8 rows per thread
+    with blocks of 64, 32 and 16 pivots: a planted integer solution comes back exactly."""
+    rng = np.random.default_rng(20 + n)
+    A = rng.integers(-(2**10), 2**10, size=(n, n), dtype=np.int64)
+    x = rng.integers(-(2**10), 2**10, size=(n, 1), dtype=np.int64)
+    b = A @ x  # |entries| < n 2^20: exact in int64
+    info = {}
+    N, d = rg.solve_integers(dev(A), dev(b), info=info)
+    assert d == 1
+    assert [row[0] for row in N] == [int(v) for v in x[:, 0]]
