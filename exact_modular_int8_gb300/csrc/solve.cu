@@ -2,13 +2,14 @@
 // residue engine ("exact-solve" page, Method):
 //   1. A^-1 mod q for every prime q < 256 at once, by Gauss-Jordan
 //      elimination over all primes, blocked: per block of pivots, one panel
-//      factorisation in shared memory and one INT8 tensor-core update;
+//      factorisation in shared memory and one tensor-core update;
 //   2. Dixon's p-adic lift with the modulus P = the product of the primes that
 //      do not divide det(A): X_i = A^-1 R_i mod P (per prime, then balanced
 //      Garner into the wide base-P digit), R_{i+1} = (R_i - A X_i) / P formed
 //      in one 64-bit limb as (R_i - A X_i) P^-1 mod 2^64 (P odd);
-//   3. on the host, rational reconstruction of one component for the common
-//      denominator, then one modular product per numerator.
+//   3. rational reconstruction of a few components on host threads for the
+//      common denominator, then every component's value and numerator on the
+//      GPU (recon.cu).
 #include <cuda_fp16.h>
 #include <cuda_runtime.h>
 
@@ -22,6 +23,7 @@
 #include <vector>
 
 #include "bigint.h"
+#include "recon.h"
 #include "rg_garner.cuh"
 #include "rg_kernels.h"
 
@@ -700,6 +702,19 @@ __global__ void __launch_bounds__(256) lift_update_kernel(const int64_t* __restr
 // Host side
 // ---------------------------------------------------------------------------
 
+// The little-endian 32-bit words of a (no leading zero word; at least
+// min_words, zero-padded).
+std::vector<uint32_t> words_of(const big::Nat& a, size_t min_words = 0) {
+  std::vector<uint32_t> w(a.v.size() * 2);
+  for (size_t i = 0; i < a.v.size(); ++i) {
+    w[2 * i] = (uint32_t)a.v[i];
+    w[2 * i + 1] = (uint32_t)(a.v[i] >> 32);
+  }
+  while (!w.empty() && w.back() == 0) w.pop_back();
+  if (w.size() < min_words) w.resize(min_words, 0);
+  return w;
+}
+
 struct DevBuf {  // stream-ordered device allocation
   void* p = nullptr;
   cudaStream_t s = nullptr;
@@ -929,6 +944,31 @@ extern "C" int rg_solve_i64(const int64_t* A_in, const int64_t* B_in, int64_t n6
   unsigned long long P64 = 1;
   for (int q : qs) P64 *= (unsigned long long)q;  // P mod 2^64
   const unsigned long long pinv64 = inverse_mod_2_64(P64);
+  // P^m, the powers P^i (i < m) and Barrett's constant for P^m, as 32-bit
+  // words, built on a host thread while the GPU lifts.
+  std::vector<uint32_t> pow_words, PMw, MUw;
+  std::vector<int> pow_idx(2 * (size_t)steps);  // offsets, then lengths
+  big::Nat Pm;
+  std::thread tables([&] {
+    Pm = big::from_u64(1);
+    for (int i = 0; i < steps; ++i) {
+      const std::vector<uint32_t> w = words_of(Pm);
+      pow_idx[i] = (int)pow_words.size();
+      pow_idx[steps + i] = (int)w.size();
+      pow_words.insert(pow_words.end(), w.begin(), w.end());
+      Pm = big::mul(Pm, Pn);
+    }
+    PMw = words_of(Pm);
+    big::Nat mu;
+    big::divmod(big::pow2((size_t)64 * PMw.size()), Pm, &mu, nullptr);
+    MUw = words_of(mu, PMw.size() + 1);
+  });
+  struct Joiner {  // the thread is joined on every return path
+    std::thread& t;
+    ~Joiner() {
+      if (t.joinable()) t.join();
+    }
+  } joiner{tables};
   DevBuf dR, dRr, dRC, dX, dlow;
   SOLVE_TRY(dR.alloc((size_t)n * c * 8, st));
   SOLVE_TRY(dRr.alloc((size_t)E * c * ld, st));
@@ -951,29 +991,64 @@ extern "C" int rg_solve_i64(const int64_t* A_in, const int64_t* B_in, int64_t n6
     SOLVE_TRY(launch_dependent(lift_update_kernel, dim3((unsigned)(((long long)n * 32 + 255) / 256)), dim3(256), 0, st,
                                A, n, c, (const unsigned long long*)dlow.p, pinv64, R));
   }
+  // 4. Reconstruction (exact-solve, Method).  The components' values and
+  // numerators are formed on the GPU; the common denominator D comes from a
+  // few components' rational reconstructions on host threads.  The tables
+  // of P^m were built by a host thread while the lift ran.
+  const long long comps = (long long)n * c;
+  // the digits to the host, for the sampled components
   std::vector<uint32_t> hX((size_t)steps * n * c * kW);
   SOLVE_TRY(cudaMemcpyAsync(hX.data(), X, hX.size() * 4, cudaMemcpyDeviceToHost, st));
   SOLVE_TRY(cudaStreamSynchronize(st));
   const double ms_lift = ms_since(t1);
   const auto t2 = clock::now();
-
-  // 4. rational reconstruction on the host
-  const big::Nat Pm = [&] {
-    big::Nat r = big::from_u64(1);
-    for (int i = 0; i < steps; ++i) r = big::mul(r, Pn);
-    return r;
-  }();
+  tables.join();
+  const int kP = (int)PMw.size();
+  const std::vector<uint32_t> Pw = words_of(Pn, kW);
   const big::Nat nbound = big::pow2((size_t)std::ceil(nbits));
   const big::Nat dbound = big::pow2((size_t)std::ceil(dbits));
-  big::Nat half;
-  big::divmod(Pm, big::from_u64(2), &half, nullptr);
-  const long long comps = (long long)n * c;
-  const size_t pl = Pn.v.size();  // limbs of P (<= 6)
-  // X_k = sum_i x_i P^i mod P^m, from the balanced digits normalised to
-  // [0, P) by borrow propagation (a final borrow is a multiple of P^m), then
+  const int bound_bits = (int)std::ceil(nbits);
+  const int wDmax = (int)(words_of(dbound).size());
+  const int blocks = recon_blocks(comps);
+  DevBuf dtab, dtabi, dY, dN, dD, dinfo, dscr;
+  const size_t ntab = pow_words.size() + Pw.size() + PMw.size() + MUw.size();
+  SOLVE_TRY(dtab.alloc(ntab * 4, st));
+  SOLVE_TRY(dtabi.alloc(pow_idx.size() * 4, st));
+  uint32_t* tabp = static_cast<uint32_t*>(dtab.p);
+  int* tabi = static_cast<int*>(dtabi.p);
+  ReconTables tab;
+  tab.pow = tabp;
+  tab.P = tabp + pow_words.size();
+  tab.PM = tab.P + Pw.size();
+  tab.MU = tab.PM + PMw.size();
+  tab.pow_off = tabi;
+  tab.pow_len = tabi + steps;
+  tab.pw = kW;
+  tab.m = steps;
+  tab.k = kP;
+  SOLVE_TRY(cudaMemcpyAsync(tabp, pow_words.data(), pow_words.size() * 4, cudaMemcpyHostToDevice, st));
+  SOLVE_TRY(cudaMemcpyAsync(const_cast<uint32_t*>(tab.P), Pw.data(), Pw.size() * 4, cudaMemcpyHostToDevice, st));
+  SOLVE_TRY(cudaMemcpyAsync(const_cast<uint32_t*>(tab.PM), PMw.data(), PMw.size() * 4, cudaMemcpyHostToDevice, st));
+  SOLVE_TRY(cudaMemcpyAsync(const_cast<uint32_t*>(tab.MU), MUw.data(), MUw.size() * 4, cudaMemcpyHostToDevice, st));
+  SOLVE_TRY(cudaMemcpyAsync(tabi, pow_idx.data(), pow_idx.size() * 4, cudaMemcpyHostToDevice, st));
+  SOLVE_TRY(dY.alloc((size_t)comps * kP * 4, st));
+  SOLVE_TRY(dN.alloc((size_t)comps * (kP + 2) * 4, st));
+  SOLVE_TRY(dD.alloc((size_t)wDmax * 4, st));
+  SOLVE_TRY(dinfo.alloc((size_t)comps * 4, st));
+  SOLVE_TRY(dscr.alloc(recon_scratch_bytes(tab, wDmax, blocks), st));
+  uint32_t* Yv = static_cast<uint32_t*>(dY.p);
+  uint32_t* Nw = static_cast<uint32_t*>(dN.p);
+  int* info = static_cast<int*>(dinfo.p);
+  uint32_t* scr = static_cast<uint32_t*>(dscr.p);
+  SOLVE_TRY(recon_values(X, comps, tab, Yv, scr, st));
+
+  // X_k = sum_i x_i P^i mod P^m on the host, for the sampled components and
+  // any whose denominator D misses: the balanced digits normalised to [0, P)
+  // by borrow propagation (a final borrow is a multiple of P^m), then
   // converted by halves with the powers P^(2^j) (big::radix_value).
+  const size_t pl = Pn.v.size();  // limbs of P (<= 6)
   struct Scratch {
-    std::vector<big::Limb> acc, tmp, un, prod;
+    std::vector<big::Limb> acc;
     std::vector<big::Limb> z;  // normalised digits, m x pl limbs
   };
   std::vector<big::Nat> pw(1, Pn);  // P^(2^j) for every 2^j below the step count
@@ -989,49 +1064,28 @@ extern "C" int rg_solve_i64(const int64_t* A_in, const int64_t* B_in, int64_t n6
       std::copy(zi.v.begin(), zi.v.end(), S.z.begin() + (size_t)i * pl);
     }
     big::radix_value(S.z.data(), (size_t)steps, pl, pw, S.acc);
-    big::Nat X;
-    X.v = S.acc;
-    big::trim(X);
-    return X;
+    big::Nat Xk;
+    Xk.v = S.acc;
+    big::trim(Xk);
+    return Xk;
   };
-  const big::Barrett bar = big::make_barrett(Pm);
-  std::vector<big::Nat> Xv(comps);
+  // The denominators of a few components, one host thread each while the
+  // GPU forms the values, give the common denominator D: their lcm divides
+  // det A, and a factor cancelled in one component's fraction rarely cancels
+  // in all of them.
   const int nthreads = std::max(1, std::min((int)std::thread::hardware_concurrency(), 64));
-  std::vector<Scratch> scratch(nthreads + 4);
-  auto parallel_from = [&](long long first, auto&& fn) {
-    std::vector<std::thread> th;
-    for (int w = 0; w < nthreads; ++w)
-      th.emplace_back([&, w] {
-        for (long long k = first + w; k < comps; k += nthreads) fn(k, scratch[w]);
-      });
-    for (auto& t : th) t.join();
-  };
-  auto parallel = [&](auto&& fn) { parallel_from(0, fn); };
-  // The denominators of a few components, reconstructed concurrently with
-  // the remaining components' values, give the common denominator D: their
-  // lcm divides det A, and a factor cancelled in one component's fraction
-  // rarely cancels in all of them.
-  // Each sampling thread forms its component's value and reconstructs it,
-  // then joins the other threads on the remaining values, which every
-  // thread takes one at a time from a shared counter.
   const long long sample = std::min<long long>(comps, std::max(1, std::min(4, nthreads / 2)));
   std::vector<big::Nat> Ds(sample);
   std::vector<char> rec_ok(sample, 0);
   {
-    std::atomic<long long> next{sample};
-    auto values = [&](Scratch& S) {
-      for (long long k = next.fetch_add(1); k < comps; k = next.fetch_add(1)) Xv[k] = value_of(k, S);
-    };
     std::vector<std::thread> th;
     for (long long k = 0; k < sample; ++k)
       th.emplace_back([&, k] {
-        Xv[k] = value_of(k, scratch[k]);
+        Scratch S;
+        const big::Nat Xk = value_of(k, S);
         big::Int Nk;
-        rec_ok[k] = big::rational_reconstruct(Xv[k], Pm, nbound, dbound, &Nk, &Ds[k]);
-        values(scratch[k]);
+        rec_ok[k] = big::rational_reconstruct(Xk, Pm, nbound, dbound, &Nk, &Ds[k]);
       });
-    const int rest = std::max(1, nthreads - (int)sample);
-    for (int w = 0; w < rest; ++w) th.emplace_back([&, w] { values(scratch[sample + w]); });
     for (auto& t : th) t.join();
   }
   big::Nat D = big::from_u64(1);
@@ -1041,48 +1095,43 @@ extern "C" int rg_solve_i64(const int64_t* A_in, const int64_t* B_in, int64_t n6
     big::divmod(Ds[k], big::gcd(D, Ds[k]), &t, nullptr);
     D = big::mul(D, t);
   }
-  // N_k = D X_k mod P^m, balanced, for every k.  A component whose N_k
-  // exceeds the numerator bound has a denominator not dividing D: its own
-  // reconstruction extends D by the missing factor t, and the numerators
-  // already found scale by t (each stays <= |det A_k| since D still divides
-  // det A).
-  std::vector<big::Int> Nv(comps);
-  std::vector<char> fits(comps, 0);
-  auto numerator = [&](long long k, Scratch& S) {
-    // D X_k < (P^m)^2: a Karatsuba product, then Barrett's reduction modulo P^m
-    big::kmul_into(D.v.data(), D.v.size(), Xv[k].v.data(), Xv[k].v.size(), S.prod);
-    big::Nat y;
-    if (!big::reduce_barrett(bar, S.prod.data(), S.prod.size(), S.un, S.tmp, &y)) {
-      fits[k] = 0;  // not reached: D <= dbound < P^m and X_k < P^m
-      return;
-    }
-    big::Int v;
-    if (big::cmp(y, half) > 0) {
-      v.mag = big::sub(Pm, y);
-      v.neg = !big::is_zero(v.mag);
-    } else {
-      v.mag = y;
-    }
-    fits[k] = big::cmp(v.mag, nbound) <= 0;
-    Nv[k] = v;
+  // N_k = D X_k mod P^m, balanced, for every k, on the GPU.  A component
+  // whose N_k exceeds the numerator bound has a denominator not dividing D:
+  // its own reconstruction extends D by the missing factor, and the
+  // numerators are formed again (each stays <= |det A_k|, since D still
+  // divides det A).
+  std::vector<int> hinfo(comps);
+  auto numerators = [&]() -> int {
+    const std::vector<uint32_t> Dw = words_of(D);
+    if ((int)Dw.size() > wDmax) return RG_ERR_RANGE;  // not reached: D <= dbound
+    SOLVE_TRY(cudaMemcpyAsync(dD.p, Dw.data(), Dw.size() * 4, cudaMemcpyHostToDevice, st));
+    SOLVE_TRY(recon_numerators(Yv, comps, tab, static_cast<const uint32_t*>(dD.p), (int)Dw.size(), bound_bits, Nw,
+                               info, scr, st));
+    SOLVE_TRY(cudaMemcpyAsync(hinfo.data(), info, (size_t)comps * 4, cudaMemcpyDeviceToHost, st));
+    SOLVE_TRY(cudaStreamSynchronize(st));
+    return RG_OK;
   };
-  parallel(numerator);
+  int rc = numerators();
+  if (rc != RG_OK) return rc;
   for (long long k = 0; k < comps; ++k) {
-    if (fits[k]) continue;
+    if (hinfo[k] >= 0) continue;
+    Scratch S;
+    const big::Nat Xk = value_of(k, S);
     big::Int Nk;
     big::Nat Dk;
-    if (!big::rational_reconstruct(Xv[k], Pm, nbound, dbound, &Nk, &Dk)) return RG_ERR_RANGE;
+    if (!big::rational_reconstruct(Xk, Pm, nbound, dbound, &Nk, &Dk)) return RG_ERR_RANGE;
     big::Nat t;
     big::divmod(Dk, big::gcd(D, Dk), &t, nullptr);
     D = big::mul(D, t);
-    for (long long j = 0; j < k; ++j) Nv[j] = big::mul(Nv[j], t);
-    parallel_from(k, numerator);  // the rest, against the new D
-    if (!fits[k]) return RG_ERR_RANGE;
+    rc = numerators();
+    if (rc != RG_OK) return rc;
+    if (hinfo[k] < 0) return RG_ERR_RANGE;
   }
-  // the numerators and the denominator as limbs
+  // the numerators and the denominator as limbs: the low limbs of each
+  // numerator's two's complement words
   size_t maxbits = big::bit_length(D);
-  for (const auto& v : Nv) maxbits = std::max(maxbits, big::bit_length(v.mag));
-  const int limbs = (int)(maxbits / 64 + 1);
+  for (long long k = 0; k < comps; ++k) maxbits = std::max(maxbits, (size_t)hinfo[k]);
+  const int limbs = (int)(maxbits / 64 + 1);  // <= (kP + 2) / 2: |N|, D < P^m < 2^(32 kP)
   out->n = n;
   out->c = c;
   out->limbs = limbs;
@@ -1091,11 +1140,12 @@ extern "C" int rg_solve_i64(const int64_t* A_in, const int64_t* B_in, int64_t n6
   out->ms_inverse = ms_inverse;
   out->ms_lift = ms_lift;
   out->values = new int64_t[(size_t)(comps + 1) * limbs];
-  for (long long k = 0; k < comps; ++k)
-    if (!big::to_limbs(Nv[k], out->values + (size_t)k * limbs, limbs)) {
-      rg_solution_free(out);
-      return RG_ERR_RANGE;
-    }
+  if (cudaMemcpy2DAsync(out->values, (size_t)limbs * 8, Nw, (size_t)(kP + 2) * 4, (size_t)limbs * 8, (size_t)comps,
+                        cudaMemcpyDeviceToHost, st) != cudaSuccess ||
+      cudaStreamSynchronize(st) != cudaSuccess) {
+    rg_solution_free(out);
+    return RG_ERR_CUDA;
+  }
   big::Int Di;
   Di.mag = D;
   if (!big::to_limbs(Di, out->values + (size_t)comps * limbs, limbs)) {

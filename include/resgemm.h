@@ -346,15 +346,17 @@ int rg_get_plan(const void* ws, void* stream, rg_plan_info* out);
  * ("exact-solve", Method).
  *  1. A^-1 mod q for all 53 primes at once by Gauss-Jordan elimination on the
  *     GPU, over all primes in each launch, blocked: per block of up to 64
- *     pivots, one panel factorisation and one INT8 tensor-core update of the
+ *     pivots, one panel factorisation and one fp16 tensor-core update of the
  *     other columns; the primes that divide det(A) are dropped.
  *  2. Dixon's p-adic lift with P = the product of the remaining primes:
  *     X_i = A^-1 R_i mod P per prime, then balanced Garner into the base-P
  *     digit; R_{i+1} = (R_i - A X_i) P^-1 mod 2^64, exact in one limb; as
  *     many steps as make P^m exceed twice the product of the Hadamard bounds
  *     of numerator and denominator.
- *  3. On the host: rational reconstruction of a component for the common
- *     denominator, then one modular product per numerator.
+ *  3. Rational reconstruction of a few components on host threads for the
+ *     common denominator d; on the GPU, every component's value from its
+ *     base-P digits and its numerator d X mod P^m (balanced), one block per
+ *     component.
  * On success `out` holds the numerators N [n][c] and the least common
  * denominator d > 0 (X = N / d exactly), as `limbs` little-endian
  * two's-complement int64 limbs each, in a host array the library allocates

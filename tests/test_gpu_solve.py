@@ -178,3 +178,17 @@ def test_planted_solution_at_every_panel_shape(rg, n):
     N, d = rg.solve_integers(dev(A), dev(b), info=info)
     assert d == 1
     assert [row[0] for row in N] == [int(v) for v in x[:, 0]]
+
+
+def test_denominators_beyond_the_sampled_components(rg):
+    """x_i = 1/p_i for distinct primes p_i above 255: every component has its own denominator, so the common
+    denominator the first few components give misses the rest, and each missing factor extends it."""
+    ps = [257, 263, 269, 271, 277, 281, 283, 293, 307, 311, 313, 317]
+    n = len(ps)
+    A = np.diag(np.array(ps, dtype=np.int64))  # det(A) = prod p_i: no lift prime divides it
+    b = np.ones((n, 1), dtype=np.int64)
+    info = {}
+    X = rg.solve(dev(A), dev(b), info=info)
+    assert X == [[Fraction(1, p)] for p in ps]
+    assert info["denominator"] == math.prod(ps)
+    assert info["primes"] == 53
