@@ -1059,28 +1059,43 @@ __constant__ IdemTables c_idem;  // idempotent-sum CRT tables, prime counts 1..k
 //    result is the one in [-(P - 1) / 2, (P - 1) / 2] (a wrong one lies at
 //    least P / 2 + 1/2 from zero, also after wrapping modulo 2^64).
 // Four integer multiply-adds per prime and entry, no modular reduction.
-template <int PP>
-__device__ __forceinline__ void idem_reconstruct4(const uint8_t* __restrict__ rc, long long plane,
-                                                  unsigned long long (&x)[4]) {
-  uint32_t rw[PP];
+template <int PP, int G>
+__device__ __forceinline__ void idem_reconstruct(const uint8_t* __restrict__ rc, long long plane,
+                                                 unsigned long long (&x)[G]) {
+  static_assert(G == 4 || G == 8, "four or eight adjacent entries");
+  constexpr int NW = G / 4;  // residue words per plane
+  uint32_t rw[PP][NW];
 #pragma unroll
-  for (int i = 0; i < PP; ++i) rw[i] = __ldg(reinterpret_cast<const uint32_t*>(rc + (long long)i * plane));
-  unsigned long long lo[4] = {0ull, 0ull, 0ull, 0ull};
-  uint32_t hi[4] = {0u, 0u, 0u, 0u}, kq[4] = {0u, 0u, 0u, 0u};
+  for (int i = 0; i < PP; ++i) {
+    if constexpr (NW == 2) {
+      const uint2 w = __ldg(reinterpret_cast<const uint2*>(rc + (long long)i * plane));
+      rw[i][0] = w.x;
+      rw[i][1] = w.y;
+    } else {
+      rw[i][0] = __ldg(reinterpret_cast<const uint32_t*>(rc + (long long)i * plane));
+    }
+  }
+  unsigned long long lo[G];
+  uint32_t hi[G], kq[G];
+#pragma unroll
+  for (int e = 0; e < G; ++e) {
+    lo[e] = 0ull;
+    hi[e] = kq[e] = 0u;
+  }
 #pragma unroll
   for (int i = 0; i < PP; ++i) {
     const uint32_t elo = c_idem.elo[PP][i], ehi = c_idem.ehi[PP][i], f = c_idem.f[PP][i];
 #pragma unroll
-    for (int e = 0; e < 4; ++e) {
-      const uint32_t r = __byte_perm(rw[i], 0u, 0x4440u + (uint32_t)e);  // byte e, zero-extended
-      lo[e] += (unsigned long long)r * elo;                                // < 12 * 250 * 2^32 < 2^44
-      hi[e] += r * ehi;                                                    // modulo 2^32
-      kq[e] += r * f;                                                      // < 12 * 250 * 2^20
+    for (int e = 0; e < G; ++e) {
+      const uint32_t r = __byte_perm(rw[i][e / 4], 0u, 0x4440u + (uint32_t)(e % 4));  // byte e, zero-extended
+      lo[e] += (unsigned long long)r * elo;                                           // < 12 * 250 * 2^32 < 2^44
+      hi[e] += r * ehi;                                                               // modulo 2^32
+      kq[e] += r * f;                                                                 // < 12 * 250 * 2^20
     }
   }
   const unsigned long long P64 = ((unsigned long long)c_idem.phi[PP] << 32) | c_idem.plo[PP];
 #pragma unroll
-  for (int e = 0; e < 4; ++e) {
+  for (int e = 0; e < G; ++e) {
     const uint32_t k = (kq[e] + (1u << (kIdemFracBits - 1))) >> kIdemFracBits;
     unsigned long long v = lo[e] + ((unsigned long long)hi[e] << 32) - (unsigned long long)k * P64;
     if constexpr (PP <= 8) {
@@ -1095,10 +1110,12 @@ __device__ __forceinline__ void idem_reconstruct4(const uint8_t* __restrict__ rc
 }
 
 // Int64 results (one limb) of up to kIdemMaxP primes by idempotent sums
-// (idem_reconstruct4), four adjacent entries per thread; the prime count is
-// dispatched to a compile-time constant, so every table entry is an
-// immediate constant operand.  Exact for every int64 result the plan (or the
-// caller's prime count) allows; rg_get_plan reports crt_rn = 2.
+// (idem_reconstruct), G adjacent entries per thread (G bytes of every
+// residue plane in one load); the prime count is dispatched to a
+// compile-time constant, so every table entry is an immediate constant
+// operand.  Exact for every int64 result the plan (or the caller's prime
+// count) allows; rg_get_plan reports crt_rn = 2.
+template <int G>
 __global__ void __launch_bounds__(128) crt_idem_kernel(const uint8_t* __restrict__ RC, long long ldc, long long plane,
                                                        long long M, long long N, RowDiv rd, DevPlan* plan,
                                                        int64_t* __restrict__ C) {
@@ -1110,38 +1127,41 @@ __global__ void __launch_bounds__(128) crt_idem_kernel(const uint8_t* __restrict
     return;
   }
   if (blockIdx.x == 0 && threadIdx.x == 0) plan->crt_rn = 2;
-  const long long per_row = (N + 3) / 4;
+  const long long per_row = (N + G - 1) / G;
   const long long item = (long long)blockIdx.x * blockDim.x + threadIdx.x;
   if (item >= M * per_row) return;
   const long long m = div_row(item, rd);  // item / per_row
-  const long long n0 = (item - m * per_row) * 4;
-  const uint8_t* rc = RC + m * ldc + n0;
-  unsigned long long v[4];
+  const long long n0 = (item - m * per_row) * G;
+  const uint8_t* rc = RC + m * ldc + n0;  // G bytes within the row's ldc (a multiple of 16)
+  unsigned long long v[G];
   switch (P) {
-    case 1: idem_reconstruct4<1>(rc, plane, v); break;
-    case 2: idem_reconstruct4<2>(rc, plane, v); break;
-    case 3: idem_reconstruct4<3>(rc, plane, v); break;
-    case 4: idem_reconstruct4<4>(rc, plane, v); break;
-    case 5: idem_reconstruct4<5>(rc, plane, v); break;
-    case 6: idem_reconstruct4<6>(rc, plane, v); break;
-    case 7: idem_reconstruct4<7>(rc, plane, v); break;
-    case 8: idem_reconstruct4<8>(rc, plane, v); break;
-    case 9: idem_reconstruct4<9>(rc, plane, v); break;
-    case 10: idem_reconstruct4<10>(rc, plane, v); break;
-    case 11: idem_reconstruct4<11>(rc, plane, v); break;
-    default: idem_reconstruct4<12>(rc, plane, v); break;
+    case 1: idem_reconstruct<1, G>(rc, plane, v); break;
+    case 2: idem_reconstruct<2, G>(rc, plane, v); break;
+    case 3: idem_reconstruct<3, G>(rc, plane, v); break;
+    case 4: idem_reconstruct<4, G>(rc, plane, v); break;
+    case 5: idem_reconstruct<5, G>(rc, plane, v); break;
+    case 6: idem_reconstruct<6, G>(rc, plane, v); break;
+    case 7: idem_reconstruct<7, G>(rc, plane, v); break;
+    case 8: idem_reconstruct<8, G>(rc, plane, v); break;
+    case 9: idem_reconstruct<9, G>(rc, plane, v); break;
+    case 10: idem_reconstruct<10, G>(rc, plane, v); break;
+    case 11: idem_reconstruct<11, G>(rc, plane, v); break;
+    default: idem_reconstruct<12, G>(rc, plane, v); break;
   }
   int64_t* out = C + m * N + n0;
-  if (n0 + 4 <= N && ((reinterpret_cast<uintptr_t>(out) & 15u) == 0)) {
-    *reinterpret_cast<ulonglong2*>(out) = make_ulonglong2(v[0], v[1]);
-    *reinterpret_cast<ulonglong2*>(out + 2) = make_ulonglong2(v[2], v[3]);
+  if (n0 + G <= N && ((reinterpret_cast<uintptr_t>(out) & 15u) == 0)) {
+#pragma unroll
+    for (int t = 0; t < G / 2; ++t) *reinterpret_cast<ulonglong2*>(out + 2 * t) = make_ulonglong2(v[2 * t], v[2 * t + 1]);
   } else {
 #pragma unroll
-    for (int e = 0; e < 4; ++e)
+    for (int e = 0; e < G; ++e)
       if (n0 + e < N) out[e] = (int64_t)v[e];
   }
 }
 static_assert(kIdemMaxP == 12, "crt_idem_kernel dispatches prime counts 1..12");
+// Entries per thread of the int64 reconstruction (ldc is a multiple of 16, so
+// every group's bytes lie within its row's padded planes).
+constexpr int kIdemGroup = 8;
 
 __device__ __forceinline__ CrtView crt_view(int P) { return CrtView{g_crt.M[P], g_crt.Pw[P], g_crt.Cw[P], g_crt.y[P]}; }
 
@@ -1683,7 +1703,8 @@ cudaError_t launch_garner(int op, const void* RC, long long ldc, long long plane
   const int mode = g_crt_mode.load();
   // mode 0: one-limb results of at most kIdemMaxP primes by idempotent sums
   if (mode == 0 && lc == 1 && pmax >= 1 && pmax <= kIdemMaxP)
-    return launch_dependent(crt_idem_kernel, blocks_for(4), 128, 0, st, rc, ldc, plane, M, N, rowdiv_for(4), plan, C);
+    return launch_dependent(crt_idem_kernel<kIdemGroup>, blocks_for(kIdemGroup), 128, 0, st, rc, ldc, plane, M, N,
+                            rowdiv_for(kIdemGroup), plan, C);
   // mode 1: int64 by round-to-nearest CRT on balanced digits when its primes allow it
   const int rn_free = op == RG_OP_I64 && mode == 1 ? 1 : 0;
   auto go = [&](auto k_small, auto k_all, int ge) {

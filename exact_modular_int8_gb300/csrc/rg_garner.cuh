@@ -60,10 +60,12 @@ __device__ __forceinline__ void add_scaled_weight(uint32_t (&x)[W], int D, int i
 // (v_{i+2} + q_{i+2} v_{i+3}), |D| <= (q_i q_{i+1} q_{i+2} q_{i+3} - 1) / 2 < 2^31:
 // the pairs in fp32 (|pair| < 2^15), the quad in int32, so the wide
 // accumulation runs once per four primes.  MAXP bounds P at compile time (the
-// packed digits take (MAXP + 3) / 4 registers per entry).
-template <int W, int GE, typename TAB, int MAXP = kNumPrimes>
+// packed digits take (MAXP + 3) / 4 registers per entry).  SHARED: rc points
+// into shared memory (one entry; plain loads instead of read-only cache loads).
+template <int W, int GE, typename TAB, int MAXP = kNumPrimes, bool SHARED = false>
 __device__ __forceinline__ void garner_reconstruct(const uint8_t* __restrict__ rc, long long plane, int P,
                                                    uint32_t (&x)[GE][W]) {
+  static_assert(!SHARED || GE == 1, "one entry from shared memory");
   static_assert(MAXP >= 1 && MAXP <= kNumPrimes, "prime bound");
   constexpr int kWords = (MAXP + 3) / 4;
   uint32_t V[GE][kWords];
@@ -87,7 +89,9 @@ __device__ __forceinline__ void garner_reconstruct(const uint8_t* __restrict__ r
       const int i = i0 + j;
       static_assert(GE == 1 || GE == 2 || GE == 4, "one, two or four adjacent entries");
       const bool in = i < P && i < MAXP;
-      if constexpr (GE == 4)
+      if constexpr (SHARED)
+        rw[j] = in ? (uint32_t)rc[(long long)i * plane] : 0u;
+      else if constexpr (GE == 4)
         rw[j] = in ? __ldg(reinterpret_cast<const uint32_t*>(rc + (long long)i * plane)) : 0u;
       else if constexpr (GE == 2)
         rw[j] = in ? (uint32_t)__ldg(reinterpret_cast<const unsigned short*>(rc + (long long)i * plane)) : 0u;

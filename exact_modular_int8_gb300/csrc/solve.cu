@@ -33,6 +33,9 @@ namespace {
 // Tables of the prime sequence a solve lifts with (a subset of the residue
 // base), uploaded once the inverse shows which primes divide det(A).
 __constant__ Tables c_sol;
+// The same tables in global memory, for reads whose index differs between the
+// lanes of a warp (divergent constant-memory reads are serialised).
+__device__ Tables g_sol;
 __constant__ Tables c_all;  // the full base, for the inverse
 
 struct SolTab {
@@ -698,6 +701,138 @@ __global__ void __launch_bounds__(256) lift_update_kernel(const int64_t* __restr
   allow_dependents();
 }
 
+// The lift's step in two kernels when B has few columns (c <= kFusedLiftCols):
+// one block per row i of the inverse planes forms the E GEMV results of
+// its c components in shared memory and reconstructs their digits there; one
+// warp per row then updates the residual and writes its residues for the
+// next step's GEMV.
+constexpr int kFusedLiftCols = 16;
+static_assert(kW == kQWords, "a digit has as many words as the mixed-radix weights");
+
+// Digits (balanced Garner) and low 64 bits of components i * c + t, t < c.
+// First RC[t][s] = (Binv[s][i][:] . Rr[s][t][:]) mod q_s, for every (s, t)
+// by a group of 16 threads (16 int8 per thread and step, dp4a; |sum| <=
+// n 125^2 < 2^31), all groups' loads independent.  Then one warp per column:
+// lane l owns primes l and l + 32; for each prime i in order its owner forms
+// v_i = bal(acc_i mod q_i) and every later prime p adds gd[p][i] v_i to its
+// acc_p (acc_p = ginv[p] r_p + sum_{j<p} gd[p][j] v_j, |acc| < 2^20); lane w
+// then sums column w of x = sum_i v_i Q_i (|.| < 2^45) and lane 0 carries the
+// columns into kW two's complement words.
+__global__ void __launch_bounds__(256) lift_row_kernel(const int8_t* __restrict__ Binv, const int8_t* __restrict__ Rr,
+                                                       int n, int c, int ld, int E, uint32_t* __restrict__ digit,
+                                                       unsigned long long* __restrict__ xlow) {
+  constexpr int G = 16;  // threads per dot product
+  __shared__ uint8_t rc[kFusedLiftCols][kNumPrimes];
+  __shared__ int gd[kNumPrimes][kGarnerWords];
+  __shared__ uint32_t Qw[kNumPrimes][kQWords];
+  __shared__ int vs[8][kNumPrimes];
+  __shared__ long long cols[8][kW];
+  for (int x = threadIdx.x; x < kNumPrimes * kGarnerWords; x += blockDim.x) (&gd[0][0])[x] = (&g_sol.gd_packed[0][0])[x];
+  for (int x = threadIdx.x; x < kNumPrimes * kQWords; x += blockDim.x) (&Qw[0][0])[x] = (&g_sol.Qw[0][0])[x];
+  wait_for_predecessor();
+  const int i = blockIdx.x, vpr = ld / 16;
+  const int grp = threadIdx.x / G, gl = threadIdx.x % G;
+  // every thread runs the same number of rounds, so that the whole warp
+  // reaches each shuffle (a group past the last task adds zeros)
+  for (int base = 0; base < E * c; base += blockDim.x / G) {
+    const int task = base + grp;
+    const bool active = task < E * c;
+    const int s = active ? task / c : 0, t = active ? task - s * c : 0;
+    const int8_t* brow = Binv + ((long long)s * n + i) * ld;
+    const int8_t* rv = Rr + ((long long)s * c + t) * ld;
+    int acc = 0;
+    for (int v = gl; active && v < vpr; v += G) {
+      const int4 a = *reinterpret_cast<const int4*>(brow + 16 * v);
+      const int4 b = *reinterpret_cast<const int4*>(rv + 16 * v);
+      acc = __dp4a(a.x, b.x, acc);
+      acc = __dp4a(a.y, b.y, acc);
+      acc = __dp4a(a.z, b.z, acc);
+      acc = __dp4a(a.w, b.w, acc);
+    }
+    for (int o = G / 2; o; o >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, o);  // within the 16-thread group
+    if (active && gl == 0) {
+      const int q = c_sol.q[s];
+      const int r = acc % q;
+      rc[t][s] = (uint8_t)(r < 0 ? r + q : r);
+    }
+  }
+  __syncthreads();
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  for (int t = warp; t < c; t += blockDim.x / 32) {
+    const int p0 = lane, p1 = lane + 32;
+    int acc0 = p0 < E ? g_sol.ginv[p0] * (int)rc[t][p0] : 0;
+    int acc1 = p1 < E ? g_sol.ginv[p1] * (int)rc[t][p1] : 0;
+    for (int pi = 0; pi < E; ++pi) {
+      const int own = pi & 31;
+      int v = 0;
+      if (lane == own) {
+        const int a = pi < 32 ? acc0 : acc1;
+        v = (int)bal_mod_small((float)a, c_sol.qf[pi], c_sol.invq[pi]);
+        vs[warp][pi] = v;
+      }
+      v = __shfl_sync(0xffffffffu, v, own);
+      const int sh = 8 * (pi & 3);
+      if (p0 > pi && p0 < E) acc0 += (int)(int8_t)(gd[p0][pi >> 2] >> sh) * v;
+      if (p1 > pi && p1 < E) acc1 += (int)(int8_t)(gd[p1][pi >> 2] >> sh) * v;
+    }
+    __syncwarp();
+    if (lane < kW) {
+      long long col = 0;
+      for (int pi = 0; pi < E; ++pi) col += (long long)vs[warp][pi] * Qw[pi][lane];
+      cols[warp][lane] = col;
+    }
+    __syncwarp();
+    if (lane == 0) {
+      const long long e = (long long)i * c + t;
+      long long carry = 0;
+      uint32_t w[kW];
+#pragma unroll
+      for (int k = 0; k < kW; ++k) {
+        const long long v = cols[warp][k] + carry;
+        w[k] = (uint32_t)v;
+        carry = v >> 32;  // arithmetic: the columns are signed
+      }
+#pragma unroll
+      for (int k = 0; k < kW; ++k) digit[e * kW + k] = w[k];
+      xlow[e] = ((unsigned long long)w[1] << 32) | w[0];
+    }
+    __syncwarp();
+  }
+  allow_dependents();
+}
+
+// R[i][t] = (R[i][t] - sum_k A[i][k] Xlow[k][t]) * P^-1 mod 2^64 (the exact
+// quotient (R - A X) / P, which fits one signed limb), then its balanced
+// residues Rr[s][t][i] for every lift prime.  One warp per row.
+__global__ void __launch_bounds__(256) lift_update_residue_kernel(const int64_t* __restrict__ A, int n, int c,
+                                                                  int ld, int E,
+                                                                  const unsigned long long* __restrict__ xlow,
+                                                                  unsigned long long pinv64, int64_t* __restrict__ R,
+                                                                  int8_t* __restrict__ Rr) {
+  wait_for_predecessor();
+  const long long warp = ((long long)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+  const int lane = threadIdx.x & 31;
+  if (warp < n) {
+    const int64_t* arow = A + warp * n;
+    for (int t = 0; t < c; ++t) {
+      unsigned long long acc = 0;
+      for (int k = lane; k < n; k += 32) acc += (unsigned long long)arow[k] * xlow[(long long)k * c + t];
+      for (int o = 16; o; o >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, o);
+      const unsigned long long r = (unsigned long long)R[warp * c + t];
+      const long long x = (long long)((r - acc) * pinv64);  // the same in every lane
+      if (lane == 0) R[warp * c + t] = x;
+      const unsigned long long u = (unsigned long long)x;
+      for (int s = lane; s < E; s += 32) {  // one prime per lane: the tables from global memory
+        int v = x < 0 ? -g_sol.wword[s][2] : 0;
+        asm("dp4a.u32.s32 %0, %1, %2, %0;" : "+r"(v) : "r"((uint32_t)u), "r"(g_sol.wbyte[s][0]));
+        asm("dp4a.u32.s32 %0, %1, %2, %0;" : "+r"(v) : "r"((uint32_t)(u >> 32)), "r"(g_sol.wbyte[s][1]));
+        Rr[((long long)s * c + t) * ld + warp] = (int8_t)bal_mod_small(int_to_float_exact(v), g_sol.qf[s], g_sol.invq[s]);
+      }
+    }
+  }
+  allow_dependents();
+}
+
 // ---------------------------------------------------------------------------
 // Host side
 // ---------------------------------------------------------------------------
@@ -924,6 +1059,7 @@ extern "C" int rg_solve_i64(const int64_t* A_in, const int64_t* B_in, int64_t n6
   Tables sol;
   build_tables_for(qs.data(), E, &sol);
   SOLVE_TRY(cudaMemcpyToSymbolAsync(c_sol, &sol, sizeof(Tables), 0, cudaMemcpyHostToDevice, st));
+  SOLVE_TRY(cudaMemcpyToSymbolAsync(g_sol, &sol, sizeof(Tables), 0, cudaMemcpyHostToDevice, st));
   DevBuf dBinv;
   SOLVE_TRY(dBinv.alloc((size_t)E * n * ld, st));
   int8_t* Binv = static_cast<int8_t*>(dBinv.p);
@@ -978,7 +1114,20 @@ extern "C" int rg_solve_i64(const int64_t* A_in, const int64_t* B_in, int64_t n6
   int64_t* R = static_cast<int64_t*>(dR.p);
   SOLVE_TRY(cudaMemcpyAsync(R, B, (size_t)n * c * 8, cudaMemcpyDeviceToDevice, st));
   uint32_t* X = static_cast<uint32_t*>(dX.p);
-  for (int i = 0; i < steps; ++i) {
+  const bool fused = c <= kFusedLiftCols;
+  if (fused)  // the residues of R = B; each step's update writes the next ones
+    SOLVE_TRY(launch_dependent(lift_residue_kernel,
+                               dim3(std::max(1u, std::min((unsigned)(((long long)c * ld + 255) / 256), 64u)), E),
+                               dim3(256), 0, st, (const int64_t*)R, n, c, ld, static_cast<int8_t*>(dRr.p)));
+  for (int i = 0; fused && i < steps; ++i) {
+    SOLVE_TRY(launch_dependent(lift_row_kernel, dim3((unsigned)n), dim3(256), 0, st, (const int8_t*)Binv,
+                               (const int8_t*)dRr.p, n, c, ld, E, X + (size_t)i * n * c * kW,
+                               static_cast<unsigned long long*>(dlow.p)));
+    SOLVE_TRY(launch_dependent(lift_update_residue_kernel, dim3((unsigned)(((long long)n * 32 + 255) / 256)),
+                               dim3(256), 0, st, A, n, c, ld, E, (const unsigned long long*)dlow.p, pinv64, R,
+                               static_cast<int8_t*>(dRr.p)));
+  }
+  for (int i = 0; !fused && i < steps; ++i) {
     SOLVE_TRY(launch_dependent(lift_residue_kernel,
                                dim3(std::max(1u, std::min((unsigned)(((long long)c * ld + 255) / 256), 64u)), E),
                                dim3(256), 0, st, (const int64_t*)R, n, c, ld, static_cast<int8_t*>(dRr.p)));

@@ -35,7 +35,7 @@ def integer_identity(A, X, b):
     return True
 
 
-@pytest.mark.parametrize("n,c,seed", [(1, 1, 0), (3, 2, 1), (7, 1, 2), (16, 3, 3), (20, 1, 4)])
+@pytest.mark.parametrize("n,c,seed", [(1, 1, 0), (3, 2, 1), (7, 1, 2), (16, 3, 3), (20, 1, 4), (24, 16, 5), (24, 17, 6)])
 def test_against_fraction_oracle(rg, n, c, seed):
     rng = np.random.default_rng(seed + 100)
     A = nonsingular(n, -(2**20), 2**20, seed)
