@@ -238,17 +238,13 @@ __device__ __forceinline__ int red_q(int x, float qf, float iq) {
 template <int B, int S, int RPT>
 __global__ void __launch_bounds__(kPanelThreads) gj_panel_kernel(uint8_t* __restrict__ M, int nE, int k0, int b,
                                                                  int kb, __half* __restrict__ Wb,
-                                                                 __half* __restrict__ RT, int* __restrict__ rowsrc,
-                                                                 int* __restrict__ sing) {
+                                                                 uint16_t* __restrict__ gsrc, int* __restrict__ sing) {
   static_assert(S % 4 == 0 && B % S == 0 && 16 % S == 0, "sub-blocks of whole words dividing every panel width");
   extern __shared__ __align__(16) uint8_t sm[];
   __shared__ uint8_t invtab[256];
   __shared__ __align__(16) int spiv[S];
   __shared__ __align__(16) uint8_t Rt[B * S];  // [panel column][t]: a sub-block's pivot rows, transposed
   __shared__ int s_piv[2];
-  __shared__ int s_nd;
-  __shared__ int s_disp[B];
-  __shared__ int s_rs[2 * B];
   constexpr int PS = B + 4;  // panel row stride: an odd number of words
   constexpr int SW = S / 4;
   const int p = blockIdx.x, tid = threadIdx.x;
@@ -262,7 +258,6 @@ __global__ void __launch_bounds__(kPanelThreads) gj_panel_kernel(uint8_t* __rest
   for (int i = tid; i < nE; i += kPanelThreads) src[i] = (uint16_t)i;
   if (tid == 0) {
     s_piv[0] = s_piv[1] = nE;
-    s_nd = 0;
   }
   wait_for_predecessor();
   if (sing[p]) return;
@@ -414,23 +409,59 @@ __global__ void __launch_bounds__(kPanelThreads) gj_panel_kernel(uint8_t* __rest
     }
     *reinterpret_cast<__half2*>(Wp + (size_t)i * kb + t) = out;
   }
+  // the original row each row of the panel holds, for the swap pass
+  for (int x = tid; x < nE; x += kPanelThreads) gsrc[(size_t)p * nE + x] = src[x];
+  allow_dependents();
+}
+
+// After a block's panel: its row swaps (gsrc[p][i], the original row that row
+// i holds after them) applied to the columns outside J.  The rows the swaps
+// move out of J get their final contents, the pivot rows' contents go,
+// balanced, transposed and as fp16, to RT[p][j][t] (zero in J's columns and
+// for t >= b), and rowsrc[p][i] follows the original row that row i of M
+// holds.  One block per prime (blockIdx.x) and chunk of kSwapCols columns
+// (blockIdx.y); it must run after every update of the previous block.
+constexpr int kMaxPanel = 64;
+size_t swap_smem(int nE) { return (size_t)2 * kMaxPanel * kSwapStride + (size_t)nE * 2; }
+
+__global__ void __launch_bounds__(kPanelThreads) gj_swap_kernel(uint8_t* __restrict__ M, int nE, int k0, int b, int kb,
+                                                                const uint16_t* __restrict__ gsrc,
+                                                                __half* __restrict__ RT, int* __restrict__ rowsrc,
+                                                                const int* __restrict__ sing) {
+  extern __shared__ __align__(16) uint8_t sm[];
+  __shared__ int s_nd;
+  __shared__ int s_disp[kMaxPanel];
+  __shared__ int s_rs[2 * kMaxPanel];
+  const int p = blockIdx.x, tid = threadIdx.x;
+  const int q = c_all.q[p], h = (q - 1) / 2;
+  uint8_t* buf = sm;  // row chunks: slot s < b the pivot row k0 + s, slot b + u the displaced row s_disp[u]
+  uint16_t* src = reinterpret_cast<uint16_t*>(sm + (size_t)2 * kMaxPanel * kSwapStride);
+  if (tid == 0) s_nd = 0;
+  wait_for_predecessor();
+  if (sing[p]) return;
+  for (int x = tid; x < nE; x += kPanelThreads) src[x] = gsrc[(size_t)p * nE + x];
+  __syncthreads();
+  uint8_t* Mp = M + (size_t)p * nE * nE;
+  const int kp = kb / 2;  // pairs of fp16 per RT row
   // rows outside J that the swaps changed (at most one per swap)
   for (int i = tid; i < nE; i += kPanelThreads)
     if ((i < k0 || i >= k0 + b) && src[i] != i) {
       const int u = atomicAdd(&s_nd, 1);
       if (u < b) s_disp[u] = i;  // always: each swap moves at most one row outside J
     }
-  __syncthreads();  // the panel is no longer needed: its space holds the row chunks below
+  __syncthreads();
   const int nd = min(s_nd, b);
   const int slots = b + nd;  // slot s < b: pivot row k0 + s; slot b + u: displaced row s_disp[u]
   // the original row each row of M holds: rowsrc[i] <- rowsrc[src[i]] for the rows the swaps changed
-  int* rs = rowsrc + (size_t)p * nE;
-  for (int s = tid; s < slots; s += kPanelThreads) s_rs[s] = rs[src[s < b ? k0 + s : s_disp[s - b]]];
-  __syncthreads();
-  for (int s = tid; s < slots; s += kPanelThreads) rs[s < b ? k0 + s : s_disp[s - b]] = s_rs[s];
-  uint8_t* buf = sm;
+  if (blockIdx.y == 0) {
+    int* rs = rowsrc + (size_t)p * nE;
+    for (int s = tid; s < slots; s += kPanelThreads) s_rs[s] = rs[src[s < b ? k0 + s : s_disp[s - b]]];
+    __syncthreads();
+    for (int s = tid; s < slots; s += kPanelThreads) rs[s < b ? k0 + s : s_disp[s - b]] = s_rs[s];
+  }
   __half* Rp = RT + (size_t)p * nE * kb;
-  for (int c0 = 0; c0 < nE; c0 += kSwapCols) {
+  {
+    const int c0 = blockIdx.y * kSwapCols;
     const int cw = min(kSwapCols, nE - c0), cwords = cw / 4;  // cw is a multiple of 16
     for (int e = tid; e < slots * cwords; e += kPanelThreads) {
       const int s = e / cwords, w = e - s * cwords;
@@ -487,26 +518,29 @@ __device__ __forceinline__ uint32_t add_mod4(uint32_t a, uint32_t b, uint32_t q4
   return (ge & __vsub4(a, c)) | (~ge & __vadd4(a, b));
 }
 
-// The columns outside J of one 128 x 128 tile of one prime's matrix (grid.z =
-// prime): X[i][j] <- base + sum_t W[i][t] RT[j][t] mod q, base = 0 in the
-// pivot rows and X[i][j] elsewhere (the panel kernel has already permuted
-// the rows the swaps moved).  The product runs on the warp-level fp16 tensor
+// One 128 x 128 tile of one prime's matrix (grid.z = prime, column tile jt0 +
+// blockIdx.x): X[i][j] <- base + sum_t W[i][t] RT[j][t] mod q for the columns
+// j in [cb, ce) outside [x0, x1) (which covers J), base = 0 in the pivot rows
+// and X[i][j] elsewhere (the swap pass has already permuted the rows the
+// swaps moved).  The product runs on the warp-level fp16 tensor
 // MMA with fp32 accumulation, exact here: the balanced residues (|r| <= 125)
 // are fp16 integers and |sum| <= 64 125^2 < 2^24.  One reduction into
 // [0, q), then one modular addition folds in the base.
 __global__ void __launch_bounds__(kUpdThreads, 2) gj_update_kernel(uint8_t* __restrict__ M, int nE, int k0, int b,
-                                                                int kb, const __half* __restrict__ Wb,
-                                                                const __half* __restrict__ RT,
-                                                                const int* __restrict__ sing) {
+                                                                   int kb, const __half* __restrict__ Wb,
+                                                                   const __half* __restrict__ RT,
+                                                                   const int* __restrict__ sing, int cb, int ce,
+                                                                   int x0, int x1, int jt0) {
   extern __shared__ __align__(16) uint8_t sm[];
   const int p = blockIdx.z;
-  const int i0 = blockIdx.y * kUpdTile, j0 = blockIdx.x * kUpdTile;
+  const int i0 = blockIdx.y * kUpdTile, j0 = (jt0 + blockIdx.x) * kUpdTile;
   const int lw = kb / 2 + 4;  // operand row stride in 32-bit words
   uint32_t* Ws = reinterpret_cast<uint32_t*>(sm);
   uint32_t* Rs = Ws + kUpdTile * lw;
   uint8_t* Cs = reinterpret_cast<uint8_t*>(Rs + kUpdTile * lw);
   wait_for_predecessor();
-  if (sing[p] || (j0 >= k0 && j0 + kUpdTile <= k0 + b)) return;
+  const int wlo = max(j0, cb), whi = min(j0 + kUpdTile, ce);  // the tile's columns in range
+  if (sing[p] || wlo >= whi || (wlo >= x0 && whi <= x1)) return;
   const __half* Wp = Wb + (size_t)p * nE * kb;
   const __half* Rp = RT + (size_t)p * nE * kb;
   const int vr = kb / 8;  // 16-byte vectors per operand row
@@ -562,7 +596,7 @@ __global__ void __launch_bounds__(kUpdThreads, 2) gj_update_kernel(uint8_t* __re
   for (int e = threadIdx.x; e < kUpdTile * (kUpdTile / 16); e += kUpdThreads) {
     const int r = e >> 3, v = e & 7;
     const int i = i0 + r, j = j0 + v * 16;
-    if (i >= nE || j >= nE || (j >= k0 && j < k0 + b)) continue;
+    if (i >= nE || j >= nE || j < cb || j >= ce || (j >= x0 && j < x1)) continue;
     uint4 o = *reinterpret_cast<const uint4*>(Cs + r * kUpdOutStride + v * 16);
     uint8_t* dst = Mp + (size_t)i * nE + j;
     if (i < k0 || i >= k0 + b) {
@@ -862,6 +896,44 @@ struct DevBuf {  // stream-ordered device allocation
   }
 };
 
+// A high- and a low-priority stream and an event for each, joined to the
+// caller's stream: open() makes both wait for the caller's stream, join() (and
+// the destructor, on an early return) makes the caller's stream wait for both.
+struct SideStreams {
+  cudaStream_t hi = nullptr, lo = nullptr, caller = nullptr;
+  cudaEvent_t ev_hi = nullptr, ev_lo = nullptr;
+  bool joined = true;
+  cudaError_t open(cudaStream_t st) {
+    caller = st;
+    int least = 0, greatest = 0;
+    cudaError_t e = cudaDeviceGetStreamPriorityRange(&least, &greatest);
+    if (e == cudaSuccess) e = cudaStreamCreateWithPriority(&hi, cudaStreamNonBlocking, greatest);
+    if (e == cudaSuccess) e = cudaStreamCreateWithPriority(&lo, cudaStreamNonBlocking, least);
+    if (e == cudaSuccess) e = cudaEventCreateWithFlags(&ev_hi, cudaEventDisableTiming);
+    if (e == cudaSuccess) e = cudaEventCreateWithFlags(&ev_lo, cudaEventDisableTiming);
+    if (e == cudaSuccess) e = cudaEventRecord(ev_hi, st);
+    if (e == cudaSuccess) e = cudaStreamWaitEvent(hi, ev_hi, 0);
+    if (e == cudaSuccess) e = cudaStreamWaitEvent(lo, ev_hi, 0);
+    joined = e != cudaSuccess;
+    return e;
+  }
+  cudaError_t join() {
+    joined = true;
+    cudaError_t e = cudaEventRecord(ev_hi, hi);
+    if (e == cudaSuccess) e = cudaEventRecord(ev_lo, lo);
+    if (e == cudaSuccess) e = cudaStreamWaitEvent(caller, ev_hi, 0);
+    if (e == cudaSuccess) e = cudaStreamWaitEvent(caller, ev_lo, 0);
+    return e;
+  }
+  ~SideStreams() {
+    if (!joined && hi && lo) join();
+    if (ev_hi) cudaEventDestroy(ev_hi);
+    if (ev_lo) cudaEventDestroy(ev_lo);
+    if (hi) cudaStreamDestroy(hi);
+    if (lo) cudaStreamDestroy(lo);
+  }
+};
+
 #define SOLVE_TRY(x)                             \
   do {                                           \
     cudaError_t e_ = (x);                        \
@@ -905,6 +977,7 @@ cudaError_t allow_panel_smem() {
   if (e == cudaSuccess) e = cudaFuncSetAttribute(gj_panel_kernel<32, 8, 4>, attr, bytes);
   if (e == cudaSuccess) e = cudaFuncSetAttribute(gj_panel_kernel<16, 4, 8>, attr, bytes);
   if (e == cudaSuccess) e = cudaFuncSetAttribute(gj_update_kernel, attr, (int)update_smem(64));
+  if (e == cudaSuccess) e = cudaFuncSetAttribute(gj_swap_kernel, attr, (int)swap_smem(kMaxSolveN));
   if (e == cudaSuccess) done[dev] = true;
   return e;
 }
@@ -1010,39 +1083,83 @@ extern "C" int rg_solve_i64(const int64_t* A_in, const int64_t* B_in, int64_t n6
   const size_t nnE = (size_t)nE * nE;
   const PanelCfg pc = panel_cfg(nE);
   const int bw = pc.B, kbw = (bw + 31) / 32 * 32;
-  DevBuf dM, dW, dRT, drowsrc, dsing;
+  DevBuf dM, dW, dRT, drowsrc, dsing, dgsrc;
+  const size_t wplane = (size_t)kNumPrimes * nE * kbw;  // fp16 entries of one block's W for every prime
   SOLVE_TRY(dM.alloc((size_t)kNumPrimes * nnE, st));
-  SOLVE_TRY(dW.alloc((size_t)kNumPrimes * nE * kbw * 2, st));
-  SOLVE_TRY(dRT.alloc((size_t)kNumPrimes * nE * kbw * 2, st));
+  SOLVE_TRY(dW.alloc(2 * wplane * 2, st));  // two blocks' W: one factored while the other is applied
+  SOLVE_TRY(dRT.alloc(wplane * 2, st));
   SOLVE_TRY(drowsrc.alloc((size_t)kNumPrimes * nE * 4, st));
   SOLVE_TRY(dsing.alloc(kNumPrimes * 4, st));
+  SOLVE_TRY(dgsrc.alloc((size_t)kNumPrimes * nE * 2, st));
   uint8_t* M = static_cast<uint8_t*>(dM.p);
-  __half* Wb = static_cast<__half*>(dW.p);
+  __half* Wbuf = static_cast<__half*>(dW.p);
   __half* RT = static_cast<__half*>(dRT.p);
   int* rowsrc = static_cast<int*>(drowsrc.p);
   int* sing = static_cast<int*>(dsing.p);
+  uint16_t* gsrc = static_cast<uint16_t*>(dgsrc.p);
   SOLVE_TRY(cudaMemsetAsync(sing, 0, kNumPrimes * 4, st));
   gj_init_kernel<<<grid_for((long long)nnE), 256, 0, st>>>(A, n, nE, M, rowsrc);
   SOLVE_TRY(cudaGetLastError());
   SOLVE_TRY(allow_panel_smem());
-  const unsigned tiles = (unsigned)((nE + kUpdTile - 1) / kUpdTile);
-  for (int k0 = 0; k0 < nE; k0 += bw) {
-    const int b = std::min(bw, nE - k0), kb = (b + 31) / 32 * 32;  // b: a multiple of 16
+  // Look-ahead: the chain panel -> swap -> update of the next panel's columns
+  // runs on a high-priority stream, and the update of the other columns on a
+  // low-priority one, so that each block's bulk update overlaps the next
+  // block's panel.  Both streams join the call's stream on every exit.
+  SideStreams ss;
+  SOLVE_TRY(ss.open(st));
+  cudaStream_t sA = ss.hi, sB = ss.lo;
+  auto W_of = [&](int blk) { return Wbuf + (size_t)(blk & 1) * wplane; };
+  // a kernel that follows a cross-stream wait is launched plainly (programmatic
+  // dependent launch relaxes only the dependency on the stream's previous kernel)
+  auto go = [&](auto kern, bool dependent, dim3 grid, dim3 block, size_t smem, cudaStream_t s,
+                auto... args) -> cudaError_t {
+    if (dependent) return launch_dependent(kern, grid, block, smem, s, args...);
+    kern<<<grid, block, smem, s>>>(args...);
+    return cudaGetLastError();
+  };
+  auto panel = [&](bool dependent, int k0, int b, int kb, __half* W) -> cudaError_t {
     const size_t smem = panel_smem(nE, bw);
     const dim3 pg(kNumPrimes), pt(kPanelThreads);
-    if (pc.RPT == 1)
-      SOLVE_TRY(launch_dependent(gj_panel_kernel<64, 16, 1>, pg, pt, smem, st, M, nE, k0, b, kb, Wb, RT, rowsrc, sing));
-    else if (pc.RPT == 2)
-      SOLVE_TRY(launch_dependent(gj_panel_kernel<64, 8, 2>, pg, pt, smem, st, M, nE, k0, b, kb, Wb, RT, rowsrc, sing));
-    else if (pc.RPT == 4)
-      SOLVE_TRY(launch_dependent(gj_panel_kernel<32, 8, 4>, pg, pt, smem, st, M, nE, k0, b, kb, Wb, RT, rowsrc, sing));
-    else
-      SOLVE_TRY(launch_dependent(gj_panel_kernel<16, 4, 8>, pg, pt, smem, st, M, nE, k0, b, kb, Wb, RT, rowsrc, sing));
-    if (b < nE)
-      SOLVE_TRY(launch_dependent(gj_update_kernel, dim3(tiles, tiles, kNumPrimes), dim3(kUpdThreads),
-                                 update_smem(kb), st, M, nE, k0, b, kb, (const __half*)Wb, (const __half*)RT,
-                                 (const int*)sing));
+    if (pc.RPT == 1) return go(gj_panel_kernel<64, 16, 1>, dependent, pg, pt, smem, sA, M, nE, k0, b, kb, W, gsrc, sing);
+    if (pc.RPT == 2) return go(gj_panel_kernel<64, 8, 2>, dependent, pg, pt, smem, sA, M, nE, k0, b, kb, W, gsrc, sing);
+    if (pc.RPT == 4) return go(gj_panel_kernel<32, 8, 4>, dependent, pg, pt, smem, sA, M, nE, k0, b, kb, W, gsrc, sing);
+    return go(gj_panel_kernel<16, 4, 8>, dependent, pg, pt, smem, sA, M, nE, k0, b, kb, W, gsrc, sing);
+  };
+  auto swap = [&](int k0, int b, int kb) -> cudaError_t {  // follows a cross-stream wait: a plain launch
+    gj_swap_kernel<<<dim3(kNumPrimes, (unsigned)((nE + kSwapCols - 1) / kSwapCols)), kPanelThreads, swap_smem(nE), sA>>>(
+        M, nE, k0, b, kb, gsrc, RT, rowsrc, sing);
+    return cudaGetLastError();
+  };
+  auto update = [&](cudaStream_t s, bool dependent, int k0, int b, int kb, const __half* W, int cb, int ce, int x0,
+                    int x1) -> cudaError_t {
+    const int jt0 = cb / kUpdTile, jt1 = (ce + kUpdTile - 1) / kUpdTile;
+    const dim3 grid((unsigned)(jt1 - jt0), (unsigned)((nE + kUpdTile - 1) / kUpdTile), kNumPrimes);
+    return go(gj_update_kernel, dependent, grid, dim3(kUpdThreads), update_smem(kb), s, M, nE, k0, b, kb, W,
+              (const __half*)RT, (const int*)sing, cb, ce, x0, x1, jt0);
+  };
+  {
+    const int b0 = std::min(bw, nE), kb0 = (b0 + 31) / 32 * 32;
+    SOLVE_TRY(panel(false, 0, b0, kb0, W_of(0)));
+    SOLVE_TRY(swap(0, b0, kb0));
   }
+  for (int blk = 0, k0 = 0; k0 < nE; ++blk, k0 += bw) {
+    const int b = std::min(bw, nE - k0), kb = (b + 31) / 32 * 32;  // b: a multiple of 16
+    const int k1 = k0 + b;
+    if (k1 >= nE) {  // the last block: the other columns at once
+      if (b < nE) SOLVE_TRY(update(sA, true, k0, b, kb, W_of(blk), 0, nE, k0, k1));
+      break;
+    }
+    const int b1 = std::min(bw, nE - k1), kb1 = (b1 + 31) / 32 * 32;
+    SOLVE_TRY(update(sA, true, k0, b, kb, W_of(blk), k1, k1 + b1, k0, k1));  // the next panel's columns
+    SOLVE_TRY(cudaEventRecord(ss.ev_hi, sA));
+    SOLVE_TRY(panel(true, k1, b1, kb1, W_of(blk + 1)));
+    SOLVE_TRY(cudaStreamWaitEvent(sB, ss.ev_hi, 0));
+    SOLVE_TRY(update(sB, false, k0, b, kb, W_of(blk), 0, nE, k0, k1 + b1));  // the rest, beside the panel
+    SOLVE_TRY(cudaEventRecord(ss.ev_lo, sB));
+    SOLVE_TRY(cudaStreamWaitEvent(sA, ss.ev_lo, 0));
+    SOLVE_TRY(swap(k1, b1, kb1));
+  }
+  SOLVE_TRY(ss.join());
   int hsing[kNumPrimes];
   SOLVE_TRY(cudaMemcpyAsync(hsing, sing, sizeof(hsing), cudaMemcpyDeviceToHost, st));
   SOLVE_TRY(cudaStreamSynchronize(st));
