@@ -325,7 +325,7 @@ int recon_blocks(long long comps) {
   cudaGetDevice(&dev);
   cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
   if (sms <= 0) sms = 148;
-  return (int)std::max(1LL, std::min(comps, 2LL * sms));
+  return (int)std::max(1LL, std::min(comps, 8LL * sms));
 }
 
 static cudaError_t allow_smem(const void* fn, size_t bytes) {
