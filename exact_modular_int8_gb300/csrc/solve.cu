@@ -745,8 +745,8 @@ static_assert(kW == kQWords, "a digit has as many words as the mixed-radix weigh
 
 // Digits (balanced Garner) and low 64 bits of components i * c + t, t < c.
 // First RC[t][s] = (Binv[s][i][:] . Rr[s][t][:]) mod q_s, for every (s, t)
-// by a group of 16 threads (16 int8 per thread and step, dp4a; |sum| <=
-// n 125^2 < 2^31), all groups' loads independent.  Then one warp per column:
+// by a group of 4 or 16 threads (16 int8 per thread and step, dp4a; |sum|
+// <= n 125^2 < 2^31), all groups' loads independent.  Then one warp per column:
 // lane l owns primes l and l + 32; for each prime i in order its owner forms
 // v_i = bal(acc_i mod q_i) and every later prime p adds gd[p][i] v_i to its
 // acc_p (acc_p = ginv[p] r_p + sum_{j<p} gd[p][j] v_j, |acc| < 2^20); lane w
@@ -755,7 +755,9 @@ static_assert(kW == kQWords, "a digit has as many words as the mixed-radix weigh
 __global__ void __launch_bounds__(256) lift_row_kernel(const int8_t* __restrict__ Binv, const int8_t* __restrict__ Rr,
                                                        int n, int c, int ld, int E, uint32_t* __restrict__ digit,
                                                        unsigned long long* __restrict__ xlow) {
-  constexpr int G = 16;  // threads per dot product
+  // threads per dot product: 4 up to rows of 1 KiB (64 dot products at once, every prime of one right-hand
+  // side), 16 for longer rows (more loads in flight per row; measured at n = 1024 and 2048)
+  const int G = ld <= 1024 ? 4 : 16;
   __shared__ uint8_t rc[kFusedLiftCols][kNumPrimes];
   __shared__ int gd[kNumPrimes][kGarnerWords];
   __shared__ uint32_t Qw[kNumPrimes][kQWords];
@@ -775,6 +777,7 @@ __global__ void __launch_bounds__(256) lift_row_kernel(const int8_t* __restrict_
     const int8_t* brow = Binv + ((long long)s * n + i) * ld;
     const int8_t* rv = Rr + ((long long)s * c + t) * ld;
     int acc = 0;
+#pragma unroll 4
     for (int v = gl; active && v < vpr; v += G) {
       const int4 a = *reinterpret_cast<const int4*>(brow + 16 * v);
       const int4 b = *reinterpret_cast<const int4*>(rv + 16 * v);
@@ -783,7 +786,7 @@ __global__ void __launch_bounds__(256) lift_row_kernel(const int8_t* __restrict_
       acc = __dp4a(a.z, b.z, acc);
       acc = __dp4a(a.w, b.w, acc);
     }
-    for (int o = G / 2; o; o >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, o);  // within the 16-thread group
+    for (int o = G / 2; o; o >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, o);  // within the group
     if (active && gl == 0) {
       const int q = c_sol.q[s];
       const int r = acc % q;
