@@ -752,12 +752,10 @@ static_assert(kW == kQWords, "a digit has as many words as the mixed-radix weigh
 // acc_p (acc_p = ginv[p] r_p + sum_{j<p} gd[p][j] v_j, |acc| < 2^20); lane w
 // then sums column w of x = sum_i v_i Q_i (|.| < 2^45) and lane 0 carries the
 // columns into kW two's complement words.
+template <int G>  // threads per dot product
 __global__ void __launch_bounds__(256) lift_row_kernel(const int8_t* __restrict__ Binv, const int8_t* __restrict__ Rr,
                                                        int n, int c, int ld, int E, uint32_t* __restrict__ digit,
                                                        unsigned long long* __restrict__ xlow) {
-  // threads per dot product: 4 up to rows of 1 KiB (64 dot products at once, every prime of one right-hand
-  // side), 16 for longer rows (more loads in flight per row; measured at n = 1024 and 2048)
-  const int G = ld <= 1024 ? 4 : 16;
   __shared__ uint8_t rc[kFusedLiftCols][kNumPrimes];
   __shared__ int gd[kNumPrimes][kGarnerWords];
   __shared__ uint32_t Qw[kNumPrimes][kQWords];
@@ -1240,8 +1238,10 @@ extern "C" int rg_solve_i64(const int64_t* A_in, const int64_t* B_in, int64_t n6
                                dim3(std::max(1u, std::min((unsigned)(((long long)c * ld + 255) / 256), 64u)), E),
                                dim3(256), 0, st, (const int64_t*)R, n, c, ld, static_cast<int8_t*>(dRr.p)));
   for (int i = 0; fused && i < steps; ++i) {
-    SOLVE_TRY(launch_dependent(lift_row_kernel, dim3((unsigned)n), dim3(256), 0, st, (const int8_t*)Binv,
-                               (const int8_t*)dRr.p, n, c, ld, E, X + (size_t)i * n * c * kW,
+    // 4 threads per dot product up to rows of 1 KiB (every prime of one right-hand side at once), 16 for
+    // longer rows (more loads in flight per row; measured at n = 1024 and 2048)
+    SOLVE_TRY(launch_dependent(ld <= 1024 ? lift_row_kernel<4> : lift_row_kernel<16>, dim3((unsigned)n), dim3(256), 0,
+                               st, (const int8_t*)Binv, (const int8_t*)dRr.p, n, c, ld, E, X + (size_t)i * n * c * kW,
                                static_cast<unsigned long long*>(dlow.p)));
     SOLVE_TRY(launch_dependent(lift_update_residue_kernel, dim3((unsigned)(((long long)n * 32 + 255) / 256)),
                                dim3(256), 0, st, A, n, c, ld, E, (const unsigned long long*)dlow.p, pinv64, R,
