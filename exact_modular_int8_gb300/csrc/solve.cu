@@ -193,12 +193,8 @@ constexpr size_t kPanelSmemLimit = 200u << 10;
 
 // Dynamic shared memory of the panel kernel for order nE and width b: the
 // panel (rows of b + 4 bytes, an odd number of words, so that one thread per
-// row reads without bank conflicts) or the permutation pass's row chunks,
-// whichever is larger, then the source-row index of every row.
-size_t panel_smem(int nE, int b) {
-  const size_t pan = (size_t)nE * (b + 4), chunk = (size_t)2 * b * kSwapStride;
-  return std::max(pan, chunk) + (size_t)nE * 2;
-}
+// row reads without bank conflicts), then the source-row index of every row.
+size_t panel_smem(int nE, int b) { return (size_t)nE * (b + 4) + (size_t)nE * 2; }
 
 // The panel kernel's shape for order nE: the block width B (its panel of
 // nE x (B + 4) bytes within kPanelSmemLimit), the sub-block S and the rows
@@ -251,8 +247,7 @@ __global__ void __launch_bounds__(kPanelThreads) gj_panel_kernel(uint8_t* __rest
   const int q = c_all.q[p], h = (q - 1) / 2;
   const float qf = c_all.qf[p], iq = c_all.invq[p];
   uint8_t* pan = sm;
-  const size_t pan_bytes = (size_t)nE * PS, chunk_bytes = (size_t)2 * B * kSwapStride;
-  const size_t body = pan_bytes > chunk_bytes ? pan_bytes : chunk_bytes;
+  const size_t body = (size_t)nE * PS;  // nE is a multiple of 16: src stays 2-byte aligned
   uint16_t* src = reinterpret_cast<uint16_t*>(sm + body);  // row i holds original row src[i]
   for (int a = tid; a < 256; a += kPanelThreads) invtab[a] = (a > 0 && a < q) ? (uint8_t)invmod(a, q) : 0;
   for (int i = tid; i < nE; i += kPanelThreads) src[i] = (uint16_t)i;
