@@ -27,7 +27,8 @@ def planted(rng, nbits, dbits, mbits):
 
 
 @pytest.mark.parametrize("nbits,dbits,mbits", [(3, 3, 10), (30, 30, 64), (60, 60, 130), (500, 400, 1000),
-                                               (2000, 1500, 3600), (9000, 3000, 12100)])
+                                               (2000, 1500, 3600), (9000, 3000, 12100),
+                                               (27200, 27100, 54400)])  # the n = 1024 solve's sizes
 def test_planted_fractions(lib, nbits, dbits, mbits):
     rng = random.Random(nbits * 7 + dbits)
     for _ in range(6):
